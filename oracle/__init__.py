@@ -1,0 +1,161 @@
+"""fp64 CPU oracle for the bf16 attention forward.  TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference leg of
+``bench.py`` may import this package.  The product library never loads it and shares no
+code with it.  The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over rows);
+this module compiles it with gcc and marshals numpy arrays through ``ctypes``.
+
+What it computes is stated in the C file's header: softmax(Q K^T / sqrt(d)) V per row, in
+fp64, two passes, rounded once to bf16 in the requested mode, following the page
+"MoonMath AI open-sources a HIP attention kernel for AMD MI300X that beats AITER"
+(opening section: definition and contract; limitations paragraph: rounding modes, NaN/Inf).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libattn_oracle.so")
+
+LAYOUTS = {"bshd": 0, "bhsd": 1}
+MODES = {"rtne": 0, "rtna": 1, "rtz": 2}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle into a shared object (gcc, -O2, OpenMP, no fast-math)."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-fno-fast-math",
+           src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _bind(lib):
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    lib.attn_oracle.restype = ctypes.c_int
+    lib.attn_oracle.argtypes = [u16p, u16p, u16p] + [ctypes.c_int64] * 5 + [
+        ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int64, u16p, f64p, f64p, f64p, f64p,
+        ctypes.c_int]
+    lib.oracle_round_bf16_array.restype = None
+    lib.oracle_round_bf16_array.argtypes = [f64p, ctypes.c_int64, ctypes.c_int, u16p]
+    lib.oracle_max_threads.restype = ctypes.c_int
+    lib.oracle_max_threads.argtypes = []
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library."""
+    global _lib
+    with _lock:
+        if path is not None:
+            return _bind(ctypes.CDLL(path))
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+        return _lib
+
+
+def _ptr(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype)) if a is not None else None
+
+
+def _as_bits(t) -> np.ndarray:
+    """Accept a torch bf16 tensor (CPU) or a uint16/int16 numpy array of bf16 bits."""
+    if isinstance(t, np.ndarray):
+        a = t
+    else:  # torch tensor
+        import torch
+        a = t.detach().cpu().contiguous().view(torch.int16).numpy()
+    return np.ascontiguousarray(a).view(np.uint16)
+
+
+def dims(q_shape, k_shape, layout: str):
+    """(B, H, Sq, Skv, d) from BSHD (B, S, H, d) or BHSD (B, H, S, d) shapes."""
+    if layout == "bshd":
+        B, Sq, H, d = q_shape
+        Skv = k_shape[1]
+    else:
+        B, H, Sq, d = q_shape
+        Skv = k_shape[2]
+    return B, H, Sq, Skv, d
+
+
+def attention(q, k, v, layout: str = "bshd", mode: str = "rtne", rows=None,
+              want_f64: bool = False, want_a: bool = False, want_lse: bool = False,
+              want_probs: bool = False, threads: int | None = None, lib=None) -> dict:
+    """Oracle attention.  Returns a dict of numpy arrays.
+
+    ``o_bits``: uint16 bf16 patterns.  With ``rows=None`` shaped (B, H, Sq, d) (BHSD order,
+    whatever the input layout); with ``rows`` (flat indices (b*H + h)*Sq + i) shaped
+    (len(rows), d).  Optional: ``o_f64``, ``a`` (forward-error scale A), ``lse`` (natural
+    log), ``probs`` (softmax weights, rows x Skv).
+    """
+    lib = lib or load()
+    qb, kb, vb = _as_bits(q), _as_bits(k), _as_bits(v)
+    B, H, Sq, Skv, d = dims(qb.shape, kb.shape, layout)
+    if rows is None:
+        n = B * H * Sq
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n = rows_arr.shape[0]
+    o_bits = np.empty((n, d), dtype=np.uint16)
+    o_f64 = np.empty((n, d), dtype=np.float64) if want_f64 else None
+    a_b = np.empty((n, d), dtype=np.float64) if want_a else None
+    lse = np.empty((n,), dtype=np.float64) if want_lse else None
+    probs = np.empty((n, Skv), dtype=np.float64) if want_probs else None
+    rc = lib.attn_oracle(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                         _ptr(vb, ctypes.c_uint16), B, H, Sq, Skv, d, LAYOUTS[layout],
+                         MODES[mode], _ptr(rows_arr, ctypes.c_int64),
+                         0 if rows_arr is None else n, _ptr(o_bits, ctypes.c_uint16),
+                         _ptr(o_f64, ctypes.c_double), _ptr(a_b, ctypes.c_double),
+                         _ptr(lse, ctypes.c_double), _ptr(probs, ctypes.c_double),
+                         int(threads or 0))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments (rc=%d)" % rc)
+    out = {"o_bits": o_bits}
+    if o_f64 is not None:
+        out["o_f64"] = o_f64
+    if a_b is not None:
+        out["a"] = a_b
+    if lse is not None:
+        out["lse"] = lse
+    if probs is not None:
+        out["probs"] = probs
+    if rows is None:
+        for key in ("o_bits", "o_f64", "a"):
+            if key in out:
+                out[key] = out[key].reshape(B, H, Sq, d)
+        if "lse" in out:
+            out["lse"] = out["lse"].reshape(B, H, Sq)
+    return out
+
+
+def round_bf16(x, mode: str = "rtne", lib=None) -> np.ndarray:
+    """Round float64 values to bf16 bit patterns with the oracle's rounding rule."""
+    lib = lib or load()
+    xa = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty(xa.shape, dtype=np.uint16)
+    lib.oracle_round_bf16_array(_ptr(xa, ctypes.c_double), xa.size, MODES[mode],
+                                _ptr(out, ctypes.c_uint16))
+    return out
+
+
+def max_threads(lib=None) -> int:
+    lib = lib or load()
+    return int(lib.oracle_max_threads())

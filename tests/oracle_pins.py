@@ -1,0 +1,387 @@
+"""Pins for the fp64 oracle: checks against what the pages and the mathematics fix.
+
+Each ``pin_*`` takes an oracle library handle (so the same checks can be run against a
+deliberately broken copy of the oracle) and raises AssertionError on a mismatch.  None of
+them re-types the oracle's formula: they use closed forms, invariants, special cases that
+reduce to a plain statistic, 50-digit brute force on tiny inputs, torch's own fp32->bf16
+conversion and an independent table-based rounding.
+
+Page cited: "MoonMath AI open-sources a HIP attention kernel for AMD MI300X that beats
+AITER" -- opening section (softmax(QK^T/sqrt(d))V, head dim 128, BSHD/BHSD, arbitrary
+lengths) and its limitations paragraph (three rounding modes, NaN/Inf, determinism).
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import oracle
+from tests import bf16_exact as bx
+from workloads import make_qkv, shape
+
+MODES = ("rtne", "rtna", "rtz")
+D = 128
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _bf16(a) -> torch.Tensor:
+    return torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+# --------------------------------------------------------------------------- rounding
+def pin_round_rtne_matches_torch(lib):
+    """RTNE of fp32-representable doubles equals torch's fp32 -> bf16 conversion."""
+    g = torch.Generator().manual_seed(7)
+    raw = torch.randint(0, 2**32, (200000,), generator=g, dtype=torch.int64)
+    u = raw.to(torch.int64) & 0xFFFFFFFF
+    # keep finite fp32 patterns; include subnormals and huge values
+    f = torch.from_numpy(u.numpy().astype(np.uint32).view(np.float32).copy())
+    f = f[torch.isfinite(f)]
+    # plus exact ties: bf16 value + half quantum, and near-overflow
+    ties = torch.from_numpy((np.arange(0, 0x7F7F, 97, dtype=np.uint32) << 16 | 0x8000)
+                            .view(np.float32).copy())
+    f = torch.cat([f, ties, -ties, torch.tensor([3.3895e38, -3.3895e38, 3.39e38])])
+    want = f.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.round_bf16(f.double().numpy(), "rtne", lib=lib)
+    assert np.array_equal(got, want), "RTNE disagrees with torch on %d values" % (
+        int((got != want).sum()))
+
+
+def pin_round_rtz_rtna_bit_rules(lib):
+    """On fp32 inputs RTZ keeps the top 16 bits; RTNA equals RTNE except on exact ties,
+    where it moves away from zero."""
+    g = torch.Generator().manual_seed(8)
+    u = torch.randint(0, 2**31 - 1, (100000,), generator=g, dtype=torch.int64).numpy()
+    u = u.astype(np.uint32)
+    u[::3] = (u[::3] & 0xFFFF0000) | 0x8000            # exact ties
+    u[1::7] |= 0x80000000                               # negatives
+    f = u.view(np.float32)
+    ok = np.isfinite(f)
+    f, u = f[ok], u[ok]
+    rtz = oracle.round_bf16(f.astype(np.float64), "rtz", lib=lib)
+    want_rtz = (u >> 16).astype(np.uint16)
+    # values beyond the largest bf16 truncate to it under RTZ, which the plain bit rule gives
+    assert np.array_equal(rtz, want_rtz)
+    rtne = oracle.round_bf16(f.astype(np.float64), "rtne", lib=lib)
+    rtna = oracle.round_bf16(f.astype(np.float64), "rtna", lib=lib)
+    tie = (u & 0xFFFF) == 0x8000
+    assert np.array_equal(rtna[~tie], rtne[~tie])
+    away = ((u[tie] >> 16) + 1).astype(np.uint16)      # magnitude up, sign kept
+    assert np.array_equal(rtna[tie], away)
+
+
+def pin_round_exact_doubles(lib):
+    """On doubles that are not fp32 values, all three modes agree with the table-based
+    rounding of the exact value, including exact midpoints and the subnormal range."""
+    rng = np.random.default_rng(9)
+    xs = list(rng.standard_normal(3000) * np.exp2(rng.integers(-140, 128, 3000)))
+    for b in range(0x0001, 0x7F7F, 251):                 # midpoints between neighbours
+        lo, hi = bx.bits_to_float(b), bx.bits_to_float(b + 1)
+        xs += [(lo + hi) / 2, -(lo + hi) / 2, np.nextafter((lo + hi) / 2, 0.0),
+               np.nextafter((lo + hi) / 2, np.inf)]
+    mx = bx.bits_to_float(0x7F7F)
+    xs += [mx + 2.0**119, mx + 2.0**119 - 2.0**80, mx, 1e300, -1e300, 5e-324, 2.0**-133,
+           2.0**-134, 3 * 2.0**-135, 0.0, -0.0]
+    xs = np.array(xs, dtype=np.float64)
+    for mode in MODES:
+        got = oracle.round_bf16(xs, mode, lib=lib)
+        want = np.array([bx.round_exact(Fraction(float(x)), mode) for x in xs],
+                        dtype=np.uint16)
+        # -0.0: Fraction loses the sign; the oracle keeps it
+        neg0 = (xs == 0) & np.signbit(xs)
+        want[neg0] = 0x8000
+        bad = np.nonzero(got != want)[0]
+        assert bad.size == 0, "%s: %r -> %04x, want %04x" % (
+            mode, xs[bad[0]], got[bad[0]], want[bad[0]])
+
+
+def pin_round_nonfinite(lib):
+    xs = np.array([np.nan, -np.nan, np.inf, -np.inf], dtype=np.float64)
+    neg_nan = np.frombuffer(np.array([0xFFF8000000000001], dtype=np.uint64).tobytes(),
+                            dtype=np.float64)
+    xs = np.concatenate([xs, neg_nan])
+    for mode in MODES:
+        got = oracle.round_bf16(xs, mode, lib=lib)
+        assert list(got) == [0x7FC0, 0x7FC0, 0x7F80, 0xFF80, 0x7FC0], (mode, got)
+
+
+# --------------------------------------------------------------------------- closed forms
+def pin_single_key_returns_v(lib):
+    """Skv = 1: the only weight is 1, so O is the V row, bit for bit, in every mode."""
+    for layout in ("bshd", "bhsd"):
+        q, k, v = make_qkv(2, 3, 5, 1, D, layout, seed=11, sigma=3.0)
+        for mode in MODES:
+            o = oracle.attention(q, k, v, layout, mode, lib=lib)["o_bits"]
+            vb = _bits(v if layout == "bhsd" else v.permute(0, 2, 1, 3))  # (B, H, 1, d)
+            assert np.array_equal(o, np.broadcast_to(vb, o.shape)), (layout, mode)
+
+
+def pin_constant_v(lib):
+    """V rows all equal to one vector c: O = c exactly (weights sum to 1).  The exact value
+    is a bf16 value, so RTNE/RTNA must return c; RTZ sits on its boundary there and may
+    return c or its neighbour toward zero, while the unrounded result is c to 1e-15."""
+    B, H, Sq, Skv = 1, 2, 7, 37
+    q, k, _ = make_qkv(B, H, Sq, Skv, D, "bhsd", seed=12, sigma=2.0)
+    c = torch.randn(D, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    v = c.view(1, 1, 1, D).expand(B, H, Skv, D).contiguous()
+    cb = np.broadcast_to(_bits(c), (B, H, Sq, D))
+    for mode in ("rtne", "rtna"):
+        o = oracle.attention(q, k, v, "bhsd", mode, lib=lib)["o_bits"]
+        assert np.array_equal(o, cb), mode
+    r = oracle.attention(q, k, v, "bhsd", "rtz", want_f64=True, lib=lib)
+    cd = c.double().numpy()
+    assert np.allclose(r["o_f64"], np.broadcast_to(cd, r["o_f64"].shape), rtol=1e-15, atol=0)
+    d = cb.astype(np.int64) - r["o_bits"].astype(np.int64)
+    assert np.all((d == 0) | ((d == 1) & (cd != 0)))
+
+
+def pin_zero_query_is_column_mean(lib):
+    """Q = 0 (and separately K = 0): all logits 0, uniform weights, O = mean of V's rows."""
+    B, H, Sq, Skv = 1, 2, 3, 29
+    q, k, v = make_qkv(B, H, Sq, Skv, D, "bshd", seed=13)
+    vv = v.permute(0, 2, 1, 3).double().numpy()                 # (B, H, Skv, d)
+    for zq, zk in ((True, False), (False, True)):
+        qq = torch.zeros_like(q) if zq else q
+        kk = torch.zeros_like(k) if zk else k
+        res = oracle.attention(qq, kk, v, "bshd", "rtne", want_f64=True, lib=lib)
+        mean = vv.mean(axis=2, keepdims=True)                    # (B, H, 1, d)
+        assert np.allclose(res["o_f64"], np.broadcast_to(mean, res["o_f64"].shape),
+                           rtol=0, atol=1e-14)
+        # exact mean (rational) rounded by the table method
+        obits = {m: oracle.attention(qq, kk, v, "bshd", m, lib=lib)["o_bits"] for m in MODES}
+        for h in range(H):
+            for x in range(0, D, 9):
+                exact = sum(Fraction(float(t)) for t in vv[0, h, :, x]) / Skv
+                if bx.near_midpoint(exact):
+                    continue
+                for mode in MODES:
+                    assert obits[mode][0, h, 0, x] == bx.round_exact(exact, mode), (h, x, mode)
+
+
+def pin_two_keys_sigmoid(lib):
+    """Two keys: O = sigma(s1 - s2) v1 + sigma(s2 - s1) v2 with s = q.k / sqrt(d)."""
+    g = torch.Generator().manual_seed(14)
+    q = torch.randn(1, 1, 4, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(1, 1, 2, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, 1, 2, D, generator=g).to(torch.bfloat16)
+    res = oracle.attention(q, k, v, "bhsd", "rtne", want_f64=True, lib=lib)
+    qd, kd, vd = q.double()[0, 0], k.double()[0, 0], v.double()[0, 0]
+    for i in range(4):
+        s = [float((qd[i] * kd[j]).sum()) / math.sqrt(D) for j in range(2)]
+        a = 1.0 / (1.0 + math.exp(s[1] - s[0]))
+        want = a * vd[0].numpy() + (1.0 - a) * vd[1].numpy()
+        assert np.allclose(res["o_f64"][0, 0, i], want, rtol=1e-13, atol=1e-14)
+
+
+def pin_dominant_key(lib):
+    """One key with a logit gap above 60 takes all the weight: O equals its V row
+    (the others' weights are below e^-60, under half an fp64-scaled bf16 quantum)."""
+    B, H, Sq, Skv = 1, 1, 3, 50
+    q, k, v = make_qkv(B, H, Sq, Skv, D, "bhsd", seed=15)
+    q = torch.zeros_like(q)
+    q[..., 0] = 1.0
+    k = k.clone()
+    k[..., 0] = 0.0
+    k[0, 0, 17, 0] = 1024.0                                   # logit 1024/sqrt(128) ~ 90.5
+    res = oracle.attention(q, k, v, "bhsd", "rtne", want_f64=True, lib=lib)
+    assert np.allclose(res["o_f64"][0, 0], v.double().numpy()[0, 0, 17][None, :],
+                       rtol=1e-20, atol=1e-25)
+    for mode in ("rtne", "rtna"):   # the exact value is within 1e-38 of a bf16 value
+        o = oracle.attention(q, k, v, "bhsd", mode, lib=lib)["o_bits"]
+        assert np.array_equal(o[0, 0], np.broadcast_to(_bits(v)[0, 0, 17], (Sq, D)))
+
+
+def pin_probs_sum_to_one(lib):
+    B, H, Sq, Skv = 1, 2, 6, 300
+    q, k, v = make_qkv(B, H, Sq, Skv, D, "bshd", seed=16, sigma=4.0)
+    res = oracle.attention(q, k, v, "bshd", "rtne", want_probs=True, lib=lib)
+    p = res["probs"]
+    assert np.all(p >= 0)
+    assert np.all(np.abs(p.sum(axis=1) - 1.0) <= 4 * Skv * 2.0**-53)
+
+
+# --------------------------------------------------------------------------- brute force
+def _mp_attention(q, k, v, mode_list, dps=50):
+    """50-digit evaluation of softmax(QK^T/sqrt(d))V for finite BHSD inputs (B = H = 1)."""
+    import mpmath
+    mpmath.mp.dps = dps
+    qd = q.double().numpy()[0, 0]
+    kd = k.double().numpy()[0, 0]
+    vd = v.double().numpy()[0, 0]
+    Sq, Skv = qd.shape[0], kd.shape[0]
+    inv = 1 / mpmath.sqrt(D)
+    out = {}
+    for i in range(Sq):
+        s = [mpmath.fsum(mpmath.mpf(float(qd[i, x])) * mpmath.mpf(float(kd[j, x]))
+                         for x in range(D)) * inv for j in range(Skv)]
+        m = max(s)
+        w = [mpmath.exp(sj - m) for sj in s]
+        l = mpmath.fsum(w)
+        for x in range(D):
+            val = mpmath.fsum(w[j] * mpmath.mpf(float(vd[j, x])) for j in range(Skv)) / l
+            out[(i, x)] = val
+    return out
+
+
+def pin_brute_force_mpmath(lib):
+    """Tiny shapes against 50-digit arithmetic: unrounded O to 1e-13 relative to A, and the
+    rounded bits in all modes except within 1e-12 of a rounding boundary."""
+    for seed, (Sq, Skv, sigma) in enumerate(((1, 1, 1.0), (2, 3, 1.0), (4, 8, 1.0),
+                                             (3, 5, 4.0), (2, 7, 0.25))):
+        q, k, v = make_qkv(1, 1, Sq, Skv, D, "bhsd", seed=100 + seed, sigma=sigma)
+        ref = _mp_attention(q, k, v, MODES)
+        res = {m: oracle.attention(q, k, v, "bhsd", m, want_f64=True, want_a=True, lib=lib)
+               for m in MODES}
+        for (i, x), val in ref.items():
+            f64 = res["rtne"]["o_f64"][0, 0, i, x]
+            a = res["rtne"]["a"][0, 0, i, x]
+            assert abs(f64 - float(val)) <= 1e-13 * max(a, 1e-300), (seed, i, x, f64, val)
+            if bx.near_midpoint(val):
+                continue
+            for m in MODES:
+                assert res[m]["o_bits"][0, 0, i, x] == bx.round_exact(val, m), (seed, i, x, m)
+
+
+# --------------------------------------------------------------------------- structure
+def pin_layouts_agree(lib):
+    """The same logical tensors in BSHD and BHSD give the same output."""
+    B, H, Sq, Skv = 2, 3, 9, 21
+    q, k, v = make_qkv(B, H, Sq, Skv, D, "bshd", seed=17)
+    a = oracle.attention(q, k, v, "bshd", "rtna", lib=lib)["o_bits"]
+    t = lambda x: x.permute(0, 2, 1, 3).contiguous()
+    b = oracle.attention(t(q), t(k), t(v), "bhsd", "rtna", lib=lib)["o_bits"]
+    assert np.array_equal(a, b)
+    # a per-head check that each (b, h) reads its own slice: swap heads 0 and 2 in BSHD
+    perm = [2, 1, 0]
+    c = oracle.attention(q[:, :, perm], k[:, :, perm], v[:, :, perm], "bshd", "rtna",
+                         lib=lib)["o_bits"]
+    assert np.array_equal(c[:, perm], a)
+
+
+def pin_key_permutation_and_rows(lib):
+    """Permuting K and V rows together changes nothing beyond fp64 summation order; the
+    row-subset entry point agrees with the full evaluation."""
+    B, H, Sq, Skv = 1, 2, 11, 64
+    q, k, v = make_qkv(B, H, Sq, Skv, D, "bhsd", seed=18)
+    full = oracle.attention(q, k, v, "bhsd", "rtne", want_f64=True, want_a=True, lib=lib)
+    perm = torch.randperm(Skv, generator=torch.Generator().manual_seed(3))
+    pk = oracle.attention(q, k[:, :, perm], v[:, :, perm], "bhsd", "rtne", want_f64=True,
+                          lib=lib)
+    assert np.all(np.abs(full["o_f64"] - pk["o_f64"]) <= 1e-14 * full["a"] + 1e-300)
+    rows = [0, 5, 10, 11, 21]
+    sub = oracle.attention(q, k, v, "bhsd", "rtne", rows=rows, lib=lib)["o_bits"]
+    assert np.array_equal(sub, full["o_bits"].reshape(-1, D)[rows])
+
+
+def pin_softmax_shift_and_scale(lib):
+    """Adding one vector c to every key row shifts each row's logits by the constant
+    q_i.c/sqrt(d), which leaves O unchanged (c = 3 e_0 on integer-valued column 0, so the
+    shifted keys are exact in bf16).  And the scale is exactly 1/sqrt(128): with two keys of
+    raw dot products 8 and 0 the first weight is sigmoid(8/sqrt(128))."""
+    B, H, Sq, Skv = 1, 1, 4, 16
+    q, k, v = make_qkv(B, H, Sq, Skv, D, "bhsd", seed=19)
+    k = k.clone()
+    g = torch.Generator().manual_seed(5)
+    k[..., 0] = torch.randint(-8, 9, (B, H, Skv), generator=g).to(torch.bfloat16)
+    k2 = k.clone()
+    k2[..., 0] = k2[..., 0] + 3.0
+    a = oracle.attention(q, k, v, "bhsd", "rtne", want_f64=True, want_a=True, lib=lib)
+    b = oracle.attention(q, k2, v, "bhsd", "rtne", want_f64=True, lib=lib)
+    assert np.all(np.abs(a["o_f64"] - b["o_f64"]) <= 1e-13 * a["a"] + 1e-300)
+    qq = torch.zeros(1, 1, 1, D, dtype=torch.bfloat16)
+    qq[..., 0] = 4.0
+    kk = torch.zeros(1, 1, 2, D, dtype=torch.bfloat16)
+    kk[0, 0, 0, 0] = 2.0                                      # raw dot 8 -> logit 8/sqrt(128)
+    vv = torch.zeros(1, 1, 2, D, dtype=torch.bfloat16)
+    vv[0, 0, 0, :] = 1.0
+    r = oracle.attention(qq, kk, vv, "bhsd", "rtne", want_f64=True, lib=lib)["o_f64"]
+    t = 8.0 / math.sqrt(128.0)
+    assert abs(r[0, 0, 0, 0] - 1.0 / (1.0 + math.exp(-t))) < 1e-15
+
+
+# --------------------------------------------------------------------------- non-finite
+def _nf_base(seed=20, Sq=4, Skv=12):
+    q, k, v = make_qkv(1, 1, Sq, Skv, D, "bhsd", seed=seed)
+    return q.clone(), k.clone(), v.clone()
+
+
+def pin_nan_in_q_poisons_only_its_row(lib):
+    q, k, v = _nf_base()
+    q[0, 0, 1, 5] = float("nan")
+    o = oracle.attention(q, k, v, "bhsd", "rtne", lib=lib)["o_bits"][0, 0]
+    assert np.all(o[1] == 0x7FC0)
+    assert np.all(bx.is_finite_bits(o[[0, 2, 3]]))
+
+
+def pin_nan_in_k_poisons_every_row(lib):
+    q, k, v = _nf_base()
+    k[0, 0, 3, 77] = float("nan")
+    o = oracle.attention(q, k, v, "bhsd", "rtz", lib=lib)["o_bits"]
+    assert np.all(o == 0x7FC0)
+
+
+def pin_inf_key_sign_rules(lib):
+    """k_j,x = +inf: rows with q_x > 0 get logit +inf (row NaN); rows with q_x < 0 get
+    logit -inf, i.e. key j drops out: equal to attention without key j -- except columns
+    where v_j is not finite, which become NaN (0 * inf); rows with q_x = 0 get NaN."""
+    q, k, v = _nf_base(Sq=3)
+    j, x = 4, 9
+    q[0, 0, 0, x] = 1.0
+    q[0, 0, 1, x] = -1.0
+    q[0, 0, 2, x] = 0.0
+    k[0, 0, j, x] = float("inf")
+    v[0, 0, j, 30] = float("inf")
+    for mode in MODES:
+        o = oracle.attention(q, k, v, "bhsd", mode, lib=lib)["o_bits"][0, 0]
+        assert np.all(o[0] == 0x7FC0) and np.all(o[2] == 0x7FC0)
+        keep = [t for t in range(k.shape[2]) if t != j]
+        ref = oracle.attention(q, k[:, :, keep], v[:, :, keep], "bhsd", mode,
+                               lib=lib)["o_bits"][0, 0]
+        want = ref[1].copy()
+        want[30] = 0x7FC0
+        assert np.array_equal(o[1], want), mode
+
+
+def pin_inf_in_v_rules(lib):
+    """Finite logits: +inf in a V column gives +inf there; +inf and -inf in one column
+    give NaN; a weight that underflows in fp64 still carries the infinity (its exact value
+    is positive)."""
+    q, k, v = _nf_base(Sq=2, Skv=6)
+    v[0, 0, 2, 3] = float("inf")
+    v[0, 0, 1, 4] = float("inf")
+    v[0, 0, 5, 4] = float("-inf")
+    o = oracle.attention(q, k, v, "bhsd", "rtne", lib=lib)["o_bits"][0, 0]
+    assert np.all(o[:, 3] == 0x7F80)
+    assert np.all(o[:, 4] == 0x7FC0)
+    finite_cols = [c for c in range(D) if c not in (3, 4)]
+    assert np.all(bx.is_finite_bits(o[:, finite_cols]))
+    # underflow: key 0 logit ~ -1000 below the max
+    q2 = torch.zeros(1, 1, 1, D, dtype=torch.bfloat16)
+    q2[..., 0] = 128.0
+    k2 = torch.zeros(1, 1, 3, D, dtype=torch.bfloat16)
+    k2[0, 0, 1, 0] = 96.0                 # logit 128*96/sqrt(128) ~ 1086
+    v2 = torch.ones(1, 1, 3, D, dtype=torch.bfloat16)
+    v2[0, 0, 0, 7] = float("-inf")        # key 0 (logit 0): weight e^-1086 underflows
+    o2 = oracle.attention(q2, k2, v2, "bhsd", "rtne", lib=lib)["o_bits"][0, 0, 0]
+    assert o2[7] == 0xFF80
+    assert np.all(np.delete(o2, 7) == 0x3F80)
+
+
+def pin_all_neginf_row_is_nan(lib):
+    q = torch.zeros(1, 1, 2, D, dtype=torch.bfloat16)
+    q[0, 0, 0, 0] = 1.0
+    q[0, 0, 1, 0] = -1.0
+    k = torch.zeros(1, 1, 3, D, dtype=torch.bfloat16)
+    k[0, 0, :, 0] = float("-inf")        # row 0: every logit -inf; row 1: every logit +inf
+    v = torch.ones(1, 1, 3, D, dtype=torch.bfloat16)
+    o = oracle.attention(q, k, v, "bhsd", "rtna", lib=lib)["o_bits"]
+    assert np.all(o == 0x7FC0)
+
+
+ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

@@ -1,0 +1,64 @@
+"""Planted mistakes in a private copy of the oracle must each fail at least one pin.
+
+Each mutation is a plausible slip (a dropped term, a wrong sign or index, a transposed
+operand, a mis-rounded tie).  The copy is compiled into a temporary directory on the CPU;
+the committed oracle is never touched.
+"""
+import os
+import shutil
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
+
+MUTANTS = {
+    "no_scale": ("s[j] = acc * scale;", "s[j] = acc;"),
+    "kv_stride_uses_Sq": ("elem_offset(layout, b, j, h, 0, Skv, H, d)",
+                          "elem_offset(layout, b, j, h, 0, Sq, H, d)"),
+    "exp_sign": ("exp(s[j] - m)", "exp(m - s[j])"),
+    "ties_to_odd": ("fmod(n, 2.0) != 0.0", "fmod(n, 2.0) == 0.0"),
+    "rtna_as_rtne": ("if (rem >= half) r = a + q;", "if (rem > half) r = a + q;"),
+    "neginf_key_drops_nan": ("term = 0.0 * vj;", "term = 0.0;"),
+    "underflow_kills_inf": ("term = vj;                       /* positive weight times +-inf */",
+                            "term = w[j] * vj;"),
+    "nan_not_canonical": ("if (isnan(x)) return 0x7FC0;", "if (isnan(x)) return 0xFFC0;"),
+    "bshd_as_bhsd": ("if (layout == ORACLE_LAYOUT_BSHD) return ((b * S + s) * H + h) * d + x;",
+                     "if (layout == ORACLE_LAYOUT_BSHD) return ((b * H + h) * S + s) * d + x;"),
+    "sum_skips_first_key": ("l += w[j];", "if (j > 0) l += w[j];"),
+    "v_transposed": ("v[elem_offset(layout, b, j, h, x, Skv, H, d)]",
+                     "v[elem_offset(layout, b, x % Skv, h, j % d, Skv, H, d)]"),
+    "posinf_logit_ignored": ("if (isnan(s[j]) || (isinf(s[j]) && s[j] > 0)) any_nan_or_posinf = 1;",
+                             "if (isnan(s[j])) any_nan_or_posinf = 1;"),
+}
+
+
+@pytest.fixture(scope="module")
+def workdir():
+    d = tempfile.mkdtemp(prefix="oracle_mut_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, workdir):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) >= 1, "mutation site vanished: %s" % name
+    src = os.path.join(workdir, name + ".c")
+    with open(src, "w") as f:
+        f.write(text.replace(old, new))
+    so = os.path.join(workdir, "lib%s.so" % name)
+    oracle.build(force=True, src=src, out=so)
+    lib = oracle.load(so)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, "no pin caught the planted mistake %r" % name
