@@ -1,0 +1,172 @@
+"""bf16 attention forward for GB300 (sm_103a): Python binding of the C-ABI library.
+
+The binding only marshals arguments: every step of the computation runs in the library's
+CUDA kernels (``csrc/attn_fwd.cu``, ABI in ``include/bf16_attn.h``).  PyTorch supplies
+device memory and the current stream.  There is no CPU fallback: if the compiled library
+is missing, importing the binding's entry points raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+LAYOUTS = {"bshd": 0, "bhsd": 1}
+MODES = {"rtne": 0, "rtna": 1, "rtz": 2}
+STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+          3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_ALIAS", 5: "ATTN_ERR_NO_DEVICE",
+          6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_CUDA", 8: "ATTN_ERR_DEVICE_TIMEOUT"}
+EXPORTS = ("attn_fwd", "attn_fwd_ws", "attn_fwd_workspace_size",
+           "attn_fwd_workspace_size_opts", "attn_plan", "attn_get_device_status",
+           "attn_status_string", "attn_version")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__("%s (%d): %s%s" % (STATUS.get(status, "?"), status,
+                                            status_string(status), (" -- " + what) if what else ""))
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("force_splits", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
+                ("wait_limit_ms", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("units", "kv_tiles", "full_items", "split_units",
+                                              "splits", "items", "grid", "workspace_bytes")]
+
+    def as_dict(self) -> dict:
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load the compiled library (it must already be built: ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError("bf16 attention library not built: %s is missing "
+                              "(run __graft_entry__.build())" % p)
+        lib = ctypes.CDLL(p)
+        i64, vp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        lib.attn_fwd.restype = i32
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, vp]
+        lib.attn_fwd_ws.restype = i32
+        lib.attn_fwd_ws.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, i32,
+                                    ctypes.POINTER(Options), vp, ctypes.c_size_t, vp]
+        lib.attn_fwd_workspace_size.restype = ctypes.c_size_t
+        lib.attn_fwd_workspace_size.argtypes = [i64] * 5
+        lib.attn_fwd_workspace_size_opts.restype = ctypes.c_size_t
+        lib.attn_fwd_workspace_size_opts.argtypes = [i64] * 5 + [ctypes.POINTER(Options)]
+        lib.attn_plan.restype = i32
+        lib.attn_plan.argtypes = [i64] * 6 + [ctypes.POINTER(Options), ctypes.POINTER(Plan)]
+        lib.attn_get_device_status.restype = i32
+        lib.attn_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_status_string.argtypes = [i32]
+        lib.attn_version.restype = i32
+        lib.attn_version.argtypes = []
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().attn_status_string(int(status)).decode()
+
+
+def _dims(q, k, layout):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k, v must be 4-D (BSHD or BHSD)")
+    if layout == "bshd":
+        B, Sq, H, d = q.shape
+        Skv = k.shape[1]
+    else:
+        B, H, Sq, d = q.shape
+        Skv = k.shape[2]
+    return int(B), int(H), int(Sq), int(Skv), int(d)
+
+
+def _opts(force_splits=0, max_ctas=0, wait_limit_ms=0):
+    if not (force_splits or max_ctas or wait_limit_ms):
+        return None
+    return Options(int(force_splits), int(max_ctas), int(wait_limit_ms), 0)
+
+
+def plan(B, H, Sq, Skv, d=128, num_sms=152, force_splits=0, max_ctas=0) -> dict:
+    """The work split the library would launch for this shape (host only)."""
+    pl = Plan()
+    o = _opts(force_splits, max_ctas)
+    st = load().attn_plan(B, H, Sq, Skv, d, num_sms, ctypes.byref(o) if o else None,
+                          ctypes.byref(pl))
+    if st != 0:
+        raise AttnError(st, "attn_plan")
+    return pl.as_dict()
+
+
+def workspace_size(B, H, Sq, Skv, d=128, force_splits=0, max_ctas=0) -> int:
+    o = _opts(force_splits, max_ctas)
+    return int(load().attn_fwd_workspace_size_opts(B, H, Sq, Skv, d,
+                                                   ctypes.byref(o) if o else None))
+
+
+def attn_fwd(q, k, v, o=None, layout: str = "bshd", round: str = "rtne", stream=None,
+             workspace=None, force_splits: int = 0, max_ctas: int = 0, wait_limit_ms: int = 0):
+    """O = softmax(Q K^T / sqrt(128)) V on CUDA tensors (bf16, contiguous, same layout).
+
+    ``workspace``: optional caller tensor (any dtype, CUDA) used through ``attn_fwd_ws``;
+    with the knobs set and no workspace, one is allocated here with torch.  Returns ``o``.
+    """
+    import torch
+    if layout not in LAYOUTS or round not in MODES:
+        raise ValueError("layout must be bshd/bhsd and round rtne/rtna/rtz")
+    for t in (q, k, v):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError("q, k, v must be CUDA bf16 tensors")
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+    B, H, Sq, Skv, d = _dims(q, k, layout)
+    if o is None:
+        o = torch.empty_like(q)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    sp = ctypes.c_void_p(s.cuda_stream if hasattr(s, "cuda_stream") else int(s))
+    lib = load()
+    opts = _opts(force_splits, max_ctas, wait_limit_ms)
+    if workspace is None and opts is None:
+        st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, Sq,
+                          Skv, d, LAYOUTS[layout], MODES[round], sp)
+    else:
+        need = workspace_size(B, H, Sq, Skv, d, force_splits, max_ctas)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        nbytes = workspace.numel() * workspace.element_size()
+        st = lib.attn_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, Sq,
+                             Skv, d, LAYOUTS[layout], MODES[round],
+                             ctypes.byref(opts) if opts else None, workspace.data_ptr(),
+                             nbytes, sp)
+    if st != 0:
+        raise AttnError(st, "attn_fwd")
+    return o
+
+
+def device_status(stream=None) -> tuple:
+    """Synchronize and read/clear the device status word: (status, wait site)."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    site = ctypes.c_int32(0)
+    st = load().attn_get_device_status(ctypes.c_void_p(s.cuda_stream), ctypes.byref(site))
+    return int(st), int(site.value)

@@ -1,0 +1,141 @@
+/*
+ * bf16_attn.h -- C ABI of the GB300 (sm_103a) bf16 attention forward library.
+ *
+ * Operation.  O = softmax(Q K^T / sqrt(d)) V, non-causal, head dimension d = 128, bf16 in
+ * and out, fp32 accumulation.  Source: "MoonMath AI open-sources a HIP attention kernel for
+ * AMD MI300X that beats AITER" (news.chathome.org), opening section: attention is the fused
+ * softmax(QK^T/sqrt(d))V; the kernel takes BSHD or BHSD tensors without transposes, head
+ * dimension fixed at 128, any query and key length including cross-attention; its
+ * limitations paragraph: three output rounding modes (RTNE, RTNA, RTZ), NaN/Inf handled
+ * bit-identically, deterministic results; section "Real use cases": a simple API that
+ * launches on the caller's stream.  The long-KV split and its log-sum-exp combine follow the
+ * section "Data placement and the 16x16x16 choice" (Flash-Decoding-style tail KV split).
+ *
+ * Layouts.  All four tensors share one layout and are dense (contiguous):
+ *   ATTN_LAYOUT_BSHD: element (b, s, h, x) at ((b*S + s)*H + h)*d + x
+ *   ATTN_LAYOUT_BHSD: element (b, s, h, x) at ((b*H + h)*S + s)*d + x
+ * with S = Sq for Q and O and S = Skv for K and V.  The scale is fixed at 1/sqrt(d).
+ *
+ * Numerics.  The output rounding mode applies to the final fp32 -> bf16 store only
+ * (softmax weights are rounded to bf16, nearest-even, before the P.V product in every mode).
+ * A row whose logits hold a NaN or +inf, or are all -inf, is NaN; every NaN is stored as
+ * 0x7FC0; +-inf outputs keep their sign.  Results are bitwise reproducible for a given shape
+ * on a given GPU model (the work split is a pure function of shape and SM count).
+ *
+ * Ownership.  The caller owns q, k, v, o and any workspace; the library never frees them.
+ * All calls are asynchronous on `stream` and return before the GPU runs.  attn_fwd() keeps
+ * one lazily grown workspace per device (guarded by a mutex): it may call cudaMalloc the
+ * first time a shape needs the split path, so call it once before any CUDA-graph capture,
+ * or use attn_fwd_ws() with caller memory.
+ *
+ * Errors.  Argument problems are reported synchronously before anything is launched.  A
+ * launch failure returns ATTN_ERR_CUDA.  Every wait inside the kernels is bounded: if one
+ * expires the kernel records ATTN_ERR_DEVICE_TIMEOUT in a per-device status word and
+ * returns (it never traps or spins forever); read it with attn_get_device_status().
+ */
+#ifndef BF16_ATTN_H_
+#define BF16_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the same handle type, declared here without the CUDA headers). */
+typedef struct CUstream_st* attn_stream_t;
+
+typedef enum { ATTN_LAYOUT_BSHD = 0, ATTN_LAYOUT_BHSD = 1 } attn_layout_t;
+
+/* Output rounding of the final fp32 value: IEEE roundTiesToEven, roundTiesToAway,
+ * roundTowardZero. */
+typedef enum { ATTN_ROUND_RTNE = 0, ATTN_ROUND_RTNA = 1, ATTN_ROUND_RTZ = 2 } attn_round_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,    /* null pointer, a size < 1, a bad enum value            */
+    ATTN_ERR_UNSUPPORTED = 2,    /* d != 128, or a size beyond the kernels' int32 indexing */
+    ATTN_ERR_MISALIGNED = 3,     /* a tensor or workspace base not 16-byte aligned         */
+    ATTN_ERR_ALIAS = 4,          /* o overlaps q, k or v                                   */
+    ATTN_ERR_NO_DEVICE = 5,      /* no CUDA device, or the current device is not sm_103    */
+    ATTN_ERR_WORKSPACE = 6,      /* workspace null or smaller than attn_fwd_workspace_size */
+    ATTN_ERR_CUDA = 7,           /* a CUDA runtime call failed                             */
+    ATTN_ERR_DEVICE_TIMEOUT = 8  /* a bounded wait inside a kernel expired                 */
+} attn_status_t;
+
+/* Optional knobs (all zero = defaults). */
+typedef struct {
+    int32_t force_splits;   /* 0: planner decides. n >= 1: split every unit's keys n ways  */
+    int32_t max_ctas;       /* 0: one persistent CTA per SM. n >= 1: at most n CTAs         */
+    uint32_t wait_limit_ms; /* 0: 2000 ms. Bound on any single wait inside the kernels      */
+    uint32_t reserved;
+} attn_options_t;
+
+/* The work split chosen for a shape (host only, launches nothing). */
+typedef struct {
+    int64_t units;          /* B*H*ceil(Sq/256): one unit = two 128-row query tiles         */
+    int64_t kv_tiles;       /* ceil(Skv/128)                                                */
+    int64_t full_items;     /* units run whole                                              */
+    int64_t split_units;    /* units whose keys are split                                   */
+    int64_t splits;         /* ways each split unit is divided                              */
+    int64_t items;          /* full_items + split_units*splits                              */
+    int64_t grid;           /* persistent CTAs launched                                     */
+    int64_t workspace_bytes;/* scratch the split path needs (0 when nothing is split)       */
+} attn_plan_t;
+
+/*
+ * attn_fwd -- O = softmax(Q K^T / sqrt(d)) V on `stream`.
+ *   q           device pointer, bf16, [B, Sq, H, d] (BSHD) or [B, H, Sq, d] (BHSD)
+ *   k, v        device pointers, bf16, same layout with Skv rows
+ *   o           device pointer, bf16, same shape as q; must not overlap q, k or v
+ *   B, H        batch and heads (>= 1);  Sq, Skv  query and key lengths (>= 1);  d = 128
+ *   layout      attn_layout_t;  round_mode  attn_round_t
+ *   stream      cudaStream_t (NULL = legacy default stream)
+ * Uses the library-owned workspace when the planner splits keys (see Ownership above).
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, int64_t B, int64_t H,
+             int64_t Sq, int64_t Skv, int64_t d, int layout, int round_mode,
+             attn_stream_t stream);
+
+/* Bytes of workspace attn_fwd_ws() needs for this shape with default options (0 if none). */
+size_t attn_fwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t d);
+
+/*
+ * attn_fwd_ws -- attn_fwd with caller-owned workspace (device memory, 16-byte aligned,
+ * at least attn_fwd_workspace_size() bytes for these options; may be NULL when that is 0)
+ * and optional knobs (opts may be NULL).  Allocates nothing.
+ */
+int attn_fwd_ws(const void* q, const void* k, const void* v, void* o, int64_t B, int64_t H,
+                int64_t Sq, int64_t Skv, int64_t d, int layout, int round_mode,
+                const attn_options_t* opts, void* workspace, size_t workspace_bytes,
+                attn_stream_t stream);
+
+/* Workspace bytes for a shape under the given options (opts may be NULL). */
+size_t attn_fwd_workspace_size_opts(int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t d,
+                                    const attn_options_t* opts);
+
+/*
+ * attn_plan -- the work split for a shape on a GPU with `num_sms` SMs (host only).  Returns
+ * ATTN_OK and fills *plan, or an argument error.  The same function drives the launches.
+ */
+int attn_plan(int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t d, int64_t num_sms,
+              const attn_options_t* opts, attn_plan_t* plan);
+
+/*
+ * attn_get_device_status -- synchronizes `stream`, then reads and clears the current
+ * device's status word.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT, or ATTN_ERR_CUDA.  If
+ * site != NULL it receives the id of the wait that expired (0 if none).
+ */
+int attn_get_device_status(attn_stream_t stream, int32_t* site);
+
+/* Static string for a status code. */
+const char* attn_status_string(int status);
+
+/* Library version, as major*10000 + minor*100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BF16_ATTN_H_ */

@@ -1,0 +1,114 @@
+"""The C-ABI library on the host: it builds, loads, exports every declared symbol, rejects
+bad arguments before touching CUDA, and its planner obeys its invariants (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import bf16_attention_forward_gb300 as attn
+from bf16_attention_forward_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bf16_attn.h")
+NO_GPU = not torch.cuda.is_available()
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return attn.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "attn_fwd" in names and "attn_fwd_ws" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(attn.EXPORTS) <= set(names)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.attn_version() >= 100
+    for code in range(9):
+        assert attn.status_string(code)
+    assert "unknown" in attn.status_string(99)
+
+
+P = 0x10000   # fake, aligned, never dereferenced: every call below fails validation first
+
+
+def call(lib, q=P, k=2 * P, v=3 * P, o=4 * P, B=1, H=1, Sq=8, Skv=8, d=128, layout=0, mode=0):
+    return lib.attn_fwd(q, k, v, o, B, H, Sq, Skv, d, layout, mode, None)
+
+
+def test_argument_errors(lib):
+    assert call(lib, q=0) == 1
+    assert call(lib, o=0) == 1
+    for kw in ({"B": 0}, {"H": -1}, {"Sq": 0}, {"Skv": 0}, {"layout": 2}, {"mode": 3},
+               {"mode": -1}):
+        assert call(lib, **kw) == 1, kw
+    assert call(lib, d=64) == 2
+    assert call(lib, Sq=(1 << 30) + 1) == 2
+    assert call(lib, q=P + 8) == 3
+    assert call(lib, o=P + 2) == 3
+    # o overlapping q: q occupies [P, P + 8*128*2)
+    assert call(lib, o=P + 1024) == 4
+    assert call(lib, o=2 * P, k=2 * P + 1024) == 4
+
+
+def test_ws_entry_validates_too(lib):
+    f = lib.attn_fwd_ws
+    assert f(0, P, P, P, 1, 1, 8, 8, 128, 0, 0, None, None, 0, None) == 1
+    assert f(P, 2 * P, 3 * P, 4 * P, 1, 1, 8, 8, 64, 0, 0, None, None, 0, None) == 2
+
+
+@pytest.mark.skipif(not NO_GPU, reason="valid arguments would launch on a real GPU")
+def test_valid_args_without_gpu_report_no_device(lib):
+    assert call(lib) == 5
+    assert lib.attn_fwd_workspace_size(1, 1, 8, 8, 128) == 0
+
+
+PLAN_SHAPES = [(1, 2, 128, 128), (4, 16, 2048, 2048), (2, 24, 4096, 300),
+               (1, 12, 32760, 32760), (1, 8, 128, 65536), (3, 5, 1000, 7), (1, 1, 1, 1),
+               (7, 3, 511, 4097), (1, 1, 256, 1 << 20)]
+
+
+@pytest.mark.parametrize("shape", PLAN_SHAPES)
+@pytest.mark.parametrize("sms", [1, 7, 148, 152])
+def test_planner_invariants(lib, shape, sms):
+    B, H, Sq, Skv = shape
+    p = attn.plan(B, H, Sq, Skv, 128, sms)
+    units = B * H * -(-Sq // 256)
+    nkv = -(-Skv // 128)
+    assert p["units"] == units and p["kv_tiles"] == nkv
+    assert p["full_items"] + p["split_units"] == units
+    assert p["items"] == p["full_items"] + p["split_units"] * p["splits"]
+    assert 1 <= p["grid"] <= min(sms, p["items"])
+    if p["split_units"]:
+        assert 2 <= p["splits"] <= nkv and nkv // p["splits"] >= 4
+        # the split tail fills at most one round, after whole rounds of full units
+        assert p["split_units"] * p["splits"] <= sms
+        assert p["full_items"] % sms == 0
+        assert p["workspace_bytes"] == p["split_units"] * p["splits"] * 256 * (128 * 4 + 4)
+    else:
+        assert p["splits"] == 1 and p["workspace_bytes"] == 0
+    assert attn.plan(B, H, Sq, Skv, 128, sms) == p          # pure function of its inputs
+
+
+def test_planner_forced_options(lib):
+    p = attn.plan(1, 2, 300, 1100, 128, 152, force_splits=3)
+    assert p["split_units"] == p["units"] and p["splits"] == 3 and p["full_items"] == 0
+    p = attn.plan(1, 2, 300, 300, 128, 152, force_splits=50)
+    assert p["splits"] == 3                                   # capped at the key tiles
+    p = attn.plan(4, 16, 2048, 2048, 128, 152, max_ctas=5)
+    assert p["grid"] == 5
+    with pytest.raises(attn.AttnError):
+        attn.plan(1, 1, 1, 1, 64)

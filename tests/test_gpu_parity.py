@@ -1,0 +1,165 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle (needs a GB300).
+
+Shapes span several query/key tiles with ragged tails, both layouts and all three rounding
+modes; the five named workloads run at full size with the oracle evaluated on a seeded
+sample of rows (always including the first and last row of every (b, h)).  Also checked:
+bitwise determinism, BSHD == BHSD, split == no split within the criteria, non-finite
+single-injection cases and the Skv = 1 / constant-V closed forms.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import parity
+from workloads import WORKLOADS, make_qkv, make_workload, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+MODES = ("rtne", "rtna", "rtz")
+
+
+@pytest.fixture(scope="module")
+def attn():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import bf16_attention_forward_gb300 as a
+    a.load()
+    return a
+
+
+def run(attn, q, k, v, layout, mode, **kw):
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    o = attn.attn_fwd(qd, kd, vd, layout=layout, round=mode, **kw)
+    torch.cuda.synchronize()
+    st, site = attn.device_status()
+    assert st == 0, "device status %d at wait site %d" % (st, site)
+    return o
+
+
+def check(attn, q, k, v, layout, mode, rows=None, **kw):
+    o = run(attn, q, k, v, layout, mode, **kw)
+    ref = oracle.attention(q, k, v, layout, mode, rows=rows, want_a=True)
+    g = parity.gpu_rows_bits(o, layout, rows)
+    res = parity.compare(g, ref["o_bits"], ref["a"])
+    assert res["ok"], res
+    return res, o
+
+
+SMALL = [  # (B, H, Sq, Skv)
+    (1, 1, 1, 1), (1, 1, 128, 128), (1, 1, 127, 129), (1, 2, 129, 127), (2, 1, 300, 300),
+    (1, 1, 1, 1000), (1, 3, 257, 64), (2, 2, 513, 385), (1, 1, 700, 900),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "B%dH%dSq%dSkv%d" % s)
+@pytest.mark.parametrize("layout", ["bshd", "bhsd"])
+def test_small_shapes_all_modes(attn, shape, layout):
+    B, H, Sq, Skv = shape
+    q, k, v = make_qkv(B, H, Sq, Skv, 128, layout, seed=sum(shape))
+    for mode in MODES:
+        check(attn, q, k, v, layout, mode)
+
+
+def test_tiny_workload(attn):
+    w = WORKLOADS["tiny"]
+    q, k, v = make_workload(w)
+    res, _ = check(attn, q, k, v, w.layout, "rtne")
+    assert res["literal_frac"] > 0.9
+
+
+@pytest.mark.parametrize("splits", [2, 3, 7])
+def test_forced_split_matches_oracle(attn, splits):
+    q, k, v = make_qkv(1, 2, 300, 1100, 128, "bhsd", seed=77, sigma=2.0)
+    check(attn, q, k, v, "bhsd", "rtna", force_splits=splits)
+
+
+def test_split_and_plain_agree_and_grid_limit(attn):
+    q, k, v = make_qkv(2, 3, 600, 1500, 128, "bshd", seed=78)
+    a = run(attn, q, k, v, "bshd", "rtne")
+    b = run(attn, q, k, v, "bshd", "rtne", force_splits=4)
+    c = run(attn, q, k, v, "bshd", "rtne", max_ctas=5)
+    ref = oracle.attention(q, k, v, "bshd", "rtne", want_a=True)
+    for o in (a, b, c):
+        r = parity.compare(parity.gpu_rows_bits(o, "bshd"), ref["o_bits"], ref["a"])
+        assert r["ok"], r
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))   # same math, fewer CTAs
+
+
+def test_deterministic(attn):
+    q, k, v = make_qkv(1, 4, 1000, 3000, 128, "bshd", seed=79)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    outs = [attn.attn_fwd(qd, kd, vd, layout="bshd", round="rtz") for _ in range(3)]
+    outs.append(attn.attn_fwd(qd, kd, vd, layout="bshd", round="rtz", force_splits=3))
+    outs.append(attn.attn_fwd(qd, kd, vd, layout="bshd", round="rtz", force_splits=3))
+    torch.cuda.synchronize()
+    for o in outs[1:3]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    assert torch.equal(outs[3].view(torch.int16), outs[4].view(torch.int16))
+
+
+def test_bshd_equals_bhsd(attn):
+    q, k, v = make_qkv(2, 3, 333, 444, 128, "bshd", seed=80)
+    t = lambda x: x.permute(0, 2, 1, 3).contiguous()
+    a = run(attn, q, k, v, "bshd", "rtne")
+    b = run(attn, t(q), t(k), t(v), "bhsd", "rtne")
+    assert torch.equal(t(a).view(torch.int16), b.view(torch.int16))
+
+
+def test_single_key_and_constant_v(attn):
+    q, k, v = make_qkv(2, 3, 200, 1, 128, "bhsd", seed=81, sigma=3.0)
+    for mode in MODES:
+        o = run(attn, q, k, v, "bhsd", mode)
+        assert torch.equal(o.cpu().view(torch.int16),
+                           v.expand(2, 3, 200, 128).contiguous().view(torch.int16))
+    q, k, _ = make_qkv(1, 2, 300, 517, 128, "bhsd", seed=82, sigma=2.0)
+    c = torch.randn(128, generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    v = c.view(1, 1, 1, 128).expand(1, 2, 517, 128).contiguous()
+    o = run(attn, q, k, v, "bhsd", "rtne")
+    d = (o.cpu().view(torch.int16).int() - c.view(torch.int16).int()).abs()
+    assert int(d.max()) <= 1
+
+
+def test_nonfinite_single_injections(attn):
+    B, H, Sq, Skv = 1, 2, 260, 300
+    q, k, v = make_qkv(B, H, Sq, Skv, 128, "bhsd", seed=83)
+    q, k, v = q.clone(), k.clone(), v.clone()
+    q[0, 0, 3, 5] = float("nan")                 # one query row NaN
+    k[0, 1, 17, 9] = float("inf")                # +/-inf logits depending on q sign
+    q[0, 1, :, 9] = torch.where(torch.arange(Sq) % 2 == 0, 1.0, -1.0).to(torch.bfloat16)
+    v[0, 1, 17, 30] = float("inf")               # -inf logit x inf v -> NaN column
+    v[0, 0, 40, 7] = float("-inf")               # finite logits: -inf column
+    v[0, 0, 41, 8] = float("inf")
+    v[0, 0, 42, 8] = float("-inf")               # +inf and -inf -> NaN column
+    for mode in MODES:
+        for fs in (0, 2):
+            check(attn, q, k, v, "bhsd", mode, force_splits=fs)
+
+
+def test_underflowed_weight_keeps_infinity(attn):
+    q = torch.zeros(1, 1, 128, 128, dtype=torch.bfloat16)
+    q[..., 0] = 128.0
+    k = torch.zeros(1, 1, 200, 128, dtype=torch.bfloat16)
+    k[0, 0, 150, 0] = 96.0                       # logit ~1086 for key 150, 0 for the rest
+    v = torch.ones(1, 1, 200, 128, dtype=torch.bfloat16)
+    v[0, 0, 0, 7] = float("-inf")                # key 0 weight e^-1086 -> still -inf
+    for fs in (0, 2):
+        check(attn, q, k, v, "bhsd", "rtne", force_splits=fs)
+
+
+@pytest.mark.parametrize("name", ["square", "cross", "video", "stress"])
+def test_workload_sampled_rows(attn, name):
+    w = WORKLOADS[name]
+    q, k, v = make_workload(w)
+    n = 256 if name == "video" else 1024
+    rows = sample_rows(w.B, w.H, w.Sq, n, seed=w.seed)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    for mode in w.modes:
+        o = attn.attn_fwd(qd, kd, vd, layout=w.layout, round=mode)
+        o2 = attn.attn_fwd(qd, kd, vd, layout=w.layout, round=mode)
+        torch.cuda.synchronize()
+        assert attn.device_status()[0] == 0
+        assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
+        ref = oracle.attention(q, k, v, w.layout, mode, rows=rows, want_a=True)
+        res = parity.compare(parity.gpu_rows_bits(o, w.layout, rows), ref["o_bits"], ref["a"])
+        assert res["ok"], (name, mode, res)
