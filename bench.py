@@ -1,0 +1,394 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 bf16 attention forward (one JSON line on rank 0).
+
+Metric: attention forward TFLOPS = 4*B*H*Sq*Skv*d per call / time, and its fraction of the
+measured GB300 dense bf16 peak.  Default workload: the square self-attention B=4, H=16,
+Sq=Skv=2048, d=128, BHSD, where one step runs the three output rounding modes (RTNE, RTNA,
+RTZ) back to back.  Inputs are seeded synthetic N(0,1) bf16 tensors already resident in HBM;
+consecutive calls rotate over enough input sets that their total exceeds the 126 MB L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+--impl reference times the CPU oracle (fp64, OpenMP) on a bounded sample of the same
+workload on the host cores.  Under torchrun (N > 1) each rank runs an independent replica
+(no collective on the data path); value = all ranks' flops / max elapsed time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, make_qkv  # noqa: E402
+
+METRIC = "attention fwd TFLOPS (4*B*H*Sq*Skv*d) and % of GB300 bf16 dense peak"
+FALLBACK_PEAK_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_STEPS = {"square": 1000, "cross": 1000, "video": 60, "stress": 1000, "tiny": 1000}
+DEFAULT_WARMUP = {"square": 100, "cross": 100, "video": 5, "stress": 100, "tiny": 100}
+L2_BYTES = 126 * 2**20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--workload", default="square", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0) or 0), \
+            float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_PEAK_TFLOPS, 0.0, FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bf16_attention_forward_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary, if it
+    was taken on the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "attn_fwd_kernel_%s_traffic.md" % workload)
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    kv = {}
+    for ln in lines:
+        if ln.startswith("- ") and ":" in ln:
+            k_, v_ = ln[2:].split(":", 1)
+            kv[k_.strip()] = v_.strip().strip("`")
+    if kv.get("source_sha256_16") != source_hash():
+        return None
+    try:
+        return int(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, enabled: bool = True):
+        self.dev = device_index
+        self.enabled = enabled
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        if not self.enabled:
+            return self
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.enabled or self.proc is None or not self.path:
+            return None
+        rows = []
+        for ln in open(self.path):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2])
+                          if v.lower().startswith("active")})
+        loaded = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_oracle_sample(w, qkv_cpu, mode: str, seconds: float, seed: int = 99):
+    """Time the oracle on a seeded row sample sized to about `seconds` of host work."""
+    import oracle
+    q, k, v = qkv_cpu
+    total = w.B * w.H * w.Sq
+    threads = len(os.sched_getaffinity(0))
+    g = torch.Generator().manual_seed(seed)
+    probe = torch.randint(0, total, (max(threads, 8),), generator=g).tolist()
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.layout, mode, rows=probe, threads=threads)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    n = int(max(threads, min(total, len(probe) * seconds / dt)))
+    rows = torch.randint(0, total, (n,), generator=g).tolist()
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.layout, mode, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    flop = 4.0 * n * w.Skv * w.d
+    return {"value": flop / dt / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d query rows (seeded), all %d keys, mode %s, %.1f s"
+                      % (n, total, w.Skv, mode, dt)}
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return 0
+    steps = args.steps if args.steps is not None else DEFAULT_STEPS[w.name]
+    warmup = args.warmup if args.warmup is not None else DEFAULT_WARMUP[w.name]
+    import oracle
+    q, k, v = make_qkv(w.B, w.H, w.Sq, w.Skv, w.d, w.layout, seed=w.seed, sigma=w.sigma,
+                       nonfinite_frac=w.nonfinite_frac)
+    threads = len(os.sched_getaffinity(0))
+    total = w.B * w.H * w.Sq
+    budget = 150.0                           # seconds for the whole run
+    g = torch.Generator().manual_seed(7)
+    probe = torch.randint(0, total, (max(threads, 8),), generator=g).tolist()
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.layout, w.modes[0], rows=probe, threads=threads)
+    per_row = max(time.perf_counter() - t0, 1e-4) / len(probe)
+    rows_per_step = int(max(1, min(total, budget / (steps + warmup) / per_row)))
+    samples = [torch.randint(0, total, (rows_per_step,), generator=g).tolist()
+               for _ in range(min(steps + warmup, 8))]
+    for i in range(warmup):
+        oracle.attention(q, k, v, w.layout, w.modes[i % len(w.modes)],
+                         rows=samples[i % len(samples)], threads=threads)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        oracle.attention(q, k, v, w.layout, w.modes[i % len(w.modes)],
+                         rows=samples[i % len(samples)], threads=threads)
+    dt = time.perf_counter() - t0
+    flop = 4.0 * rows_per_step * w.Skv * w.d * steps
+    val = flop / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOPS", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": dt * 1e3 / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,%g) bf16)" % w.sigma,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Skv": w.Skv, "d": w.d,
+                   "layout": w.layout, "modes": list(w.modes),
+                   "step": "oracle on %d seeded query rows (all keys)" % rows_per_step},
+        "cpu_baseline": {"value": val, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": "%d of %d query rows per step" % (rows_per_step, total)},
+        "e2e": {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import bf16_attention_forward_gb300 as attn
+    attn.load()
+
+    steps = args.steps if args.steps is not None else DEFAULT_STEPS[w.name]
+    warmup = max(3, args.warmup if args.warmup is not None else DEFAULT_WARMUP[w.name])
+    modes = list(w.modes)
+    set_bytes = 2 * w.B * w.H * w.d * (2 * w.Sq + 2 * w.Skv)   # q, k, v, o
+    nsets = max(1, -(-(2 * L2_BYTES) // set_bytes)) if set_bytes < 2 * L2_BYTES else 1
+    cpu_sets = [make_qkv(w.B, w.H, w.Sq, w.Skv, w.d, w.layout, seed=w.seed + 1000 * i,
+                         sigma=w.sigma, nonfinite_frac=w.nonfinite_frac) for i in range(nsets)]
+    sets = [tuple(t.to(dev) for t in s) for s in cpu_sets]
+    outs = [torch.empty_like(s[0]) for s in sets]
+    plan = attn.plan(w.B, w.H, w.Sq, w.Skv, w.d, torch.cuda.get_device_properties(dev).multi_processor_count)
+    split = plan["split_units"] > 0
+    ws_bytes = attn.workspace_size(w.B, w.H, w.Sq, w.Skv, w.d)
+    workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    calls_per_step = len(modes)
+    n_launch = steps * calls_per_step
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_launch)]
+    for trio in ev:            # torch creates the CUDA event on its first record
+        for e in trio:
+            e.record(stream)
+
+    def call(i, mode, events=None):
+        s = sets[i % nsets]
+        attn.attn_fwd(s[0], s[1], s[2], outs[i % nsets], layout=w.layout, round=mode,
+                      workspace=workspace, events=events)
+
+    for i in range(warmup * calls_per_step):
+        call(i, modes[i % calls_per_step])
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local, enabled=not args.no_clocks) as clocks:
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        t_start.record(stream)
+        for i in range(n_launch):
+            call(i, modes[i % calls_per_step], events=ev[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+    st, site = attn.device_status()
+    assert st == 0, "device status %d at wait site %d" % (st, site)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    main_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    comb_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    flop_call = w.flop
+    value = world * flop_call * n_launch / (elapsed_ms * 1e-3) / 1e12
+
+    peak, peak_sust, hbm, peak_src = measured_peaks()
+    main_avg = statistics.mean(main_ms)
+    achieved = flop_call / (main_avg * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                "kernel": "attn_fwd_kernel", "peak_source": peak_src + " burst bf16 (cuBLAS)",
+                "frac_of_sustained": (achieved / peak_sust) if peak_sust else None,
+                "kernel_ms_avg": main_avg, "kernel_ms_median": statistics.median(main_ms)}
+    extra = {}
+    if split:
+        rows = plan["split_units"] * 256
+        comb_bytes = rows * plan["splits"] * (128 * 4 + 4) + min(rows, w.B * w.H * w.Sq) * 256
+        ca = statistics.mean(comb_ms)
+        extra["combine"] = {"ms_avg": ca, "algorithmic_bytes": comb_bytes,
+                            "achieved_gbs": comb_bytes / (ca * 1e-3) / 1e9, "peak_gbs": hbm,
+                            "frac": comb_bytes / (ca * 1e-3) / 1e9 / hbm}
+
+    # end to end through the public API with host buffers (pinned), copies timed
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.pin_memory() for t in cpu_sets[0])
+        ho = [torch.empty(hq.shape, dtype=hq.dtype).pin_memory() for _ in modes]
+        dq, dk, dv = (torch.empty_like(sets[0][0]), torch.empty_like(sets[0][1]),
+                      torch.empty_like(sets[0][2]))
+        do = [torch.empty_like(sets[0][0]) for _ in modes]
+        e2e_steps = max(3, min(steps, 50))
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            for m, mode in enumerate(modes):
+                attn.attn_fwd(dq, dk, dv, do[m], layout=w.layout, round=mode,
+                              workspace=workspace)
+                ho[m].copy_(do[m], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = sum(t.numel() * 2 for t in (hq, hk, hv))
+        d2h = sum(t.numel() * 2 for t in ho)
+        e2e = {"value": world * flop_call * len(modes) * e2e_steps / (e2e_ms * 1e-3) / 1e12,
+               "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(w, cpu_sets[0], modes[0], seconds=12.0)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": elapsed_ms / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,%g) bf16%s)" % (
+                w.sigma, ", %g non-finite K/V" % w.nonfinite_frac if w.nonfinite_frac else ""),
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Skv": w.Skv,
+                       "d": w.d, "layout": w.layout, "modes": modes,
+                       "step": "%d calls (one per rounding mode)" % calls_per_step,
+                       "l2": ("rotating %d input sets, %.0f MB > 126 MB L2" % (nsets, nsets * set_bytes / 2**20))
+                             if nsets > 1 else "inputs %.0f MB > 126 MB L2" % (set_bytes / 2**20),
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "plan": plan},
+            "pct_of_peak": 100.0 * value / peak,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks.summary(),
+            "gpu_launches": n_launch * (2 if split else 1),
+            "source_sha256_16": source_hash(),
+        }
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

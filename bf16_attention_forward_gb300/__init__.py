@@ -32,7 +32,8 @@ class AttnError(RuntimeError):
 
 class Options(ctypes.Structure):
     _fields_ = [("force_splits", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
-                ("wait_limit_ms", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+                ("wait_limit_ms", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
+                ("events", ctypes.c_void_p * 3)]
 
 
 class Plan(ctypes.Structure):
@@ -101,10 +102,14 @@ def _dims(q, k, layout):
     return int(B), int(H), int(Sq), int(Skv), int(d)
 
 
-def _opts(force_splits=0, max_ctas=0, wait_limit_ms=0):
-    if not (force_splits or max_ctas or wait_limit_ms):
+def _opts(force_splits=0, max_ctas=0, wait_limit_ms=0, events=None):
+    if not (force_splits or max_ctas or wait_limit_ms or events):
         return None
-    return Options(int(force_splits), int(max_ctas), int(wait_limit_ms), 0)
+    o = Options(int(force_splits), int(max_ctas), int(wait_limit_ms), 0)
+    if events:
+        for i, e in enumerate(events[:3]):
+            o.events[i] = None if e is None else int(e.cuda_event)
+    return o
 
 
 def plan(B, H, Sq, Skv, d=128, num_sms=152, force_splits=0, max_ctas=0) -> dict:
@@ -125,11 +130,14 @@ def workspace_size(B, H, Sq, Skv, d=128, force_splits=0, max_ctas=0) -> int:
 
 
 def attn_fwd(q, k, v, o=None, layout: str = "bshd", round: str = "rtne", stream=None,
-             workspace=None, force_splits: int = 0, max_ctas: int = 0, wait_limit_ms: int = 0):
+             workspace=None, force_splits: int = 0, max_ctas: int = 0, wait_limit_ms: int = 0,
+             events=None):
     """O = softmax(Q K^T / sqrt(128)) V on CUDA tensors (bf16, contiguous, same layout).
 
     ``workspace``: optional caller tensor (any dtype, CUDA) used through ``attn_fwd_ws``;
-    with the knobs set and no workspace, one is allocated here with torch.  Returns ``o``.
+    with the knobs set and no workspace, one is allocated here with torch.  ``events``: up to
+    three ``torch.cuda.Event`` recorded around the attention and combine kernels on the
+    launching stream.  Returns ``o``.
     """
     import torch
     if layout not in LAYOUTS or round not in MODES:
@@ -145,7 +153,7 @@ def attn_fwd(q, k, v, o=None, layout: str = "bshd", round: str = "rtne", stream=
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     sp = ctypes.c_void_p(s.cuda_stream if hasattr(s, "cuda_stream") else int(s))
     lib = load()
-    opts = _opts(force_splits, max_ctas, wait_limit_ms)
+    opts = _opts(force_splits, max_ctas, wait_limit_ms, events)
     if workspace is None and opts is None:
         st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, Sq,
                           Skv, d, LAYOUTS[layout], MODES[round], sp)

@@ -55,13 +55,25 @@ constexpr int kThreads = 384;      // WG0, WG1 softmax; warp 8 TMA; warp 9 MMA; 
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
 constexpr int kMinTilesPerSplit = 4;
+// Register split (launch: 384 threads x 168 = 64512).  Softmax warpgroups 0-1 grow to 200,
+// warpgroup 2 (TMA, MMA, two spare warps) shrinks to 104: 256*200 + 128*104 = 64512.
+constexpr uint32_t kRegsSoftmax = 200;
+constexpr uint32_t kRegsOther = 104;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= 65536 / kThreads * kThreads,
+              "register split exceeds the launch budget");
 constexpr uint32_t kTmemCols = 512;   // S0 | S1 | O0 | O1, 128 fp32 columns each
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int kSmemQ = 0;
 constexpr int kSmemRing = kSmemQ + kQTiles * kTileBytes;
-constexpr int kSmemBars = kSmemRing + kStages * kTileBytes;
-constexpr int kNumBars = 2 * kStages + 2 + 3 * kQTiles + 1;
+// Output staging: one 8 KB region per TMEM lane quarter (32 rows x 256 B of bf16, as two
+// 64-column halves in the 128-byte swizzle TMA expects), shared by the two query tiles' warps
+// of that quarter in turn.
+constexpr int kStageRowsPerWarp = 32;
+constexpr int kStageBytes = kStageRowsPerWarp * kD * 2;
+constexpr int kSmemStage = kSmemRing + kStages * kTileBytes;
+constexpr int kSmemBars = kSmemStage + 4 * kStageBytes;
+constexpr int kNumBars = 2 * kStages + 2 + 3 * kQTiles + 1 + 4;
 constexpr int kSmemMisc = kSmemBars + kNumBars * 8;
 constexpr int kSmemUsed = kSmemMisc + 16;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
@@ -75,11 +87,12 @@ constexpr int kBarSFull = kBarQEmpty + 1;   // [2] S_i ready in TMEM
 constexpr int kBarPFull = kBarSFull + 2;    // [2] P_i written (and O_i rescaled)
 constexpr int kBarOFull = kBarPFull + 2;    // [2] last PV of the unit done
 constexpr int kBarDrain = kBarOFull + 2;
+constexpr int kBarStageFree = kBarDrain + 1;  // [4] staging region q read out by its TMA store
 
 // wait sites reported through the status word
 enum : uint32_t {
     kSiteQEmpty = 1, kSiteRingEmpty, kSiteQFull, kSiteRingFull, kSitePFull, kSiteSFull,
-    kSiteOFull, kSiteDrain, kSiteTeardown
+    kSiteOFull, kSiteDrain, kSiteTeardown, kSiteStage
 };
 
 __device__ uint32_t g_status[2];   // [0] status code, [1] wait site
@@ -130,7 +143,7 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int k) {
 
 // Bounded mbarrier wait.  On expiry it records the site in the status word, raises the
 // CTA's abort flag and returns false; every other wait then gives up at once.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t site,
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t site,
                                       volatile uint32_t* abort_flag,
                                       unsigned long long limit_ns) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -176,17 +189,22 @@ __device__ __forceinline__ uint32_t round_bf16_bits(float f, int mode) {
     return u >> 16;
 }
 
-// softmax weight exponent for logit s: x = s*c - m*c, kept >= -125 when s is finite so that
-// a finite logit always has a positive bf16 weight; -inf stays -inf (weight exactly 0) and
-// NaN stays NaN.  The fma with 2^-40 moves finite x by < 1e-9 relative.
-__device__ __forceinline__ float weight_exponent(float s, float c, float neg_mc) {
-    const float x = fmaf(s, c, neg_mc);
-    return fmaf(x, 0x1p-40f, ptx::fmax_nan(x, -125.0f));
+// softmax weight exponent for logit s relative to the reference m: x = (s - m) * c, which is
+// exactly 0 for the key that set m (so a lone key gets weight 1 and O = its V row), kept
+// >= -125.02 when s is finite so that a finite logit always has a positive (normal) weight;
+// -inf stays -inf (weight exactly 0) and NaN stays NaN.  For x >= -124 the fma returns x
+// unchanged (x * 2^-126 is far below half an ulp of x); for finite x < -124 it gives
+// -124 - |x| * 2^-126 >= -125.02 since |x| < 2^127.
+constexpr float kMinExponent = -124.0f;
+__device__ __forceinline__ float weight_exponent(float s, float c, float m) {
+    const float x = (s - m) * c;
+    return fmaf(x, 0x1p-126f, ptx::fmax_nan(x, kMinExponent));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                const __grid_constant__ CUtensorMap vmap, const FwdParams p) {
+                const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                const FwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = ptx::smem_u32(smem);
@@ -211,6 +229,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             ptx::mbar_init(bar(kBarOFull + i), 1);
         }
         ptx::mbar_init(bar(kBarDrain), 1);
+        for (int q = 0; q < 4; ++q) ptx::mbar_init(bar(kBarStageFree + q), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
@@ -224,14 +243,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     const uint32_t tmem = *tmem_holder;
     const unsigned long long lim = p.wait_limit_ns;
 
-    if (warp == kWarpTma) {
-        // ------------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+    if (warp >= 8) {
+        ptx::reg_dealloc<kRegsOther>();
+        if (warp == kWarpTma && lane == 0) {
+            // -------------------------------------------------------------- TMA producer
             const uint64_t pol_kv = ptx::policy_evict_last();
             const uint64_t pol_q = ptx::policy_evict_first();
             uint32_t pos = 0;             // ring position (monotonic)
-            int last_pos[kStages];
-            for (int s = 0; s < kStages; ++s) last_pos[s] = -1;
             int u = 0;
             bool ok = true;
             for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
@@ -264,43 +282,59 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                             else
                                 ptx::tma_load_4d(dst, map, bar(kBarFull + slot), c * 64, j * kBN, it.h, it.b, pol_kv);
                         }
-                        last_pos[slot] = (int)pos;
                     }
                 }
             }
-            // every load issued has landed before the CTA may exit
-            for (int s = 0; s < kStages; ++s)
-                if (last_pos[s] >= 0) {
-                    const uint32_t ph = ((uint32_t)last_pos[s] / kStages) & 1u;
-                    const uint64_t t0 = ptx::globaltimer_ns();
-                    while (!ptx::mbar_try_wait(bar(kBarFull + s), ph) &&
-                           ptx::globaltimer_ns() - t0 < lim) {
-                    }
+            // every load issued has landed before the CTA may exit: the last kStages
+            // positions cover each slot's most recent load
+            for (uint32_t q = (pos > kStages ? pos - kStages : 0); q < pos; ++q) {
+                const uint32_t ph = (q / kStages) & 1u;
+                const uint64_t t0 = ptx::globaltimer_ns();
+                while (!ptx::mbar_try_wait(bar(kBarFull + q % kStages), ph) && ptx::globaltimer_ns() - t0 < lim) {
                 }
-        }
-    } else if (warp == kWarpMma) {
-        // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+            }
+        } else if (warp == kWarpMma && lane == 0) {
+            // -------------------------------------------------------------- MMA issuer
             constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16(kBM, kD, false, true);
-            const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
-            const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
+            // TMEM columns: S_t at 128*t, O_t at 256 + 128*t
             // Q_i / K_j: K-major, 128 B rows, 8-row swizzle atoms 1024 B apart; the k-th
             // 16-element step sits 32 B further inside the atom, the second 64-column half
             // 16 KB further.  V_j: MN-major (d contiguous), the two 64-column halves 16 KB
             // apart (leading offset), 8-key groups 1024 B apart (stride offset); the k-th
             // 16-key step is 2 KB further.
-            auto qdesc = [&](int t, int kk) {
-                return sdesc(sbase + kSmemQ + (t * 2 + (kk >> 2)) * kChunkBytes + (kk & 3) * 32, 16, 1024);
+            // Base descriptors; the address field counts 16-byte units, so moving the start
+            // address by b bytes adds b >> 4 to the descriptor (no carry out of the field:
+            // every address stays below 256 KB).
+            const uint64_t dq0 = sdesc(sbase + kSmemQ, 16, 1024);
+            const uint64_t dring = sdesc(sbase + kSmemRing, 16, 1024);
+            const uint64_t dvring = sdesc(sbase + kSmemRing, kChunkBytes, 1024);
+            // S_t = Q_t K^T: 8 steps of 16 along d (32 B inside a 64-column half, then the
+            // other half 16 KB on).  Fully unrolled with constant offsets from one base
+            // descriptor per operand: a rolled loop that recomputes descriptors costs ~200
+            // cycles per MMA in issue, three times the 64-cycle MMA itself.
+            auto issue_s = [&](int t, uint32_t kslot) {
+                const uint64_t a0 = dq0 + (uint64_t)((t * 2 * kChunkBytes) >> 4);
+                const uint64_t b0 = dring + (uint64_t)((kslot * kTileBytes) >> 4);
+                const uint32_t d = tmem + 128u * t;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4);
+                    ptx::mma_ss(d, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u);
+                }
             };
-            auto kdesc = [&](uint32_t slot, int kk) {
-                return sdesc(sbase + kSmemRing + slot * kTileBytes + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024);
-            };
-            auto vdesc = [&](uint32_t slot, int kk) {
-                return sdesc(sbase + kSmemRing + slot * kTileBytes + kk * 2048, kChunkBytes, 1024);
+            // O_t += P_t V: 8 steps of 16 keys (P: 8 TMEM columns each; V: 2 KB each)
+            auto issue_o = [&](int t, uint32_t vslot, bool first) {
+                const uint64_t b0 = dvring + (uint64_t)((vslot * kTileBytes) >> 4);
+                const uint32_t d = tmem + 256u + 128u * t, a = tmem + 128u * t;
+                const uint32_t acc0 = first ? 0u : 1u;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    ptx::mma_ts(d, a + (uint32_t)kk * 8u, b0 + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                kk > 0 ? 1u : acc0);
             };
             uint32_t pos = 0;
-            uint32_t pcount[2] = {0u, 0u};
+            uint32_t pcount = 0;   // P_t phases consumed (same count for both tiles)
             int u = 0;
             bool ok = true;
             for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
@@ -312,8 +346,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     break;
                 ptx::tc_fence_after();
                 for (int t = 0; t < kQTiles; ++t) {
-                    for (int kk = 0; kk < kD / 16; ++kk)
-                        ptx::mma_ss(tS[t], qdesc(t, kk), kdesc(kslot, kk), idesc_s, kk > 0);
+                    issue_s(t, kslot);
                     ptx::mma_commit(bar(kBarSFull + t));
                 }
                 ptx::mma_commit(bar(kBarEmpty + kslot));
@@ -328,13 +361,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     const uint32_t kpos = vpos + 1;
                     kslot = kpos % kStages;
                     for (int t = 0; t < kQTiles; ++t) {
-                        if (!(ok = wait_bar(bar(kBarPFull + t), pcount[t] & 1u, kSitePFull, abort_flag, lim)))
+                        if (!(ok = wait_bar(bar(kBarPFull + t), pcount & 1u, kSitePFull, abort_flag, lim)))
                             break;
-                        ++pcount[t];
                         ptx::tc_fence_after();
-                        for (int kk = 0; kk < kBN / 16; ++kk)
-                            ptx::mma_ts(tO[t], tS[t] + (uint32_t)kk * 8u, vdesc(vslot, kk), idesc_o,
-                                        (jj > 0 || kk > 0) ? 1u : 0u);
+                        issue_o(t, vslot, jj == 0);
                         if (!more) ptx::mma_commit(bar(kBarOFull + t));
                         if (t == kQTiles - 1) ptx::mma_commit(bar(kBarEmpty + vslot));
                         if (more) {
@@ -344,8 +374,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                                     break;
                                 ptx::tc_fence_after();
                             }
-                            for (int kk = 0; kk < kD / 16; ++kk)
-                                ptx::mma_ss(tS[t], qdesc(t, kk), kdesc(kslot, kk), idesc_s, kk > 0);
+                            issue_s(t, kslot);
                             ptx::mma_commit(bar(kBarSFull + t));
                             if (t == kQTiles - 1) {
                                 ptx::mma_commit(bar(kBarEmpty + kslot));
@@ -353,6 +382,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                             }
                         }
                     }
+                    ++pcount;
                     pos += more ? 2 : 1;
                 }
             }
@@ -362,7 +392,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             while (!ptx::mbar_try_wait(bar(kBarDrain), 0) && ptx::globaltimer_ns() - t0 < lim) {
             }
         }
-    } else if (warp < 2 * 4) {
+    } else {
+        ptx::reg_alloc<kRegsSoftmax>();
         // ------------------------------------------------------------------ softmax + epilogue
         const int t = warp >> 2;                    // query tile owned by this warpgroup
         const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
@@ -383,27 +414,34 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 ++scount;
                 ptx::tc_fence_after();
-                uint32_t s[4][32];
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) ptx::tmem_ld32(tS + ch * 32, s[ch]);
+                uint32_t s[128];
+                ptx::tmem_ld128(tS, s);
                 const int valid = p.Skv - j * kBN;   // keys of this tile that exist
                 if (valid < kBN) {
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (ch * 32 + e >= valid) s[ch][e] = __float_as_uint(-INFINITY);
+                    for (int e = 0; e < 128; ++e)
+                        if (e >= valid) s[e] = __float_as_uint(-INFINITY);
                 }
-                // row max as 8 independent chains, then a tree
-                float mp[8];
+                // row max and min: 3-input trees over 4 independent chains each
+                float mxa[4], mna[4];
 #pragma unroll
-                for (int q8 = 0; q8 < 8; ++q8) mp[q8] = __uint_as_float(s[0][q8]);
+                for (int q4 = 0; q4 < 4; ++q4) mxa[q4] = mna[q4] = __uint_as_float(s[q4]);
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
+                for (int e = 4; e < 124; e += 8) {
 #pragma unroll
-                    for (int e = (ch == 0 ? 8 : 0); e < 32; ++e) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(s[ch][e]));
-                const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                                       fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const float a = __uint_as_float(s[e + q4]), b = __uint_as_float(s[e + 4 + q4]);
+                        mxa[q4] = ptx::fmax3(mxa[q4], a, b);
+                        mna[q4] = ptx::fmin3(mna[q4], a, b);
+                    }
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    mxa[q4] = fmaxf(mxa[q4], __uint_as_float(s[124 + q4]));
+                    mna[q4] = fminf(mna[q4], __uint_as_float(s[124 + q4]));
+                }
+                const float mx = ptx::fmax3(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3]));
+                const float mn = ptx::fmin3(mna[0], mna[1], fminf(mna[2], mna[3]));
                 const float m_new = fmaxf(m_ref, mx);
                 bool rescale_o = false;
                 float alpha = 1.0f;
@@ -417,30 +455,49 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     l *= alpha;
                     m_ref = m_new;
                 }
-                const float neg_mc = (m_ref == -INFINITY) ? 0.0f : -m_ref * c;
-                float lp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // independent partial sums
+                const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+                // Every exponent of this row is >= -124 and no logit is -inf: the clamp that
+                // keeps underflowing finite weights positive cannot fire, so skip it.
+                const bool plain = mn > -INFINITY && (mn - m_use) * c >= kMinExponent;
+                const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
+                float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                  make_float2(0.f, 0.f)};
+                uint32_t pk[64];
+                if (__all_sync(0xFFFFFFFFu, plain)) {
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t pk[16];
+                    for (int e = 0; e < 64; ++e) {
+                        const float2 x = __fmul2_rn(
+                            __fadd2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), nm2), c2);
+                        const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+                        lsum[e & 3] = __fadd2_rn(lsum[e & 3], pp);
+                        pk[e] = ptx::pack_bf16x2(pp.x, pp.y);
+                    }
+                } else {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float p0 = ptx::ex2_approx(weight_exponent(__uint_as_float(s[ch][2 * e]), c, neg_mc));
-                        const float p1 = ptx::ex2_approx(weight_exponent(__uint_as_float(s[ch][2 * e + 1]), c, neg_mc));
-                        lp[(2 * e) & 7] += p0;
-                        lp[(2 * e + 1) & 7] += p1;
+                    for (int e = 0; e < 64; ++e) {
+                        const float p0 = ptx::ex2_approx(weight_exponent(__uint_as_float(s[2 * e]), c, m_use));
+                        const float p1 = ptx::ex2_approx(weight_exponent(__uint_as_float(s[2 * e + 1]), c, m_use));
+                        lsum[e & 3] = __fadd2_rn(lsum[e & 3], make_float2(p0, p1));
                         pk[e] = ptx::pack_bf16x2(p0, p1);
                     }
-                    ptx::tmem_st16(tS + ch * 16, pk);
                 }
-                l += ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
+                ptx::tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+                ptx::tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+                const float2 ls = __fadd2_rn(__fadd2_rn(lsum[0], lsum[1]), __fadd2_rn(lsum[2], lsum[3]));
+                l += ls.x + ls.y;
                 if (__any_sync(0xFFFFFFFFu, rescale_o)) {
                     const float a = rescale_o ? alpha : 1.0f;
+                    const float2 a2 = make_float2(a, a);
 #pragma unroll 1
                     for (int ch = 0; ch < 4; ++ch) {
                         uint32_t o[32];
                         ptx::tmem_ld32(tO + ch * 32, o);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), a2);
+                            o[2 * e] = __float_as_uint(v.x);
+                            o[2 * e + 1] = __float_as_uint(v.y);
+                        }
                         ptx::tmem_st32(tO + ch * 32, o);
                     }
                 }
@@ -455,10 +512,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             ptx::tc_fence_after();
             const int qrow = it.qb * kUnitRows + t * kBM + row;
             const bool valid_row = qrow < p.Sq;
+            // staging region of this lane quarter: query tile 0's warp and tile 1's warp take
+            // turns (tile 0 of item u, tile 1 of item u, tile 0 of item u+1, ...), so region
+            // release number 2u + t is this warp's; it waits for number 2u + t - 1
+            const uint32_t region = sbase + kSmemStage + (uint32_t)(quarter * kStageBytes);
+            if (u > 0 || t == 1) {
+                ok = wait_bar(bar(kBarStageFree + quarter), t == 0 ? 1u : 0u, kSiteStage, abort_flag, lim);
+                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+            }
             if (it.split_slot < 0) {
                 const float inv = 1.0f / l;
-                __nv_bfloat16* orow = p.o + (long long)it.b * p.o_sb + (long long)qrow * p.o_ss +
-                                      (long long)it.h * p.o_sh;
 #pragma unroll 1
                 for (int ch = 0; ch < 4; ++ch) {
                     uint32_t o[32];
@@ -470,12 +533,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                         const uint32_t hi = round_bf16_bits(__uint_as_float(o[2 * e + 1]) * inv, p.round_mode);
                         w[e] = lo | (hi << 16);
                     }
-                    if (valid_row) {
-                        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+                    // row `lane` of the region; 16-byte piece pc of the 64-column half is stored
+                    // at piece pc ^ (lane & 7) (128-byte swizzle)
+                    const uint32_t half = region + (uint32_t)((ch >> 1) * (kStageBytes / 2)) + (uint32_t)lane * 128u;
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        const uint32_t pc = (uint32_t)((ch & 1) * 4 + v4);
+                        ptx::st_shared_v4(half + ((pc ^ (uint32_t)(lane & 7)) << 4), w[4 * v4], w[4 * v4 + 1],
+                                          w[4 * v4 + 2], w[4 * v4 + 3]);
                     }
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int r0 = it.qb * kUnitRows + t * kBM + quarter * kStageRowsPerWarp;
+                    for (int hc = 0; hc < 2; ++hc) {
+                        const uint32_t src = region + (uint32_t)(hc * (kStageBytes / 2));
+                        if (p.bshd) ptx::tma_store_4d(&omap, src, hc * 64, it.h, r0, it.b);
+                        else ptx::tma_store_4d(&omap, src, hc * 64, r0, it.h, it.b);
+                    }
+                    ptx::bulk_commit();
+                    ptx::bulk_wait_read0();
+                    ptx::mbar_arrive(bar(kBarStageFree + quarter));
                 }
             } else {
                 // split partial: O/l in fp32 (the raw sum when l == 0) and LSE in log2 units
@@ -495,11 +574,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     }
                 }
                 if (valid_row) p.ws_lse[wrow] = m_ref * c + log2f(l);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(kBarStageFree + quarter));
             }
         }
     }
 
     // ---------------------------------------------------------------------- teardown
+    if (warp < 8 && lane == 0) ptx::bulk_wait0();   // this warp's output stores are complete
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == kWarpMma) {
@@ -666,18 +748,18 @@ int device_info(DeviceInfo** out) {
 
 // Tensor map over one bf16 tensor, dims ordered innermost-first so strides increase:
 // BSHD -> (d, H, S, B), BHSD -> (d, S, H, B); box = 64 d x 128 rows, 128-byte swizzle.
-bool encode_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t H, int64_t S, bool bshd) {
+bool encode_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t H, int64_t S, bool bshd, uint32_t rows = kBM) {
     cuuint64_t dims[4], strides[3];
     cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
     dims[0] = kD;
     if (bshd) {
         dims[1] = H; dims[2] = S; dims[3] = B;
         strides[0] = kD * 2; strides[1] = H * kD * 2; strides[2] = S * H * kD * 2;
-        box[0] = 64; box[1] = 1; box[2] = kBM; box[3] = 1;
+        box[0] = 64; box[1] = 1; box[2] = rows; box[3] = 1;
     } else {
         dims[1] = S; dims[2] = H; dims[3] = B;
         strides[0] = kD * 2; strides[1] = S * kD * 2; strides[2] = H * S * kD * 2;
-        box[0] = 64; box[1] = kBM; box[2] = 1; box[3] = 1;
+        box[0] = 64; box[1] = rows; box[2] = 1; box[3] = 1;
     }
     const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -689,9 +771,9 @@ int launch(const void* q, const void* k, const void* v, void* o, int64_t B, int6
            int layout, int round_mode, const attn_plan_t& pl, const attn_options_t* opts, void* ws,
            cudaStream_t stream) {
     const bool bshd = layout == ATTN_LAYOUT_BSHD;
-    CUtensorMap qm, km, vm;
+    CUtensorMap qm, km, vm, om;
     if (!encode_map(&qm, q, B, H, Sq, bshd) || !encode_map(&km, k, B, H, Skv, bshd) ||
-        !encode_map(&vm, v, B, H, Skv, bshd))
+        !encode_map(&vm, v, B, H, Skv, bshd) || !encode_map(&om, o, B, H, Sq, bshd, kStageRowsPerWarp))
         return ATTN_ERR_CUDA;
     FwdParams p;
     memset(&p, 0, sizeof p);
@@ -715,8 +797,11 @@ int launch(const void* q, const void* k, const void* v, void* o, int64_t B, int6
     const uint32_t ms = (opts && opts->wait_limit_ms) ? opts->wait_limit_ms : 2000u;
     p.wait_limit_ns = (unsigned long long)ms * 1000000ull;
 
-    attn_fwd_kernel<<<(unsigned)pl.grid, kThreads, kSmemAlloc, stream>>>(qm, km, vm, p);
+    const attn_event_t* ev = opts ? opts->events : nullptr;
+    if (ev && ev[0] && cudaEventRecord((cudaEvent_t)ev[0], stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    attn_fwd_kernel<<<(unsigned)pl.grid, kThreads, kSmemAlloc, stream>>>(qm, km, vm, om, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    if (ev && ev[1] && cudaEventRecord((cudaEvent_t)ev[1], stream) != cudaSuccess) return ATTN_ERR_CUDA;
     if (pl.split_units) {
         CombineParams c;
         c.H = (int)H; c.Sq = (int)Sq; c.nq = p.nq; c.nsplit = p.nsplit; c.n_full = p.n_full;
@@ -729,6 +814,7 @@ int launch(const void* q, const void* k, const void* v, void* o, int64_t B, int6
         attn_combine_kernel<<<blocks, warps_per_block * 32, 0, stream>>>(c);
         if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     }
+    if (ev && ev[2] && cudaEventRecord((cudaEvent_t)ev[2], stream) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
 

@@ -64,12 +64,19 @@ typedef enum {
     ATTN_ERR_DEVICE_TIMEOUT = 8  /* a bounded wait inside a kernel expired                 */
 } attn_status_t;
 
-/* Optional knobs (all zero = defaults). */
+/* A cudaEvent_t (the same handle type). */
+typedef struct CUevent_st* attn_event_t;
+
+/* Optional knobs (all zero / NULL = defaults). */
 typedef struct {
     int32_t force_splits;   /* 0: planner decides. n >= 1: split every unit's keys n ways  */
     int32_t max_ctas;       /* 0: one persistent CTA per SM. n >= 1: at most n CTAs         */
     uint32_t wait_limit_ms; /* 0: 2000 ms. Bound on any single wait inside the kernels      */
     uint32_t reserved;
+    /* Events recorded on `stream` (NULL entries skipped): [0] before the attention kernel,
+     * [1] after it, [2] after the split-combine kernel (or right after [1] if none runs).
+     * They let a caller time the two kernels separately on the launching stream. */
+    attn_event_t events[3];
 } attn_options_t;
 
 /* The work split chosen for a shape (host only, launches nothing). */

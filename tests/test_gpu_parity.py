@@ -78,12 +78,14 @@ def test_split_and_plain_agree_and_grid_limit(attn):
     q, k, v = make_qkv(2, 3, 600, 1500, 128, "bshd", seed=78)
     a = run(attn, q, k, v, "bshd", "rtne")
     b = run(attn, q, k, v, "bshd", "rtne", force_splits=4)
-    c = run(attn, q, k, v, "bshd", "rtne", max_ctas=5)
+    c = run(attn, q, k, v, "bshd", "rtne", force_splits=1)
+    d = run(attn, q, k, v, "bshd", "rtne", force_splits=1, max_ctas=5)
     ref = oracle.attention(q, k, v, "bshd", "rtne", want_a=True)
-    for o in (a, b, c):
+    for o in (a, b, c, d):
         r = parity.compare(parity.gpu_rows_bits(o, "bshd"), ref["o_bits"], ref["a"])
         assert r["ok"], r
-    assert torch.equal(a.view(torch.int16), c.view(torch.int16))   # same math, fewer CTAs
+    # the same unsplit plan run by 5 persistent CTAs instead of one per unit: same bits
+    assert torch.equal(c.view(torch.int16), d.view(torch.int16))
 
 
 def test_deterministic(attn):
@@ -145,6 +147,16 @@ def test_underflowed_weight_keeps_infinity(attn):
     v[0, 0, 0, 7] = float("-inf")                # key 0 weight e^-1086 -> still -inf
     for fs in (0, 2):
         check(attn, q, k, v, "bhsd", "rtne", force_splits=fs)
+    # a finite logit far below the max (-2^60 / sqrt(128), inside fp32 range): its weight is
+    # still positive, so the +inf in its V row must survive
+    q = torch.zeros(1, 1, 130, 128, dtype=torch.bfloat16)
+    q[..., 0] = 2.0 ** 30
+    k = torch.zeros(1, 1, 140, 128, dtype=torch.bfloat16)
+    k[0, 0, 3, 0] = -(2.0 ** 30)
+    v = torch.ones(1, 1, 140, 128, dtype=torch.bfloat16)
+    v[0, 0, 3, 11] = float("inf")
+    for fs in (0, 2):
+        check(attn, q, k, v, "bhsd", "rtna", force_splits=fs)
 
 
 @pytest.mark.parametrize("name", ["square", "cross", "video", "stress"])
