@@ -18,7 +18,7 @@ MODES = {"rtne": 0, "rtna": 1, "rtz": 2}
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_ALIAS", 5: "ATTN_ERR_NO_DEVICE",
           6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_CUDA", 8: "ATTN_ERR_DEVICE_TIMEOUT"}
-EXPORTS = ("attn_fwd", "attn_fwd_ws", "attn_fwd_workspace_size",
+EXPORTS = ("attn_fwd", "attn_fwd_ws", "attn_fwd_noalloc", "attn_fwd_workspace_size",
            "attn_fwd_workspace_size_opts", "attn_plan", "attn_get_device_status",
            "attn_status_string", "attn_version")
 
@@ -69,6 +69,8 @@ def load(path: str | None = None):
         lib.attn_fwd_ws.restype = i32
         lib.attn_fwd_ws.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, i32,
                                     ctypes.POINTER(Options), vp, ctypes.c_size_t, vp]
+        lib.attn_fwd_noalloc.restype = i32
+        lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, vp]
         lib.attn_fwd_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_workspace_size.argtypes = [i64] * 5
         lib.attn_fwd_workspace_size_opts.restype = ctypes.c_size_t

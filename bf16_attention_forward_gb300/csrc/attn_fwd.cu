@@ -818,6 +818,35 @@ int launch(const void* q, const void* k, const void* v, void* o, int64_t B, int6
     return ATTN_OK;
 }
 
+// ------------------------------------------------------------------------------ static scratch
+// Scratch for attn_fwd_noalloc(): the split path's partial outputs live in this array compiled
+// into the library instead of in memory the library allocates.  Every GPU that loads the
+// library holds it until the process exits.  Host code must not pass the symbol itself to a
+// kernel (on the host it only names a stand-in); noalloc_scratch() looks up the device address.
+constexpr size_t kStaticScratchBytes = (size_t)24 << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+void* g_static_scratch_ptr[kMaxDevices];
+
+// Device address of the static scratch on the current device (looked up once per device).
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return ATTN_ERR_NO_DEVICE;
+    }
+    std::lock_guard<std::mutex> g(g_mutex);
+    if (!g_static_scratch_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+        g_static_scratch_ptr[dev] = ptr;
+    }
+    *out = g_static_scratch_ptr[dev];
+    return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -882,6 +911,24 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, int64_t B, in
             di->ws_bytes = (size_t)pl.workspace_bytes;
         }
         ws = di->ws;
+    }
+    return launch(q, k, v, o, B, H, Sq, Skv, layout, round_mode, pl, nullptr, ws, (cudaStream_t)stream);
+}
+
+int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, int64_t B, int64_t H, int64_t Sq,
+                     int64_t Skv, int64_t d, int layout, int round_mode, attn_stream_t stream) {
+    int st = validate(q, k, v, o, B, H, Sq, Skv, d, layout, round_mode);
+    if (st != ATTN_OK) return st;
+    DeviceInfo* di = nullptr;
+    if ((st = device_info(&di)) != ATTN_OK) return st;
+    attn_plan_t pl;
+    make_plan(B, H, Sq, Skv, di->sms, nullptr, &pl);
+    void* ws = nullptr;
+    if (pl.workspace_bytes) {
+        if ((size_t)pl.workspace_bytes > kStaticScratchBytes) return ATTN_ERR_WORKSPACE;
+        // every scratch byte the combine reads is written by the attention kernel of the same
+        // call, so stale contents from an earlier call need no clearing
+        if ((st = noalloc_scratch(&ws)) != ATTN_OK) return st;
     }
     return launch(q, k, v, o, B, H, Sq, Skv, layout, round_mode, pl, nullptr, ws, (cudaStream_t)stream);
 }

@@ -130,6 +130,29 @@ int attn_plan(int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t d, int64_t 
               const attn_options_t* opts, attn_plan_t* plan);
 
 /*
+ * attn_fwd_noalloc -- attn_fwd for callers that cannot allocate device memory.  (The paper
+ * has no counterpart; this entry point exists for integration.)  Some callers must not see a
+ * library call cudaMalloc: code recording a CUDA graph (an allocation there breaks the
+ * capture), programs that hand all device memory to their own allocator or run under a fixed
+ * memory budget, and host frameworks that forbid libraries from allocating on their behalf.
+ * This call allocates nothing and frees nothing.  When the planner splits keys, the partial
+ * results go to a scratch array of ATTN_NOALLOC_SCRATCH_BYTES (24 MiB) compiled into the
+ * library; every GPU that loads the library holds that array until the process exits.
+ *   Arguments, layouts, numerics and errors are those of attn_fwd, plus:
+ *   - a shape whose split needs more scratch than the array holds returns ATTN_ERR_WORKSPACE
+ *     (with the default planner that needs more than 190 SMs' worth of split work);
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture;
+ *   - all calls share the one array: each call writes every scratch byte it reads, so nothing
+ *     carries over, but calls that can run at the same time on the GPU (unordered streams)
+ *     race on it and must be serialized by the caller.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)24 << 20)
+int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, int64_t B, int64_t H,
+                     int64_t Sq, int64_t Skv, int64_t d, int layout, int round_mode,
+                     attn_stream_t stream);
+
+/*
  * attn_get_device_status -- synchronizes `stream`, then reads and clears the current
  * device's status word.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT, or ATTN_ERR_CUDA.  If
  * site != NULL it receives the id of the wait that expired (0 if none).
