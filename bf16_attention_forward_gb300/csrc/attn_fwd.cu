@@ -242,6 +242,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const unsigned long long lim = p.wait_limit_ns;
+    // the split-combine kernel may be scheduled as CTAs retire; it waits for this grid's memory
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp >= 8) {
         ptx::reg_dealloc<kRegsOther>();
@@ -599,9 +601,14 @@ struct CombineParams {
     long long o_sb, o_ss, o_sh;
 };
 
-// One warp per output row of a split unit: merge the nsplit partials in fixed order s = 0..n-1
-// with weights 2^(LSE_s - max LSE).  [MoonMath] "Data placement ..." (tail KV split).
+// One warp per output row of a split unit: merge the nsplit partials with weights
+// 2^(LSE_s - max LSE), accumulating in fixed order s = 0..n-1.  Lanes read the split LSEs in
+// parallel (a row's chain of dependent loads is the combine's cost when nsplit is large); each
+// lane then owns 4 of the 128 columns.  Launched as a programmatic dependent of the attention
+// kernel: it starts as that kernel's CTAs retire and waits for its memory before reading.
+// [MoonMath] "Data placement and the 16x16x16 choice" (tail KV split).
 __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (gw >= (long long)p.split_units * kUnitRows) return;
@@ -613,26 +620,38 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p
     const int qrow = qb * kUnitRows + r;
     if (qrow >= p.Sq) return;
     const long long base = (long long)t * p.nsplit * kUnitRows + r;
+    // split LSEs: lane s holds split s (and s + 32, ...)
     float mx = -INFINITY;
     bool any_nan = false;
-    for (int s = 0; s < p.nsplit; ++s) {
+    for (int s = lane; s < p.nsplit; s += 32) {
         const float e = p.ws_lse[base + (long long)s * kUnitRows];
         any_nan |= (e != e);
         mx = fmaxf(mx, e);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+    any_nan = __any_sync(0xFFFFFFFFu, any_nan);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float wsum = 0.f;
-    for (int s = 0; s < p.nsplit; ++s) {
-        const float e = p.ws_lse[base + (long long)s * kUnitRows];
-        float w;
-        if (e == -INFINITY) w = 0.0f;
-        else w = ptx::ex2_approx(fmaxf(e - mx, -125.0f));
-        wsum += w;
-        const float4 v = *reinterpret_cast<const float4*>(p.ws_o + (base + (long long)s * kUnitRows) * kD + lane * 4);
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-        acc[2] += w * v.z;
-        acc[3] += w * v.w;
+    for (int s0 = 0; s0 < p.nsplit; s0 += 32) {
+        const int sl = s0 + lane;
+        float w = 0.0f;
+        if (sl < p.nsplit) {
+            const float e = p.ws_lse[base + (long long)sl * kUnitRows];
+            w = (e == -INFINITY) ? 0.0f : ptx::ex2_approx(fmaxf(e - mx, -125.0f));
+        }
+        const int n = min(32, p.nsplit - s0);
+        const float* src = p.ws_o + (base + (long long)s0 * kUnitRows) * kD + lane * 4;
+#pragma unroll 4
+        for (int q = 0; q < n; ++q) {
+            const float wq = __shfl_sync(0xFFFFFFFFu, w, q);
+            const float4 v = *reinterpret_cast<const float4*>(src + (long long)q * kUnitRows * kD);
+            wsum += wq;
+            acc[0] += wq * v.x;
+            acc[1] += wq * v.y;
+            acc[2] += wq * v.z;
+            acc[3] += wq * v.w;
+        }
     }
     const bool nan_row = any_nan || mx == -INFINITY;
     const float inv = 1.0f / wsum;
@@ -811,8 +830,21 @@ int launch(const void* q, const void* k, const void* v, void* o, int64_t B, int6
         const long long rows = pl.split_units * kUnitRows;
         const int warps_per_block = 8;
         const unsigned blocks = (unsigned)cdiv(rows, warps_per_block);
-        attn_combine_kernel<<<blocks, warps_per_block * 32, 0, stream>>>(c);
-        if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(blocks);
+        cfg.blockDim = dim3(warps_per_block * 32);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, attn_combine_kernel, c) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
     }
     if (ev && ev[2] && cudaEventRecord((cudaEvent_t)ev[2], stream) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
