@@ -52,6 +52,10 @@ def _bind(lib):
     lib.attn_oracle.argtypes = [u16p, u16p, u16p] + [ctypes.c_int64] * 5 + [
         ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int64, u16p, f64p, f64p, f64p, f64p,
         ctypes.c_int]
+    lib.attn_oracle_ex.restype = ctypes.c_int
+    lib.attn_oracle_ex.argtypes = [u16p, u16p, u16p] + [ctypes.c_int64] * 6 + [
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int64, u16p, f64p, f64p,
+        f64p, f64p, ctypes.c_int]
     lib.oracle_round_bf16_array.restype = None
     lib.oracle_round_bf16_array.argtypes = [f64p, ctypes.c_int64, ctypes.c_int, u16p]
     lib.oracle_max_threads.restype = ctypes.c_int
@@ -95,10 +99,18 @@ def dims(q_shape, k_shape, layout: str):
     return B, H, Sq, Skv, d
 
 
+def kv_heads(k_shape, layout: str) -> int:
+    return k_shape[2] if layout == "bshd" else k_shape[1]
+
+
 def attention(q, k, v, layout: str = "bshd", mode: str = "rtne", rows=None,
               want_f64: bool = False, want_a: bool = False, want_lse: bool = False,
-              want_probs: bool = False, threads: int | None = None, lib=None) -> dict:
+              want_probs: bool = False, threads: int | None = None, lib=None,
+              causal: bool = False) -> dict:
     """Oracle attention.  Returns a dict of numpy arrays.
+
+    K and V may have fewer heads than Q (grouped heads: query head h reads K/V head
+    h // (H // Hkv)); ``causal`` makes key j visible to query i iff j <= i + (Skv - Sq).
 
     ``o_bits``: uint16 bf16 patterns.  With ``rows=None`` shaped (B, H, Sq, d) (BHSD order,
     whatever the input layout); with ``rows`` (flat indices (b*H + h)*Sq + i) shaped
@@ -119,9 +131,10 @@ def attention(q, k, v, layout: str = "bshd", mode: str = "rtne", rows=None,
     a_b = np.empty((n, d), dtype=np.float64) if want_a else None
     lse = np.empty((n,), dtype=np.float64) if want_lse else None
     probs = np.empty((n, Skv), dtype=np.float64) if want_probs else None
-    rc = lib.attn_oracle(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
-                         _ptr(vb, ctypes.c_uint16), B, H, Sq, Skv, d, LAYOUTS[layout],
-                         MODES[mode], _ptr(rows_arr, ctypes.c_int64),
+    Hkv = kv_heads(kb.shape, layout)
+    rc = lib.attn_oracle_ex(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                         _ptr(vb, ctypes.c_uint16), B, H, Hkv, Sq, Skv, d, LAYOUTS[layout],
+                         MODES[mode], 1 if causal else 0, _ptr(rows_arr, ctypes.c_int64),
                          0 if rows_arr is None else n, _ptr(o_bits, ctypes.c_uint16),
                          _ptr(o_f64, ctypes.c_double), _ptr(a_b, ctypes.c_double),
                          _ptr(lse, ctypes.c_double), _ptr(probs, ctypes.c_double),

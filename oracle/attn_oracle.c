@@ -31,6 +31,15 @@
  * names as IEEE roundTiesToEven / roundTiesToAway / roundTowardZero on the final value)
  * are where the pages are silent; they are listed with the other readings in the design
  * notes of this repository.
+ *
+ * Extensions named by the same article's limitations paragraph (causal masking and GQA are
+ * listed there as not yet supported by the MI300X kernel):
+ *   - causal: key j is visible to query i iff j <= i + (Skv - Sq) (aligned at the last
+ *     query/key; plain causal when Sq = Skv).  Masked keys are left out of the row entirely;
+ *     a row with no visible key is NaN (empty softmax) with log-sum-exp -inf.
+ *   - grouped K/V heads: Hkv divides H, and query head h reads K/V head h / (H / Hkv).
+ *   - lse: natural log of sum_j exp(s_j) over the visible keys; NaN for a row holding a NaN
+ *     or +inf logit, -inf when every visible logit is -inf or no key is visible.
  */
 #include <math.h>
 #include <stdint.h>
@@ -105,7 +114,8 @@ uint16_t oracle_round_bf16(double x, int mode) {
 /* Per-row work.  Outputs for the row are written at slot `slot` (row-major, d wide). */
 static void oracle_row(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                        int64_t b, int64_t h, int64_t i,
-                       int64_t H, int64_t Sq, int64_t Skv, int64_t d, int layout, int mode,
+                       int64_t H, int64_t Hkv, int64_t Sq, int64_t Skv, int64_t d, int causal,
+                       int layout, int mode,
                        double* s, double* w, double* qrow,
                        uint16_t* o_bits, double* o_f64, double* a_bound, double* lse,
                        double* probs, int64_t slot) {
@@ -113,12 +123,20 @@ static void oracle_row(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     for (int64_t x = 0; x < d; ++x)
         qrow[x] = bf16_bits_to_double(q[elem_offset(layout, b, i, h, x, Sq, H, d)]);
 
+    /* Visible keys: all, or with the causal mask keys 0 .. i + (Skv - Sq). */
+    int64_t nvis = Skv;
+    if (causal) {
+        const int64_t last = i + (Skv - Sq);
+        nvis = last < 0 ? 0 : (last + 1 < Skv ? last + 1 : Skv);
+    }
+    const int64_t kvh = h / (H / Hkv);   /* grouped K/V head read by query head h */
+
     /* Logits, [MoonMath] opening section: Q K^T / sqrt(d). */
     int any_nan_or_posinf = 0, all_neginf = 1;
     double m = -INFINITY;
-    for (int64_t j = 0; j < Skv; ++j) {
+    for (int64_t j = 0; j < nvis; ++j) {
         double acc = 0.0;
-        const int64_t kb = elem_offset(layout, b, j, h, 0, Skv, H, d);
+        const int64_t kb = elem_offset(layout, b, j, kvh, 0, Skv, Hkv, d);
         for (int64_t x = 0; x < d; ++x) acc += qrow[x] * bf16_bits_to_double(k[kb + x]);
         s[j] = acc * scale;
         if (isnan(s[j]) || (isinf(s[j]) && s[j] > 0)) any_nan_or_posinf = 1;
@@ -127,13 +145,14 @@ static void oracle_row(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     }
 
     if (any_nan_or_posinf || all_neginf) {
-        /* softmax of a row holding NaN or +inf, or only -inf, is NaN everywhere */
+        /* softmax of a row holding NaN or +inf, or only -inf (or no visible key), is NaN
+         * everywhere; its log-sum-exp is NaN, or -inf (log 0) when nothing but -inf is seen */
         for (int64_t x = 0; x < d; ++x) {
             o_bits[slot * d + x] = 0x7FC0;
             if (o_f64) o_f64[slot * d + x] = NAN;
             if (a_bound) a_bound[slot * d + x] = NAN;
         }
-        if (lse) lse[slot] = NAN;
+        if (lse) lse[slot] = any_nan_or_posinf ? NAN : -INFINITY;
         if (probs)
             for (int64_t j = 0; j < Skv; ++j) probs[slot * Skv + j] = NAN;
         return;
@@ -141,18 +160,18 @@ static void oracle_row(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 
     /* Weights relative to the row maximum: exp(s_j - m), 0 for -inf logits. */
     double l = 0.0;
-    for (int64_t j = 0; j < Skv; ++j) {
+    for (int64_t j = 0; j < nvis; ++j) {
         w[j] = isfinite(s[j]) ? exp(s[j] - m) : 0.0;
         l += w[j];
     }
     if (lse) lse[slot] = m + log(l);
     if (probs)
-        for (int64_t j = 0; j < Skv; ++j) probs[slot * Skv + j] = w[j] / l;
+        for (int64_t j = 0; j < Skv; ++j) probs[slot * Skv + j] = j < nvis ? w[j] / l : 0.0;
 
     for (int64_t x = 0; x < d; ++x) {
         double num = 0.0, absnum = 0.0;
-        for (int64_t j = 0; j < Skv; ++j) {
-            const double vj = bf16_bits_to_double(v[elem_offset(layout, b, j, h, x, Skv, H, d)]);
+        for (int64_t j = 0; j < nvis; ++j) {
+            const double vj = bf16_bits_to_double(v[elem_offset(layout, b, j, kvh, x, Skv, Hkv, d)]);
             double term;
             if (!isfinite(s[j])) {
                 term = 0.0 * vj;                 /* -inf logit: weight exactly 0 */
@@ -172,27 +191,29 @@ static void oracle_row(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 }
 
 /*
- * attn_oracle -- reference attention forward in fp64.
+ * attn_oracle_ex -- reference attention forward in fp64.
  *
- * q, k, v   bf16 bit patterns in `layout` (0 = BSHD, 1 = BHSD); q has Sq rows per (b, h),
- *           k and v have Skv rows per (b, h).
+ * q, k, v   bf16 bit patterns in `layout` (0 = BSHD, 1 = BHSD); q has Sq rows per (b, h)
+ *           over H heads, k and v have Skv rows per (b, kv head) over Hkv heads (Hkv | H).
+ * causal    0: every key visible; 1: key j visible to query i iff j <= i + (Skv - Sq).
  * rows      optional list of nrows flat row indices r = (b*H + h)*Sq + i; NULL means every
  *           row, in that (b, h, i) order.
  * o_bits    out, [nrows][d] bf16 bit patterns in list order.
  * o_f64     optional out, [nrows][d] unrounded result.
  * a_bound   optional out, [nrows][d] A = sum_j w_j |v_jx| / l (forward-error scale).
- * lse       optional out, [nrows] natural-log log-sum-exp of the scaled logits.
+ * lse       optional out, [nrows] natural-log log-sum-exp of the visible scaled logits.
  * probs     optional out, [nrows][Skv] softmax weights w_j / l.
  * nthreads  OpenMP threads (<= 0: runtime default).
  * Returns 0 on success, -1 on bad arguments.
  */
-int attn_oracle(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t d,
-                int layout, int mode, const int64_t* rows, int64_t nrows,
-                uint16_t* o_bits, double* o_f64, double* a_bound, double* lse,
-                double* probs, int nthreads) {
+int attn_oracle_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                   int64_t B, int64_t H, int64_t Hkv, int64_t Sq, int64_t Skv, int64_t d,
+                   int layout, int mode, int causal, const int64_t* rows, int64_t nrows,
+                   uint16_t* o_bits, double* o_f64, double* a_bound, double* lse,
+                   double* probs, int nthreads) {
     if (!q || !k || !v || !o_bits) return -1;
-    if (B < 1 || H < 1 || Sq < 1 || Skv < 1 || d < 1) return -1;
+    if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || Sq < 1 || Skv < 1 || d < 1) return -1;
+    if (causal != 0 && causal != 1) return -1;
     if (layout != ORACLE_LAYOUT_BSHD && layout != ORACLE_LAYOUT_BHSD) return -1;
     if (mode < ORACLE_ROUND_RTNE || mode > ORACLE_ROUND_RTZ) return -1;
     const int64_t total = B * H * Sq;
@@ -221,8 +242,8 @@ int attn_oracle(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                 const int64_t i = flat % Sq;
                 const int64_t h = (flat / Sq) % H;
                 const int64_t b = flat / (Sq * H);
-                oracle_row(q, k, v, b, h, i, H, Sq, Skv, d, layout, mode, s, w, qrow,
-                           o_bits, o_f64, a_bound, lse, probs, r);
+                oracle_row(q, k, v, b, h, i, H, Hkv, Sq, Skv, d, causal, layout, mode, s, w,
+                           qrow, o_bits, o_f64, a_bound, lse, probs, r);
             }
         }
         free(s);
@@ -230,6 +251,16 @@ int attn_oracle(const uint16_t* q, const uint16_t* k, const uint16_t* v,
         free(qrow);
     }
     return bad ? -1 : 0;
+}
+
+/* attn_oracle_ex with one K/V head per query head and no mask. */
+int attn_oracle(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t d,
+                int layout, int mode, const int64_t* rows, int64_t nrows,
+                uint16_t* o_bits, double* o_f64, double* a_bound, double* lse,
+                double* probs, int nthreads) {
+    return attn_oracle_ex(q, k, v, B, H, H, Sq, Skv, d, layout, mode, 0, rows, nrows, o_bits,
+                          o_f64, a_bound, lse, probs, nthreads);
 }
 
 /* Batch rounding helper so the rounding rule can be tested on its own. */

@@ -384,4 +384,112 @@ def pin_all_neginf_row_is_nan(lib):
     assert np.all(o == 0x7FC0)
 
 
+# --------------------------------------------------------------------------- causal / GQA / LSE
+def pin_causal_rows_are_prefix_attention(lib):
+    """Causal row i (Sq = Skv) is plain attention over keys 0..i; with Skv = Sq + off it is
+    attention over keys 0..i+off; rows with no visible key are NaN with LSE -inf."""
+    for (Sq, Skv) in ((7, 7), (4, 9), (9, 4)):
+        q, k, v = make_qkv(1, 2, Sq, Skv, D, "bhsd", seed=200 + Sq * 10 + Skv)
+        for mode in ("rtne", "rtz"):
+            c = oracle.attention(q, k, v, "bhsd", mode, causal=True, want_lse=True, lib=lib)
+            for i in range(Sq):
+                nvis = min(Skv, i + (Skv - Sq) + 1)
+                if nvis <= 0:
+                    assert np.all(c["o_bits"][:, :, i] == 0x7FC0)
+                    assert np.all(np.isneginf(c["lse"][:, :, i]))
+                    continue
+                ref = oracle.attention(q[:, :, i:i + 1], k[:, :, :nvis], v[:, :, :nvis], "bhsd",
+                                       mode, want_lse=True, lib=lib)
+                assert np.array_equal(c["o_bits"][:, :, i], ref["o_bits"][:, :, 0]), (Sq, Skv, i)
+                assert np.array_equal(c["lse"][:, :, i], ref["lse"][:, :, 0])
+
+
+def pin_causal_first_row_is_first_value(lib):
+    """Sq = Skv: query 0 sees only key 0, so its output is V row 0 in every mode."""
+    q, k, v = make_qkv(2, 3, 6, 6, D, "bshd", seed=210, sigma=3.0)
+    for mode in MODES:
+        o = oracle.attention(q, k, v, "bshd", mode, causal=True, lib=lib)["o_bits"]
+        vb = _bits(v.permute(0, 2, 1, 3).contiguous())          # (B, H, S, d)
+        assert np.array_equal(o[:, :, 0], vb[:, :, 0]), mode
+
+
+def pin_grouped_heads_equal_repeated_heads(lib):
+    """K/V with Hkv heads (query head h reads K/V head h // (H/Hkv)) equal plain attention
+    with each K/V head repeated H/Hkv times; Hkv = 1 is multi-query attention."""
+    B, H, Sq, Skv = 2, 6, 5, 11
+    for Hkv in (1, 2, 3, 6):
+        for layout in ("bshd", "bhsd"):
+            g = torch.Generator().manual_seed(220 + Hkv)
+            q = torch.randn(shape(layout, B, H, Sq, D), generator=g).to(torch.bfloat16)
+            k = torch.randn(shape(layout, B, Hkv, Skv, D), generator=g).to(torch.bfloat16)
+            v = torch.randn(shape(layout, B, Hkv, Skv, D), generator=g).to(torch.bfloat16)
+            ax = 2 if layout == "bshd" else 1
+            kr = k.repeat_interleave(H // Hkv, dim=ax).contiguous()
+            vr = v.repeat_interleave(H // Hkv, dim=ax).contiguous()
+            for causal in (False, True):
+                a = oracle.attention(q, k, v, layout, "rtna", causal=causal, lib=lib)["o_bits"]
+                b = oracle.attention(q, kr, vr, layout, "rtna", causal=causal, lib=lib)["o_bits"]
+                assert np.array_equal(a, b), (Hkv, layout, causal)
+
+
+def pin_lse_closed_forms(lib):
+    """LSE = log sum_j exp(s_j): two keys give log(e^s1 + e^s2); Q = 0 gives log(Skv);
+    NaN rows give NaN; an all -inf row gives -inf."""
+    g = torch.Generator().manual_seed(230)
+    q = torch.randn(1, 1, 3, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(1, 1, 2, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, 1, 2, D, generator=g).to(torch.bfloat16)
+    lse = oracle.attention(q, k, v, "bhsd", "rtne", want_lse=True, lib=lib)["lse"][0, 0]
+    qd, kd = q.double()[0, 0], k.double()[0, 0]
+    for i in range(3):
+        s = [float((qd[i] * kd[j]).sum()) / math.sqrt(D) for j in range(2)]
+        mx = max(s)
+        assert abs(lse[i] - (mx + math.log(sum(math.exp(x - mx) for x in s)))) < 1e-13
+    q0 = torch.zeros(1, 2, 4, D, dtype=torch.bfloat16)
+    kk = torch.randn(1, 2, 37, D, generator=g).to(torch.bfloat16)
+    vv = torch.randn(1, 2, 37, D, generator=g).to(torch.bfloat16)
+    l0 = oracle.attention(q0, kk, vv, "bhsd", "rtne", want_lse=True, lib=lib)["lse"]
+    assert np.allclose(l0, math.log(37), rtol=0, atol=1e-14)
+    qn = q.clone()
+    qn[0, 0, 1, 0] = float("nan")
+    ln = oracle.attention(qn, k, v, "bhsd", "rtne", want_lse=True, lib=lib)["lse"][0, 0]
+    assert math.isnan(ln[1]) and math.isfinite(ln[0])
+    qi = torch.zeros(1, 1, 1, D, dtype=torch.bfloat16)
+    qi[..., 0] = 1.0
+    ki = torch.zeros(1, 1, 3, D, dtype=torch.bfloat16)
+    ki[..., 0] = float("-inf")
+    li = oracle.attention(qi, ki, v[:, :, :1].expand(1, 1, 3, D).contiguous(), "bhsd", "rtne",
+                          want_lse=True, lib=lib)["lse"]
+    assert np.isneginf(li).all()
+
+
+def pin_brute_force_causal_lse_mpmath(lib):
+    """Causal, grouped heads and LSE on tiny shapes against 50-digit arithmetic."""
+    import mpmath
+    mpmath.mp.dps = 50
+    B, H, Hkv, Sq, Skv = 1, 2, 1, 3, 5
+    g = torch.Generator().manual_seed(240)
+    q = torch.randn(B, H, Sq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Hkv, Skv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Hkv, Skv, D, generator=g).to(torch.bfloat16)
+    res = oracle.attention(q, k, v, "bhsd", "rtne", causal=True, want_f64=True, want_lse=True,
+                           want_a=True, lib=lib)
+    inv = 1 / mpmath.sqrt(D)
+    for h in range(H):
+        qd, kd, vd = q.double().numpy()[0, h], k.double().numpy()[0, 0], v.double().numpy()[0, 0]
+        for i in range(Sq):
+            nvis = i + (Skv - Sq) + 1
+            s = [mpmath.fsum(mpmath.mpf(float(qd[i, x])) * mpmath.mpf(float(kd[j, x]))
+                             for x in range(D)) * inv for j in range(nvis)]
+            m = max(s)
+            w = [mpmath.exp(sj - m) for sj in s]
+            l = mpmath.fsum(w)
+            assert abs(res["lse"][0, h, i] - float(m + mpmath.log(l))) < 1e-13
+            for x in range(0, D, 7):
+                val = mpmath.fsum(w[j] * mpmath.mpf(float(vd[j, x])) for j in range(nvis)) / l
+                assert abs(res["o_f64"][0, h, i, x] - float(val)) <= 1e-13 * res["a"][0, h, i, x]
+                if not bx.near_midpoint(val):
+                    assert res["o_bits"][0, h, i, x] == bx.round_exact(val, "rtne")
+
+
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

@@ -18,8 +18,8 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
 
 MUTANTS = {
     "no_scale": ("s[j] = acc * scale;", "s[j] = acc;"),
-    "kv_stride_uses_Sq": ("elem_offset(layout, b, j, h, 0, Skv, H, d)",
-                          "elem_offset(layout, b, j, h, 0, Sq, H, d)"),
+    "kv_stride_uses_Sq": ("elem_offset(layout, b, j, kvh, 0, Skv, Hkv, d)",
+                          "elem_offset(layout, b, j, kvh, 0, Sq, Hkv, d)"),
     "exp_sign": ("exp(s[j] - m)", "exp(m - s[j])"),
     "ties_to_odd": ("fmod(n, 2.0) != 0.0", "fmod(n, 2.0) == 0.0"),
     "rtna_as_rtne": ("if (rem >= half) r = a + q;", "if (rem > half) r = a + q;"),
@@ -30,8 +30,12 @@ MUTANTS = {
     "bshd_as_bhsd": ("if (layout == ORACLE_LAYOUT_BSHD) return ((b * S + s) * H + h) * d + x;",
                      "if (layout == ORACLE_LAYOUT_BSHD) return ((b * H + h) * S + s) * d + x;"),
     "sum_skips_first_key": ("l += w[j];", "if (j > 0) l += w[j];"),
-    "v_transposed": ("v[elem_offset(layout, b, j, h, x, Skv, H, d)]",
-                     "v[elem_offset(layout, b, x % Skv, h, j % d, Skv, H, d)]"),
+    "v_transposed": ("v[elem_offset(layout, b, j, kvh, x, Skv, Hkv, d)]",
+                     "v[elem_offset(layout, b, x % Skv, kvh, j % d, Skv, Hkv, d)]"),
+    "causal_off_by_one": ("nvis = last < 0 ? 0 : (last + 1 < Skv ? last + 1 : Skv);",
+                          "nvis = last < 0 ? 0 : (last < Skv ? last : Skv);"),
+    "gqa_head_interleaved": ("const int64_t kvh = h / (H / Hkv);", "const int64_t kvh = h % Hkv;"),
+    "lse_drops_max": ("if (lse) lse[slot] = m + log(l);", "if (lse) lse[slot] = log(l);"),
     "posinf_logit_ignored": ("if (isnan(s[j]) || (isinf(s[j]) && s[j] > 0)) any_nan_or_posinf = 1;",
                              "if (isnan(s[j])) any_nan_or_posinf = 1;"),
 }
