@@ -18,9 +18,9 @@ MODES = {"rtne": 0, "rtna": 1, "rtz": 2}
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_ALIAS", 5: "ATTN_ERR_NO_DEVICE",
           6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_CUDA", 8: "ATTN_ERR_DEVICE_TIMEOUT"}
-EXPORTS = ("attn_fwd", "attn_fwd_ws", "attn_fwd_noalloc", "attn_fwd_workspace_size",
-           "attn_fwd_workspace_size_opts", "attn_plan", "attn_get_device_status",
-           "attn_status_string", "attn_version")
+EXPORTS = ("attn_fwd", "attn_fwd_ws", "attn_fwd_noalloc", "attn_fwd_ex", "attn_fwd_workspace_size",
+           "attn_fwd_workspace_size_opts", "attn_fwd_ex_workspace_size", "attn_plan",
+           "attn_plan_ex", "attn_get_device_status", "attn_status_string", "attn_version")
 
 
 class AttnError(RuntimeError):
@@ -34,6 +34,14 @@ class Options(ctypes.Structure):
     _fields_ = [("force_splits", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
                 ("wait_limit_ms", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
                 ("events", ctypes.c_void_p * 3)]
+
+
+class Args(ctypes.Structure):
+    """attn_args_t: the full argument set of attn_fwd_ex."""
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p)] + \
+               [(n, ctypes.c_int64) for n in ("B", "H", "Hkv", "Sq", "Skv", "d")] + \
+               [(n, ctypes.c_int32) for n in ("layout", "round_mode", "causal", "reserved")]
 
 
 class Plan(ctypes.Structure):
@@ -75,6 +83,14 @@ def load(path: str | None = None):
         lib.attn_fwd_workspace_size.argtypes = [i64] * 5
         lib.attn_fwd_workspace_size_opts.restype = ctypes.c_size_t
         lib.attn_fwd_workspace_size_opts.argtypes = [i64] * 5 + [ctypes.POINTER(Options)]
+        lib.attn_fwd_ex.restype = i32
+        lib.attn_fwd_ex.argtypes = [ctypes.POINTER(Args), ctypes.POINTER(Options), vp,
+                                    ctypes.c_size_t, vp]
+        lib.attn_fwd_ex_workspace_size.restype = ctypes.c_size_t
+        lib.attn_fwd_ex_workspace_size.argtypes = [ctypes.POINTER(Args), ctypes.POINTER(Options)]
+        lib.attn_plan_ex.restype = i32
+        lib.attn_plan_ex.argtypes = [ctypes.POINTER(Args), i64, ctypes.POINTER(Options),
+                                     ctypes.POINTER(Plan)]
         lib.attn_plan.restype = i32
         lib.attn_plan.argtypes = [i64] * 6 + [ctypes.POINTER(Options), ctypes.POINTER(Plan)]
         lib.attn_get_device_status.restype = i32
@@ -92,16 +108,44 @@ def status_string(status: int) -> str:
     return load().attn_status_string(int(status)).decode()
 
 
-def _dims(q, k, layout):
-    if q.dim() != 4 or k.dim() != 4:
+def _dims(q, k, v, layout, grouped=False):
+    """(B, H, Hkv, Sq, Skv, d) from the tensors' shapes, checking that they agree."""
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D (BSHD or BHSD)")
+    if tuple(k.shape) != tuple(v.shape):
+        raise ValueError("k and v must have the same shape")
     if layout == "bshd":
-        B, Sq, H, d = q.shape
-        Skv = k.shape[1]
+        (B, Sq, H, d), (Bk, Skv, Hkv, dk) = q.shape, k.shape
     else:
-        B, H, Sq, d = q.shape
-        Skv = k.shape[2]
-    return int(B), int(H), int(Sq), int(Skv), int(d)
+        (B, H, Sq, d), (Bk, Hkv, Skv, dk) = q.shape, k.shape
+    if Bk != B or dk != d:
+        raise ValueError("q and k/v differ in batch or head dimension")
+    if (Hkv != H) if not grouped else (Hkv < 1 or H % Hkv != 0):
+        raise ValueError("k/v heads (%d) must %s the query heads (%d)"
+                         % (Hkv, "divide" if grouped else "equal", H))
+    return int(B), int(H), int(Hkv), int(Sq), int(Skv), int(d)
+
+
+def _check_tensors(q, k, v):
+    import torch
+    for t in (q, k, v):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError("q, k, v must be CUDA bf16 tensors")
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+
+
+def _check_out(o, q):
+    import torch
+    if (not isinstance(o, torch.Tensor) or o.dtype != torch.bfloat16 or not o.is_cuda
+            or not o.is_contiguous() or tuple(o.shape) != tuple(q.shape)):
+        raise ValueError("o must be a contiguous CUDA bf16 tensor shaped like q")
+
+
+def _stream_ptr(stream, device):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream if hasattr(s, "cuda_stream") else int(s))
 
 
 def _opts(force_splits=0, max_ctas=0, wait_limit_ms=0, events=None):
@@ -144,16 +188,12 @@ def attn_fwd(q, k, v, o=None, layout: str = "bshd", round: str = "rtne", stream=
     import torch
     if layout not in LAYOUTS or round not in MODES:
         raise ValueError("layout must be bshd/bhsd and round rtne/rtna/rtz")
-    for t in (q, k, v):
-        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
-            raise TypeError("q, k, v must be CUDA bf16 tensors")
-        if not t.is_contiguous():
-            raise ValueError("q, k, v must be contiguous")
-    B, H, Sq, Skv, d = _dims(q, k, layout)
+    _check_tensors(q, k, v)
+    B, H, _, Sq, Skv, d = _dims(q, k, v, layout)
     if o is None:
         o = torch.empty_like(q)
-    s = stream if stream is not None else torch.cuda.current_stream(q.device)
-    sp = ctypes.c_void_p(s.cuda_stream if hasattr(s, "cuda_stream") else int(s))
+    _check_out(o, q)
+    sp = _stream_ptr(stream, q.device)
     lib = load()
     opts = _opts(force_splits, max_ctas, wait_limit_ms, events)
     if workspace is None and opts is None:
@@ -171,6 +211,77 @@ def attn_fwd(q, k, v, o=None, layout: str = "bshd", round: str = "rtne", stream=
     if st != 0:
         raise AttnError(st, "attn_fwd")
     return o
+
+
+def _args(q, k, v, o, lse, layout, round, causal) -> Args:
+    B, H, Hkv, Sq, Skv, d = _dims(q, k, v, layout, grouped=True)
+    a = Args()
+    a.q, a.k, a.v, a.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
+    a.lse = None if lse is None else lse.data_ptr()
+    a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d = B, H, Hkv, Sq, Skv, d
+    a.layout, a.round_mode, a.causal, a.reserved = LAYOUTS[layout], MODES[round], int(causal), 0
+    return a
+
+
+def plan_ex(B, H, Sq, Skv, Hkv=None, d=128, causal=False, num_sms=152, force_splits=0,
+            max_ctas=0) -> dict:
+    """attn_plan_ex: the work split for the full argument set (host only)."""
+    a = Args()
+    a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d = B, H, H if Hkv is None else Hkv, Sq, Skv, d
+    a.causal = int(causal)
+    pl = Plan()
+    o = _opts(force_splits, max_ctas)
+    st = load().attn_plan_ex(ctypes.byref(a), num_sms, ctypes.byref(o) if o else None,
+                             ctypes.byref(pl))
+    if st != 0:
+        raise AttnError(st, "attn_plan_ex")
+    return pl.as_dict()
+
+
+def attn_fwd_ex(q, k, v, o=None, lse=None, layout: str = "bshd", round: str = "rtne",
+                causal: bool = False, return_lse: bool = False, stream=None, workspace=None,
+                force_splits: int = 0, max_ctas: int = 0, wait_limit_ms: int = 0, events=None):
+    """attn_fwd with grouped K/V heads (k, v carry Hkv heads, Hkv dividing H), the causal mask
+    (key j visible to query i iff j <= i + Skv - Sq) and the fp32 row log-sum-exp.
+
+    ``lse``: optional CUDA fp32 tensor of B*H*Sq elements laid out [B][H][Sq]; with
+    ``return_lse`` and no ``lse`` one is allocated.  Returns ``o`` or ``(o, lse)``.
+    ``workspace``: optional caller tensor; without it the library-owned workspace is used.
+    """
+    import torch
+    if layout not in LAYOUTS or round not in MODES:
+        raise ValueError("layout must be bshd/bhsd and round rtne/rtna/rtz")
+    _check_tensors(q, k, v)
+    B, H, _, Sq, _, _ = _dims(q, k, v, layout, grouped=True)
+    if o is None:
+        o = torch.empty_like(q)
+    _check_out(o, q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous()
+                            or lse.numel() != B * H * Sq):
+        raise ValueError("lse must be a contiguous CUDA fp32 tensor of B*H*Sq elements")
+    a = _args(q, k, v, o, lse, layout, round, causal)
+    opts = _opts(force_splits, max_ctas, wait_limit_ms, events)
+    lib = load()
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = lib.attn_fwd_ex(ctypes.byref(a), ctypes.byref(opts) if opts else None, ws_ptr, ws_bytes,
+                         _stream_ptr(stream, q.device))
+    if st != 0:
+        raise AttnError(st, "attn_fwd_ex")
+    return (o, lse) if (return_lse or lse is not None) else o
+
+
+def workspace_size_ex(q, k, v, layout="bshd", causal=False, force_splits=0, max_ctas=0) -> int:
+    """attn_fwd_ex_workspace_size for tensors shaped like q, k, v."""
+    B, H, Hkv, Sq, Skv, d = _dims(q, k, v, layout, grouped=True)
+    a = Args()
+    a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d, a.causal = B, H, Hkv, Sq, Skv, d, int(causal)
+    a.layout = LAYOUTS[layout]
+    o = _opts(force_splits, max_ctas)
+    return int(load().attn_fwd_ex_workspace_size(ctypes.byref(a), ctypes.byref(o) if o else None))
 
 
 def device_status(stream=None) -> tuple:

@@ -99,6 +99,9 @@ __device__ uint32_t g_status[2];   // [0] status code, [1] wait site
 
 struct FwdParams {
     int B, H, Sq, Skv;
+    int group;             // query heads per K/V head (H / Hkv)
+    int causal;            // 1: key j visible to query i iff j <= i + causal_off
+    int causal_off;        // Skv - Sq
     int nq, nkv;           // 256-row query blocks per (b, h); 128-key tiles
     int n_items, n_full;   // work items; items >= n_full are key splits of tail units
     int nsplit;
@@ -110,6 +113,7 @@ struct FwdParams {
     float* ws_o;           // [split items][256][128] fp32
     float* ws_lse;         // [split items][256] fp32, base-2 log-sum-exp
     long long o_sb, o_ss, o_sh;   // element strides of O for b, s, h
+    float* lse;            // optional [B][H][Sq] natural-log log-sum-exp, or null
     unsigned long long wait_limit_ns;
 };
 
@@ -133,6 +137,19 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int k) {
         it.kv_begin = s * base + (s < rem ? s : rem);
         it.kv_end = it.kv_begin + base + (s < rem ? 1 : 0);
         it.split_slot = r;
+    }
+    if (p.causal) {
+        // heaviest first: query blocks nearest the end see the most keys; each block runs
+        // only the key tiles up to its diagonal (at least one, which the mask then empties)
+        const int bhn = p.B * p.H;
+        it.qb = p.nq - 1 - unit / bhn;
+        const int bh = unit % bhn;
+        it.h = bh % p.H;
+        it.b = bh / p.H;
+        const int last = it.qb * kUnitRows + kUnitRows - 1 + p.causal_off;   // last visible key
+        const int need = last < 0 ? 1 : last / kBN + 1;
+        it.kv_end = need < it.kv_end ? need : it.kv_end;
+        return it;
     }
     it.qb = unit % p.nq;
     const int bh = unit / p.nq;
@@ -196,6 +213,7 @@ __device__ __forceinline__ uint32_t round_bf16_bits(float f, int mode) {
 // unchanged (x * 2^-126 is far below half an ulp of x); for finite x < -124 it gives
 // -124 - |x| * 2^-126 >= -125.02 since |x| < 2^127.
 constexpr float kMinExponent = -124.0f;
+constexpr float kLn2 = 0.693147180559945309f;
 __device__ __forceinline__ float weight_exponent(float s, float c, float m) {
     const float x = (s - m) * c;
     return fmaf(x, 0x1p-126f, ptx::fmax_nan(x, kMinExponent));
@@ -280,9 +298,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                         for (int c = 0; c < 2; ++c) {
                             const uint32_t dst = sbase + kSmemRing + slot * kTileBytes + c * kChunkBytes;
                             if (p.bshd)
-                                ptx::tma_load_4d(dst, map, bar(kBarFull + slot), c * 64, it.h, j * kBN, it.b, pol_kv);
+                                ptx::tma_load_4d(dst, map, bar(kBarFull + slot), c * 64, it.h / p.group, j * kBN, it.b, pol_kv);
                             else
-                                ptx::tma_load_4d(dst, map, bar(kBarFull + slot), c * 64, j * kBN, it.h, it.b, pol_kv);
+                                ptx::tma_load_4d(dst, map, bar(kBarFull + slot), c * 64, j * kBN, it.h / p.group, it.b, pol_kv);
                         }
                     }
                 }
@@ -418,11 +436,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 ptx::tc_fence_after();
                 uint32_t s[128];
                 ptx::tmem_ld128(tS, s);
-                const int valid = p.Skv - j * kBN;   // keys of this tile that exist
-                if (valid < kBN) {
+                // keys of this tile past `limit` are absent: beyond Skv, or (causal) past this
+                // row's diagonal; they get -inf logits and so weight 0
+                int limit = p.Skv - j * kBN - 1;
+                if (p.causal) {
+                    const int diag = it.qb * kUnitRows + t * kBM + row + p.causal_off - j * kBN;
+                    limit = diag < limit ? diag : limit;
+                }
+                if (__any_sync(0xFFFFFFFFu, limit < kBN - 1)) {
 #pragma unroll
                     for (int e = 0; e < 128; ++e)
-                        if (e >= valid) s[e] = __float_as_uint(-INFINITY);
+                        if (e > limit) s[e] = __float_as_uint(-INFINITY);
                 }
                 // row max and min: 3-input trees over 4 independent chains each
                 float mxa[4], mna[4];
@@ -524,6 +548,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             }
             if (it.split_slot < 0) {
                 const float inv = 1.0f / l;
+                // natural-log log-sum-exp of the scaled logits: (m_ref*c + log2 l) * ln 2
+                if (p.lse && valid_row)
+                    p.lse[((long long)it.b * p.H + it.h) * p.Sq + qrow] = (m_ref * c + log2f(l)) * kLn2;
 #pragma unroll 1
                 for (int ch = 0; ch < 4; ++ch) {
                     uint32_t o[32];
@@ -599,6 +626,7 @@ struct CombineParams {
     const float* ws_lse;
     __nv_bfloat16* o;
     long long o_sb, o_ss, o_sh;
+    float* lse;            // optional [B][H][Sq] natural-log log-sum-exp, or null
 };
 
 // One warp per output row of a split unit: merge the nsplit partials with weights
@@ -655,6 +683,9 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p
     }
     const bool nan_row = any_nan || mx == -INFINITY;
     const float inv = 1.0f / wsum;
+    // sum_s 2^LSE_s = 2^mx * wsum (base 2), reported in natural log
+    if (p.lse && lane == 0)
+        p.lse[((long long)b * p.H + h) * p.Sq + qrow] = any_nan ? NAN : (mx + log2f(wsum)) * kLn2;
     uint32_t bits[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) bits[e] = nan_row ? 0x7FC0u : round_bf16_bits(acc[e] * inv, p.round_mode);
@@ -677,37 +708,64 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int validate(const void* q, const void* k, const void* v, const void* o, int64_t B, int64_t H,
-             int64_t Sq, int64_t Skv, int64_t d, int layout, int round_mode) {
-    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || Sq < 1 || Skv < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
-    if (layout != ATTN_LAYOUT_BSHD && layout != ATTN_LAYOUT_BHSD) return ATTN_ERR_INVALID_ARG;
-    if (round_mode < ATTN_ROUND_RTNE || round_mode > ATTN_ROUND_RTZ) return ATTN_ERR_INVALID_ARG;
-    if (d != kD) return ATTN_ERR_UNSUPPORTED;
+attn_args_t plain_args(const void* q, const void* k, const void* v, void* o, int64_t B, int64_t H, int64_t Sq,
+                       int64_t Skv, int64_t d, int layout, int round_mode) {
+    attn_args_t a;
+    memset(&a, 0, sizeof a);
+    a.q = q; a.k = k; a.v = v; a.o = o;
+    a.B = B; a.H = H; a.Hkv = H; a.Sq = Sq; a.Skv = Skv; a.d = d;
+    a.layout = layout; a.round_mode = round_mode;
+    return a;
+}
+
+// Shape checks shared by the planner and the launchers (pointers are not looked at).
+int validate_shape(const attn_args_t& a, const attn_options_t* opts) {
+    if (a.B < 1 || a.H < 1 || a.Hkv < 1 || a.Sq < 1 || a.Skv < 1 || a.d < 1) return ATTN_ERR_INVALID_ARG;
+    if (a.H % a.Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (a.layout != ATTN_LAYOUT_BSHD && a.layout != ATTN_LAYOUT_BHSD) return ATTN_ERR_INVALID_ARG;
+    if (a.round_mode < ATTN_ROUND_RTNE || a.round_mode > ATTN_ROUND_RTZ) return ATTN_ERR_INVALID_ARG;
+    if ((a.causal != 0 && a.causal != 1) || a.reserved != 0) return ATTN_ERR_INVALID_ARG;
+    if (a.d != kD) return ATTN_ERR_UNSUPPORTED;
+    if (a.causal && opts && opts->force_splits > 1) return ATTN_ERR_UNSUPPORTED;
     // TMA coordinates and the kernels' unit/row indices are int32
     const int64_t lim = (int64_t)1 << 30;
-    if (Sq > lim || Skv > lim || B > lim || H > lim) return ATTN_ERR_UNSUPPORTED;
-    if (B * H > lim || B * H * cdiv(Sq, kUnitRows) > lim) return ATTN_ERR_UNSUPPORTED;
-    if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)o) & 15u) return ATTN_ERR_MISALIGNED;
-    const uintptr_t ob = (uintptr_t)o, oe = ob + (uintptr_t)(B * H * Sq * d * 2);
-    const uintptr_t qb = (uintptr_t)q, qe = qb + (uintptr_t)(B * H * Sq * d * 2);
-    const uintptr_t kb = (uintptr_t)k, ke = kb + (uintptr_t)(B * H * Skv * d * 2);
-    const uintptr_t vb = (uintptr_t)v, ve = vb + (uintptr_t)(B * H * Skv * d * 2);
-    auto overlap = [](uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; };
-    if (overlap(ob, oe, qb, qe) || overlap(ob, oe, kb, ke) || overlap(ob, oe, vb, ve)) return ATTN_ERR_ALIAS;
+    if (a.Sq > lim || a.Skv > lim || a.B > lim || a.H > lim) return ATTN_ERR_UNSUPPORTED;
+    if (a.B * a.H > lim || a.B * a.H * cdiv(a.Sq, kUnitRows) > lim) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
 
-void make_plan(int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t sms, const attn_options_t* opts,
-               attn_plan_t* pl) {
-    const int64_t nq = cdiv(Sq, kUnitRows);
-    const int64_t U = B * H * nq;
-    const int64_t nkv = cdiv(Skv, kBN);
+int validate(const attn_args_t& a, const attn_options_t* opts) {
+    if (!a.q || !a.k || !a.v || !a.o) return ATTN_ERR_INVALID_ARG;
+    const int st = validate_shape(a, opts);
+    if (st != ATTN_OK) return st;
+    if (((uintptr_t)a.q | (uintptr_t)a.k | (uintptr_t)a.v | (uintptr_t)a.o) & 15u) return ATTN_ERR_MISALIGNED;
+    if ((uintptr_t)a.lse & 3u) return ATTN_ERR_MISALIGNED;
+    const uintptr_t qbytes = (uintptr_t)(a.B * a.H * a.Sq * a.d * 2), kvbytes = (uintptr_t)(a.B * a.Hkv * a.Skv * a.d * 2);
+    const uintptr_t ob = (uintptr_t)a.o, oe = ob + qbytes;
+    const uintptr_t qb = (uintptr_t)a.q, qe = qb + qbytes;
+    const uintptr_t kb = (uintptr_t)a.k, ke = kb + kvbytes;
+    const uintptr_t vb = (uintptr_t)a.v, ve = vb + kvbytes;
+    auto overlap = [](uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; };
+    if (overlap(ob, oe, qb, qe) || overlap(ob, oe, kb, ke) || overlap(ob, oe, vb, ve)) return ATTN_ERR_ALIAS;
+    if (a.lse) {
+        const uintptr_t lb = (uintptr_t)a.lse, le = lb + (uintptr_t)(a.B * a.H * a.Sq * 4);
+        if (overlap(lb, le, ob, oe) || overlap(lb, le, qb, qe) || overlap(lb, le, kb, ke) || overlap(lb, le, vb, ve))
+            return ATTN_ERR_ALIAS;
+    }
+    return ATTN_OK;
+}
+
+void make_plan(const attn_args_t& a, int64_t sms, const attn_options_t* opts, attn_plan_t* pl) {
+    const int64_t nq = cdiv(a.Sq, kUnitRows);
+    const int64_t U = a.B * a.H * nq;
+    const int64_t nkv = cdiv(a.Skv, kBN);
     int64_t G = sms;
     if (opts && opts->max_ctas > 0 && opts->max_ctas < G) G = opts->max_ctas;
     if (G < 1) G = 1;
     int64_t full = U, split_units = 0, ns = 1;
-    if (opts && opts->force_splits > 0) {
+    if (a.causal) {
+        // causal units differ in length and run heaviest first: no key split
+    } else if (opts && opts->force_splits > 0) {
         ns = opts->force_splits < nkv ? opts->force_splits : nkv;
         if (ns > 1) { full = 0; split_units = U; }
         else ns = 1;
@@ -786,17 +844,22 @@ bool encode_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t H, int64_t S
     return r == CUDA_SUCCESS;
 }
 
-int launch(const void* q, const void* k, const void* v, void* o, int64_t B, int64_t H, int64_t Sq, int64_t Skv,
-           int layout, int round_mode, const attn_plan_t& pl, const attn_options_t* opts, void* ws,
-           cudaStream_t stream) {
-    const bool bshd = layout == ATTN_LAYOUT_BSHD;
+int launch(const attn_args_t& a, const attn_plan_t& pl, const attn_options_t* opts, void* ws, cudaStream_t stream) {
+    const int64_t B = a.B, H = a.H, Sq = a.Sq, Skv = a.Skv;
+    const int round_mode = a.round_mode;
+    void* o = a.o;
+    const bool bshd = a.layout == ATTN_LAYOUT_BSHD;
     CUtensorMap qm, km, vm, om;
-    if (!encode_map(&qm, q, B, H, Sq, bshd) || !encode_map(&km, k, B, H, Skv, bshd) ||
-        !encode_map(&vm, v, B, H, Skv, bshd) || !encode_map(&om, o, B, H, Sq, bshd, kStageRowsPerWarp))
+    if (!encode_map(&qm, a.q, B, H, Sq, bshd) || !encode_map(&km, a.k, B, a.Hkv, Skv, bshd) ||
+        !encode_map(&vm, a.v, B, a.Hkv, Skv, bshd) || !encode_map(&om, o, B, H, Sq, bshd, kStageRowsPerWarp))
         return ATTN_ERR_CUDA;
     FwdParams p;
     memset(&p, 0, sizeof p);
     p.B = (int)B; p.H = (int)H; p.Sq = (int)Sq; p.Skv = (int)Skv;
+    p.group = (int)(H / a.Hkv);
+    p.causal = a.causal;
+    p.causal_off = (int)(Skv - Sq);
+    p.lse = a.lse;
     p.nq = (int)cdiv(Sq, kUnitRows);
     p.nkv = (int)pl.kv_tiles;
     p.n_items = (int)pl.items;
@@ -827,6 +890,7 @@ int launch(const void* q, const void* k, const void* v, void* o, int64_t B, int6
         c.split_units = (int)pl.split_units; c.round_mode = round_mode;
         c.ws_o = p.ws_o; c.ws_lse = p.ws_lse; c.o = p.o;
         c.o_sb = p.o_sb; c.o_ss = p.o_ss; c.o_sh = p.o_sh;
+        c.lse = a.lse;
         const long long rows = pl.split_units * kUnitRows;
         const int warps_per_block = 8;
         const unsigned blocks = (unsigned)cdiv(rows, warps_per_block);
@@ -879,90 +943,118 @@ int noalloc_scratch(void** out) {
     return ATTN_OK;
 }
 
+// Library-owned workspace of the current device, grown on demand (guarded by g_mutex).
+int library_workspace(DeviceInfo* di, size_t bytes, void** ws) {
+    std::lock_guard<std::mutex> g(g_mutex);
+    if (di->ws_bytes < bytes) {
+        if (di->ws) cudaFree(di->ws);   // synchronizes the device: old users are done
+        di->ws = nullptr;
+        di->ws_bytes = 0;
+        if (cudaMalloc(&di->ws, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+        di->ws_bytes = bytes;
+    }
+    *ws = di->ws;
+    return ATTN_OK;
+}
+
+// The launch path shared by every entry point.  ws_mode: 0 = caller workspace (must be large
+// enough), 1 = caller workspace or, if null, the library-owned one, 2 = the static scratch.
+int run(const attn_args_t& a, const attn_options_t* opts, void* workspace, size_t workspace_bytes, int ws_mode,
+        cudaStream_t stream) {
+    int st = validate(a, opts);
+    if (st != ATTN_OK) return st;
+    DeviceInfo* di = nullptr;
+    if ((st = device_info(&di)) != ATTN_OK) return st;
+    attn_plan_t pl;
+    make_plan(a, di->sms, opts, &pl);
+    void* ws = nullptr;
+    if (pl.workspace_bytes) {
+        const size_t need = (size_t)pl.workspace_bytes;
+        if (ws_mode == 2) {
+            if (need > kStaticScratchBytes) return ATTN_ERR_WORKSPACE;
+            // every scratch byte the combine reads is written by the attention kernel of the
+            // same call, so stale contents from an earlier call need no clearing
+            if ((st = noalloc_scratch(&ws)) != ATTN_OK) return st;
+        } else if (workspace) {
+            if (workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+            if ((uintptr_t)workspace & 15u) return ATTN_ERR_MISALIGNED;
+            ws = workspace;
+        } else if (ws_mode == 1) {
+            if ((st = library_workspace(di, need, &ws)) != ATTN_OK) return st;
+        } else {
+            return ATTN_ERR_WORKSPACE;
+        }
+    }
+    return launch(a, pl, opts, ws, stream);
+}
+
+size_t workspace_for(const attn_args_t& a, const attn_options_t* opts) {
+    if (validate_shape(a, opts) != ATTN_OK) return 0;
+    DeviceInfo* di = nullptr;
+    if (device_info(&di) != ATTN_OK) return 0;
+    attn_plan_t pl;
+    make_plan(a, di->sms, opts, &pl);
+    return (size_t)pl.workspace_bytes;
+}
+
 }  // namespace
 
 extern "C" {
 
+int attn_plan_ex(const attn_args_t* args, int64_t num_sms, const attn_options_t* opts, attn_plan_t* plan) {
+    if (!args || !plan || num_sms < 1) return ATTN_ERR_INVALID_ARG;
+    const int st = validate_shape(*args, opts);
+    if (st != ATTN_OK) return st;
+    make_plan(*args, num_sms, opts, plan);
+    return ATTN_OK;
+}
+
 int attn_plan(int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t d, int64_t num_sms,
               const attn_options_t* opts, attn_plan_t* plan) {
-    if (!plan || B < 1 || H < 1 || Sq < 1 || Skv < 1 || num_sms < 1) return ATTN_ERR_INVALID_ARG;
-    if (d != kD) return ATTN_ERR_UNSUPPORTED;
-    make_plan(B, H, Sq, Skv, num_sms, opts, plan);
-    return ATTN_OK;
+    const attn_args_t a = plain_args(nullptr, nullptr, nullptr, nullptr, B, H, Sq, Skv, d, 0, 0);
+    return attn_plan_ex(&a, num_sms, opts, plan);
+}
+
+size_t attn_fwd_ex_workspace_size(const attn_args_t* args, const attn_options_t* opts) {
+    return args ? workspace_for(*args, opts) : 0;
 }
 
 size_t attn_fwd_workspace_size_opts(int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t d,
                                     const attn_options_t* opts) {
-    if (B < 1 || H < 1 || Sq < 1 || Skv < 1 || d != kD) return 0;
-    DeviceInfo* di = nullptr;
-    if (device_info(&di) != ATTN_OK) return 0;
-    attn_plan_t pl;
-    make_plan(B, H, Sq, Skv, di->sms, opts, &pl);
-    return (size_t)pl.workspace_bytes;
+    const attn_args_t a = plain_args(nullptr, nullptr, nullptr, nullptr, B, H, Sq, Skv, d, 0, 0);
+    return workspace_for(a, opts);
 }
 
 size_t attn_fwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t d) {
     return attn_fwd_workspace_size_opts(B, H, Sq, Skv, d, nullptr);
 }
 
+int attn_fwd_ex(const attn_args_t* args, const attn_options_t* opts, void* workspace, size_t workspace_bytes,
+                attn_stream_t stream) {
+    if (!args) return ATTN_ERR_INVALID_ARG;
+    return run(*args, opts, workspace, workspace_bytes, 1, (cudaStream_t)stream);
+}
+
 int attn_fwd_ws(const void* q, const void* k, const void* v, void* o, int64_t B, int64_t H, int64_t Sq,
                 int64_t Skv, int64_t d, int layout, int round_mode, const attn_options_t* opts, void* workspace,
                 size_t workspace_bytes, attn_stream_t stream) {
-    int st = validate(q, k, v, o, B, H, Sq, Skv, d, layout, round_mode);
-    if (st != ATTN_OK) return st;
-    DeviceInfo* di = nullptr;
-    if ((st = device_info(&di)) != ATTN_OK) return st;
-    attn_plan_t pl;
-    make_plan(B, H, Sq, Skv, di->sms, opts, &pl);
-    if (pl.workspace_bytes) {
-        if (!workspace || workspace_bytes < (size_t)pl.workspace_bytes) return ATTN_ERR_WORKSPACE;
-        if ((uintptr_t)workspace & 15u) return ATTN_ERR_MISALIGNED;
-    }
-    return launch(q, k, v, o, B, H, Sq, Skv, layout, round_mode, pl, opts, workspace, (cudaStream_t)stream);
+    const attn_args_t a = plain_args(q, k, v, o, B, H, Sq, Skv, d, layout, round_mode);
+    return run(a, opts, workspace, workspace_bytes, 0, (cudaStream_t)stream);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, int64_t B, int64_t H, int64_t Sq, int64_t Skv,
              int64_t d, int layout, int round_mode, attn_stream_t stream) {
-    int st = validate(q, k, v, o, B, H, Sq, Skv, d, layout, round_mode);
-    if (st != ATTN_OK) return st;
-    DeviceInfo* di = nullptr;
-    if ((st = device_info(&di)) != ATTN_OK) return st;
-    attn_plan_t pl;
-    make_plan(B, H, Sq, Skv, di->sms, nullptr, &pl);
-    void* ws = nullptr;
-    if (pl.workspace_bytes) {
-        std::lock_guard<std::mutex> g(g_mutex);
-        if (di->ws_bytes < (size_t)pl.workspace_bytes) {
-            if (di->ws) cudaFree(di->ws);   // synchronizes the device: old users are done
-            di->ws = nullptr;
-            di->ws_bytes = 0;
-            if (cudaMalloc(&di->ws, (size_t)pl.workspace_bytes) != cudaSuccess) {
-                cudaGetLastError();
-                return ATTN_ERR_CUDA;
-            }
-            di->ws_bytes = (size_t)pl.workspace_bytes;
-        }
-        ws = di->ws;
-    }
-    return launch(q, k, v, o, B, H, Sq, Skv, layout, round_mode, pl, nullptr, ws, (cudaStream_t)stream);
+    const attn_args_t a = plain_args(q, k, v, o, B, H, Sq, Skv, d, layout, round_mode);
+    return run(a, nullptr, nullptr, 0, 1, (cudaStream_t)stream);
 }
 
 int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, int64_t B, int64_t H, int64_t Sq,
                      int64_t Skv, int64_t d, int layout, int round_mode, attn_stream_t stream) {
-    int st = validate(q, k, v, o, B, H, Sq, Skv, d, layout, round_mode);
-    if (st != ATTN_OK) return st;
-    DeviceInfo* di = nullptr;
-    if ((st = device_info(&di)) != ATTN_OK) return st;
-    attn_plan_t pl;
-    make_plan(B, H, Sq, Skv, di->sms, nullptr, &pl);
-    void* ws = nullptr;
-    if (pl.workspace_bytes) {
-        if ((size_t)pl.workspace_bytes > kStaticScratchBytes) return ATTN_ERR_WORKSPACE;
-        // every scratch byte the combine reads is written by the attention kernel of the same
-        // call, so stale contents from an earlier call need no clearing
-        if ((st = noalloc_scratch(&ws)) != ATTN_OK) return st;
-    }
-    return launch(q, k, v, o, B, H, Sq, Skv, layout, round_mode, pl, nullptr, ws, (cudaStream_t)stream);
+    const attn_args_t a = plain_args(q, k, v, o, B, H, Sq, Skv, d, layout, round_mode);
+    return run(a, nullptr, nullptr, 0, 2, (cudaStream_t)stream);
 }
 
 int attn_get_device_status(attn_stream_t stream, int32_t* site) {

@@ -92,6 +92,39 @@ typedef struct {
 } attn_plan_t;
 
 /*
+ * Full argument set of the attention forward, for attn_fwd_ex().  Beyond attn_fwd it adds the
+ * two features the MoonMath article's limitations paragraph lists as missing from its MI300X
+ * kernel -- causal masking and grouped K/V heads (GQA; MQA when Hkv = 1) -- and the row
+ * log-sum-exp, the intermediate that "AMD zverejnilo postup pre custom diffusion attention
+ * kernel vo FlyDSL na ROCm" (section "Debug, profiling and integration") checks against a
+ * baseline and that a backward pass needs.
+ *   q            bf16, [B, Sq, H, d] (BSHD) or [B, H, Sq, d] (BHSD)
+ *   k, v         bf16, same layout with Skv rows and Hkv heads; query head h reads K/V head
+ *                h / (H / Hkv); Hkv must divide H
+ *   o            bf16, like q; must not overlap q, k, v or lse
+ *   lse          optional fp32 output, [B][H][Sq] (row (b, h, i) at (b*H + h)*Sq + i): natural
+ *                log of sum_j exp(s_j) over the visible keys, s_j = q_i.k_j / sqrt(d); NaN for a
+ *                row whose visible logits hold a NaN or +inf, -inf when every visible logit is
+ *                -inf or no key is visible.  NULL: not written.  4-byte aligned.
+ *   causal       0: every key visible.  1: key j visible to query i iff j <= i + (Skv - Sq)
+ *                (aligned at the last query and key; plain causal when Sq = Skv).  Masked keys
+ *                take no part in the row; a query with no visible key gets NaN outputs.  Known
+ *                deviation: a masked key inside the 128-key tile that holds the row's diagonal
+ *                still meets the P.V product with weight 0, so a +-inf or NaN in its V row turns
+ *                that output column NaN (0 * inf).
+ *   reserved     must be 0.
+ */
+typedef struct {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;
+    int64_t B, H, Hkv, Sq, Skv, d;
+    int32_t layout, round_mode, causal, reserved;
+} attn_args_t;
+
+/*
  * attn_fwd -- O = softmax(Q K^T / sqrt(d)) V on `stream`.
  *   q           device pointer, bf16, [B, Sq, H, d] (BSHD) or [B, H, Sq, d] (BHSD)
  *   k, v        device pointers, bf16, same layout with Skv rows
@@ -128,6 +161,23 @@ size_t attn_fwd_workspace_size_opts(int64_t B, int64_t H, int64_t Sq, int64_t Sk
  */
 int attn_plan(int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t d, int64_t num_sms,
               const attn_options_t* opts, attn_plan_t* plan);
+
+/*
+ * attn_fwd_ex -- the attention forward with every option (attn_args_t) on `stream`.
+ * workspace: caller device memory of at least attn_fwd_ex_workspace_size() bytes, 16-byte
+ * aligned; or NULL to use the library-owned workspace (which may be grown with cudaMalloc, as
+ * in attn_fwd).  The causal planner never splits keys (no workspace); opts->force_splits > 1
+ * with causal = 1 is ATTN_ERR_UNSUPPORTED.  Errors as for attn_fwd.
+ */
+int attn_fwd_ex(const attn_args_t* args, const attn_options_t* opts, void* workspace,
+                size_t workspace_bytes, attn_stream_t stream);
+
+/* Workspace bytes attn_fwd_ex needs for these arguments and options (0 if none or invalid). */
+size_t attn_fwd_ex_workspace_size(const attn_args_t* args, const attn_options_t* opts);
+
+/* attn_plan for the full argument set (host only; pointers in args are not read). */
+int attn_plan_ex(const attn_args_t* args, int64_t num_sms, const attn_options_t* opts,
+                 attn_plan_t* plan);
 
 /*
  * attn_fwd_noalloc -- attn_fwd for callers that cannot allocate device memory.  (The paper

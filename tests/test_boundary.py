@@ -112,3 +112,59 @@ def test_planner_forced_options(lib):
     assert p["grid"] == 5
     with pytest.raises(attn.AttnError):
         attn.plan(1, 1, 1, 1, 64)
+
+
+def ex_args(q=P, k=2 * P, v=3 * P, o=4 * P, lse=0, B=1, H=2, Hkv=2, Sq=8, Skv=8, d=128, layout=0,
+            mode=0, causal=0, reserved=0):
+    a = attn.Args()
+    a.q, a.k, a.v, a.o, a.lse = q, k, v, o, (lse or None)
+    a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d = B, H, Hkv, Sq, Skv, d
+    a.layout, a.round_mode, a.causal, a.reserved = layout, mode, causal, reserved
+    return a
+
+
+def call_ex(lib, opts=None, **kw):
+    return lib.attn_fwd_ex(ctypes.byref(ex_args(**kw)), ctypes.byref(opts) if opts else None,
+                           None, 0, None)
+
+
+def test_ex_argument_errors(lib):
+    assert lib.attn_fwd_ex(None, None, None, 0, None) == 1
+    assert call_ex(lib, q=0) == 1
+    for kw in ({"Hkv": 0}, {"Hkv": 3, "H": 4}, {"Hkv": 4, "H": 2}, {"causal": 2},
+               {"causal": -1}, {"reserved": 1}, {"layout": 5}, {"mode": 7}):
+        assert call_ex(lib, **kw) == 1, kw
+    assert call_ex(lib, d=64) == 2
+    # causal with a forced key split is refused: the causal planner never splits
+    assert call_ex(lib, causal=1, opts=attn.Options(3, 0, 0, 0)) == 2
+    assert call_ex(lib, lse=5 * P + 2) == 3
+    # lse [B*H*Sq] fp32 = 64 bytes: overlapping o, q or v is an alias
+    assert call_ex(lib, lse=4 * P + 16) == 4
+    assert call_ex(lib, lse=P + 2044) == 4
+    assert call_ex(lib, lse=3 * P - 32) == 4
+    # k, v hold B*Hkv*Skv*d elements: with Hkv=1 they end earlier, so o right after k fits
+    assert call_ex(lib, H=2, Hkv=1, o=2 * P + 8 * 128 * 2, q=6 * P) != 4
+
+
+@pytest.mark.skipif(not NO_GPU, reason="valid arguments would launch on a real GPU")
+def test_ex_valid_args_without_gpu_report_no_device(lib):
+    assert call_ex(lib) == 5
+    W = 1 << 24   # far apart: no overlap at this size
+    assert call_ex(lib, q=W, k=2 * W, v=3 * W, o=4 * W, lse=5 * W, H=8, Hkv=1, causal=1, Sq=100,
+                   Skv=300, layout=1, mode=2) == 5
+    assert lib.attn_fwd_ex_workspace_size(ctypes.byref(ex_args()), None) == 0
+
+
+@pytest.mark.parametrize("shape", PLAN_SHAPES)
+def test_planner_ex_matches_plain_and_causal_never_splits(lib, shape):
+    B, H, Sq, Skv = shape
+    assert attn.plan_ex(B, H, Sq, Skv) == attn.plan(B, H, Sq, Skv)
+    # grouped heads do not change the work split: units are query-head row tiles
+    if H % 2 == 0:
+        assert attn.plan_ex(B, H, Sq, Skv, Hkv=H // 2) == attn.plan(B, H, Sq, Skv)
+    p = attn.plan_ex(B, H, Sq, Skv, causal=True)
+    assert p["split_units"] == 0 and p["splits"] == 1 and p["workspace_bytes"] == 0
+    assert p["full_items"] == p["units"] == B * H * -(-Sq // 256)
+    assert 1 <= p["grid"] <= min(152, p["units"])
+    with pytest.raises(attn.AttnError):
+        attn.plan_ex(B, H, Sq, Skv, causal=True, force_splits=2)

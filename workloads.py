@@ -3,10 +3,11 @@
 Both the oracle side and the CUDA side draw their inputs from this module and nothing
 else; it holds no step of the method.  Shapes and value distributions follow the pages'
 workloads: i.i.d. N(0, sigma^2) entries drawn in fp32 then rounded to bf16 (RTNE), in the
-BSHD (B, S, H, d) or BHSD (B, H, S, d) layout, d = 128.  The five named workloads are a
-tiny self-attention, a square self-attention, a diffusion-style cross-attention with a KV
-length that is not a tile multiple, a video-diffusion self-attention (1536 hidden =
-12 heads x 128) and a long-KV stress case with large logits and sparse non-finite entries.
+BSHD (B, S, H, d) or BHSD (B, H, S, d) layout, d = 128.  The named workloads are a tiny
+self-attention, a square self-attention, a diffusion-style cross-attention with a KV length
+that is not a tile multiple, a video-diffusion self-attention (1536 hidden = 12 heads x 128),
+a long-KV stress case with large logits and sparse non-finite entries, and a decoder-style
+causal prefill whose K and V carry a quarter of the query heads.
 """
 from __future__ import annotations
 
@@ -28,21 +29,39 @@ class Workload:
     sigma: float = 1.0
     nonfinite_frac: float = 0.0   # fraction of K and V entries set to +inf/-inf/NaN
     seed: int = 0
+    Hkv: int = 0                  # K/V heads; 0 means H (no grouping)
+    causal: bool = False          # key j visible to query i iff j <= i + Skv - Sq
+
+    @property
+    def kv_heads(self) -> int:
+        return self.Hkv or self.H
+
+    @property
+    def visible_pairs(self) -> int:
+        """Number of (query, key) pairs that take part, per (b, h)."""
+        if not self.causal:
+            return self.Sq * self.Skv
+        off = self.Skv - self.Sq
+        # row i sees min(max(i + off + 1, 0), Skv) keys
+        return sum(min(max(i + off + 1, 0), self.Skv) for i in range(self.Sq))
 
     @property
     def flop(self) -> int:
-        """4*B*H*Sq*Skv*d: two matrix products of 2*Sq*Skv*d flops per (b, h)."""
-        return 4 * self.B * self.H * self.Sq * self.Skv * self.d
+        """4*d flops per visible (query, key) pair and head: the two matrix products (2*d
+        each); 4*B*H*Sq*Skv*d without the causal mask."""
+        return 4 * self.B * self.H * self.visible_pairs * self.d
 
     @property
     def min_bytes(self) -> int:
-        """Q, K, V read once and O written once, bf16."""
-        return 2 * self.B * self.H * self.d * (2 * self.Sq + 2 * self.Skv)
+        """Q read and O written once, K and V (Hkv heads) read once, bf16."""
+        return 2 * self.B * self.d * (2 * self.H * self.Sq + 2 * self.kv_heads * self.Skv)
 
     def describe(self) -> str:
-        return ("B=%d H=%d Sq=%d Skv=%d d=%d %s sigma=%g nonfinite=%g seed=%d"
+        extra = (" Hkv=%d" % self.kv_heads if self.kv_heads != self.H else "") + \
+                (" causal" if self.causal else "")
+        return ("B=%d H=%d Sq=%d Skv=%d d=%d %s sigma=%g nonfinite=%g seed=%d%s"
                 % (self.B, self.H, self.Sq, self.Skv, self.d, self.layout.upper(),
-                   self.sigma, self.nonfinite_frac, self.seed))
+                   self.sigma, self.nonfinite_frac, self.seed, extra))
 
 
 WORKLOADS = {
@@ -53,6 +72,9 @@ WORKLOADS = {
     "video": Workload("video", 1, 12, 32760, 32760, 128, "bshd", ("rtne", "rtz"), seed=3),
     "stress": Workload("stress", 1, 8, 128, 65536, 128, "bhsd", ("rtna",), sigma=4.0,
                        nonfinite_frac=1e-4, seed=4),
+    # decoder-style prefill: causal mask with 4 query heads per K/V head
+    "causal_gqa": Workload("causal_gqa", 2, 32, 8192, 8192, 128, "bshd", ("rtne",), seed=5,
+                           Hkv=8, causal=True),
 }
 
 
@@ -80,13 +102,15 @@ def _plant_nonfinite(gen: torch.Generator, t: torch.Tensor, frac: float) -> None
 
 
 def make_qkv(B: int, H: int, Sq: int, Skv: int, d: int = 128, layout: str = "bshd",
-             seed: int = 0, sigma: float = 1.0, nonfinite_frac: float = 0.0):
-    """Draw Q, then K, then V (CPU bf16 tensors) from one seeded generator."""
+             seed: int = 0, sigma: float = 1.0, nonfinite_frac: float = 0.0, Hkv: int | None = None):
+    """Draw Q, then K, then V (CPU bf16 tensors) from one seeded generator.  K and V carry
+    ``Hkv`` heads (default H; fewer for grouped-query or multi-query attention)."""
+    Hkv = H if Hkv is None else Hkv
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
     q = _randn_bf16(gen, shape(layout, B, H, Sq, d), sigma)
-    k = _randn_bf16(gen, shape(layout, B, H, Skv, d), sigma)
-    v = _randn_bf16(gen, shape(layout, B, H, Skv, d), sigma)
+    k = _randn_bf16(gen, shape(layout, B, Hkv, Skv, d), sigma)
+    v = _randn_bf16(gen, shape(layout, B, Hkv, Skv, d), sigma)
     if nonfinite_frac > 0:
         _plant_nonfinite(gen, k, nonfinite_frac)
         _plant_nonfinite(gen, v, nonfinite_frac)
@@ -95,7 +119,7 @@ def make_qkv(B: int, H: int, Sq: int, Skv: int, d: int = 128, layout: str = "bsh
 
 def make_workload(w: Workload):
     return make_qkv(w.B, w.H, w.Sq, w.Skv, w.d, w.layout, w.seed, w.sigma,
-                    w.nonfinite_frac)
+                    w.nonfinite_frac, Hkv=w.kv_heads)
 
 
 def sample_rows(B: int, H: int, Sq: int, n: int, seed: int = 1234) -> torch.Tensor:
