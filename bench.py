@@ -9,6 +9,9 @@ consecutive calls rotate over enough input sets that their total exceeds the 126
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
+Causal workloads count 4*d flops per visible (query, key) pair and head, i.e. the masked
+half of the score matrix is not counted as work.
+
 --impl reference times the CPU oracle (fp64, OpenMP) on a bounded sample of the same
 workload on the host cores.  Under torchrun (N > 1) each rank runs an independent replica
 (no collective on the data path); value = all ranks' flops / max elapsed time over ranks.
@@ -35,8 +38,10 @@ from workloads import WORKLOADS, make_qkv  # noqa: E402
 METRIC = "attention fwd TFLOPS (4*B*H*Sq*Skv*d) and % of GB300 bf16 dense peak"
 FALLBACK_PEAK_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
-DEFAULT_STEPS = {"square": 1000, "cross": 1000, "video": 60, "stress": 1000, "tiny": 1000}
-DEFAULT_WARMUP = {"square": 100, "cross": 100, "video": 5, "stress": 100, "tiny": 100}
+DEFAULT_STEPS = {"square": 1000, "cross": 1000, "video": 60, "stress": 1000, "tiny": 1000,
+                 "causal_gqa": 200}
+DEFAULT_WARMUP = {"square": 100, "cross": 100, "video": 5, "stress": 100, "tiny": 100,
+                  "causal_gqa": 20}
 L2_BYTES = 126 * 2**20
 
 
@@ -175,6 +180,14 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def visible_keys(w, rows) -> int:
+    """Keys that take part, summed over flat query rows (b*H + h)*Sq + i."""
+    if not w.causal:
+        return len(rows) * w.Skv
+    off = w.Skv - w.Sq
+    return sum(min(max(r % w.Sq + off + 1, 0), w.Skv) for r in rows)
+
+
 def cpu_oracle_sample(w, qkv_cpu, mode: str, seconds: float, seed: int = 99):
     """Time the oracle on a seeded row sample sized to about `seconds` of host work."""
     import oracle
@@ -183,19 +196,20 @@ def cpu_oracle_sample(w, qkv_cpu, mode: str, seconds: float, seed: int = 99):
     threads = len(os.sched_getaffinity(0))
     g = torch.Generator().manual_seed(seed)
     probe = torch.randint(0, total, (8 * threads,), generator=g).tolist()
-    oracle.attention(q, k, v, w.layout, mode, rows=probe[:threads], threads=threads)   # warm-up
+    oracle.attention(q, k, v, w.layout, mode, rows=probe[:threads], threads=threads,
+                     causal=w.causal)   # warm-up
     t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.layout, mode, rows=probe, threads=threads)
+    oracle.attention(q, k, v, w.layout, mode, rows=probe, threads=threads, causal=w.causal)
     dt = max(time.perf_counter() - t0, 1e-4)
     n = int(max(threads, min(total, len(probe) * seconds / dt)))
     rows = torch.randint(0, total, (n,), generator=g).tolist()
     t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.layout, mode, rows=rows, threads=threads)
+    oracle.attention(q, k, v, w.layout, mode, rows=rows, threads=threads, causal=w.causal)
     dt = time.perf_counter() - t0
-    flop = 4.0 * n * w.Skv * w.d
+    flop = 4.0 * visible_keys(w, rows) * w.d
     return {"value": flop / dt / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
-            "sample": "%d of %d query rows (seeded), all %d keys, mode %s, %.1f s"
-                      % (n, total, w.Skv, mode, dt)}
+            "sample": "%d of %d query rows (seeded), %s keys, mode %s, %.1f s"
+                      % (n, total, "their visible" if w.causal else "all %d" % w.Skv, mode, dt)}
 
 
 def run_reference(args, w, rank, world):
@@ -205,36 +219,38 @@ def run_reference(args, w, rank, world):
     warmup = args.warmup if args.warmup is not None else DEFAULT_WARMUP[w.name]
     import oracle
     q, k, v = make_qkv(w.B, w.H, w.Sq, w.Skv, w.d, w.layout, seed=w.seed, sigma=w.sigma,
-                       nonfinite_frac=w.nonfinite_frac)
+                       nonfinite_frac=w.nonfinite_frac, Hkv=w.kv_heads)
     threads = len(os.sched_getaffinity(0))
     total = w.B * w.H * w.Sq
     budget = 150.0                           # seconds for the whole run
     g = torch.Generator().manual_seed(7)
     probe = torch.randint(0, total, (max(threads, 8),), generator=g).tolist()
     t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.layout, w.modes[0], rows=probe, threads=threads)
+    oracle.attention(q, k, v, w.layout, w.modes[0], rows=probe, threads=threads, causal=w.causal)
     per_row = max(time.perf_counter() - t0, 1e-4) / len(probe)
     rows_per_step = int(max(1, min(total, budget / (steps + warmup) / per_row)))
     samples = [torch.randint(0, total, (rows_per_step,), generator=g).tolist()
                for _ in range(min(steps + warmup, 8))]
     for i in range(warmup):
         oracle.attention(q, k, v, w.layout, w.modes[i % len(w.modes)],
-                         rows=samples[i % len(samples)], threads=threads)
+                         rows=samples[i % len(samples)], threads=threads, causal=w.causal)
     t0 = time.perf_counter()
     for i in range(steps):
         oracle.attention(q, k, v, w.layout, w.modes[i % len(w.modes)],
-                         rows=samples[i % len(samples)], threads=threads)
+                         rows=samples[i % len(samples)], threads=threads, causal=w.causal)
     dt = time.perf_counter() - t0
-    flop = 4.0 * rows_per_step * w.Skv * w.d * steps
+    flop = 4.0 * w.d * sum(visible_keys(w, samples[i % len(samples)]) for i in range(steps))
     val = flop / dt / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOPS", "n_gpus": world,
         "steps": steps, "warmup": warmup, "ms_per_step": dt * 1e3 / steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,%g) bf16)" % w.sigma,
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Skv": w.Skv, "d": w.d,
-                   "layout": w.layout, "modes": list(w.modes),
-                   "step": "oracle on %d seeded query rows (all keys)" % rows_per_step},
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.kv_heads, "Sq": w.Sq,
+                   "Skv": w.Skv, "d": w.d, "causal": w.causal, "layout": w.layout,
+                   "modes": list(w.modes),
+                   "step": "oracle on %d seeded query rows (%s keys)"
+                           % (rows_per_step, "visible" if w.causal else "all")},
         "cpu_baseline": {"value": val, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
                          "sample": "%d of %d query rows per step" % (rows_per_step, total)},
         "e2e": {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -263,15 +279,18 @@ def main():
     steps = args.steps if args.steps is not None else DEFAULT_STEPS[w.name]
     warmup = max(3, args.warmup if args.warmup is not None else DEFAULT_WARMUP[w.name])
     modes = list(w.modes)
-    set_bytes = 2 * w.B * w.H * w.d * (2 * w.Sq + 2 * w.Skv)   # q, k, v, o
+    set_bytes = w.min_bytes                                     # q, k, v, o
     nsets = max(1, -(-(2 * L2_BYTES) // set_bytes)) if set_bytes < 2 * L2_BYTES else 1
     cpu_sets = [make_qkv(w.B, w.H, w.Sq, w.Skv, w.d, w.layout, seed=w.seed + 1000 * i,
-                         sigma=w.sigma, nonfinite_frac=w.nonfinite_frac) for i in range(nsets)]
+                         sigma=w.sigma, nonfinite_frac=w.nonfinite_frac, Hkv=w.kv_heads)
+                for i in range(nsets)]
     sets = [tuple(t.to(dev) for t in s) for s in cpu_sets]
     outs = [torch.empty_like(s[0]) for s in sets]
-    plan = attn.plan(w.B, w.H, w.Sq, w.Skv, w.d, torch.cuda.get_device_properties(dev).multi_processor_count)
+    extended = w.causal or w.kv_heads != w.H
+    plan = attn.plan_ex(w.B, w.H, w.Sq, w.Skv, Hkv=w.kv_heads, d=w.d, causal=w.causal,
+                        num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)
     split = plan["split_units"] > 0
-    ws_bytes = attn.workspace_size(w.B, w.H, w.Sq, w.Skv, w.d)
+    ws_bytes = attn.workspace_size_ex(*sets[0], layout=w.layout, causal=w.causal)
     workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     calls_per_step = len(modes)
@@ -281,10 +300,17 @@ def main():
         for e in trio:
             e.record(stream)
 
+    def fwd(q, k, v, o, mode, events=None):
+        if extended:
+            attn.attn_fwd_ex(q, k, v, o, layout=w.layout, round=mode, causal=w.causal,
+                             workspace=workspace, events=events)
+        else:
+            attn.attn_fwd(q, k, v, o, layout=w.layout, round=mode, workspace=workspace,
+                          events=events)
+
     def call(i, mode, events=None):
         s = sets[i % nsets]
-        attn.attn_fwd(s[0], s[1], s[2], outs[i % nsets], layout=w.layout, round=mode,
-                      workspace=workspace, events=events)
+        fwd(s[0], s[1], s[2], outs[i % nsets], mode, events)
 
     for i in range(warmup * calls_per_step):
         call(i, modes[i % calls_per_step])
@@ -350,8 +376,7 @@ def main():
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
             for m, mode in enumerate(modes):
-                attn.attn_fwd(dq, dk, dv, do[m], layout=w.layout, round=mode,
-                              workspace=workspace)
+                fwd(dq, dk, dv, do[m], mode)
                 ho[m].copy_(do[m], non_blocking=True)
 
         for _ in range(3):
@@ -383,8 +408,9 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,%g) bf16%s)" % (
                 w.sigma, ", %g non-finite K/V" % w.nonfinite_frac if w.nonfinite_frac else ""),
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Skv": w.Skv,
-                       "d": w.d, "layout": w.layout, "modes": modes,
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.kv_heads, "Sq": w.Sq,
+                       "Skv": w.Skv, "d": w.d, "causal": w.causal, "layout": w.layout,
+                       "modes": modes, "flop_per_call": flop_call,
                        "step": "%d calls (one per rounding mode)" % calls_per_step,
                        "l2": ("rotating %d input sets, %.0f MB > 126 MB L2" % (nsets, nsets * set_bytes / 2**20))
                              if nsets > 1 else "inputs %.0f MB > 126 MB L2" % (set_bytes / 2**20),

@@ -48,7 +48,7 @@ constexpr int kBM = 128;           // query rows per tile (one TMEM lane per row
 constexpr int kBN = 128;           // keys per KV tile
 constexpr int kQTiles = 2;         // query tiles per work unit
 constexpr int kUnitRows = kBM * kQTiles;
-constexpr int kStages = 4;         // K/V ring depth
+constexpr int kStages = 3;         // K/V ring depth (three 32 KB slots: K_j, V_j, K_j+1)
 constexpr int kTileBytes = kBM * kD * 2;       // 32 KB: 128 rows x 128 bf16
 constexpr int kChunkBytes = kTileBytes / 2;    // 16 KB: 128 rows x 64 bf16 (one TMA box)
 constexpr int kThreads = 384;      // WG0, WG1 softmax; warp 8 TMA; warp 9 MMA; 10-11 spare
@@ -66,14 +66,15 @@ constexpr uint32_t kTmemCols = 512;   // S0 | S1 | O0 | O1, 128 fp32 columns eac
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int kSmemQ = 0;
 constexpr int kSmemRing = kSmemQ + kQTiles * kTileBytes;
-// Output staging: one 8 KB region per TMEM lane quarter (32 rows x 256 B of bf16, as two
-// 64-column halves in the 128-byte swizzle TMA expects), shared by the two query tiles' warps
-// of that quarter in turn.
+// Output staging: one 4 KB region per softmax warp (its 32 rows x 64 bf16 columns in the
+// 128-byte swizzle TMA expects), filled twice per tile (column halves 0 and 1).  Only the
+// warp's own TMA stores read it, so the warp's lane 0 waits for its previous store's read
+// before refilling, and nothing else orders it.
 constexpr int kStageRowsPerWarp = 32;
-constexpr int kStageBytes = kStageRowsPerWarp * kD * 2;
+constexpr int kStageBytes = kStageRowsPerWarp * 64 * 2;
 constexpr int kSmemStage = kSmemRing + kStages * kTileBytes;
-constexpr int kSmemBars = kSmemStage + 4 * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 2 + 3 * kQTiles + 1 + 4;
+constexpr int kSmemBars = kSmemStage + 8 * kStageBytes;
+constexpr int kNumBars = 2 * kStages + 2 + 3 * kQTiles + 1;
 constexpr int kSmemMisc = kSmemBars + kNumBars * 8;
 constexpr int kSmemUsed = kSmemMisc + 16;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
@@ -87,12 +88,11 @@ constexpr int kBarSFull = kBarQEmpty + 1;   // [2] S_i ready in TMEM
 constexpr int kBarPFull = kBarSFull + 2;    // [2] P_i written (and O_i rescaled)
 constexpr int kBarOFull = kBarPFull + 2;    // [2] last PV of the unit done
 constexpr int kBarDrain = kBarOFull + 2;
-constexpr int kBarStageFree = kBarDrain + 1;  // [4] staging region q read out by its TMA store
 
 // wait sites reported through the status word
 enum : uint32_t {
     kSiteQEmpty = 1, kSiteRingEmpty, kSiteQFull, kSiteRingFull, kSitePFull, kSiteSFull,
-    kSiteOFull, kSiteDrain, kSiteTeardown, kSiteStage
+    kSiteOFull, kSiteDrain, kSiteTeardown
 };
 
 __device__ uint32_t g_status[2];   // [0] status code, [1] wait site
@@ -206,6 +206,39 @@ __device__ __forceinline__ uint32_t round_bf16_bits(float f, int mode) {
     return u >> 16;
 }
 
+// Scale 2*N fp32 accumulator columns (bit patterns in o) by inv and round each pair to one
+// packed bf16x2 word in `mode`: the conversion instruction for RTNE and RTZ, and for RTNA the
+// carry of half an ulp into the kept bits (magnitude rounds up at the tie, overflow carries
+// into the exponent and gives inf).  These agree with round_bf16_bits on every non-NaN value;
+// a NaN anywhere among the scaled values sends the whole group to round_bf16_bits, which
+// gives NaN the pattern 0x7FC0.
+template <int N>
+__device__ __forceinline__ void scale_round_pairs(const uint32_t* o, float inv, int mode, uint32_t* w) {
+    const float2 iv = make_float2(inv, inv);
+    float2 x[N];
+    float probe = 0.0f;
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+        x[e] = __fmul2_rn(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), iv);
+        probe = ptx::fmax3_nan(probe, x[e].x, x[e].y);
+    }
+    if (probe != probe) {
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+            w[e] = round_bf16_bits(x[e].x, mode) | (round_bf16_bits(x[e].y, mode) << 16);
+    } else if (mode == ATTN_ROUND_RTNE) {
+#pragma unroll
+        for (int e = 0; e < N; ++e) w[e] = ptx::pack_bf16x2(x[e].x, x[e].y);
+    } else if (mode == ATTN_ROUND_RTZ) {
+#pragma unroll
+        for (int e = 0; e < N; ++e) w[e] = ptx::pack_bf16x2_rz(x[e].x, x[e].y);
+    } else {
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+            w[e] = __byte_perm(__float_as_uint(x[e].x) + 0x8000u, __float_as_uint(x[e].y) + 0x8000u, 0x7632);
+    }
+}
+
 // softmax weight exponent for logit s relative to the reference m: x = (s - m) * c, which is
 // exactly 0 for the key that set m (so a lone key gets weight 1 and O = its V row), kept
 // >= -125.02 when s is finite so that a finite logit always has a positive (normal) weight;
@@ -247,7 +280,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             ptx::mbar_init(bar(kBarOFull + i), 1);
         }
         ptx::mbar_init(bar(kBarDrain), 1);
-        for (int q = 0; q < 4; ++q) ptx::mbar_init(bar(kBarStageFree + q), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
@@ -538,73 +570,50 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             ptx::tc_fence_after();
             const int qrow = it.qb * kUnitRows + t * kBM + row;
             const bool valid_row = qrow < p.Sq;
-            // staging region of this lane quarter: query tile 0's warp and tile 1's warp take
-            // turns (tile 0 of item u, tile 1 of item u, tile 0 of item u+1, ...), so region
-            // release number 2u + t is this warp's; it waits for number 2u + t - 1
-            const uint32_t region = sbase + kSmemStage + (uint32_t)(quarter * kStageBytes);
-            if (u > 0 || t == 1) {
-                ok = wait_bar(bar(kBarStageFree + quarter), t == 0 ? 1u : 0u, kSiteStage, abort_flag, lim);
-                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-            }
+            // the whole O_t row in registers with one TMEM wait
+            uint32_t o[128];
+            ptx::tmem_ld128(tO, o);
             if (it.split_slot < 0) {
                 const float inv = 1.0f / l;
                 // natural-log log-sum-exp of the scaled logits: (m_ref*c + log2 l) * ln 2
                 if (p.lse && valid_row)
                     p.lse[((long long)it.b * p.H + it.h) * p.Sq + qrow] = (m_ref * c + log2f(l)) * kLn2;
-#pragma unroll 1
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32(tO + ch * 32, o);
-                    uint32_t w[16];
+                const uint32_t region = sbase + kSmemStage + (uint32_t)(warp * kStageBytes);
+                const int r0 = it.qb * kUnitRows + t * kBM + quarter * kStageRowsPerWarp;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const uint32_t lo = round_bf16_bits(__uint_as_float(o[2 * e]) * inv, p.round_mode);
-                        const uint32_t hi = round_bf16_bits(__uint_as_float(o[2 * e + 1]) * inv, p.round_mode);
-                        w[e] = lo | (hi << 16);
-                    }
-                    // row `lane` of the region; 16-byte piece pc of the 64-column half is stored
-                    // at piece pc ^ (lane & 7) (128-byte swizzle)
-                    const uint32_t half = region + (uint32_t)((ch >> 1) * (kStageBytes / 2)) + (uint32_t)lane * 128u;
+                for (int hc = 0; hc < 2; ++hc) {
+                    uint32_t w[32];
+                    scale_round_pairs<32>(o + 64 * hc, inv, p.round_mode, w);
+                    // the region's previous TMA store (if any) has finished reading it
+                    if (lane == 0) ptx::bulk_wait_read0();
+                    __syncwarp();
+                    // row `lane` of the region; 16-byte piece pc is stored at pc ^ (lane & 7)
+                    // (128-byte swizzle)
+                    const uint32_t rowaddr = region + (uint32_t)lane * 128u;
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        const uint32_t pc = (uint32_t)((ch & 1) * 4 + v4);
-                        ptx::st_shared_v4(half + ((pc ^ (uint32_t)(lane & 7)) << 4), w[4 * v4], w[4 * v4 + 1],
-                                          w[4 * v4 + 2], w[4 * v4 + 3]);
+                    for (int pc = 0; pc < 8; ++pc)
+                        ptx::st_shared_v4(rowaddr + (((uint32_t)pc ^ (uint32_t)(lane & 7)) << 4), w[4 * pc],
+                                          w[4 * pc + 1], w[4 * pc + 2], w[4 * pc + 3]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (p.bshd) ptx::tma_store_4d(&omap, region, hc * 64, it.h, r0, it.b);
+                        else ptx::tma_store_4d(&omap, region, hc * 64, r0, it.h, it.b);
+                        ptx::bulk_commit();
                     }
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const int r0 = it.qb * kUnitRows + t * kBM + quarter * kStageRowsPerWarp;
-                    for (int hc = 0; hc < 2; ++hc) {
-                        const uint32_t src = region + (uint32_t)(hc * (kStageBytes / 2));
-                        if (p.bshd) ptx::tma_store_4d(&omap, src, hc * 64, it.h, r0, it.b);
-                        else ptx::tma_store_4d(&omap, src, hc * 64, r0, it.h, it.b);
-                    }
-                    ptx::bulk_commit();
-                    ptx::bulk_wait_read0();
-                    ptx::mbar_arrive(bar(kBarStageFree + quarter));
                 }
             } else {
                 // split partial: O/l in fp32 (the raw sum when l == 0) and LSE in log2 units
                 const float inv = (l > 0.0f) ? 1.0f / l : 1.0f;
                 const long long wrow = (long long)it.split_slot * kUnitRows + t * kBM + row;
-                float* dst = p.ws_o + wrow * kD;
-#pragma unroll 1
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32(tO + ch * 32, o);
-                    if (valid_row) {
-                        float4* d4 = reinterpret_cast<float4*>(dst + ch * 32);
+                if (valid_row) {
+                    float4* d4 = reinterpret_cast<float4*>(p.ws_o + wrow * kD);
 #pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            d4[v4] = make_float4(__uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
-                                                 __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
-                    }
+                    for (int v4 = 0; v4 < 32; ++v4)
+                        d4[v4] = make_float4(__uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
+                                             __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
+                    p.ws_lse[wrow] = m_ref * c + log2f(l);
                 }
-                if (valid_row) p.ws_lse[wrow] = m_ref * c + log2f(l);
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(kBarStageFree + quarter));
             }
         }
     }

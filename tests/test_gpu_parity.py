@@ -175,3 +175,34 @@ def test_workload_sampled_rows(attn, name):
         ref = oracle.attention(q, k, v, w.layout, mode, rows=rows, want_a=True)
         res = parity.compare(parity.gpu_rows_bits(o, w.layout, rows), ref["o_bits"], ref["a"])
         assert res["ok"], (name, mode, res)
+
+
+def _mean_of_values_case(Skv, e_lo, e_hi, seed, Sq=130):
+    """Zero keys make every logit 0, so every weight is exactly 1, l = Skv and O is the plain
+    mean of the V rows: with Skv a power of two and V entries +-(1 + k/128) * 2^e (|e| small)
+    the fp32 sum and the scaling by 1/Skv are exact, so O's rounding alone decides the bits,
+    and about half the columns of a two-key mean sit exactly on a bf16 tie."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(1, 2, Sq, 128, generator=g).to(torch.bfloat16)
+    k = torch.zeros(1, 2, Skv, 128, dtype=torch.bfloat16)
+    mant = 1.0 + torch.randint(0, 128, (1, 2, Skv, 128), generator=g).float() / 128.0
+    ex = torch.randint(e_lo, e_hi + 1, (1, 2, Skv, 128), generator=g).float()
+    sign = torch.where(torch.rand(1, 2, Skv, 128, generator=g) < 0.5, -1.0, 1.0)
+    v = (sign * mant * torch.exp2(ex)).to(torch.bfloat16)
+    assert torch.equal(v.float(), sign * mant * torch.exp2(ex))      # exactly representable
+    return q, k, v
+
+
+@pytest.mark.parametrize("Skv", [2, 4, 64])
+def test_rounding_modes_bit_exact_on_exact_means(attn, Skv):
+    q, k, v = _mean_of_values_case(Skv, -3, 3, seed=90 + Skv)
+    for mode in MODES:
+        for fs in (0, 2) if Skv >= 8 else (0,):
+            o = run(attn, q, k, v, "bhsd", mode, force_splits=fs)
+            ref = oracle.attention(q, k, v, "bhsd", mode)
+            g = parity.gpu_rows_bits(o, "bhsd").reshape(ref["o_bits"].shape)
+            assert np.array_equal(g, ref["o_bits"]), (mode, fs, int((g != ref["o_bits"]).sum()))
+    # the three modes really differ on these inputs (ties and inexact values are present)
+    outs = [run(attn, q, k, v, "bhsd", m).view(torch.int16) for m in MODES]
+    if Skv == 2:
+        assert not torch.equal(outs[0], outs[1]) and not torch.equal(outs[0], outs[2])
