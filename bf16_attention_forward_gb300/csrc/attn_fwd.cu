@@ -48,7 +48,7 @@ constexpr int kBM = 128;           // query rows per tile (one TMEM lane per row
 constexpr int kBN = 128;           // keys per KV tile
 constexpr int kQTiles = 2;         // query tiles per work unit
 constexpr int kUnitRows = kBM * kQTiles;
-constexpr int kStages = 3;         // K/V ring depth (three 32 KB slots: K_j, V_j, K_j+1)
+constexpr int kStages = 4;         // K/V ring depth (four 32 KB slots: two K/V pairs in flight)
 constexpr int kTileBytes = kBM * kD * 2;       // 32 KB: 128 rows x 128 bf16
 constexpr int kChunkBytes = kTileBytes / 2;    // 16 KB: 128 rows x 64 bf16 (one TMA box)
 constexpr int kThreads = 384;      // WG0, WG1 softmax; warp 8 TMA; warp 9 MMA; 10-11 spare
@@ -118,9 +118,12 @@ struct FwdParams {
 };
 
 struct Item {
-    int b, h, qb, kv_begin, kv_end, split_slot;
+    int b, h, hk, qb, kv_begin, kv_end, split_slot;   // hk: the K/V head query head h reads
 };
 
+// Work item k of the static schedule.  kCausal is a template parameter so that the
+// unmasked kernel carries none of the causal code.
+template <bool kCausal>
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int k) {
     Item it;
     int unit;
@@ -138,7 +141,7 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int k) {
         it.kv_end = it.kv_begin + base + (s < rem ? 1 : 0);
         it.split_slot = r;
     }
-    if (p.causal) {
+    if constexpr (kCausal) {
         // heaviest first: query blocks nearest the end see the most keys; each block runs
         // only the key tiles up to its diagonal (at least one, which the mask then empties)
         const int bhn = p.B * p.H;
@@ -149,12 +152,13 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int k) {
         const int last = it.qb * kUnitRows + kUnitRows - 1 + p.causal_off;   // last visible key
         const int need = last < 0 ? 1 : last / kBN + 1;
         it.kv_end = need < it.kv_end ? need : it.kv_end;
-        return it;
+    } else {
+        it.qb = unit % p.nq;
+        const int bh = unit / p.nq;
+        it.h = bh % p.H;
+        it.b = bh / p.H;
     }
-    it.qb = unit % p.nq;
-    const int bh = unit / p.nq;
-    it.h = bh % p.H;
-    it.b = bh / p.H;
+    it.hk = p.group == 1 ? it.h : it.h / p.group;
     return it;
 }
 
@@ -252,6 +256,7 @@ __device__ __forceinline__ float weight_exponent(float s, float c, float m) {
     return fmaf(x, 0x1p-126f, ptx::fmax_nan(x, kMinExponent));
 }
 
+template <bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -305,7 +310,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             int u = 0;
             bool ok = true;
             for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
-                const Item it = decode_item(p, k);
+                const Item it = decode_item<kCausal>(p, k);
                 if (u > 0 && !(ok = wait_bar(bar(kBarQEmpty), (u - 1) & 1, kSiteQEmpty, abort_flag, lim)))
                     break;
                 ptx::mbar_arrive_expect_tx(bar(kBarQFull), kQTiles * kTileBytes);
@@ -330,9 +335,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                         for (int c = 0; c < 2; ++c) {
                             const uint32_t dst = sbase + kSmemRing + slot * kTileBytes + c * kChunkBytes;
                             if (p.bshd)
-                                ptx::tma_load_4d(dst, map, bar(kBarFull + slot), c * 64, it.h / p.group, j * kBN, it.b, pol_kv);
+                                ptx::tma_load_4d(dst, map, bar(kBarFull + slot), c * 64, it.hk, j * kBN, it.b, pol_kv);
                             else
-                                ptx::tma_load_4d(dst, map, bar(kBarFull + slot), c * 64, j * kBN, it.h / p.group, it.b, pol_kv);
+                                ptx::tma_load_4d(dst, map, bar(kBarFull + slot), c * 64, j * kBN, it.hk, it.b, pol_kv);
                         }
                     }
                 }
@@ -390,7 +395,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             int u = 0;
             bool ok = true;
             for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
-                const Item it = decode_item(p, k);
+                const Item it = decode_item<kCausal>(p, k);
                 const int nk = it.kv_end - it.kv_begin;
                 if (!(ok = wait_bar(bar(kBarQFull), u & 1, kSiteQFull, abort_flag, lim))) break;
                 uint32_t kslot = pos % kStages;
@@ -458,7 +463,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         int u = 0;
         bool ok = true;
         for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
-            const Item it = decode_item(p, k);
+            const Item it = decode_item<kCausal>(p, k);
             float m_ref = -INFINITY;      // running max of raw logits at the last rescale
             float l = 0.0f;               // running sum of weights relative to m_ref
             for (int j = it.kv_begin; j < it.kv_end; ++j) {
@@ -470,15 +475,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 ptx::tmem_ld128(tS, s);
                 // keys of this tile past `limit` are absent: beyond Skv, or (causal) past this
                 // row's diagonal; they get -inf logits and so weight 0
-                int limit = p.Skv - j * kBN - 1;
-                if (p.causal) {
+                if constexpr (kCausal) {
+                    int limit = p.Skv - j * kBN - 1;
                     const int diag = it.qb * kUnitRows + t * kBM + row + p.causal_off - j * kBN;
                     limit = diag < limit ? diag : limit;
-                }
-                if (__any_sync(0xFFFFFFFFu, limit < kBN - 1)) {
+                    if (__any_sync(0xFFFFFFFFu, limit < kBN - 1)) {
 #pragma unroll
-                    for (int e = 0; e < 128; ++e)
-                        if (e > limit) s[e] = __float_as_uint(-INFINITY);
+                        for (int e = 0; e < 128; ++e)
+                            if (e > limit) s[e] = __float_as_uint(-INFINITY);
+                    }
+                } else {
+                    const int valid = p.Skv - j * kBN;   // the same for every row of the tile
+                    if (valid < kBN) {
+#pragma unroll
+                        for (int e = 0; e < 128; ++e)
+                            if (e >= valid) s[e] = __float_as_uint(-INFINITY);
+                    }
                 }
                 // row max and min: 3-input trees over 4 independent chains each
                 float mxa[4], mna[4];
@@ -814,8 +826,10 @@ int device_info(DeviceInfo** out) {
     }
     if (di.major != 10 || di.minor != 3) return ATTN_ERR_NO_DEVICE;
     if (!di.attr_set) {
-        if (cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+                cudaSuccess)
             return ATTN_ERR_CUDA;
         di.attr_set = true;
     }
@@ -890,7 +904,10 @@ int launch(const attn_args_t& a, const attn_plan_t& pl, const attn_options_t* op
 
     const attn_event_t* ev = opts ? opts->events : nullptr;
     if (ev && ev[0] && cudaEventRecord((cudaEvent_t)ev[0], stream) != cudaSuccess) return ATTN_ERR_CUDA;
-    attn_fwd_kernel<<<(unsigned)pl.grid, kThreads, kSmemAlloc, stream>>>(qm, km, vm, om, p);
+    if (p.causal)
+        attn_fwd_kernel<true><<<(unsigned)pl.grid, kThreads, kSmemAlloc, stream>>>(qm, km, vm, om, p);
+    else
+        attn_fwd_kernel<false><<<(unsigned)pl.grid, kThreads, kSmemAlloc, stream>>>(qm, km, vm, om, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     if (ev && ev[1] && cudaEventRecord((cudaEvent_t)ev[1], stream) != cudaSuccess) return ATTN_ERR_CUDA;
     if (pl.split_units) {
