@@ -214,16 +214,16 @@ def _mp_attention(q, k, v, mode_list, dps=50):
     qd = q.double().numpy()[0, 0]
     kd = k.double().numpy()[0, 0]
     vd = v.double().numpy()[0, 0]
-    Sq, Skv = qd.shape[0], kd.shape[0]
-    inv = 1 / mpmath.sqrt(D)
+    Sq, Skv, d = qd.shape[0], kd.shape[0], qd.shape[1]
+    inv = 1 / mpmath.sqrt(d)
     out = {}
     for i in range(Sq):
         s = [mpmath.fsum(mpmath.mpf(float(qd[i, x])) * mpmath.mpf(float(kd[j, x]))
-                         for x in range(D)) * inv for j in range(Skv)]
+                         for x in range(d)) * inv for j in range(Skv)]
         m = max(s)
         w = [mpmath.exp(sj - m) for sj in s]
         l = mpmath.fsum(w)
-        for x in range(D):
+        for x in range(d):
             val = mpmath.fsum(w[j] * mpmath.mpf(float(vd[j, x])) for j in range(Skv)) / l
             out[(i, x)] = val
     return out
@@ -246,6 +246,30 @@ def pin_brute_force_mpmath(lib):
                 continue
             for m in MODES:
                 assert res[m]["o_bits"][0, 0, i, x] == bx.round_exact(val, m), (seed, i, x, m)
+
+
+def pin_head_dim_64_brute_force_mpmath(lib):
+    """Head dimension 64 (the scale is 1/sqrt(64) = 1/8) against 50-digit arithmetic, and the
+    closed form Q = 0 -> column mean at d = 64 in both layouts."""
+    for seed, (Sq, Skv, sigma) in enumerate(((1, 1, 1.0), (3, 6, 1.0), (2, 5, 3.0))):
+        q, k, v = make_qkv(1, 1, Sq, Skv, 64, "bhsd", seed=300 + seed, sigma=sigma)
+        ref = _mp_attention(q, k, v, MODES)
+        res = {m: oracle.attention(q, k, v, "bhsd", m, want_f64=True, want_a=True, lib=lib)
+               for m in MODES}
+        for (i, x), val in ref.items():
+            assert abs(res["rtne"]["o_f64"][0, 0, i, x] - float(val)) <= \
+                1e-13 * max(res["rtne"]["a"][0, 0, i, x], 1e-300), (seed, i, x)
+            if bx.near_midpoint(val):
+                continue
+            for m in MODES:
+                assert res[m]["o_bits"][0, 0, i, x] == bx.round_exact(val, m), (seed, i, x, m)
+    g = torch.Generator().manual_seed(310)
+    v = torch.randn(2, 9, 3, 64, generator=g).to(torch.bfloat16)          # BSHD, Skv = 9
+    k = torch.randn(2, 9, 3, 64, generator=g).to(torch.bfloat16)
+    q = torch.zeros(2, 4, 3, 64, dtype=torch.bfloat16)
+    o = oracle.attention(q, k, v, "bshd", "rtne", want_f64=True, lib=lib)["o_f64"]
+    mean = v.double().mean(dim=1).numpy()                                 # (B, H, d)
+    assert np.allclose(o, mean[:, :, None, :], rtol=0, atol=1e-15)
 
 
 # --------------------------------------------------------------------------- structure

@@ -18,6 +18,8 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
 
 MUTANTS = {
     "no_scale": ("s[j] = acc * scale;", "s[j] = acc;"),
+    "scale_fixed_at_d128": ("const double scale = 1.0 / sqrt((double)d);",
+                            "const double scale = 1.0 / sqrt(128.0);"),
     "kv_stride_uses_Sq": ("elem_offset(layout, b, j, kvh, 0, Skv, Hkv, d)",
                           "elem_offset(layout, b, j, kvh, 0, Sq, Hkv, d)"),
     "exp_sign": ("exp(s[j] - m)", "exp(m - s[j])"),
