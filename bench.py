@@ -39,9 +39,9 @@ METRIC = "attention fwd TFLOPS (4*B*H*Sq*Skv*d) and % of GB300 bf16 dense peak"
 FALLBACK_PEAK_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 DEFAULT_STEPS = {"square": 1000, "cross": 1000, "video": 60, "stress": 1000, "tiny": 1000,
-                 "causal_gqa": 200}
+                 "causal_gqa": 200, "square_d64": 1000}
 DEFAULT_WARMUP = {"square": 100, "cross": 100, "video": 5, "stress": 100, "tiny": 100,
-                  "causal_gqa": 20}
+                  "causal_gqa": 20, "square_d64": 100}
 L2_BYTES = 126 * 2**20
 
 

@@ -1,7 +1,8 @@
 // attn_fwd.cu -- bf16 attention forward for GB300 (sm_103a): kernels and the C ABI.
 //
-// O = softmax(Q K^T / sqrt(128)) V, non-causal, BSHD or BHSD, any Sq/Skv, output rounded
-// RTNE/RTNA/RTZ.  Source page: "MoonMath AI open-sources a HIP attention kernel for AMD
+// O = softmax(Q K^T / sqrt(d)) V, d = 128 (or 64), BSHD or BHSD, any Sq/Skv, output rounded
+// RTNE/RTNA/RTZ; optionally causal, with grouped K/V heads, and with the row log-sum-exp.
+// Source page: "MoonMath AI open-sources a HIP attention kernel for AMD
 // MI300X that beats AITER" (news.chathome.org), cited below as [MoonMath]:
 //   opening section        -- the operation, layouts, d = 128, arbitrary lengths;
 //   limitations paragraph  -- rounding modes, NaN/Inf bit-identical, determinism;
@@ -16,7 +17,8 @@
 //   * one persistent CTA per SM, static round-robin over work items (deterministic);
 //   * a work unit = one (b, h) and two 128-row query tiles (256 rows), so each K/V tile
 //     feeds two query tiles;
-//   * warp 8 streams Q and a K,V,K,V,... ring (4 x 32 KB stages) with TMA + mbarriers;
+//   * warp 8 streams Q and a K,V,K,V,... ring (128 KB: 4 x 32 KB stages at d = 128, 8 x 16 KB
+//     at d = 64) with TMA + mbarriers;
 //   * warp 9 (one thread) issues tcgen05.mma: S_i = Q_i K_j^T into tensor memory (TMEM) and
 //     O_i += P_i V_j with P_i read from TMEM (it overwrites S_i, so P never goes through
 //     shared memory) and V used as stored (MN-major operand, no transpose);
@@ -27,7 +29,11 @@
 //     softmax running while the tensor core works on the other (the two-groups-out-of-phase
 //     idea on tcgen05);
 //   * tail units that would leave SMs idle in the last round are split along the keys;
-//     each split writes fp32 O/l and a base-2 log-sum-exp, and a combine kernel merges them.
+//     each split writes fp32 O/l and a base-2 log-sum-exp, and a combine kernel merges them;
+//   * the kernel is a template on the head dimension and on the causal mask.  The causal
+//     mask and grouped K/V heads are the features the [MoonMath] limitations paragraph lists
+//     as missing; d = 64 is the second tile configuration of "HipKittens: Fast and Furious
+//     AMD Kernels (MLSys 2026)", "Experiments and results".
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -43,14 +49,11 @@
 
 namespace {
 
-constexpr int kD = 128;            // head dimension
 constexpr int kBM = 128;           // query rows per tile (one TMEM lane per row)
 constexpr int kBN = 128;           // keys per KV tile
 constexpr int kQTiles = 2;         // query tiles per work unit
 constexpr int kUnitRows = kBM * kQTiles;
-constexpr int kStages = 4;         // K/V ring depth (four 32 KB slots: two K/V pairs in flight)
-constexpr int kTileBytes = kBM * kD * 2;       // 32 KB: 128 rows x 128 bf16
-constexpr int kChunkBytes = kTileBytes / 2;    // 16 KB: 128 rows x 64 bf16 (one TMA box)
+constexpr int kChunkBytes = kBM * 64 * 2;     // 16 KB: 128 rows x 64 bf16 (one TMA box)
 constexpr int kThreads = 384;      // WG0, WG1 softmax; warp 8 TMA; warp 9 MMA; 10-11 spare
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
@@ -63,31 +66,40 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= 65536 / kThreads * kT
               "register split exceeds the launch budget");
 constexpr uint32_t kTmemCols = 512;   // S0 | S1 | O0 | O1, 128 fp32 columns each
 
-// shared memory map (offsets from a 1024-byte aligned base)
-constexpr int kSmemQ = 0;
-constexpr int kSmemRing = kSmemQ + kQTiles * kTileBytes;
 // Output staging: one 4 KB region per softmax warp (its 32 rows x 64 bf16 columns in the
-// 128-byte swizzle TMA expects), filled twice per tile (column halves 0 and 1).  Only the
+// 128-byte swizzle TMA expects), filled once per 64 columns of the head dimension.  Only the
 // warp's own TMA stores read it, so the warp's lane 0 waits for its previous store's read
 // before refilling, and nothing else orders it.
 constexpr int kStageRowsPerWarp = 32;
 constexpr int kStageBytes = kStageRowsPerWarp * 64 * 2;
-constexpr int kSmemStage = kSmemRing + kStages * kTileBytes;
-constexpr int kSmemBars = kSmemStage + 8 * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 2 + 3 * kQTiles + 1;
-constexpr int kSmemMisc = kSmemBars + kNumBars * 8;
-constexpr int kSmemUsed = kSmemMisc + 16;
-constexpr int kSmemAlloc = kSmemUsed + 1024;
 
-// barrier indices
-constexpr int kBarFull = 0;                 // [kStages] ring slot loaded
-constexpr int kBarEmpty = kStages;          // [kStages] ring slot released by the MMAs
-constexpr int kBarQFull = 2 * kStages;
-constexpr int kBarQEmpty = kBarQFull + 1;
-constexpr int kBarSFull = kBarQEmpty + 1;   // [2] S_i ready in TMEM
-constexpr int kBarPFull = kBarSFull + 2;    // [2] P_i written (and O_i rescaled)
-constexpr int kBarOFull = kBarPFull + 2;    // [2] last PV of the unit done
-constexpr int kBarDrain = kBarOFull + 2;
+// Head-dimension dependent geometry (D = 128 or 64).  Shared memory offsets are from a
+// 1024-byte aligned base.
+template <int D>
+struct Geo {
+    static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+    static constexpr int kChunks = D / 64;                    // 64-column TMA boxes per row
+    static constexpr int kTileBytes = kBM * D * 2;            // one 128-row tile of Q, K or V
+    static constexpr int kStages = 4 * 128 / D;               // K/V ring: 128 KB in flight
+    static constexpr int kSmemQ = 0;
+    static constexpr int kSmemRing = kSmemQ + kQTiles * kTileBytes;
+    static constexpr int kSmemStage = kSmemRing + kStages * kTileBytes;
+    static constexpr int kSmemBars = kSmemStage + 8 * kStageBytes;
+    // barrier indices
+    static constexpr int kBarFull = 0;                // [kStages] ring slot loaded
+    static constexpr int kBarEmpty = kStages;         // [kStages] ring slot released by the MMAs
+    static constexpr int kBarQFull = 2 * kStages;
+    static constexpr int kBarQEmpty = kBarQFull + 1;
+    static constexpr int kBarSFull = kBarQEmpty + 1;  // [2] S_i ready in TMEM
+    static constexpr int kBarPFull = kBarSFull + 2;   // [2] P_i written (and O_i rescaled)
+    static constexpr int kBarOFull = kBarPFull + 2;   // [2] last PV of the unit done
+    static constexpr int kBarDrain = kBarOFull + 2;
+    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kSmemMisc = kSmemBars + kNumBars * 8;
+    static constexpr int kSmemUsed = kSmemMisc + 16;
+    static constexpr int kSmemAlloc = kSmemUsed + 1024;
+    static_assert(kSmemAlloc <= 232448, "shared memory over the 227 KB limit");
+};
 
 // wait sites reported through the status word
 enum : uint32_t {
@@ -256,35 +268,36 @@ __device__ __forceinline__ float weight_exponent(float s, float c, float m) {
     return fmaf(x, 0x1p-126f, ptx::fmax_nan(x, kMinExponent));
 }
 
-template <bool kCausal>
+template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
                 const FwdParams p) {
+    using G = Geo<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = ptx::smem_u32(smem);
-    const uint32_t bars = sbase + kSmemBars;
+    const uint32_t bars = sbase + G::kSmemBars;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    uint32_t* tmem_holder = (uint32_t*)(smem + kSmemMisc);
-    volatile uint32_t* abort_flag = (volatile uint32_t*)(smem + kSmemMisc + 4);
+    uint32_t* tmem_holder = (uint32_t*)(smem + G::kSmemMisc);
+    volatile uint32_t* abort_flag = (volatile uint32_t*)(smem + G::kSmemMisc + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(bar(kBarFull + s), 1);
-            ptx::mbar_init(bar(kBarEmpty + s), 1);
+        for (int s = 0; s < G::kStages; ++s) {
+            ptx::mbar_init(bar(G::kBarFull + s), 1);
+            ptx::mbar_init(bar(G::kBarEmpty + s), 1);
         }
-        ptx::mbar_init(bar(kBarQFull), 1);
-        ptx::mbar_init(bar(kBarQEmpty), 1);
+        ptx::mbar_init(bar(G::kBarQFull), 1);
+        ptx::mbar_init(bar(G::kBarQEmpty), 1);
         for (int i = 0; i < kQTiles; ++i) {
-            ptx::mbar_init(bar(kBarSFull + i), 1);
-            ptx::mbar_init(bar(kBarPFull + i), kBM);
-            ptx::mbar_init(bar(kBarOFull + i), 1);
+            ptx::mbar_init(bar(G::kBarSFull + i), 1);
+            ptx::mbar_init(bar(G::kBarPFull + i), kBM);
+            ptx::mbar_init(bar(G::kBarOFull + i), 1);
         }
-        ptx::mbar_init(bar(kBarDrain), 1);
+        ptx::mbar_init(bar(G::kBarDrain), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
@@ -311,49 +324,49 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             bool ok = true;
             for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
                 const Item it = decode_item<kCausal>(p, k);
-                if (u > 0 && !(ok = wait_bar(bar(kBarQEmpty), (u - 1) & 1, kSiteQEmpty, abort_flag, lim)))
+                if (u > 0 && !(ok = wait_bar(bar(G::kBarQEmpty), (u - 1) & 1, kSiteQEmpty, abort_flag, lim)))
                     break;
-                ptx::mbar_arrive_expect_tx(bar(kBarQFull), kQTiles * kTileBytes);
+                ptx::mbar_arrive_expect_tx(bar(G::kBarQFull), kQTiles * G::kTileBytes);
                 for (int t = 0; t < kQTiles; ++t) {
                     const int row = it.qb * kUnitRows + t * kBM;
-                    for (int c = 0; c < 2; ++c) {
-                        const uint32_t dst = sbase + kSmemQ + (t * 2 + c) * kChunkBytes;
+                    for (int c = 0; c < G::kChunks; ++c) {
+                        const uint32_t dst = sbase + G::kSmemQ + t * G::kTileBytes + c * kChunkBytes;
                         if (p.bshd)
-                            ptx::tma_load_4d(dst, &qmap, bar(kBarQFull), c * 64, it.h, row, it.b, pol_q);
+                            ptx::tma_load_4d(dst, &qmap, bar(G::kBarQFull), c * 64, it.h, row, it.b, pol_q);
                         else
-                            ptx::tma_load_4d(dst, &qmap, bar(kBarQFull), c * 64, row, it.h, it.b, pol_q);
+                            ptx::tma_load_4d(dst, &qmap, bar(G::kBarQFull), c * 64, row, it.h, it.b, pol_q);
                     }
                 }
                 for (int j = it.kv_begin; j < it.kv_end && ok; ++j) {
                     for (int kv = 0; kv < 2; ++kv, ++pos) {
-                        const uint32_t slot = pos % kStages;
-                        const uint32_t ph = (pos / kStages) & 1u;
-                        if (!(ok = wait_bar(bar(kBarEmpty + slot), ph ^ 1u, kSiteRingEmpty, abort_flag, lim)))
+                        const uint32_t slot = pos % G::kStages;
+                        const uint32_t ph = (pos / G::kStages) & 1u;
+                        if (!(ok = wait_bar(bar(G::kBarEmpty + slot), ph ^ 1u, kSiteRingEmpty, abort_flag, lim)))
                             break;
-                        ptx::mbar_arrive_expect_tx(bar(kBarFull + slot), kTileBytes);
+                        ptx::mbar_arrive_expect_tx(bar(G::kBarFull + slot), G::kTileBytes);
                         const void* map = kv ? (const void*)&vmap : (const void*)&kmap;
-                        for (int c = 0; c < 2; ++c) {
-                            const uint32_t dst = sbase + kSmemRing + slot * kTileBytes + c * kChunkBytes;
+                        for (int c = 0; c < G::kChunks; ++c) {
+                            const uint32_t dst = sbase + G::kSmemRing + slot * G::kTileBytes + c * kChunkBytes;
                             if (p.bshd)
-                                ptx::tma_load_4d(dst, map, bar(kBarFull + slot), c * 64, it.hk, j * kBN, it.b, pol_kv);
+                                ptx::tma_load_4d(dst, map, bar(G::kBarFull + slot), c * 64, it.hk, j * kBN, it.b, pol_kv);
                             else
-                                ptx::tma_load_4d(dst, map, bar(kBarFull + slot), c * 64, j * kBN, it.hk, it.b, pol_kv);
+                                ptx::tma_load_4d(dst, map, bar(G::kBarFull + slot), c * 64, j * kBN, it.hk, it.b, pol_kv);
                         }
                     }
                 }
             }
-            // every load issued has landed before the CTA may exit: the last kStages
+            // every load issued has landed before the CTA may exit: the last G::kStages
             // positions cover each slot's most recent load
-            for (uint32_t q = (pos > kStages ? pos - kStages : 0); q < pos; ++q) {
-                const uint32_t ph = (q / kStages) & 1u;
+            for (uint32_t q = (pos > G::kStages ? pos - G::kStages : 0); q < pos; ++q) {
+                const uint32_t ph = (q / G::kStages) & 1u;
                 const uint64_t t0 = ptx::globaltimer_ns();
-                while (!ptx::mbar_try_wait(bar(kBarFull + q % kStages), ph) && ptx::globaltimer_ns() - t0 < lim) {
+                while (!ptx::mbar_try_wait(bar(G::kBarFull + q % G::kStages), ph) && ptx::globaltimer_ns() - t0 < lim) {
                 }
             }
         } else if (warp == kWarpMma && lane == 0) {
             // -------------------------------------------------------------- MMA issuer
             constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false, false);
-            constexpr uint32_t idesc_o = idesc_bf16(kBM, kD, false, true);
+            constexpr uint32_t idesc_o = idesc_bf16(kBM, D, false, true);
             // TMEM columns: S_t at 128*t, O_t at 256 + 128*t
             // Q_i / K_j: K-major, 128 B rows, 8-row swizzle atoms 1024 B apart; the k-th
             // 16-element step sits 32 B further inside the atom, the second 64-column half
@@ -363,27 +376,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             // Base descriptors; the address field counts 16-byte units, so moving the start
             // address by b bytes adds b >> 4 to the descriptor (no carry out of the field:
             // every address stays below 256 KB).
-            const uint64_t dq0 = sdesc(sbase + kSmemQ, 16, 1024);
-            const uint64_t dring = sdesc(sbase + kSmemRing, 16, 1024);
-            const uint64_t dvring = sdesc(sbase + kSmemRing, kChunkBytes, 1024);
+            const uint64_t dq0 = sdesc(sbase + G::kSmemQ, 16, 1024);
+            const uint64_t dring = sdesc(sbase + G::kSmemRing, 16, 1024);
+            const uint64_t dvring = sdesc(sbase + G::kSmemRing, kChunkBytes, 1024);
             // S_t = Q_t K^T: 8 steps of 16 along d (32 B inside a 64-column half, then the
             // other half 16 KB on).  Fully unrolled with constant offsets from one base
             // descriptor per operand: a rolled loop that recomputes descriptors costs ~200
             // cycles per MMA in issue, three times the 64-cycle MMA itself.
             auto issue_s = [&](int t, uint32_t kslot) {
-                const uint64_t a0 = dq0 + (uint64_t)((t * 2 * kChunkBytes) >> 4);
-                const uint64_t b0 = dring + (uint64_t)((kslot * kTileBytes) >> 4);
+                const uint64_t a0 = dq0 + (uint64_t)((t * G::kTileBytes) >> 4);
+                const uint64_t b0 = dring + (uint64_t)((kslot * G::kTileBytes) >> 4);
                 const uint32_t d = tmem + 128u * t;
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4);
                     ptx::mma_ss(d, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u);
                 }
             };
             // O_t += P_t V: 8 steps of 16 keys (P: 8 TMEM columns each; V: 2 KB each)
             auto issue_o = [&](int t, uint32_t vslot, bool first) {
-                const uint64_t b0 = dvring + (uint64_t)((vslot * kTileBytes) >> 4);
-                const uint32_t d = tmem + 256u + 128u * t, a = tmem + 128u * t;
+                const uint64_t b0 = dvring + (uint64_t)((vslot * G::kTileBytes) >> 4);
+                const uint32_t d = tmem + 256u + (uint32_t)D * t, a = tmem + 128u * t;
                 const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
@@ -397,45 +410,45 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
                 const Item it = decode_item<kCausal>(p, k);
                 const int nk = it.kv_end - it.kv_begin;
-                if (!(ok = wait_bar(bar(kBarQFull), u & 1, kSiteQFull, abort_flag, lim))) break;
-                uint32_t kslot = pos % kStages;
-                if (!(ok = wait_bar(bar(kBarFull + kslot), (pos / kStages) & 1u, kSiteRingFull, abort_flag, lim)))
+                if (!(ok = wait_bar(bar(G::kBarQFull), u & 1, kSiteQFull, abort_flag, lim))) break;
+                uint32_t kslot = pos % G::kStages;
+                if (!(ok = wait_bar(bar(G::kBarFull + kslot), (pos / G::kStages) & 1u, kSiteRingFull, abort_flag, lim)))
                     break;
                 ptx::tc_fence_after();
                 for (int t = 0; t < kQTiles; ++t) {
                     issue_s(t, kslot);
-                    ptx::mma_commit(bar(kBarSFull + t));
+                    ptx::mma_commit(bar(G::kBarSFull + t));
                 }
-                ptx::mma_commit(bar(kBarEmpty + kslot));
-                if (nk == 1) ptx::mma_commit(bar(kBarQEmpty));
+                ptx::mma_commit(bar(G::kBarEmpty + kslot));
+                if (nk == 1) ptx::mma_commit(bar(G::kBarQEmpty));
                 ++pos;
                 for (int jj = 0; jj < nk && ok; ++jj) {
                     const uint32_t vpos = pos;
-                    const uint32_t vslot = vpos % kStages;
+                    const uint32_t vslot = vpos % G::kStages;
                     const bool more = jj + 1 < nk;
-                    if (!(ok = wait_bar(bar(kBarFull + vslot), (vpos / kStages) & 1u, kSiteRingFull, abort_flag, lim)))
+                    if (!(ok = wait_bar(bar(G::kBarFull + vslot), (vpos / G::kStages) & 1u, kSiteRingFull, abort_flag, lim)))
                         break;
                     const uint32_t kpos = vpos + 1;
-                    kslot = kpos % kStages;
+                    kslot = kpos % G::kStages;
                     for (int t = 0; t < kQTiles; ++t) {
-                        if (!(ok = wait_bar(bar(kBarPFull + t), pcount & 1u, kSitePFull, abort_flag, lim)))
+                        if (!(ok = wait_bar(bar(G::kBarPFull + t), pcount & 1u, kSitePFull, abort_flag, lim)))
                             break;
                         ptx::tc_fence_after();
                         issue_o(t, vslot, jj == 0);
-                        if (!more) ptx::mma_commit(bar(kBarOFull + t));
-                        if (t == kQTiles - 1) ptx::mma_commit(bar(kBarEmpty + vslot));
+                        if (!more) ptx::mma_commit(bar(G::kBarOFull + t));
+                        if (t == kQTiles - 1) ptx::mma_commit(bar(G::kBarEmpty + vslot));
                         if (more) {
                             if (t == 0) {
-                                if (!(ok = wait_bar(bar(kBarFull + kslot), (kpos / kStages) & 1u, kSiteRingFull,
+                                if (!(ok = wait_bar(bar(G::kBarFull + kslot), (kpos / G::kStages) & 1u, kSiteRingFull,
                                                     abort_flag, lim)))
                                     break;
                                 ptx::tc_fence_after();
                             }
                             issue_s(t, kslot);
-                            ptx::mma_commit(bar(kBarSFull + t));
+                            ptx::mma_commit(bar(G::kBarSFull + t));
                             if (t == kQTiles - 1) {
-                                ptx::mma_commit(bar(kBarEmpty + kslot));
-                                if (jj + 2 == nk) ptx::mma_commit(bar(kBarQEmpty));
+                                ptx::mma_commit(bar(G::kBarEmpty + kslot));
+                                if (jj + 2 == nk) ptx::mma_commit(bar(G::kBarQEmpty));
                             }
                         }
                     }
@@ -444,9 +457,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 }
             }
             // drain: every MMA this thread issued has finished before TMEM is released
-            ptx::mma_commit(bar(kBarDrain));
+            ptx::mma_commit(bar(G::kBarDrain));
             const uint64_t t0 = ptx::globaltimer_ns();
-            while (!ptx::mbar_try_wait(bar(kBarDrain), 0) && ptx::globaltimer_ns() - t0 < lim) {
+            while (!ptx::mbar_try_wait(bar(G::kBarDrain), 0) && ptx::globaltimer_ns() - t0 < lim) {
             }
         }
     } else {
@@ -457,7 +470,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         const int row = quarter * 32 + lane;        // row within the tile
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_off + (uint32_t)(t * 128);
-        const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(t * 128);
+        const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(t * D);
         const float c = p.scale_log2;
         uint32_t scount = 0;
         int u = 0;
@@ -467,7 +480,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             float m_ref = -INFINITY;      // running max of raw logits at the last rescale
             float l = 0.0f;               // running sum of weights relative to m_ref
             for (int j = it.kv_begin; j < it.kv_end; ++j) {
-                ok = wait_bar(bar(kBarSFull + t), scount & 1u, kSiteSFull, abort_flag, lim);
+                ok = wait_bar(bar(G::kBarSFull + t), scount & 1u, kSiteSFull, abort_flag, lim);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 ++scount;
                 ptx::tc_fence_after();
@@ -559,7 +572,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     const float a = rescale_o ? alpha : 1.0f;
                     const float2 a2 = make_float2(a, a);
 #pragma unroll 1
-                    for (int ch = 0; ch < 4; ++ch) {
+                    for (int ch = 0; ch < D / 32; ++ch) {
                         uint32_t o[32];
                         ptx::tmem_ld32(tO + ch * 32, o);
 #pragma unroll
@@ -573,27 +586,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 }
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(bar(kBarPFull + t));
+                ptx::mbar_arrive(bar(G::kBarPFull + t));
             }
             if (!ok) break;
             // epilogue: O / l, rounding, store
-            ok = wait_bar(bar(kBarOFull + t), u & 1, kSiteOFull, abort_flag, lim);
+            ok = wait_bar(bar(G::kBarOFull + t), u & 1, kSiteOFull, abort_flag, lim);
             if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             ptx::tc_fence_after();
             const int qrow = it.qb * kUnitRows + t * kBM + row;
             const bool valid_row = qrow < p.Sq;
             // the whole O_t row in registers with one TMEM wait
-            uint32_t o[128];
-            ptx::tmem_ld128(tO, o);
+            uint32_t o[D];
+            if constexpr (D == 128) ptx::tmem_ld128(tO, o);
+            else ptx::tmem_ld64(tO, o);
             if (it.split_slot < 0) {
                 const float inv = 1.0f / l;
                 // natural-log log-sum-exp of the scaled logits: (m_ref*c + log2 l) * ln 2
                 if (p.lse && valid_row)
                     p.lse[((long long)it.b * p.H + it.h) * p.Sq + qrow] = (m_ref * c + log2f(l)) * kLn2;
-                const uint32_t region = sbase + kSmemStage + (uint32_t)(warp * kStageBytes);
+                const uint32_t region = sbase + G::kSmemStage + (uint32_t)(warp * kStageBytes);
                 const int r0 = it.qb * kUnitRows + t * kBM + quarter * kStageRowsPerWarp;
 #pragma unroll
-                for (int hc = 0; hc < 2; ++hc) {
+                for (int hc = 0; hc < D / 64; ++hc) {
                     uint32_t w[32];
                     scale_round_pairs<32>(o + 64 * hc, inv, p.round_mode, w);
                     // the region's previous TMA store (if any) has finished reading it
@@ -619,9 +633,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 const float inv = (l > 0.0f) ? 1.0f / l : 1.0f;
                 const long long wrow = (long long)it.split_slot * kUnitRows + t * kBM + row;
                 if (valid_row) {
-                    float4* d4 = reinterpret_cast<float4*>(p.ws_o + wrow * kD);
+                    float4* d4 = reinterpret_cast<float4*>(p.ws_o + wrow * D);
 #pragma unroll
-                    for (int v4 = 0; v4 < 32; ++v4)
+                    for (int v4 = 0; v4 < D / 4; ++v4)
                         d4[v4] = make_float4(__uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
                                              __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
                     p.ws_lse[wrow] = m_ref * c + log2f(l);
@@ -653,10 +667,12 @@ struct CombineParams {
 // One warp per output row of a split unit: merge the nsplit partials with weights
 // 2^(LSE_s - max LSE), accumulating in fixed order s = 0..n-1.  Lanes read the split LSEs in
 // parallel (a row's chain of dependent loads is the combine's cost when nsplit is large); each
-// lane then owns 4 of the 128 columns.  Launched as a programmatic dependent of the attention
+// lane then owns D/32 of the D columns.  Launched as a programmatic dependent of the attention
 // kernel: it starts as that kernel's CTAs retire and waits for its memory before reading.
 // [MoonMath] "Data placement and the 16x16x16 choice" (tail KV split).
+template <int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p) {
+    constexpr int kC = D / 32;   // columns per lane: 4 or 2
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -680,7 +696,9 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
     any_nan = __any_sync(0xFFFFFFFFu, any_nan);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[kC];
+#pragma unroll
+    for (int e = 0; e < kC; ++e) acc[e] = 0.f;
     float wsum = 0.f;
     for (int s0 = 0; s0 < p.nsplit; s0 += 32) {
         const int sl = s0 + lane;
@@ -690,16 +708,23 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p
             w = (e == -INFINITY) ? 0.0f : ptx::ex2_approx(fmaxf(e - mx, -125.0f));
         }
         const int n = min(32, p.nsplit - s0);
-        const float* src = p.ws_o + (base + (long long)s0 * kUnitRows) * kD + lane * 4;
+        const float* src = p.ws_o + (base + (long long)s0 * kUnitRows) * D + lane * kC;
 #pragma unroll 4
         for (int q = 0; q < n; ++q) {
             const float wq = __shfl_sync(0xFFFFFFFFu, w, q);
-            const float4 v = *reinterpret_cast<const float4*>(src + (long long)q * kUnitRows * kD);
+            const float* vq = src + (long long)q * kUnitRows * D;
             wsum += wq;
-            acc[0] += wq * v.x;
-            acc[1] += wq * v.y;
-            acc[2] += wq * v.z;
-            acc[3] += wq * v.w;
+            if constexpr (kC == 4) {
+                const float4 v = *reinterpret_cast<const float4*>(vq);
+                acc[0] += wq * v.x;
+                acc[1] += wq * v.y;
+                acc[2] += wq * v.z;
+                acc[3] += wq * v.w;
+            } else {
+                const float2 v = *reinterpret_cast<const float2*>(vq);
+                acc[0] += wq * v.x;
+                acc[1] += wq * v.y;
+            }
         }
     }
     const bool nan_row = any_nan || mx == -INFINITY;
@@ -707,11 +732,14 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p
     // sum_s 2^LSE_s = 2^mx * wsum (base 2), reported in natural log
     if (p.lse && lane == 0)
         p.lse[((long long)b * p.H + h) * p.Sq + qrow] = any_nan ? NAN : (mx + log2f(wsum)) * kLn2;
-    uint32_t bits[4];
+    uint32_t bits[kC];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) bits[e] = nan_row ? 0x7FC0u : round_bf16_bits(acc[e] * inv, p.round_mode);
+    for (int e = 0; e < kC; ++e) bits[e] = nan_row ? 0x7FC0u : round_bf16_bits(acc[e] * inv, p.round_mode);
     __nv_bfloat16* orow = p.o + (long long)b * p.o_sb + (long long)qrow * p.o_ss + (long long)h * p.o_sh;
-    *reinterpret_cast<uint2*>(orow + lane * 4) = make_uint2(bits[0] | (bits[1] << 16), bits[2] | (bits[3] << 16));
+    if constexpr (kC == 4)
+        *reinterpret_cast<uint2*>(orow + lane * 4) = make_uint2(bits[0] | (bits[1] << 16), bits[2] | (bits[3] << 16));
+    else
+        *reinterpret_cast<uint32_t*>(orow + lane * 2) = bits[0] | (bits[1] << 16);
 }
 
 // ------------------------------------------------------------------------------ host side
@@ -746,7 +774,7 @@ int validate_shape(const attn_args_t& a, const attn_options_t* opts) {
     if (a.layout != ATTN_LAYOUT_BSHD && a.layout != ATTN_LAYOUT_BHSD) return ATTN_ERR_INVALID_ARG;
     if (a.round_mode < ATTN_ROUND_RTNE || a.round_mode > ATTN_ROUND_RTZ) return ATTN_ERR_INVALID_ARG;
     if ((a.causal != 0 && a.causal != 1) || a.reserved != 0) return ATTN_ERR_INVALID_ARG;
-    if (a.d != kD) return ATTN_ERR_UNSUPPORTED;
+    if (a.d != 128 && a.d != 64) return ATTN_ERR_UNSUPPORTED;
     if (a.causal && opts && opts->force_splits > 1) return ATTN_ERR_UNSUPPORTED;
     // TMA coordinates and the kernels' unit/row indices are int32
     const int64_t lim = (int64_t)1 << 30;
@@ -806,7 +834,7 @@ void make_plan(const attn_args_t& a, int64_t sms, const attn_options_t* opts, at
     pl->splits = split_units ? ns : 1;
     pl->items = full + split_units * pl->splits;
     pl->grid = pl->items < G ? pl->items : G;
-    pl->workspace_bytes = split_units ? split_units * pl->splits * kUnitRows * (kD * 4 + 4) : 0;
+    pl->workspace_bytes = split_units ? split_units * pl->splits * kUnitRows * (a.d * 4 + 4) : 0;
 }
 
 int device_info(DeviceInfo** out) {
@@ -826,9 +854,14 @@ int device_info(DeviceInfo** out) {
     }
     if (di.major != 10 || di.minor != 3) return ATTN_ERR_NO_DEVICE;
     if (!di.attr_set) {
-        if (cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+        const int s128 = Geo<128>::kSmemAlloc, s64 = Geo<64>::kSmemAlloc;
+        if (cudaFuncSetAttribute(attn_fwd_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s128) !=
                 cudaSuccess ||
-            cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+            cudaFuncSetAttribute(attn_fwd_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s128) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(attn_fwd_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s64) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(attn_fwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s64) !=
                 cudaSuccess)
             return ATTN_ERR_CUDA;
         di.attr_set = true;
@@ -848,17 +881,18 @@ int device_info(DeviceInfo** out) {
 
 // Tensor map over one bf16 tensor, dims ordered innermost-first so strides increase:
 // BSHD -> (d, H, S, B), BHSD -> (d, S, H, B); box = 64 d x 128 rows, 128-byte swizzle.
-bool encode_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t H, int64_t S, bool bshd, uint32_t rows = kBM) {
+bool encode_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t H, int64_t S, int64_t d, bool bshd,
+                uint32_t rows = kBM) {
     cuuint64_t dims[4], strides[3];
     cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
-    dims[0] = kD;
+    dims[0] = (cuuint64_t)d;
     if (bshd) {
         dims[1] = H; dims[2] = S; dims[3] = B;
-        strides[0] = kD * 2; strides[1] = H * kD * 2; strides[2] = S * H * kD * 2;
+        strides[0] = d * 2; strides[1] = H * d * 2; strides[2] = S * H * d * 2;
         box[0] = 64; box[1] = 1; box[2] = rows; box[3] = 1;
     } else {
         dims[1] = S; dims[2] = H; dims[3] = B;
-        strides[0] = kD * 2; strides[1] = S * kD * 2; strides[2] = H * S * kD * 2;
+        strides[0] = d * 2; strides[1] = S * d * 2; strides[2] = H * S * d * 2;
         box[0] = 64; box[1] = rows; box[2] = 1; box[3] = 1;
     }
     const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
@@ -868,13 +902,13 @@ bool encode_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t H, int64_t S
 }
 
 int launch(const attn_args_t& a, const attn_plan_t& pl, const attn_options_t* opts, void* ws, cudaStream_t stream) {
-    const int64_t B = a.B, H = a.H, Sq = a.Sq, Skv = a.Skv;
+    const int64_t B = a.B, H = a.H, Sq = a.Sq, Skv = a.Skv, d = a.d;
     const int round_mode = a.round_mode;
     void* o = a.o;
     const bool bshd = a.layout == ATTN_LAYOUT_BSHD;
     CUtensorMap qm, km, vm, om;
-    if (!encode_map(&qm, a.q, B, H, Sq, bshd) || !encode_map(&km, a.k, B, a.Hkv, Skv, bshd) ||
-        !encode_map(&vm, a.v, B, a.Hkv, Skv, bshd) || !encode_map(&om, o, B, H, Sq, bshd, kStageRowsPerWarp))
+    if (!encode_map(&qm, a.q, B, H, Sq, d, bshd) || !encode_map(&km, a.k, B, a.Hkv, Skv, d, bshd) ||
+        !encode_map(&vm, a.v, B, a.Hkv, Skv, d, bshd) || !encode_map(&om, o, B, H, Sq, d, bshd, kStageRowsPerWarp))
         return ATTN_ERR_CUDA;
     FwdParams p;
     memset(&p, 0, sizeof p);
@@ -890,24 +924,28 @@ int launch(const attn_args_t& a, const attn_plan_t& pl, const attn_options_t* op
     p.nsplit = (int)pl.splits;
     p.bshd = bshd ? 1 : 0;
     p.round_mode = round_mode;
-    p.scale_log2 = (float)((1.0 / std::sqrt((double)kD)) * 1.4426950408889634);
+    p.scale_log2 = (float)((1.0 / std::sqrt((double)d)) * 1.4426950408889634);
     p.tau = 8.0f;
     p.o = reinterpret_cast<__nv_bfloat16*>(o);
     if (pl.split_units) {
         p.ws_o = reinterpret_cast<float*>(ws);
-        p.ws_lse = p.ws_o + pl.split_units * pl.splits * kUnitRows * kD;
+        p.ws_lse = p.ws_o + pl.split_units * pl.splits * kUnitRows * d;
     }
-    if (bshd) { p.o_sb = Sq * H * kD; p.o_ss = H * kD; p.o_sh = kD; }
-    else { p.o_sb = H * Sq * kD; p.o_ss = kD; p.o_sh = Sq * kD; }
+    if (bshd) { p.o_sb = Sq * H * d; p.o_ss = H * d; p.o_sh = d; }
+    else { p.o_sb = H * Sq * d; p.o_ss = d; p.o_sh = Sq * d; }
     const uint32_t ms = (opts && opts->wait_limit_ms) ? opts->wait_limit_ms : 2000u;
     p.wait_limit_ns = (unsigned long long)ms * 1000000ull;
 
     const attn_event_t* ev = opts ? opts->events : nullptr;
     if (ev && ev[0] && cudaEventRecord((cudaEvent_t)ev[0], stream) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (p.causal)
-        attn_fwd_kernel<true><<<(unsigned)pl.grid, kThreads, kSmemAlloc, stream>>>(qm, km, vm, om, p);
-    else
-        attn_fwd_kernel<false><<<(unsigned)pl.grid, kThreads, kSmemAlloc, stream>>>(qm, km, vm, om, p);
+    const unsigned grid = (unsigned)pl.grid;
+    if (d == 128) {
+        if (p.causal) attn_fwd_kernel<128, true><<<grid, kThreads, Geo<128>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
+        else attn_fwd_kernel<128, false><<<grid, kThreads, Geo<128>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
+    } else {
+        if (p.causal) attn_fwd_kernel<64, true><<<grid, kThreads, Geo<64>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
+        else attn_fwd_kernel<64, false><<<grid, kThreads, Geo<64>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
+    }
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     if (ev && ev[1] && cudaEventRecord((cudaEvent_t)ev[1], stream) != cudaSuccess) return ATTN_ERR_CUDA;
     if (pl.split_units) {
@@ -931,7 +969,9 @@ int launch(const attn_args_t& a, const attn_plan_t& pl, const attn_options_t* op
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, attn_combine_kernel, c) != cudaSuccess) {
+        const cudaError_t ce = d == 128 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<128>, c)
+                                        : cudaLaunchKernelEx(&cfg, attn_combine_kernel<64>, c);
+        if (ce != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_CUDA;
         }
@@ -1101,7 +1141,7 @@ const char* attn_status_string(int status) {
     switch (status) {
         case ATTN_OK: return "ok";
         case ATTN_ERR_INVALID_ARG: return "invalid argument";
-        case ATTN_ERR_UNSUPPORTED: return "unsupported shape (d must be 128; sizes within int32 indexing)";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported shape (d must be 64 or 128; sizes within int32 indexing)";
         case ATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
         case ATTN_ERR_ALIAS: return "output overlaps an input";
         case ATTN_ERR_NO_DEVICE: return "no sm_103 CUDA device current";

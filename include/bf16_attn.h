@@ -1,8 +1,8 @@
 /*
  * bf16_attn.h -- C ABI of the GB300 (sm_103a) bf16 attention forward library.
  *
- * Operation.  O = softmax(Q K^T / sqrt(d)) V, non-causal, head dimension d = 128, bf16 in
- * and out, fp32 accumulation.  Source: "MoonMath AI open-sources a HIP attention kernel for
+ * Operation.  O = softmax(Q K^T / sqrt(d)) V, non-causal, head dimension d = 128 (64 is
+ * accepted too), bf16 in and out, fp32 accumulation.  Source: "MoonMath AI open-sources a HIP attention kernel for
  * AMD MI300X that beats AITER" (news.chathome.org), opening section: attention is the fused
  * softmax(QK^T/sqrt(d))V; the kernel takes BSHD or BHSD tensors without transposes, head
  * dimension fixed at 128, any query and key length including cross-attention; its
@@ -10,6 +10,8 @@
  * bit-identically, deterministic results; section "Real use cases": a simple API that
  * launches on the caller's stream.  The long-KV split and its log-sum-exp combine follow the
  * section "Data placement and the 16x16x16 choice" (Flash-Decoding-style tail KV split).
+ * Head dimension 64 is the second tile configuration of "HipKittens: Fast and Furious AMD
+ * Kernels (MLSys 2026)", "Experiments and results" (attention forward at d = 64 and 128).
  *
  * Layouts.  All four tensors share one layout and are dense (contiguous):
  *   ATTN_LAYOUT_BSHD: element (b, s, h, x) at ((b*S + s)*H + h)*d + x
@@ -55,7 +57,7 @@ typedef enum { ATTN_ROUND_RTNE = 0, ATTN_ROUND_RTNA = 1, ATTN_ROUND_RTZ = 2 } at
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,    /* null pointer, a size < 1, a bad enum value            */
-    ATTN_ERR_UNSUPPORTED = 2,    /* d != 128, or a size beyond the kernels' int32 indexing */
+    ATTN_ERR_UNSUPPORTED = 2,    /* d not 64 or 128, or a size beyond the kernels' int32 indexing */
     ATTN_ERR_MISALIGNED = 3,     /* a tensor or workspace base not 16-byte aligned         */
     ATTN_ERR_ALIAS = 4,          /* o overlaps q, k or v                                   */
     ATTN_ERR_NO_DEVICE = 5,      /* no CUDA device, or the current device is not sm_103    */
@@ -129,7 +131,7 @@ typedef struct {
  *   q           device pointer, bf16, [B, Sq, H, d] (BSHD) or [B, H, Sq, d] (BHSD)
  *   k, v        device pointers, bf16, same layout with Skv rows
  *   o           device pointer, bf16, same shape as q; must not overlap q, k or v
- *   B, H        batch and heads (>= 1);  Sq, Skv  query and key lengths (>= 1);  d = 128
+ *   B, H        batch and heads (>= 1);  Sq, Skv  query and key lengths (>= 1);  d = 128 or 64
  *   layout      attn_layout_t;  round_mode  attn_round_t
  *   stream      cudaStream_t (NULL = legacy default stream)
  * Uses the library-owned workspace when the planner splits keys (see Ownership above).

@@ -55,7 +55,8 @@ def test_argument_errors(lib):
     for kw in ({"B": 0}, {"H": -1}, {"Sq": 0}, {"Skv": 0}, {"layout": 2}, {"mode": 3},
                {"mode": -1}):
         assert call(lib, **kw) == 1, kw
-    assert call(lib, d=64) == 2
+    assert call(lib, d=32) == 2
+    assert call(lib, d=256) == 2
     assert call(lib, Sq=(1 << 30) + 1) == 2
     assert call(lib, q=P + 8) == 3
     assert call(lib, o=P + 2) == 3
@@ -67,12 +68,13 @@ def test_argument_errors(lib):
 def test_ws_entry_validates_too(lib):
     f = lib.attn_fwd_ws
     assert f(0, P, P, P, 1, 1, 8, 8, 128, 0, 0, None, None, 0, None) == 1
-    assert f(P, 2 * P, 3 * P, 4 * P, 1, 1, 8, 8, 64, 0, 0, None, None, 0, None) == 2
+    assert f(P, 2 * P, 3 * P, 4 * P, 1, 1, 8, 8, 96, 0, 0, None, None, 0, None) == 2
 
 
 @pytest.mark.skipif(not NO_GPU, reason="valid arguments would launch on a real GPU")
 def test_valid_args_without_gpu_report_no_device(lib):
     assert call(lib) == 5
+    assert call(lib, d=64) == 5
     assert lib.attn_fwd_workspace_size(1, 1, 8, 8, 128) == 0
 
 
@@ -111,7 +113,7 @@ def test_planner_forced_options(lib):
     p = attn.plan(4, 16, 2048, 2048, 128, 152, max_ctas=5)
     assert p["grid"] == 5
     with pytest.raises(attn.AttnError):
-        attn.plan(1, 1, 1, 1, 64)
+        attn.plan(1, 1, 1, 1, 32)
 
 
 def ex_args(q=P, k=2 * P, v=3 * P, o=4 * P, lse=0, B=1, H=2, Hkv=2, Sq=8, Skv=8, d=128, layout=0,
@@ -134,7 +136,7 @@ def test_ex_argument_errors(lib):
     for kw in ({"Hkv": 0}, {"Hkv": 3, "H": 4}, {"Hkv": 4, "H": 2}, {"causal": 2},
                {"causal": -1}, {"reserved": 1}, {"layout": 5}, {"mode": 7}):
         assert call_ex(lib, **kw) == 1, kw
-    assert call_ex(lib, d=64) == 2
+    assert call_ex(lib, d=48) == 2
     # causal with a forced key split is refused: the causal planner never splits
     assert call_ex(lib, causal=1, opts=attn.Options(3, 0, 0, 0)) == 2
     assert call_ex(lib, lse=5 * P + 2) == 3
@@ -168,3 +170,13 @@ def test_planner_ex_matches_plain_and_causal_never_splits(lib, shape):
     assert 1 <= p["grid"] <= min(152, p["units"])
     with pytest.raises(attn.AttnError):
         attn.plan_ex(B, H, Sq, Skv, causal=True, force_splits=2)
+
+
+@pytest.mark.parametrize("shape", PLAN_SHAPES)
+def test_planner_head_dim_64(lib, shape):
+    B, H, Sq, Skv = shape
+    p128, p64 = attn.plan(B, H, Sq, Skv, 128), attn.plan(B, H, Sq, Skv, 64)
+    # the work split does not depend on d; the split partials are d fp32 + 1 LSE per row
+    assert {k: v for k, v in p64.items() if k != "workspace_bytes"} == \
+           {k: v for k, v in p128.items() if k != "workspace_bytes"}
+    assert p64["workspace_bytes"] == p64["split_units"] * p64["splits"] * 256 * (64 * 4 + 4)

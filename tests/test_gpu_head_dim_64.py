@@ -1,0 +1,94 @@
+"""GPU parity at head dimension 64 (the second tile configuration) against the fp64 oracle.
+
+Same criteria as at d = 128: ordinal bf16 distance <= 2 or the forward-error bound, bitwise
+equal non-finite outputs, LSE within the derived tolerance, and the exact-mean cases bit-exact
+in all three rounding modes.  Shapes span several query and key tiles with ragged tails, both
+layouts, the key split, the causal mask and grouped K/V heads.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import parity
+from tests.test_gpu_causal_gqa import check_ex, run_ex
+from tests.test_gpu_parity import _mean_of_values_case
+from workloads import WORKLOADS, make_qkv, make_workload, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+MODES = ("rtne", "rtna", "rtz")
+D = 64
+
+
+@pytest.fixture(scope="module")
+def attn():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import bf16_attention_forward_gb300 as a
+    a.load()
+    return a
+
+
+SMALL = [  # (B, H, Sq, Skv)
+    (1, 1, 1, 1), (1, 2, 128, 128), (1, 1, 127, 129), (2, 3, 257, 385), (1, 1, 700, 900),
+    (1, 2, 1, 1000),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "B%dH%dSq%dSkv%d" % s)
+@pytest.mark.parametrize("layout", ["bshd", "bhsd"])
+def test_small_shapes_all_modes(attn, shape, layout):
+    B, H, Sq, Skv = shape
+    q, k, v = make_qkv(B, H, Sq, Skv, D, layout, seed=3000 + sum(shape))
+    for mode in MODES:
+        check_ex(attn, q, k, v, layout, mode)
+
+
+@pytest.mark.parametrize("splits", [2, 5])
+def test_split_path(attn, splits):
+    q, k, v = make_qkv(1, 3, 300, 1500, D, "bhsd", seed=3100 + splits, sigma=2.0)
+    check_ex(attn, q, k, v, "bhsd", "rtna", force_splits=splits)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_heads_and_causal(attn, causal):
+    for layout in ("bshd", "bhsd"):
+        q, k, v = make_qkv(1, 8, 333, 517, D, layout, seed=3200, Hkv=2)
+        check_ex(attn, q, k, v, layout, "rtne", causal=causal)
+    q, k, v = make_qkv(2, 4, 600, 600, D, "bshd", seed=3201, Hkv=1)
+    check_ex(attn, q, k, v, "bshd", "rtz", causal=causal)
+
+
+def test_single_key_returns_v_and_layouts_agree(attn):
+    q, k, v = make_qkv(2, 3, 200, 1, D, "bhsd", seed=3300, sigma=3.0)
+    for mode in MODES:
+        o, _ = run_ex(attn, q, k, v, "bhsd", mode)
+        assert torch.equal(o.cpu().view(torch.int16),
+                           v.expand(2, 3, 200, D).contiguous().view(torch.int16))
+    q, k, v = make_qkv(2, 3, 333, 444, D, "bshd", seed=3301)
+    t = lambda x: x.permute(0, 2, 1, 3).contiguous()
+    a, _ = run_ex(attn, q, k, v, "bshd", "rtne")
+    b, _ = run_ex(attn, t(q), t(k), t(v), "bhsd", "rtne")
+    a2, _ = run_ex(attn, q, k, v, "bshd", "rtne")
+    assert torch.equal(t(a).view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a.view(torch.int16), a2.view(torch.int16))
+
+
+@pytest.mark.parametrize("Skv", [2, 64])
+def test_rounding_modes_bit_exact_on_exact_means(attn, Skv):
+    q, k, v = _mean_of_values_case(Skv, -3, 3, seed=3400 + Skv)
+    q, k, v = (x[..., :D].contiguous() for x in (q, k, v))
+    for mode in MODES:
+        o, _ = run_ex(attn, q, k, v, "bhsd", mode)
+        ref = oracle.attention(q, k, v, "bhsd", mode)
+        g = parity.gpu_rows_bits(o, "bhsd").reshape(ref["o_bits"].shape)
+        assert np.array_equal(g, ref["o_bits"]), (mode, int((g != ref["o_bits"]).sum()))
+
+
+def test_workload_sampled_rows(attn):
+    w = WORKLOADS["square_d64"]
+    q, k, v = make_workload(w)
+    rows = sample_rows(w.B, w.H, w.Sq, 512, seed=w.seed)
+    for mode in w.modes:
+        check_ex(attn, q, k, v, w.layout, mode, rows=rows)

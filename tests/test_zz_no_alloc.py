@@ -90,6 +90,6 @@ def test_noalloc_rejects_bad_arguments(lib):
     assert lib.attn_fwd_noalloc(None, k.data_ptr(), v.data_ptr(), o.data_ptr(), 1, 1, 8, 8, 128,
                                 1, 0, stream) == 1
     assert lib.attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), 1, 1, 8,
-                                8, 64, 1, 0, stream) == 2
+                                8, 96, 1, 0, stream) == 2
     assert lib.attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), q.data_ptr(), 1, 1, 8,
                                 8, 128, 1, 0, stream) == 4

@@ -3,11 +3,12 @@
 Both the oracle side and the CUDA side draw their inputs from this module and nothing
 else; it holds no step of the method.  Shapes and value distributions follow the pages'
 workloads: i.i.d. N(0, sigma^2) entries drawn in fp32 then rounded to bf16 (RTNE), in the
-BSHD (B, S, H, d) or BHSD (B, H, S, d) layout, d = 128.  The named workloads are a tiny
-self-attention, a square self-attention, a diffusion-style cross-attention with a KV length
-that is not a tile multiple, a video-diffusion self-attention (1536 hidden = 12 heads x 128),
-a long-KV stress case with large logits and sparse non-finite entries, and a decoder-style
-causal prefill whose K and V carry a quarter of the query heads.
+BSHD (B, S, H, d) or BHSD (B, H, S, d) layout, d = 128 (64 for one workload).  The named
+workloads are a tiny self-attention, a square self-attention, a diffusion-style
+cross-attention with a KV length that is not a tile multiple, a video-diffusion
+self-attention (1536 hidden = 12 heads x 128), a long-KV stress case with large logits and
+sparse non-finite entries, a decoder-style causal prefill whose K and V carry a quarter of
+the query heads, and the square case at head dimension 64.
 """
 from __future__ import annotations
 
@@ -75,6 +76,8 @@ WORKLOADS = {
     # decoder-style prefill: causal mask with 4 query heads per K/V head
     "causal_gqa": Workload("causal_gqa", 2, 32, 8192, 8192, 128, "bshd", ("rtne",), seed=5,
                            Hkv=8, causal=True),
+    # head dimension 64: the square self-attention's hidden size 2048 as 32 heads x 64
+    "square_d64": Workload("square_d64", 4, 32, 2048, 2048, 64, "bhsd", ("rtne",), seed=6),
 }
 
 
