@@ -2,8 +2,9 @@
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference leg of
 ``bench.py`` may import this package.  The product library never loads it and shares no
-code with it.  The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over rows);
-this module compiles it with gcc and marshals numpy arrays through ``ctypes``.
+code with it.  The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over rows)
+and, for the backward, ``attn_oracle_bwd.c``; this module compiles them with gcc and
+marshals numpy arrays through ``ctypes``.
 
 What it computes is stated in the C file's header: softmax(Q K^T / sqrt(d)) V per row, in
 fp64, two passes, rounded once to bf16 in the requested mode, following the page
@@ -21,6 +22,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
+_SRC_BWD = os.path.join(_HERE, "attn_oracle_bwd.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libattn_oracle.so")
 
@@ -31,14 +33,18 @@ _lock = threading.Lock()
 _lib = None
 
 
-def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
-    """Compile the oracle into a shared object (gcc, -O2, OpenMP, no fast-math)."""
-    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH,
+          bwd_src: str = _SRC_BWD) -> str:
+    """Compile the oracle (``src``, the forward, and ``bwd_src``, the backward) into a shared
+    object (gcc, -O2, OpenMP, no fast-math)."""
+    srcs = [src, bwd_src]
+    if not force and os.path.exists(out) and \
+            all(os.path.getmtime(out) >= os.path.getmtime(f) for f in srcs):
         return out
     os.makedirs(os.path.dirname(out), exist_ok=True)
     tmp = out + ".tmp%d" % os.getpid()
     cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-fno-fast-math",
-           src, "-o", tmp, "-lm"]
+           *srcs, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -60,6 +66,12 @@ def _bind(lib):
     lib.oracle_round_bf16_array.argtypes = [f64p, ctypes.c_int64, ctypes.c_int, u16p]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
+    lib.attn_oracle_f64_forward.restype = ctypes.c_int
+    lib.attn_oracle_f64_forward.argtypes = [f64p, f64p, f64p] + [ctypes.c_int64] * 6 + [
+        ctypes.c_int, ctypes.c_int, f64p]
+    lib.attn_oracle_bwd.restype = ctypes.c_int
+    lib.attn_oracle_bwd.argtypes = [u16p, u16p, u16p, u16p] + [ctypes.c_int64] * 6 + [
+        ctypes.c_int, ctypes.c_int] + [f64p] * 7 + [ctypes.c_int]
     return lib
 
 
@@ -172,3 +184,54 @@ def round_bf16(x, mode: str = "rtne", lib=None) -> np.ndarray:
 def max_threads(lib=None) -> int:
     lib = lib or load()
     return int(lib.oracle_max_threads())
+
+
+def forward_f64(q, k, v, layout: str = "bshd", causal: bool = False, lib=None) -> np.ndarray:
+    """softmax(Q K^T / sqrt(d)) V on float64 arrays (no rounding): the function whose
+    derivative :func:`backward` computes.  Shapes as for :func:`attention`."""
+    lib = lib or load()
+    qa, ka, va = (np.ascontiguousarray(np.asarray(t, dtype=np.float64)) for t in (q, k, v))
+    B, H, Sq, Skv, d = dims(qa.shape, ka.shape, layout)
+    o = np.empty_like(qa)
+    rc = lib.attn_oracle_f64_forward(_ptr(qa, ctypes.c_double), _ptr(ka, ctypes.c_double),
+                                     _ptr(va, ctypes.c_double), B, H, kv_heads(ka.shape, layout),
+                                     Sq, Skv, d, LAYOUTS[layout], 1 if causal else 0,
+                                     _ptr(o, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments (rc=%d)" % rc)
+    return o
+
+
+def backward(q, k, v, dout, layout: str = "bshd", causal: bool = False, want_a: bool = False,
+             want_delta: bool = False, threads: int | None = None, lib=None) -> dict:
+    """fp64 gradients of softmax(Q K^T / sqrt(d)) V for bf16 q, k, v and upstream gradient
+    dout (shaped like q).  Returns ``dq``, ``dk``, ``dv`` (float64, in the input layouts),
+    their ``*_bits`` (bf16, RTNE), optionally forward-error scales ``dq_a``, ``dk_a``,
+    ``dv_a`` and ``delta`` (D_i = dO_i . O_i, [B][H][Sq])."""
+    lib = lib or load()
+    qb, kb, vb, gb = _as_bits(q), _as_bits(k), _as_bits(v), _as_bits(dout)
+    B, H, Sq, Skv, d = dims(qb.shape, kb.shape, layout)
+    Hkv = kv_heads(kb.shape, layout)
+    dq = np.empty(qb.shape, dtype=np.float64)
+    dk = np.empty(kb.shape, dtype=np.float64)
+    dv = np.empty(kb.shape, dtype=np.float64)
+    dq_a = np.empty_like(dq) if want_a else None
+    dk_a = np.empty_like(dk) if want_a else None
+    dv_a = np.empty_like(dv) if want_a else None
+    delta = np.empty((B, H, Sq), dtype=np.float64) if want_delta else None
+    rc = lib.attn_oracle_bwd(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                             _ptr(vb, ctypes.c_uint16), _ptr(gb, ctypes.c_uint16), B, H, Hkv,
+                             Sq, Skv, d, LAYOUTS[layout], 1 if causal else 0,
+                             *(_ptr(a, ctypes.c_double) for a in (dq, dk, dv, dq_a, dk_a, dv_a,
+                                                                   delta)),
+                             int(threads or 0))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments (rc=%d)" % rc)
+    out = {"dq": dq, "dk": dk, "dv": dv}
+    for key in ("dq", "dk", "dv"):
+        out[key + "_bits"] = round_bf16(out[key], "rtne", lib=lib)
+    if want_a:
+        out.update(dq_a=dq_a, dk_a=dk_a, dv_a=dv_a)
+    if want_delta:
+        out["delta"] = delta
+    return out

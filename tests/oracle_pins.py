@@ -516,4 +516,77 @@ def pin_brute_force_causal_lse_mpmath(lib):
                     assert res["o_bits"][0, h, i, x] == bx.round_exact(val, "rtne")
 
 
+# --------------------------------------------------------------------------- backward
+def _fd_gradients(q, k, v, g, layout, causal, lib, h=1e-6):
+    """Central differences of L = sum(dO * O) through the fp64 forward, for every element of
+    q, k and v (tiny shapes only)."""
+    base = [np.ascontiguousarray(t.double().numpy()) for t in (q, k, v)]
+    gd = g.double().numpy()
+    out = []
+    for which in range(3):
+        grad = np.empty_like(base[which])
+        flat = grad.reshape(-1)
+        for idx in range(flat.size):
+            vals = []
+            for sgn in (1.0, -1.0):
+                ts = [b.copy() for b in base]
+                ts[which].reshape(-1)[idx] += sgn * h
+                o = oracle.forward_f64(*ts, layout=layout, causal=causal, lib=lib)
+                vals.append(float((o * gd).sum()))
+            flat[idx] = (vals[0] - vals[1]) / (2 * h)
+        out.append(grad)
+    return out
+
+
+def pin_bwd_matches_finite_differences(lib):
+    """dQ, dK, dV equal the numerical derivative of sum(dO * O) through the fp64 forward, with
+    and without the causal mask and with grouped K/V heads (2 query heads per K/V head)."""
+    g0 = torch.Generator().manual_seed(400)
+    for causal, (Sq, Skv), layout in ((False, (3, 5), "bshd"), (True, (4, 4), "bhsd"),
+                                      (True, (2, 5), "bshd")):
+        shp_q = shape(layout, 1, 2, Sq, 16)
+        shp_k = shape(layout, 1, 1, Skv, 16)
+        q = torch.randn(shp_q, generator=g0).to(torch.bfloat16)
+        k = torch.randn(shp_k, generator=g0).to(torch.bfloat16)
+        v = torch.randn(shp_k, generator=g0).to(torch.bfloat16)
+        g = torch.randn(shp_q, generator=g0).to(torch.bfloat16)
+        res = oracle.backward(q, k, v, g, layout, causal=causal, lib=lib)
+        fd = _fd_gradients(q, k, v, g, layout, causal, lib)
+        for name, num in zip(("dq", "dk", "dv"), fd):
+            err = np.abs(res[name] - num)
+            assert np.all(err <= 1e-7 * (1 + np.abs(num))), (causal, name, float(err.max()))
+
+
+def pin_bwd_forward_f64_equals_forward(lib):
+    """The fp64-input forward used for the derivative equals the bf16 oracle's unrounded
+    output on bf16-representable inputs."""
+    q, k, v = make_qkv(2, 4, 9, 13, 32, "bshd", seed=410, Hkv=2)
+    for causal in (False, True):
+        o64 = oracle.forward_f64(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                                 "bshd", causal=causal, lib=lib)
+        ref = oracle.attention(q, k, v, "bshd", "rtne", want_f64=True, causal=causal,
+                               lib=lib)["o_f64"]                    # (B, H, Sq, d)
+        assert np.allclose(o64.transpose(0, 2, 1, 3), ref, rtol=1e-14, atol=1e-15)
+
+
+def pin_bwd_single_key_and_delta(lib):
+    """One key: every weight is 1, so dS = 0 (dQ = dK = 0) and dV is the sum of dO over the
+    rows and query heads that read it; D_i equals dO_i . O_i from the forward."""
+    g0 = torch.Generator().manual_seed(420)
+    q = torch.randn(1, 4, 6, 32, generator=g0).to(torch.bfloat16)
+    k = torch.randn(1, 2, 1, 32, generator=g0).to(torch.bfloat16)
+    v = torch.randn(1, 2, 1, 32, generator=g0).to(torch.bfloat16)
+    g = torch.randn(1, 4, 6, 32, generator=g0).to(torch.bfloat16)
+    res = oracle.backward(q, k, v, g, "bhsd", want_delta=True, lib=lib)
+    assert np.all(res["dq"] == 0) and np.all(res["dk"] == 0)
+    gd = g.double().numpy()
+    want = np.stack([gd[0, 0:2].sum(axis=(0, 1)), gd[0, 2:4].sum(axis=(0, 1))])[None, :, None, :]
+    assert np.allclose(res["dv"], want, rtol=1e-14, atol=1e-13)
+    q, k, v = make_qkv(1, 2, 7, 11, 32, "bhsd", seed=421)
+    g = torch.randn(1, 2, 7, 32, generator=g0).to(torch.bfloat16)
+    res = oracle.backward(q, k, v, g, "bhsd", want_delta=True, lib=lib)
+    o = oracle.attention(q, k, v, "bhsd", "rtne", want_f64=True, lib=lib)["o_f64"]
+    assert np.allclose(res["delta"], (g.double().numpy() * o).sum(axis=-1), rtol=1e-13, atol=1e-14)
+
+
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

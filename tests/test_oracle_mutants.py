@@ -15,6 +15,7 @@ import oracle
 from tests import oracle_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
+SRC_BWD = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle_bwd.c")
 
 MUTANTS = {
     "no_scale": ("s[j] = acc * scale;", "s[j] = acc;"),
@@ -42,6 +43,15 @@ MUTANTS = {
                              "if (isnan(s[j])) any_nan_or_posinf = 1;"),
 }
 
+# planted mistakes in the backward source
+MUTANTS_BWD = {
+    "bwd_ds_drops_delta": ("const double ds = p[j] * (dp[j] - Di);", "const double ds = p[j] * dp[j];"),
+    "bwd_dk_unscaled": ("dk[off] += c * ds * qi[x];", "dk[off] += ds * qi[x];"),
+    "bwd_dv_uses_ds": ("dv[off] += p[j] * gi[x];", "dv[off] += (p[j] - Di * 0.0 + dp[j] * p[j]) * gi[x];"),
+    "bwd_dq_sign": ("acc += p[j] * (dp[j] - Di) * kjx;", "acc += p[j] * (Di - dp[j]) * kjx;"),
+    "bwd_causal_sees_all": ("if (!causal) return Skv;", "return Skv;"),
+}
+
 
 @pytest.fixture(scope="module")
 def workdir():
@@ -50,16 +60,20 @@ def workdir():
     shutil.rmtree(d, ignore_errors=True)
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
+@pytest.mark.parametrize("name", sorted(MUTANTS) + sorted(MUTANTS_BWD))
 def test_mutant_is_caught(name, workdir):
-    old, new = MUTANTS[name]
-    text = open(SRC).read()
+    bwd = name in MUTANTS_BWD
+    old, new = (MUTANTS_BWD if bwd else MUTANTS)[name]
+    text = open(SRC_BWD if bwd else SRC).read()
     assert text.count(old) >= 1, "mutation site vanished: %s" % name
     src = os.path.join(workdir, name + ".c")
     with open(src, "w") as f:
         f.write(text.replace(old, new))
     so = os.path.join(workdir, "lib%s.so" % name)
-    oracle.build(force=True, src=src, out=so)
+    if bwd:
+        oracle.build(force=True, out=so, bwd_src=src)
+    else:
+        oracle.build(force=True, src=src, out=so)
     lib = oracle.load(so)
     failed = []
     for pin in oracle_pins.ALL_PINS:
