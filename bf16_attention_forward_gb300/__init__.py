@@ -20,7 +20,8 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_CUDA", 8: "ATTN_ERR_DEVICE_TIMEOUT"}
 EXPORTS = ("attn_fwd", "attn_fwd_ws", "attn_fwd_noalloc", "attn_fwd_ex", "attn_fwd_workspace_size",
            "attn_fwd_workspace_size_opts", "attn_fwd_ex_workspace_size", "attn_plan",
-           "attn_plan_ex", "attn_get_device_status", "attn_status_string", "attn_version")
+           "attn_plan_ex", "attn_get_device_status", "attn_status_string", "attn_version",
+           "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_get_device_status")
 
 
 class AttnError(RuntimeError):
@@ -42,6 +43,13 @@ class Args(ctypes.Structure):
                 ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p)] + \
                [(n, ctypes.c_int64) for n in ("B", "H", "Hkv", "Sq", "Skv", "d")] + \
                [(n, ctypes.c_int32) for n in ("layout", "round_mode", "causal", "reserved")]
+
+
+class BwdArgs(ctypes.Structure):
+    """attn_bwd_args_t: the argument set of attn_bwd."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv")] + \
+               [(n, ctypes.c_int64) for n in ("B", "H", "Hkv", "Sq", "Skv", "d")] + \
+               [(n, ctypes.c_int32) for n in ("layout", "causal", "reserved0", "reserved1")]
 
 
 class Plan(ctypes.Structure):
@@ -91,6 +99,12 @@ def load(path: str | None = None):
         lib.attn_plan_ex.restype = i32
         lib.attn_plan_ex.argtypes = [ctypes.POINTER(Args), i64, ctypes.POINTER(Options),
                                      ctypes.POINTER(Plan)]
+        lib.attn_bwd.restype = i32
+        lib.attn_bwd.argtypes = [ctypes.POINTER(BwdArgs), vp, ctypes.c_size_t, vp]
+        lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.attn_bwd_workspace_size.argtypes = [ctypes.POINTER(BwdArgs)]
+        lib.attn_bwd_get_device_status.restype = i32
+        lib.attn_bwd_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         lib.attn_plan.restype = i32
         lib.attn_plan.argtypes = [i64] * 6 + [ctypes.POINTER(Options), ctypes.POINTER(Plan)]
         lib.attn_get_device_status.restype = i32
@@ -290,4 +304,51 @@ def device_status(stream=None) -> tuple:
     s = stream if stream is not None else torch.cuda.current_stream()
     site = ctypes.c_int32(0)
     st = load().attn_get_device_status(ctypes.c_void_p(s.cuda_stream), ctypes.byref(site))
+    return int(st), int(site.value)
+
+
+def attn_bwd(q, k, v, o, dout, lse, layout: str = "bshd", causal: bool = False, dq=None, dk=None,
+             dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of softmax(Q K^T / sqrt(d)) V for the upstream gradient ``dout``,
+    from the forward's inputs, output ``o`` and fp32 row log-sum-exp ``lse`` ([B][H][Sq], as
+    returned by :func:`attn_fwd_ex` with ``return_lse``).  d = 128.  Returns (dq, dk, dv)."""
+    import torch
+    if layout not in LAYOUTS:
+        raise ValueError("layout must be bshd or bhsd")
+    _check_tensors(q, k, v)
+    _check_tensors(o, dout, dout)
+    B, H, Hkv, Sq, Skv, d = _dims(q, k, v, layout, grouped=True)
+    for t in (o, dout):
+        if tuple(t.shape) != tuple(q.shape):
+            raise ValueError("o and dout must be shaped like q")
+    if (lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous()
+            or lse.numel() != B * H * Sq):
+        raise ValueError("lse must be a contiguous CUDA fp32 tensor of B*H*Sq elements")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for g, ref in ((dq, q), (dk, k), (dv, v)):
+        _check_out(g, ref)
+    a = BwdArgs()
+    a.q, a.k, a.v, a.o, a.dout = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr()
+    a.lse, a.dq, a.dk, a.dv = lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d = B, H, Hkv, Sq, Skv, d
+    a.layout, a.causal, a.reserved0, a.reserved1 = LAYOUTS[layout], int(causal), 0, 0
+    lib = load()
+    need = int(lib.attn_bwd_workspace_size(ctypes.byref(a)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib.attn_bwd(ctypes.byref(a), workspace.data_ptr(), nbytes, _stream_ptr(stream, q.device))
+    if st != 0:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def bwd_device_status(stream=None) -> tuple:
+    """Synchronize and read/clear the backward kernel's status word: (status, wait site)."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    site = ctypes.c_int32(0)
+    st = load().attn_bwd_get_device_status(ctypes.c_void_p(s.cuda_stream), ctypes.byref(site))
     return int(st), int(site.value)

@@ -7,7 +7,7 @@ import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = [os.path.join(CSRC, "attn_fwd.cu")]
+SOURCES = [os.path.join(CSRC, "attn_fwd.cu"), os.path.join(CSRC, "attn_bwd.cu")]
 HEADERS = [os.path.join(CSRC, "ptx.cuh"),
            os.path.join(os.path.dirname(HERE), "include", "bf16_attn.h")]
 BUILD_DIR = os.path.join(HERE, "_build")

@@ -1,0 +1,678 @@
+// attn_bwd.cu -- attention backward for GB300 (sm_103a): dQ, dK, dV of
+// O = softmax(Q K^T / sqrt(d)) V, d = 128, on tcgen05 tensor cores, and its C ABI.
+//
+// Source pages: "HipKittens: Fast and Furious AMD Kernels (MLSys 2026)", "Key observations"
+// (observation 3) and "Attention backward": the attention backward is the next kernel after
+// the forward; "MoonMath AI open-sources a HIP attention kernel for AMD MI300X that beats
+// AITER", opening section: the forward being differentiated.  With c = 1/sqrt(d),
+// P = softmax(c Q K^T) recomputed from the forward's row log-sum-exp, and the upstream
+// gradient dO:
+//   dV = P^T dO,   dP = dO V^T,   D_i = dO_i . O_i,   dS = P * (dP - D),
+//   dQ = c dS K,   dK = c dS^T Q.
+// GB300 design:
+//   * a preprocessing kernel forms D_i (fp32) and the base-2 log-sum-exp per query row;
+//   * the main kernel gives each work unit one (b, K/V head) and one 128-key tile: K_j and
+//     V_j stay in shared memory while the unit walks every query tile of every query head
+//     that reads that K/V head.  Per query tile i it runs five tcgen05 GEMMs with the key
+//     tile on the M side, so the recomputed probabilities come out transposed (one TMEM lane
+//     per key) and feed the dV and dK products straight from tensor memory:
+//       S^T  = K_j Q_i^T          (both operands K-major in shared memory)
+//       dP^T = V_j dO_i^T
+//       dV  += P^T dO_i           (P^T read from TMEM, dO_i an MN-major operand)
+//       dK  += dS^T Q_i           (dS^T read from TMEM)
+//       dQ_i = dS K_j             (dS^T also written to shared memory, read as an MN-major
+//                                  A operand; K_j as an MN-major B operand)
+//     dV and dK accumulate in TMEM for the whole unit; dQ_i is added into an fp32
+//     accumulator in global memory (vector reductions), since many key tiles contribute;
+//   * a last kernel rounds the dQ accumulator to bf16 (round to nearest even).
+// Roles: warp 8 TMA producer, warp 9 (one thread) MMA issuer, warpgroup 0 recomputes P and
+// forms dS, warpgroup 1 drains dQ and writes dK, dV.  Every wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "../../include/bf16_attn.h"
+#include "ptx.cuh"
+
+namespace {
+
+constexpr int kD = 128;                       // head dimension
+constexpr int kBM = 128;                      // query rows per query tile
+constexpr int kBN = 128;                      // keys per key tile (one unit)
+constexpr int kTileBytes = kBM * kD * 2;      // 32 KB: 128 rows x 128 bf16
+constexpr int kChunkBytes = kTileBytes / 2;   // 16 KB: one 64-column TMA box
+constexpr int kThreads = 384;
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
+constexpr uint32_t kTmemCols = 512;           // S^T/P^T/dQ | dP^T/dS^T | dV | dK
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr int kSmemK = 0;
+constexpr int kSmemV = kSmemK + kTileBytes;
+constexpr int kSmemQ = kSmemV + kTileBytes;
+constexpr int kSmemDO = kSmemQ + kTileBytes;
+constexpr int kSmemDS = kSmemDO + kTileBytes;   // dS^T: 128 key rows x 128 query columns
+constexpr int kSmemStats = kSmemDS + kTileBytes; // base-2 LSE [128] then D [128]
+constexpr int kSmemBars = kSmemStats + 2 * kBM * 4;
+enum {
+    kBarKV = 0,      // K_j, V_j loaded
+    kBarKVEmpty,     // the unit's last GEMM reading K_j, V_j is done
+    kBarQFull,       // Q_i, dO_i and their row statistics loaded
+    kBarQEmpty,      // the GEMMs reading Q_i, dO_i are done
+    kBarSFull,       // S^T and dP^T in TMEM
+    kBarPFull,       // P^T, dS^T in TMEM and dS^T in shared memory (128 arrivals)
+    kBarDQFull,      // dQ_i in TMEM
+    kBarDQEmpty,     // dQ_i read out of TMEM (128 arrivals)
+    kBarDKVFull,     // the unit's dK, dV final in TMEM
+    kBarDKVEmpty,    // dK, dV read out of TMEM (128 arrivals)
+    kBarDrain,
+    kNumBars
+};
+constexpr int kSmemMisc = kSmemBars + kNumBars * 8;
+constexpr int kSmemUsed = kSmemMisc + 16;
+constexpr int kSmemAlloc = kSmemUsed + 1024;
+
+enum : uint32_t {
+    kSiteKV = 1, kSiteKVEmpty, kSiteQFull, kSiteQEmpty, kSiteSFull, kSitePFull, kSiteDQFull,
+    kSiteDQEmpty, kSiteDKVFull, kSiteDKVEmpty
+};
+
+__device__ uint32_t g_bwd_status[2];   // [0] status code, [1] wait site
+
+struct BwdParams {
+    int B, H, Hkv, Sq, Skv, group;
+    int nq, nkv, nq_pad_rows;    // query tiles, key tiles, rows per (b, h) in the stat arrays
+    int n_units;
+    int causal, causal_off;      // key j visible to query i iff j <= i + causal_off
+    int bshd;
+    float scale;                 // 1/sqrt(d)
+    float scale_log2;            // log2(e)/sqrt(d)
+    const float* lse2;           // [B*H][nq_pad_rows] base-2 log-sum-exp
+    const float* delta;          // [B*H][nq_pad_rows] D_i
+    float* dq_acc;               // [B][H][Sq][d] fp32
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    long long kv_sb, kv_ss, kv_sh;   // element strides of dK/dV for b, s, h
+    unsigned long long wait_limit_ns;
+};
+
+struct Unit {
+    int b, kvh, jt;          // batch, K/V head, key tile
+    int it_lo;               // first query tile with a visible key
+    int nsteps;              // query tiles x query heads of the group
+};
+
+__device__ __forceinline__ Unit decode_unit(const BwdParams& p, int k) {
+    Unit u;
+    u.jt = k % p.nkv;
+    const int bk = k / p.nkv;
+    u.kvh = bk % p.Hkv;
+    u.b = bk / p.Hkv;
+    u.it_lo = 0;
+    if (p.causal) {
+        // the first query that sees key jt*128 is jt*128 - causal_off
+        const int first_q = u.jt * kBN - p.causal_off;
+        u.it_lo = first_q <= 0 ? 0 : first_q / kBM;
+    }
+    const int nt = u.it_lo < p.nq ? p.nq - u.it_lo : 0;
+    u.nsteps = nt * p.group;
+    return u;
+}
+
+__device__ __forceinline__ bool bwd_wait(uint32_t bar, uint32_t parity, uint32_t site,
+                                         volatile uint32_t* abort_flag, unsigned long long limit_ns) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > limit_ns) {
+            if (atomicCAS(&g_bwd_status[0], 0u, (uint32_t)ATTN_ERR_DEVICE_TIMEOUT) == 0u)
+                atomicExch(&g_bwd_status[1], site);
+            *abort_flag = 1u;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;              // 128-byte swizzle
+    return d;
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// fp32 -> bf16 bits, round to nearest even (the conversion instruction), NaN stays NaN
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) { return ptx::pack_bf16x2(lo, hi); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap domap,
+                const BwdParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const uint32_t bars = sbase + kSmemBars;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    uint32_t* tmem_holder = (uint32_t*)(smem + kSmemMisc);
+    volatile uint32_t* abort_flag = (volatile uint32_t*)(smem + kSmemMisc + 4);
+    const float* s_lse2 = (const float*)(smem + kSmemStats);
+    const float* s_delta = s_lse2 + kBM;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar(kBarKV), 1);
+        ptx::mbar_init(bar(kBarKVEmpty), 1);
+        ptx::mbar_init(bar(kBarQFull), 1);
+        ptx::mbar_init(bar(kBarQEmpty), 1);
+        ptx::mbar_init(bar(kBarSFull), 1);
+        ptx::mbar_init(bar(kBarPFull), kBN);
+        ptx::mbar_init(bar(kBarDQFull), 1);
+        ptx::mbar_init(bar(kBarDQEmpty), kBM);
+        ptx::mbar_init(bar(kBarDKVFull), 1);
+        ptx::mbar_init(bar(kBarDKVEmpty), kBN);
+        ptx::mbar_init(bar(kBarDrain), 1);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+    }
+    if (warp == kWarpMma) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const unsigned long long lim = p.wait_limit_ns;
+    const uint32_t tS = tmem, tDP = tmem + 128u, tDV = tmem + 256u, tDK = tmem + 384u;
+
+    if (warp == kWarpTma && lane == 0) {
+        // -------------------------------------------------------------------- TMA producer
+        const uint64_t pol_kv = ptx::policy_evict_last();
+        const uint64_t pol_q = ptx::policy_evict_last();
+        uint32_t s = 0, u = 0, q_issued = 0;
+        bool ok = true;
+        for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x, ++u) {
+            const Unit un = decode_unit(p, k);
+            if (u > 0 && !(ok = bwd_wait(bar(kBarKVEmpty), (u - 1) & 1u, kSiteKVEmpty, abort_flag, lim))) break;
+            ptx::mbar_arrive_expect_tx(bar(kBarKV), 2 * kTileBytes);
+            for (int c = 0; c < 2; ++c) {
+                const uint32_t dk = sbase + kSmemK + c * kChunkBytes, dv = sbase + kSmemV + c * kChunkBytes;
+                if (p.bshd) {
+                    ptx::tma_load_4d(dk, &kmap, bar(kBarKV), c * 64, un.kvh, un.jt * kBN, un.b, pol_kv);
+                    ptx::tma_load_4d(dv, &vmap, bar(kBarKV), c * 64, un.kvh, un.jt * kBN, un.b, pol_kv);
+                } else {
+                    ptx::tma_load_4d(dk, &kmap, bar(kBarKV), c * 64, un.jt * kBN, un.kvh, un.b, pol_kv);
+                    ptx::tma_load_4d(dv, &vmap, bar(kBarKV), c * 64, un.jt * kBN, un.kvh, un.b, pol_kv);
+                }
+            }
+            for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
+                const int h = un.kvh * p.group + st % p.group;
+                const int it = un.it_lo + st / p.group;
+                if (s > 0 && !(ok = bwd_wait(bar(kBarQEmpty), (s - 1) & 1u, kSiteQEmpty, abort_flag, lim))) break;
+                ptx::mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes + 2 * kBM * 4);
+                for (int c = 0; c < 2; ++c) {
+                    const uint32_t dq = sbase + kSmemQ + c * kChunkBytes, dd = sbase + kSmemDO + c * kChunkBytes;
+                    if (p.bshd) {
+                        ptx::tma_load_4d(dq, &qmap, bar(kBarQFull), c * 64, h, it * kBM, un.b, pol_q);
+                        ptx::tma_load_4d(dd, &domap, bar(kBarQFull), c * 64, h, it * kBM, un.b, pol_q);
+                    } else {
+                        ptx::tma_load_4d(dq, &qmap, bar(kBarQFull), c * 64, it * kBM, h, un.b, pol_q);
+                        ptx::tma_load_4d(dd, &domap, bar(kBarQFull), c * 64, it * kBM, h, un.b, pol_q);
+                    }
+                }
+                const long long srow = ((long long)un.b * p.H + h) * p.nq_pad_rows + (long long)it * kBM;
+                ptx::bulk_load_1d(sbase + kSmemStats, p.lse2 + srow, kBM * 4, bar(kBarQFull));
+                ptx::bulk_load_1d(sbase + kSmemStats + kBM * 4, p.delta + srow, kBM * 4, bar(kBarQFull));
+                ++q_issued;
+            }
+        }
+        // every issued load has landed before the CTA may exit
+        if (u > 0) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(bar(kBarKV), (u - 1) & 1u) && ptx::globaltimer_ns() - t0 < lim) {
+            }
+        }
+        if (q_issued > 0) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(bar(kBarQFull), (s - 1) & 1u) && ptx::globaltimer_ns() - t0 < lim) {
+            }
+        }
+    } else if (warp == kWarpMma && lane == 0) {
+        // -------------------------------------------------------------------- MMA issuer
+        constexpr uint32_t idesc_s = idesc_bf16(kBN, kBM, false, false);  // K-major x K-major
+        constexpr uint32_t idesc_o = idesc_bf16(kBN, kD, false, true);     // TMEM A x MN-major B
+        constexpr uint32_t idesc_q = idesc_bf16(kBM, kD, true, true);      // MN-major A x MN-major B
+        const uint64_t dK_k = sdesc(sbase + kSmemK, 16, 1024), dV_k = sdesc(sbase + kSmemV, 16, 1024);
+        const uint64_t dQ_k = sdesc(sbase + kSmemQ, 16, 1024), dDO_k = sdesc(sbase + kSmemDO, 16, 1024);
+        const uint64_t dQ_mn = sdesc(sbase + kSmemQ, kChunkBytes, 1024);
+        const uint64_t dDO_mn = sdesc(sbase + kSmemDO, kChunkBytes, 1024);
+        const uint64_t dDS_mn = sdesc(sbase + kSmemDS, kChunkBytes, 1024);
+        const uint64_t dK_mn = sdesc(sbase + kSmemK, kChunkBytes, 1024);
+        // D = A B^T over d: 8 K-steps of 16 (32 B inside a 64-column half, then the other half)
+        auto gemm_kk = [&](uint32_t d, uint64_t a, uint64_t b) {
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4);
+                ptx::mma_ss(d, a + off, b + off, idesc_s, kk > 0 ? 1u : 0u);
+            }
+        };
+        // D (+)= A[TMEM] B over 128 queries: 8 K-steps of 16 (8 TMEM columns of bf16 pairs; 2 KB of B)
+        auto gemm_tm = [&](uint32_t d, uint32_t a, uint64_t b, bool acc) {
+#pragma unroll
+            for (int kk = 0; kk < kBM / 16; ++kk)
+                ptx::mma_ts(d, a + (uint32_t)kk * 8u, b + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                            (kk > 0 || acc) ? 1u : 0u);
+        };
+        // dQ = dS K over 128 keys: both operands MN-major, 8 K-steps of 16 rows (2 KB each)
+        auto gemm_mm = [&](uint32_t d, uint64_t a, uint64_t b) {
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+                ptx::mma_ss(d, a + (uint64_t)((kk * 2048) >> 4), b + (uint64_t)((kk * 2048) >> 4), idesc_q,
+                            kk > 0 ? 1u : 0u);
+        };
+        uint32_t s = 0, u = 0;
+        bool ok = true;
+        for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x, ++u) {
+            const Unit un = decode_unit(p, k);
+            if (!(ok = bwd_wait(bar(kBarKV), u & 1u, kSiteKV, abort_flag, lim))) break;
+            for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
+                if (!(ok = bwd_wait(bar(kBarQFull), s & 1u, kSiteQFull, abort_flag, lim))) break;
+                // TMEM columns 0..127 hold the previous dQ until it has been read out
+                if (s > 0 && !(ok = bwd_wait(bar(kBarDQEmpty), (s - 1) & 1u, kSiteDQEmpty, abort_flag, lim))) break;
+                ptx::tc_fence_after();
+                gemm_kk(tS, dK_k, dQ_k);      // S^T  = K_j Q_i^T
+                gemm_kk(tDP, dV_k, dDO_k);    // dP^T = V_j dO_i^T
+                ptx::mma_commit(bar(kBarSFull));
+                if (!(ok = bwd_wait(bar(kBarPFull), s & 1u, kSitePFull, abort_flag, lim))) break;
+                // the previous unit's dK, dV have been read before the first step overwrites them
+                if (st == 0 && u > 0 && !(ok = bwd_wait(bar(kBarDKVEmpty), (u - 1) & 1u, kSiteDKVEmpty, abort_flag, lim)))
+                    break;
+                ptx::tc_fence_after();
+                gemm_tm(tDV, tS, dDO_mn, st > 0);    // dV += P^T dO_i
+                gemm_tm(tDK, tDP, dQ_mn, st > 0);    // dK += dS^T Q_i
+                ptx::mma_commit(bar(kBarQEmpty));
+                gemm_mm(tS, dDS_mn, dK_mn);          // dQ_i = dS K_j
+                ptx::mma_commit(bar(kBarDQFull));
+            }
+            if (!ok) break;
+            if (un.nsteps == 0 && u > 0 &&
+                !(ok = bwd_wait(bar(kBarDKVEmpty), (u - 1) & 1u, kSiteDKVEmpty, abort_flag, lim)))
+                break;
+            ptx::mma_commit(bar(kBarDKVFull));
+            ptx::mma_commit(bar(kBarKVEmpty));
+        }
+        ptx::mma_commit(bar(kBarDrain));
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(bar(kBarDrain), 0) && ptx::globaltimer_ns() - t0 < lim) {
+        }
+    } else if (warp < 4) {
+        // -------------------------------------------------------------------- P^T and dS^T
+        const int row = warp * 32 + lane;                        // key row of the tile
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const float cl = p.scale_log2;
+        uint32_t s = 0;
+        bool ok = true;
+        for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x) {
+            const Unit un = decode_unit(p, k);
+            const int kj = un.jt * kBN + row;
+            for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
+                const int it = un.it_lo + st / p.group;
+                ok = bwd_wait(bar(kBarQFull), s & 1u, kSiteQFull, abort_flag, lim) &&
+                     bwd_wait(bar(kBarSFull), s & 1u, kSiteSFull, abort_flag, lim);
+                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                ptx::tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t sv[32], dp[32];
+                    ptx::tmem_ld32(tS + lane_off + 32u * c, sv);
+                    ptx::tmem_ld32(tDP + lane_off + 32u * c, dp);
+                    uint32_t pw[16], dw[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float pr[2], dr[2];
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int col = 32 * c + e + h2;
+                            const int q = it * kBM + col;
+                            const bool vis = q < p.Sq && (!p.causal || kj <= q + p.causal_off);
+                            const float x = fmaf(__uint_as_float(sv[e + h2]), cl, -s_lse2[col]);
+                            const float pp = vis ? ptx::ex2_approx(x) : 0.0f;
+                            pr[h2] = pp;
+                            dr[h2] = pp * (__uint_as_float(dp[e + h2]) - s_delta[col]);
+                        }
+                        pw[e / 2] = pack2(pr[0], pr[1]);
+                        dw[e / 2] = pack2(dr[0], dr[1]);
+                    }
+                    ptx::tmem_st16(tS + lane_off + 16u * c, pw);
+                    ptx::tmem_st16(tDP + lane_off + 16u * c, dw);
+                    // dS^T row `row`, queries 32c..32c+31: 16-byte pieces (c & 1)*4 + v of the
+                    // 64-query chunk c >> 1, at piece ^ (row & 7) (128-byte swizzle)
+                    const uint32_t rowaddr = sbase + kSmemDS + (uint32_t)((c >> 1) * kChunkBytes) + (uint32_t)row * 128u;
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        const uint32_t pc = (uint32_t)((c & 1) * 4 + v4);
+                        ptx::st_shared_v4(rowaddr + ((pc ^ (uint32_t)(row & 7)) << 4), dw[4 * v4], dw[4 * v4 + 1],
+                                          dw[4 * v4 + 2], dw[4 * v4 + 3]);
+                    }
+                }
+                ptx::tmem_wait_st();
+                ptx::fence_proxy_async_smem();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(kBarPFull));
+            }
+        }
+    } else if (warp < 8) {
+        // -------------------------------------------------------------------- dQ, dK, dV out
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        uint32_t s = 0, u = 0;
+        bool ok = true;
+        for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x, ++u) {
+            const Unit un = decode_unit(p, k);
+            for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
+                const int h = un.kvh * p.group + st % p.group;
+                const int q = (un.it_lo + st / p.group) * kBM + row;
+                ok = bwd_wait(bar(kBarDQFull), s & 1u, kSiteDQFull, abort_flag, lim);
+                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                ptx::tc_fence_after();
+                float* dst = p.dq_acc + (((long long)un.b * p.H + h) * p.Sq + q) * kD;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(tS + lane_off + 32u * c, v);
+                    if (c == 3) {
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(bar(kBarDQEmpty));
+                    }
+                    if (q < p.Sq) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4)
+                            ptx::red_add_v4(dst + 32 * c + 4 * v4, __uint_as_float(v[4 * v4]) * p.scale,
+                                            __uint_as_float(v[4 * v4 + 1]) * p.scale,
+                                            __uint_as_float(v[4 * v4 + 2]) * p.scale,
+                                            __uint_as_float(v[4 * v4 + 3]) * p.scale);
+                    }
+                }
+            }
+            if (!ok) break;
+            ok = bwd_wait(bar(kBarDKVFull), u & 1u, kSiteDKVFull, abort_flag, lim);
+            if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const int kj = un.jt * kBN + row;
+            const long long off = (long long)un.b * p.kv_sb + (long long)kj * p.kv_ss + (long long)un.kvh * p.kv_sh;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {     // 0: dV, 1: dK (times 1/sqrt(d))
+                __nv_bfloat16* out = (which ? p.dk : p.dv) + off;
+                const float sc = which ? p.scale : 1.0f;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    if (un.nsteps > 0) {
+                        ptx::tmem_ld32((which ? tDK : tDV) + lane_off + 32u * c, v);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = 0u;
+                    }
+                    if (kj < p.Skv) {
+                        uint4* o4 = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            o4[v4] = make_uint4(pack2(__uint_as_float(v[8 * v4]) * sc, __uint_as_float(v[8 * v4 + 1]) * sc),
+                                                pack2(__uint_as_float(v[8 * v4 + 2]) * sc, __uint_as_float(v[8 * v4 + 3]) * sc),
+                                                pack2(__uint_as_float(v[8 * v4 + 4]) * sc, __uint_as_float(v[8 * v4 + 5]) * sc),
+                                                pack2(__uint_as_float(v[8 * v4 + 6]) * sc, __uint_as_float(v[8 * v4 + 7]) * sc));
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(kBarDKVEmpty));
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// D_i = dO_i . O_i in fp32 and the base-2 log-sum-exp, one warp per padded query row;
+// rows past Sq get zeros.
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout,
+                                                            const float* lse, float* lse2, float* delta, int H,
+                                                            int Sq, int nq_pad_rows, long long rows,
+                                                            long long o_sb, long long o_ss, long long o_sh) {
+    const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= rows) return;
+    const long long bh = gw / nq_pad_rows;
+    const int q = (int)(gw % nq_pad_rows);
+    const int b = (int)(bh / H), h = (int)(bh % H);
+    float acc = 0.0f;
+    if (q < Sq) {
+        const long long off = (long long)b * o_sb + (long long)q * o_ss + (long long)h * o_sh + lane * 4;
+        const uint2 ov = *reinterpret_cast<const uint2*>(o + off);
+        const uint2 gv = *reinterpret_cast<const uint2*>(dout + off);
+        const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
+        const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float2 of = __bfloat1622float2(op[e]), gf = __bfloat1622float2(gp[e]);
+            acc = fmaf(of.x, gf.x, acc);
+            acc = fmaf(of.y, gf.y, acc);
+        }
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, s);
+    if (lane == 0) {
+        delta[gw] = acc;
+        lse2[gw] = q < Sq ? lse[bh * Sq + q] * 1.4426950408889634f : 0.0f;
+    }
+}
+
+// dq (bf16, the caller's layout) = dq_acc (fp32 [B][H][Sq][d]), round to nearest even.
+__global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const float* dq_acc, __nv_bfloat16* dq, int H, int Sq,
+                                                          long long n4, long long o_sb, long long o_ss,
+                                                          long long o_sh) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // group of 4 columns
+    if (i >= n4) return;
+    const long long row = i / (kD / 4);
+    const int x = (int)(i % (kD / 4)) * 4;
+    const int q = (int)(row % Sq);
+    const long long bh = row / Sq;
+    const int h = (int)(bh % H), b = (int)(bh / H);
+    const float4 v = *reinterpret_cast<const float4*>(dq_acc + row * kD + x);
+    __nv_bfloat16* dst = dq + (long long)b * o_sb + (long long)q * o_ss + (long long)h * o_sh + x;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack2(v.x, v.y), pack2(v.z, v.w));
+}
+
+// ------------------------------------------------------------------------------ host side
+std::mutex g_bwd_mutex;
+PFN_cuTensorMapEncodeTiled_v12000 g_bwd_encode = nullptr;
+bool g_bwd_attr[64] = {};
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool encode(CUtensorMap* m, const void* ptr, int64_t B, int64_t H, int64_t S, bool bshd) {
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+    dims[0] = kD;
+    if (bshd) {
+        dims[1] = H; dims[2] = S; dims[3] = B;
+        strides[0] = kD * 2; strides[1] = H * kD * 2; strides[2] = S * H * kD * 2;
+        box[0] = 64; box[1] = 1; box[2] = kBM; box[3] = 1;
+    } else {
+        dims[1] = S; dims[2] = H; dims[3] = B;
+        strides[0] = kD * 2; strides[1] = S * kD * 2; strides[2] = H * S * kD * 2;
+        box[0] = 64; box[1] = kBM; box[2] = 1; box[3] = 1;
+    }
+    return g_bwd_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int check_shape(const attn_bwd_args_t& a) {
+    if (a.B < 1 || a.H < 1 || a.Hkv < 1 || a.Sq < 1 || a.Skv < 1 || a.d < 1) return ATTN_ERR_INVALID_ARG;
+    if (a.H % a.Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (a.layout != ATTN_LAYOUT_BSHD && a.layout != ATTN_LAYOUT_BHSD) return ATTN_ERR_INVALID_ARG;
+    if ((a.causal != 0 && a.causal != 1) || a.reserved0 != 0 || a.reserved1 != 0) return ATTN_ERR_INVALID_ARG;
+    if (a.d != kD) return ATTN_ERR_UNSUPPORTED;
+    const int64_t lim = (int64_t)1 << 30;
+    if (a.Sq > lim || a.Skv > lim || a.B * a.H > lim || a.B * a.Hkv * cdiv(a.Skv, kBN) > lim ||
+        a.B * a.H * cdiv(a.Sq, kBM) * kBM > lim)
+        return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+size_t ws_bytes(const attn_bwd_args_t& a) {
+    const int64_t rows_pad = a.B * a.H * cdiv(a.Sq, kBM) * kBM;
+    return (size_t)(a.B * a.H * a.Sq * kD * 4) + (size_t)(2 * rows_pad * 4);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_bwd_workspace_size(const attn_bwd_args_t* args) {
+    if (!args || check_shape(*args) != ATTN_OK) return 0;
+    return ws_bytes(*args);
+}
+
+int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_bytes, attn_stream_t stream_) {
+    if (!args) return ATTN_ERR_INVALID_ARG;
+    const attn_bwd_args_t& a = *args;
+    if (!a.q || !a.k || !a.v || !a.o || !a.dout || !a.lse || !a.dq || !a.dk || !a.dv) return ATTN_ERR_INVALID_ARG;
+    int st = check_shape(a);
+    if (st != ATTN_OK) return st;
+    const uintptr_t al = (uintptr_t)a.q | (uintptr_t)a.k | (uintptr_t)a.v | (uintptr_t)a.o | (uintptr_t)a.dout |
+                         (uintptr_t)a.dq | (uintptr_t)a.dk | (uintptr_t)a.dv | (uintptr_t)workspace;
+    if ((al & 15u) || ((uintptr_t)a.lse & 3u)) return ATTN_ERR_MISALIGNED;
+    const size_t need = ws_bytes(a);
+    if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    // the gradients must not overlap the inputs or each other
+    const uintptr_t qb = (uintptr_t)(a.B * a.H * a.Sq * kD * 2), kb = (uintptr_t)(a.B * a.Hkv * a.Skv * kD * 2);
+    const uintptr_t outs[3][2] = {{(uintptr_t)a.dq, qb}, {(uintptr_t)a.dk, kb}, {(uintptr_t)a.dv, kb}};
+    const uintptr_t ins[6][2] = {{(uintptr_t)a.q, qb}, {(uintptr_t)a.k, kb}, {(uintptr_t)a.v, kb},
+                                 {(uintptr_t)a.o, qb}, {(uintptr_t)a.dout, qb}, {(uintptr_t)workspace, need}};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 6; ++j)
+            if (outs[i][0] < ins[j][0] + ins[j][1] && ins[j][0] < outs[i][0] + outs[i][1]) return ATTN_ERR_ALIAS;
+        for (int j = 0; j < i; ++j)
+            if (outs[i][0] < outs[j][0] + outs[j][1] && outs[j][0] < outs[i][0] + outs[i][1]) return ATTN_ERR_ALIAS;
+    }
+    cudaStream_t stream = (cudaStream_t)stream_;
+    int dev = 0, sms = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_NO_DEVICE;
+    }
+    if (major != 10 || minor != 3) return ATTN_ERR_NO_DEVICE;
+    {
+        std::lock_guard<std::mutex> g(g_bwd_mutex);
+        if (!g_bwd_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult qr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) !=
+                    cudaSuccess ||
+                qr != cudaDriverEntryPointSuccess || !fn)
+                return ATTN_ERR_CUDA;
+            g_bwd_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+        }
+        if (!g_bwd_attr[dev]) {
+            if (cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+                cudaSuccess)
+                return ATTN_ERR_CUDA;
+            g_bwd_attr[dev] = true;
+        }
+    }
+    const bool bshd = a.layout == ATTN_LAYOUT_BSHD;
+    CUtensorMap qm, km, vm, dom;
+    if (!encode(&qm, a.q, a.B, a.H, a.Sq, bshd) || !encode(&km, a.k, a.B, a.Hkv, a.Skv, bshd) ||
+        !encode(&vm, a.v, a.B, a.Hkv, a.Skv, bshd) || !encode(&dom, a.dout, a.B, a.H, a.Sq, bshd))
+        return ATTN_ERR_CUDA;
+
+    BwdParams p;
+    memset(&p, 0, sizeof p);
+    p.B = (int)a.B; p.H = (int)a.H; p.Hkv = (int)a.Hkv; p.Sq = (int)a.Sq; p.Skv = (int)a.Skv;
+    p.group = (int)(a.H / a.Hkv);
+    p.nq = (int)cdiv(a.Sq, kBM);
+    p.nkv = (int)cdiv(a.Skv, kBN);
+    p.nq_pad_rows = p.nq * kBM;
+    p.n_units = (int)(a.B * a.Hkv * p.nkv);
+    p.causal = a.causal;
+    p.causal_off = (int)(a.Skv - a.Sq);
+    p.bshd = bshd ? 1 : 0;
+    p.scale = (float)(1.0 / std::sqrt((double)kD));
+    p.scale_log2 = (float)((1.0 / std::sqrt((double)kD)) * 1.4426950408889634);
+    float* dq_acc = reinterpret_cast<float*>(workspace);
+    float* lse2 = dq_acc + a.B * a.H * a.Sq * kD;
+    float* delta = lse2 + a.B * a.H * p.nq_pad_rows;
+    p.lse2 = lse2;
+    p.delta = delta;
+    p.dq_acc = dq_acc;
+    p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
+    p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
+    long long q_sb, q_ss, q_sh;
+    if (bshd) {
+        p.kv_sb = a.Skv * a.Hkv * kD; p.kv_ss = a.Hkv * kD; p.kv_sh = kD;
+        q_sb = a.Sq * a.H * kD; q_ss = a.H * kD; q_sh = kD;
+    } else {
+        p.kv_sb = a.Hkv * a.Skv * kD; p.kv_ss = kD; p.kv_sh = a.Skv * kD;
+        q_sb = a.H * a.Sq * kD; q_ss = kD; q_sh = a.Sq * kD;
+    }
+    p.wait_limit_ns = 2000ull * 1000000ull;
+
+    if (cudaMemsetAsync(dq_acc, 0, (size_t)(a.B * a.H * a.Sq * kD * 4), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    const long long prows = a.B * a.H * (long long)p.nq_pad_rows;
+    attn_bwd_prep_kernel<<<(unsigned)cdiv(prows, 8), 256, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(a.o), reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, lse2,
+        delta, p.H, p.Sq, p.nq_pad_rows, prows, q_sb, q_ss, q_sh);
+    const int grid = p.n_units < sms ? p.n_units : sms;
+    attn_bwd_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(qm, km, vm, dom, p);
+    const long long n4 = a.B * a.H * a.Sq * (kD / 4);
+    attn_bwd_dq_kernel<<<(unsigned)cdiv(n4, 256), 256, 0, stream>>>(dq_acc, reinterpret_cast<__nv_bfloat16*>(a.dq),
+                                                                    p.H, p.Sq, n4, q_sb, q_ss, q_sh);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+int attn_bwd_get_device_status(attn_stream_t stream, int32_t* site) {
+    if (site) *site = 0;
+    uint32_t h[2] = {0u, 0u};
+    const uint32_t zero[2] = {0u, 0u};
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess ||
+        cudaMemcpyFromSymbol(h, g_bwd_status, sizeof h) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_bwd_status, zero, sizeof zero) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    if (site) *site = (int32_t)h[1];
+    return (int)h[0];
+}
+
+}  // extern "C"

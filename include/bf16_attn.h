@@ -217,6 +217,50 @@ const char* attn_status_string(int status);
 /* Library version, as major*10000 + minor*100 + patch. */
 int attn_version(void);
 
+/*
+ * Attention backward (d = 128): the gradients of O = softmax(Q K^T / sqrt(d)) V with respect
+ * to Q, K and V, with the causal mask and grouped K/V heads as in attn_fwd_ex.  Source:
+ * "HipKittens: Fast and Furious AMD Kernels (MLSys 2026)", "Key observations" (observation 3)
+ * and "Attention backward" -- the backward is the kernel after the forward.  With
+ * c = 1/sqrt(d), P recomputed from the forward's row log-sum-exp, and the upstream gradient dO:
+ *   dV = P^T dO,  dS = P * (dO V^T - D) with D_i = dO_i . O_i,  dQ = c dS K,  dK = c dS^T Q.
+ *   q, k, v, o   the forward's inputs and output (bf16, one layout, as in attn_fwd_ex)
+ *   dout         dO, bf16, like o
+ *   lse          the forward's fp32 [B][H][Sq] natural-log log-sum-exp (attn_fwd_ex's lse)
+ *   dq, dk, dv   outputs, bf16, like q, k, v (round to nearest even); must not overlap the
+ *                inputs, each other or the workspace
+ *   causal       0 or 1, as in the forward;  reserved0, reserved1 must be 0
+ * Rows of K/V that no query sees get zero gradients.  Inputs are expected finite.
+ */
+typedef struct {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* o;
+    const void* dout;
+    const float* lse;
+    void* dq;
+    void* dk;
+    void* dv;
+    int64_t B, H, Hkv, Sq, Skv, d;
+    int32_t layout, causal, reserved0, reserved1;
+} attn_bwd_args_t;
+
+/* Workspace bytes attn_bwd needs (fp32 dQ accumulator and per-row statistics; 0 if invalid). */
+size_t attn_bwd_workspace_size(const attn_bwd_args_t* args);
+
+/*
+ * attn_bwd -- the backward on `stream`: zeroes the dQ accumulator, forms D and the base-2
+ * LSE, runs the tcgen05 backward kernel and rounds dQ.  workspace: caller device memory of
+ * at least attn_bwd_workspace_size() bytes, 16-byte aligned (required).  Errors as for
+ * attn_fwd; device-side wait expiries are read with attn_bwd_get_device_status().
+ */
+int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_bytes,
+             attn_stream_t stream);
+
+/* Synchronize `stream`, then read and clear the backward kernel's device status word. */
+int attn_bwd_get_device_status(attn_stream_t stream, int32_t* site);
+
 #ifdef __cplusplus
 }
 #endif

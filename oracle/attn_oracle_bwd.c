@@ -118,10 +118,12 @@ int attn_oracle_f64_forward(const double* q, const double* k, const double* v, i
  *   dq [like q], dk, dv [like k / v]     fp64 outputs (required)
  *   dq_a, dk_a, dv_a                     optional fp64 forward-error scales, same shapes:
  *                                        dV: sum_i p_ij |dO_ix|
- *                                        dQ: c sum_j p_ij (|dP_ij| + |D_i|) |k_jx|
- *                                        dK: c sum_i p_ij (|dP_ij| + |D_i|) |q_ix|
- *                                        (the sums of the terms' magnitudes, with dS bounded
- *                                        by p (|dP| + |D|))
+ *                                        dQ: c sum_j p_ij (|dP_ij| + |D|_i) |k_jx|
+ *                                        dK: c sum_i p_ij (|dP_ij| + |D|_i) |q_ix|
+ *                                        with |D|_i = sum_x |dO_ix| |O_ix| (the sums of the
+ *                                        terms' magnitudes; dS is bounded by p (|dP| + |D|),
+ *                                        and |D| also bounds D's error when it is formed from
+ *                                        a rounded O)
  *   delta                                optional fp64 [B][H][Sq]: D_i
  * Work is split over (b, K/V head): each owns its dK and dV rows and the dQ rows of the
  * query heads that read it, so no two threads write the same output.
@@ -190,6 +192,15 @@ int attn_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                             dp[j] = acc;
                             Di += p[j] * acc;
                         }
+                        /* |D|_i = sum_x |dO_ix| |O_ix| for the error scales */
+                        double Dabs = 0.0;
+                        if (dq_a || dk_a)
+                            for (int64_t x = 0; x < d; ++x) {
+                                double ox = 0.0;
+                                for (int64_t j = 0; j < nvis; ++j)
+                                    ox += p[j] * bwd_bits_to_double(v[bwd_offset(layout, b, j, kvh, x, Skv, Hkv, d)]);
+                                Dabs += fabs(gi[x]) * fabs(ox);
+                            }
                         if (delta) delta[(b * H + h) * Sq + i] = Di;
                         /* dQ_i = c sum_j p_ij (dP_ij - D_i) k_j */
                         for (int64_t x = 0; x < d; ++x) {
@@ -197,7 +208,7 @@ int attn_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                             for (int64_t j = 0; j < nvis; ++j) {
                                 const double kjx = bwd_bits_to_double(k[bwd_offset(layout, b, j, kvh, x, Skv, Hkv, d)]);
                                 acc += p[j] * (dp[j] - Di) * kjx;
-                                mag += p[j] * (fabs(dp[j]) + fabs(Di)) * fabs(kjx);
+                                mag += p[j] * (fabs(dp[j]) + Dabs) * fabs(kjx);
                             }
                             const int64_t off = bwd_offset(layout, b, i, h, x, Sq, H, d);
                             dq[off] = c * acc;
@@ -206,7 +217,7 @@ int attn_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         /* dK_j += c dS_ij q_i,  dV_j += p_ij dO_i */
                         for (int64_t j = 0; j < nvis; ++j) {
                             const double ds = p[j] * (dp[j] - Di);
-                            const double dsa = p[j] * (fabs(dp[j]) + fabs(Di));
+                            const double dsa = p[j] * (fabs(dp[j]) + Dabs);
                             for (int64_t x = 0; x < d; ++x) {
                                 const int64_t off = bwd_offset(layout, b, j, kvh, x, Skv, Hkv, d);
                                 dk[off] += c * ds * qi[x];

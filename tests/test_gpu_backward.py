@@ -1,0 +1,107 @@
+"""GPU parity of the attention backward (attn_bwd) against the fp64 backward oracle.
+
+The GPU path recomputes P from the forward's fp32 log-sum-exp, rounds P and dS to bf16
+before the tensor-core products, and forms D from the forward's bf16 output, so an element
+of dQ, dK or dV passes when |gpu - oracle| <= 2^-7 * A + ulp(oracle), with A the oracle's
+sum of term magnitudes (dV: sum_i p |dO|; dQ, dK: c sum p (|dP| + |D|) |k| or |q|, where
+|D| = sum |dO| |O| also covers D formed from the rounded O).  2^-7 is four times bf16's unit
+roundoff: P (or dS) rounding, the rounding of O inside D, and the final bf16 store.  The
+oracle itself is pinned against numerical differentiation of the forward.  dQ is summed with
+atomic adds across key tiles, so its last bits may differ between runs; dK and dV are
+accumulated in a fixed order and are bitwise reproducible.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import parity
+from workloads import make_qkv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def attn():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import bf16_attention_forward_gb300 as a
+    a.load()
+    return a
+
+
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def run_bwd(attn, q, k, v, g, layout, causal):
+    qd, kd, vd, gd = (t.cuda() for t in (q, k, v, g))
+    o, lse = attn.attn_fwd_ex(qd, kd, vd, layout=layout, causal=causal, return_lse=True)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, gd, lse, layout=layout, causal=causal)
+    torch.cuda.synchronize()
+    assert attn.device_status()[0] == 0
+    st, site = attn.bwd_device_status()
+    assert st == 0, "backward device status %d at wait site %d" % (st, site)
+    return dq, dk, dv
+
+
+def check_bwd(attn, q, k, v, g, layout, causal=False):
+    dq, dk, dv = run_bwd(attn, q, k, v, g, layout, causal)
+    ref = oracle.backward(q, k, v, g, layout, causal=causal, want_a=True)
+    worst = {}
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        gb = _bits(got).astype(np.uint16).reshape(-1)
+        r = ref[name].reshape(-1)
+        a = ref[name + "_a"].reshape(-1)
+        gf = parity.bits_to_f64(gb)
+        rb = ref[name + "_bits"].reshape(-1).astype(np.uint16)
+        err = np.abs(gf - r)
+        tol = 2.0 ** -7 * a + parity.bf16_ulp(rb)
+        bad = ~(err <= tol)
+        assert not bad.any(), (name, int(bad.sum()), float((err / np.maximum(a, 1e-30))[bad].max()))
+        worst[name] = float(np.max(err / np.maximum(a, 1e-30)))
+    return worst, (dq, dk, dv)
+
+
+SHAPES = [  # (B, H, Hkv, Sq, Skv)
+    (1, 1, 1, 128, 128), (1, 2, 2, 300, 200), (2, 2, 1, 129, 257), (1, 4, 2, 256, 384),
+    (1, 1, 1, 1, 1), (1, 2, 1, 77, 1000),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "B%dH%dHkv%dSq%dSkv%d" % s)
+@pytest.mark.parametrize("layout", ["bshd", "bhsd"])
+def test_backward_matches_oracle(attn, shape, layout):
+    B, H, Hkv, Sq, Skv = shape
+    q, k, v = make_qkv(B, H, Sq, Skv, 128, layout, seed=5000 + sum(shape), Hkv=Hkv)
+    g = make_qkv(B, H, Sq, 1, 128, layout, seed=5100 + sum(shape))[0]
+    check_bwd(attn, q, k, v, g, layout)
+
+
+@pytest.mark.parametrize("Sq,Skv", [(300, 300), (200, 456), (456, 200), (640, 640)])
+def test_backward_causal(attn, Sq, Skv):
+    q, k, v = make_qkv(1, 4, Sq, Skv, 128, "bshd", seed=5200 + Sq, Hkv=2)
+    g = make_qkv(1, 4, Sq, 1, 128, "bshd", seed=5300 + Skv)[0]
+    check_bwd(attn, q, k, v, g, "bshd", causal=True)
+
+
+def test_backward_dk_dv_reproducible_and_large_logits(attn):
+    q, k, v = make_qkv(1, 2, 384, 512, 128, "bhsd", seed=5400, sigma=2.0)
+    g = make_qkv(1, 2, 384, 1, 128, "bhsd", seed=5401)[0]
+    _, (dq1, dk1, dv1) = check_bwd(attn, q, k, v, g, "bhsd")
+    dq2, dk2, dv2 = run_bwd(attn, q, k, v, g, "bhsd", False)
+    assert torch.equal(dk1.view(torch.int16), dk2.view(torch.int16))
+    assert torch.equal(dv1.view(torch.int16), dv2.view(torch.int16))
+
+
+def test_backward_argument_errors(attn):
+    q, k, v = (t.cuda() for t in make_qkv(1, 1, 8, 8, 128, "bshd", seed=1))
+    o, lse = attn.attn_fwd_ex(q, k, v, return_lse=True)
+    with pytest.raises(ValueError):
+        attn.attn_bwd(q, k, v, o, o, lse[:, :, :4].contiguous())
+    with pytest.raises(attn.AttnError):           # the gradient may not alias an input
+        attn.attn_bwd(q, k, v, o, o, lse, dq=q)
+    q64, k64, v64 = (t.cuda() for t in make_qkv(1, 1, 8, 8, 64, "bshd", seed=2))
+    o64, l64 = attn.attn_fwd_ex(q64, k64, v64, return_lse=True)
+    with pytest.raises(attn.AttnError):           # d = 64 has no backward kernel
+        attn.attn_bwd(q64, k64, v64, o64, o64, l64)
