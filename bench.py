@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", default="fwd", choices=["fwd", "bwd"],
+                    help="bwd: time the attention backward (attn_bwd) instead of the forward")
     return ap.parse_args()
 
 
@@ -260,12 +262,77 @@ def run_reference(args, w, rank, world):
     return 0
 
 
+def run_backward(args, w):
+    """Time attn_bwd on resident inputs (the forward's output and LSE made beforehand).
+    FLOP per call: five matrix products of 2*d per visible (query, key) pair and head."""
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    dev = torch.device("cuda", 0)
+    import bf16_attention_forward_gb300 as attn
+    attn.load()
+    steps = args.steps if args.steps is not None else 100
+    warmup = max(3, args.warmup if args.warmup is not None else 10)
+    q, k, v = (t.to(dev) for t in make_qkv(w.B, w.H, w.Sq, w.Skv, w.d, w.layout, seed=w.seed,
+                                               sigma=w.sigma, Hkv=w.kv_heads))
+    g = make_qkv(w.B, w.H, w.Sq, 1, w.d, w.layout, seed=w.seed + 77)[0].to(dev)
+    o, lse = attn.attn_fwd_ex(q, k, v, layout=w.layout, causal=w.causal, return_lse=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    a_ws = None
+
+    def call():
+        nonlocal a_ws
+        attn.attn_bwd(q, k, v, o, g, lse, layout=w.layout, causal=w.causal, dq=dq, dk=dk, dv=dv,
+                      workspace=a_ws)
+
+    # size the workspace once, outside the timed region
+    import ctypes
+    a = attn.BwdArgs()
+    a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d = w.B, w.H, w.kv_heads, w.Sq, w.Skv, w.d
+    a.layout, a.causal = attn.LAYOUTS[w.layout], int(w.causal)
+    a_ws = torch.empty(max(int(attn.load().attn_bwd_workspace_size(ctypes.byref(a))), 16),
+                       dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0, enabled=not args.no_clocks) as clocks:
+        t0.record()
+        for _ in range(steps):
+            call()
+        t1.record()
+        torch.cuda.synchronize(dev)
+    st, site = attn.bwd_device_status()
+    assert st == 0, "backward device status %d at wait site %d" % (st, site)
+    ms = t0.elapsed_time(t1) / steps
+    flop = 10 * w.B * w.H * w.visible_pairs * w.d
+    value = flop / (ms * 1e-3) / 1e12
+    peak, peak_sust, _, peak_src = measured_peaks()
+    line = {
+        "metric": "attention bwd TFLOPS (10*B*H*Sq*Skv*d: five products per visible pair)",
+        "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": steps, "warmup": warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,%g) bf16)" % w.sigma,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.kv_heads, "Sq": w.Sq,
+                   "Skv": w.Skv, "d": w.d, "causal": w.causal, "layout": w.layout,
+                   "step": "one attn_bwd call: dQ zeroing, D/LSE preprocessing, the tcgen05 "
+                           "backward kernel and the dQ rounding"},
+        "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
+                     "frac": value / peak, "peak_source": peak_src + " burst bf16 (cuBLAS)",
+                     "timed": "whole call"},
+        "clocks": clocks.summary(),
+        "gpu_launches": 3 * steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w, rank, world)
+    if args.op == "bwd":
+        return run_backward(args, w)
 
     import torch.distributed as dist
     if world > 1:

@@ -25,8 +25,9 @@
 //     dV and dK accumulate in TMEM for the whole unit; dQ_i is added into an fp32
 //     accumulator in global memory (vector reductions), since many key tiles contribute;
 //   * a last kernel rounds the dQ accumulator to bf16 (round to nearest even).
-// Roles: warp 8 TMA producer, warp 9 (one thread) MMA issuer, warpgroup 0 recomputes P and
-// forms dS, warpgroup 1 drains dQ and writes dK, dV.  Every wait is bounded.
+// Roles: warp 8 TMA producer, warp 9 (one thread) MMA issuer; warpgroups 0 and 1 recompute P
+// and form dS for query columns 0..63 and 64..127 of each step, and warpgroup 1 then drains dQ
+// and, at the end of a unit, writes dK and dV.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -55,18 +56,24 @@ constexpr uint32_t kTmemCols = 512;           // S^T/P^T/dQ | dP^T/dS^T | dV | d
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int kSmemK = 0;
 constexpr int kSmemV = kSmemK + kTileBytes;
-constexpr int kSmemQ = kSmemV + kTileBytes;
-constexpr int kSmemDO = kSmemQ + kTileBytes;
-constexpr int kSmemDS = kSmemDO + kTileBytes;   // dS^T: 128 key rows x 128 query columns
-constexpr int kSmemStats = kSmemDS + kTileBytes; // base-2 LSE [128] then D [128]
+// Q_i and dO_i go through a two-stage ring (stage s % 2 for step s) so the next query
+// tile loads while the current one is in use; each stage is Q then dO.
+constexpr int kStages = 2;
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kSmemStage0 = kSmemV + kTileBytes;
+constexpr int kSmemDS = kSmemStage0 + kStages * kStageBytes;   // dS^T: 128 keys x 128 queries
+constexpr int kSmemStats = kSmemDS + kTileBytes;               // base-2 LSE [128] then D [128]
 constexpr int kSmemBars = kSmemStats + 2 * kBM * 4;
 enum {
     kBarKV = 0,      // K_j, V_j loaded
     kBarKVEmpty,     // the unit's last GEMM reading K_j, V_j is done
-    kBarQFull,       // Q_i, dO_i and their row statistics loaded
-    kBarQEmpty,      // the GEMMs reading Q_i, dO_i are done
-    kBarSFull,       // S^T and dP^T in TMEM
-    kBarPFull,       // P^T, dS^T in TMEM and dS^T in shared memory (128 arrivals)
+    kBarQFull,       // [2] Q_i, dO_i of stage s % 2 loaded
+    kBarQEmpty = kBarQFull + kStages,   // [2] the GEMMs reading that stage are done
+    kBarStats = kBarQEmpty + kStages,   // the step's row statistics loaded
+    kBarSFull,       // S^T in TMEM
+    kBarDPFull,      // dP^T in TMEM
+    kBarPFull,       // P^T, dS^T in TMEM and dS^T in shared memory (256 arrivals)
+    kBarRead,        // both warpgroups have read S^T and dP^T out of TMEM (256 arrivals)
     kBarDQFull,      // dQ_i in TMEM
     kBarDQEmpty,     // dQ_i read out of TMEM (128 arrivals)
     kBarDKVFull,     // the unit's dK, dV final in TMEM
@@ -80,7 +87,7 @@ constexpr int kSmemAlloc = kSmemUsed + 1024;
 
 enum : uint32_t {
     kSiteKV = 1, kSiteKVEmpty, kSiteQFull, kSiteQEmpty, kSiteSFull, kSitePFull, kSiteDQFull,
-    kSiteDQEmpty, kSiteDKVFull, kSiteDKVEmpty
+    kSiteDQEmpty, kSiteDKVFull, kSiteDKVEmpty, kSiteStats, kSiteDPFull, kSiteRead
 };
 
 __device__ uint32_t g_bwd_status[2];   // [0] status code, [1] wait site
@@ -179,10 +186,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar(kBarKV), 1);
         ptx::mbar_init(bar(kBarKVEmpty), 1);
-        ptx::mbar_init(bar(kBarQFull), 1);
-        ptx::mbar_init(bar(kBarQEmpty), 1);
+        for (int i = 0; i < kStages; ++i) {
+            ptx::mbar_init(bar(kBarQFull + i), 1);
+            ptx::mbar_init(bar(kBarQEmpty + i), 1);
+        }
+        ptx::mbar_init(bar(kBarStats), 1);
         ptx::mbar_init(bar(kBarSFull), 1);
-        ptx::mbar_init(bar(kBarPFull), kBN);
+        ptx::mbar_init(bar(kBarDPFull), 1);
+        ptx::mbar_init(bar(kBarPFull), 2 * kBN);
+        ptx::mbar_init(bar(kBarRead), 2 * kBN);
         ptx::mbar_init(bar(kBarDQFull), 1);
         ptx::mbar_init(bar(kBarDQEmpty), kBM);
         ptx::mbar_init(bar(kBarDKVFull), 1);
@@ -200,7 +212,88 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const unsigned long long lim = p.wait_limit_ns;
-    const uint32_t tS = tmem, tDP = tmem + 128u, tDV = tmem + 256u, tDK = tmem + 384u;
+    // TMEM: S^T then P^T | dP^T then dS^T, later dQ_i | dV | dK.  dQ_i goes where dP^T was, so
+    // the next step's S^T GEMM does not wait for dQ_i to be read out.
+    const uint32_t tS = tmem, tDP = tmem + 128u, tDV = tmem + 256u, tDK = tmem + 384u, tDQ = tDP;
+
+    // P^T = 2^(S^T log2(e)/sqrt(d) - LSE2) and dS^T = P^T (dP^T - D) for this thread's key row
+    // and query columns 64*half .. 64*half + 63 of step s (warpgroup `half` runs it).  The
+    // bf16 results go to TMEM over S^T and dP^T, where they take half the columns: column c of
+    // P^T holds queries 2c and 2c+1, so warpgroup 1's results land on columns warpgroup 0
+    // still reads.  Both warpgroups therefore read and compute first, meet on a barrier, and
+    // only then store to TMEM.  dS^T also goes to shared memory (its own region) for dQ.
+    auto pds_step = [&](const Unit& un, int it, uint32_t s, int half) -> bool {
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;                     // key row of the tile
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int kj = un.jt * kBN + row;
+        bool ok = bwd_wait(bar(kBarStats), s & 1u, kSiteStats, abort_flag, lim) &&
+                  bwd_wait(bar(kBarSFull), s & 1u, kSiteSFull, abort_flag, lim) &&
+                  bwd_wait(bar(kBarDPFull), s & 1u, kSiteDPFull, abort_flag, lim);
+        if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+        ptx::tc_fence_after();
+        const float cl = p.scale_log2;
+        uint32_t pw[2][16], dw[2][16];
+#pragma unroll
+        for (int ci = 0; ci < 2; ++ci) {
+            const int c = 2 * half + ci;
+            uint32_t sv[32], dp[32];
+            ptx::tmem_ld32(tS + lane_off + 32u * c, sv);
+            ptx::tmem_ld32(tDP + lane_off + 32u * c, dp);
+            const int q0 = it * kBM + 32 * c;
+            // every column of this chunk visible to this key: no per-element test
+            const bool all_vis = q0 + 31 < p.Sq && (!p.causal || kj <= q0 + p.causal_off);
+#pragma unroll
+            for (int g4 = 0; g4 < 8; ++g4) {
+                const float4 l4 = *reinterpret_cast<const float4*>(s_lse2 + 32 * c + 4 * g4);
+                const float4 d4 = *reinterpret_cast<const float4*>(s_delta + 32 * c + 4 * g4);
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                float pr[4], dr[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int col = 4 * g4 + e;
+                    const float x = fmaf(__uint_as_float(sv[col]), cl, -lv[e]);
+                    float pp = ptx::ex2_approx(x);
+                    if (!all_vis) {
+                        const int q = q0 + col;
+                        if (!(q < p.Sq && (!p.causal || kj <= q + p.causal_off))) pp = 0.0f;
+                    }
+                    pr[e] = pp;
+                    dr[e] = pp * (__uint_as_float(dp[col]) - dv4[e]);
+                }
+                pw[ci][2 * g4] = pack2(pr[0], pr[1]);
+                pw[ci][2 * g4 + 1] = pack2(pr[2], pr[3]);
+                dw[ci][2 * g4] = pack2(dr[0], dr[1]);
+                dw[ci][2 * g4 + 1] = pack2(dr[2], dr[3]);
+            }
+            // dS^T row `row`, queries 32c..32c+31: 16-byte pieces (c & 1)*4 + v of the 64-query
+            // chunk c >> 1, at piece ^ (row & 7) (128-byte swizzle)
+            const uint32_t rowaddr = sbase + kSmemDS + (uint32_t)((c >> 1) * kChunkBytes) + (uint32_t)row * 128u;
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+                const uint32_t pc = (uint32_t)((c & 1) * 4 + v4);
+                ptx::st_shared_v4(rowaddr + ((pc ^ (uint32_t)(row & 7)) << 4), dw[ci][4 * v4], dw[ci][4 * v4 + 1],
+                                  dw[ci][4 * v4 + 2], dw[ci][4 * v4 + 3]);
+            }
+        }
+        // every S^T and dP^T column has been read by both warpgroups
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(kBarRead));
+        ok = bwd_wait(bar(kBarRead), s & 1u, kSiteRead, abort_flag, lim);
+        if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int ci = 0; ci < 2; ++ci) {
+            const int c = 2 * half + ci;
+            ptx::tmem_st16(tS + lane_off + 16u * c, pw[ci]);
+            ptx::tmem_st16(tDP + lane_off + 16u * c, dw[ci]);
+        }
+        ptx::tmem_wait_st();
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(kBarPFull));
+        return true;
+    };
 
     if (warp == kWarpTma && lane == 0) {
         // -------------------------------------------------------------------- TMA producer
@@ -225,21 +318,29 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
                 const int h = un.kvh * p.group + st % p.group;
                 const int it = un.it_lo + st / p.group;
-                if (s > 0 && !(ok = bwd_wait(bar(kBarQEmpty), (s - 1) & 1u, kSiteQEmpty, abort_flag, lim))) break;
-                ptx::mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes + 2 * kBM * 4);
+                const uint32_t sg = s % kStages;
+                // the stage's previous occupant (step s - 2) has had its last GEMM
+                if (s >= (uint32_t)kStages &&
+                    !(ok = bwd_wait(bar(kBarQEmpty + sg), ((s / kStages) - 1u) & 1u, kSiteQEmpty, abort_flag, lim)))
+                    break;
+                ptx::mbar_arrive_expect_tx(bar(kBarQFull + sg), 2 * kTileBytes);
+                const uint32_t qd = sbase + kSmemStage0 + sg * kStageBytes;
                 for (int c = 0; c < 2; ++c) {
-                    const uint32_t dq = sbase + kSmemQ + c * kChunkBytes, dd = sbase + kSmemDO + c * kChunkBytes;
+                    const uint32_t dq = qd + c * kChunkBytes, dd = qd + kTileBytes + c * kChunkBytes;
                     if (p.bshd) {
-                        ptx::tma_load_4d(dq, &qmap, bar(kBarQFull), c * 64, h, it * kBM, un.b, pol_q);
-                        ptx::tma_load_4d(dd, &domap, bar(kBarQFull), c * 64, h, it * kBM, un.b, pol_q);
+                        ptx::tma_load_4d(dq, &qmap, bar(kBarQFull + sg), c * 64, h, it * kBM, un.b, pol_q);
+                        ptx::tma_load_4d(dd, &domap, bar(kBarQFull + sg), c * 64, h, it * kBM, un.b, pol_q);
                     } else {
-                        ptx::tma_load_4d(dq, &qmap, bar(kBarQFull), c * 64, it * kBM, h, un.b, pol_q);
-                        ptx::tma_load_4d(dd, &domap, bar(kBarQFull), c * 64, it * kBM, h, un.b, pol_q);
+                        ptx::tma_load_4d(dq, &qmap, bar(kBarQFull + sg), c * 64, it * kBM, h, un.b, pol_q);
+                        ptx::tma_load_4d(dd, &domap, bar(kBarQFull + sg), c * 64, it * kBM, h, un.b, pol_q);
                     }
                 }
+                // the statistics buffer is free once the previous step's P^T/dS^T are done
+                if (s > 0 && !(ok = bwd_wait(bar(kBarPFull), (s - 1) & 1u, kSitePFull, abort_flag, lim))) break;
+                ptx::mbar_arrive_expect_tx(bar(kBarStats), 2 * kBM * 4);
                 const long long srow = ((long long)un.b * p.H + h) * p.nq_pad_rows + (long long)it * kBM;
-                ptx::bulk_load_1d(sbase + kSmemStats, p.lse2 + srow, kBM * 4, bar(kBarQFull));
-                ptx::bulk_load_1d(sbase + kSmemStats + kBM * 4, p.delta + srow, kBM * 4, bar(kBarQFull));
+                ptx::bulk_load_1d(sbase + kSmemStats, p.lse2 + srow, kBM * 4, bar(kBarStats));
+                ptx::bulk_load_1d(sbase + kSmemStats + kBM * 4, p.delta + srow, kBM * 4, bar(kBarStats));
                 ++q_issued;
             }
         }
@@ -249,9 +350,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             while (!ptx::mbar_try_wait(bar(kBarKV), (u - 1) & 1u) && ptx::globaltimer_ns() - t0 < lim) {
             }
         }
+        for (uint32_t n = (q_issued > (uint32_t)kStages ? q_issued - kStages : 0u); n < q_issued; ++n) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(bar(kBarQFull + n % kStages), (n / kStages) & 1u) &&
+                   ptx::globaltimer_ns() - t0 < lim) {
+            }
+        }
         if (q_issued > 0) {
             const uint64_t t0 = ptx::globaltimer_ns();
-            while (!ptx::mbar_try_wait(bar(kBarQFull), (s - 1) & 1u) && ptx::globaltimer_ns() - t0 < lim) {
+            while (!ptx::mbar_try_wait(bar(kBarStats), (s - 1) & 1u) && ptx::globaltimer_ns() - t0 < lim) {
             }
         }
     } else if (warp == kWarpMma && lane == 0) {
@@ -260,9 +367,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         constexpr uint32_t idesc_o = idesc_bf16(kBN, kD, false, true);     // TMEM A x MN-major B
         constexpr uint32_t idesc_q = idesc_bf16(kBM, kD, true, true);      // MN-major A x MN-major B
         const uint64_t dK_k = sdesc(sbase + kSmemK, 16, 1024), dV_k = sdesc(sbase + kSmemV, 16, 1024);
-        const uint64_t dQ_k = sdesc(sbase + kSmemQ, 16, 1024), dDO_k = sdesc(sbase + kSmemDO, 16, 1024);
-        const uint64_t dQ_mn = sdesc(sbase + kSmemQ, kChunkBytes, 1024);
-        const uint64_t dDO_mn = sdesc(sbase + kSmemDO, kChunkBytes, 1024);
+        // stage 0's Q and dO; stage 1 is kStageBytes further (added to the address field)
+        const uint64_t dQ_k = sdesc(sbase + kSmemStage0, 16, 1024);
+        const uint64_t dDO_k = sdesc(sbase + kSmemStage0 + kTileBytes, 16, 1024);
+        const uint64_t dQ_mn = sdesc(sbase + kSmemStage0, kChunkBytes, 1024);
+        const uint64_t dDO_mn = sdesc(sbase + kSmemStage0 + kTileBytes, kChunkBytes, 1024);
         const uint64_t dDS_mn = sdesc(sbase + kSmemDS, kChunkBytes, 1024);
         const uint64_t dK_mn = sdesc(sbase + kSmemK, kChunkBytes, 1024);
         // D = A B^T over d: 8 K-steps of 16 (32 B inside a 64-column half, then the other half)
@@ -293,22 +402,26 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             const Unit un = decode_unit(p, k);
             if (!(ok = bwd_wait(bar(kBarKV), u & 1u, kSiteKV, abort_flag, lim))) break;
             for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
-                if (!(ok = bwd_wait(bar(kBarQFull), s & 1u, kSiteQFull, abort_flag, lim))) break;
-                // TMEM columns 0..127 hold the previous dQ until it has been read out
+                const uint32_t sg = s % kStages;
+                const uint64_t so = (uint64_t)((sg * kStageBytes) >> 4);
+                if (!(ok = bwd_wait(bar(kBarQFull + sg), (s / kStages) & 1u, kSiteQFull, abort_flag, lim))) break;
+                ptx::tc_fence_after();
+                gemm_kk(tS, dK_k, dQ_k + so);        // S^T = K_j Q_i^T
+                ptx::mma_commit(bar(kBarSFull));
+                // TMEM columns 128..255 hold the previous dQ until it has been read out
                 if (s > 0 && !(ok = bwd_wait(bar(kBarDQEmpty), (s - 1) & 1u, kSiteDQEmpty, abort_flag, lim))) break;
                 ptx::tc_fence_after();
-                gemm_kk(tS, dK_k, dQ_k);      // S^T  = K_j Q_i^T
-                gemm_kk(tDP, dV_k, dDO_k);    // dP^T = V_j dO_i^T
-                ptx::mma_commit(bar(kBarSFull));
+                gemm_kk(tDP, dV_k, dDO_k + so);      // dP^T = V_j dO_i^T
+                ptx::mma_commit(bar(kBarDPFull));
                 if (!(ok = bwd_wait(bar(kBarPFull), s & 1u, kSitePFull, abort_flag, lim))) break;
                 // the previous unit's dK, dV have been read before the first step overwrites them
                 if (st == 0 && u > 0 && !(ok = bwd_wait(bar(kBarDKVEmpty), (u - 1) & 1u, kSiteDKVEmpty, abort_flag, lim)))
                     break;
                 ptx::tc_fence_after();
-                gemm_tm(tDV, tS, dDO_mn, st > 0);    // dV += P^T dO_i
-                gemm_tm(tDK, tDP, dQ_mn, st > 0);    // dK += dS^T Q_i
-                ptx::mma_commit(bar(kBarQEmpty));
-                gemm_mm(tS, dDS_mn, dK_mn);          // dQ_i = dS K_j
+                gemm_tm(tDV, tS, dDO_mn + so, st > 0);    // dV += P^T dO_i
+                gemm_tm(tDK, tDP, dQ_mn + so, st > 0);    // dK += dS^T Q_i
+                ptx::mma_commit(bar(kBarQEmpty + sg));
+                gemm_mm(tDQ, dDS_mn, dK_mn);              // dQ_i = dS K_j
                 ptx::mma_commit(bar(kBarDQFull));
             }
             if (!ok) break;
@@ -323,60 +436,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         while (!ptx::mbar_try_wait(bar(kBarDrain), 0) && ptx::globaltimer_ns() - t0 < lim) {
         }
     } else if (warp < 4) {
-        // -------------------------------------------------------------------- P^T and dS^T
-        const int row = warp * 32 + lane;                        // key row of the tile
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const float cl = p.scale_log2;
+        // -------------------------------------------------------------------- P^T and dS^T, query columns 0..63
         uint32_t s = 0;
         bool ok = true;
         for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x) {
             const Unit un = decode_unit(p, k);
-            const int kj = un.jt * kBN + row;
-            for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
-                const int it = un.it_lo + st / p.group;
-                ok = bwd_wait(bar(kBarQFull), s & 1u, kSiteQFull, abort_flag, lim) &&
-                     bwd_wait(bar(kBarSFull), s & 1u, kSiteSFull, abort_flag, lim);
-                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-                ptx::tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t sv[32], dp[32];
-                    ptx::tmem_ld32(tS + lane_off + 32u * c, sv);
-                    ptx::tmem_ld32(tDP + lane_off + 32u * c, dp);
-                    uint32_t pw[16], dw[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float pr[2], dr[2];
-#pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            const int col = 32 * c + e + h2;
-                            const int q = it * kBM + col;
-                            const bool vis = q < p.Sq && (!p.causal || kj <= q + p.causal_off);
-                            const float x = fmaf(__uint_as_float(sv[e + h2]), cl, -s_lse2[col]);
-                            const float pp = vis ? ptx::ex2_approx(x) : 0.0f;
-                            pr[h2] = pp;
-                            dr[h2] = pp * (__uint_as_float(dp[e + h2]) - s_delta[col]);
-                        }
-                        pw[e / 2] = pack2(pr[0], pr[1]);
-                        dw[e / 2] = pack2(dr[0], dr[1]);
-                    }
-                    ptx::tmem_st16(tS + lane_off + 16u * c, pw);
-                    ptx::tmem_st16(tDP + lane_off + 16u * c, dw);
-                    // dS^T row `row`, queries 32c..32c+31: 16-byte pieces (c & 1)*4 + v of the
-                    // 64-query chunk c >> 1, at piece ^ (row & 7) (128-byte swizzle)
-                    const uint32_t rowaddr = sbase + kSmemDS + (uint32_t)((c >> 1) * kChunkBytes) + (uint32_t)row * 128u;
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        const uint32_t pc = (uint32_t)((c & 1) * 4 + v4);
-                        ptx::st_shared_v4(rowaddr + ((pc ^ (uint32_t)(row & 7)) << 4), dw[4 * v4], dw[4 * v4 + 1],
-                                          dw[4 * v4 + 2], dw[4 * v4 + 3]);
-                    }
-                }
-                ptx::tmem_wait_st();
-                ptx::fence_proxy_async_smem();
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(bar(kBarPFull));
-            }
+            for (int st = 0; st < un.nsteps && ok; ++st, ++s)
+                ok = pds_step(un, un.it_lo + st / p.group, s, 0);
         }
     } else if (warp < 8) {
         // -------------------------------------------------------------------- dQ, dK, dV out
@@ -390,26 +456,24 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
                 const int h = un.kvh * p.group + st % p.group;
                 const int q = (un.it_lo + st / p.group) * kBM + row;
+                // query columns 64..127 of this step's P^T and dS^T, then its dQ
+                if (!(ok = pds_step(un, un.it_lo + st / p.group, s, 1))) break;
                 ok = bwd_wait(bar(kBarDQFull), s & 1u, kSiteDQFull, abort_flag, lim);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 ptx::tc_fence_after();
                 float* dst = p.dq_acc + (((long long)un.b * p.H + h) * p.Sq + q) * kD;
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    ptx::tmem_ld32(tS + lane_off + 32u * c, v);
-                    if (c == 3) {
-                        ptx::tc_fence_before();
-                        ptx::mbar_arrive(bar(kBarDQEmpty));
-                    }
-                    if (q < p.Sq) {
+                // all of dQ_i into registers, release TMEM, then the reductions
+                uint32_t v[128];
+                ptx::tmem_ld128(tDQ + lane_off, v);
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(kBarDQEmpty));
+                if (q < p.Sq) {
 #pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            ptx::red_add_v4(dst + 32 * c + 4 * v4, __uint_as_float(v[4 * v4]) * p.scale,
-                                            __uint_as_float(v[4 * v4 + 1]) * p.scale,
-                                            __uint_as_float(v[4 * v4 + 2]) * p.scale,
-                                            __uint_as_float(v[4 * v4 + 3]) * p.scale);
-                    }
+                    for (int v4 = 0; v4 < 32; ++v4)
+                        ptx::red_add_v4(dst + 4 * v4, __uint_as_float(v[4 * v4]) * p.scale,
+                                        __uint_as_float(v[4 * v4 + 1]) * p.scale,
+                                        __uint_as_float(v[4 * v4 + 2]) * p.scale,
+                                        __uint_as_float(v[4 * v4 + 3]) * p.scale);
                 }
             }
             if (!ok) break;
