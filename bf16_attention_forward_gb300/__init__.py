@@ -311,7 +311,7 @@ def attn_bwd(q, k, v, o, dout, lse, layout: str = "bshd", causal: bool = False, 
              dv=None, workspace=None, stream=None):
     """Gradients (dq, dk, dv) of softmax(Q K^T / sqrt(d)) V for the upstream gradient ``dout``,
     from the forward's inputs, output ``o`` and fp32 row log-sum-exp ``lse`` ([B][H][Sq], as
-    returned by :func:`attn_fwd_ex` with ``return_lse``).  d = 128.  Returns (dq, dk, dv)."""
+    returned by :func:`attn_fwd_ex` with ``return_lse``).  d = 128 or 64.  Returns (dq, dk, dv)."""
     import torch
     if layout not in LAYOUTS:
         raise ValueError("layout must be bshd or bhsd")

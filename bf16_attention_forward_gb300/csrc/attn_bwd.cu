@@ -1,5 +1,5 @@
 // attn_bwd.cu -- attention backward for GB300 (sm_103a): dQ, dK, dV of
-// O = softmax(Q K^T / sqrt(d)) V, d = 128, on tcgen05 tensor cores, and its C ABI.
+// O = softmax(Q K^T / sqrt(d)) V, d = 128 or 64, on tcgen05 tensor cores, and its C ABI.
 //
 // Source pages: "HipKittens: Fast and Furious AMD Kernels (MLSys 2026)", "Key observations"
 // (observation 3) and "Attention backward": the attention backward is the next kernel after
@@ -43,27 +43,34 @@
 
 namespace {
 
-constexpr int kD = 128;                       // head dimension
 constexpr int kBM = 128;                      // query rows per query tile
 constexpr int kBN = 128;                      // keys per key tile (one unit)
-constexpr int kTileBytes = kBM * kD * 2;      // 32 KB: 128 rows x 128 bf16
-constexpr int kChunkBytes = kTileBytes / 2;   // 16 KB: one 64-column TMA box
+constexpr int kChunkBytes = kBM * 64 * 2;     // 16 KB: one 64-column TMA box of 128 rows
 constexpr int kThreads = 384;
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
 constexpr uint32_t kTmemCols = 512;           // S^T/P^T/dQ | dP^T/dS^T | dV | dK
 
-// shared memory map (offsets from a 1024-byte aligned base)
-constexpr int kSmemK = 0;
-constexpr int kSmemV = kSmemK + kTileBytes;
 // Q_i and dO_i go through a two-stage ring (stage s % 2 for step s) so the next query
 // tile loads while the current one is in use; each stage is Q then dO.
 constexpr int kStages = 2;
-constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kSmemStage0 = kSmemV + kTileBytes;
-constexpr int kSmemDS = kSmemStage0 + kStages * kStageBytes;   // dS^T: 128 keys x 128 queries
-constexpr int kSmemStats = kSmemDS + kTileBytes;               // base-2 LSE [128] then D [128]
-constexpr int kSmemBars = kSmemStats + 2 * kBM * 4;
+constexpr int kDSBytes = kBM * kBN * 2;       // dS^T: 128 keys x 128 queries, bf16
+
+// Head-dimension dependent geometry (D = 128 or 64); shared memory offsets are from a
+// 1024-byte aligned base.
+template <int D>
+struct BGeo {
+    static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+    static constexpr int kChunks = D / 64;                    // 64-column TMA boxes per row
+    static constexpr int kTileBytes = kBM * D * 2;            // one 128-row tile of Q, K, V or dO
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kSmemK = 0;
+    static constexpr int kSmemV = kSmemK + kTileBytes;
+    static constexpr int kSmemStage0 = kSmemV + kTileBytes;
+    static constexpr int kSmemDS = kSmemStage0 + kStages * kStageBytes;
+    static constexpr int kSmemStats = kSmemDS + kDSBytes;     // base-2 LSE [128] then D [128]
+    static constexpr int kSmemBars = kSmemStats + 2 * kBM * 4;
+};
 enum {
     kBarKV = 0,      // K_j, V_j loaded
     kBarKVEmpty,     // the unit's last GEMM reading K_j, V_j is done
@@ -81,9 +88,11 @@ enum {
     kBarDrain,
     kNumBars
 };
-constexpr int kSmemMisc = kSmemBars + kNumBars * 8;
-constexpr int kSmemUsed = kSmemMisc + 16;
-constexpr int kSmemAlloc = kSmemUsed + 1024;
+template <int D>
+__host__ __device__ constexpr int smem_misc() { return BGeo<D>::kSmemBars + kNumBars * 8; }
+template <int D>
+__host__ __device__ constexpr int smem_alloc() { return smem_misc<D>() + 16 + 1024; }
+static_assert(smem_alloc<128>() <= 232448, "shared memory over the 227 KB limit");
 
 enum : uint32_t {
     kSiteKV = 1, kSiteKVEmpty, kSiteQFull, kSiteQEmpty, kSiteSFull, kSitePFull, kSiteDQFull,
@@ -166,18 +175,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
 // fp32 -> bf16 bits, round to nearest even (the conversion instruction), NaN stays NaN
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) { return ptx::pack_bf16x2(lo, hi); }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap domap,
                 const BwdParams p) {
+    using G = BGeo<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = ptx::smem_u32(smem);
-    const uint32_t bars = sbase + kSmemBars;
+    const uint32_t bars = sbase + G::kSmemBars;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    uint32_t* tmem_holder = (uint32_t*)(smem + kSmemMisc);
-    volatile uint32_t* abort_flag = (volatile uint32_t*)(smem + kSmemMisc + 4);
-    const float* s_lse2 = (const float*)(smem + kSmemStats);
+    uint32_t* tmem_holder = (uint32_t*)(smem + smem_misc<D>());
+    volatile uint32_t* abort_flag = (volatile uint32_t*)(smem + smem_misc<D>() + 4);
+    const float* s_lse2 = (const float*)(smem + G::kSmemStats);
     const float* s_delta = s_lse2 + kBM;
 
     const int warp = threadIdx.x >> 5;
@@ -214,7 +225,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     const unsigned long long lim = p.wait_limit_ns;
     // TMEM: S^T then P^T | dP^T then dS^T, later dQ_i | dV | dK.  dQ_i goes where dP^T was, so
     // the next step's S^T GEMM does not wait for dQ_i to be read out.
-    const uint32_t tS = tmem, tDP = tmem + 128u, tDV = tmem + 256u, tDK = tmem + 384u, tDQ = tDP;
+    const uint32_t tS = tmem, tDP = tmem + 128u, tDV = tmem + 256u, tDK = tmem + 256u + (uint32_t)D, tDQ = tDP;
 
     // P^T = 2^(S^T log2(e)/sqrt(d) - LSE2) and dS^T = P^T (dP^T - D) for this thread's key row
     // and query columns 64*half .. 64*half + 63 of step s (warpgroup `half` runs it).  The
@@ -254,12 +265,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     const int col = 4 * g4 + e;
                     const float x = fmaf(__uint_as_float(sv[col]), cl, -lv[e]);
                     float pp = ptx::ex2_approx(x);
+                    float ds = pp * (__uint_as_float(dp[col]) - dv4[e]);
                     if (!all_vis) {
+                        // a masked pair takes no part: both zero, even where D is NaN (a
+                        // query with no visible key has a NaN output row)
                         const int q = q0 + col;
-                        if (!(q < p.Sq && (!p.causal || kj <= q + p.causal_off))) pp = 0.0f;
+                        if (!(q < p.Sq && (!p.causal || kj <= q + p.causal_off))) pp = ds = 0.0f;
                     }
                     pr[e] = pp;
-                    dr[e] = pp * (__uint_as_float(dp[col]) - dv4[e]);
+                    dr[e] = ds;
                 }
                 pw[ci][2 * g4] = pack2(pr[0], pr[1]);
                 pw[ci][2 * g4 + 1] = pack2(pr[2], pr[3]);
@@ -268,7 +282,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             }
             // dS^T row `row`, queries 32c..32c+31: 16-byte pieces (c & 1)*4 + v of the 64-query
             // chunk c >> 1, at piece ^ (row & 7) (128-byte swizzle)
-            const uint32_t rowaddr = sbase + kSmemDS + (uint32_t)((c >> 1) * kChunkBytes) + (uint32_t)row * 128u;
+            const uint32_t rowaddr = sbase + G::kSmemDS + (uint32_t)((c >> 1) * kChunkBytes) + (uint32_t)row * 128u;
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
                 const uint32_t pc = (uint32_t)((c & 1) * 4 + v4);
@@ -304,9 +318,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x, ++u) {
             const Unit un = decode_unit(p, k);
             if (u > 0 && !(ok = bwd_wait(bar(kBarKVEmpty), (u - 1) & 1u, kSiteKVEmpty, abort_flag, lim))) break;
-            ptx::mbar_arrive_expect_tx(bar(kBarKV), 2 * kTileBytes);
-            for (int c = 0; c < 2; ++c) {
-                const uint32_t dk = sbase + kSmemK + c * kChunkBytes, dv = sbase + kSmemV + c * kChunkBytes;
+            ptx::mbar_arrive_expect_tx(bar(kBarKV), 2 * G::kTileBytes);
+            for (int c = 0; c < G::kChunks; ++c) {
+                const uint32_t dk = sbase + G::kSmemK + c * kChunkBytes, dv = sbase + G::kSmemV + c * kChunkBytes;
                 if (p.bshd) {
                     ptx::tma_load_4d(dk, &kmap, bar(kBarKV), c * 64, un.kvh, un.jt * kBN, un.b, pol_kv);
                     ptx::tma_load_4d(dv, &vmap, bar(kBarKV), c * 64, un.kvh, un.jt * kBN, un.b, pol_kv);
@@ -323,10 +337,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 if (s >= (uint32_t)kStages &&
                     !(ok = bwd_wait(bar(kBarQEmpty + sg), ((s / kStages) - 1u) & 1u, kSiteQEmpty, abort_flag, lim)))
                     break;
-                ptx::mbar_arrive_expect_tx(bar(kBarQFull + sg), 2 * kTileBytes);
-                const uint32_t qd = sbase + kSmemStage0 + sg * kStageBytes;
-                for (int c = 0; c < 2; ++c) {
-                    const uint32_t dq = qd + c * kChunkBytes, dd = qd + kTileBytes + c * kChunkBytes;
+                ptx::mbar_arrive_expect_tx(bar(kBarQFull + sg), 2 * G::kTileBytes);
+                const uint32_t qd = sbase + G::kSmemStage0 + sg * G::kStageBytes;
+                for (int c = 0; c < G::kChunks; ++c) {
+                    const uint32_t dq = qd + c * kChunkBytes, dd = qd + G::kTileBytes + c * kChunkBytes;
                     if (p.bshd) {
                         ptx::tma_load_4d(dq, &qmap, bar(kBarQFull + sg), c * 64, h, it * kBM, un.b, pol_q);
                         ptx::tma_load_4d(dd, &domap, bar(kBarQFull + sg), c * 64, h, it * kBM, un.b, pol_q);
@@ -339,8 +353,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 if (s > 0 && !(ok = bwd_wait(bar(kBarPFull), (s - 1) & 1u, kSitePFull, abort_flag, lim))) break;
                 ptx::mbar_arrive_expect_tx(bar(kBarStats), 2 * kBM * 4);
                 const long long srow = ((long long)un.b * p.H + h) * p.nq_pad_rows + (long long)it * kBM;
-                ptx::bulk_load_1d(sbase + kSmemStats, p.lse2 + srow, kBM * 4, bar(kBarStats));
-                ptx::bulk_load_1d(sbase + kSmemStats + kBM * 4, p.delta + srow, kBM * 4, bar(kBarStats));
+                ptx::bulk_load_1d(sbase + G::kSmemStats, p.lse2 + srow, kBM * 4, bar(kBarStats));
+                ptx::bulk_load_1d(sbase + G::kSmemStats + kBM * 4, p.delta + srow, kBM * 4, bar(kBarStats));
                 ++q_issued;
             }
         }
@@ -364,20 +378,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     } else if (warp == kWarpMma && lane == 0) {
         // -------------------------------------------------------------------- MMA issuer
         constexpr uint32_t idesc_s = idesc_bf16(kBN, kBM, false, false);  // K-major x K-major
-        constexpr uint32_t idesc_o = idesc_bf16(kBN, kD, false, true);     // TMEM A x MN-major B
-        constexpr uint32_t idesc_q = idesc_bf16(kBM, kD, true, true);      // MN-major A x MN-major B
-        const uint64_t dK_k = sdesc(sbase + kSmemK, 16, 1024), dV_k = sdesc(sbase + kSmemV, 16, 1024);
-        // stage 0's Q and dO; stage 1 is kStageBytes further (added to the address field)
-        const uint64_t dQ_k = sdesc(sbase + kSmemStage0, 16, 1024);
-        const uint64_t dDO_k = sdesc(sbase + kSmemStage0 + kTileBytes, 16, 1024);
-        const uint64_t dQ_mn = sdesc(sbase + kSmemStage0, kChunkBytes, 1024);
-        const uint64_t dDO_mn = sdesc(sbase + kSmemStage0 + kTileBytes, kChunkBytes, 1024);
-        const uint64_t dDS_mn = sdesc(sbase + kSmemDS, kChunkBytes, 1024);
-        const uint64_t dK_mn = sdesc(sbase + kSmemK, kChunkBytes, 1024);
+        constexpr uint32_t idesc_o = idesc_bf16(kBN, D, false, true);     // TMEM A x MN-major B
+        constexpr uint32_t idesc_q = idesc_bf16(kBM, D, true, true);      // MN-major A x MN-major B
+        const uint64_t dK_k = sdesc(sbase + G::kSmemK, 16, 1024), dV_k = sdesc(sbase + G::kSmemV, 16, 1024);
+        // stage 0's Q and dO; stage 1 is G::kStageBytes further (added to the address field)
+        const uint64_t dQ_k = sdesc(sbase + G::kSmemStage0, 16, 1024);
+        const uint64_t dDO_k = sdesc(sbase + G::kSmemStage0 + G::kTileBytes, 16, 1024);
+        const uint64_t dQ_mn = sdesc(sbase + G::kSmemStage0, kChunkBytes, 1024);
+        const uint64_t dDO_mn = sdesc(sbase + G::kSmemStage0 + G::kTileBytes, kChunkBytes, 1024);
+        const uint64_t dDS_mn = sdesc(sbase + G::kSmemDS, kChunkBytes, 1024);
+        const uint64_t dK_mn = sdesc(sbase + G::kSmemK, kChunkBytes, 1024);
         // D = A B^T over d: 8 K-steps of 16 (32 B inside a 64-column half, then the other half)
         auto gemm_kk = [&](uint32_t d, uint64_t a, uint64_t b) {
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
+            for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t off = (uint64_t)(((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4);
                 ptx::mma_ss(d, a + off, b + off, idesc_s, kk > 0 ? 1u : 0u);
             }
@@ -403,7 +417,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             if (!(ok = bwd_wait(bar(kBarKV), u & 1u, kSiteKV, abort_flag, lim))) break;
             for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
                 const uint32_t sg = s % kStages;
-                const uint64_t so = (uint64_t)((sg * kStageBytes) >> 4);
+                const uint64_t so = (uint64_t)((sg * G::kStageBytes) >> 4);
                 if (!(ok = bwd_wait(bar(kBarQFull + sg), (s / kStages) & 1u, kSiteQFull, abort_flag, lim))) break;
                 ptx::tc_fence_after();
                 gemm_kk(tS, dK_k, dQ_k + so);        // S^T = K_j Q_i^T
@@ -461,15 +475,16 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 ok = bwd_wait(bar(kBarDQFull), s & 1u, kSiteDQFull, abort_flag, lim);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 ptx::tc_fence_after();
-                float* dst = p.dq_acc + (((long long)un.b * p.H + h) * p.Sq + q) * kD;
+                float* dst = p.dq_acc + (((long long)un.b * p.H + h) * p.Sq + q) * D;
                 // all of dQ_i into registers, release TMEM, then the reductions
-                uint32_t v[128];
-                ptx::tmem_ld128(tDQ + lane_off, v);
+                uint32_t v[D];
+                if constexpr (D == 128) ptx::tmem_ld128(tDQ + lane_off, v);
+                else ptx::tmem_ld64(tDQ + lane_off, v);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(kBarDQEmpty));
                 if (q < p.Sq) {
 #pragma unroll
-                    for (int v4 = 0; v4 < 32; ++v4)
+                    for (int v4 = 0; v4 < D / 4; ++v4)
                         ptx::red_add_v4(dst + 4 * v4, __uint_as_float(v[4 * v4]) * p.scale,
                                         __uint_as_float(v[4 * v4 + 1]) * p.scale,
                                         __uint_as_float(v[4 * v4 + 2]) * p.scale,
@@ -487,7 +502,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 __nv_bfloat16* out = (which ? p.dk : p.dv) + off;
                 const float sc = which ? p.scale : 1.0f;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t v[32];
                     if (un.nsteps > 0) {
                         ptx::tmem_ld32((which ? tDK : tDV) + lane_off + 32u * c, v);
@@ -521,6 +536,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
 
 // D_i = dO_i . O_i in fp32 and the base-2 log-sum-exp, one warp per padded query row;
 // rows past Sq get zeros.
+template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout,
                                                             const float* lse, float* lse2, float* delta, int H,
                                                             int Sq, int nq_pad_rows, long long rows,
@@ -533,13 +549,12 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __nv_bfloat16*
     const int b = (int)(bh / H), h = (int)(bh % H);
     float acc = 0.0f;
     if (q < Sq) {
-        const long long off = (long long)b * o_sb + (long long)q * o_ss + (long long)h * o_sh + lane * 4;
-        const uint2 ov = *reinterpret_cast<const uint2*>(o + off);
-        const uint2 gv = *reinterpret_cast<const uint2*>(dout + off);
-        const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
-        const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gv);
+        constexpr int kE = D / 32;     // elements per lane: 4 or 2
+        const long long off = (long long)b * o_sb + (long long)q * o_ss + (long long)h * o_sh + lane * kE;
+        const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(o + off);
+        const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(dout + off);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
+        for (int e = 0; e < kE / 2; ++e) {
             const float2 of = __bfloat1622float2(op[e]), gf = __bfloat1622float2(gp[e]);
             acc = fmaf(of.x, gf.x, acc);
             acc = fmaf(of.y, gf.y, acc);
@@ -554,17 +569,18 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __nv_bfloat16*
 }
 
 // dq (bf16, the caller's layout) = dq_acc (fp32 [B][H][Sq][d]), round to nearest even.
+template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const float* dq_acc, __nv_bfloat16* dq, int H, int Sq,
                                                           long long n4, long long o_sb, long long o_ss,
                                                           long long o_sh) {
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // group of 4 columns
     if (i >= n4) return;
-    const long long row = i / (kD / 4);
-    const int x = (int)(i % (kD / 4)) * 4;
+    const long long row = i / (D / 4);
+    const int x = (int)(i % (D / 4)) * 4;
     const int q = (int)(row % Sq);
     const long long bh = row / Sq;
     const int h = (int)(bh % H), b = (int)(bh / H);
-    const float4 v = *reinterpret_cast<const float4*>(dq_acc + row * kD + x);
+    const float4 v = *reinterpret_cast<const float4*>(dq_acc + row * D + x);
     __nv_bfloat16* dst = dq + (long long)b * o_sb + (long long)q * o_ss + (long long)h * o_sh + x;
     *reinterpret_cast<uint2*>(dst) = make_uint2(pack2(v.x, v.y), pack2(v.z, v.w));
 }
@@ -576,17 +592,17 @@ bool g_bwd_attr[64] = {};
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-bool encode(CUtensorMap* m, const void* ptr, int64_t B, int64_t H, int64_t S, bool bshd) {
+bool encode(CUtensorMap* m, const void* ptr, int64_t B, int64_t H, int64_t S, int64_t d, bool bshd) {
     cuuint64_t dims[4], strides[3];
     cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
-    dims[0] = kD;
+    dims[0] = (cuuint64_t)d;
     if (bshd) {
         dims[1] = H; dims[2] = S; dims[3] = B;
-        strides[0] = kD * 2; strides[1] = H * kD * 2; strides[2] = S * H * kD * 2;
+        strides[0] = d * 2; strides[1] = H * d * 2; strides[2] = S * H * d * 2;
         box[0] = 64; box[1] = 1; box[2] = kBM; box[3] = 1;
     } else {
         dims[1] = S; dims[2] = H; dims[3] = B;
-        strides[0] = kD * 2; strides[1] = S * kD * 2; strides[2] = H * S * kD * 2;
+        strides[0] = d * 2; strides[1] = S * d * 2; strides[2] = H * S * d * 2;
         box[0] = 64; box[1] = kBM; box[2] = 1; box[3] = 1;
     }
     return g_bwd_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -599,7 +615,7 @@ int check_shape(const attn_bwd_args_t& a) {
     if (a.H % a.Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (a.layout != ATTN_LAYOUT_BSHD && a.layout != ATTN_LAYOUT_BHSD) return ATTN_ERR_INVALID_ARG;
     if ((a.causal != 0 && a.causal != 1) || a.reserved0 != 0 || a.reserved1 != 0) return ATTN_ERR_INVALID_ARG;
-    if (a.d != kD) return ATTN_ERR_UNSUPPORTED;
+    if (a.d != 128 && a.d != 64) return ATTN_ERR_UNSUPPORTED;
     const int64_t lim = (int64_t)1 << 30;
     if (a.Sq > lim || a.Skv > lim || a.B * a.H > lim || a.B * a.Hkv * cdiv(a.Skv, kBN) > lim ||
         a.B * a.H * cdiv(a.Sq, kBM) * kBM > lim)
@@ -609,7 +625,7 @@ int check_shape(const attn_bwd_args_t& a) {
 
 size_t ws_bytes(const attn_bwd_args_t& a) {
     const int64_t rows_pad = a.B * a.H * cdiv(a.Sq, kBM) * kBM;
-    return (size_t)(a.B * a.H * a.Sq * kD * 4) + (size_t)(2 * rows_pad * 4);
+    return (size_t)(a.B * a.H * a.Sq * a.d * 4) + (size_t)(2 * rows_pad * 4);
 }
 
 }  // namespace
@@ -633,7 +649,7 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     const size_t need = ws_bytes(a);
     if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
     // the gradients must not overlap the inputs or each other
-    const uintptr_t qb = (uintptr_t)(a.B * a.H * a.Sq * kD * 2), kb = (uintptr_t)(a.B * a.Hkv * a.Skv * kD * 2);
+    const uintptr_t qb = (uintptr_t)(a.B * a.H * a.Sq * a.d * 2), kb = (uintptr_t)(a.B * a.Hkv * a.Skv * a.d * 2);
     const uintptr_t outs[3][2] = {{(uintptr_t)a.dq, qb}, {(uintptr_t)a.dk, kb}, {(uintptr_t)a.dv, kb}};
     const uintptr_t ins[6][2] = {{(uintptr_t)a.q, qb}, {(uintptr_t)a.k, kb}, {(uintptr_t)a.v, kb},
                                  {(uintptr_t)a.o, qb}, {(uintptr_t)a.dout, qb}, {(uintptr_t)workspace, need}};
@@ -665,16 +681,19 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
             g_bwd_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
         }
         if (!g_bwd_attr[dev]) {
-            if (cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
-                cudaSuccess)
+            if (cudaFuncSetAttribute(attn_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     smem_alloc<128>()) != cudaSuccess ||
+                cudaFuncSetAttribute(attn_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     smem_alloc<64>()) != cudaSuccess)
                 return ATTN_ERR_CUDA;
             g_bwd_attr[dev] = true;
         }
     }
     const bool bshd = a.layout == ATTN_LAYOUT_BSHD;
     CUtensorMap qm, km, vm, dom;
-    if (!encode(&qm, a.q, a.B, a.H, a.Sq, bshd) || !encode(&km, a.k, a.B, a.Hkv, a.Skv, bshd) ||
-        !encode(&vm, a.v, a.B, a.Hkv, a.Skv, bshd) || !encode(&dom, a.dout, a.B, a.H, a.Sq, bshd))
+    const int64_t d = a.d;
+    if (!encode(&qm, a.q, a.B, a.H, a.Sq, d, bshd) || !encode(&km, a.k, a.B, a.Hkv, a.Skv, d, bshd) ||
+        !encode(&vm, a.v, a.B, a.Hkv, a.Skv, d, bshd) || !encode(&dom, a.dout, a.B, a.H, a.Sq, d, bshd))
         return ATTN_ERR_CUDA;
 
     BwdParams p;
@@ -688,10 +707,10 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     p.causal = a.causal;
     p.causal_off = (int)(a.Skv - a.Sq);
     p.bshd = bshd ? 1 : 0;
-    p.scale = (float)(1.0 / std::sqrt((double)kD));
-    p.scale_log2 = (float)((1.0 / std::sqrt((double)kD)) * 1.4426950408889634);
+    p.scale = (float)(1.0 / std::sqrt((double)d));
+    p.scale_log2 = (float)((1.0 / std::sqrt((double)d)) * 1.4426950408889634);
     float* dq_acc = reinterpret_cast<float*>(workspace);
-    float* lse2 = dq_acc + a.B * a.H * a.Sq * kD;
+    float* lse2 = dq_acc + a.B * a.H * a.Sq * d;
     float* delta = lse2 + a.B * a.H * p.nq_pad_rows;
     p.lse2 = lse2;
     p.delta = delta;
@@ -700,27 +719,32 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
     long long q_sb, q_ss, q_sh;
     if (bshd) {
-        p.kv_sb = a.Skv * a.Hkv * kD; p.kv_ss = a.Hkv * kD; p.kv_sh = kD;
-        q_sb = a.Sq * a.H * kD; q_ss = a.H * kD; q_sh = kD;
+        p.kv_sb = a.Skv * a.Hkv * d; p.kv_ss = a.Hkv * d; p.kv_sh = d;
+        q_sb = a.Sq * a.H * d; q_ss = a.H * d; q_sh = d;
     } else {
-        p.kv_sb = a.Hkv * a.Skv * kD; p.kv_ss = kD; p.kv_sh = a.Skv * kD;
-        q_sb = a.H * a.Sq * kD; q_ss = kD; q_sh = a.Sq * kD;
+        p.kv_sb = a.Hkv * a.Skv * d; p.kv_ss = d; p.kv_sh = a.Skv * d;
+        q_sb = a.H * a.Sq * d; q_ss = d; q_sh = a.Sq * d;
     }
     p.wait_limit_ns = 2000ull * 1000000ull;
 
-    if (cudaMemsetAsync(dq_acc, 0, (size_t)(a.B * a.H * a.Sq * kD * 4), stream) != cudaSuccess) {
+    if (cudaMemsetAsync(dq_acc, 0, (size_t)(a.B * a.H * a.Sq * d * 4), stream) != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_CUDA;
     }
     const long long prows = a.B * a.H * (long long)p.nq_pad_rows;
-    attn_bwd_prep_kernel<<<(unsigned)cdiv(prows, 8), 256, 0, stream>>>(
+    auto prep = d == 128 ? attn_bwd_prep_kernel<128> : attn_bwd_prep_kernel<64>;
+    prep<<<(unsigned)cdiv(prows, 8), 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16*>(a.o), reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, lse2,
         delta, p.H, p.Sq, p.nq_pad_rows, prows, q_sb, q_ss, q_sh);
     const int grid = p.n_units < sms ? p.n_units : sms;
-    attn_bwd_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(qm, km, vm, dom, p);
-    const long long n4 = a.B * a.H * a.Sq * (kD / 4);
-    attn_bwd_dq_kernel<<<(unsigned)cdiv(n4, 256), 256, 0, stream>>>(dq_acc, reinterpret_cast<__nv_bfloat16*>(a.dq),
-                                                                    p.H, p.Sq, n4, q_sb, q_ss, q_sh);
+    if (d == 128)
+        attn_bwd_kernel<128><<<(unsigned)grid, kThreads, smem_alloc<128>(), stream>>>(qm, km, vm, dom, p);
+    else
+        attn_bwd_kernel<64><<<(unsigned)grid, kThreads, smem_alloc<64>(), stream>>>(qm, km, vm, dom, p);
+    const long long n4 = a.B * a.H * a.Sq * (d / 4);
+    auto conv = d == 128 ? attn_bwd_dq_kernel<128> : attn_bwd_dq_kernel<64>;
+    conv<<<(unsigned)cdiv(n4, 256), 256, 0, stream>>>(dq_acc, reinterpret_cast<__nv_bfloat16*>(a.dq), p.H, p.Sq, n4,
+                                                      q_sb, q_ss, q_sh);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
 }

@@ -218,7 +218,7 @@ const char* attn_status_string(int status);
 int attn_version(void);
 
 /*
- * Attention backward (d = 128): the gradients of O = softmax(Q K^T / sqrt(d)) V with respect
+ * Attention backward (d = 128 or 64): the gradients of O = softmax(Q K^T / sqrt(d)) V with respect
  * to Q, K and V, with the causal mask and grouped K/V heads as in attn_fwd_ex.  Source:
  * "HipKittens: Fast and Furious AMD Kernels (MLSys 2026)", "Key observations" (observation 3)
  * and "Attention backward" -- the backward is the kernel after the forward.  With
@@ -230,7 +230,8 @@ int attn_version(void);
  *   dq, dk, dv   outputs, bf16, like q, k, v (round to nearest even); must not overlap the
  *                inputs, each other or the workspace
  *   causal       0 or 1, as in the forward;  reserved0, reserved1 must be 0
- * Rows of K/V that no query sees get zero gradients.  Inputs are expected finite.
+ * Rows of K/V that no query sees, and queries that see no key (causal, Sq > Skv; their
+ * forward output is NaN), get zero gradients.  Inputs are expected finite.
  */
 typedef struct {
     const void* q;

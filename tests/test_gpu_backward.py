@@ -1,4 +1,5 @@
-"""GPU parity of the attention backward (attn_bwd) against the fp64 backward oracle.
+"""GPU parity of the attention backward (attn_bwd, d = 128 and 64) against the fp64 backward
+oracle.
 
 The GPU path recomputes P from the forward's fp32 log-sum-exp, rounds P and dS to bf16
 before the tensor-core products, and forms D from the forward's bf16 output, so an element
@@ -78,7 +79,7 @@ def test_backward_matches_oracle(attn, shape, layout):
     check_bwd(attn, q, k, v, g, layout)
 
 
-@pytest.mark.parametrize("Sq,Skv", [(300, 300), (200, 456), (456, 200), (640, 640)])
+@pytest.mark.parametrize("Sq,Skv", [(300, 300), (200, 456), (456, 200), (640, 640), (300, 200)])
 def test_backward_causal(attn, Sq, Skv):
     q, k, v = make_qkv(1, 4, Sq, Skv, 128, "bshd", seed=5200 + Sq, Hkv=2)
     g = make_qkv(1, 4, Sq, 1, 128, "bshd", seed=5300 + Skv)[0]
@@ -101,7 +102,16 @@ def test_backward_argument_errors(attn):
         attn.attn_bwd(q, k, v, o, o, lse[:, :, :4].contiguous())
     with pytest.raises(attn.AttnError):           # the gradient may not alias an input
         attn.attn_bwd(q, k, v, o, o, lse, dq=q)
-    q64, k64, v64 = (t.cuda() for t in make_qkv(1, 1, 8, 8, 64, "bshd", seed=2))
-    o64, l64 = attn.attn_fwd_ex(q64, k64, v64, return_lse=True)
-    with pytest.raises(attn.AttnError):           # d = 64 has no backward kernel
-        attn.attn_bwd(q64, k64, v64, o64, o64, l64)
+    q96, k96, v96 = (t.cuda() for t in make_qkv(1, 1, 8, 8, 96, "bshd", seed=2))
+    l96 = torch.zeros(8, device="cuda")
+    with pytest.raises(attn.AttnError):           # head dimension 96 is not supported
+        attn.attn_bwd(q96, k96, v96, q96, q96, l96)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("layout", ["bshd", "bhsd"])
+def test_backward_head_dim_64(attn, causal, layout):
+    for (B, H, Hkv, Sq, Skv) in ((1, 2, 2, 300, 200), (2, 4, 1, 129, 257)):
+        q, k, v = make_qkv(B, H, Sq, Skv, 64, layout, seed=5500 + Sq, Hkv=Hkv)
+        g = make_qkv(B, H, Sq, 1, 64, layout, seed=5600 + Skv)[0]
+        check_bwd(attn, q, k, v, g, layout, causal=causal)
