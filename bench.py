@@ -102,10 +102,10 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, kernel: str = "attn_fwd_kernel"):
     """DRAM bytes per launch of the attention kernel from the committed ncu summary, if it
     was taken on the current kernel source; otherwise None."""
-    path = os.path.join(ROOT, "profiles", "attn_fwd_kernel_%s_traffic.md" % workload)
+    path = os.path.join(ROOT, "profiles", "%s_%s_traffic.md" % (kernel, workload))
     try:
         lines = open(path).read().splitlines()
     except OSError:
@@ -414,14 +414,30 @@ def main():
     peak, peak_sust, hbm, peak_src = measured_peaks()
     main_avg = statistics.mean(main_ms)
     achieved = flop_call / (main_avg * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": recorded_traffic(w.name),
-                "kernel": "attn_fwd_kernel", "peak_source": peak_src + " burst bf16 (cuBLAS)",
-                "frac_of_sustained": (achieved / peak_sust) if peak_sust else None,
-                "kernel_ms_avg": main_avg, "kernel_ms_median": statistics.median(main_ms)}
+    # the kernel that runs: one 128-row query tile per (b, h) takes the short-query kernel
+    kernel = "attn_fwd_short_kernel" if w.Sq <= 128 else "attn_fwd_kernel"
+    # the bound is the roofline the workload's arithmetic intensity (FLOP per algorithmic
+    # byte) meets first: below the ridge (peak FLOP/s over HBM bytes/s) it is HBM
+    intensity = flop_call / w.min_bytes
+    ridge = peak * 1e12 / (hbm * 1e9)
+    if intensity < ridge:
+        achieved_gbs = w.min_bytes / (main_avg * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
+                    "frac": achieved_gbs / hbm, "traffic": recorded_traffic(w.name, kernel),
+                    "peak_source": peak_src + " HBM copy",
+                    "tensor_tflops": achieved, "tensor_frac": achieved / peak}
+    else:
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": recorded_traffic(w.name, kernel),
+                    "peak_source": peak_src + " burst bf16 (cuBLAS)",
+                    "frac_of_sustained": (achieved / peak_sust) if peak_sust else None}
+    roofline.update({"kernel": kernel, "algorithmic_bytes": w.min_bytes, "flop_per_launch": flop_call,
+                     "intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
+                     "kernel_ms_avg": main_avg, "kernel_ms_median": statistics.median(main_ms)})
     extra = {}
     if split:
-        rows = plan["split_units"] * 256
+        # workspace rows that hold real queries: 256 per split unit, Sq when that is fewer
+        rows = plan["split_units"] * min(256, w.Sq)
         comb_bytes = rows * plan["splits"] * (128 * 4 + 4) + min(rows, w.B * w.H * w.Sq) * 256
         ca = statistics.mean(comb_ms)
         extra["combine"] = {"ms_avg": ca, "algorithmic_bytes": comb_bytes,

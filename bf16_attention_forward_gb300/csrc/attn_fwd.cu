@@ -30,7 +30,9 @@
 //     idea on tcgen05);
 //   * tail units that would leave SMs idle in the last round are split along the keys;
 //     each split writes fp32 O/l and a base-2 log-sum-exp, and a combine kernel merges them;
-//   * the kernel is a template on the head dimension and on the causal mask.  The causal
+//   * for Sq <= 128 (one query tile per (b, h)) a second kernel, attn_fwd_short_kernel, runs
+//     the same work items without the empty second tile (see "short queries" below);
+//   * the kernels are templates on the head dimension and on the causal mask.  The causal
 //     mask and grouped K/V heads are the features the [MoonMath] limitations paragraph lists
 //     as missing; d = 64 is the second tile configuration of "HipKittens: Fast and Furious
 //     AMD Kernels (MLSys 2026)", "Experiments and results".
@@ -104,7 +106,7 @@ struct Geo {
 // wait sites reported through the status word
 enum : uint32_t {
     kSiteQEmpty = 1, kSiteRingEmpty, kSiteQFull, kSiteRingFull, kSitePFull, kSiteSFull,
-    kSiteOFull, kSiteDrain, kSiteTeardown
+    kSiteOFull, kSiteDrain, kSiteTeardown, kSitePVDone, kSiteOEmpty, kSiteStats
 };
 
 __device__ uint32_t g_status[2];   // [0] status code, [1] wait site
@@ -654,6 +656,507 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     }
 }
 
+// ------------------------------------------------------------------------- short queries
+// For Sq <= 128 every (b, h) has a single 128-row query tile, which the kernel above would run
+// beside an empty second tile.  attn_fwd_short_kernel takes that one tile as its unit (same
+// work items, planner, key splits and workspace rows as above; the unit's rows 128..255 do
+// not exist) and keeps the tensor core busy without a second tile:
+//   * two S buffers in TMEM, so S_{g+1} = Q K_{g+1}^T is computed while the softmax of step g
+//     runs (P_g overwrites S_g in place);
+//   * warpgroups 0 and 1 each own one 64-key half of every key tile: an online softmax of its
+//     own (running max m_h, sum l_h) into its own accumulator O_h;
+//   * warpgroup 2 merges the halves, O = (w_a O_a + w_b O_b) / (w_a l_a + w_b l_b) with
+//     w_h = 2^((m_h - m) c) (the combine kernel's clamped rule), and runs the epilogue;
+//   * warp 12 streams Q and K_g, V_g into step slot g & 1; warp 14 issues the S GEMMs and
+//     warp 13 the PV GEMMs, two issuing threads on different sub-partitions (a single
+//     thread's tcgen05.mma issue rate is what bounds these pipelines).
+// TMEM: S buffer 0 | S buffer 1 | O_a | O_b.
+namespace sq {
+constexpr int kHalfN = kBN / 2;    // keys of a tile that one softmax warpgroup owns
+constexpr int kThreads = 512;      // 128 registers per thread
+constexpr int kWarpEpi = 8;        // warps 8-11: merge and epilogue
+constexpr int kWarpTma = 12;
+constexpr int kWarpMma = 13;       // PV GEMMs (and TMEM allocation)
+constexpr int kWarpMmaS = 14;      // S GEMMs
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct Geo {
+    static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+    static constexpr int kChunks = D / 64;                    // 64-column TMA boxes per row
+    static constexpr int kTileBytes = kBM * D * 2;            // one 128-row tile of Q, K or V
+    static constexpr int kStepSlots = 2;                      // K_g and V_g go to step slot g & 1
+    static constexpr int kSmemQ = 0;                          // [2] query tiles, by unit parity
+    static constexpr int kSmemRing = kSmemQ + 2 * kTileBytes;
+    static constexpr int kSmemStage = kSmemRing + kStepSlots * 2 * kTileBytes;
+    static constexpr int kSmemStats = kSmemStage + 4 * kStageBytes;   // [2 unit parity][2 halves][128] (m, l)
+    static constexpr int kSmemBars = kSmemStats + 2 * 2 * kBM * 8;
+    // barrier indices
+    static constexpr int kBarKFull = 0;               // [step slot] K_g loaded
+    static constexpr int kBarVFull = 2;               // [step slot] V_g loaded
+    static constexpr int kBarQFull = 4;               // [2] query buffer loaded
+    static constexpr int kBarQEmpty = kBarQFull + 2;  // [2] query buffer's last S GEMM done
+    static constexpr int kBarSFull = kBarQEmpty + 2;  // [S buffer] S_g done (and K_g's slot free)
+    static constexpr int kBarPFull = kBarSFull + 2;   // [S buffer] P_g written by both halves (and O rescaled)
+    static constexpr int kBarPVDone = kBarPFull + 2;  // [S buffer] PV_g done (P_g read, V_g's slot free)
+    static constexpr int kBarOFull = kBarPVDone + 2;  // the unit's last PV GEMMs done
+    static constexpr int kBarOEmpty = kBarOFull + 1;  // the epilogue has read O_a and O_b
+    static constexpr int kBarStats = kBarOEmpty + 1;  // [unit parity] both halves' (m, l) written
+    static constexpr int kBarDrain = kBarStats + 2;
+    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kSmemMisc = kSmemBars + kNumBars * 8;
+    static constexpr int kSmemUsed = kSmemMisc + 16;
+    static constexpr int kSmemAlloc = kSmemUsed + 1024;
+    static_assert(kSmemAlloc <= 232448, "shared memory over the 227 KB limit");
+};
+}  // namespace sq
+
+template <int D, bool kCausal>
+__global__ void __launch_bounds__(sq::kThreads, 1)
+attn_fwd_short_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                const FwdParams p) {
+    using G = sq::Geo<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const uint32_t bars = sbase + G::kSmemBars;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    uint32_t* tmem_holder = (uint32_t*)(smem + G::kSmemMisc);
+    volatile uint32_t* abort_flag = (volatile uint32_t*)(smem + G::kSmemMisc + 4);
+    float2* stats = (float2*)(smem + G::kSmemStats);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(bar(G::kBarKFull + i), 1);
+            ptx::mbar_init(bar(G::kBarVFull + i), 1);
+            ptx::mbar_init(bar(G::kBarQFull + i), 1);
+            ptx::mbar_init(bar(G::kBarQEmpty + i), 1);
+            ptx::mbar_init(bar(G::kBarSFull + i), 1);
+            ptx::mbar_init(bar(G::kBarPFull + i), 2 * kBM);
+            ptx::mbar_init(bar(G::kBarPVDone + i), 1);
+            ptx::mbar_init(bar(G::kBarStats + i), 2 * kBM);
+        }
+        ptx::mbar_init(bar(G::kBarOFull), 1);
+        ptx::mbar_init(bar(G::kBarOEmpty), kBM);
+        ptx::mbar_init(bar(G::kBarDrain), 2);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+    }
+    if (warp == sq::kWarpMma) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), sq::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const unsigned long long lim = p.wait_limit_ns;
+    // the split-combine kernel may be scheduled as CTAs retire; it waits for this grid's memory
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (warp == sq::kWarpTma) {
+        if (lane == 0) {
+            // -------------------------------------------------------------- TMA producer
+            // Per unit: its query tile into buffer u & 1 (once the unit two back has had its
+            // last S GEMM), then K_j, V_j for each key tile through the ring.
+            const uint64_t pol_kv = ptx::policy_evict_last();
+            const uint64_t pol_q = ptx::policy_evict_first();
+            uint32_t g = 0;               // step index (monotonic over the CTA's units)
+            int u = 0;
+            bool ok = true;
+            for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
+                const Item it = decode_item<kCausal>(p, k);
+                const int qb = u & 1;
+                if (u >= 2 &&
+                    !(ok = wait_bar(bar(G::kBarQEmpty + qb), ((u >> 1) - 1) & 1, kSiteQEmpty, abort_flag, lim)))
+                    break;
+                ptx::mbar_arrive_expect_tx(bar(G::kBarQFull + qb), G::kTileBytes);
+                const int row = it.qb * kUnitRows;
+                for (int c = 0; c < G::kChunks; ++c) {
+                    const uint32_t dst = sbase + G::kSmemQ + qb * G::kTileBytes + c * kChunkBytes;
+                    if (p.bshd)
+                        ptx::tma_load_4d(dst, &qmap, bar(G::kBarQFull + qb), c * 64, it.h, row, it.b, pol_q);
+                    else
+                        ptx::tma_load_4d(dst, &qmap, bar(G::kBarQFull + qb), c * 64, row, it.h, it.b, pol_q);
+                }
+                for (int j = it.kv_begin; j < it.kv_end && ok; ++j, ++g) {
+                    // K_g into step slot g & 1 once S_{g-2} has read it, V_g once PV_{g-2} has
+                    const uint32_t ss = g & 1u, ph = ((g - 2u) >> 1) & 1u;
+                    for (int kv = 0; kv < 2 && ok; ++kv) {
+                        if (g >= 2u && !(ok = wait_bar(bar((kv ? G::kBarPVDone : G::kBarSFull) + (int)ss), ph,
+                                                       kSiteRingEmpty, abort_flag, lim)))
+                            break;
+                        const uint32_t full = bar((kv ? G::kBarVFull : G::kBarKFull) + (int)ss);
+                        ptx::mbar_arrive_expect_tx(full, G::kTileBytes);
+                        const void* map = kv ? (const void*)&vmap : (const void*)&kmap;
+                        const uint32_t base = sbase + G::kSmemRing + (2u * ss + (uint32_t)kv) * G::kTileBytes;
+                        for (int c = 0; c < G::kChunks; ++c) {
+                            const uint32_t dst = base + c * kChunkBytes;
+                            if (p.bshd)
+                                ptx::tma_load_4d(dst, map, full, c * 64, it.hk, j * kBN, it.b, pol_kv);
+                            else
+                                ptx::tma_load_4d(dst, map, full, c * 64, j * kBN, it.hk, it.b, pol_kv);
+                        }
+                    }
+                }
+            }
+            // every load issued has landed before the CTA may exit: the last two steps' loads
+            for (uint32_t q = (g > 2u ? g - 2u : 0u); q < g; ++q) {
+                for (int kv = 0; kv < 2; ++kv) {
+                    const uint64_t t0 = ptx::globaltimer_ns();
+                    while (!ptx::mbar_try_wait(bar((kv ? G::kBarVFull : G::kBarKFull) + (int)(q & 1u)), (q >> 1) & 1u) &&
+                           ptx::globaltimer_ns() - t0 < lim) {
+                    }
+                }
+            }
+        }
+    } else if ((warp == sq::kWarpMma || warp == sq::kWarpMmaS) && lane == 0) {
+        // ------------------------------------------------------------------ MMA issuers
+        // Two threads on different sub-partitions: this one issues the S GEMMs, warp 13's
+        // the PV GEMMs.  The CTA's steps (one per key tile of each of its units) run in
+        // order g = 0, 1, ...: K_g is ring position 2g, V_g position 2g + 1, S_g goes to S
+        // buffer g & 1, and P_g overwrites it.  S_g may be issued once PV_{g-2} (the last
+        // reader of that buffer) is done, so the next tile's logits are ready when the
+        // softmax finishes P_{g-1}, also across a unit boundary.
+        constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false, false);
+        constexpr uint32_t idesc_o = idesc_bf16(kBM, D, false, true);
+        // Q_u / K_j: K-major, 128 B rows, 8-row swizzle atoms 1024 B apart; the k-th 16-element
+        // step sits 32 B further inside the atom, the second 64-column half 16 KB further.
+        // V_j: MN-major (d contiguous), the two 64-column halves 16 KB apart (leading offset),
+        // 8-key groups 1024 B apart (stride offset); the k-th 16-key step is 2 KB further.
+        // The address field counts 16-byte units, so moving the start address by b bytes adds
+        // b >> 4 to the descriptor (no carry out of the field: every address stays below 256 KB).
+        const uint64_t dq0 = sdesc(sbase + G::kSmemQ, 16, 1024);
+        const uint64_t dring = sdesc(sbase + G::kSmemRing, 16, 1024);
+        const uint64_t dvring = sdesc(sbase + G::kSmemRing, kChunkBytes, 1024);
+        bool ok = true;
+        uint32_t g = 0;
+        int u = 0;
+        if (warp == sq::kWarpMmaS) {
+            for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
+                const Item it = decode_item<kCausal>(p, k);
+                const int nk = it.kv_end - it.kv_begin;
+                const int qbuf = u & 1;
+                if (!(ok = wait_bar(bar(G::kBarQFull + qbuf), (uint32_t)(u >> 1) & 1u, kSiteQFull, abort_flag, lim)))
+                    break;
+                for (int jj = 0; jj < nk; ++jj, ++g) {
+                    const uint32_t sb = g & 1u;
+                    if (!(ok = wait_bar(bar(G::kBarKFull + (int)sb), (g >> 1) & 1u, kSiteRingFull, abort_flag, lim)))
+                        break;
+                    // the PV GEMMs of step g - 2 have read their P from this buffer
+                    if (g >= 2u &&
+                        !(ok = wait_bar(bar(G::kBarPVDone + (int)sb), ((g - 2u) >> 1) & 1u, kSitePVDone, abort_flag, lim)))
+                        break;
+                    ptx::tc_fence_after();
+                    // S = Q K^T: D/16 steps of 16 along d, fully unrolled with constant offsets
+                    // from one base descriptor per operand (a rolled loop that recomputes
+                    // descriptors costs ~200 cycles per MMA in issue)
+                    const uint64_t a0 = dq0 + (uint64_t)((qbuf * G::kTileBytes) >> 4);
+                    const uint64_t b0 = dring + (uint64_t)((2u * sb * G::kTileBytes) >> 4);
+                    const uint32_t d = tmem + 128u * sb;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t off = (uint64_t)(((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4);
+                        ptx::mma_ss(d, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(bar(G::kBarSFull + sb));
+                    if (jj + 1 == nk) ptx::mma_commit(bar(G::kBarQEmpty + qbuf));
+                }
+            }
+        } else {
+            for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
+                const Item it = decode_item<kCausal>(p, k);
+                const int nk = it.kv_end - it.kv_begin;
+                for (int jj = 0; jj < nk; ++jj, ++g) {
+                    const uint32_t sb = g & 1u;
+                    if (!(ok = wait_bar(bar(G::kBarVFull + (int)sb), (g >> 1) & 1u, kSiteRingFull, abort_flag, lim)))
+                        break;
+                    // the unit's first PV overwrites O_a, O_b: the previous unit's epilogue has read them
+                    if (jj == 0 && u > 0 &&
+                        !(ok = wait_bar(bar(G::kBarOEmpty), (uint32_t)(u - 1) & 1u, kSiteOEmpty, abort_flag, lim)))
+                        break;
+                    const uint64_t b0 = dvring + (uint64_t)(((2u * sb + 1u) * G::kTileBytes) >> 4);
+                    // one barrier per S buffer: the softmax may finish the next step before
+                    // this wait, and that arrival must not land on the barrier waited on here
+                    if (!(ok = wait_bar(bar(G::kBarPFull + (int)sb), (g >> 1) & 1u, kSitePFull, abort_flag, lim)))
+                        break;
+                    ptx::tc_fence_after();
+                    for (int h = 0; h < 2; ++h) {
+                        // O_h += P_h V[64h .. 64h + 63]: 4 steps of 16 keys (P_h: 8 TMEM columns
+                        // each, the first 32 columns of its half of the S buffer; V: 2 KB each)
+                        const uint32_t dO = tmem + 256u + (uint32_t)(D * h), a = tmem + 128u * sb + (uint32_t)(sq::kHalfN * h);
+#pragma unroll
+                        for (int k4 = 0; k4 < sq::kHalfN / 16; ++k4) {
+                            const int kk = h * (sq::kHalfN / 16) + k4;
+                            ptx::mma_ts(dO, a + (uint32_t)k4 * 8u, b0 + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                        (k4 > 0 || jj > 0) ? 1u : 0u);
+                        }
+                    }
+                    ptx::mma_commit(bar(G::kBarPVDone + (int)sb));
+                    if (jj + 1 == nk) ptx::mma_commit(bar(G::kBarOFull));
+                }
+            }
+        }
+        // drain: every MMA this thread issued has finished before TMEM is released
+        ptx::mma_commit(bar(G::kBarDrain));
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(bar(G::kBarDrain), 0) && ptx::globaltimer_ns() - t0 < lim) {
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ softmax, key half h
+        // Thread = one query row (its TMEM lane) and keys 64h .. 64h + 63 of every tile: an
+        // online softmax of its own over those keys, into its own accumulator O_h, with its
+        // own running max m_h and sum l_h (the two halves are merged by the epilogue).
+        const int h = warp >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;        // row within the tile
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(D * h);
+        const float c = p.scale_log2;
+        uint32_t g = 0;
+        int u = 0;
+        bool ok = true;
+        for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
+            const Item it = decode_item<kCausal>(p, k);
+            float m_ref = -INFINITY;      // running max of raw logits at the last rescale
+            float l = 0.0f;               // running sum of weights relative to m_ref
+            for (int j = it.kv_begin; j < it.kv_end; ++j, ++g) {
+                const uint32_t tS = tmem + lane_off + 128u * (g & 1u) + (uint32_t)(sq::kHalfN * h);
+                ok = wait_bar(bar(G::kBarSFull + (g & 1u)), (g >> 1) & 1u, kSiteSFull, abort_flag, lim);
+                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                ptx::tc_fence_after();
+                uint32_t s[sq::kHalfN];
+                ptx::tmem_ld64(tS, s);
+                // keys of this half past `limit` are absent: beyond Skv, or (causal) past this
+                // row's diagonal; they get -inf logits and so weight 0
+                const int key0 = j * kBN + sq::kHalfN * h;
+                if constexpr (kCausal) {
+                    int limit = p.Skv - key0 - 1;
+                    const int diag = it.qb * kUnitRows + row + p.causal_off - key0;
+                    limit = diag < limit ? diag : limit;
+                    if (__any_sync(0xFFFFFFFFu, limit < sq::kHalfN - 1)) {
+#pragma unroll
+                        for (int e = 0; e < sq::kHalfN; ++e)
+                            if (e > limit) s[e] = __float_as_uint(-INFINITY);
+                    }
+                } else {
+                    const int valid = p.Skv - key0;   // the same for every row of the tile
+                    if (valid < sq::kHalfN) {
+#pragma unroll
+                        for (int e = 0; e < sq::kHalfN; ++e)
+                            if (e >= valid) s[e] = __float_as_uint(-INFINITY);
+                    }
+                }
+                // row max and min: 3-input trees over 4 independent chains each
+                float mxa[4], mna[4];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) mxa[q4] = mna[q4] = __uint_as_float(s[q4]);
+#pragma unroll
+                for (int e = 4; e < sq::kHalfN - 4; e += 8) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const float a = __uint_as_float(s[e + q4]), b = __uint_as_float(s[e + 4 + q4]);
+                        mxa[q4] = ptx::fmax3(mxa[q4], a, b);
+                        mna[q4] = ptx::fmin3(mna[q4], a, b);
+                    }
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    mxa[q4] = fmaxf(mxa[q4], __uint_as_float(s[sq::kHalfN - 4 + q4]));
+                    mna[q4] = fminf(mna[q4], __uint_as_float(s[sq::kHalfN - 4 + q4]));
+                }
+                const float mx = ptx::fmax3(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3]));
+                const float mn = ptx::fmin3(mna[0], mna[1], fminf(mna[2], mna[3]));
+                const float m_new = fmaxf(m_ref, mx);
+                bool rescale_o = false;
+                float alpha = 1.0f;
+                if (m_new > m_ref && (m_new - m_ref) * c > p.tau) {
+                    if (m_ref == -INFINITY) {
+                        alpha = 0.0f;      // nothing accumulated yet but 0*v terms
+                    } else {
+                        alpha = ptx::ex2_approx(fmaxf((m_ref - m_new) * c, -125.0f));
+                        rescale_o = j > it.kv_begin;
+                    }
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+                // Every exponent of this row is >= -124 and no logit is -inf: the clamp that
+                // keeps underflowing finite weights positive cannot fire, so skip it.
+                const bool plain = mn > -INFINITY && (mn - m_use) * c >= kMinExponent;
+                const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
+                float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                  make_float2(0.f, 0.f)};
+                uint32_t pk[sq::kHalfN / 2];
+                if (__all_sync(0xFFFFFFFFu, plain)) {
+#pragma unroll
+                    for (int e = 0; e < sq::kHalfN / 2; ++e) {
+                        const float2 x = __fmul2_rn(
+                            __fadd2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), nm2), c2);
+                        const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+                        lsum[e & 3] = __fadd2_rn(lsum[e & 3], pp);
+                        pk[e] = ptx::pack_bf16x2(pp.x, pp.y);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < sq::kHalfN / 2; ++e) {
+                        const float p0 = ptx::ex2_approx(weight_exponent(__uint_as_float(s[2 * e]), c, m_use));
+                        const float p1 = ptx::ex2_approx(weight_exponent(__uint_as_float(s[2 * e + 1]), c, m_use));
+                        lsum[e & 3] = __fadd2_rn(lsum[e & 3], make_float2(p0, p1));
+                        pk[e] = ptx::pack_bf16x2(p0, p1);
+                    }
+                }
+                // P_h over the first 32 columns of this half: the logits were read above, and
+                // the other half's columns are not touched
+                ptx::tmem_st32(tS, pk);
+                const float2 ls = __fadd2_rn(__fadd2_rn(lsum[0], lsum[1]), __fadd2_rn(lsum[2], lsum[3]));
+                l += ls.x + ls.y;
+                if (__any_sync(0xFFFFFFFFu, rescale_o)) {
+                    // O_h is stable once the previous step's PV into it is done (S_g was issued
+                    // ahead of that PV, so S being ready does not imply it)
+                    ok = wait_bar(bar(G::kBarPVDone + (int)((g - 1u) & 1u)), ((g - 1u) >> 1) & 1u, kSitePVDone,
+                                  abort_flag, lim);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const float a = rescale_o ? alpha : 1.0f;
+                    const float2 a2 = make_float2(a, a);
+#pragma unroll 1
+                    for (int ch = 0; ch < D / 32; ++ch) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(tO + ch * 32, o);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), a2);
+                            o[2 * e] = __float_as_uint(v.x);
+                            o[2 * e + 1] = __float_as_uint(v.y);
+                        }
+                        ptx::tmem_st32(tO + ch * 32, o);
+                    }
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(G::kBarPFull + (int)(g & 1u)));
+            }
+            if (!ok) break;
+            // this half's (m, l) for the epilogue; the buffer of the unit two back was read
+            // before that unit's O was released, which this thread's PV waits have followed
+            stats[((u & 1) * 2 + h) * kBM + row] = make_float2(m_ref, l);
+            ptx::mbar_arrive(bar(G::kBarStats + (u & 1)));
+        }
+    } else if (warp < sq::kWarpEpi + 4) {
+        // ------------------------------------------------ merge of the halves and epilogue
+        // O = (w_a O_a + w_b O_b) / (w_a l_a + w_b l_b) with w_h = 2^((m_h - m) c), m the
+        // larger reference; a finite m_h keeps w_h >= 2^-125 (a finite logit never loses its
+        // weight entirely) and m_h = -inf (no key of the half seen) gives w_h = 0.  The same
+        // rule merges key splits in the combine kernel.
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tOa = tmem + lane_off + 256u, tOb = tOa + (uint32_t)D;
+        const float c = p.scale_log2;
+        const uint32_t region = sbase + G::kSmemStage + (uint32_t)((warp - sq::kWarpEpi) * kStageBytes);
+        int u = 0;
+        bool ok = true;
+        for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
+            const Item it = decode_item<kCausal>(p, k);
+            ok = wait_bar(bar(G::kBarOFull), (uint32_t)u & 1u, kSiteOFull, abort_flag, lim) &&
+                 wait_bar(bar(G::kBarStats + (u & 1)), (uint32_t)(u >> 1) & 1u, kSiteStats, abort_flag, lim);
+            if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const float2 sa = stats[((u & 1) * 2 + 0) * kBM + row];
+            const float2 sb = stats[((u & 1) * 2 + 1) * kBM + row];
+            const float m = fmaxf(sa.x, sb.x);
+            const float wa = (sa.x == -INFINITY) ? 0.0f : ptx::ex2_approx(fmaxf((sa.x - m) * c, -125.0f));
+            const float wb = (sb.x == -INFINITY) ? 0.0f : ptx::ex2_approx(fmaxf((sb.x - m) * c, -125.0f));
+            const float l = fmaf(wa, sa.y, wb * sb.y);
+            const int qrow = it.qb * kUnitRows + row;
+            const bool valid_row = qrow < p.Sq;
+            // 16 merged columns of O (still unnormalised) from the two accumulators
+            auto merged16 = [&](int c16, uint32_t (&y)[16]) {
+                uint32_t a[16], b[16];
+                ptx::tmem_ld16_nowait(tOa + 16u * c16, a);
+                ptx::tmem_ld16_nowait(tOb + 16u * c16, b);
+                ptx::tmem_wait_ld16(a);
+                ptx::tmem_wait_ld16(b);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    y[e] = __float_as_uint(fmaf(wa, __uint_as_float(a[e]), wb * __uint_as_float(b[e])));
+            };
+            if (it.split_slot < 0) {
+                const float inv = 1.0f / l;
+                // natural-log log-sum-exp of the scaled logits: (m*c + log2 l) * ln 2
+                if (p.lse && valid_row)
+                    p.lse[((long long)it.b * p.H + it.h) * p.Sq + qrow] = (m * c + log2f(l)) * kLn2;
+                const int r0 = it.qb * kUnitRows + quarter * kStageRowsPerWarp;
+#pragma unroll
+                for (int hc = 0; hc < G::kChunks; ++hc) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t y[16];
+                        merged16(4 * hc + q, y);
+                        scale_round_pairs<8>(y, inv, p.round_mode, w + 8 * q);
+                    }
+                    if (hc == G::kChunks - 1) {
+                        // O_a and O_b are read: the next unit's PV GEMMs may overwrite them
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(bar(G::kBarOEmpty));
+                    }
+                    // the region's previous TMA store (if any) has finished reading it
+                    if (lane == 0) ptx::bulk_wait_read0();
+                    __syncwarp();
+                    // row `lane` of the region; 16-byte piece pc is stored at pc ^ (lane & 7)
+                    // (128-byte swizzle)
+                    const uint32_t rowaddr = region + (uint32_t)lane * 128u;
+#pragma unroll
+                    for (int pc = 0; pc < 8; ++pc)
+                        ptx::st_shared_v4(rowaddr + (((uint32_t)pc ^ (uint32_t)(lane & 7)) << 4), w[4 * pc],
+                                          w[4 * pc + 1], w[4 * pc + 2], w[4 * pc + 3]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (p.bshd) ptx::tma_store_4d(&omap, region, hc * 64, it.h, r0, it.b);
+                        else ptx::tma_store_4d(&omap, region, hc * 64, r0, it.h, it.b);
+                        ptx::bulk_commit();
+                    }
+                }
+            } else {
+                // split partial: O/l in fp32 (the raw sum when l == 0) and LSE in log2 units
+                const float inv = (l > 0.0f) ? 1.0f / l : 1.0f;
+                const long long wrow = (long long)it.split_slot * kUnitRows + row;
+#pragma unroll 1
+                for (int c16 = 0; c16 < D / 16; ++c16) {
+                    uint32_t y[16];
+                    merged16(c16, y);
+                    if (valid_row) {
+                        float4* d4 = reinterpret_cast<float4*>(p.ws_o + wrow * D + 16 * c16);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            d4[v4] = make_float4(__uint_as_float(y[4 * v4]) * inv, __uint_as_float(y[4 * v4 + 1]) * inv,
+                                                 __uint_as_float(y[4 * v4 + 2]) * inv, __uint_as_float(y[4 * v4 + 3]) * inv);
+                    }
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(G::kBarOEmpty));
+                if (valid_row) p.ws_lse[wrow] = m * c + log2f(l);
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------------- teardown
+    if (warp >= sq::kWarpEpi && warp < sq::kWarpEpi + 4 && lane == 0) ptx::bulk_wait0();   // output stores complete
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == sq::kWarpMma) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, sq::kTmemCols);
+    }
+}
+
 // ------------------------------------------------------------------------------ combine
 struct CombineParams {
     int H, Sq, nq, nsplit, n_full, split_units, round_mode;
@@ -864,6 +1367,16 @@ int device_info(DeviceInfo** out) {
             cudaFuncSetAttribute(attn_fwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s64) !=
                 cudaSuccess)
             return ATTN_ERR_CUDA;
+        const int t128 = sq::Geo<128>::kSmemAlloc, t64 = sq::Geo<64>::kSmemAlloc;
+        if (cudaFuncSetAttribute(attn_fwd_short_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 t128) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_fwd_short_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 t128) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_fwd_short_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, t64) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(attn_fwd_short_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, t64) !=
+                cudaSuccess)
+            return ATTN_ERR_CUDA;
         di.attr_set = true;
     }
     if (!g_encode) {
@@ -939,7 +1452,20 @@ int launch(const attn_args_t& a, const attn_plan_t& pl, const attn_options_t* op
     const attn_event_t* ev = opts ? opts->events : nullptr;
     if (ev && ev[0] && cudaEventRecord((cudaEvent_t)ev[0], stream) != cudaSuccess) return ATTN_ERR_CUDA;
     const unsigned grid = (unsigned)pl.grid;
-    if (d == 128) {
+    if (Sq <= kBM) {
+        // one query tile per (b, h): the short-query kernel (same items and workspace rows)
+        if (d == 128) {
+            if (p.causal)
+                attn_fwd_short_kernel<128, true><<<grid, sq::kThreads, sq::Geo<128>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
+            else
+                attn_fwd_short_kernel<128, false><<<grid, sq::kThreads, sq::Geo<128>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
+        } else {
+            if (p.causal)
+                attn_fwd_short_kernel<64, true><<<grid, sq::kThreads, sq::Geo<64>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
+            else
+                attn_fwd_short_kernel<64, false><<<grid, sq::kThreads, sq::Geo<64>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
+        }
+    } else if (d == 128) {
         if (p.causal) attn_fwd_kernel<128, true><<<grid, kThreads, Geo<128>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
         else attn_fwd_kernel<128, false><<<grid, kThreads, Geo<128>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
     } else {
