@@ -175,11 +175,26 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
 // fp32 -> bf16 bits, round to nearest even (the conversion instruction), NaN stays NaN
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) { return ptx::pack_bf16x2(lo, hi); }
 
+// global[tile at (c0, c1, c2)] += shared (fp32 add, done by the TMA unit; out-of-range
+// elements of the box are skipped)
+__device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// wait until at most one committed bulk group still reads its shared-memory source
+__device__ __forceinline__ void bulk_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap domap,
-                const BwdParams p) {
+                const __grid_constant__ CUtensorMap dqmap, const BwdParams p) {
     using G = BGeo<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -280,17 +295,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 dw[ci][2 * g4] = pack2(dr[0], dr[1]);
                 dw[ci][2 * g4 + 1] = pack2(dr[2], dr[3]);
             }
-            // dS^T row `row`, queries 32c..32c+31: 16-byte pieces (c & 1)*4 + v of the 64-query
-            // chunk c >> 1, at piece ^ (row & 7) (128-byte swizzle)
-            const uint32_t rowaddr = sbase + G::kSmemDS + (uint32_t)((c >> 1) * kChunkBytes) + (uint32_t)row * 128u;
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-                const uint32_t pc = (uint32_t)((c & 1) * 4 + v4);
-                ptx::st_shared_v4(rowaddr + ((pc ^ (uint32_t)(row & 7)) << 4), dw[ci][4 * v4], dw[ci][4 * v4 + 1],
-                                  dw[ci][4 * v4 + 2], dw[ci][4 * v4 + 3]);
-            }
         }
-        // every S^T and dP^T column has been read by both warpgroups
+        // every S^T and dP^T column has been read by both warpgroups; warpgroup 1's reductions of
+        // the previous dQ have finished reading their staging (the dS region)
+        if (half == 1) {
+            if (lane == 0) ptx::bulk_wait_read0();
+            __syncwarp();
+        }
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(kBarRead));
         ok = bwd_wait(bar(kBarRead), s & 1u, kSiteRead, abort_flag, lim);
@@ -301,6 +312,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             const int c = 2 * half + ci;
             ptx::tmem_st16(tS + lane_off + 16u * c, pw[ci]);
             ptx::tmem_st16(tDP + lane_off + 16u * c, dw[ci]);
+            // dS^T row `row`, queries 32c..32c+31: 16-byte pieces (c & 1)*4 + v of the 64-query
+            // chunk c >> 1, at piece ^ (row & 7) (128-byte swizzle)
+            const uint32_t rowaddr = sbase + G::kSmemDS + (uint32_t)((c >> 1) * kChunkBytes) + (uint32_t)row * 128u;
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+                const uint32_t pc = (uint32_t)((c & 1) * 4 + v4);
+                ptx::st_shared_v4(rowaddr + ((pc ^ (uint32_t)(row & 7)) << 4), dw[ci][4 * v4], dw[ci][4 * v4 + 1],
+                                  dw[ci][4 * v4 + 2], dw[ci][4 * v4 + 3]);
+            }
         }
         ptx::tmem_wait_st();
         ptx::fence_proxy_async_smem();
@@ -469,26 +489,47 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             const Unit un = decode_unit(p, k);
             for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
                 const int h = un.kvh * p.group + st % p.group;
-                const int q = (un.it_lo + st / p.group) * kBM + row;
                 // query columns 64..127 of this step's P^T and dS^T, then its dQ
                 if (!(ok = pds_step(un, un.it_lo + st / p.group, s, 1))) break;
                 ok = bwd_wait(bar(kBarDQFull), s & 1u, kSiteDQFull, abort_flag, lim);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 ptx::tc_fence_after();
-                float* dst = p.dq_acc + (((long long)un.b * p.H + h) * p.Sq + q) * D;
-                // all of dQ_i into registers, release TMEM, then the reductions
+                // all of dQ_i into registers and release TMEM; then, per 32 columns, this warp's
+                // 32 rows (times 1/sqrt(d)) into a 4 KB staging buffer of the dS region (free
+                // until the next step's dS, which waits for these reads) in the 128-byte swizzle,
+                // and one TMA reduction adds the box into the fp32 dQ accumulator.  The TMA unit
+                // does the additions: per-thread atomics here stalled the MMA thread's issue.
                 uint32_t v[D];
                 if constexpr (D == 128) ptx::tmem_ld128(tDQ + lane_off, v);
                 else ptx::tmem_ld64(tDQ + lane_off, v);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(kBarDQEmpty));
-                if (q < p.Sq) {
+                const uint32_t stage = sbase + G::kSmemDS + (uint32_t)(quarter * 8192);
+                const int q0 = (un.it_lo + st / p.group) * kBM + quarter * 32;
 #pragma unroll
-                    for (int v4 = 0; v4 < D / 4; ++v4)
-                        ptx::red_add_v4(dst + 4 * v4, __uint_as_float(v[4 * v4]) * p.scale,
-                                        __uint_as_float(v[4 * v4 + 1]) * p.scale,
-                                        __uint_as_float(v[4 * v4 + 2]) * p.scale,
-                                        __uint_as_float(v[4 * v4 + 3]) * p.scale);
+                for (int c = 0; c < D / 32; ++c) {
+                    const uint32_t buf = stage + (uint32_t)((c & 1) * 4096);
+                    if (c >= 2) {
+                        // this buffer's previous box has been read
+                        if (lane == 0) bulk_wait_read1();
+                        __syncwarp();
+                    }
+                    const uint32_t rowaddr = buf + (uint32_t)lane * 128u;
+#pragma unroll
+                    for (int pc = 0; pc < 8; ++pc) {
+                        const int e = 32 * c + 4 * pc;
+                        ptx::st_shared_v4(rowaddr + (((uint32_t)pc ^ (uint32_t)(lane & 7)) << 4),
+                                          __float_as_uint(__uint_as_float(v[e]) * p.scale),
+                                          __float_as_uint(__uint_as_float(v[e + 1]) * p.scale),
+                                          __float_as_uint(__uint_as_float(v[e + 2]) * p.scale),
+                                          __float_as_uint(__uint_as_float(v[e + 3]) * p.scale));
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_reduce_add_3d(&dqmap, buf, 32 * c, q0, un.b * p.H + h);
+                        ptx::bulk_commit();
+                    }
                 }
             }
             if (!ok) break;
@@ -526,6 +567,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         }
     }
 
+    // warpgroup 1's dQ reductions are complete before the CTA (and its shared memory) goes
+    if (warp >= 4 && warp < 8 && lane == 0) ptx::bulk_wait0();
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == kWarpMma) {
@@ -591,6 +634,17 @@ PFN_cuTensorMapEncodeTiled_v12000 g_bwd_encode = nullptr;
 bool g_bwd_attr[64] = {};
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The fp32 dQ accumulator [B*H][Sq][d] for TMA reductions: box 32 columns x 32 rows, 128-byte
+// swizzle (32 fp32 = 128 bytes per row); rows past Sq are out of range and skipped.
+bool encode_dq(CUtensorMap* m, float* ptr, int64_t BH, int64_t Sq, int64_t d) {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Sq, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)(d * 4), (cuuint64_t)(Sq * d * 4)};
+    cuuint32_t box[3] = {32, 32, 1}, estr[3] = {1, 1, 1};
+    return g_bwd_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool encode(CUtensorMap* m, const void* ptr, int64_t B, int64_t H, int64_t S, int64_t d, bool bshd) {
     cuuint64_t dims[4], strides[3];
@@ -715,6 +769,8 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     p.lse2 = lse2;
     p.delta = delta;
     p.dq_acc = dq_acc;
+    CUtensorMap dqm;
+    if (!encode_dq(&dqm, dq_acc, a.B * a.H, a.Sq, d)) return ATTN_ERR_CUDA;
     p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
     p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
     long long q_sb, q_ss, q_sh;
@@ -738,9 +794,9 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
         delta, p.H, p.Sq, p.nq_pad_rows, prows, q_sb, q_ss, q_sh);
     const int grid = p.n_units < sms ? p.n_units : sms;
     if (d == 128)
-        attn_bwd_kernel<128><<<(unsigned)grid, kThreads, smem_alloc<128>(), stream>>>(qm, km, vm, dom, p);
+        attn_bwd_kernel<128><<<(unsigned)grid, kThreads, smem_alloc<128>(), stream>>>(qm, km, vm, dom, dqm, p);
     else
-        attn_bwd_kernel<64><<<(unsigned)grid, kThreads, smem_alloc<64>(), stream>>>(qm, km, vm, dom, p);
+        attn_bwd_kernel<64><<<(unsigned)grid, kThreads, smem_alloc<64>(), stream>>>(qm, km, vm, dom, dqm, p);
     const long long n4 = a.B * a.H * a.Sq * (d / 4);
     auto conv = d == 128 ? attn_bwd_dq_kernel<128> : attn_bwd_dq_kernel<64>;
     conv<<<(unsigned)cdiv(n4, 256), 256, 0, stream>>>(dq_acc, reinterpret_cast<__nv_bfloat16*>(a.dq), p.H, p.Sq, n4,
