@@ -185,6 +185,14 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src
         : "memory");
 }
 
+// four floats from shared memory (an explicit shared-space load: through a generic pointer
+// the loads went down the generic path, whose latency every element's chain then waited on)
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
 // wait until at most one committed bulk group still reads its shared-memory source
 __device__ __forceinline__ void bulk_wait_read1() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -203,8 +211,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     uint32_t* tmem_holder = (uint32_t*)(smem + smem_misc<D>());
     volatile uint32_t* abort_flag = (volatile uint32_t*)(smem + smem_misc<D>() + 4);
-    const float* s_lse2 = (const float*)(smem + G::kSmemStats);
-    const float* s_delta = s_lse2 + kBM;
+    const uint32_t s_lse2 = ptx::smem_u32(smem + G::kSmemStats);   // base-2 LSE [128], then D [128]
+    const uint32_t s_delta = s_lse2 + kBM * 4;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -271,8 +279,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             const bool all_vis = q0 + 31 < p.Sq && (!p.causal || kj <= q0 + p.causal_off);
 #pragma unroll
             for (int g4 = 0; g4 < 8; ++g4) {
-                const float4 l4 = *reinterpret_cast<const float4*>(s_lse2 + 32 * c + 4 * g4);
-                const float4 d4 = *reinterpret_cast<const float4*>(s_delta + 32 * c + 4 * g4);
+                const float4 l4 = ld_shared_f4(s_lse2 + (uint32_t)(4 * (32 * c + 4 * g4)));
+                const float4 d4 = ld_shared_f4(s_delta + (uint32_t)(4 * (32 * c + 4 * g4)));
                 const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
                 float pr[4], dr[4];
 #pragma unroll
