@@ -277,6 +277,31 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             const int q0 = it * kBM + 32 * c;
             // every column of this chunk visible to this key: no per-element test
             const bool all_vis = q0 + 31 < p.Sq && (!p.causal || kj <= q0 + p.causal_off);
+            if (all_vis) {
+                // the same arithmetic on pairs (packed fp32), no mask
+                const float2 c2 = make_float2(cl, cl);
+#pragma unroll
+                for (int g4 = 0; g4 < 8; ++g4) {
+                    const float4 l4 = ld_shared_f4(s_lse2 + (uint32_t)(4 * (32 * c + 4 * g4)));
+                    const float4 d4 = ld_shared_f4(s_delta + (uint32_t)(4 * (32 * c + 4 * g4)));
+                    const int col = 4 * g4;
+                    const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(sv[col]), __uint_as_float(sv[col + 1])), c2,
+                                                  make_float2(-l4.x, -l4.y));
+                    const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(sv[col + 2]), __uint_as_float(sv[col + 3])), c2,
+                                                  make_float2(-l4.z, -l4.w));
+                    const float2 p01 = make_float2(ptx::ex2_approx(x01.x), ptx::ex2_approx(x01.y));
+                    const float2 p23 = make_float2(ptx::ex2_approx(x23.x), ptx::ex2_approx(x23.y));
+                    const float2 s01 = __fmul2_rn(p01, __fadd2_rn(make_float2(__uint_as_float(dp[col]), __uint_as_float(dp[col + 1])),
+                                                                   make_float2(-d4.x, -d4.y)));
+                    const float2 s23 = __fmul2_rn(p23, __fadd2_rn(make_float2(__uint_as_float(dp[col + 2]), __uint_as_float(dp[col + 3])),
+                                                                   make_float2(-d4.z, -d4.w)));
+                    pw[ci][2 * g4] = pack2(p01.x, p01.y);
+                    pw[ci][2 * g4 + 1] = pack2(p23.x, p23.y);
+                    dw[ci][2 * g4] = pack2(s01.x, s01.y);
+                    dw[ci][2 * g4 + 1] = pack2(s23.x, s23.y);
+                }
+                continue;
+            }
 #pragma unroll
             for (int g4 = 0; g4 < 8; ++g4) {
                 const float4 l4 = ld_shared_f4(s_lse2 + (uint32_t)(4 * (32 * c + 4 * g4)));
@@ -289,12 +314,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     const float x = fmaf(__uint_as_float(sv[col]), cl, -lv[e]);
                     float pp = ptx::ex2_approx(x);
                     float ds = pp * (__uint_as_float(dp[col]) - dv4[e]);
-                    if (!all_vis) {
-                        // a masked pair takes no part: both zero, even where D is NaN (a
-                        // query with no visible key has a NaN output row)
-                        const int q = q0 + col;
-                        if (!(q < p.Sq && (!p.causal || kj <= q + p.causal_off))) pp = ds = 0.0f;
-                    }
+                    // a masked pair takes no part: both zero, even where D is NaN (a query
+                    // with no visible key has a NaN output row)
+                    const int q = q0 + col;
+                    if (!(q < p.Sq && (!p.causal || kj <= q + p.causal_off))) pp = ds = 0.0f;
                     pr[e] = pp;
                     dr[e] = ds;
                 }
