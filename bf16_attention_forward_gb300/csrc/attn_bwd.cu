@@ -23,7 +23,7 @@
 //       dQ_i = dS K_j             (dS^T also written to shared memory, read as an MN-major
 //                                  A operand; K_j as an MN-major B operand)
 //     dV and dK accumulate in TMEM for the whole unit; dQ_i is added into an fp32
-//     accumulator in global memory (vector reductions), since many key tiles contribute;
+//     accumulator in global memory by TMA tensor reductions (many key tiles contribute);
 //   * a last kernel rounds the dQ accumulator to bf16 (round to nearest even).
 // Roles: warp 8 TMA producer, warp 9 (one thread) MMA issuer; warpgroups 0 and 1 recompute P
 // and form dS for query columns 0..63 and 64..127 of each step, and warpgroup 1 then drains dQ

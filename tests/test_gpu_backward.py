@@ -8,7 +8,7 @@ sum of term magnitudes (dV: sum_i p |dO|; dQ, dK: c sum p (|dP| + |D|) |k| or |q
 |D| = sum |dO| |O| also covers D formed from the rounded O).  2^-7 is four times bf16's unit
 roundoff: P (or dS) rounding, the rounding of O inside D, and the final bf16 store.  The
 oracle itself is pinned against numerical differentiation of the forward.  dQ is summed with
-atomic adds across key tiles, so its last bits may differ between runs; dK and dV are
+reductions in L2 across key tiles in no fixed order, so its last bits may differ between runs; dK and dV are
 accumulated in a fixed order and are bitwise reproducible.
 """
 import numpy as np
