@@ -277,9 +277,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             const int q0 = it * kBM + 32 * c;
             // every column of this chunk visible to this key: no per-element test
             const bool all_vis = q0 + 31 < p.Sq && (!p.causal || kj <= q0 + p.causal_off);
+            const float2 c2 = make_float2(cl, cl);
             if (all_vis) {
-                // the same arithmetic on pairs (packed fp32), no mask
-                const float2 c2 = make_float2(cl, cl);
+                // the packed arithmetic below without the mask
 #pragma unroll
                 for (int g4 = 0; g4 < 8; ++g4) {
                     const float4 l4 = ld_shared_f4(s_lse2 + (uint32_t)(4 * (32 * c + 4 * g4)));
@@ -302,29 +302,38 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 }
                 continue;
             }
+            // pair (this key, query q0 + col) is visible iff lo <= col < hi: hi from Sq, lo from
+            // the causal diagonal (key kj <= q + causal_off)
+            const int hi = p.Sq - q0;
+            const long long lo64 = p.causal ? (long long)kj - p.causal_off - q0 : 0ll;
+            const int lo = lo64 < -1 ? -1 : (lo64 > 33 ? 33 : (int)lo64);
 #pragma unroll
             for (int g4 = 0; g4 < 8; ++g4) {
                 const float4 l4 = ld_shared_f4(s_lse2 + (uint32_t)(4 * (32 * c + 4 * g4)));
                 const float4 d4 = ld_shared_f4(s_delta + (uint32_t)(4 * (32 * c + 4 * g4)));
-                const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-                float pr[4], dr[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int col = 4 * g4 + e;
-                    const float x = fmaf(__uint_as_float(sv[col]), cl, -lv[e]);
-                    float pp = ptx::ex2_approx(x);
-                    float ds = pp * (__uint_as_float(dp[col]) - dv4[e]);
-                    // a masked pair takes no part: both zero, even where D is NaN (a query
-                    // with no visible key has a NaN output row)
-                    const int q = q0 + col;
-                    if (!(q < p.Sq && (!p.causal || kj <= q + p.causal_off))) pp = ds = 0.0f;
-                    pr[e] = pp;
-                    dr[e] = ds;
-                }
-                pw[ci][2 * g4] = pack2(pr[0], pr[1]);
-                pw[ci][2 * g4 + 1] = pack2(pr[2], pr[3]);
-                dw[ci][2 * g4] = pack2(dr[0], dr[1]);
-                dw[ci][2 * g4 + 1] = pack2(dr[2], dr[3]);
+                const int col = 4 * g4;
+                const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(sv[col]), __uint_as_float(sv[col + 1])), c2,
+                                              make_float2(-l4.x, -l4.y));
+                const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(sv[col + 2]), __uint_as_float(sv[col + 3])), c2,
+                                              make_float2(-l4.z, -l4.w));
+                float2 p01 = make_float2(ptx::ex2_approx(x01.x), ptx::ex2_approx(x01.y));
+                float2 p23 = make_float2(ptx::ex2_approx(x23.x), ptx::ex2_approx(x23.y));
+                float2 s01 = __fmul2_rn(p01, __fadd2_rn(make_float2(__uint_as_float(dp[col]), __uint_as_float(dp[col + 1])),
+                                                         make_float2(-d4.x, -d4.y)));
+                float2 s23 = __fmul2_rn(p23, __fadd2_rn(make_float2(__uint_as_float(dp[col + 2]), __uint_as_float(dp[col + 3])),
+                                                         make_float2(-d4.z, -d4.w)));
+                // a masked pair takes no part: both zero, even where D is NaN (a query with no
+                // visible key has a NaN output row); selects, no branches
+                const bool v0 = (col >= lo) & (col < hi), v1 = (col + 1 >= lo) & (col + 1 < hi);
+                const bool v2 = (col + 2 >= lo) & (col + 2 < hi), v3 = (col + 3 >= lo) & (col + 3 < hi);
+                p01.x = v0 ? p01.x : 0.0f; s01.x = v0 ? s01.x : 0.0f;
+                p01.y = v1 ? p01.y : 0.0f; s01.y = v1 ? s01.y : 0.0f;
+                p23.x = v2 ? p23.x : 0.0f; s23.x = v2 ? s23.x : 0.0f;
+                p23.y = v3 ? p23.y : 0.0f; s23.y = v3 ? s23.y : 0.0f;
+                pw[ci][2 * g4] = pack2(p01.x, p01.y);
+                pw[ci][2 * g4 + 1] = pack2(p23.x, p23.y);
+                dw[ci][2 * g4] = pack2(s01.x, s01.y);
+                dw[ci][2 * g4 + 1] = pack2(s23.x, s23.y);
             }
         }
         // every S^T and dP^T column has been read by both warpgroups; warpgroup 1's reductions of
