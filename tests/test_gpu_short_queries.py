@@ -75,3 +75,19 @@ def test_half_without_visible_keys(attn):
         q, k, v = make_qkv(1, 2, 128, 128, d, "bshd", seed=3400 + d)
         for mode in MODES:
             check_ex(attn, q, k, v, "bshd", mode, causal=True)
+
+
+@pytest.mark.parametrize("max_ctas", [0, 7, 1])
+def test_short_queries_many_units_per_cta(attn, max_ctas):
+    # B*H = 320 units of one query tile each, 3 key tiles per unit (an odd count, so the two S
+    # buffers alternate across unit boundaries); max_ctas caps the grid so each CTA runs up to
+    # all 320 units in turn (query double buffer, per-unit statistics, O hand-off)
+    q, k, v = make_qkv(4, 80, 64, 300, 128, "bshd", seed=3500, Hkv=20)
+    check_ex(attn, q, k, v, "bshd", "rtne", max_ctas=max_ctas)
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_short_queries_many_units_causal_and_splits(attn, d):
+    q, k, v = make_qkv(2, 100, 100, 400, d, "bhsd", seed=3600 + d)
+    check_ex(attn, q, k, v, "bhsd", "rtna", causal=True, max_ctas=19)
+    check_ex(attn, q, k, v, "bhsd", "rtz", force_splits=2, max_ctas=23)
