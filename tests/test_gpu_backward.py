@@ -115,3 +115,16 @@ def test_backward_head_dim_64(attn, causal, layout):
         q, k, v = make_qkv(B, H, Sq, Skv, 64, layout, seed=5500 + Sq, Hkv=Hkv)
         g = make_qkv(B, H, Sq, 1, 64, layout, seed=5600 + Skv)[0]
         check_bwd(attn, q, k, v, g, layout, causal=causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_many_units_per_cta(attn, causal):
+    # more (b, K/V head, key tile) units than SMs: CTAs run several units in turn, so the dK/dV
+    # hand-off between units and the Q/dO ring across unit boundaries are exercised
+    if causal:
+        B, H, Hkv, Sq, Skv = 2, 16, 8, 300, 1300      # 2 * 8 * 11 = 176 units
+    else:
+        B, H, Hkv, Sq, Skv = 4, 16, 16, 130, 1280     # 4 * 16 * 10 = 640 units
+    q, k, v = make_qkv(B, H, Sq, Skv, 128, "bshd", seed=5700 + causal, Hkv=Hkv)
+    g = make_qkv(B, H, Sq, 1, 128, "bshd", seed=5800 + causal)[0]
+    check_bwd(attn, q, k, v, g, "bshd", causal=causal)
