@@ -702,7 +702,8 @@ struct Geo {
     static constexpr int kBarOFull = kBarPVDone + 2;  // the unit's last PV GEMMs done
     static constexpr int kBarOEmpty = kBarOFull + 1;  // the epilogue has read O_a and O_b
     static constexpr int kBarStats = kBarOEmpty + 1;  // [unit parity] both halves' (m, l) written
-    static constexpr int kBarDrain = kBarStats + 2;
+    static constexpr int kBarStatsFree = kBarStats + 2;   // [unit parity] the epilogue has read them
+    static constexpr int kBarDrain = kBarStatsFree + 2;
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kSmemMisc = kSmemBars + kNumBars * 8;
     static constexpr int kSmemUsed = kSmemMisc + 16;
@@ -739,6 +740,7 @@ attn_fwd_short_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_con
             ptx::mbar_init(bar(G::kBarPFull + i), 2 * kBM);
             ptx::mbar_init(bar(G::kBarPVDone + i), 1);
             ptx::mbar_init(bar(G::kBarStats + i), 2 * kBM);
+            ptx::mbar_init(bar(G::kBarStatsFree + i), kBM);
         }
         ptx::mbar_init(bar(G::kBarOFull), 1);
         ptx::mbar_init(bar(G::kBarOEmpty), kBM);
@@ -762,7 +764,7 @@ attn_fwd_short_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_con
         if (lane == 0) {
             // -------------------------------------------------------------- TMA producer
             // Per unit: its query tile into buffer u & 1 (once the unit two back has had its
-            // last S GEMM), then K_j, V_j for each key tile through the ring.
+            // last S GEMM), then K_j, V_j for each key tile into step slot g & 1.
             const uint64_t pol_kv = ptx::policy_evict_last();
             const uint64_t pol_q = ptx::policy_evict_first();
             uint32_t g = 0;               // step index (monotonic over the CTA's units)
@@ -818,8 +820,8 @@ attn_fwd_short_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_con
         // ------------------------------------------------------------------ MMA issuers
         // Two threads on different sub-partitions: this one issues the S GEMMs, warp 13's
         // the PV GEMMs.  The CTA's steps (one per key tile of each of its units) run in
-        // order g = 0, 1, ...: K_g is ring position 2g, V_g position 2g + 1, S_g goes to S
-        // buffer g & 1, and P_g overwrites it.  S_g may be issued once PV_{g-2} (the last
+        // order g = 0, 1, ...: K_g and V_g are in step slot g & 1, S_g goes to S buffer g & 1,
+        // and P_g overwrites it.  S_g may be issued once PV_{g-2} (the last
         // reader of that buffer) is done, so the next tile's logits are ready when the
         // softmax finishes P_{g-1}, also across a unit boundary.
         constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false, false);
@@ -1042,8 +1044,13 @@ attn_fwd_short_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_con
                 ptx::mbar_arrive(bar(G::kBarPFull + (int)(g & 1u)));
             }
             if (!ok) break;
-            // this half's (m, l) for the epilogue; the buffer of the unit two back was read
-            // before that unit's O was released, which this thread's PV waits have followed
+            // this half's (m, l) for the epilogue, into the buffer of the unit two back once the
+            // epilogue has read that unit's (units of one key tile can run that far ahead)
+            if (u >= 2) {
+                ok = wait_bar(bar(G::kBarStatsFree + (u & 1)), (uint32_t)((u >> 1) - 1) & 1u, kSiteStats, abort_flag,
+                              lim);
+                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+            }
             stats[((u & 1) * 2 + h) * kBM + row] = make_float2(m_ref, l);
             ptx::mbar_arrive(bar(G::kBarStats + (u & 1)));
         }
@@ -1069,6 +1076,7 @@ attn_fwd_short_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_con
             ptx::tc_fence_after();
             const float2 sa = stats[((u & 1) * 2 + 0) * kBM + row];
             const float2 sb = stats[((u & 1) * 2 + 1) * kBM + row];
+            ptx::mbar_arrive(bar(G::kBarStatsFree + (u & 1)));
             const float m = fmaxf(sa.x, sb.x);
             const float wa = (sa.x == -INFINITY) ? 0.0f : ptx::ex2_approx(fmaxf((sa.x - m) * c, -125.0f));
             const float wb = (sb.x == -INFINITY) ? 0.0f : ptx::ex2_approx(fmaxf((sb.x - m) * c, -125.0f));

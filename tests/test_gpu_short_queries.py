@@ -91,3 +91,18 @@ def test_short_queries_many_units_causal_and_splits(attn, d):
     q, k, v = make_qkv(2, 100, 100, 400, d, "bhsd", seed=3600 + d)
     check_ex(attn, q, k, v, "bhsd", "rtna", causal=True, max_ctas=19)
     check_ex(attn, q, k, v, "bhsd", "rtz", force_splits=2, max_ctas=23)
+
+
+@pytest.mark.parametrize("case", ["skv_le_128", "one_tile_splits", "causal_one_tile"])
+def test_short_queries_one_tile_units_many_per_cta(attn, case):
+    # units (or key splits) of a single key tile, many per CTA: the softmax warpgroups can then
+    # finish a unit two ahead of the epilogue, and the per-unit statistics hand-off must hold
+    if case == "skv_le_128":
+        q, k, v = make_qkv(4, 100, 32, 100, 128, "bshd", seed=3700)
+        check_ex(attn, q, k, v, "bshd", "rtne", max_ctas=3)
+    elif case == "one_tile_splits":
+        q, k, v = make_qkv(1, 8, 64, 512, 128, "bhsd", seed=3701)
+        check_ex(attn, q, k, v, "bhsd", "rtz", force_splits=4, max_ctas=2)
+    else:
+        q, k, v = make_qkv(2, 200, 100, 100, 64, "bhsd", seed=3702)
+        check_ex(attn, q, k, v, "bhsd", "rtna", causal=True, max_ctas=5)
