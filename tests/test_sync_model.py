@@ -1,8 +1,10 @@
-"""Executable model of the short-query forward kernel's synchronisation (host only, no GPU).
+"""Executable models of the forward kernels' synchronisation (host only, no GPU).
 
 attn_fwd_short_kernel (csrc/attn_fwd.cu) runs six roles per CTA that meet only through
 mbarriers: the TMA producer, the S-GEMM issuer, the PV-GEMM issuer, the two softmax halves and
-the merge/epilogue warpgroup.  This model restates each role as a sequence of barrier waits,
+the merge/epilogue warpgroup (`Model`); attn_fwd_kernel runs four (the producer with its K/V
+ring, one MMA thread, two softmax warpgroups; `MainModel`).  Each model restates every role
+as a sequence of barrier waits,
 arrivals and asynchronous completions (TMA loads, tcgen05 commits), in the kernel's order, and
 runs it under many random schedules and unit lengths.  It checks:
 
@@ -14,7 +16,8 @@ runs it under many random schedules and unit lengths.  It checks:
   memory; Q, K, V tiles; the per-unit statistics) never meets a buffer holding the wrong step's
   or unit's data.
 
-A planted mistake (the statistics buffer reused without the epilogue's release) must be caught.
+Planted mistakes (the statistics buffer reused without the epilogue's release; a ring slot
+refilled without its release) must be caught.
 The model mirrors the protocol, not the arithmetic; a change to the kernel's barriers must be
 made here too.
 """
@@ -221,12 +224,17 @@ class Model:
     def run(self, max_events=200000):
         roles = {"producer": self.producer(), "s": self.s_issuer(), "pv": self.pv_issuer(),
                  "sm0": self.softmax(0), "sm1": self.softmax(1), "epi": self.epilogue()}
+        self._schedule(roles, max_events)
+
+    def _schedule(self, roles, max_events):
+        """Advance a random runnable role, or complete the earliest asynchronous operation
+        (always when every role is blocked, sometimes otherwise); no role runnable and nothing
+        in flight is a deadlock."""
         blocked = {}
         for _ in range(max_events):
             live = [r for r in roles if roles[r] is not None]
             if not live and not self.pending:
                 return
-            # runnable roles: not blocked, or blocked on a barrier that may have moved
             cand = live[:]
             self.rng.shuffle(cand)
             progressed = False
@@ -279,6 +287,159 @@ def test_planted_missing_statistics_release_is_caught():
     for seed in range(400):
         try:
             Model([1] * 8, random.Random(seed), release_stats=False).run()
+        except (Violation, Deadlock):
+            found = True
+            break
+    assert found
+
+
+class MainModel(Model):
+    """attn_fwd_kernel's protocol: one CTA, units of two query tiles, a K,V,K,V ring of
+    `stages` slots with full/empty barriers, one MMA thread issuing S_t(j+1) right after
+    PV_t(j) (in order), and two softmax warpgroups that each run their tile's epilogue."""
+
+    def __init__(self, units, rng, stages=4, wait_empty=True):
+        self.units, self.rng, self.S, self.wait_empty = units, rng, stages, wait_empty
+        self.b = {}
+        for i in range(stages):
+            self.b[("Full", i)] = Barrier("Full[%d]" % i, 1)
+            self.b[("Empty", i)] = Barrier("Empty[%d]" % i, 1)
+        for t in range(2):
+            for n in ("SFull", "PFull", "OFull"):
+                self.b[(n, t)] = Barrier("%s[%d]" % (n, t), 1)
+        self.b[("QFull", 0)] = Barrier("QFull", 1)
+        self.b[("QEmpty", 0)] = Barrier("QEmpty", 1)
+        self.ring = [None] * stages            # ring position held by each slot
+        self.q = None                          # unit whose Q tiles are loaded
+        self.s_buf = [None, None]              # ("S", step) / ("P", step) per tile
+        self.o = [None, None]                  # (unit, steps accumulated) per tile
+        self.pending, self.now, self.seq, self.last_done = [], 0, 0, {}
+
+    def producer(self):
+        pos = 0
+        for u, nk in enumerate(self.units):
+            if u > 0:
+                yield from self.wait(("QEmpty", 0), u - 1)
+
+            def load_q(u=u):
+                self.q = u
+                self.b[("QFull", 0)].arrive()
+            self.later(load_q)
+            for _ in range(nk):
+                for _kv in range(2):
+                    slot = pos % self.S
+                    if pos >= self.S and self.wait_empty:
+                        yield from self.wait(("Empty", slot), pos // self.S - 1)
+                    self.check(self.ring[slot] in (None, pos - self.S), "ring slot overwritten early")
+
+                    def load(slot=slot, pos=pos):
+                        self.ring[slot] = pos
+                        self.b[("Full", slot)].arrive()
+                    self.later(load)
+                    pos += 1
+                yield ("step",)
+
+    def mma(self):
+        pos = 0
+        g = 0                                  # steps consumed (same count for both tiles)
+        for u, nk in enumerate(self.units):
+            yield from self.wait(("QFull", 0), u)
+            kslot = pos % self.S
+            yield from self.wait(("Full", kslot), pos // self.S)
+            for t in range(2):
+                self.later(self._s(t, u, g, kslot, pos), channel="mma")
+            self.later(self._commit(("Empty", kslot)), channel="mma")
+            if nk == 1:
+                self.later(self._commit(("QEmpty", 0)), channel="mma")
+            pos += 1
+            for jj in range(nk):
+                vpos = pos
+                vslot = vpos % self.S
+                more = jj + 1 < nk
+                yield from self.wait(("Full", vslot), vpos // self.S)
+                kpos = vpos + 1
+                kslot = kpos % self.S
+                for t in range(2):
+                    yield from self.wait(("PFull", t), g)
+                    self.later(self._pv(t, u, g, jj, vslot, vpos), channel="mma")
+                    if not more:
+                        self.later(self._commit(("OFull", t)), channel="mma")
+                    if t == 1:
+                        self.later(self._commit(("Empty", vslot)), channel="mma")
+                    if more:
+                        if t == 0:
+                            yield from self.wait(("Full", kslot), kpos // self.S)
+                        self.later(self._s(t, u, g + 1, kslot, kpos), channel="mma")
+                        if t == 1:
+                            self.later(self._commit(("Empty", kslot)), channel="mma")
+                            if jj + 2 == nk:
+                                self.later(self._commit(("QEmpty", 0)), channel="mma")
+                g += 1
+                pos += 2 if more else 1
+                yield ("step",)
+
+    def _commit(self, key):
+        return lambda: self.b[key].arrive()
+
+    def _s(self, t, u, g, kslot, kpos):
+        def run():
+            self.check(self.q == u, "S GEMM read another unit's Q")
+            self.check(self.ring[kslot] == kpos, "S GEMM read the wrong K")
+            self.check(self.s_buf[t] in (None, ("P", g - 1)), "S overwrote P before its PV")
+            self.s_buf[t] = ("S", g)
+            self.b[("SFull", t)].arrive()
+        return run
+
+    def _pv(self, t, u, g, jj, vslot, vpos):
+        def run():
+            self.check(self.s_buf[t] == ("P", g), "PV read the wrong P")
+            self.check(self.ring[vslot] == vpos, "PV read the wrong V")
+            if jj == 0:
+                self.check(self.o[t] is None, "PV overwrote O before the epilogue read it")
+                self.o[t] = (u, 0)
+            self.check(self.o[t] == (u, jj), "PV accumulated out of order")
+            self.o[t] = (u, jj + 1)
+        return run
+
+    def softmax(self, t):
+        g = 0
+        for u, nk in enumerate(self.units):
+            for jj in range(nk):
+                yield from self.wait(("SFull", t), g)
+                self.check(self.s_buf[t] == ("S", g), "softmax read the wrong S")
+                if jj > 0 and self.rng.random() < 0.2:
+                    # lazy rescale reads O_t: S_t(g) completing implies PV_t(g-1) did (in order)
+                    self.check(self.o[t] == (u, jj), "rescale met O mid-update")
+                yield ("step",)
+                self.s_buf[t] = ("P", g)
+                self.b[("PFull", t)].arrive()
+                g += 1
+            yield from self.wait(("OFull", t), u)
+            self.check(self.o[t] == (u, nk), "epilogue read an unfinished O")
+            yield ("step",)
+            self.o[t] = None                   # read out; the next unit's first PV may write
+
+    def run(self, max_events=200000):
+        roles = {"producer": self.producer(), "mma": self.mma(), "sm0": self.softmax(0),
+                 "sm1": self.softmax(1)}
+        self._schedule(roles, max_events)
+
+
+
+
+@pytest.mark.parametrize("stages", [4, 8])
+@pytest.mark.parametrize("units", UNIT_PATTERNS, ids=lambda u: "-".join(map(str, u)))
+def test_main_kernel_protocol(units, stages):
+    for seed in range(100):
+        MainModel(units, random.Random(seed * 104729 + stages), stages).run()
+
+
+def test_main_kernel_planted_missing_release_is_caught():
+    # a producer that refills a ring slot without waiting for its release must be caught
+    found = False
+    for seed in range(300):
+        try:
+            MainModel([3, 2, 4], random.Random(seed), 4, wait_empty=False).run()
         except (Violation, Deadlock):
             found = True
             break
