@@ -516,6 +516,135 @@ def pin_brute_force_causal_lse_mpmath(lib):
                     assert res["o_bits"][0, h, i, x] == bx.round_exact(val, "rtne")
 
 
+# --------------------------------------------------------------------------- error scales
+# A = sum_j w_j |v_jx| / l is the forward-error scale of output column x: the parity
+# criterion accepts |gpu - O| <= 2^-8 A + ulp(O) where the literal 2-ULP rule cannot hold.
+# A too large would silently widen every GPU check, so its value is pinned here on its own.
+def pin_error_scale_nonnegative_v_is_output(lib):
+    """V >= 0: every term w_j v_jx is non-negative, so A equals O itself (the same sums)."""
+    for layout in ("bshd", "bhsd"):
+        q, k, v = make_qkv(1, 2, 5, 70, D, layout, seed=500, sigma=2.0)
+        v = v.abs()
+        res = oracle.attention(q, k, v, layout, "rtne", want_f64=True, want_a=True, lib=lib)
+        assert np.all(res["o_f64"] > 0)
+        assert np.allclose(res["a"], res["o_f64"], rtol=1e-14, atol=0), layout
+
+
+def pin_error_scale_uniform_weights(lib):
+    """Q = 0: every logit is 0, every weight 1 and l = Skv, so A is the column mean of |V|
+    (and |O| <= A, with equality only where a column has one sign)."""
+    q, k, v = make_qkv(1, 2, 3, 41, D, "bshd", seed=501)
+    q = torch.zeros_like(q)
+    res = oracle.attention(q, k, v, "bshd", "rtne", want_f64=True, want_a=True, lib=lib)
+    vv = v.permute(0, 2, 1, 3).double().numpy()                  # (B, H, Skv, d)
+    mean_abs = np.abs(vv).mean(axis=2, keepdims=True)
+    assert np.allclose(res["a"], np.broadcast_to(mean_abs, res["a"].shape), rtol=1e-14, atol=0)
+    assert np.all(np.abs(res["o_f64"]) <= res["a"] * (1 + 1e-14))
+    assert np.any(np.abs(res["o_f64"]) < 0.5 * res["a"])          # cancellation is present
+
+
+def pin_error_scale_two_keys(lib):
+    """Two keys: A = sigma(s1 - s2) |v1| + sigma(s2 - s1) |v2| with s = q.k / sqrt(d)."""
+    g = torch.Generator().manual_seed(502)
+    q = torch.randn(1, 1, 6, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(1, 1, 2, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, 1, 2, D, generator=g).to(torch.bfloat16)
+    res = oracle.attention(q, k, v, "bhsd", "rtne", want_a=True, lib=lib)
+    qd, kd, vd = q.double()[0, 0], k.double()[0, 0], v.double()[0, 0].abs().numpy()
+    for i in range(6):
+        s = [float((qd[i] * kd[j]).sum()) / math.sqrt(D) for j in range(2)]
+        a = 1.0 / (1.0 + math.exp(s[1] - s[0]))
+        want = a * vd[0] + (1.0 - a) * vd[1]
+        assert np.allclose(res["a"][0, 0, i], want, rtol=1e-13, atol=0), i
+
+
+def pin_error_scale_brute_force_mpmath(lib):
+    """A against 50-digit arithmetic on tiny shapes (d = 128 and 64), to 1e-13 relative."""
+    import mpmath
+    mpmath.mp.dps = 50
+    for seed, (Sq, Skv, d, sigma) in enumerate(((2, 3, D, 1.0), (3, 6, D, 4.0), (2, 5, 64, 2.0))):
+        q, k, v = make_qkv(1, 1, Sq, Skv, d, "bhsd", seed=510 + seed, sigma=sigma)
+        res = oracle.attention(q, k, v, "bhsd", "rtne", want_a=True, lib=lib)
+        qd, kd, vd = (t.double().numpy()[0, 0] for t in (q, k, v))
+        inv = 1 / mpmath.sqrt(d)
+        for i in range(Sq):
+            s = [mpmath.fsum(mpmath.mpf(float(qd[i, x])) * mpmath.mpf(float(kd[j, x]))
+                             for x in range(d)) * inv for j in range(Skv)]
+            m = max(s)
+            w = [mpmath.exp(sj - m) for sj in s]
+            l = mpmath.fsum(w)
+            for x in range(d):
+                want = mpmath.fsum(w[j] * abs(mpmath.mpf(float(vd[j, x]))) for j in range(Skv)) / l
+                got = res["a"][0, 0, i, x]
+                assert abs(got - float(want)) <= 1e-13 * float(want), (seed, i, x, got, want)
+
+
+def pin_bwd_error_scales_single_key(lib):
+    """One key: p = 1 for every row, so with dP_i = dO_i.v and |D|_i = sum_x |dO_ix| |v_x|
+    (O_i = v):  dV_a = sum over the rows and query heads of |dO_i|,
+    dQ_a[i, x] = c (|dP_i| + |D|_i) |k_x|,  dK_a[x] = c sum_i (|dP_i| + |D|_i) |q_ix|."""
+    g0 = torch.Generator().manual_seed(520)
+    H, Hkv, Sq, d = 4, 2, 5, 32
+    q = torch.randn(1, H, Sq, d, generator=g0).to(torch.bfloat16)
+    k = torch.randn(1, Hkv, 1, d, generator=g0).to(torch.bfloat16)
+    v = torch.randn(1, Hkv, 1, d, generator=g0).to(torch.bfloat16)
+    g = torch.randn(1, H, Sq, d, generator=g0).to(torch.bfloat16)
+    res = oracle.backward(q, k, v, g, "bhsd", want_a=True, lib=lib)
+    c = 1.0 / math.sqrt(d)
+    qd, kd, vd, gd = (t.double().numpy()[0] for t in (q, k, v, g))
+    grp = H // Hkv
+    for kh in range(Hkv):
+        heads = range(kh * grp, (kh + 1) * grp)
+        dv_a = sum(np.abs(gd[h]).sum(axis=0) for h in heads)
+        assert np.allclose(res["dv_a"][0, kh, 0], dv_a, rtol=1e-14, atol=0), kh
+        dk_a = np.zeros(d)
+        for h in heads:
+            dp = gd[h] @ vd[kh, 0]                                  # (Sq,)
+            dabs = np.abs(gd[h]) @ np.abs(vd[kh, 0])                # (Sq,)
+            coef = np.abs(dp) + dabs
+            want_dq = c * coef[:, None] * np.abs(kd[kh, 0])[None, :]
+            assert np.allclose(res["dq_a"][0, h], want_dq, rtol=1e-13, atol=0), h
+            dk_a += c * (coef[:, None] * np.abs(qd[h])).sum(axis=0)
+        assert np.allclose(res["dk_a"][0, kh, 0], dk_a, rtol=1e-13, atol=0), kh
+
+
+def pin_bwd_error_scales_brute_force_mpmath(lib):
+    """dQ_a, dK_a and dV_a against 50-digit sums of the term magnitudes on a 2 x 3 case:
+    dV_a[j] = sum_i p_ij |dO_i|, dQ_a[i] = c sum_j p_ij (|dP_ij| + |D|_i) |k_j| and
+    dK_a[j] = c sum_i p_ij (|dP_ij| + |D|_i) |q_i|, with |D|_i = sum_x |dO_ix| |O_ix|."""
+    import mpmath
+    mpmath.mp.dps = 50
+    g0 = torch.Generator().manual_seed(530)
+    Sq, Skv, d = 2, 3, 16
+    q, k, v, g = (torch.randn(1, 1, n, d, generator=g0).to(torch.bfloat16)
+                  for n in (Sq, Skv, Skv, Sq))
+    res = oracle.backward(q, k, v, g, "bhsd", want_a=True, lib=lib)
+    mp = lambda t: [[mpmath.mpf(float(x)) for x in row] for row in t.double().numpy()[0, 0]]
+    Q, K, V, G = mp(q), mp(k), mp(v), mp(g)
+    c = 1 / mpmath.sqrt(d)
+    dot = lambda a, b: mpmath.fsum(x * y for x, y in zip(a, b))
+    P, coef = [], []
+    for i in range(Sq):
+        s = [c * dot(Q[i], K[j]) for j in range(Skv)]
+        m = max(s)
+        w = [mpmath.exp(t - m) for t in s]
+        l = mpmath.fsum(w)
+        p = [t / l for t in w]
+        o = [mpmath.fsum(p[j] * V[j][x] for j in range(Skv)) for x in range(d)]
+        dabs = mpmath.fsum(abs(G[i][x]) * abs(o[x]) for x in range(d))
+        P.append(p)
+        coef.append([p[j] * (abs(dot(G[i], V[j])) + dabs) for j in range(Skv)])
+    for x in range(d):
+        for i in range(Sq):
+            want = c * mpmath.fsum(coef[i][j] * abs(K[j][x]) for j in range(Skv))
+            assert abs(res["dq_a"][0, 0, i, x] - float(want)) <= 1e-13 * float(want), (i, x)
+        for j in range(Skv):
+            want_k = c * mpmath.fsum(coef[i][j] * abs(Q[i][x]) for i in range(Sq))
+            want_v = mpmath.fsum(P[i][j] * abs(G[i][x]) for i in range(Sq))
+            assert abs(res["dk_a"][0, 0, j, x] - float(want_k)) <= 1e-13 * float(want_k), (j, x)
+            assert abs(res["dv_a"][0, 0, j, x] - float(want_v)) <= 1e-13 * float(want_v), (j, x)
+
+
 # --------------------------------------------------------------------------- backward
 def _fd_gradients(q, k, v, g, layout, causal, lib, h=1e-6):
     """Central differences of L = sum(dO * O) through the fp64 forward, for every element of

@@ -41,6 +41,11 @@ MUTANTS = {
     "lse_drops_max": ("if (lse) lse[slot] = m + log(l);", "if (lse) lse[slot] = log(l);"),
     "posinf_logit_ignored": ("if (isnan(s[j]) || (isinf(s[j]) && s[j] > 0)) any_nan_or_posinf = 1;",
                              "if (isnan(s[j])) any_nan_or_posinf = 1;"),
+    # the forward-error scale A, which sets the parity tolerance
+    "a_not_divided_by_l": ("isfinite(ox) ? absnum / l : NAN", "isfinite(ox) ? absnum : NAN"),
+    "a_divided_by_l_twice": ("isfinite(ox) ? absnum / l : NAN", "isfinite(ox) ? absnum / l / l : NAN"),
+    "a_unweighted": ("absnum += w[j] * fabs(vj);", "absnum += fabs(vj);"),
+    "a_signed": ("absnum += w[j] * fabs(vj);", "absnum += w[j] * vj;"),
 }
 
 # planted mistakes in the backward source
@@ -50,6 +55,12 @@ MUTANTS_BWD = {
     "bwd_dv_uses_ds": ("dv[off] += p[j] * gi[x];", "dv[off] += (p[j] - Di * 0.0 + dp[j] * p[j]) * gi[x];"),
     "bwd_dq_sign": ("acc += p[j] * (dp[j] - Di) * kjx;", "acc += p[j] * (Di - dp[j]) * kjx;"),
     "bwd_causal_sees_all": ("if (!causal) return Skv;", "return Skv;"),
+    # the backward's error scales
+    "bwd_dabs_is_abs_delta": ("(fabs(dp[j]) + Dabs)", "(fabs(dp[j]) + fabs(Di))"),
+    "bwd_dv_a_unweighted": ("dv_a[off] += p[j] * fabs(gi[x]);", "dv_a[off] += fabs(gi[x]);"),
+    "bwd_dq_a_unscaled": ("if (dq_a) dq_a[off] = c * mag;", "if (dq_a) dq_a[off] = mag;"),
+    "bwd_dk_a_drops_dp": ("const double dsa = p[j] * (fabs(dp[j]) + Dabs);",
+                          "const double dsa = p[j] * Dabs;"),
 }
 
 
