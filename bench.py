@@ -2,10 +2,15 @@
 """Benchmark of the GB300 bf16 attention forward (one JSON line on rank 0).
 
 Metric: attention forward TFLOPS = 4*B*H*Sq*Skv*d per call / time, and its fraction of the
-measured GB300 dense bf16 peak.  Default workload: the square self-attention B=4, H=16,
-Sq=Skv=2048, d=128, BHSD, where one step runs the three output rounding modes (RTNE, RTNA,
-RTZ) back to back.  Inputs are seeded synthetic N(0,1) bf16 tensors already resident in HBM;
-consecutive calls rotate over enough input sets that their total exceeds the 126 MB L2.
+measured GB300 dense bf16 peak.  Default workload: the largest single-GPU configuration, the
+video-diffusion self-attention B=1, H=12, Sq=Skv=32760, d=128, BSHD, where one step runs its
+two output rounding modes (RTNE, RTZ) back to back.  Inputs are seeded synthetic N(0,1) bf16
+tensors already resident in HBM; where one input set is smaller than twice the 126 MB L2,
+consecutive calls rotate over enough sets that their total exceeds it.
+
+The roofline's kernel time is the timed per-call time times the attention kernel's share of
+a call, measured in a second pass with events around each kernel; it can never exceed the
+per-call time.  The raw event time of the second pass is reported beside it.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -50,7 +55,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
-    ap.add_argument("--workload", default="square", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="video", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -412,7 +417,14 @@ def main():
     value = whole_job_tflops(world, flop_call, n_launch, elapsed_ms)
 
     peak, peak_sust, hbm, peak_src = measured_peaks()
-    main_avg = statistics.mean(main_ms)
+    # The attention kernel's time: the timed per-call time times the kernel's share of a
+    # call in the event pass (events between the kernels serialise the combine's launch and
+    # add their own cost, so the raw event times run long on short calls).
+    call_ms = elapsed_ms / n_launch
+    main_ev, comb_ev = statistics.mean(main_ms), statistics.mean(comb_ms)
+    share = main_ev / (main_ev + comb_ev) if split else 1.0
+    main_avg = call_ms * share
+    assert main_avg <= call_ms * (1 + 1e-12), (main_avg, call_ms)
     achieved = flop_call / (main_avg * 1e-3) / 1e12
     # the kernel that runs: one 128-row query tile per (b, h) takes the short-query kernel
     kernel = "attn_fwd_short_kernel" if w.Sq <= 128 else "attn_fwd_kernel"
@@ -433,16 +445,19 @@ def main():
                     "frac_of_sustained": (achieved / peak_sust) if peak_sust else None}
     roofline.update({"kernel": kernel, "algorithmic_bytes": w.min_bytes, "flop_per_launch": flop_call,
                      "intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
-                     "kernel_ms_avg": main_avg, "kernel_ms_median": statistics.median(main_ms)})
+                     "kernel_ms_avg": main_avg, "call_ms_avg": call_ms, "kernel_share_of_call": share,
+                     "kernel_ms_events_avg": main_ev,
+                     "kernel_ms_events_median": statistics.median(main_ms)})
     extra = {}
     if split:
         # workspace rows that hold real queries: 256 per split unit, Sq when that is fewer
         rows = plan["split_units"] * min(256, w.Sq)
-        comb_bytes = rows * plan["splits"] * (128 * 4 + 4) + min(rows, w.B * w.H * w.Sq) * 256
-        ca = statistics.mean(comb_ms)
-        extra["combine"] = {"ms_avg": ca, "algorithmic_bytes": comb_bytes,
+        comb_bytes = rows * plan["splits"] * (w.d * 4 + 4) + min(rows, w.B * w.H * w.Sq) * 2 * w.d
+        ca = call_ms - main_avg
+        extra["combine"] = {"ms_avg": ca, "ms_events_avg": comb_ev, "algorithmic_bytes": comb_bytes,
                             "achieved_gbs": comb_bytes / (ca * 1e-3) / 1e9, "peak_gbs": hbm,
-                            "frac": comb_bytes / (ca * 1e-3) / 1e9 / hbm}
+                            "frac": comb_bytes / (ca * 1e-3) / 1e9 / hbm,
+                            "traffic": recorded_traffic(w.name, "attn_combine_kernel")}
 
     # end to end through the public API with host buffers (pinned), copies timed
     e2e = None

@@ -33,7 +33,7 @@ class AttnError(RuntimeError):
 
 class Options(ctypes.Structure):
     _fields_ = [("force_splits", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
-                ("wait_limit_ms", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
+                ("wait_limit_ms", ctypes.c_uint32), ("test_hooks", ctypes.c_uint32),
                 ("events", ctypes.c_void_p * 3)]
 
 
@@ -49,7 +49,7 @@ class BwdArgs(ctypes.Structure):
     """attn_bwd_args_t: the argument set of attn_bwd."""
     _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv")] + \
                [(n, ctypes.c_int64) for n in ("B", "H", "Hkv", "Sq", "Skv", "d")] + \
-               [(n, ctypes.c_int32) for n in ("layout", "causal", "reserved0", "reserved1")]
+               [(n, ctypes.c_int32) for n in ("layout", "causal", "wait_limit_ms", "test_hooks")]
 
 
 class Plan(ctypes.Structure):
@@ -162,10 +162,10 @@ def _stream_ptr(stream, device):
     return ctypes.c_void_p(s.cuda_stream if hasattr(s, "cuda_stream") else int(s))
 
 
-def _opts(force_splits=0, max_ctas=0, wait_limit_ms=0, events=None):
-    if not (force_splits or max_ctas or wait_limit_ms or events):
+def _opts(force_splits=0, max_ctas=0, wait_limit_ms=0, events=None, test_hooks=0):
+    if not (force_splits or max_ctas or wait_limit_ms or events or test_hooks):
         return None
-    o = Options(int(force_splits), int(max_ctas), int(wait_limit_ms), 0)
+    o = Options(int(force_splits), int(max_ctas), int(wait_limit_ms), int(test_hooks))
     if events:
         for i, e in enumerate(events[:3]):
             o.events[i] = None if e is None else int(e.cuda_event)
@@ -191,13 +191,15 @@ def workspace_size(B, H, Sq, Skv, d=128, force_splits=0, max_ctas=0) -> int:
 
 def attn_fwd(q, k, v, o=None, layout: str = "bshd", round: str = "rtne", stream=None,
              workspace=None, force_splits: int = 0, max_ctas: int = 0, wait_limit_ms: int = 0,
-             events=None):
-    """O = softmax(Q K^T / sqrt(128)) V on CUDA tensors (bf16, contiguous, same layout).
+             events=None, test_hooks: int = 0):
+    """O = softmax(Q K^T / sqrt(d)) V on CUDA tensors (bf16, contiguous, same layout; d is
+    the head dimension, 128 or 64).
 
     ``workspace``: optional caller tensor (any dtype, CUDA) used through ``attn_fwd_ws``;
     with the knobs set and no workspace, one is allocated here with torch.  ``events``: up to
     three ``torch.cuda.Event`` recorded around the attention and combine kernels on the
-    launching stream.  Returns ``o``.
+    launching stream.  ``test_hooks``: 0 for normal use (ATTN_TEST_WITHHOLD_O_READY = 1 makes a
+    bounded wait expire, to test that path).  Returns ``o``.
     """
     import torch
     if layout not in LAYOUTS or round not in MODES:
@@ -209,7 +211,7 @@ def attn_fwd(q, k, v, o=None, layout: str = "bshd", round: str = "rtne", stream=
     _check_out(o, q)
     sp = _stream_ptr(stream, q.device)
     lib = load()
-    opts = _opts(force_splits, max_ctas, wait_limit_ms, events)
+    opts = _opts(force_splits, max_ctas, wait_limit_ms, events, test_hooks)
     if workspace is None and opts is None:
         st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, Sq,
                           Skv, d, LAYOUTS[layout], MODES[round], sp)
@@ -308,10 +310,12 @@ def device_status(stream=None) -> tuple:
 
 
 def attn_bwd(q, k, v, o, dout, lse, layout: str = "bshd", causal: bool = False, dq=None, dk=None,
-             dv=None, workspace=None, stream=None):
+             dv=None, workspace=None, stream=None, wait_limit_ms: int = 0, test_hooks: int = 0):
     """Gradients (dq, dk, dv) of softmax(Q K^T / sqrt(d)) V for the upstream gradient ``dout``,
     from the forward's inputs, output ``o`` and fp32 row log-sum-exp ``lse`` ([B][H][Sq], as
-    returned by :func:`attn_fwd_ex` with ``return_lse``).  d = 128 or 64.  Returns (dq, dk, dv)."""
+    returned by :func:`attn_fwd_ex` with ``return_lse``).  d = 128 or 64.  ``wait_limit_ms``
+    bounds each wait in the kernel (0: 2000 ms); ``test_hooks`` is 0 for normal use (1 makes a
+    bounded wait expire, to test that path).  Returns (dq, dk, dv)."""
     import torch
     if layout not in LAYOUTS:
         raise ValueError("layout must be bshd or bhsd")
@@ -333,7 +337,8 @@ def attn_bwd(q, k, v, o, dout, lse, layout: str = "bshd", causal: bool = False, 
     a.q, a.k, a.v, a.o, a.dout = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr()
     a.lse, a.dq, a.dk, a.dv = lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
     a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d = B, H, Hkv, Sq, Skv, d
-    a.layout, a.causal, a.reserved0, a.reserved1 = LAYOUTS[layout], int(causal), 0, 0
+    a.layout, a.causal = LAYOUTS[layout], int(causal)
+    a.wait_limit_ms, a.test_hooks = int(wait_limit_ms), int(test_hooks)
     lib = load()
     need = int(lib.attn_bwd_workspace_size(ctypes.byref(a)))
     if workspace is None:

@@ -98,6 +98,7 @@ enum : uint32_t {
     kSiteKV = 1, kSiteKVEmpty, kSiteQFull, kSiteQEmpty, kSiteSFull, kSitePFull, kSiteDQFull,
     kSiteDQEmpty, kSiteDKVFull, kSiteDKVEmpty, kSiteStats, kSiteDPFull, kSiteRead
 };
+static_assert(kSiteDKVFull == ATTN_BWD_SITE_DKV_READY, "the dK/dV-ready wait site is part of the ABI");
 
 __device__ uint32_t g_bwd_status[2];   // [0] status code, [1] wait site
 
@@ -116,6 +117,7 @@ struct BwdParams {
     __nv_bfloat16* dv;
     long long kv_sb, kv_ss, kv_sh;   // element strides of dK/dV for b, s, h
     unsigned long long wait_limit_ns;
+    int test_hooks;              // ATTN_TEST_WITHHOLD_O_READY: CTA 0 skips its first unit's dK/dV-ready signal
 };
 
 struct Unit {
@@ -502,7 +504,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             if (un.nsteps == 0 && u > 0 &&
                 !(ok = bwd_wait(bar(kBarDKVEmpty), (u - 1) & 1u, kSiteDKVEmpty, abort_flag, lim)))
                 break;
-            ptx::mma_commit(bar(kBarDKVFull));
+            // (test hook: CTA 0 withholds its first unit's dK/dV-ready signal, so that the
+            // writer's bounded wait expires)
+            if (!(p.test_hooks && u == 0 && blockIdx.x == 0)) ptx::mma_commit(bar(kBarDKVFull));
             ptx::mma_commit(bar(kBarKVEmpty));
         }
         ptx::mma_commit(bar(kBarDrain));
@@ -708,7 +712,8 @@ int check_shape(const attn_bwd_args_t& a) {
     if (a.B < 1 || a.H < 1 || a.Hkv < 1 || a.Sq < 1 || a.Skv < 1 || a.d < 1) return ATTN_ERR_INVALID_ARG;
     if (a.H % a.Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (a.layout != ATTN_LAYOUT_BSHD && a.layout != ATTN_LAYOUT_BHSD) return ATTN_ERR_INVALID_ARG;
-    if ((a.causal != 0 && a.causal != 1) || a.reserved0 != 0 || a.reserved1 != 0) return ATTN_ERR_INVALID_ARG;
+    if ((a.causal != 0 && a.causal != 1) || a.wait_limit_ms < 0) return ATTN_ERR_INVALID_ARG;
+    if (a.test_hooks != 0 && a.test_hooks != ATTN_TEST_WITHHOLD_O_READY) return ATTN_ERR_INVALID_ARG;
     if (a.d != 128 && a.d != 64) return ATTN_ERR_UNSUPPORTED;
     const int64_t lim = (int64_t)1 << 30;
     if (a.Sq > lim || a.Skv > lim || a.B * a.H > lim || a.B * a.Hkv * cdiv(a.Skv, kBN) > lim ||
@@ -821,7 +826,8 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
         p.kv_sb = a.Hkv * a.Skv * d; p.kv_ss = d; p.kv_sh = a.Skv * d;
         q_sb = a.H * a.Sq * d; q_ss = d; q_sh = a.Sq * d;
     }
-    p.wait_limit_ns = 2000ull * 1000000ull;
+    p.wait_limit_ns = (unsigned long long)(a.wait_limit_ms > 0 ? a.wait_limit_ms : 2000) * 1000000ull;
+    p.test_hooks = a.test_hooks;
 
     if (cudaMemsetAsync(dq_acc, 0, (size_t)(a.B * a.H * a.Sq * d * 4), stream) != cudaSuccess) {
         cudaGetLastError();

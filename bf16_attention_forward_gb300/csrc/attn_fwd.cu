@@ -108,6 +108,7 @@ enum : uint32_t {
     kSiteQEmpty = 1, kSiteRingEmpty, kSiteQFull, kSiteRingFull, kSitePFull, kSiteSFull,
     kSiteOFull, kSiteDrain, kSiteTeardown, kSitePVDone, kSiteOEmpty, kSiteStats
 };
+static_assert(kSiteOFull == ATTN_SITE_O_READY, "the O-ready wait site is part of the ABI");
 
 __device__ uint32_t g_status[2];   // [0] status code, [1] wait site
 
@@ -129,6 +130,7 @@ struct FwdParams {
     long long o_sb, o_ss, o_sh;   // element strides of O for b, s, h
     float* lse;            // optional [B][H][Sq] natural-log log-sum-exp, or null
     unsigned long long wait_limit_ns;
+    int test_hooks;        // ATTN_TEST_WITHHOLD_O_READY: CTA 0 skips its first unit's O-ready signal
 };
 
 struct Item {
@@ -437,7 +439,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                             break;
                         ptx::tc_fence_after();
                         issue_o(t, vslot, jj == 0);
-                        if (!more) ptx::mma_commit(bar(G::kBarOFull + t));
+                        // (test hook: CTA 0 withholds its first unit's O-ready signal for tile 0,
+                        // so that the epilogue's bounded wait expires)
+                        if (!more && !(p.test_hooks && u == 0 && t == 0 && blockIdx.x == 0))
+                            ptx::mma_commit(bar(G::kBarOFull + t));
                         if (t == kQTiles - 1) ptx::mma_commit(bar(G::kBarEmpty + vslot));
                         if (more) {
                             if (t == 0) {
@@ -899,7 +904,9 @@ attn_fwd_short_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_con
                         }
                     }
                     ptx::mma_commit(bar(G::kBarPVDone + (int)sb));
-                    if (jj + 1 == nk) ptx::mma_commit(bar(G::kBarOFull));
+                    // (test hook: CTA 0 withholds its first unit's O-ready signal)
+                    if (jj + 1 == nk && !(p.test_hooks && u == 0 && blockIdx.x == 0))
+                        ptx::mma_commit(bar(G::kBarOFull));
                 }
             }
         }
@@ -1287,6 +1294,7 @@ int validate_shape(const attn_args_t& a, const attn_options_t* opts) {
     if ((a.causal != 0 && a.causal != 1) || a.reserved != 0) return ATTN_ERR_INVALID_ARG;
     if (a.d != 128 && a.d != 64) return ATTN_ERR_UNSUPPORTED;
     if (a.causal && opts && opts->force_splits > 1) return ATTN_ERR_UNSUPPORTED;
+    if (opts && opts->test_hooks != 0 && opts->test_hooks != ATTN_TEST_WITHHOLD_O_READY) return ATTN_ERR_INVALID_ARG;
     // TMA coordinates and the kernels' unit/row indices are int32
     const int64_t lim = (int64_t)1 << 30;
     if (a.Sq > lim || a.Skv > lim || a.B > lim || a.H > lim) return ATTN_ERR_UNSUPPORTED;
@@ -1456,6 +1464,7 @@ int launch(const attn_args_t& a, const attn_plan_t& pl, const attn_options_t* op
     else { p.o_sb = H * Sq * d; p.o_ss = d; p.o_sh = Sq * d; }
     const uint32_t ms = (opts && opts->wait_limit_ms) ? opts->wait_limit_ms : 2000u;
     p.wait_limit_ns = (unsigned long long)ms * 1000000ull;
+    p.test_hooks = opts ? (int)opts->test_hooks : 0;
 
     const attn_event_t* ev = opts ? opts->events : nullptr;
     if (ev && ev[0] && cudaEventRecord((cudaEvent_t)ev[0], stream) != cudaSuccess) return ATTN_ERR_CUDA;

@@ -78,12 +78,6 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint
         : "memory");
 }
 
-// Four fp32 additions to consecutive global floats (16-byte aligned), no return value.
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-
 // 4-D tiled bulk tensor store shared -> global (bulk-group completion).  Rows outside the
 // tensor's extent are clipped by the hardware.
 __device__ __forceinline__ void tma_store_4d(const void* tmap, uint32_t src, int c0, int c1, int c2,

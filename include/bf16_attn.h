@@ -74,12 +74,23 @@ typedef struct {
     int32_t force_splits;   /* 0: planner decides. n >= 1: split every unit's keys n ways  */
     int32_t max_ctas;       /* 0: one persistent CTA per SM. n >= 1: at most n CTAs         */
     uint32_t wait_limit_ms; /* 0: 2000 ms. Bound on any single wait inside the kernels      */
-    uint32_t reserved;
+    /* 0 for normal use.  ATTN_TEST_WITHHOLD_O_READY makes the first CTA skip the signal that
+     * its first unit's output accumulator is complete, so that the epilogue's bounded wait
+     * expires: the call then reports ATTN_ERR_DEVICE_TIMEOUT at site ATTN_SITE_O_READY
+     * through attn_get_device_status(), with its output partly unwritten, and the device
+     * stays usable.  It exists to test that path; any other value is ATTN_ERR_INVALID_ARG. */
+    uint32_t test_hooks;
     /* Events recorded on `stream` (NULL entries skipped): [0] before the attention kernel,
      * [1] after it, [2] after the split-combine kernel (or right after [1] if none runs).
      * They let a caller time the two kernels separately on the launching stream. */
     attn_event_t events[3];
 } attn_options_t;
+
+/* attn_options_t.test_hooks / attn_bwd_args_t.test_hooks value, and the wait site the
+ * expired wait reports (the forward's O-ready wait; the backward's dK/dV-ready wait). */
+#define ATTN_TEST_WITHHOLD_O_READY 1
+#define ATTN_SITE_O_READY 7
+#define ATTN_BWD_SITE_DKV_READY 9
 
 /* The work split chosen for a shape (host only, launches nothing). */
 typedef struct {
@@ -229,7 +240,13 @@ int attn_version(void);
  *   lse          the forward's fp32 [B][H][Sq] natural-log log-sum-exp (attn_fwd_ex's lse)
  *   dq, dk, dv   outputs, bf16, like q, k, v (round to nearest even); must not overlap the
  *                inputs, each other or the workspace
- *   causal       0 or 1, as in the forward;  reserved0, reserved1 must be 0
+ *   causal       0 or 1, as in the forward
+ *   wait_limit_ms  0: 2000 ms; otherwise the bound, in ms, on any single wait in the kernel
+ *   test_hooks   0 for normal use; ATTN_TEST_WITHHOLD_O_READY makes the first CTA skip the
+ *                signal that its first unit's dK/dV accumulators are complete, so that the
+ *                writer's bounded wait expires and attn_bwd_get_device_status() reports
+ *                ATTN_ERR_DEVICE_TIMEOUT at site ATTN_BWD_SITE_DKV_READY (the outputs are then
+ *                partly unwritten; the device stays usable).  It exists to test that path.
  * Rows of K/V that no query sees, and queries that see no key (causal, Sq > Skv; their
  * forward output is NaN), get zero gradients.  Inputs are expected finite.
  */
@@ -244,7 +261,7 @@ typedef struct {
     void* dk;
     void* dv;
     int64_t B, H, Hkv, Sq, Skv, d;
-    int32_t layout, causal, reserved0, reserved1;
+    int32_t layout, causal, wait_limit_ms, test_hooks;
 } attn_bwd_args_t;
 
 /* Workspace bytes attn_bwd needs (fp32 dQ accumulator and per-row statistics; 0 if invalid). */

@@ -8,6 +8,9 @@ The fraction that meets the literal rule is reported next to the pass/fail verdi
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 from tests import bf16_exact as bx
@@ -25,6 +28,14 @@ def bf16_ulp(bits: np.ndarray) -> np.ndarray:
     mag = bits.astype(np.int64) & 0x7FFF
     exp = np.maximum(mag >> 7, 1)
     return np.exp2(exp.astype(np.float64) - 127 - 7)
+
+
+def log_result(tag: str, res: dict) -> None:
+    """Append one comparison's summary to the JSON-lines file named by PARITY_LOG, if set."""
+    path = os.environ.get("PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(res, tag=tag)) + "\n")
 
 
 def compare(gpu_bits: np.ndarray, ref_bits: np.ndarray, ref_a: np.ndarray) -> dict:

@@ -180,3 +180,26 @@ def test_planner_head_dim_64(lib, shape):
     assert {k: v for k, v in p64.items() if k != "workspace_bytes"} == \
            {k: v for k, v in p128.items() if k != "workspace_bytes"}
     assert p64["workspace_bytes"] == p64["split_units"] * p64["splits"] * 256 * (64 * 4 + 4)
+
+
+def test_test_hooks_and_bwd_wait_limit_are_validated(lib):
+    """The forward's test_hooks accepts 0 or ATTN_TEST_WITHHOLD_O_READY only; the backward's
+    wait_limit_ms must be >= 0 and its test_hooks 0 or 1 (checked before any device call)."""
+    pl = attn.Plan()
+    o = attn.Options(0, 0, 0, 2)
+    assert lib.attn_plan(1, 1, 8, 8, 128, 152, ctypes.byref(o), ctypes.byref(pl)) == 1
+    o.test_hooks = 1
+    assert lib.attn_plan(1, 1, 8, 8, 128, 152, ctypes.byref(o), ctypes.byref(pl)) == 0
+    a = attn.BwdArgs()
+    for i, n in enumerate(("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv")):
+        setattr(a, n, (i + 1) * P)
+    a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d = 1, 1, 1, 8, 8, 128
+    ws = 16 * P
+    for bad in ({"wait_limit_ms": -1}, {"test_hooks": 2}, {"test_hooks": -1}):
+        a.wait_limit_ms, a.test_hooks = 0, 0
+        for k_, v_ in bad.items():
+            setattr(a, k_, v_)
+        assert lib.attn_bwd(ctypes.byref(a), ws, 1 << 20, None) == 1, bad
+        assert lib.attn_bwd_workspace_size(ctypes.byref(a)) == 0, bad
+    a.wait_limit_ms, a.test_hooks = 50, 1
+    assert lib.attn_bwd_workspace_size(ctypes.byref(a)) > 0

@@ -104,7 +104,7 @@ def test_backward_writes_stay_in_bounds(attn, case):
         outs.append((buf, view.view(ref.shape)))
     a = attn.BwdArgs()
     a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d = B, H, Hkv, Sq, Skv, d
-    a.layout, a.causal, a.reserved0, a.reserved1 = attn.LAYOUTS[layout], int(causal), 0, 0
+    a.layout, a.causal, a.wait_limit_ms, a.test_hooks = attn.LAYOUTS[layout], int(causal), 0, 0
     need = int(attn.load().attn_bwd_workspace_size(ctypes.byref(a)))
     assert need > 0
     wbuf, ws = guarded(need, "ws")

@@ -215,4 +215,7 @@ def test_workload_sampled_rows(attn, name):
     q, k, v = make_workload(w)
     rows = sample_rows(w.B, w.H, w.Sq, 96, seed=7)
     for mode in w.modes:
-        check_ex(attn, q, k, v, w.layout, mode, causal=w.causal, rows=rows)
+        res, _, _ = check_ex(attn, q, k, v, w.layout, mode, causal=w.causal, rows=rows)
+        parity.log_result("%s/%s" % (name, mode), res)
+        # fraction within 2 bf16 ULP of the oracle, floor just under the measured value
+        assert res["literal_frac"] >= 0.90, res

@@ -65,6 +65,7 @@ def test_tiny_workload(attn):
     w = WORKLOADS["tiny"]
     q, k, v = make_workload(w)
     res, _ = check(attn, q, k, v, w.layout, "rtne")
+    parity.log_result("tiny/rtne", res)
     assert res["literal_frac"] > 0.9
 
 
@@ -159,6 +160,12 @@ def test_underflowed_weight_keeps_infinity(attn):
         check(attn, q, k, v, "bhsd", "rtna", force_splits=fs)
 
 
+# Floors on the fraction of finite sampled outputs within 2 bf16 ULP of the oracle (the
+# literal rule; the rest pass the A-bound), set just under the measured values so that a
+# precision regression cannot hide behind the A-bound.  Stress has no finite output.
+LITERAL_FLOOR = {"square": 0.90, "cross": 0.90, "video": 0.90, "stress": 1.0}
+
+
 @pytest.mark.parametrize("name", ["square", "cross", "video", "stress"])
 def test_workload_sampled_rows(attn, name):
     w = WORKLOADS[name]
@@ -174,7 +181,9 @@ def test_workload_sampled_rows(attn, name):
         assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
         ref = oracle.attention(q, k, v, w.layout, mode, rows=rows, want_a=True)
         res = parity.compare(parity.gpu_rows_bits(o, w.layout, rows), ref["o_bits"], ref["a"])
+        parity.log_result("%s/%s" % (name, mode), res)
         assert res["ok"], (name, mode, res)
+        assert res["literal_frac"] >= LITERAL_FLOOR[name], (name, mode, res)
 
 
 def _mean_of_values_case(Skv, e_lo, e_hi, seed, Sq=130):
