@@ -218,4 +218,4 @@ def test_workload_sampled_rows(attn, name):
         res, _, _ = check_ex(attn, q, k, v, w.layout, mode, causal=w.causal, rows=rows)
         parity.log_result("%s/%s" % (name, mode), res)
         # fraction within 2 bf16 ULP of the oracle, floor just under the measured value
-        assert res["literal_frac"] >= 0.90, res
+        assert res["literal_frac"] >= 0.935, res

@@ -94,4 +94,4 @@ def test_workload_sampled_rows(attn):
         res, _, _ = check_ex(attn, q, k, v, w.layout, mode, rows=rows)
         parity.log_result("square_d64/%s" % mode, res)
         # fraction within 2 bf16 ULP of the oracle, floor just under the measured value
-        assert res["literal_frac"] >= 0.90, res
+        assert res["literal_frac"] >= 0.91, res

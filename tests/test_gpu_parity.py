@@ -66,7 +66,7 @@ def test_tiny_workload(attn):
     q, k, v = make_workload(w)
     res, _ = check(attn, q, k, v, w.layout, "rtne")
     parity.log_result("tiny/rtne", res)
-    assert res["literal_frac"] > 0.9
+    assert res["literal_frac"] >= 0.93
 
 
 @pytest.mark.parametrize("splits", [2, 3, 7])
@@ -163,7 +163,7 @@ def test_underflowed_weight_keeps_infinity(attn):
 # Floors on the fraction of finite sampled outputs within 2 bf16 ULP of the oracle (the
 # literal rule; the rest pass the A-bound), set just under the measured values so that a
 # precision regression cannot hide behind the A-bound.  Stress has no finite output.
-LITERAL_FLOOR = {"square": 0.90, "cross": 0.90, "video": 0.90, "stress": 1.0}
+LITERAL_FLOOR = {"square": 0.91, "cross": 0.915, "video": 0.91, "stress": 1.0}
 
 
 @pytest.mark.parametrize("name", ["square", "cross", "video", "stress"])
