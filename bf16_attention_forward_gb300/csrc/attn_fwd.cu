@@ -1182,69 +1182,104 @@ struct CombineParams {
     float* lse;            // optional [B][H][Sq] natural-log log-sum-exp, or null
 };
 
-// One warp per output row of a split unit: merge the nsplit partials with weights
-// 2^(LSE_s - max LSE), accumulating in fixed order s = 0..n-1.  Lanes read the split LSEs in
-// parallel (a row's chain of dependent loads is the combine's cost when nsplit is large); each
-// lane then owns D/32 of the D columns.  Launched as a programmatic dependent of the attention
-// kernel: it starts as that kernel's CTAs retire and waits for its memory before reading.
-// [MoonMath] "Data placement and the 16x16x16 choice" (tail KV split).
-template <int D>
+// Merge of the split partials: one output row of a split unit per group of W warps (W = 1,
+// 2, 4 or 8 by split count; 8 / W rows per 256-thread block).  Warp w of a row takes splits
+// w, w + W, w + 2W, ..., four at a time, with all four partial rows and their LSEs loaded
+// before the row's maximum LSE (read by the lanes in parallel) is reduced, so a row costs one
+// memory round trip when it has at most 4W splits.  Weights are 2^(LSE_s - max), clamped at
+// >= 2^-125 for a finite LSE_s; a -inf LSE weighs 0.  Each warp sums its splits in increasing
+// order, and the row's warps are then summed in warp order through shared memory: a fixed
+// order, so results are deterministic.  Each lane owns D/32 of the D columns.  Launched as a
+// programmatic dependent of the attention kernel: it starts as that kernel's CTAs retire and
+// waits for its memory before reading.  [MoonMath] "Data placement and the 16x16x16 choice"
+// (tail KV split).
+template <int D, int W>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p) {
-    constexpr int kC = D / 32;   // columns per lane: 4 or 2
+    constexpr int kC = D / 32;                 // columns per lane: 4 or 2
+    constexpr int kRowsPerBlock = 8 / W;
+    constexpr int kLoads = 4;                  // splits a warp has in flight
+    __shared__ float red[kRowsPerBlock][W > 1 ? W : 1][D + 1];   // per-warp sums (+ weight sum)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= (long long)p.split_units * kUnitRows) return;
-    const int t = (int)(gw / kUnitRows);
-    const int r = (int)(gw % kUnitRows);
-    const int unit = p.n_full + t;
-    const int qb = unit % p.nq, bh = unit / p.nq;
-    const int h = bh % p.H, b = bh / p.H;
-    const int qrow = qb * kUnitRows + r;
-    if (qrow >= p.Sq) return;
-    const long long base = (long long)t * p.nsplit * kUnitRows + r;
-    // split LSEs: lane s holds split s (and s + 32, ...)
-    float mx = -INFINITY;
-    bool any_nan = false;
-    for (int s = lane; s < p.nsplit; s += 32) {
-        const float e = p.ws_lse[base + (long long)s * kUnitRows];
-        any_nan |= (e != e);
-        mx = fmaxf(mx, e);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rsub = warp / W, w = warp % W;
+    const long long gr = (long long)blockIdx.x * kRowsPerBlock + rsub;
+    int t = 0, r = 0, b = 0, h = 0, qrow = 0;
+    bool valid = gr < (long long)p.split_units * kUnitRows;
+    if (valid) {
+        t = (int)(gr / kUnitRows);
+        r = (int)(gr % kUnitRows);
+        const int unit = p.n_full + t;
+        const int qb = unit % p.nq, bh = unit / p.nq;
+        h = bh % p.H;
+        b = bh / p.H;
+        qrow = qb * kUnitRows + r;
+        valid = qrow < p.Sq;
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-    any_nan = __any_sync(0xFFFFFFFFu, any_nan);
     float acc[kC];
 #pragma unroll
     for (int e = 0; e < kC; ++e) acc[e] = 0.f;
-    float wsum = 0.f;
-    for (int s0 = 0; s0 < p.nsplit; s0 += 32) {
-        const int sl = s0 + lane;
-        float w = 0.0f;
-        if (sl < p.nsplit) {
-            const float e = p.ws_lse[base + (long long)sl * kUnitRows];
-            w = (e == -INFINITY) ? 0.0f : ptx::ex2_approx(fmaxf(e - mx, -125.0f));
-        }
-        const int n = min(32, p.nsplit - s0);
-        const float* src = p.ws_o + (base + (long long)s0 * kUnitRows) * D + lane * kC;
-#pragma unroll 4
-        for (int q = 0; q < n; ++q) {
-            const float wq = __shfl_sync(0xFFFFFFFFu, w, q);
-            const float* vq = src + (long long)q * kUnitRows * D;
-            wsum += wq;
+    float wsum = 0.f, mx = -INFINITY;
+    bool any_nan = false;
+    if (valid) {
+        const long long base = (long long)t * p.nsplit * kUnitRows + r;
+        const float* src = p.ws_o + base * D + lane * kC;
+        auto load = [&](int s, float (&v)[kC], float& e) {
+            const float* vq = src + (long long)s * kUnitRows * D;
             if constexpr (kC == 4) {
-                const float4 v = *reinterpret_cast<const float4*>(vq);
-                acc[0] += wq * v.x;
-                acc[1] += wq * v.y;
-                acc[2] += wq * v.z;
-                acc[3] += wq * v.w;
+                const float4 x = *reinterpret_cast<const float4*>(vq);
+                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
             } else {
-                const float2 v = *reinterpret_cast<const float2*>(vq);
-                acc[0] += wq * v.x;
-                acc[1] += wq * v.y;
+                const float2 x = *reinterpret_cast<const float2*>(vq);
+                v[0] = x.x; v[1] = x.y;
+            }
+            e = p.ws_lse[base + (long long)s * kUnitRows];
+        };
+        // this warp's first splits, in flight while the row maximum is found
+        float v[kLoads][kC], lse[kLoads];
+#pragma unroll
+        for (int i = 0; i < kLoads; ++i)
+            if (w + i * W < p.nsplit) load(w + i * W, v[i], lse[i]);
+        for (int s = lane; s < p.nsplit; s += 32) {
+            const float e = p.ws_lse[base + (long long)s * kUnitRows];
+            any_nan |= (e != e);
+            mx = fmaxf(mx, e);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+        any_nan = __any_sync(0xFFFFFFFFu, any_nan);
+        for (int s0 = w;; s0 += kLoads * W) {
+#pragma unroll
+            for (int i = 0; i < kLoads; ++i) {
+                if (s0 + i * W < p.nsplit) {
+                    const float wt = (lse[i] == -INFINITY) ? 0.0f : ptx::ex2_approx(fmaxf(lse[i] - mx, -125.0f));
+                    wsum += wt;
+#pragma unroll
+                    for (int e = 0; e < kC; ++e) acc[e] += wt * v[i][e];
+                }
+            }
+            if (s0 + kLoads * W >= p.nsplit) break;
+#pragma unroll
+            for (int i = 0; i < kLoads; ++i)
+                if (s0 + (kLoads + i) * W < p.nsplit) load(s0 + (kLoads + i) * W, v[i], lse[i]);
+        }
+    }
+    if constexpr (W > 1) {
+        if (valid && w > 0) {
+#pragma unroll
+            for (int e = 0; e < kC; ++e) red[rsub][w][lane * kC + e] = acc[e];
+            if (lane == 0) red[rsub][w][D] = wsum;
+        }
+        __syncthreads();
+        if (valid && w == 0) {
+#pragma unroll 1
+            for (int ww = 1; ww < W; ++ww) {
+#pragma unroll
+                for (int e = 0; e < kC; ++e) acc[e] += red[rsub][ww][lane * kC + e];
+                wsum += red[rsub][ww][D];
             }
         }
     }
+    if (!valid || w != 0) return;
     const bool nan_row = any_nan || mx == -INFINITY;
     const float inv = 1.0f / wsum;
     // sum_s 2^LSE_s = 2^mx * wsum (base 2), reported in natural log
@@ -1498,9 +1533,11 @@ int launch(const attn_args_t& a, const attn_plan_t& pl, const attn_options_t* op
         c.ws_o = p.ws_o; c.ws_lse = p.ws_lse; c.o = p.o;
         c.o_sb = p.o_sb; c.o_ss = p.o_ss; c.o_sh = p.o_sh;
         c.lse = a.lse;
+        // warps per row by split count, so that a warp has at most four splits in flight
+        const int W = pl.splits <= 4 ? 1 : pl.splits <= 8 ? 2 : pl.splits <= 16 ? 4 : 8;
         const long long rows = pl.split_units * kUnitRows;
         const int warps_per_block = 8;
-        const unsigned blocks = (unsigned)cdiv(rows, warps_per_block);
+        const unsigned blocks = (unsigned)cdiv(rows, warps_per_block / W);
         cudaLaunchConfig_t cfg;
         memset(&cfg, 0, sizeof cfg);
         cfg.gridDim = dim3(blocks);
@@ -1512,8 +1549,17 @@ int launch(const attn_args_t& a, const attn_plan_t& pl, const attn_options_t* op
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        const cudaError_t ce = d == 128 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<128>, c)
-                                        : cudaLaunchKernelEx(&cfg, attn_combine_kernel<64>, c);
+        cudaError_t ce;
+        if (d == 128)
+            ce = W == 1 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<128, 1>, c)
+               : W == 2 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<128, 2>, c)
+               : W == 4 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<128, 4>, c)
+                        : cudaLaunchKernelEx(&cfg, attn_combine_kernel<128, 8>, c);
+        else
+            ce = W == 1 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<64, 1>, c)
+               : W == 2 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<64, 2>, c)
+               : W == 4 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<64, 4>, c)
+                        : cudaLaunchKernelEx(&cfg, attn_combine_kernel<64, 8>, c);
         if (ce != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_CUDA;

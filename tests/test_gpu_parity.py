@@ -75,6 +75,16 @@ def test_forced_split_matches_oracle(attn, splits):
     check(attn, q, k, v, "bhsd", "rtna", force_splits=splits)
 
 
+@pytest.mark.parametrize("splits,layout", [(12, "bshd"), (45, "bhsd")])
+def test_many_splits_match_oracle(attn, splits, layout):
+    # 12 splits: four warps per merged row; 45 splits: eight warps per row, each taking its
+    # splits in two rounds of four; deterministic across repeated calls
+    q, k, v = make_qkv(1, 2, 300, 6000, 128, layout, seed=76 + splits, sigma=2.0)
+    res, o = check(attn, q, k, v, layout, "rtne", force_splits=splits)
+    o2 = run(attn, q, k, v, layout, "rtne", force_splits=splits)
+    assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
+
+
 def test_split_and_plain_agree_and_grid_limit(attn):
     q, k, v = make_qkv(2, 3, 600, 1500, 128, "bshd", seed=78)
     a = run(attn, q, k, v, "bshd", "rtne")
