@@ -128,3 +128,24 @@ def test_backward_many_units_per_cta(attn, causal):
     q, k, v = make_qkv(B, H, Sq, Skv, 128, "bshd", seed=5700 + causal, Hkv=Hkv)
     g = make_qkv(B, H, Sq, 1, 128, "bshd", seed=5800 + causal)[0]
     check_bwd(attn, q, k, v, g, "bshd", causal=causal)
+
+
+def test_backward_square_workload_sampled_heads(attn):
+    """The square workload's shape (B4 H16 Sq=Skv=2048, d = 128, BHSD) at full size on the GPU;
+    without grouped heads every (b, h) is an independent problem, so the oracle runs on three
+    sampled (b, h) slices (first, last and a middle one) and their dQ, dK and dV must meet the
+    criteria element by element."""
+    from workloads import WORKLOADS
+    w = WORKLOADS["square"]
+    q, k, v = make_qkv(w.B, w.H, w.Sq, w.Skv, w.d, w.layout, seed=w.seed)
+    g = make_qkv(w.B, w.H, w.Sq, 1, w.d, w.layout, seed=w.seed + 77)[0]
+    dq, dk, dv = run_bwd(attn, q, k, v, g, w.layout, False)
+    heads = ((0, 0), (w.B - 1, w.H - 1), (1, 7))
+    pick = lambda t: torch.cat([t[b:b + 1, h:h + 1] for b, h in heads], dim=0)   # a batch of 3 heads
+    ref = oracle.backward(pick(q), pick(k), pick(v), pick(g), w.layout, want_a=True)
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        gf = parity.bits_to_f64(_bits(pick(got.cpu())).reshape(-1))
+        r = ref[name].reshape(-1)
+        tol = 2.0 ** -7 * ref[name + "_a"].reshape(-1) + parity.bf16_ulp(ref[name + "_bits"].reshape(-1))
+        bad = ~(np.abs(gf - r) <= tol)
+        assert not bad.any(), (name, int(bad.sum()))
