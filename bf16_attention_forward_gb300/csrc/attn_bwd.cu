@@ -76,13 +76,14 @@ enum {
     kBarKVEmpty,     // the unit's last GEMM reading K_j, V_j is done
     kBarQFull,       // [2] Q_i, dO_i of stage s % 2 loaded
     kBarQEmpty = kBarQFull + kStages,   // [2] the GEMMs reading that stage are done
-    kBarStats = kBarQEmpty + kStages,   // the step's row statistics loaded
+    kBarStageFree = kBarQEmpty + kStages,   // [2] the dQ reductions staged there have read it (8 arrivals)
+    kBarStats = kBarStageFree + kStages,    // the step's row statistics loaded
     kBarSFull,       // S^T in TMEM
     kBarDPFull,      // dP^T in TMEM
     kBarPFull,       // P^T, dS^T in TMEM and dS^T in shared memory (256 arrivals)
     kBarRead,        // both warpgroups have read S^T and dP^T out of TMEM (256 arrivals)
     kBarDQFull,      // dQ_i in TMEM
-    kBarDQEmpty,     // dQ_i read out of TMEM (128 arrivals)
+    kBarDQEmpty,     // dQ_i read out of TMEM (256 arrivals: each warpgroup reads half its columns)
     kBarDKVFull,     // the unit's dK, dV final in TMEM
     kBarDKVEmpty,    // dK, dV read out of TMEM (128 arrivals)
     kBarDrain,
@@ -225,6 +226,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(bar(kBarQFull + i), 1);
             ptx::mbar_init(bar(kBarQEmpty + i), 1);
+            ptx::mbar_init(bar(kBarStageFree + i), 8);
         }
         ptx::mbar_init(bar(kBarStats), 1);
         ptx::mbar_init(bar(kBarSFull), 1);
@@ -232,7 +234,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         ptx::mbar_init(bar(kBarPFull), 2 * kBN);
         ptx::mbar_init(bar(kBarRead), 2 * kBN);
         ptx::mbar_init(bar(kBarDQFull), 1);
-        ptx::mbar_init(bar(kBarDQEmpty), kBM);
+        ptx::mbar_init(bar(kBarDQEmpty), 2 * kBM);
         ptx::mbar_init(bar(kBarDKVFull), 1);
         ptx::mbar_init(bar(kBarDKVEmpty), kBN);
         ptx::mbar_init(bar(kBarDrain), 1);
@@ -338,12 +340,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 dw[ci][2 * g4 + 1] = pack2(s23.x, s23.y);
             }
         }
-        // every S^T and dP^T column has been read by both warpgroups; warpgroup 1's reductions of
-        // the previous dQ have finished reading their staging (the dS region)
-        if (half == 1) {
-            if (lane == 0) ptx::bulk_wait_read0();
-            __syncwarp();
+        // this warp's reductions of the previous step's dQ have read their staging (that step's
+        // Q/dO stage), which the producer may then refill
+        if (lane == 0) {
+            ptx::bulk_wait_read0();
+            if (s > 0) ptx::mbar_arrive(bar(kBarStageFree + (int)((s - 1) % kStages)));
         }
+        __syncwarp();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(kBarRead));
         ok = bwd_wait(bar(kBarRead), s & 1u, kSiteRead, abort_flag, lim);
@@ -395,9 +398,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 const int h = un.kvh * p.group + st % p.group;
                 const int it = un.it_lo + st / p.group;
                 const uint32_t sg = s % kStages;
-                // the stage's previous occupant (step s - 2) has had its last GEMM
+                // the stage's previous occupant (step s - 2) has had its last GEMM, and the dQ
+                // reductions staged there after it have read it
                 if (s >= (uint32_t)kStages &&
-                    !(ok = bwd_wait(bar(kBarQEmpty + sg), ((s / kStages) - 1u) & 1u, kSiteQEmpty, abort_flag, lim)))
+                    !(ok = bwd_wait(bar(kBarQEmpty + sg), ((s / kStages) - 1u) & 1u, kSiteQEmpty, abort_flag, lim) &&
+                           bwd_wait(bar(kBarStageFree + sg), ((s / kStages) - 1u) & 1u, kSiteQEmpty, abort_flag, lim)))
                     break;
                 ptx::mbar_arrive_expect_tx(bar(kBarQFull + sg), 2 * G::kTileBytes);
                 const uint32_t qd = sbase + G::kSmemStage0 + sg * G::kStageBytes;
@@ -513,55 +518,51 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         const uint64_t t0 = ptx::globaltimer_ns();
         while (!ptx::mbar_try_wait(bar(kBarDrain), 0) && ptx::globaltimer_ns() - t0 < lim) {
         }
-    } else if (warp < 4) {
-        // -------------------------------------------------------------------- P^T and dS^T, query columns 0..63
-        uint32_t s = 0;
-        bool ok = true;
-        for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x) {
-            const Unit un = decode_unit(p, k);
-            for (int st = 0; st < un.nsteps && ok; ++st, ++s)
-                ok = pds_step(un, un.it_lo + st / p.group, s, 0);
-        }
     } else if (warp < 8) {
-        // -------------------------------------------------------------------- dQ, dK, dV out
+        // -------------------------------------------------------------------- P^T, dS^T and dQ; dK, dV out
+        // Warpgroup `half` forms P^T and dS^T for query columns 64*half .. 64*half + 63 of each
+        // step, then drains its half of dQ_i's columns; warpgroup 1 also writes dK and dV at the
+        // end of a unit.  Splitting the dQ drain keeps both warpgroups equally loaded: with one
+        // warpgroup draining all of dQ it reached the next step ~1200 cycles after the other,
+        // which waited for it where the two meet.
+        const int half = warp >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        constexpr int kHC = D / 2;              // dQ columns per warpgroup
+        // staging for dQ_i: the step's own Q/dO stage, which its last GEMMs have read by the time
+        // dQ_i is ready and which is not refilled before these reductions have read it; one 4 KB
+        // box (32 rows x 32 fp32) per warp and 32 columns
+        static_assert(8 * (kHC / 32) * 4096 == G::kStageBytes, "the dQ boxes fill one Q/dO stage");
         uint32_t s = 0, u = 0;
         bool ok = true;
         for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x, ++u) {
             const Unit un = decode_unit(p, k);
             for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
                 const int h = un.kvh * p.group + st % p.group;
-                // query columns 64..127 of this step's P^T and dS^T, then its dQ
-                if (!(ok = pds_step(un, un.it_lo + st / p.group, s, 1))) break;
+                if (!(ok = pds_step(un, un.it_lo + st / p.group, s, half))) break;
                 ok = bwd_wait(bar(kBarDQFull), s & 1u, kSiteDQFull, abort_flag, lim);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 ptx::tc_fence_after();
-                // all of dQ_i into registers and release TMEM; then, per 32 columns, this warp's
-                // 32 rows (times 1/sqrt(d)) into a 4 KB staging buffer of the dS region (free
-                // until the next step's dS, which waits for these reads) in the 128-byte swizzle,
-                // and one TMA reduction adds the box into the fp32 dQ accumulator.  The TMA unit
-                // does the additions: per-thread atomics here stalled the MMA thread's issue.
-                uint32_t v[D];
-                if constexpr (D == 128) ptx::tmem_ld128(tDQ + lane_off, v);
-                else ptx::tmem_ld64(tDQ + lane_off, v);
+                // this warpgroup's half of dQ_i into registers, then release TMEM; per 32 columns,
+                // this warp's 32 rows (times 1/sqrt(d)) into its staging box (free until the next
+                // step's dS, which waits for these reads) in the 128-byte swizzle, and one TMA
+                // reduction adds the box into the fp32 dQ accumulator.  The TMA unit does the
+                // additions: per-thread atomics here stalled the MMA thread's issue.
+                uint32_t v[kHC];
+                if constexpr (kHC == 64) ptx::tmem_ld64(tDQ + lane_off + 64u * half, v);
+                else ptx::tmem_ld32(tDQ + lane_off + 32u * half, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(kBarDQEmpty));
-                const uint32_t stage = sbase + G::kSmemDS + (uint32_t)(quarter * 8192);
                 const int q0 = (un.it_lo + st / p.group) * kBM + quarter * 32;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    const uint32_t buf = stage + (uint32_t)((c & 1) * 4096);
-                    if (c >= 2) {
-                        // this buffer's previous box has been read
-                        if (lane == 0) bulk_wait_read1();
-                        __syncwarp();
-                    }
-                    const uint32_t rowaddr = buf + (uint32_t)lane * 128u;
+                for (int cc = 0; cc < kHC / 32; ++cc) {
+                    const uint32_t box = sbase + G::kSmemStage0 + (s % kStages) * G::kStageBytes +
+                                         (uint32_t)(((half * 4 + quarter) * (kHC / 32) + cc) * 4096);
+                    const uint32_t rowaddr = box + (uint32_t)lane * 128u;
 #pragma unroll
                     for (int pc = 0; pc < 8; ++pc) {
-                        const int e = 32 * c + 4 * pc;
+                        const int e = 32 * cc + 4 * pc;
                         ptx::st_shared_v4(rowaddr + (((uint32_t)pc ^ (uint32_t)(lane & 7)) << 4),
                                           __float_as_uint(__uint_as_float(v[e]) * p.scale),
                                           __float_as_uint(__uint_as_float(v[e + 1]) * p.scale),
@@ -571,12 +572,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_reduce_add_3d(&dqmap, buf, 32 * c, q0, un.b * p.H + h);
+                        tma_reduce_add_3d(&dqmap, box, kHC * half + 32 * cc, q0, un.b * p.H + h);
                         ptx::bulk_commit();
                     }
                 }
             }
-            if (!ok) break;
+            if (!ok || half == 0) continue;
             ok = bwd_wait(bar(kBarDKVFull), u & 1u, kSiteDKVFull, abort_flag, lim);
             if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             ptx::tc_fence_after();
@@ -611,8 +612,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         }
     }
 
-    // warpgroup 1's dQ reductions are complete before the CTA (and its shared memory) goes
-    if (warp >= 4 && warp < 8 && lane == 0) ptx::bulk_wait0();
+    // the dQ reductions are complete before the CTA (and its shared memory) goes
+    if (warp < 8 && lane == 0) ptx::bulk_wait0();
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == kWarpMma) {

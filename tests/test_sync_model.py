@@ -452,19 +452,22 @@ def test_main_kernel_planted_missing_release_is_caught():
 class BwdModel(Model):
     """attn_bwd_kernel's protocol: units (b, K/V head, key tile) of `nsteps` query steps each
     (0 for a causal key tile no query sees), a TMA producer (K and V per unit, a two-stage Q/dO
-    ring, the step's row statistics), one MMA thread, and two P/dS warpgroups; warpgroup 1 also
-    reads dQ out (staging it in the dS region for TMA reductions) and writes dK, dV."""
+    ring, the step's row statistics), one MMA thread, and two P/dS warpgroups; each warpgroup
+    also reads its half of dQ's columns out, staging them for TMA reductions in the step's own
+    Q/dO stage (free once the step's GEMMs are done; released to the producer after the
+    reductions have read it, at the next step's P/dS), and warpgroup 1 writes dK, dV."""
 
     def __init__(self, units, rng, wait_reduce_reads=True):
         self.units, self.rng, self.wait_reduce_reads = units, rng, wait_reduce_reads
         self.b = {}
         for n, c in (("KV", 1), ("KVEmpty", 1), ("Stats", 1), ("SFull", 1), ("DPFull", 1),
-                     ("PFull", 2), ("Read", 2), ("DQFull", 1), ("DQEmpty", 1), ("DKVFull", 1),
+                     ("PFull", 2), ("Read", 2), ("DQFull", 1), ("DQEmpty", 2), ("DKVFull", 1),
                      ("DKVEmpty", 1)):
             self.b[(n, 0)] = Barrier(n, c)
         for i in range(2):
             self.b[("QFull", i)] = Barrier("QFull[%d]" % i, 1)
             self.b[("QEmpty", i)] = Barrier("QEmpty[%d]" % i, 1)
+            self.b[("StageFree", i)] = Barrier("StageFree[%d]" % i, 2)
         self.kv = None                   # unit whose K, V are in shared memory
         self.qdo = [None, None]          # step whose Q, dO are in each ring stage
         self.stats = None                # step whose statistics are loaded
@@ -472,7 +475,8 @@ class BwdModel(Model):
         self.t_dp = None                 # TMEM 128-255: ("dP", s), ("dS", s) or ("dQ", s)
         self.dkv = None                  # (unit, steps accumulated) in the dV, dK columns
         self.ds_smem = None              # ("dS", s) or ("stage", s): the dS region
-        self.reduce_reading = None       # step whose staged dQ the TMA reductions still read
+        self.reduce_reading = [None, None]   # per warpgroup: step whose staged dQ its reductions read
+        self.dq_read = set()             # warpgroups that have read the current dQ out of TMEM
         self.pending, self.now, self.seq, self.last_done = [], 0, 0, {}
 
     def producer(self):
@@ -489,7 +493,10 @@ class BwdModel(Model):
                 sg = s % 2
                 if s >= 2:
                     yield from self.wait(("QEmpty", sg), s // 2 - 1)
-                self.check(self.qdo[sg] in (None, s - 2), "Q/dO stage overwritten early")
+                    yield from self.wait(("StageFree", sg), s // 2 - 1)
+                self.check(self.qdo[sg] in (None, s - 2, ("stage", s - 2)), "Q/dO stage overwritten early")
+                self.check(s - 2 not in self.reduce_reading or s < 2,
+                           "Q/dO stage refilled while dQ reductions still read it")
 
                 def load_q(sg=sg, s=s):
                     self.qdo[sg] = s
@@ -570,13 +577,14 @@ class BwdModel(Model):
         self.check(self.t_sp in (("S", s), ("P", s)) and self.t_dp in (("dP", s), ("dS", s)),
                    "P/dS read the wrong S^T or dP^T")
         yield ("step",)
-        if half == 1 and self.wait_reduce_reads:
-            # lane 0 waits for its reductions' reads of the staging (the dS region)
-            while self.reduce_reading is not None:
+        if half == 1 or self.wait_reduce_reads:
+            # lane 0 waits for its reductions' reads of the previous step's staging
+            while self.reduce_reading[half] is not None:
                 yield ("wait", "bulk read", s)
+        if s > 0:
+            self.b[("StageFree", (s - 1) % 2)].arrive()
         self.b[("Read", 0)].arrive()
         yield from self.wait(("Read", 0), s)
-        self.check(self.reduce_reading is None, "dS stored over staging still being read")
         self.t_sp, self.t_dp, self.ds_smem = ("P", s), ("dS", s), ("dS", s)
         self.b[("PFull", 0)].arrive()
 
@@ -585,20 +593,23 @@ class BwdModel(Model):
         for u, n in enumerate(self.units):
             for _ in range(n):
                 yield from self.pds(half, s, u)
-                if half == 1:
-                    yield from self.wait(("DQFull", 0), s)
-                    self.check(self.t_dp == ("dQ", s), "dQ readout met the wrong TMEM contents")
-                    self.t_dp = ("dQ", s, "read")
-                    self.b[("DQEmpty", 0)].arrive()
-                    # stage into the dS region (the dQ GEMM has read it) and start the reductions
-                    self.check(self.ds_smem == ("dS", s), "staging overwrote an unread dS")
-                    self.ds_smem = ("stage", s)
-                    self.reduce_reading = s
+                yield from self.wait(("DQFull", 0), s)
+                self.check(self.t_dp == ("dQ", s), "dQ readout met the wrong TMEM contents")
+                self.dq_read.add(half)
+                if self.dq_read == {0, 1}:
+                    self.t_dp, self.dq_read = ("dQ", s, "read"), set()
+                self.b[("DQEmpty", 0)].arrive()
+                # stage into its boxes of the step's Q/dO stage (its GEMMs are done) and start the
+                # reductions
+                sg = s % 2
+                self.check(self.qdo[sg] in (s, ("stage", s)), "staging overwrote another step's Q/dO")
+                self.qdo[sg] = ("stage", s)
+                self.reduce_reading[half] = s
 
-                    def reads_done(s=s):
-                        if self.reduce_reading == s:
-                            self.reduce_reading = None
-                    self.later(reads_done, channel="tma_reduce")
+                def reads_done(s=s, half=half):
+                    if self.reduce_reading[half] == s:
+                        self.reduce_reading[half] = None
+                self.later(reads_done, channel="tma_reduce%d" % half)
                 s += 1
                 yield ("step",)
             if half == 1:
@@ -630,8 +641,8 @@ def test_backward_random_unit_lengths():
 
 
 def test_backward_planted_early_dS_store_is_caught():
-    # warpgroup 1 arriving at the read barrier before its dQ reductions have read the staging
-    # lets the next dS land on data the TMA unit still reads: some schedule must expose it
+    # warpgroup 0 releasing a Q/dO stage before its dQ reductions have read their staging
+    # lets the producer refill it under the TMA unit: some schedule must expose it
     found = False
     for seed in range(400):
         try:
