@@ -26,8 +26,8 @@
 //     accumulator in global memory by TMA tensor reductions (many key tiles contribute);
 //   * a last kernel rounds the dQ accumulator to bf16 (round to nearest even).
 // Roles: warp 8 TMA producer, warp 9 (one thread) MMA issuer; warpgroups 0 and 1 recompute P
-// and form dS for query columns 0..63 and 64..127 of each step, and warpgroup 1 then drains dQ
-// and, at the end of a unit, writes dK and dV.  Every wait is bounded.
+// and form dS for query columns 0..63 and 64..127 of each step, then each drains half of dQ's
+// columns; warpgroup 1 also writes dK and dV at the end of a unit.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
