@@ -76,8 +76,8 @@ enum {
     kBarKVEmpty,     // the unit's last GEMM reading K_j, V_j is done
     kBarQFull,       // [2] Q_i, dO_i of stage s % 2 loaded
     kBarQEmpty = kBarQFull + kStages,   // [2] the GEMMs reading that stage are done
-    kBarStageFree = kBarQEmpty + kStages,   // [2] the dQ reductions staged there have read it (8 arrivals)
-    kBarStats = kBarStageFree + kStages,    // the step's row statistics loaded
+    kBarStaged = kBarQEmpty + kStages,   // [2] the step's dQ staged in that stage (8 arrivals)
+    kBarStats = kBarStaged + kStages,    // the step's row statistics loaded
     kBarSFull,       // S^T in TMEM
     kBarDPFull,      // dP^T in TMEM
     kBarPFull,       // P^T, dS^T in TMEM and dS^T in shared memory (256 arrivals)
@@ -196,10 +196,6 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
     return v;
 }
 
-// wait until at most one committed bulk group still reads its shared-memory source
-__device__ __forceinline__ void bulk_wait_read1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -226,7 +222,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(bar(kBarQFull + i), 1);
             ptx::mbar_init(bar(kBarQEmpty + i), 1);
-            ptx::mbar_init(bar(kBarStageFree + i), 8);
+            ptx::mbar_init(bar(kBarStaged + i), 8);
         }
         ptx::mbar_init(bar(kBarStats), 1);
         ptx::mbar_init(bar(kBarSFull), 1);
@@ -340,13 +336,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 dw[ci][2 * g4 + 1] = pack2(s23.x, s23.y);
             }
         }
-        // this warp's reductions of the previous step's dQ have read their staging (that step's
-        // Q/dO stage), which the producer may then refill
-        if (lane == 0) {
-            ptx::bulk_wait_read0();
-            if (s > 0) ptx::mbar_arrive(bar(kBarStageFree + (int)((s - 1) % kStages)));
-        }
-        __syncwarp();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(kBarRead));
         ok = bwd_wait(bar(kBarRead), s & 1u, kSiteRead, abort_flag, lim);
@@ -380,6 +369,26 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         const uint64_t pol_q = ptx::policy_evict_last();
         uint32_t s = 0, u = 0, q_issued = 0;
         bool ok = true;
+        // dQ of step t is staged in stage t % 2 by the P/dS warps; this thread adds it into the
+        // fp32 accumulator with 8 * (D/64) TMA reductions (one 32 x 32 box per warp and 32
+        // columns) just before it refills the stage, and waits for them to have read it.  Doing
+        // this here rather than in the staging warps keeps the TMA unit's queue (a step's 64 KB
+        // of reductions) off their path.
+        int hist_it[kStages] = {0, 0}, hist_bh[kStages] = {0, 0};
+        auto reduce_step = [&](uint32_t t) -> bool {
+            const uint32_t tg = t % kStages;
+            if (!bwd_wait(bar(kBarStaged + tg), (t / kStages) & 1u, kSiteDQEmpty, abort_flag, lim)) return false;
+            const uint32_t stage = sbase + G::kSmemStage0 + tg * G::kStageBytes;
+            constexpr int kHC = D / 2;
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+#pragma unroll
+                for (int cc = 0; cc < kHC / 32; ++cc)
+                    tma_reduce_add_3d(&dqmap, stage + (uint32_t)((w * (kHC / 32) + cc) * 4096), kHC * (w >> 2) + 32 * cc,
+                                      hist_it[tg] * kBM + 32 * (w & 3), hist_bh[tg]);
+            ptx::bulk_commit();
+            return true;
+        };
         for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x, ++u) {
             const Unit un = decode_unit(p, k);
             if (u > 0 && !(ok = bwd_wait(bar(kBarKVEmpty), (u - 1) & 1u, kSiteKVEmpty, abort_flag, lim))) break;
@@ -398,12 +407,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 const int h = un.kvh * p.group + st % p.group;
                 const int it = un.it_lo + st / p.group;
                 const uint32_t sg = s % kStages;
-                // the stage's previous occupant (step s - 2) has had its last GEMM, and the dQ
-                // reductions staged there after it have read it
-                if (s >= (uint32_t)kStages &&
-                    !(ok = bwd_wait(bar(kBarQEmpty + sg), ((s / kStages) - 1u) & 1u, kSiteQEmpty, abort_flag, lim) &&
-                           bwd_wait(bar(kBarStageFree + sg), ((s / kStages) - 1u) & 1u, kSiteQEmpty, abort_flag, lim)))
-                    break;
+                // the stage's previous occupant (step s - 2) has had its last GEMM and its dQ,
+                // staged there afterwards, has gone out and been read
+                if (s >= (uint32_t)kStages) {
+                    if (!(ok = bwd_wait(bar(kBarQEmpty + sg), ((s / kStages) - 1u) & 1u, kSiteQEmpty, abort_flag, lim) &&
+                               reduce_step(s - kStages)))
+                        break;
+                    ptx::bulk_wait_read0();
+                }
                 ptx::mbar_arrive_expect_tx(bar(kBarQFull + sg), 2 * G::kTileBytes);
                 const uint32_t qd = sbase + G::kSmemStage0 + sg * G::kStageBytes;
                 for (int c = 0; c < G::kChunks; ++c) {
@@ -422,9 +433,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 const long long srow = ((long long)un.b * p.H + h) * p.nq_pad_rows + (long long)it * kBM;
                 ptx::bulk_load_1d(sbase + G::kSmemStats, p.lse2 + srow, kBM * 4, bar(kBarStats));
                 ptx::bulk_load_1d(sbase + G::kSmemStats + kBM * 4, p.delta + srow, kBM * 4, bar(kBarStats));
+                hist_it[sg] = it;
+                hist_bh[sg] = un.b * p.H + h;
                 ++q_issued;
             }
         }
+        // the last steps' dQ (at most two stages' worth) goes out after the loop
+        for (uint32_t t = (s > (uint32_t)kStages ? s - kStages : 0u); t < s && ok; ++t) ok = reduce_step(t);
+        ptx::bulk_wait0();
         // every issued load has landed before the CTA may exit
         if (u > 0) {
             const uint64_t t0 = ptx::globaltimer_ns();
@@ -539,22 +555,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x, ++u) {
             const Unit un = decode_unit(p, k);
             for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
-                const int h = un.kvh * p.group + st % p.group;
                 if (!(ok = pds_step(un, un.it_lo + st / p.group, s, half))) break;
                 ok = bwd_wait(bar(kBarDQFull), s & 1u, kSiteDQFull, abort_flag, lim);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 ptx::tc_fence_after();
                 // this warpgroup's half of dQ_i into registers, then release TMEM; per 32 columns,
-                // this warp's 32 rows (times 1/sqrt(d)) into its staging box (free until the next
-                // step's dS, which waits for these reads) in the 128-byte swizzle, and one TMA
-                // reduction adds the box into the fp32 dQ accumulator.  The TMA unit does the
-                // additions: per-thread atomics here stalled the MMA thread's issue.
+                // this warp's 32 rows (times 1/sqrt(d)) into its staging box in the 128-byte
+                // swizzle; the producer thread then adds the boxes into the fp32 dQ accumulator
+                // with TMA reductions.  The TMA unit does the additions: per-thread atomics here
+                // stalled the MMA thread's issue.
                 uint32_t v[kHC];
                 if constexpr (kHC == 64) ptx::tmem_ld64(tDQ + lane_off + 64u * half, v);
                 else ptx::tmem_ld32(tDQ + lane_off + 32u * half, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(kBarDQEmpty));
-                const int q0 = (un.it_lo + st / p.group) * kBM + quarter * 32;
 #pragma unroll
                 for (int cc = 0; cc < kHC / 32; ++cc) {
                     const uint32_t box = sbase + G::kSmemStage0 + (s % kStages) * G::kStageBytes +
@@ -569,13 +583,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                                           __float_as_uint(__uint_as_float(v[e + 2]) * p.scale),
                                           __float_as_uint(__uint_as_float(v[e + 3]) * p.scale));
                     }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_reduce_add_3d(&dqmap, box, kHC * half + 32 * cc, q0, un.b * p.H + h);
-                        ptx::bulk_commit();
-                    }
                 }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(kBarStaged + (int)(s % kStages)));
             }
             if (!ok || half == 0) continue;
             ok = bwd_wait(bar(kBarDKVFull), u & 1u, kSiteDKVFull, abort_flag, lim);
@@ -612,8 +623,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         }
     }
 
-    // the dQ reductions are complete before the CTA (and its shared memory) goes
-    if (warp < 8 && lane == 0) ptx::bulk_wait0();
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == kWarpMma) {

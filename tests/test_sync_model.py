@@ -453,11 +453,13 @@ class BwdModel(Model):
     """attn_bwd_kernel's protocol: units (b, K/V head, key tile) of `nsteps` query steps each
     (0 for a causal key tile no query sees), a TMA producer (K and V per unit, a two-stage Q/dO
     ring, the step's row statistics), one MMA thread, and two P/dS warpgroups; each warpgroup
-    also reads its half of dQ's columns out, staging them for TMA reductions in the step's own
-    Q/dO stage (free once the step's GEMMs are done; released to the producer after the
-    reductions have read it, at the next step's P/dS), and warpgroup 1 writes dK, dV."""
+    also reads its half of dQ's columns out and stages them in the step's own Q/dO stage (free
+    once the step's GEMMs are done), and warpgroup 1 writes dK, dV.  The producer issues a
+    stage's dQ reductions just before refilling it and waits for them to have read it."""
 
     def __init__(self, units, rng, wait_reduce_reads=True):
+        # wait_reduce_reads=False plants a mistake: the producer refills a stage without waiting
+        # for the reductions issued from it to have read it
         self.units, self.rng, self.wait_reduce_reads = units, rng, wait_reduce_reads
         self.b = {}
         for n, c in (("KV", 1), ("KVEmpty", 1), ("Stats", 1), ("SFull", 1), ("DPFull", 1),
@@ -467,7 +469,7 @@ class BwdModel(Model):
         for i in range(2):
             self.b[("QFull", i)] = Barrier("QFull[%d]" % i, 1)
             self.b[("QEmpty", i)] = Barrier("QEmpty[%d]" % i, 1)
-            self.b[("StageFree", i)] = Barrier("StageFree[%d]" % i, 2)
+            self.b[("Staged", i)] = Barrier("Staged[%d]" % i, 2)
         self.kv = None                   # unit whose K, V are in shared memory
         self.qdo = [None, None]          # step whose Q, dO are in each ring stage
         self.stats = None                # step whose statistics are loaded
@@ -475,7 +477,7 @@ class BwdModel(Model):
         self.t_dp = None                 # TMEM 128-255: ("dP", s), ("dS", s) or ("dQ", s)
         self.dkv = None                  # (unit, steps accumulated) in the dV, dK columns
         self.ds_smem = None              # ("dS", s) or ("stage", s): the dS region
-        self.reduce_reading = [None, None]   # per warpgroup: step whose staged dQ its reductions read
+        self.reduce_reading = None       # step whose staged dQ the producer's reductions still read
         self.dq_read = set()             # warpgroups that have read the current dQ out of TMEM
         self.pending, self.now, self.seq, self.last_done = [], 0, 0, {}
 
@@ -493,9 +495,9 @@ class BwdModel(Model):
                 sg = s % 2
                 if s >= 2:
                     yield from self.wait(("QEmpty", sg), s // 2 - 1)
-                    yield from self.wait(("StageFree", sg), s // 2 - 1)
-                self.check(self.qdo[sg] in (None, s - 2, ("stage", s - 2)), "Q/dO stage overwritten early")
-                self.check(s - 2 not in self.reduce_reading or s < 2,
+                    yield from self.reduce(s - 2)
+                self.check(self.qdo[sg] in (None, ("stage", s - 2)), "Q/dO stage overwritten early")
+                self.check(self.reduce_reading != s - 2 or s < 2,
                            "Q/dO stage refilled while dQ reductions still read it")
 
                 def load_q(sg=sg, s=s):
@@ -512,6 +514,22 @@ class BwdModel(Model):
                 self.later(load_stats)
                 s += 1
                 yield ("step",)
+        for t in range(max(s - 2, 0), s):
+            yield from self.reduce(t)
+
+    def reduce(self, t):
+        """The producer's TMA reductions of step t's staged dQ, then (normally) a wait for
+        their reads of the stage."""
+        yield from self.wait(("Staged", t % 2), t // 2)
+        self.check(self.qdo[t % 2] == ("stage", t), "reductions read a stage not holding dQ")
+        self.reduce_reading = t
+
+        def reads_done(t=t):
+            if self.reduce_reading == t:
+                self.reduce_reading = None
+        self.later(reads_done, channel="tma_reduce")
+        while self.wait_reduce_reads and self.reduce_reading is not None:
+            yield ("wait", "bulk read", t)
 
     def mma(self):
         s = 0
@@ -577,12 +595,6 @@ class BwdModel(Model):
         self.check(self.t_sp in (("S", s), ("P", s)) and self.t_dp in (("dP", s), ("dS", s)),
                    "P/dS read the wrong S^T or dP^T")
         yield ("step",)
-        if half == 1 or self.wait_reduce_reads:
-            # lane 0 waits for its reductions' reads of the previous step's staging
-            while self.reduce_reading[half] is not None:
-                yield ("wait", "bulk read", s)
-        if s > 0:
-            self.b[("StageFree", (s - 1) % 2)].arrive()
         self.b[("Read", 0)].arrive()
         yield from self.wait(("Read", 0), s)
         self.t_sp, self.t_dp, self.ds_smem = ("P", s), ("dS", s), ("dS", s)
@@ -599,17 +611,13 @@ class BwdModel(Model):
                 if self.dq_read == {0, 1}:
                     self.t_dp, self.dq_read = ("dQ", s, "read"), set()
                 self.b[("DQEmpty", 0)].arrive()
-                # stage into its boxes of the step's Q/dO stage (its GEMMs are done) and start the
-                # reductions
+                # stage into its boxes of the step's Q/dO stage (its GEMMs are done) for the
+                # producer's reductions
                 sg = s % 2
                 self.check(self.qdo[sg] in (s, ("stage", s)), "staging overwrote another step's Q/dO")
                 self.qdo[sg] = ("stage", s)
-                self.reduce_reading[half] = s
-
-                def reads_done(s=s, half=half):
-                    if self.reduce_reading[half] == s:
-                        self.reduce_reading[half] = None
-                self.later(reads_done, channel="tma_reduce%d" % half)
+                yield ("step",)
+                self.b[("Staged", sg)].arrive()
                 s += 1
                 yield ("step",)
             if half == 1:
@@ -641,8 +649,8 @@ def test_backward_random_unit_lengths():
 
 
 def test_backward_planted_early_dS_store_is_caught():
-    # warpgroup 0 releasing a Q/dO stage before its dQ reductions have read their staging
-    # lets the producer refill it under the TMA unit: some schedule must expose it
+    # the producer refilling a Q/dO stage before the dQ reductions issued from it have read
+    # it: some schedule must expose it
     found = False
     for seed in range(400):
         try:
