@@ -246,6 +246,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const unsigned long long lim = p.wait_limit_ns;
+    // the dQ rounding kernel may be scheduled as CTAs retire; it waits for this grid's memory
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // TMEM: S^T then P^T | dP^T then dS^T, later dQ_i | dV | dK.  dQ_i goes where dP^T was, so
     // the next step's S^T GEMM does not wait for dQ_i to be read out.
     const uint32_t tS = tmem, tDP = tmem + 128u, tDV = tmem + 256u, tDK = tmem + 256u + (uint32_t)D, tDQ = tDP;
@@ -375,6 +377,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         // this here rather than in the staging warps keeps the TMA unit's queue (a step's 64 KB
         // of reductions) off their path.
         int hist_it[kStages] = {0, 0}, hist_bh[kStages] = {0, 0};
+        // the preprocessing kernel's D, LSE and zeroed accumulator are waited for once, before
+        // the first statistics load (every reduction comes after it), and in any case before
+        // exit, so this grid's completion implies that kernel's
+        bool dep_done = false;
+        auto dep_wait = [&]() {
+            if (!dep_done) asm volatile("griddepcontrol.wait;" ::: "memory");
+            dep_done = true;
+        };
         auto reduce_step = [&](uint32_t t) -> bool {
             const uint32_t tg = t % kStages;
             if (!bwd_wait(bar(kBarStaged + tg), (t / kStages) & 1u, kSiteDQEmpty, abort_flag, lim)) return false;
@@ -429,6 +439,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 }
                 // the statistics buffer is free once the previous step's P^T/dS^T are done
                 if (s > 0 && !(ok = bwd_wait(bar(kBarPFull), (s - 1) & 1u, kSitePFull, abort_flag, lim))) break;
+                dep_wait();
                 ptx::mbar_arrive_expect_tx(bar(kBarStats), 2 * kBM * 4);
                 const long long srow = ((long long)un.b * p.H + h) * p.nq_pad_rows + (long long)it * kBM;
                 ptx::bulk_load_1d(sbase + G::kSmemStats, p.lse2 + srow, kBM * 4, bar(kBarStats));
@@ -458,6 +469,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             while (!ptx::mbar_try_wait(bar(kBarStats), (s - 1) & 1u) && ptx::globaltimer_ns() - t0 < lim) {
             }
         }
+        dep_wait();
     } else if (warp == kWarpMma && lane == 0) {
         // -------------------------------------------------------------------- MMA issuer
         constexpr uint32_t idesc_s = idesc_bf16(kBN, kBM, false, false);  // K-major x K-major
@@ -631,55 +643,73 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     }
 }
 
-// D_i = dO_i . O_i in fp32 and the base-2 log-sum-exp, one warp per padded query row;
-// rows past Sq get zeros.
+// Preprocessing, one pass over O and dO: D_i = dO_i . O_i in fp32, the base-2 log-sum-exp,
+// and zeros into query row i of the fp32 dQ accumulator.  D / 8 lanes per padded query row,
+// 8 columns (16-byte loads) per lane, grid-stride over rows; padded rows (q >= Sq) get D_i = 0
+// and LSE 0 and have no accumulator row.  The row count is a multiple of 128, so every warp's
+// rows are all in range or all out and its shuffles see all 32 lanes.  The main kernel is this
+// kernel's programmatic dependent: it may launch as soon as every CTA here has started, and
+// its producer waits for this kernel's memory before the first statistics load or reduction.
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout,
-                                                            const float* lse, float* lse2, float* delta, int H,
-                                                            int Sq, int nq_pad_rows, long long rows,
-                                                            long long o_sb, long long o_ss, long long o_sh) {
-    const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= rows) return;
-    const long long bh = gw / nq_pad_rows;
-    const int q = (int)(gw % nq_pad_rows);
-    const int b = (int)(bh / H), h = (int)(bh % H);
-    float acc = 0.0f;
-    if (q < Sq) {
-        constexpr int kE = D / 32;     // elements per lane: 4 or 2
-        const long long off = (long long)b * o_sb + (long long)q * o_ss + (long long)h * o_sh + lane * kE;
-        const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(o + off);
-        const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(dout + off);
+                                                            const float* lse, float* lse2, float* delta,
+                                                            float* dq_acc, int H, int Sq, int nq_pad_rows,
+                                                            long long rows, long long o_sb, long long o_ss,
+                                                            long long o_sh) {
+    constexpr int kL = D / 8;                  // lanes per row: 16 or 8
+    constexpr int kRows = 256 / kL;            // rows per block and pass
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int sub = threadIdx.x / kL, c = (threadIdx.x % kL) * 8;
+    for (long long r = (long long)blockIdx.x * kRows + sub; r < rows; r += (long long)gridDim.x * kRows) {
+        const long long bh = r / nq_pad_rows;
+        const int q = (int)(r % nq_pad_rows);
+        const int b = (int)(bh / H), h = (int)(bh % H);
+        float acc = 0.0f;
+        if (q < Sq) {
+            const long long off = (long long)b * o_sb + (long long)q * o_ss + (long long)h * o_sh + c;
+            const uint4 ov = *reinterpret_cast<const uint4*>(o + off);
+            const uint4 gv = *reinterpret_cast<const uint4*>(dout + off);
+            const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-        for (int e = 0; e < kE / 2; ++e) {
-            const float2 of = __bfloat1622float2(op[e]), gf = __bfloat1622float2(gp[e]);
-            acc = fmaf(of.x, gf.x, acc);
-            acc = fmaf(of.y, gf.y, acc);
+            for (int e = 0; e < 4; ++e) {
+                const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+                const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+                acc = fmaf(of.x, gf.x, acc);
+                acc = fmaf(of.y, gf.y, acc);
+            }
+            float4* z = reinterpret_cast<float4*>(dq_acc + (bh * Sq + q) * D + c);
+            z[0] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            z[1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
-    }
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, s);
-    if (lane == 0) {
-        delta[gw] = acc;
-        lse2[gw] = q < Sq ? lse[bh * Sq + q] * 1.4426950408889634f : 0.0f;
+        for (int s = kL / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, s);
+        if (c == 0) {
+            delta[r] = acc;
+            lse2[r] = q < Sq ? lse[bh * Sq + q] * 1.4426950408889634f : 0.0f;
+        }
     }
 }
 
-// dq (bf16, the caller's layout) = dq_acc (fp32 [B][H][Sq][d]), round to nearest even.
+// dq (bf16, the caller's layout) = dq_acc (fp32 [B][H][Sq][d]), round to nearest even; 8
+// columns per thread (two 16-byte loads, one 16-byte store), grid-stride.  Launched as a
+// programmatic dependent of the main kernel: it waits for that kernel's memory first.
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const float* dq_acc, __nv_bfloat16* dq, int H, int Sq,
-                                                          long long n4, long long o_sb, long long o_ss,
+                                                          long long n8, long long o_sb, long long o_ss,
                                                           long long o_sh) {
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // group of 4 columns
-    if (i >= n4) return;
-    const long long row = i / (D / 4);
-    const int x = (int)(i % (D / 4)) * 4;
-    const int q = (int)(row % Sq);
-    const long long bh = row / Sq;
-    const int h = (int)(bh % H), b = (int)(bh / H);
-    const float4 v = *reinterpret_cast<const float4*>(dq_acc + row * D + x);
-    __nv_bfloat16* dst = dq + (long long)b * o_sb + (long long)q * o_ss + (long long)h * o_sh + x;
-    *reinterpret_cast<uint2*>(dst) = make_uint2(pack2(v.x, v.y), pack2(v.z, v.w));
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
+        const long long row = i / (D / 8);
+        const int x = (int)(i % (D / 8)) * 8;
+        const int q = (int)(row % Sq);
+        const long long bh = row / Sq;
+        const int h = (int)(bh % H), b = (int)(bh / H);
+        const float4* src = reinterpret_cast<const float4*>(dq_acc + row * D + x);
+        const float4 v0 = src[0], v1 = src[1];
+        __nv_bfloat16* dst = dq + (long long)b * o_sb + (long long)q * o_ss + (long long)h * o_sh + x;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(pack2(v0.x, v0.y), pack2(v0.z, v0.w), pack2(v1.x, v1.y),
+                                                    pack2(v1.z, v1.w));
+    }
 }
 
 // ------------------------------------------------------------------------------ host side
@@ -839,24 +869,47 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     p.wait_limit_ns = (unsigned long long)(a.wait_limit_ms > 0 ? a.wait_limit_ms : 2000) * 1000000ull;
     p.test_hooks = a.test_hooks;
 
-    if (cudaMemsetAsync(dq_acc, 0, (size_t)(a.B * a.H * a.Sq * d * 4), stream) != cudaSuccess) {
+    // preprocessing (also zeroes the dQ accumulator) -> main kernel -> dQ rounding; the last
+    // two are programmatic dependents of the kernel before them
+    const long long prows = a.B * a.H * (long long)p.nq_pad_rows;
+    const long long fill = (long long)sms * 8;             // resident 256-thread blocks
+    auto prep = d == 128 ? attn_bwd_prep_kernel<128> : attn_bwd_prep_kernel<64>;
+    const long long prep_blocks = cdiv(prows, 256 / (d / 8));
+    prep<<<(unsigned)(prep_blocks < fill ? prep_blocks : fill), 256, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(a.o), reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, lse2,
+        delta, dq_acc, p.H, p.Sq, p.nq_pad_rows, prows, q_sb, q_ss, q_sh);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(p.n_units < sms ? p.n_units : sms));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = d == 128 ? smem_alloc<128>() : smem_alloc<64>();
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t ce = d == 128 ? cudaLaunchKernelEx(&cfg, attn_bwd_kernel<128>, qm, km, vm, dom, dqm, p)
+                              : cudaLaunchKernelEx(&cfg, attn_bwd_kernel<64>, qm, km, vm, dom, dqm, p);
+    if (ce != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_CUDA;
     }
-    const long long prows = a.B * a.H * (long long)p.nq_pad_rows;
-    auto prep = d == 128 ? attn_bwd_prep_kernel<128> : attn_bwd_prep_kernel<64>;
-    prep<<<(unsigned)cdiv(prows, 8), 256, 0, stream>>>(
-        reinterpret_cast<const __nv_bfloat16*>(a.o), reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, lse2,
-        delta, p.H, p.Sq, p.nq_pad_rows, prows, q_sb, q_ss, q_sh);
-    const int grid = p.n_units < sms ? p.n_units : sms;
-    if (d == 128)
-        attn_bwd_kernel<128><<<(unsigned)grid, kThreads, smem_alloc<128>(), stream>>>(qm, km, vm, dom, dqm, p);
-    else
-        attn_bwd_kernel<64><<<(unsigned)grid, kThreads, smem_alloc<64>(), stream>>>(qm, km, vm, dom, dqm, p);
-    const long long n4 = a.B * a.H * a.Sq * (d / 4);
-    auto conv = d == 128 ? attn_bwd_dq_kernel<128> : attn_bwd_dq_kernel<64>;
-    conv<<<(unsigned)cdiv(n4, 256), 256, 0, stream>>>(dq_acc, reinterpret_cast<__nv_bfloat16*>(a.dq), p.H, p.Sq, n4,
-                                                      q_sb, q_ss, q_sh);
+    const long long n8 = a.B * a.H * a.Sq * (d / 8);
+    const long long conv_blocks = cdiv(n8, 256);
+    cfg.gridDim = dim3((unsigned)(conv_blocks < fill ? conv_blocks : fill));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    __nv_bfloat16* dqo = reinterpret_cast<__nv_bfloat16*>(a.dq);
+    ce = d == 128 ? cudaLaunchKernelEx(&cfg, attn_bwd_dq_kernel<128>, (const float*)dq_acc, dqo, p.H, p.Sq, n8, q_sb,
+                                       q_ss, q_sh)
+                  : cudaLaunchKernelEx(&cfg, attn_bwd_dq_kernel<64>, (const float*)dq_acc, dqo, p.H, p.Sq, n8, q_sb,
+                                       q_ss, q_sh);
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
