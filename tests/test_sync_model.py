@@ -457,10 +457,12 @@ class BwdModel(Model):
     once the step's GEMMs are done), and warpgroup 1 writes dK, dV.  The producer issues a
     stage's dQ reductions just before refilling it and waits for them to have read it."""
 
-    def __init__(self, units, rng, wait_reduce_reads=True):
+    def __init__(self, units, rng, wait_reduce_reads=True, read_barrier=True):
         # wait_reduce_reads=False plants a mistake: the producer refills a stage without waiting
-        # for the reductions issued from it to have read it
+        # for the reductions issued from it to have read it; read_barrier=False another: a
+        # warpgroup stores P^T and dS^T without waiting for the other to have loaded S^T, dP^T
         self.units, self.rng, self.wait_reduce_reads = units, rng, wait_reduce_reads
+        self.read_barrier = read_barrier
         self.b = {}
         for n, c in (("KV", 1), ("KVEmpty", 1), ("Stats", 1), ("SFull", 1), ("DPFull", 1),
                      ("PFull", 2), ("Read", 2), ("DQFull", 1), ("DQEmpty", 2), ("DKVFull", 1),
@@ -592,11 +594,11 @@ class BwdModel(Model):
         yield from self.wait(("SFull", 0), s)
         yield from self.wait(("DPFull", 0), s)
         self.check(self.stats == s, "P/dS read the wrong statistics")
-        self.check(self.t_sp in (("S", s), ("P", s)) and self.t_dp in (("dP", s), ("dS", s)),
-                   "P/dS read the wrong S^T or dP^T")
+        self.check(self.t_sp == ("S", s) and self.t_dp == ("dP", s), "P/dS read the wrong S^T or dP^T")
         yield ("step",)
-        self.b[("Read", 0)].arrive()
-        yield from self.wait(("Read", 0), s)
+        if self.read_barrier:
+            self.b[("Read", 0)].arrive()
+            yield from self.wait(("Read", 0), s)
         self.t_sp, self.t_dp, self.ds_smem = ("P", s), ("dS", s), ("dS", s)
         self.b[("PFull", 0)].arrive()
 
@@ -655,6 +657,19 @@ def test_backward_planted_early_dS_store_is_caught():
     for seed in range(400):
         try:
             BwdModel([3, 2], random.Random(seed), wait_reduce_reads=False).run()
+        except (Violation, Deadlock):
+            found = True
+            break
+    assert found
+
+
+def test_backward_planted_early_p_store_is_caught():
+    # a warpgroup storing P^T and dS^T over S^T and dP^T before the other warpgroup has loaded
+    # its columns of them
+    found = False
+    for seed in range(400):
+        try:
+            BwdModel([2, 1], random.Random(seed), read_barrier=False).run()
         except (Violation, Deadlock):
             found = True
             break
