@@ -650,7 +650,7 @@ def test_backward_random_unit_lengths():
         BwdModel(units, random.Random(rng.random())).run()
 
 
-def test_backward_planted_early_dS_store_is_caught():
+def test_backward_planted_early_stage_refill_is_caught():
     # the producer refilling a Q/dO stage before the dQ reductions issued from it have read
     # it: some schedule must expose it
     found = False
