@@ -314,6 +314,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const unsigned long long lim = p.wait_limit_ns;
+    // launched as a programmatic dependent of the stream's previous kernel, whose output Q, K
+    // and V may be and whose input O may be: only the prologue above overlaps its tail, and
+    // every thread waits for its memory here before touching global memory
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // the split-combine kernel may be scheduled as CTAs retire; it waits for this grid's memory
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -762,6 +766,10 @@ attn_fwd_short_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_con
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const unsigned long long lim = p.wait_limit_ns;
+    // launched as a programmatic dependent of the stream's previous kernel, whose output Q, K
+    // and V may be and whose input O may be: only the prologue above overlaps its tail, and
+    // every thread waits for its memory here before touching global memory
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // the split-combine kernel may be scheduled as CTAs retire; it waits for this grid's memory
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -1503,26 +1511,45 @@ int launch(const attn_args_t& a, const attn_plan_t& pl, const attn_options_t* op
 
     const attn_event_t* ev = opts ? opts->events : nullptr;
     if (ev && ev[0] && cudaEventRecord((cudaEvent_t)ev[0], stream) != cudaSuccess) return ATTN_ERR_CUDA;
-    const unsigned grid = (unsigned)pl.grid;
+    // the attention kernel is a programmatic dependent of the stream's previous kernel (it
+    // waits for that kernel's memory after its prologue); the combine kernel is one of it
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t lc;
+    memset(&lc, 0, sizeof lc);
+    lc.gridDim = dim3((unsigned)pl.grid);
+    lc.stream = stream;
+    lc.attrs = pdl;
+    lc.numAttrs = 1;
+    cudaError_t le;
     if (Sq <= kBM) {
         // one query tile per (b, h): the short-query kernel (same items and workspace rows)
+        lc.blockDim = dim3(sq::kThreads);
         if (d == 128) {
-            if (p.causal)
-                attn_fwd_short_kernel<128, true><<<grid, sq::kThreads, sq::Geo<128>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
-            else
-                attn_fwd_short_kernel<128, false><<<grid, sq::kThreads, sq::Geo<128>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
+            lc.dynamicSmemBytes = sq::Geo<128>::kSmemAlloc;
+            le = p.causal ? cudaLaunchKernelEx(&lc, attn_fwd_short_kernel<128, true>, qm, km, vm, om, p)
+                          : cudaLaunchKernelEx(&lc, attn_fwd_short_kernel<128, false>, qm, km, vm, om, p);
         } else {
-            if (p.causal)
-                attn_fwd_short_kernel<64, true><<<grid, sq::kThreads, sq::Geo<64>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
-            else
-                attn_fwd_short_kernel<64, false><<<grid, sq::kThreads, sq::Geo<64>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
+            lc.dynamicSmemBytes = sq::Geo<64>::kSmemAlloc;
+            le = p.causal ? cudaLaunchKernelEx(&lc, attn_fwd_short_kernel<64, true>, qm, km, vm, om, p)
+                          : cudaLaunchKernelEx(&lc, attn_fwd_short_kernel<64, false>, qm, km, vm, om, p);
         }
-    } else if (d == 128) {
-        if (p.causal) attn_fwd_kernel<128, true><<<grid, kThreads, Geo<128>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
-        else attn_fwd_kernel<128, false><<<grid, kThreads, Geo<128>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
     } else {
-        if (p.causal) attn_fwd_kernel<64, true><<<grid, kThreads, Geo<64>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
-        else attn_fwd_kernel<64, false><<<grid, kThreads, Geo<64>::kSmemAlloc, stream>>>(qm, km, vm, om, p);
+        lc.blockDim = dim3(kThreads);
+        if (d == 128) {
+            lc.dynamicSmemBytes = Geo<128>::kSmemAlloc;
+            le = p.causal ? cudaLaunchKernelEx(&lc, attn_fwd_kernel<128, true>, qm, km, vm, om, p)
+                          : cudaLaunchKernelEx(&lc, attn_fwd_kernel<128, false>, qm, km, vm, om, p);
+        } else {
+            lc.dynamicSmemBytes = Geo<64>::kSmemAlloc;
+            le = p.causal ? cudaLaunchKernelEx(&lc, attn_fwd_kernel<64, true>, qm, km, vm, om, p)
+                          : cudaLaunchKernelEx(&lc, attn_fwd_kernel<64, false>, qm, km, vm, om, p);
+        }
+    }
+    if (le != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     if (ev && ev[1] && cudaEventRecord((cudaEvent_t)ev[1], stream) != cudaSuccess) return ATTN_ERR_CUDA;
