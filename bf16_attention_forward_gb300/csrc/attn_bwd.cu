@@ -647,8 +647,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
 // and zeros into query row i of the fp32 dQ accumulator.  D / 8 lanes per padded query row,
 // 8 columns (16-byte loads) per lane, grid-stride over rows; padded rows (q >= Sq) get D_i = 0
 // and LSE 0 and have no accumulator row.  The row count is a multiple of 128, so every warp's
-// rows are all in range or all out and its shuffles see all 32 lanes.  The main kernel is this
-// kernel's programmatic dependent: it may launch as soon as every CTA here has started, and
+// rows are all in range or all out and its shuffles see all 32 lanes.  This kernel is itself a
+// programmatic dependent of the stream's previous kernel (which may have written O, dO or the
+// LSE, or still read the accumulator) and waits for its memory first.  The main kernel is this
+// kernel's programmatic dependent: it may launch once every CTA here is past that wait, and
 // its producer waits for this kernel's memory before the first statistics load or reduction.
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout,
@@ -658,6 +660,9 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __nv_bfloat16*
                                                             long long o_sh) {
     constexpr int kL = D / 8;                  // lanes per row: 16 or 8
     constexpr int kRows = 256 / kL;            // rows per block and pass
+    // wait before letting the main kernel launch: it loads Q, K, V and dO before it waits for
+    // this kernel, so it must not start before the previous kernel is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int sub = threadIdx.x / kL, c = (threadIdx.x % kL) * 8;
     for (long long r = (long long)blockIdx.x * kRows + sub; r < rows; r += (long long)gridDim.x * kRows) {
@@ -869,19 +874,28 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     p.wait_limit_ns = (unsigned long long)(a.wait_limit_ms > 0 ? a.wait_limit_ms : 2000) * 1000000ull;
     p.test_hooks = a.test_hooks;
 
-    // preprocessing (also zeroes the dQ accumulator) -> main kernel -> dQ rounding; the last
-    // two are programmatic dependents of the kernel before them
+    // preprocessing (also zeroes the dQ accumulator) -> main kernel -> dQ rounding, each a
+    // programmatic dependent of the kernel before it in the stream
     const long long prows = a.B * a.H * (long long)p.nq_pad_rows;
     const long long fill = (long long)sms * 8;             // resident 256-thread blocks
     auto prep = d == 128 ? attn_bwd_prep_kernel<128> : attn_bwd_prep_kernel<64>;
     const long long prep_blocks = cdiv(prows, 256 / (d / 8));
-    prep<<<(unsigned)(prep_blocks < fill ? prep_blocks : fill), 256, 0, stream>>>(
-        reinterpret_cast<const __nv_bfloat16*>(a.o), reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, lse2,
-        delta, dq_acc, p.H, p.Sq, p.nq_pad_rows, prows, q_sb, q_ss, q_sh);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t pc;
+    memset(&pc, 0, sizeof pc);
+    pc.gridDim = dim3((unsigned)(prep_blocks < fill ? prep_blocks : fill));
+    pc.blockDim = dim3(256);
+    pc.stream = stream;
+    pc.attrs = attr;
+    pc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&pc, prep, reinterpret_cast<const __nv_bfloat16*>(a.o),
+                           reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, lse2, delta, dq_acc, p.H, p.Sq,
+                           p.nq_pad_rows, prows, q_sb, q_ss, q_sh) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3((unsigned)(p.n_units < sms ? p.n_units : sms));
