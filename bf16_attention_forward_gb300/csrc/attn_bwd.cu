@@ -27,7 +27,8 @@
 //   * a last kernel rounds the dQ accumulator to bf16 (round to nearest even).
 // Roles: warp 8 TMA producer, warp 9 (one thread) MMA issuer; warpgroups 0 and 1 recompute P
 // and form dS for query columns 0..63 and 64..127 of each step, then each drains half of dQ's
-// columns; warpgroup 1 also writes dK and dV at the end of a unit.  Every wait is bounded.
+// columns; at the end of a unit warpgroup 0 writes dV and warpgroup 1 dK.  Every wait is
+// bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -85,7 +86,7 @@ enum {
     kBarDQFull,      // dQ_i in TMEM
     kBarDQEmpty,     // dQ_i read out of TMEM (256 arrivals: each warpgroup reads half its columns)
     kBarDKVFull,     // the unit's dK, dV final in TMEM
-    kBarDKVEmpty,    // dK, dV read out of TMEM (128 arrivals)
+    kBarDKVEmpty,    // dK, dV read out of TMEM (256 arrivals)
     kBarDrain,
     kNumBars
 };
@@ -188,6 +189,14 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src
         : "memory");
 }
 
+// a 4-D tile of a tensor into L2 (a hint: no completion to wait for)
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
 // four floats from shared memory (an explicit shared-space load: through a generic pointer
 // the loads went down the generic path, whose latency every element's chain then waited on)
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
@@ -232,7 +241,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         ptx::mbar_init(bar(kBarDQFull), 1);
         ptx::mbar_init(bar(kBarDQEmpty), 2 * kBM);
         ptx::mbar_init(bar(kBarDKVFull), 1);
-        ptx::mbar_init(bar(kBarDKVEmpty), kBN);
+        ptx::mbar_init(bar(kBarDKVEmpty), 2 * kBN);
         ptx::mbar_init(bar(kBarDrain), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
@@ -399,44 +408,70 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             ptx::bulk_commit();
             return true;
         };
+        // Q_i and dO_i of step s into its ring stage, once the stage's previous occupant (step
+        // s - 2) has had its last GEMM and its dQ, staged there afterwards, has gone out and
+        // been read
+        auto load_q = [&](const Unit& un, int st, uint32_t s) -> bool {
+            const int h = un.kvh * p.group + st % p.group;
+            const int it = un.it_lo + st / p.group;
+            const uint32_t sg = s % kStages;
+            if (s >= (uint32_t)kStages) {
+                if (!(bwd_wait(bar(kBarQEmpty + sg), ((s / kStages) - 1u) & 1u, kSiteQEmpty, abort_flag, lim) &&
+                      reduce_step(s - kStages)))
+                    return false;
+                ptx::bulk_wait_read0();
+            }
+            ptx::mbar_arrive_expect_tx(bar(kBarQFull + sg), 2 * G::kTileBytes);
+            const uint32_t qd = sbase + G::kSmemStage0 + sg * G::kStageBytes;
+            for (int c = 0; c < G::kChunks; ++c) {
+                const uint32_t dq = qd + c * kChunkBytes, dd = qd + G::kTileBytes + c * kChunkBytes;
+                if (p.bshd) {
+                    ptx::tma_load_4d(dq, &qmap, bar(kBarQFull + sg), c * 64, h, it * kBM, un.b, pol_q);
+                    ptx::tma_load_4d(dd, &domap, bar(kBarQFull + sg), c * 64, h, it * kBM, un.b, pol_q);
+                } else {
+                    ptx::tma_load_4d(dq, &qmap, bar(kBarQFull + sg), c * 64, it * kBM, h, un.b, pol_q);
+                    ptx::tma_load_4d(dd, &domap, bar(kBarQFull + sg), c * 64, it * kBM, h, un.b, pol_q);
+                }
+            }
+            hist_it[sg] = it;
+            hist_bh[sg] = un.b * p.H + h;
+            ++q_issued;
+            return true;
+        };
+        // coordinates 1 and 2 of a unit's K_j, V_j boxes (the layout's order)
+        auto kv_coords = [&](const Unit& un, int& c1, int& c2) {
+            c1 = p.bshd ? un.kvh : un.jt * kBN;
+            c2 = p.bshd ? un.jt * kBN : un.kvh;
+        };
         for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x, ++u) {
             const Unit un = decode_unit(p, k);
+            // the unit's first Q/dO goes in before the wait for the previous unit's K/V to be
+            // released, so that it does not wait behind that unit's last GEMMs
+            if (un.nsteps > 0 && !(ok = load_q(un, 0, s))) break;
             if (u > 0 && !(ok = bwd_wait(bar(kBarKVEmpty), (u - 1) & 1u, kSiteKVEmpty, abort_flag, lim))) break;
             ptx::mbar_arrive_expect_tx(bar(kBarKV), 2 * G::kTileBytes);
             for (int c = 0; c < G::kChunks; ++c) {
                 const uint32_t dk = sbase + G::kSmemK + c * kChunkBytes, dv = sbase + G::kSmemV + c * kChunkBytes;
-                if (p.bshd) {
-                    ptx::tma_load_4d(dk, &kmap, bar(kBarKV), c * 64, un.kvh, un.jt * kBN, un.b, pol_kv);
-                    ptx::tma_load_4d(dv, &vmap, bar(kBarKV), c * 64, un.kvh, un.jt * kBN, un.b, pol_kv);
-                } else {
-                    ptx::tma_load_4d(dk, &kmap, bar(kBarKV), c * 64, un.jt * kBN, un.kvh, un.b, pol_kv);
-                    ptx::tma_load_4d(dv, &vmap, bar(kBarKV), c * 64, un.jt * kBN, un.kvh, un.b, pol_kv);
+                int c1, c2;
+                kv_coords(un, c1, c2);
+                ptx::tma_load_4d(dk, &kmap, bar(kBarKV), c * 64, c1, c2, un.b, pol_kv);
+                ptx::tma_load_4d(dv, &vmap, bar(kBarKV), c * 64, c1, c2, un.b, pol_kv);
+            }
+            // the next unit's K_j, V_j toward L2 now, so that its reload at the boundary does
+            // not wait on DRAM
+            if (k + (int)gridDim.x < p.n_units) {
+                const Unit nx = decode_unit(p, k + (int)gridDim.x);
+                for (int c = 0; c < G::kChunks; ++c) {
+                    int c1, c2;
+                    kv_coords(nx, c1, c2);
+                    tma_prefetch_l2_4d(&kmap, c * 64, c1, c2, nx.b);
+                    tma_prefetch_l2_4d(&vmap, c * 64, c1, c2, nx.b);
                 }
             }
             for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
                 const int h = un.kvh * p.group + st % p.group;
                 const int it = un.it_lo + st / p.group;
-                const uint32_t sg = s % kStages;
-                // the stage's previous occupant (step s - 2) has had its last GEMM and its dQ,
-                // staged there afterwards, has gone out and been read
-                if (s >= (uint32_t)kStages) {
-                    if (!(ok = bwd_wait(bar(kBarQEmpty + sg), ((s / kStages) - 1u) & 1u, kSiteQEmpty, abort_flag, lim) &&
-                               reduce_step(s - kStages)))
-                        break;
-                    ptx::bulk_wait_read0();
-                }
-                ptx::mbar_arrive_expect_tx(bar(kBarQFull + sg), 2 * G::kTileBytes);
-                const uint32_t qd = sbase + G::kSmemStage0 + sg * G::kStageBytes;
-                for (int c = 0; c < G::kChunks; ++c) {
-                    const uint32_t dq = qd + c * kChunkBytes, dd = qd + G::kTileBytes + c * kChunkBytes;
-                    if (p.bshd) {
-                        ptx::tma_load_4d(dq, &qmap, bar(kBarQFull + sg), c * 64, h, it * kBM, un.b, pol_q);
-                        ptx::tma_load_4d(dd, &domap, bar(kBarQFull + sg), c * 64, h, it * kBM, un.b, pol_q);
-                    } else {
-                        ptx::tma_load_4d(dq, &qmap, bar(kBarQFull + sg), c * 64, it * kBM, h, un.b, pol_q);
-                        ptx::tma_load_4d(dd, &domap, bar(kBarQFull + sg), c * 64, it * kBM, h, un.b, pol_q);
-                    }
-                }
+                if (st > 0 && !(ok = load_q(un, st, s))) break;
                 // the statistics buffer is free once the previous step's P^T/dS^T are done
                 if (s > 0 && !(ok = bwd_wait(bar(kBarPFull), (s - 1) & 1u, kSitePFull, abort_flag, lim))) break;
                 dep_wait();
@@ -444,9 +479,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 const long long srow = ((long long)un.b * p.H + h) * p.nq_pad_rows + (long long)it * kBM;
                 ptx::bulk_load_1d(sbase + G::kSmemStats, p.lse2 + srow, kBM * 4, bar(kBarStats));
                 ptx::bulk_load_1d(sbase + G::kSmemStats + kBM * 4, p.delta + srow, kBM * 4, bar(kBarStats));
-                hist_it[sg] = it;
-                hist_bh[sg] = un.b * p.H + h;
-                ++q_issued;
             }
         }
         // the last steps' dQ (at most two stages' worth) goes out after the loop
@@ -549,10 +581,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     } else if (warp < 8) {
         // -------------------------------------------------------------------- P^T, dS^T and dQ; dK, dV out
         // Warpgroup `half` forms P^T and dS^T for query columns 64*half .. 64*half + 63 of each
-        // step, then drains its half of dQ_i's columns; warpgroup 1 also writes dK and dV at the
-        // end of a unit.  Splitting the dQ drain keeps both warpgroups equally loaded: with one
-        // warpgroup draining all of dQ it reached the next step ~1200 cycles after the other,
-        // which waited for it where the two meet.
+        // step, then drains its half of dQ_i's columns; at the end of a unit warpgroup 0 writes
+        // dV and warpgroup 1 dK.  Splitting this work keeps both warpgroups equally loaded: with
+        // one warpgroup draining all of dQ it reached the next step ~1200 cycles after the
+        // other, which waited for it where the two meet.
         const int half = warp >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
@@ -600,14 +632,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(kBarStaged + (int)(s % kStages)));
             }
-            if (!ok || half == 0) continue;
+            if (!ok) continue;
+            // warpgroup 0 writes dV, warpgroup 1 dK (times 1/sqrt(d)), at the same time
             ok = bwd_wait(bar(kBarDKVFull), u & 1u, kSiteDKVFull, abort_flag, lim);
             if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             ptx::tc_fence_after();
             const int kj = un.jt * kBN + row;
             const long long off = (long long)un.b * p.kv_sb + (long long)kj * p.kv_ss + (long long)un.kvh * p.kv_sh;
-#pragma unroll 1
-            for (int which = 0; which < 2; ++which) {     // 0: dV, 1: dK (times 1/sqrt(d))
+            {
+                const int which = half;
                 __nv_bfloat16* out = (which ? p.dk : p.dv) + off;
                 const float sc = which ? p.scale : 1.0f;
 #pragma unroll 1

@@ -466,7 +466,7 @@ class BwdModel(Model):
         self.b = {}
         for n, c in (("KV", 1), ("KVEmpty", 1), ("Stats", 1), ("SFull", 1), ("DPFull", 1),
                      ("PFull", 2), ("Read", 2), ("DQFull", 1), ("DQEmpty", 2), ("DKVFull", 1),
-                     ("DKVEmpty", 1)):
+                     ("DKVEmpty", 2)):
             self.b[(n, 0)] = Barrier(n, c)
         for i in range(2):
             self.b[("QFull", i)] = Barrier("QFull[%d]" % i, 1)
@@ -481,31 +481,24 @@ class BwdModel(Model):
         self.ds_smem = None              # ("dS", s) or ("stage", s): the dS region
         self.reduce_reading = None       # step whose staged dQ the producer's reductions still read
         self.dq_read = set()             # warpgroups that have read the current dQ out of TMEM
+        self.dkv_read = set()            # warpgroups that have written their half of dK/dV out
         self.pending, self.now, self.seq, self.last_done = [], 0, 0, {}
 
     def producer(self):
         s = 0
         for u, n in enumerate(self.units):
-            if u > 0:
-                yield from self.wait(("KVEmpty", 0), u - 1)
-
             def load_kv(u=u):
                 self.kv = u
                 self.b[("KV", 0)].arrive()
+            # the unit's first Q/dO goes in before the wait for the previous unit's K/V release
+            if n > 0:
+                yield from self.load_q(s)
+            if u > 0:
+                yield from self.wait(("KVEmpty", 0), u - 1)
             self.later(load_kv)
-            for _ in range(n):
-                sg = s % 2
-                if s >= 2:
-                    yield from self.wait(("QEmpty", sg), s // 2 - 1)
-                    yield from self.reduce(s - 2)
-                self.check(self.qdo[sg] in (None, ("stage", s - 2)), "Q/dO stage overwritten early")
-                self.check(self.reduce_reading != s - 2 or s < 2,
-                           "Q/dO stage refilled while dQ reductions still read it")
-
-                def load_q(sg=sg, s=s):
-                    self.qdo[sg] = s
-                    self.b[("QFull", sg)].arrive()
-                self.later(load_q)
+            for st in range(n):
+                if st > 0:
+                    yield from self.load_q(s)
                 if s > 0:
                     yield from self.wait(("PFull", 0), s - 1)
 
@@ -518,6 +511,22 @@ class BwdModel(Model):
                 yield ("step",)
         for t in range(max(s - 2, 0), s):
             yield from self.reduce(t)
+
+    def load_q(self, s):
+        """Refill ring stage s % 2 with step s's Q/dO once its previous occupant's GEMMs are
+        done and the dQ staged there has been read by the reductions."""
+        sg = s % 2
+        if s >= 2:
+            yield from self.wait(("QEmpty", sg), s // 2 - 1)
+            yield from self.reduce(s - 2)
+        self.check(self.qdo[sg] in (None, ("stage", s - 2)), "Q/dO stage overwritten early")
+        self.check(self.reduce_reading != s - 2 or s < 2,
+                   "Q/dO stage refilled while dQ reductions still read it")
+
+        def load(sg=sg, s=s):
+            self.qdo[sg] = s
+            self.b[("QFull", sg)].arrive()
+        self.later(load)
 
     def reduce(self, t):
         """The producer's TMA reductions of step t's staged dQ, then (normally) a wait for
@@ -622,12 +631,14 @@ class BwdModel(Model):
                 self.b[("Staged", sg)].arrive()
                 s += 1
                 yield ("step",)
-            if half == 1:
-                yield from self.wait(("DKVFull", 0), u)
-                self.check(self.dkv == (u, n), "dK/dV read out unfinished")
-                yield ("step",)
-                self.dkv = None
-                self.b[("DKVEmpty", 0)].arrive()
+            # warpgroup 0 writes dV out, warpgroup 1 dK
+            yield from self.wait(("DKVFull", 0), u)
+            self.check(self.dkv == (u, n), "dK/dV read out unfinished")
+            yield ("step",)
+            self.dkv_read.add(half)
+            if self.dkv_read == {0, 1}:
+                self.dkv, self.dkv_read = None, set()
+            self.b[("DKVEmpty", 0)].arrive()
 
     def run(self, max_events=200000):
         roles = {"producer": self.producer(), "mma": self.mma(), "wg0": self.wg(0), "wg1": self.wg(1)}
