@@ -87,7 +87,9 @@ enum {
     kBarDQEmpty,     // dQ_i read out of TMEM (256 arrivals: each warpgroup reads half its columns)
     kBarDKVFull,     // the unit's dK, dV final in TMEM
     kBarDKVEmpty,    // dK, dV read out of TMEM (256 arrivals)
-    kBarDrain,
+    kBarOutStaged,   // [2] warpgroup h's dV (h = 0) or dK (h = 1) rows staged in the dS region (128 arrivals)
+    kBarOutFree = kBarOutStaged + 2,   // [2] warpgroup h's tile store has read the dS region
+    kBarDrain = kBarOutFree + 2,
     kNumBars
 };
 template <int D>
@@ -98,7 +100,8 @@ static_assert(smem_alloc<128>() <= 232448, "shared memory over the 227 KB limit"
 
 enum : uint32_t {
     kSiteKV = 1, kSiteKVEmpty, kSiteQFull, kSiteQEmpty, kSiteSFull, kSitePFull, kSiteDQFull,
-    kSiteDQEmpty, kSiteDKVFull, kSiteDKVEmpty, kSiteStats, kSiteDPFull, kSiteRead
+    kSiteDQEmpty, kSiteDKVFull, kSiteDKVEmpty, kSiteStats, kSiteDPFull, kSiteRead, kSiteOutStaged,
+    kSiteOutFree
 };
 static_assert(kSiteDKVFull == ATTN_BWD_SITE_DKV_READY, "the dK/dV-ready wait site is part of the ABI");
 
@@ -210,7 +213,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap domap,
-                const __grid_constant__ CUtensorMap dqmap, const BwdParams p) {
+                const __grid_constant__ CUtensorMap dqmap, const __grid_constant__ CUtensorMap dkmap,
+                const __grid_constant__ CUtensorMap dvmap, const BwdParams p) {
     using G = BGeo<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -242,6 +246,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         ptx::mbar_init(bar(kBarDQEmpty), 2 * kBM);
         ptx::mbar_init(bar(kBarDKVFull), 1);
         ptx::mbar_init(bar(kBarDKVEmpty), 2 * kBN);
+        ptx::mbar_init(bar(kBarOutStaged), kBN);
+        ptx::mbar_init(bar(kBarOutStaged + 1), kBN);
+        ptx::mbar_init(bar(kBarOutFree), 1);
+        ptx::mbar_init(bar(kBarOutFree + 1), 1);
         ptx::mbar_init(bar(kBarDrain), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
@@ -633,39 +641,74 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 if (lane == 0) ptx::mbar_arrive(bar(kBarStaged + (int)(s % kStages)));
             }
             if (!ok) continue;
-            // warpgroup 0 writes dV, warpgroup 1 dK (times 1/sqrt(d)), at the same time
+            // warpgroup 0 writes dV, warpgroup 1 dK (times 1/sqrt(d)): each reads its rows out of
+            // TMEM into the dS^T region (free from the unit's last GEMMs to the next unit's first
+            // dS^T), warpgroup 0 first, then releases TMEM, and one thread per warpgroup stores
+            // the tile with TMA (rows past Skv are clipped).  Per-thread row
+            // stores took ~5000-8000 cycles per unit here; a tile store is one TMA request per
+            // 64 columns.
             ok = bwd_wait(bar(kBarDKVFull), u & 1u, kSiteDKVFull, abort_flag, lim);
             if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             ptx::tc_fence_after();
-            const int kj = un.jt * kBN + row;
-            const long long off = (long long)un.b * p.kv_sb + (long long)kj * p.kv_ss + (long long)un.kvh * p.kv_sh;
-            {
-                const int which = half;
-                __nv_bfloat16* out = (which ? p.dk : p.dv) + off;
-                const float sc = which ? p.scale : 1.0f;
+            // the region holds the other warpgroup's tile until its store has read it: dV of this
+            // unit for warpgroup 1; dK of the previous unit for warpgroup 0 (the next unit may
+            // have no steps, so no dS^T write in between orders the two)
+            if (half == 1 || u > 0) {
+                ok = bwd_wait(bar(kBarOutFree + (half ^ 1)), (half ? u : u - 1) & 1u, kSiteOutFree, abort_flag, lim);
+                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+            }
+            const float sc = half ? p.scale : 1.0f;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t v[32];
-                    if (un.nsteps > 0) {
-                        ptx::tmem_ld32((which ? tDK : tDV) + lane_off + 32u * c, v);
-                    } else {
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                if (un.nsteps > 0) {
+                    ptx::tmem_ld32((half ? tDK : tDV) + lane_off + 32u * c, v);
+                } else {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = 0u;
-                    }
-                    if (kj < p.Skv) {
-                        uint4* o4 = reinterpret_cast<uint4*>(out + 32 * c);
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
+                // row `row`, columns 32c..32c+31: 16-byte pieces (c & 1)*4 + v4 of the 64-column
+                // chunk c >> 1 (16 KB apart, rows 128 B apart), at piece ^ (row & 7) (the tensor
+                // map's 128-byte swizzle)
+                const uint32_t rowaddr = sbase + G::kSmemDS + (uint32_t)((c >> 1) * kChunkBytes) + (uint32_t)row * 128u;
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            o4[v4] = make_uint4(pack2(__uint_as_float(v[8 * v4]) * sc, __uint_as_float(v[8 * v4 + 1]) * sc),
-                                                pack2(__uint_as_float(v[8 * v4 + 2]) * sc, __uint_as_float(v[8 * v4 + 3]) * sc),
-                                                pack2(__uint_as_float(v[8 * v4 + 4]) * sc, __uint_as_float(v[8 * v4 + 5]) * sc),
-                                                pack2(__uint_as_float(v[8 * v4 + 6]) * sc, __uint_as_float(v[8 * v4 + 7]) * sc));
-                    }
+                for (int v4 = 0; v4 < 4; ++v4) {
+                    const uint32_t pc = (uint32_t)((c & 1) * 4 + v4);
+                    const int e = 8 * v4;
+                    ptx::st_shared_v4(rowaddr + ((pc ^ (uint32_t)(row & 7)) << 4),
+                                      pack2(__uint_as_float(v[e]) * sc, __uint_as_float(v[e + 1]) * sc),
+                                      pack2(__uint_as_float(v[e + 2]) * sc, __uint_as_float(v[e + 3]) * sc),
+                                      pack2(__uint_as_float(v[e + 4]) * sc, __uint_as_float(v[e + 5]) * sc),
+                                      pack2(__uint_as_float(v[e + 6]) * sc, __uint_as_float(v[e + 7]) * sc));
                 }
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(kBarDKVEmpty));
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(bar(kBarOutStaged + half));
+            if (quarter == 0) {
+                if (lane == 0) {
+                    ok = bwd_wait(bar(kBarOutStaged + half), u & 1u, kSiteOutStaged, abort_flag, lim);
+                    if (ok) {
+                        int c1, c2;
+                        c1 = p.bshd ? un.kvh : un.jt * kBN;
+                        c2 = p.bshd ? un.jt * kBN : un.kvh;
+                        for (int cc = 0; cc < D / 64; ++cc)
+                            ptx::tma_store_4d(half ? (const void*)&dkmap : (const void*)&dvmap,
+                                              sbase + G::kSmemDS + (uint32_t)(cc * kChunkBytes), cc * 64, c1, c2, un.b);
+                        ptx::bulk_commit();
+                        // the region is rewritten (dK rows, or the next unit's dS^T) only after
+                        // the store has read it
+                        ptx::bulk_wait_read0();
+                        ptx::mbar_arrive(bar(kBarOutFree + half));
+                    }
+                }
+                ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+            }
         }
+        // the dK, dV stores complete before the CTA exits
+        if (quarter == 0 && lane == 0) ptx::bulk_wait0();
     }
 
     ptx::tc_fence_before();
@@ -892,8 +935,10 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     p.lse2 = lse2;
     p.delta = delta;
     p.dq_acc = dq_acc;
-    CUtensorMap dqm;
-    if (!encode_dq(&dqm, dq_acc, a.B * a.H, a.Sq, d)) return ATTN_ERR_CUDA;
+    CUtensorMap dqm, dkm, dvm;
+    if (!encode_dq(&dqm, dq_acc, a.B * a.H, a.Sq, d) || !encode(&dkm, a.dk, a.B, a.Hkv, a.Skv, d, bshd) ||
+        !encode(&dvm, a.dv, a.B, a.Hkv, a.Skv, d, bshd))
+        return ATTN_ERR_CUDA;
     p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
     p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
     long long q_sb, q_ss, q_sh;
@@ -937,8 +982,8 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t ce = d == 128 ? cudaLaunchKernelEx(&cfg, attn_bwd_kernel<128>, qm, km, vm, dom, dqm, p)
-                              : cudaLaunchKernelEx(&cfg, attn_bwd_kernel<64>, qm, km, vm, dom, dqm, p);
+    cudaError_t ce = d == 128 ? cudaLaunchKernelEx(&cfg, attn_bwd_kernel<128>, qm, km, vm, dom, dqm, dkm, dvm, p)
+                              : cudaLaunchKernelEx(&cfg, attn_bwd_kernel<64>, qm, km, vm, dom, dqm, dkm, dvm, p);
     if (ce != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_CUDA;

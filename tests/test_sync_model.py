@@ -457,17 +457,22 @@ class BwdModel(Model):
     once the step's GEMMs are done), and warpgroup 1 writes dK, dV.  The producer issues a
     stage's dQ reductions just before refilling it and waits for them to have read it."""
 
-    def __init__(self, units, rng, wait_reduce_reads=True, read_barrier=True):
+    def __init__(self, units, rng, wait_reduce_reads=True, read_barrier=True, out_free_wait=True):
         # wait_reduce_reads=False plants a mistake: the producer refills a stage without waiting
         # for the reductions issued from it to have read it; read_barrier=False another: a
         # warpgroup stores P^T and dS^T without waiting for the other to have loaded S^T, dP^T
         self.units, self.rng, self.wait_reduce_reads = units, rng, wait_reduce_reads
         self.read_barrier = read_barrier
+        # out_free_wait=False plants a third: warpgroup 0 stages its dV tile without waiting for
+        # warpgroup 1's previous dK store to have read the region
+        self.out_free_wait = out_free_wait
         self.b = {}
         for n, c in (("KV", 1), ("KVEmpty", 1), ("Stats", 1), ("SFull", 1), ("DPFull", 1),
                      ("PFull", 2), ("Read", 2), ("DQFull", 1), ("DQEmpty", 2), ("DKVFull", 1),
                      ("DKVEmpty", 2)):
             self.b[(n, 0)] = Barrier(n, c)
+        for i in range(2):
+            self.b[("OutFree", i)] = Barrier("OutFree[%d]" % i, 1)
         for i in range(2):
             self.b[("QFull", i)] = Barrier("QFull[%d]" % i, 1)
             self.b[("QEmpty", i)] = Barrier("QEmpty[%d]" % i, 1)
@@ -608,6 +613,8 @@ class BwdModel(Model):
         if self.read_barrier:
             self.b[("Read", 0)].arrive()
             yield from self.wait(("Read", 0), s)
+        self.check(self.ds_smem is None or self.ds_smem[0] == "dS" or self.ds_smem[-1] == "read",
+                   "dS^T overwrote an unread dK/dV tile")
         self.t_sp, self.t_dp, self.ds_smem = ("P", s), ("dS", s), ("dS", s)
         self.b[("PFull", 0)].arrive()
 
@@ -631,14 +638,26 @@ class BwdModel(Model):
                 self.b[("Staged", sg)].arrive()
                 s += 1
                 yield ("step",)
-            # warpgroup 0 writes dV out, warpgroup 1 dK
+            # warpgroup 0 writes dV out, warpgroup 1 dK, each staged in the dS region (warpgroup
+            # 1 after warpgroup 0's tile store has read it) and stored by TMA
             yield from self.wait(("DKVFull", 0), u)
             self.check(self.dkv == (u, n), "dK/dV read out unfinished")
+            if half == 1:
+                yield from self.wait(("OutFree", 0), u)
+            elif u > 0 and self.out_free_wait:
+                yield from self.wait(("OutFree", 1), u - 1)
+            self.check(self.ds_smem is None or self.ds_smem[0] == "dS" or self.ds_smem[-1] == "read",
+                       "dK/dV staging overwrote an unread tile")
+            self.ds_smem = ("out", u, half)
             yield ("step",)
             self.dkv_read.add(half)
             if self.dkv_read == {0, 1}:
                 self.dkv, self.dkv_read = None, set()
             self.b[("DKVEmpty", 0)].arrive()
+            yield ("step",)
+            self.check(self.ds_smem == ("out", u, half), "dK/dV store read another tile")
+            self.ds_smem = ("out", u, half, "read")
+            self.b[("OutFree", half)].arrive()
 
     def run(self, max_events=200000):
         roles = {"producer": self.producer(), "mma": self.mma(), "wg0": self.wg(0), "wg1": self.wg(1)}
@@ -681,6 +700,19 @@ def test_backward_planted_early_p_store_is_caught():
     for seed in range(400):
         try:
             BwdModel([2, 1], random.Random(seed), read_barrier=False).run()
+        except (Violation, Deadlock):
+            found = True
+            break
+    assert found
+
+
+def test_backward_planted_early_dv_staging_is_caught():
+    # with a unit that has no steps, nothing but the store-read barrier keeps warpgroup 0's dV
+    # staging off warpgroup 1's previous dK tile
+    found = False
+    for seed in range(400):
+        try:
+            BwdModel([1, 0, 1], random.Random(seed), out_free_wait=False).run()
         except (Violation, Deadlock):
             found = True
             break
