@@ -192,14 +192,6 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src
         : "memory");
 }
 
-// a 4-D tile of a tensor into L2 (a hint: no completion to wait for)
-__device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int c0, int c1, int c2, int c3) {
-    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-                 : "memory");
-}
-
 // four floats from shared memory (an explicit shared-space load: through a generic pointer
 // the loads went down the generic path, whose latency every element's chain then waited on)
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
@@ -464,17 +456,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 kv_coords(un, c1, c2);
                 ptx::tma_load_4d(dk, &kmap, bar(kBarKV), c * 64, c1, c2, un.b, pol_kv);
                 ptx::tma_load_4d(dv, &vmap, bar(kBarKV), c * 64, c1, c2, un.b, pol_kv);
-            }
-            // the next unit's K_j, V_j toward L2 now, so that its reload at the boundary does
-            // not wait on DRAM
-            if (k + (int)gridDim.x < p.n_units) {
-                const Unit nx = decode_unit(p, k + (int)gridDim.x);
-                for (int c = 0; c < G::kChunks; ++c) {
-                    int c1, c2;
-                    kv_coords(nx, c1, c2);
-                    tma_prefetch_l2_4d(&kmap, c * 64, c1, c2, nx.b);
-                    tma_prefetch_l2_4d(&vmap, c * 64, c1, c2, nx.b);
-                }
             }
             for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
                 const int h = un.kvh * p.group + st % p.group;
