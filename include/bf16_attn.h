@@ -25,7 +25,10 @@
  * on a given GPU model (the work split is a pure function of shape and SM count).
  *
  * Ownership.  The caller owns q, k, v, o and any workspace; the library never frees them.
- * All calls are asynchronous on `stream` and return before the GPU runs.  attn_fwd() keeps
+ * All calls are asynchronous on `stream` and return before the GPU runs.  Each kernel is
+ * launched as a programmatic dependent of the kernel before it on `stream`: it may start its
+ * prologue while that kernel finishes, but waits for that kernel's memory before it reads or
+ * writes global memory, so calls are ordered exactly as plain stream launches.  attn_fwd() keeps
  * one lazily grown workspace per device (guarded by a mutex): it may call cudaMalloc the
  * first time a shape needs the split path, so call it once before any CUDA-graph capture,
  * or use attn_fwd_ws() with caller memory.
@@ -239,7 +242,9 @@ int attn_version(void);
  *   dout         dO, bf16, like o
  *   lse          the forward's fp32 [B][H][Sq] natural-log log-sum-exp (attn_fwd_ex's lse)
  *   dq, dk, dv   outputs, bf16, like q, k, v (round to nearest even); must not overlap the
- *                inputs, each other or the workspace
+ *                inputs, each other or the workspace.  dk and dv are bitwise reproducible;
+ *                the last bits of dq can differ between runs (its fp32 accumulator takes one
+ *                addition per key tile, in no fixed order)
  *   causal       0 or 1, as in the forward
  *   wait_limit_ms  0: 2000 ms; otherwise the bound, in ms, on any single wait in the kernel
  *   test_hooks   0 for normal use; ATTN_TEST_WITHHOLD_O_READY makes the first CTA skip the
