@@ -499,43 +499,69 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 ptx::tmem_ld128(tS, s);
                 // keys of this tile past `limit` are absent: beyond Skv, or (causal) past this
                 // row's diagonal; they get -inf logits and so weight 0
+                int limit = kBN - 1;
                 if constexpr (kCausal) {
-                    int limit = p.Skv - j * kBN - 1;
+                    limit = p.Skv - j * kBN - 1;
                     const int diag = it.qb * kUnitRows + t * kBM + row + p.causal_off - j * kBN;
                     limit = diag < limit ? diag : limit;
-                    if (__any_sync(0xFFFFFFFFu, limit < kBN - 1)) {
-#pragma unroll
-                        for (int e = 0; e < 128; ++e)
-                            if (e > limit) s[e] = __float_as_uint(-INFINITY);
-                    }
                 } else {
                     const int valid = p.Skv - j * kBN;   // the same for every row of the tile
-                    if (valid < kBN) {
-#pragma unroll
-                        for (int e = 0; e < 128; ++e)
-                            if (e >= valid) s[e] = __float_as_uint(-INFINITY);
-                    }
+                    limit = valid < kBN ? valid - 1 : kBN - 1;
                 }
-                // row max and min: 3-input trees over 4 independent chains each
-                float mxa[4], mna[4];
+                float mx, mn;
+                if (__any_sync(0xFFFFFFFFu, limit < kBN - 1)) {
+                    // the row min (which only decides whether the exponent clamp below can be
+                    // skipped) over the raw logits, before the mask: a masked key's weight is
+                    // exactly 0 from its -inf and needs no clamp, and counting masked keys' raw
+                    // logits (zero past Skv, where K is zero-filled) only makes the test stricter
+                    float mna[4], mxa[4];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) mxa[q4] = mna[q4] = __uint_as_float(s[q4]);
+                    for (int q4 = 0; q4 < 4; ++q4) mna[q4] = __uint_as_float(s[q4]);
 #pragma unroll
-                for (int e = 4; e < 124; e += 8) {
+                    for (int e = 4; e < 124; e += 8) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            mna[q4] = ptx::fmin3(mna[q4], __uint_as_float(s[e + q4]), __uint_as_float(s[e + 4 + q4]));
+                    }
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) mna[q4] = fminf(mna[q4], __uint_as_float(s[124 + q4]));
+                    mn = ptx::fmin3(mna[0], mna[1], fminf(mna[2], mna[3]));
+#pragma unroll
+                    for (int e = 0; e < 128; ++e)
+                        if (e > limit) s[e] = __float_as_uint(-INFINITY);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) mxa[q4] = __uint_as_float(s[q4]);
+#pragma unroll
+                    for (int e = 4; e < 124; e += 8) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            mxa[q4] = ptx::fmax3(mxa[q4], __uint_as_float(s[e + q4]), __uint_as_float(s[e + 4 + q4]));
+                    }
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) mxa[q4] = fmaxf(mxa[q4], __uint_as_float(s[124 + q4]));
+                    mx = ptx::fmax3(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3]));
+                } else {
+                    // row max and min: 3-input trees over 4 independent chains each
+                    float mxa[4], mna[4];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) mxa[q4] = mna[q4] = __uint_as_float(s[q4]);
+#pragma unroll
+                    for (int e = 4; e < 124; e += 8) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const float a = __uint_as_float(s[e + q4]), b = __uint_as_float(s[e + 4 + q4]);
+                            mxa[q4] = ptx::fmax3(mxa[q4], a, b);
+                            mna[q4] = ptx::fmin3(mna[q4], a, b);
+                        }
+                    }
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
-                        const float a = __uint_as_float(s[e + q4]), b = __uint_as_float(s[e + 4 + q4]);
-                        mxa[q4] = ptx::fmax3(mxa[q4], a, b);
-                        mna[q4] = ptx::fmin3(mna[q4], a, b);
+                        mxa[q4] = fmaxf(mxa[q4], __uint_as_float(s[124 + q4]));
+                        mna[q4] = fminf(mna[q4], __uint_as_float(s[124 + q4]));
                     }
+                    mx = ptx::fmax3(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3]));
+                    mn = ptx::fmin3(mna[0], mna[1], fminf(mna[2], mna[3]));
                 }
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    mxa[q4] = fmaxf(mxa[q4], __uint_as_float(s[124 + q4]));
-                    mna[q4] = fminf(mna[q4], __uint_as_float(s[124 + q4]));
-                }
-                const float mx = ptx::fmax3(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3]));
-                const float mn = ptx::fmin3(mna[0], mna[1], fminf(mna[2], mna[3]));
                 const float m_new = fmaxf(m_ref, mx);
                 bool rescale_o = false;
                 float alpha = 1.0f;
