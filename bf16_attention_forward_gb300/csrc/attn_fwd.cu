@@ -137,6 +137,17 @@ struct Item {
     int b, h, hk, qb, kv_begin, kv_end, split_slot;   // hk: the K/V head query head h reads
 };
 
+// The item a CTA runs in its r-th round: round-robin, and for causal launches in alternating
+// direction (CTA c takes position c of even rounds and G - 1 - c of odd ones).  Causal items
+// run heaviest first and shrink from round to round, so plain round-robin gives the low CTAs
+// the heavier item of every round (a trace on the causal prefill had the first CTA done 13 %
+// before the last); alternating cancels that.  Within a CTA, items still increase with r.
+template <bool kCausal>
+__device__ __forceinline__ int round_item(int r) {
+    const int c = (kCausal && (r & 1)) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    return r * (int)gridDim.x + c;
+}
+
 // Work item k of the static schedule.  kCausal is a template parameter so that the
 // unmasked kernel carries none of the causal code.
 template <bool kCausal>
@@ -330,7 +341,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             uint32_t pos = 0;             // ring position (monotonic)
             int u = 0;
             bool ok = true;
-            for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
+            for (int r = 0, k = round_item<kCausal>(0); k < p.n_items && ok; k = round_item<kCausal>(++r), ++u) {
                 const Item it = decode_item<kCausal>(p, k);
                 if (u > 0 && !(ok = wait_bar(bar(G::kBarQEmpty), (u - 1) & 1, kSiteQEmpty, abort_flag, lim)))
                     break;
@@ -415,7 +426,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             uint32_t pcount = 0;   // P_t phases consumed (same count for both tiles)
             int u = 0;
             bool ok = true;
-            for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
+            for (int r = 0, k = round_item<kCausal>(0); k < p.n_items && ok; k = round_item<kCausal>(++r), ++u) {
                 const Item it = decode_item<kCausal>(p, k);
                 const int nk = it.kv_end - it.kv_begin;
                 if (!(ok = wait_bar(bar(G::kBarQFull), u & 1, kSiteQFull, abort_flag, lim))) break;
@@ -486,7 +497,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         uint32_t scount = 0;
         int u = 0;
         bool ok = true;
-        for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++u) {
+        for (int r = 0, k = round_item<kCausal>(0); k < p.n_items && ok; k = round_item<kCausal>(++r), ++u) {
             const Item it = decode_item<kCausal>(p, k);
             float m_ref = -INFINITY;      // running max of raw logits at the last rescale
             float l = 0.0f;               // running sum of weights relative to m_ref
