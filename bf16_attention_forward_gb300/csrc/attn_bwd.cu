@@ -111,6 +111,7 @@ struct BwdParams {
     int B, H, Hkv, Sq, Skv, group;
     int nq, nkv, nq_pad_rows;    // query tiles, key tiles, rows per (b, h) in the stat arrays
     int n_units;
+    int paired;                  // 1: the paired schedule of causal units (sched_pos, unit_at)
     int causal, causal_off;      // key j visible to query i iff j <= i + causal_off
     int bshd;
     float scale;                 // 1/sqrt(d)
@@ -146,6 +147,26 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams& p, int k) {
     const int nt = u.it_lo < p.nq ? p.nq - u.it_lo : 0;
     u.nsteps = nt * p.group;
     return u;
+}
+
+// The schedule: a CTA's n-th unit sits at position sched_pos(n) of the unit order, and
+// unit_at() maps a position to a unit.  Without the mask every unit has the same length and
+// positions go round-robin.  Causal units shrink with their key tile (fewer query tiles see
+// later keys), and round-robin left CTAs up to 1.3-1.7x the mean load (a model of per-CTA
+// query steps on the causal prefill and square shapes); so positions within each (b, K/V
+// head) take key tiles 0, n-1, 1, n-2, ... and each CTA takes two consecutive positions per
+// round, a pair whose lengths add up to about the same total.  A round still covers
+// consecutive (b, K/V head) groups, so the Q and dO those units read stay shared in L2.
+// Pairs are used (p.paired) for causal launches with at least two units per CTA.
+__device__ __forceinline__ int sched_pos(const BwdParams& p, int n) {
+    if (!p.paired) return n * (int)gridDim.x + (int)blockIdx.x;
+    return (n >> 1) * 2 * (int)gridDim.x + 2 * (int)blockIdx.x + (n & 1);
+}
+__device__ __forceinline__ int unit_at(const BwdParams& p, int pos) {
+    if (!p.paired) return pos;
+    const int g = pos / p.nkv, i = pos % p.nkv;
+    const int jt = (i & 1) ? p.nkv - 1 - (i >> 1) : (i >> 1);
+    return g * p.nkv + jt;
 }
 
 __device__ __forceinline__ bool bwd_wait(uint32_t bar, uint32_t parity, uint32_t site,
@@ -443,8 +464,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             c1 = p.bshd ? un.kvh : un.jt * kBN;
             c2 = p.bshd ? un.jt * kBN : un.kvh;
         };
-        for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x, ++u) {
-            const Unit un = decode_unit(p, k);
+        for (int n = 0, k = sched_pos(p, 0); k < p.n_units && ok; k = sched_pos(p, ++n), ++u) {
+            const Unit un = decode_unit(p, unit_at(p, k));
             // the unit's first Q/dO goes in before the wait for the previous unit's K/V to be
             // released, so that it does not wait behind that unit's last GEMMs
             if (un.nsteps > 0 && !(ok = load_q(un, 0, s))) break;
@@ -528,8 +549,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         };
         uint32_t s = 0, u = 0;
         bool ok = true;
-        for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x, ++u) {
-            const Unit un = decode_unit(p, k);
+        for (int n = 0, k = sched_pos(p, 0); k < p.n_units && ok; k = sched_pos(p, ++n), ++u) {
+            const Unit un = decode_unit(p, unit_at(p, k));
             if (!(ok = bwd_wait(bar(kBarKV), u & 1u, kSiteKV, abort_flag, lim))) break;
             for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
                 const uint32_t sg = s % kStages;
@@ -585,8 +606,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         static_assert(8 * (kHC / 32) * 4096 == G::kStageBytes, "the dQ boxes fill one Q/dO stage");
         uint32_t s = 0, u = 0;
         bool ok = true;
-        for (int k = blockIdx.x; k < p.n_units && ok; k += gridDim.x, ++u) {
-            const Unit un = decode_unit(p, k);
+        for (int n = 0, k = sched_pos(p, 0); k < p.n_units && ok; k = sched_pos(p, ++n), ++u) {
+            const Unit un = decode_unit(p, unit_at(p, k));
             for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
                 if (!(ok = pds_step(un, un.it_lo + st / p.group, s, half))) break;
                 ok = bwd_wait(bar(kBarDQFull), s & 1u, kSiteDQFull, abort_flag, lim);
@@ -907,6 +928,7 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     p.n_units = (int)(a.B * a.Hkv * p.nkv);
     p.causal = a.causal;
     p.causal_off = (int)(a.Skv - a.Sq);
+    p.paired = (a.causal && p.n_units >= 2 * sms) ? 1 : 0;
     p.bshd = bshd ? 1 : 0;
     p.scale = (float)(1.0 / std::sqrt((double)d));
     p.scale_log2 = (float)((1.0 / std::sqrt((double)d)) * 1.4426950408889634);

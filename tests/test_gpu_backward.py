@@ -149,3 +149,16 @@ def test_backward_square_workload_sampled_heads(attn):
         tol = 2.0 ** -7 * ref[name + "_a"].reshape(-1) + parity.bf16_ulp(ref[name + "_bits"].reshape(-1))
         bad = ~(np.abs(gf - r) <= tol)
         assert not bad.any(), (name, int(bad.sum()))
+
+
+@pytest.mark.parametrize("shape", [(2, 32, 16, 1280, 1280, "bshd"), (1, 40, 40, 700, 1000, "bhsd")],
+                         ids=lambda s: "B%dH%dHkv%dSq%dSkv%d%s" % s)
+def test_backward_causal_paired_schedule(attn, shape):
+    # at least two causal units per SM: the backward then runs its paired schedule (key tiles
+    # jt and n-1-jt of one (b, K/V head) on the same CTA, two positions per round)
+    B, H, Hkv, Sq, Skv, layout = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert B * Hkv * -(-Skv // 128) >= 2 * sms, "shape too small for the paired schedule"
+    q, k, v = make_qkv(B, H, Sq, Skv, 128, layout, seed=5900 + Sq, Hkv=Hkv)
+    g = make_qkv(B, H, Sq, 1, 128, layout, seed=5950 + Skv)[0]
+    check_bwd(attn, q, k, v, g, layout, causal=True)
