@@ -111,6 +111,8 @@ struct BwdParams {
     int B, H, Hkv, Sq, Skv, group;
     int nq, nkv, nq_pad_rows;    // query tiles, key tiles, rows per (b, h) in the stat arrays
     int n_units;
+    int n_items, n_full;         // work items; items >= n_full are query-range parts of tail units
+    int nsplit;                  // parts per split unit (1: nothing split)
     int paired;                  // 1: the paired schedule of causal units (sched_pos, unit_at)
     int causal, causal_off;      // key j visible to query i iff j <= i + causal_off
     int bshd;
@@ -119,6 +121,7 @@ struct BwdParams {
     const float* lse2;           // [B*H][nq_pad_rows] base-2 log-sum-exp
     const float* delta;          // [B*H][nq_pad_rows] D_i
     float* dq_acc;               // [B][H][Sq][d] fp32
+    float* ws_dkv;               // [split items][2: dV, dK][128][d] fp32 partials
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     long long kv_sb, kv_ss, kv_sh;   // element strides of dK/dV for b, s, h
@@ -130,6 +133,8 @@ struct Unit {
     int b, kvh, jt;          // batch, K/V head, key tile
     int it_lo;               // first query tile with a visible key
     int nsteps;              // query tiles x query heads of the group
+    int st0, st1;            // the steps this work item runs, [st0, st1): all of them unless split
+    int slot;                // split item: the row of its dV/dK partials in the workspace; else -1
 };
 
 __device__ __forceinline__ Unit decode_unit(const BwdParams& p, int k) {
@@ -167,6 +172,27 @@ __device__ __forceinline__ int unit_at(const BwdParams& p, int pos) {
     const int g = pos / p.nkv, i = pos % p.nkv;
     const int jt = (i & 1) ? p.nkv - 1 - (i >> 1) : (i >> 1);
     return g * p.nkv + jt;
+}
+
+// Work item at schedule position pos.  Items below n_full are whole units (the paired causal
+// schedule maps positions to units first); the rest split the last, partial round's units into
+// nsplit ranges of query steps each, whose dK/dV partials a final kernel adds in part order.
+__device__ __forceinline__ Unit decode_item(const BwdParams& p, int pos) {
+    Unit u;
+    if (pos < p.n_full) {
+        u = decode_unit(p, unit_at(p, pos));
+        u.st0 = 0;
+        u.st1 = u.nsteps;
+        u.slot = -1;
+    } else {
+        const int r = pos - p.n_full, t = r / p.nsplit, part = r % p.nsplit;
+        u = decode_unit(p, p.n_full + t);
+        const int base = u.nsteps / p.nsplit, rem = u.nsteps % p.nsplit;
+        u.st0 = part * base + (part < rem ? part : rem);
+        u.st1 = u.st0 + base + (part < rem ? 1 : 0);
+        u.slot = r;
+    }
+    return u;
 }
 
 __device__ __forceinline__ bool bwd_wait(uint32_t bar, uint32_t parity, uint32_t site,
@@ -464,11 +490,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             c1 = p.bshd ? un.kvh : un.jt * kBN;
             c2 = p.bshd ? un.jt * kBN : un.kvh;
         };
-        for (int n = 0, k = sched_pos(p, 0); k < p.n_units && ok; k = sched_pos(p, ++n), ++u) {
-            const Unit un = decode_unit(p, unit_at(p, k));
+        for (int n = 0, k = sched_pos(p, 0); k < p.n_items && ok; k = sched_pos(p, ++n), ++u) {
+            const Unit un = decode_item(p, k);
             // the unit's first Q/dO goes in before the wait for the previous unit's K/V to be
             // released, so that it does not wait behind that unit's last GEMMs
-            if (un.nsteps > 0 && !(ok = load_q(un, 0, s))) break;
+            if (un.st1 > un.st0 && !(ok = load_q(un, un.st0, s))) break;
             if (u > 0 && !(ok = bwd_wait(bar(kBarKVEmpty), (u - 1) & 1u, kSiteKVEmpty, abort_flag, lim))) break;
             ptx::mbar_arrive_expect_tx(bar(kBarKV), 2 * G::kTileBytes);
             for (int c = 0; c < G::kChunks; ++c) {
@@ -478,10 +504,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 ptx::tma_load_4d(dk, &kmap, bar(kBarKV), c * 64, c1, c2, un.b, pol_kv);
                 ptx::tma_load_4d(dv, &vmap, bar(kBarKV), c * 64, c1, c2, un.b, pol_kv);
             }
-            for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
+            for (int st = un.st0; st < un.st1 && ok; ++st, ++s) {
                 const int h = un.kvh * p.group + st % p.group;
                 const int it = un.it_lo + st / p.group;
-                if (st > 0 && !(ok = load_q(un, st, s))) break;
+                if (st > un.st0 && !(ok = load_q(un, st, s))) break;
                 // the statistics buffer is free once the previous step's P^T/dS^T are done
                 if (s > 0 && !(ok = bwd_wait(bar(kBarPFull), (s - 1) & 1u, kSitePFull, abort_flag, lim))) break;
                 dep_wait();
@@ -549,10 +575,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         };
         uint32_t s = 0, u = 0;
         bool ok = true;
-        for (int n = 0, k = sched_pos(p, 0); k < p.n_units && ok; k = sched_pos(p, ++n), ++u) {
-            const Unit un = decode_unit(p, unit_at(p, k));
+        for (int n = 0, k = sched_pos(p, 0); k < p.n_items && ok; k = sched_pos(p, ++n), ++u) {
+            const Unit un = decode_item(p, k);
             if (!(ok = bwd_wait(bar(kBarKV), u & 1u, kSiteKV, abort_flag, lim))) break;
-            for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
+            for (int st = un.st0; st < un.st1 && ok; ++st, ++s) {
                 const uint32_t sg = s % kStages;
                 const uint64_t so = (uint64_t)((sg * G::kStageBytes) >> 4);
                 if (!(ok = bwd_wait(bar(kBarQFull + sg), (s / kStages) & 1u, kSiteQFull, abort_flag, lim))) break;
@@ -566,17 +592,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 ptx::mma_commit(bar(kBarDPFull));
                 if (!(ok = bwd_wait(bar(kBarPFull), s & 1u, kSitePFull, abort_flag, lim))) break;
                 // the previous unit's dK, dV have been read before the first step overwrites them
-                if (st == 0 && u > 0 && !(ok = bwd_wait(bar(kBarDKVEmpty), (u - 1) & 1u, kSiteDKVEmpty, abort_flag, lim)))
+                if (st == un.st0 && u > 0 && !(ok = bwd_wait(bar(kBarDKVEmpty), (u - 1) & 1u, kSiteDKVEmpty, abort_flag, lim)))
                     break;
                 ptx::tc_fence_after();
-                gemm_tm(tDV, tS, dDO_mn + so, st > 0);    // dV += P^T dO_i
-                gemm_tm(tDK, tDP, dQ_mn + so, st > 0);    // dK += dS^T Q_i
+                gemm_tm(tDV, tS, dDO_mn + so, st > un.st0);    // dV += P^T dO_i
+                gemm_tm(tDK, tDP, dQ_mn + so, st > un.st0);    // dK += dS^T Q_i
                 ptx::mma_commit(bar(kBarQEmpty + sg));
                 gemm_mm(tDQ, dDS_mn, dK_mn);              // dQ_i = dS K_j
                 ptx::mma_commit(bar(kBarDQFull));
             }
             if (!ok) break;
-            if (un.nsteps == 0 && u > 0 &&
+            if (un.st1 == un.st0 && u > 0 &&
                 !(ok = bwd_wait(bar(kBarDKVEmpty), (u - 1) & 1u, kSiteDKVEmpty, abort_flag, lim)))
                 break;
             // (test hook: CTA 0 withholds its first unit's dK/dV-ready signal, so that the
@@ -606,9 +632,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         static_assert(8 * (kHC / 32) * 4096 == G::kStageBytes, "the dQ boxes fill one Q/dO stage");
         uint32_t s = 0, u = 0;
         bool ok = true;
-        for (int n = 0, k = sched_pos(p, 0); k < p.n_units && ok; k = sched_pos(p, ++n), ++u) {
-            const Unit un = decode_unit(p, unit_at(p, k));
-            for (int st = 0; st < un.nsteps && ok; ++st, ++s) {
+        for (int n = 0, k = sched_pos(p, 0); k < p.n_items && ok; k = sched_pos(p, ++n), ++u) {
+            const Unit un = decode_item(p, k);
+            for (int st = un.st0; st < un.st1 && ok; ++st, ++s) {
                 if (!(ok = pds_step(un, un.it_lo + st / p.group, s, half))) break;
                 ok = bwd_wait(bar(kBarDQFull), s & 1u, kSiteDQFull, abort_flag, lim);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
@@ -652,6 +678,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             ok = bwd_wait(bar(kBarDKVFull), u & 1u, kSiteDKVFull, abort_flag, lim);
             if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             ptx::tc_fence_after();
+            // a split item's dV/dK are partial sums: they go, unscaled and in fp32, to the item's
+            // row of the workspace (plain stores; one split item per CTA at most), and the final
+            // kernel adds the parts in order.  The barrier steps below run the same either way.
+            const bool split = un.slot >= 0;
             // the region holds the other warpgroup's tile until its store has read it: dV of this
             // unit for warpgroup 1; dK of the previous unit for warpgroup 0 (the next unit may
             // have no steps, so no dS^T write in between orders the two)
@@ -663,11 +693,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
-                if (un.nsteps > 0) {
+                if (un.st1 > un.st0) {
                     ptx::tmem_ld32((half ? tDK : tDV) + lane_off + 32u * c, v);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
+                if (split) {
+                    float4* dst = reinterpret_cast<float4*>(
+                        p.ws_dkv + ((size_t)(un.slot * 2 + half) * kBN + (size_t)row) * D + 32 * c);
+#pragma unroll
+                    for (int v4 = 0; v4 < 8; ++v4)
+                        dst[v4] = make_float4(__uint_as_float(v[4 * v4]), __uint_as_float(v[4 * v4 + 1]),
+                                              __uint_as_float(v[4 * v4 + 2]), __uint_as_float(v[4 * v4 + 3]));
+                    continue;
                 }
                 // row `row`, columns 32c..32c+31: 16-byte pieces (c & 1)*4 + v4 of the 64-column
                 // chunk c >> 1 (16 KB apart, rows 128 B apart), at piece ^ (row & 7) (the tensor
@@ -691,7 +730,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             if (quarter == 0) {
                 if (lane == 0) {
                     ok = bwd_wait(bar(kBarOutStaged + half), u & 1u, kSiteOutStaged, abort_flag, lim);
-                    if (ok) {
+                    if (ok && split) {
+                        ptx::mbar_arrive(bar(kBarOutFree + half));
+                    } else if (ok) {
                         int c1, c2;
                         c1 = p.bshd ? un.kvh : un.jt * kBN;
                         c2 = p.bshd ? un.jt * kBN : un.kvh;
@@ -773,26 +814,70 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __nv_bfloat16*
     }
 }
 
-// dq (bf16, the caller's layout) = dq_acc (fp32 [B][H][Sq][d]), round to nearest even; 8
-// columns per thread (two 16-byte loads, one 16-byte store), grid-stride.  Launched as a
-// programmatic dependent of the main kernel: it waits for that kernel's memory first.
+// The split units' dK, dV: the sum of their parts' fp32 partials, in part order (a fixed
+// order, so results are deterministic), dK times 1/sqrt(d), rounded to nearest even.
+struct DkvCombine {
+    const float* ws;             // [T * P items][2: dV, dK][128][d]
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    int T, P, n_full, nkv, Hkv, Skv;
+    long long kv_sb, kv_ss, kv_sh;
+    float scale;
+};
+
+// The backward's last kernel.  Blocks [0, dq_blocks): dq (bf16, the caller's layout) = dq_acc
+// (fp32 [B][H][Sq][d]), round to nearest even, 8 columns per thread (two 16-byte loads, one
+// 16-byte store), grid-stride.  Blocks from dq_blocks on: the split units' dK/dV, one warp per
+// (unit, tensor, key row), D/32 columns per lane.  Launched as a programmatic dependent of the
+// main kernel: it waits for that kernel's memory first.
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const float* dq_acc, __nv_bfloat16* dq, int H, int Sq,
                                                           long long n8, long long o_sb, long long o_ss,
-                                                          long long o_sh) {
+                                                          long long o_sh, int dq_blocks, const DkvCombine cb) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
-        const long long row = i / (D / 8);
-        const int x = (int)(i % (D / 8)) * 8;
-        const int q = (int)(row % Sq);
-        const long long bh = row / Sq;
-        const int h = (int)(bh % H), b = (int)(bh / H);
-        const float4* src = reinterpret_cast<const float4*>(dq_acc + row * D + x);
-        const float4 v0 = src[0], v1 = src[1];
-        __nv_bfloat16* dst = dq + (long long)b * o_sb + (long long)q * o_ss + (long long)h * o_sh + x;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(pack2(v0.x, v0.y), pack2(v0.z, v0.w), pack2(v1.x, v1.y),
-                                                    pack2(v1.z, v1.w));
+    if ((int)blockIdx.x < dq_blocks) {
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+             i += (long long)dq_blocks * blockDim.x) {
+            const long long row = i / (D / 8);
+            const int x = (int)(i % (D / 8)) * 8;
+            const int q = (int)(row % Sq);
+            const long long bh = row / Sq;
+            const int h = (int)(bh % H), b = (int)(bh / H);
+            const float4* src = reinterpret_cast<const float4*>(dq_acc + row * D + x);
+            const float4 v0 = src[0], v1 = src[1];
+            __nv_bfloat16* dst = dq + (long long)b * o_sb + (long long)q * o_ss + (long long)h * o_sh + x;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(pack2(v0.x, v0.y), pack2(v0.z, v0.w), pack2(v1.x, v1.y),
+                                                        pack2(v1.z, v1.w));
+        }
+        return;
     }
+    const long long w = (long long)((int)blockIdx.x - dq_blocks) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (w >= (long long)cb.T * 2 * kBN) return;
+    const int r = (int)(w % kBN);
+    const int which = (int)((w / kBN) % 2);            // 0: dV, 1: dK
+    const int t = (int)(w / (2 * kBN));
+    const int unit = cb.n_full + t;
+    const int jt = unit % cb.nkv, bk = unit / cb.nkv;
+    const int kvh = bk % cb.Hkv, b = bk / cb.Hkv;
+    const int kj = jt * kBN + r;
+    if (kj >= cb.Skv) return;
+    constexpr int kC = D / 32;                         // columns per lane: 4 or 2
+    float acc[kC];
+#pragma unroll
+    for (int e = 0; e < kC; ++e) acc[e] = 0.0f;
+    for (int part = 0; part < cb.P; ++part) {
+        const float* src = cb.ws + ((size_t)((t * cb.P + part) * 2 + which) * kBN + (size_t)r) * D + lane * kC;
+#pragma unroll
+        for (int e = 0; e < kC; ++e) acc[e] += src[e];
+    }
+    const float sc = which ? cb.scale : 1.0f;
+    __nv_bfloat16* out = (which ? cb.dk : cb.dv) + (long long)b * cb.kv_sb + (long long)kj * cb.kv_ss +
+                         (long long)kvh * cb.kv_sh + lane * kC;
+    if constexpr (kC == 4)
+        *reinterpret_cast<uint2*>(out) = make_uint2(pack2(acc[0] * sc, acc[1] * sc), pack2(acc[2] * sc, acc[3] * sc));
+    else
+        *reinterpret_cast<uint32_t*>(out) = pack2(acc[0] * sc, acc[1] * sc);
 }
 
 // ------------------------------------------------------------------------------ host side
@@ -850,13 +935,57 @@ size_t ws_bytes(const attn_bwd_args_t& a) {
     return (size_t)(a.B * a.H * a.Sq * a.d * 4) + (size_t)(2 * rows_pad * 4);
 }
 
+// Query-range split of the units of the last, partial round (none for causal launches, whose
+// units run on the paired schedule).  With T = units mod G left over (or all units when there
+// are fewer than G), each is cut into P parts of at least kMinSplitSteps query steps, P chosen
+// to minimise the longest CTA's load in the tail, ceil(T P / G) * (ceil(steps / P) + 3) (a
+// part costs about three steps more than its steps: its K/V load, its pipeline fill and its
+// partials' write; with one step of overhead the square backward split its 112 tail units 4
+// ways and lost 5 %), the fewest parts among equals, with T P at most 4 G.  P = 1: nothing
+// split.
+constexpr int64_t kMinSplitSteps = 4;
+struct BwdSplit {
+    int64_t T, P;
+};
+BwdSplit bwd_split(const attn_bwd_args_t& a, int64_t G) {
+    if (a.causal || G < 1) return {0, 1};
+    const int64_t n_units = a.B * a.Hkv * cdiv(a.Skv, kBN);
+    const int64_t steps = (a.H / a.Hkv) * cdiv(a.Sq, kBM);
+    const int64_t T = n_units % G;
+    if (T == 0) return {0, 1};
+    int64_t bestP = 1, best = steps + 3;
+    for (int64_t P = 2; P * kMinSplitSteps <= steps && T * P <= 4 * G; ++P) {
+        const int64_t cost = cdiv(T * P, G) * (cdiv(steps, P) + 3);
+        if (cost < best) {
+            best = cost;
+            bestP = P;
+        }
+    }
+    return bestP > 1 ? BwdSplit{T, bestP} : BwdSplit{0, 1};
+}
+
+// the split partials' bytes: [T * P][2][128][d] fp32
+size_t split_bytes(const attn_bwd_args_t& a, const BwdSplit& sp) {
+    return (size_t)(sp.T * sp.P * 2 * kBN * a.d * 4);
+}
+
+// SM count of the current device (0 if there is none): the split depends on it
+int64_t current_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return sms;
+}
+
 }  // namespace
 
 extern "C" {
 
 size_t attn_bwd_workspace_size(const attn_bwd_args_t* args) {
     if (!args || check_shape(*args) != ATTN_OK) return 0;
-    return ws_bytes(*args);
+    return ws_bytes(*args) + split_bytes(*args, bwd_split(*args, current_sms()));
 }
 
 int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_bytes, attn_stream_t stream_) {
@@ -868,8 +997,13 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     const uintptr_t al = (uintptr_t)a.q | (uintptr_t)a.k | (uintptr_t)a.v | (uintptr_t)a.o | (uintptr_t)a.dout |
                          (uintptr_t)a.dq | (uintptr_t)a.dk | (uintptr_t)a.dv | (uintptr_t)workspace;
     if ((al & 15u) || ((uintptr_t)a.lse & 3u)) return ATTN_ERR_MISALIGNED;
-    const size_t need = ws_bytes(a);
-    if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    const size_t need_min = ws_bytes(a);
+    if (!workspace || workspace_bytes < need_min) return ATTN_ERR_WORKSPACE;
+    // the tail split needs room for its partials; a workspace sized without it (another GPU
+    // model, an older size query) just runs unsplit
+    BwdSplit sp = bwd_split(a, current_sms());
+    if (workspace_bytes < need_min + split_bytes(a, sp)) sp = BwdSplit{0, 1};
+    const size_t need = need_min + split_bytes(a, sp);
     // the gradients must not overlap the inputs or each other
     const uintptr_t qb = (uintptr_t)(a.B * a.H * a.Sq * a.d * 2), kb = (uintptr_t)(a.B * a.Hkv * a.Skv * a.d * 2);
     const uintptr_t outs[3][2] = {{(uintptr_t)a.dq, qb}, {(uintptr_t)a.dk, kb}, {(uintptr_t)a.dv, kb}};
@@ -926,6 +1060,9 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     p.nkv = (int)cdiv(a.Skv, kBN);
     p.nq_pad_rows = p.nq * kBM;
     p.n_units = (int)(a.B * a.Hkv * p.nkv);
+    p.nsplit = (int)sp.P;
+    p.n_full = (int)(p.n_units - sp.T);
+    p.n_items = (int)(p.n_full + sp.T * sp.P);
     p.causal = a.causal;
     p.causal_off = (int)(a.Skv - a.Sq);
     p.paired = (a.causal && p.n_units >= 2 * sms) ? 1 : 0;
@@ -935,6 +1072,7 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     float* dq_acc = reinterpret_cast<float*>(workspace);
     float* lse2 = dq_acc + a.B * a.H * a.Sq * d;
     float* delta = lse2 + a.B * a.H * p.nq_pad_rows;
+    p.ws_dkv = delta + a.B * a.H * p.nq_pad_rows;      // split partials (16-byte aligned)
     p.lse2 = lse2;
     p.delta = delta;
     p.dq_acc = dq_acc;
@@ -979,7 +1117,7 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     }
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3((unsigned)(p.n_units < sms ? p.n_units : sms));
+    cfg.gridDim = dim3((unsigned)(p.n_items < sms ? p.n_items : sms));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = d == 128 ? smem_alloc<128>() : smem_alloc<64>();
     cfg.stream = stream;
@@ -993,14 +1131,31 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     }
     const long long n8 = a.B * a.H * a.Sq * (d / 8);
     const long long conv_blocks = cdiv(n8, 256);
-    cfg.gridDim = dim3((unsigned)(conv_blocks < fill ? conv_blocks : fill));
+    const int dq_blocks = (int)(conv_blocks < fill ? conv_blocks : fill);
+    DkvCombine cb;
+    memset(&cb, 0, sizeof cb);
+    cb.ws = p.ws_dkv;
+    cb.dk = p.dk;
+    cb.dv = p.dv;
+    cb.T = (int)sp.T;
+    cb.P = (int)sp.P;
+    cb.n_full = p.n_full;
+    cb.nkv = p.nkv;
+    cb.Hkv = p.Hkv;
+    cb.Skv = p.Skv;
+    cb.kv_sb = p.kv_sb;
+    cb.kv_ss = p.kv_ss;
+    cb.kv_sh = p.kv_sh;
+    cb.scale = p.scale;
+    const long long comb_blocks = sp.T * 2 * kBN / 8;   // one warp per (unit, tensor, key row)
+    cfg.gridDim = dim3((unsigned)(dq_blocks + comb_blocks));
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     __nv_bfloat16* dqo = reinterpret_cast<__nv_bfloat16*>(a.dq);
     ce = d == 128 ? cudaLaunchKernelEx(&cfg, attn_bwd_dq_kernel<128>, (const float*)dq_acc, dqo, p.H, p.Sq, n8, q_sb,
-                                       q_ss, q_sh)
+                                       q_ss, q_sh, dq_blocks, cb)
                   : cudaLaunchKernelEx(&cfg, attn_bwd_dq_kernel<64>, (const float*)dq_acc, dqo, p.H, p.Sq, n8, q_sb,
-                                       q_ss, q_sh);
+                                       q_ss, q_sh, dq_blocks, cb);
     if (ce != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_CUDA;

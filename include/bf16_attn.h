@@ -269,7 +269,10 @@ typedef struct {
     int32_t layout, causal, wait_limit_ms, test_hooks;
 } attn_bwd_args_t;
 
-/* Workspace bytes attn_bwd needs (fp32 dQ accumulator and per-row statistics; 0 if invalid). */
+/* Workspace bytes attn_bwd needs (0 if invalid): the fp32 dQ accumulator and per-row
+ * statistics, plus fp32 dK/dV partials when the last, partial round of work units is split by
+ * query range.  That split depends on the current device's SM count; attn_bwd given a
+ * workspace sized without the partials runs unsplit (same results up to rounding). */
 size_t attn_bwd_workspace_size(const attn_bwd_args_t* args);
 
 /*
