@@ -324,8 +324,8 @@ def run_backward(args, w):
         "data": "synthetic (seeded N(0,%g) bf16)" % w.sigma,
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.kv_heads, "Sq": w.Sq,
                    "Skv": w.Skv, "d": w.d, "causal": w.causal, "layout": w.layout,
-                   "step": "one attn_bwd call: dQ zeroing, D/LSE preprocessing, the tcgen05 "
-                           "backward kernel and the dQ rounding"},
+                   "step": "one attn_bwd call: D/LSE preprocessing with the dQ zeroing, the tcgen05 "
+                           "backward kernel, and the dQ rounding with any split units' dK/dV sums"},
         "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
                      "frac": value / peak, "peak_source": peak_src + " burst bf16 (cuBLAS)",
                      "timed": "whole call"},
