@@ -10,7 +10,8 @@
 //   dV = P^T dO,   dP = dO V^T,   D_i = dO_i . O_i,   dS = P * (dP - D),
 //   dQ = c dS K,   dK = c dS^T Q.
 // GB300 design:
-//   * a preprocessing kernel forms D_i (fp32) and the base-2 log-sum-exp per query row;
+//   * a preprocessing kernel forms D_i (fp32) and the base-2 log-sum-exp per query row and
+//     zeroes the fp32 dQ accumulator;
 //   * the main kernel gives each work unit one (b, K/V head) and one 128-key tile: K_j and
 //     V_j stay in shared memory while the unit walks every query tile of every query head
 //     that reads that K/V head.  Per query tile i it runs five tcgen05 GEMMs with the key
@@ -22,9 +23,14 @@
 //       dK  += dS^T Q_i           (dS^T read from TMEM)
 //       dQ_i = dS K_j             (dS^T also written to shared memory, read as an MN-major
 //                                  A operand; K_j as an MN-major B operand)
-//     dV and dK accumulate in TMEM for the whole unit; dQ_i is added into an fp32
-//     accumulator in global memory by TMA tensor reductions (many key tiles contribute);
-//   * a last kernel rounds the dQ accumulator to bf16 (round to nearest even).
+//     dV and dK accumulate in TMEM for the whole unit and go out as TMA tile stores; dQ_i is
+//     added into an fp32 accumulator in global memory by TMA tensor reductions (many key
+//     tiles contribute).  Causal units (which shrink with their key tile) run on a paired
+//     schedule, and otherwise the units of a last, partial round run as query-range parts
+//     whose fp32 dK/dV partials are added at the end;
+//   * a last kernel rounds the dQ accumulator to bf16 (round to nearest even) and adds the
+//     split units' dK/dV partials in part order.
+// Each kernel is a programmatic dependent of the one before it in the stream.
 // Roles: warp 8 TMA producer, warp 9 (one thread) MMA issuer; warpgroups 0 and 1 recompute P
 // and form dS for query columns 0..63 and 64..127 of each step, then each drains half of dQ's
 // columns; at the end of a unit warpgroup 0 writes dV and warpgroup 1 dK.  Every wait is
