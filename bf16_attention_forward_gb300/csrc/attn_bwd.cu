@@ -93,9 +93,9 @@ enum {
     kBarDQEmpty,     // dQ_i read out of TMEM (256 arrivals: each warpgroup reads half its columns)
     kBarDKVFull,     // the unit's dK, dV final in TMEM
     kBarDKVEmpty,    // dK, dV read out of TMEM (256 arrivals)
-    kBarOutStaged,   // [2] warpgroup h's dV (h = 0) or dK (h = 1) rows staged in the dS region (128 arrivals)
-    kBarOutFree = kBarOutStaged + 2,   // [2] warpgroup h's tile store has read the dS region
-    kBarDrain = kBarOutFree + 2,
+    kBarOutStaged,   // [2] warpgroup h's 64 columns of dV (h = 0) or dK (h = 1) staged in box h (128 arrivals)
+    kBarBoxFree = kBarOutStaged + 2,   // [2] warpgroup h's box store has read box h
+    kBarDrain = kBarBoxFree + 2,
     kNumBars
 };
 template <int D>
@@ -293,8 +293,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         ptx::mbar_init(bar(kBarDKVEmpty), 2 * kBN);
         ptx::mbar_init(bar(kBarOutStaged), kBN);
         ptx::mbar_init(bar(kBarOutStaged + 1), kBN);
-        ptx::mbar_init(bar(kBarOutFree), 1);
-        ptx::mbar_init(bar(kBarOutFree + 1), 1);
+        ptx::mbar_init(bar(kBarBoxFree), 1);
+        ptx::mbar_init(bar(kBarBoxFree + 1), 1);
         ptx::mbar_init(bar(kBarDrain), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
@@ -675,12 +675,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 if (lane == 0) ptx::mbar_arrive(bar(kBarStaged + (int)(s % kStages)));
             }
             if (!ok) continue;
-            // warpgroup 0 writes dV, warpgroup 1 dK (times 1/sqrt(d)): each reads its rows out of
-            // TMEM into the dS^T region (free from the unit's last GEMMs to the next unit's first
-            // dS^T), warpgroup 0 first, then releases TMEM, and one thread per warpgroup stores
-            // the tile with TMA (rows past Skv are clipped).  Per-thread row
-            // stores took ~5000-8000 cycles per unit here; a tile store is one TMA request per
-            // 64 columns.
+            // warpgroup h writes its tensor (0: dV, 1: dK times 1/sqrt(d)) through box h of the
+            // dS^T region (16 KB, 128 rows x 64 columns; the region is free from the unit's last
+            // GEMMs to the next unit's first dS^T), 64 columns at a time: it reads them out of
+            // TMEM and stages them in the box, and one thread stores the box with TMA (rows past
+            // Skv are clipped) and waits for the store to have read it before the box is
+            // refilled.  The two warpgroups work on their own boxes at the same time.  (One
+            // warpgroup writing all of dK and dV row by row took ~5000-8000 cycles per unit;
+            // the two tiles staged one after the other through the whole region, ~7000.)
             ok = bwd_wait(bar(kBarDKVFull), u & 1u, kSiteDKVFull, abort_flag, lim);
             if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             ptx::tc_fence_after();
@@ -688,73 +690,74 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             // row of the workspace (plain stores; one split item per CTA at most), and the final
             // kernel adds the parts in order.  The barrier steps below run the same either way.
             const bool split = un.slot >= 0;
-            // the region holds the other warpgroup's tile until its store has read it: dV of this
-            // unit for warpgroup 1; dK of the previous unit for warpgroup 0 (the next unit may
-            // have no steps, so no dS^T write in between orders the two)
-            if (half == 1 || u > 0) {
-                ok = bwd_wait(bar(kBarOutFree + (half ^ 1)), (half ? u : u - 1) & 1u, kSiteOutFree, abort_flag, lim);
-                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-            }
             const float sc = half ? p.scale : 1.0f;
+            const uint32_t box = sbase + G::kSmemDS + (uint32_t)(half * kChunkBytes);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                if (un.st1 > un.st0) {
-                    ptx::tmem_ld32((half ? tDK : tDV) + lane_off + 32u * c, v);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+            for (int cc = 0; cc < D / 64 && ok; ++cc) {
+                const uint32_t rnd = u * (uint32_t)(D / 64) + (uint32_t)cc;   // this warpgroup's round
+                // the box's previous store (this warpgroup's last round) has read it
+                if (rnd > 0) {
+                    ok = bwd_wait(bar(kBarBoxFree + half), (rnd - 1u) & 1u, kSiteOutFree, abort_flag, lim);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 }
-                if (split) {
-                    float4* dst = reinterpret_cast<float4*>(
-                        p.ws_dkv + ((size_t)(un.slot * 2 + half) * kBN + (size_t)row) * D + 32 * c);
+#pragma unroll 1
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int c = 2 * cc + c2;              // 32-column chunk of the row
+                    uint32_t v[32];
+                    if (un.st1 > un.st0) {
+                        ptx::tmem_ld32((half ? tDK : tDV) + lane_off + 32u * c, v);
+                    } else {
 #pragma unroll
-                    for (int v4 = 0; v4 < 8; ++v4)
-                        dst[v4] = make_float4(__uint_as_float(v[4 * v4]), __uint_as_float(v[4 * v4 + 1]),
-                                              __uint_as_float(v[4 * v4 + 2]), __uint_as_float(v[4 * v4 + 3]));
-                    continue;
-                }
-                // row `row`, columns 32c..32c+31: 16-byte pieces (c & 1)*4 + v4 of the 64-column
-                // chunk c >> 1 (16 KB apart, rows 128 B apart), at piece ^ (row & 7) (the tensor
-                // map's 128-byte swizzle)
-                const uint32_t rowaddr = sbase + G::kSmemDS + (uint32_t)((c >> 1) * kChunkBytes) + (uint32_t)row * 128u;
+                        for (int e = 0; e < 32; ++e) v[e] = 0u;
+                    }
+                    if (split) {
+                        float4* dst = reinterpret_cast<float4*>(
+                            p.ws_dkv + ((size_t)(un.slot * 2 + half) * kBN + (size_t)row) * D + 32 * c);
 #pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4) {
-                    const uint32_t pc = (uint32_t)((c & 1) * 4 + v4);
-                    const int e = 8 * v4;
-                    ptx::st_shared_v4(rowaddr + ((pc ^ (uint32_t)(row & 7)) << 4),
-                                      pack2(__uint_as_float(v[e]) * sc, __uint_as_float(v[e + 1]) * sc),
-                                      pack2(__uint_as_float(v[e + 2]) * sc, __uint_as_float(v[e + 3]) * sc),
-                                      pack2(__uint_as_float(v[e + 4]) * sc, __uint_as_float(v[e + 5]) * sc),
-                                      pack2(__uint_as_float(v[e + 6]) * sc, __uint_as_float(v[e + 7]) * sc));
-                }
-            }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(kBarDKVEmpty));
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(bar(kBarOutStaged + half));
-            if (quarter == 0) {
-                if (lane == 0) {
-                    ok = bwd_wait(bar(kBarOutStaged + half), u & 1u, kSiteOutStaged, abort_flag, lim);
-                    if (ok && split) {
-                        ptx::mbar_arrive(bar(kBarOutFree + half));
-                    } else if (ok) {
-                        int c1, c2;
-                        c1 = p.bshd ? un.kvh : un.jt * kBN;
-                        c2 = p.bshd ? un.jt * kBN : un.kvh;
-                        for (int cc = 0; cc < D / 64; ++cc)
-                            ptx::tma_store_4d(half ? (const void*)&dkmap : (const void*)&dvmap,
-                                              sbase + G::kSmemDS + (uint32_t)(cc * kChunkBytes), cc * 64, c1, c2, un.b);
-                        ptx::bulk_commit();
-                        // the region is rewritten (dK rows, or the next unit's dS^T) only after
-                        // the store has read it
-                        ptx::bulk_wait_read0();
-                        ptx::mbar_arrive(bar(kBarOutFree + half));
+                        for (int v4 = 0; v4 < 8; ++v4)
+                            dst[v4] = make_float4(__uint_as_float(v[4 * v4]), __uint_as_float(v[4 * v4 + 1]),
+                                                  __uint_as_float(v[4 * v4 + 2]), __uint_as_float(v[4 * v4 + 3]));
+                        continue;
+                    }
+                    // row `row` of the box, columns 32*c2 .. +31: 16-byte pieces c2*4 + v4 at
+                    // piece ^ (row & 7) (the tensor map's 128-byte swizzle)
+                    const uint32_t rowaddr = box + (uint32_t)row * 128u;
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        const uint32_t pc = (uint32_t)(c2 * 4 + v4);
+                        const int e = 8 * v4;
+                        ptx::st_shared_v4(rowaddr + ((pc ^ (uint32_t)(row & 7)) << 4),
+                                          pack2(__uint_as_float(v[e]) * sc, __uint_as_float(v[e + 1]) * sc),
+                                          pack2(__uint_as_float(v[e + 2]) * sc, __uint_as_float(v[e + 3]) * sc),
+                                          pack2(__uint_as_float(v[e + 4]) * sc, __uint_as_float(v[e + 5]) * sc),
+                                          pack2(__uint_as_float(v[e + 6]) * sc, __uint_as_float(v[e + 7]) * sc));
                     }
                 }
-                ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-                if (!ok) break;
+                if (cc == D / 64 - 1) {                       // TMEM read out: the next unit may start
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(bar(kBarDKVEmpty));
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(bar(kBarOutStaged + half));
+                if (quarter == 0) {
+                    if (lane == 0) {
+                        ok = bwd_wait(bar(kBarOutStaged + half), rnd & 1u, kSiteOutStaged, abort_flag, lim);
+                        if (ok) {
+                            if (!split) {
+                                const int y1 = p.bshd ? un.kvh : un.jt * kBN;
+                                const int y2 = p.bshd ? un.jt * kBN : un.kvh;
+                                ptx::tma_store_4d(half ? (const void*)&dkmap : (const void*)&dvmap, box, cc * 64, y1,
+                                                  y2, un.b);
+                                ptx::bulk_commit();
+                                ptx::bulk_wait_read0();
+                            }
+                            ptx::mbar_arrive(bar(kBarBoxFree + half));
+                        }
+                    }
+                    ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+                }
             }
+            if (!ok) break;
         }
         // the dK, dV stores complete before the CTA exits
         if (quarter == 0 && lane == 0) ptx::bulk_wait0();

@@ -457,22 +457,23 @@ class BwdModel(Model):
     once the step's GEMMs are done), and warpgroup 1 writes dK, dV.  The producer issues a
     stage's dQ reductions just before refilling it and waits for them to have read it."""
 
-    def __init__(self, units, rng, wait_reduce_reads=True, read_barrier=True, out_free_wait=True):
+    def __init__(self, units, rng, wait_reduce_reads=True, read_barrier=True, box_free_wait=True,
+                 rounds=2):
         # wait_reduce_reads=False plants a mistake: the producer refills a stage without waiting
         # for the reductions issued from it to have read it; read_barrier=False another: a
         # warpgroup stores P^T and dS^T without waiting for the other to have loaded S^T, dP^T
         self.units, self.rng, self.wait_reduce_reads = units, rng, wait_reduce_reads
         self.read_barrier = read_barrier
-        # out_free_wait=False plants a third: warpgroup 0 stages its dV tile without waiting for
-        # warpgroup 1's previous dK store to have read the region
-        self.out_free_wait = out_free_wait
+        # box_free_wait=False plants a third: a warpgroup restages its half of the dS region for
+        # the next 64 columns of dV/dK without waiting for the previous box store to have read it
+        self.box_free_wait, self.rounds = box_free_wait, rounds
         self.b = {}
         for n, c in (("KV", 1), ("KVEmpty", 1), ("Stats", 1), ("SFull", 1), ("DPFull", 1),
                      ("PFull", 2), ("Read", 2), ("DQFull", 1), ("DQEmpty", 2), ("DKVFull", 1),
                      ("DKVEmpty", 2)):
             self.b[(n, 0)] = Barrier(n, c)
         for i in range(2):
-            self.b[("OutFree", i)] = Barrier("OutFree[%d]" % i, 1)
+            self.b[("BoxFree", i)] = Barrier("BoxFree[%d]" % i, 1)
         for i in range(2):
             self.b[("QFull", i)] = Barrier("QFull[%d]" % i, 1)
             self.b[("QEmpty", i)] = Barrier("QEmpty[%d]" % i, 1)
@@ -483,7 +484,7 @@ class BwdModel(Model):
         self.t_sp = None                 # TMEM columns 0-127: ("S", s) or ("P", s)
         self.t_dp = None                 # TMEM 128-255: ("dP", s), ("dS", s) or ("dQ", s)
         self.dkv = None                  # (unit, steps accumulated) in the dV, dK columns
-        self.ds_smem = None              # ("dS", s) or ("stage", s): the dS region
+        self.ds_box = [None, None]       # the dS region's halves: ("dS", s) or a staged dV/dK box
         self.reduce_reading = None       # step whose staged dQ the producer's reductions still read
         self.dq_read = set()             # warpgroups that have read the current dQ out of TMEM
         self.dkv_read = set()            # warpgroups that have written their half of dK/dV out
@@ -586,7 +587,7 @@ class BwdModel(Model):
                 self.later(gemm_dvdk, channel="mma")
 
                 def gemm_dq(s=s, u=u):
-                    self.check(self.ds_smem == ("dS", s) and self.kv == u, "dQ read the wrong dS or K")
+                    self.check(self.ds_box == [("dS", s), ("dS", s)] and self.kv == u, "dQ read the wrong dS or K")
                     self.t_dp = ("dQ", s)
                     self.b[("DQFull", 0)].arrive()
                 self.later(gemm_dq, channel="mma")
@@ -613,9 +614,9 @@ class BwdModel(Model):
         if self.read_barrier:
             self.b[("Read", 0)].arrive()
             yield from self.wait(("Read", 0), s)
-        self.check(self.ds_smem is None or self.ds_smem[0] == "dS" or self.ds_smem[-1] == "read",
-                   "dS^T overwrote an unread dK/dV tile")
-        self.t_sp, self.t_dp, self.ds_smem = ("P", s), ("dS", s), ("dS", s)
+        for box in self.ds_box:
+            self.check(box is None or box[0] == "dS" or box[-1] == "read", "dS^T overwrote an unread dK/dV box")
+        self.t_sp, self.t_dp, self.ds_box = ("P", s), ("dS", s), [("dS", s), ("dS", s)]
         self.b[("PFull", 0)].arrive()
 
     def wg(self, half):
@@ -638,26 +639,34 @@ class BwdModel(Model):
                 self.b[("Staged", sg)].arrive()
                 s += 1
                 yield ("step",)
-            # warpgroup 0 writes dV out, warpgroup 1 dK, each staged in the dS region (warpgroup
-            # 1 after warpgroup 0's tile store has read it) and stored by TMA
+            # warpgroup 0 writes dV out, warpgroup 1 dK, each through its half (box) of the dS
+            # region, 64 columns per round: stage, then a TMA store whose read of the box
+            # completes later; the next round waits for it, and so (through the read barrier the
+            # storing warp must reach) does the next unit's dS^T
             yield from self.wait(("DKVFull", 0), u)
             self.check(self.dkv == (u, n), "dK/dV read out unfinished")
-            if half == 1:
-                yield from self.wait(("OutFree", 0), u)
-            elif u > 0 and self.out_free_wait:
-                yield from self.wait(("OutFree", 1), u - 1)
-            self.check(self.ds_smem is None or self.ds_smem[0] == "dS" or self.ds_smem[-1] == "read",
-                       "dK/dV staging overwrote an unread tile")
-            self.ds_smem = ("out", u, half)
-            yield ("step",)
-            self.dkv_read.add(half)
-            if self.dkv_read == {0, 1}:
-                self.dkv, self.dkv_read = None, set()
-            self.b[("DKVEmpty", 0)].arrive()
-            yield ("step",)
-            self.check(self.ds_smem == ("out", u, half), "dK/dV store read another tile")
-            self.ds_smem = ("out", u, half, "read")
-            self.b[("OutFree", half)].arrive()
+            for cc in range(self.rounds):
+                rnd = u * self.rounds + cc
+                if rnd > 0 and self.box_free_wait:
+                    yield from self.wait(("BoxFree", half), rnd - 1)
+                box = self.ds_box[half]
+                self.check(box is None or box[0] == "dS" or box[-1] == "read",
+                           "dK/dV staging overwrote an unread box")
+                self.ds_box[half] = ("out", u, half, cc)
+                yield ("step",)
+                if cc == self.rounds - 1:
+                    self.dkv_read.add(half)
+                    if self.dkv_read == {0, 1}:
+                        self.dkv, self.dkv_read = None, set()
+                    self.b[("DKVEmpty", 0)].arrive()
+
+                def read_done(half=half, u=u, cc=cc):
+                    self.check(self.ds_box[half] == ("out", u, half, cc), "dK/dV store read another box")
+                    self.ds_box[half] = ("out", u, half, cc, "read")
+                    self.b[("BoxFree", half)].arrive()
+                self.later(read_done, channel="tma_store%d" % half)
+                yield ("step",)
+            yield from self.wait(("BoxFree", half), (u + 1) * self.rounds - 1)
 
     def run(self, max_events=200000):
         roles = {"producer": self.producer(), "mma": self.mma(), "wg0": self.wg(0), "wg1": self.wg(1)}
@@ -706,13 +715,13 @@ def test_backward_planted_early_p_store_is_caught():
     assert found
 
 
-def test_backward_planted_early_dv_staging_is_caught():
-    # with a unit that has no steps, nothing but the store-read barrier keeps warpgroup 0's dV
-    # staging off warpgroup 1's previous dK tile
+def test_backward_planted_early_box_restage_is_caught():
+    # a warpgroup staging its next 64 columns of dV/dK before the previous box store has read
+    # its half of the dS region
     found = False
     for seed in range(400):
         try:
-            BwdModel([1, 0, 1], random.Random(seed), out_free_wait=False).run()
+            BwdModel([1, 0, 1], random.Random(seed), box_free_wait=False).run()
         except (Violation, Deadlock):
             found = True
             break
