@@ -68,6 +68,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--op", default="fwd", choices=["fwd", "bwd"],
                     help="bwd: time the attention backward (attn_bwd) instead of the forward")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="with --op bwd: the deterministic backward (dQ summed in key-tile order)")
     return ap.parse_args()
 
 
@@ -292,13 +294,14 @@ def run_backward(args, w):
     def call():
         nonlocal a_ws
         attn.attn_bwd(q, k, v, o, g, lse, layout=w.layout, causal=w.causal, dq=dq, dk=dk, dv=dv,
-                      workspace=a_ws)
+                      workspace=a_ws, deterministic=args.deterministic)
 
     # size the workspace once, outside the timed region
     import ctypes
     a = attn.BwdArgs()
     a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d = w.B, w.H, w.kv_heads, w.Sq, w.Skv, w.d
     a.layout, a.causal = attn.LAYOUTS[w.layout], int(w.causal)
+    a.deterministic = int(args.deterministic)
     a_ws = torch.empty(max(int(attn.load().attn_bwd_workspace_size(ctypes.byref(a))), 16),
                        dtype=torch.uint8, device=dev)
     for _ in range(warmup):
@@ -324,8 +327,12 @@ def run_backward(args, w):
         "data": "synthetic (seeded N(0,%g) bf16)" % w.sigma,
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.kv_heads, "Sq": w.Sq,
                    "Skv": w.Skv, "d": w.d, "causal": w.causal, "layout": w.layout,
-                   "step": "one attn_bwd call: D/LSE preprocessing with the dQ zeroing, the tcgen05 "
-                           "backward kernel, and the dQ rounding with any split units' dK/dV sums"},
+                   "deterministic": bool(args.deterministic),
+                   "step": ("one deterministic attn_bwd call: D/LSE preprocessing, the tcgen05 backward "
+                            "kernel storing each key tile's dQ terms, and the ordered dQ sum and rounding "
+                            "with any split units' dK/dV sums") if args.deterministic else
+                           ("one attn_bwd call: D/LSE preprocessing with the dQ zeroing, the tcgen05 "
+                            "backward kernel, and the dQ rounding with any split units' dK/dV sums")},
         "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
                      "frac": value / peak, "peak_source": peak_src + " burst bf16 (cuBLAS)",
                      "timed": "whole call"},

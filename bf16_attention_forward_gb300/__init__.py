@@ -49,7 +49,8 @@ class BwdArgs(ctypes.Structure):
     """attn_bwd_args_t: the argument set of attn_bwd."""
     _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv")] + \
                [(n, ctypes.c_int64) for n in ("B", "H", "Hkv", "Sq", "Skv", "d")] + \
-               [(n, ctypes.c_int32) for n in ("layout", "causal", "wait_limit_ms", "test_hooks")]
+               [(n, ctypes.c_int32) for n in ("layout", "causal", "wait_limit_ms", "test_hooks",
+                                              "deterministic", "reserved")]
 
 
 class Plan(ctypes.Structure):
@@ -310,12 +311,15 @@ def device_status(stream=None) -> tuple:
 
 
 def attn_bwd(q, k, v, o, dout, lse, layout: str = "bshd", causal: bool = False, dq=None, dk=None,
-             dv=None, workspace=None, stream=None, wait_limit_ms: int = 0, test_hooks: int = 0):
+             dv=None, workspace=None, stream=None, wait_limit_ms: int = 0, test_hooks: int = 0,
+             deterministic: bool = False):
     """Gradients (dq, dk, dv) of softmax(Q K^T / sqrt(d)) V for the upstream gradient ``dout``,
     from the forward's inputs, output ``o`` and fp32 row log-sum-exp ``lse`` ([B][H][Sq], as
     returned by :func:`attn_fwd_ex` with ``return_lse``).  d = 128 or 64.  ``wait_limit_ms``
     bounds each wait in the kernel (0: 2000 ms); ``test_hooks`` is 0 for normal use (1 makes a
-    bounded wait expire, to test that path).  Returns (dq, dk, dv)."""
+    bounded wait expire, to test that path).  ``deterministic``: dq bitwise reproducible too
+    (dk and dv always are), at the cost of one fp32 dQ-sized workspace slice per 128-key tile.
+    Returns (dq, dk, dv)."""
     import torch
     if layout not in LAYOUTS:
         raise ValueError("layout must be bshd or bhsd")
@@ -339,6 +343,7 @@ def attn_bwd(q, k, v, o, dout, lse, layout: str = "bshd", causal: bool = False, 
     a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d = B, H, Hkv, Sq, Skv, d
     a.layout, a.causal = LAYOUTS[layout], int(causal)
     a.wait_limit_ms, a.test_hooks = int(wait_limit_ms), int(test_hooks)
+    a.deterministic = int(bool(deterministic))
     lib = load()
     need = int(lib.attn_bwd_workspace_size(ctypes.byref(a)))
     if workspace is None:

@@ -25,11 +25,13 @@
 //                                  A operand; K_j as an MN-major B operand)
 //     dV and dK accumulate in TMEM for the whole unit and go out as TMA tile stores; dQ_i is
 //     added into an fp32 accumulator in global memory by TMA tensor reductions (many key
-//     tiles contribute).  Causal units (which shrink with their key tile) run on a paired
+//     tiles contribute, in no fixed order), or, in the deterministic mode, stored into an fp32
+//     slice of its own key tile.  Causal units (which shrink with their key tile) run on a paired
 //     schedule, and otherwise the units of a last, partial round run as query-range parts
 //     whose fp32 dK/dV partials are added at the end;
-//   * a last kernel rounds the dQ accumulator to bf16 (round to nearest even) and adds the
-//     split units' dK/dV partials in part order.
+//   * a last kernel rounds the dQ accumulator to bf16 (round to nearest even), or first adds
+//     each row's key-tile slices in key-tile order (deterministic mode), and adds the split
+//     units' dK/dV partials in part order.
 // Each kernel is a programmatic dependent of the one before it in the stream.
 // Roles: warp 8 TMA producer, warp 9 (one thread) MMA issuer; warpgroups 0 and 1 recompute P
 // and form dS for query columns 0..63 and 64..127 of each step, then each drains half of dQ's
@@ -126,7 +128,7 @@ struct BwdParams {
     float scale_log2;            // log2(e)/sqrt(d)
     const float* lse2;           // [B*H][nq_pad_rows] base-2 log-sum-exp
     const float* delta;          // [B*H][nq_pad_rows] D_i
-    float* dq_acc;               // [B][H][Sq][d] fp32
+    float* dq_acc;               // [B][H][Sq][d] fp32, or the deterministic mode's key-tile slices
     float* ws_dkv;               // [split items][2: dV, dK][128][d] fp32 partials
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
@@ -254,7 +256,9 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
 }
 
 
-template <int D>
+// kDet: the deterministic mode (dQ terms stored to per-key-tile slices, not added); a separate
+// instance, so the default one carries none of it.
+template <int D, bool kDet>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap domap,
@@ -437,8 +441,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         // fp32 accumulator with 8 * (D/64) TMA reductions (one 32 x 32 box per warp and 32
         // columns) just before it refills the stage, and waits for them to have read it.  Doing
         // this here rather than in the staging warps keeps the TMA unit's queue (a step's 64 KB
-        // of reductions) off their path.
-        int hist_it[kStages] = {0, 0}, hist_bh[kStages] = {0, 0};
+        // of reductions) off their path.  In the deterministic mode the same boxes are stored,
+        // not added, into the slice of the unit's key tile ([key tile][B*H][Sq][d]); each
+        // (key tile, query row) is written by one step only, and the final kernel adds the
+        // slices in key-tile order.
+        int hist_it[kStages] = {0, 0}, hist_bh[kStages] = {0, 0}, hist_jt[kStages] = {0, 0};
         // the preprocessing kernel's D, LSE and zeroed accumulator are waited for once, before
         // the first statistics load (every reduction comes after it), and in any case before
         // exit, so this grid's completion implies that kernel's
@@ -455,9 +462,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
 #pragma unroll
             for (int w = 0; w < 8; ++w)
 #pragma unroll
-                for (int cc = 0; cc < kHC / 32; ++cc)
-                    tma_reduce_add_3d(&dqmap, stage + (uint32_t)((w * (kHC / 32) + cc) * 4096), kHC * (w >> 2) + 32 * cc,
-                                      hist_it[tg] * kBM + 32 * (w & 3), hist_bh[tg]);
+                for (int cc = 0; cc < kHC / 32; ++cc) {
+                    const uint32_t src = stage + (uint32_t)((w * (kHC / 32) + cc) * 4096);
+                    const int x = kHC * (w >> 2) + 32 * cc, y = hist_it[tg] * kBM + 32 * (w & 3);
+                    if constexpr (kDet) ptx::tma_store_4d(&dqmap, src, x, y, hist_bh[tg], hist_jt[tg]);
+                    else tma_reduce_add_3d(&dqmap, src, x, y, hist_bh[tg]);
+                }
             ptx::bulk_commit();
             return true;
         };
@@ -488,6 +498,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             }
             hist_it[sg] = it;
             hist_bh[sg] = un.b * p.H + h;
+            hist_jt[sg] = un.jt;
             ++q_issued;
             return true;
         };
@@ -772,7 +783,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
 }
 
 // Preprocessing, one pass over O and dO: D_i = dO_i . O_i in fp32, the base-2 log-sum-exp,
-// and zeros into query row i of the fp32 dQ accumulator.  D / 8 lanes per padded query row,
+// and zeros into query row i of the fp32 dQ accumulator (when there is one: the deterministic
+// mode stores every slice row it reads and needs no zeros).  D / 8 lanes per padded query row,
 // 8 columns (16-byte loads) per lane, grid-stride over rows; padded rows (q >= Sq) get D_i = 0
 // and LSE 0 and have no accumulator row.  The row count is a multiple of 128, so every warp's
 // rows are all in range or all out and its shuffles see all 32 lanes.  This kernel is itself a
@@ -810,9 +822,11 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __nv_bfloat16*
                 acc = fmaf(of.x, gf.x, acc);
                 acc = fmaf(of.y, gf.y, acc);
             }
-            float4* z = reinterpret_cast<float4*>(dq_acc + (bh * Sq + q) * D + c);
-            z[0] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            z[1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (dq_acc) {
+                float4* z = reinterpret_cast<float4*>(dq_acc + (bh * Sq + q) * D + c);
+                z[0] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                z[1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
         }
 #pragma unroll
         for (int s = kL / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, s);
@@ -834,15 +848,26 @@ struct DkvCombine {
     float scale;
 };
 
+// The deterministic mode's dQ terms: nkv slices [key tile][B*H][Sq][d] of `slice` elements
+// each; key tile j holds a row's terms if the row sees a key of that tile (j * 128 <= q +
+// causal_off under the mask), and only those slices are read.  nkv = 0: a plain accumulator.
+struct DqSlices {
+    int nkv, causal, causal_off;
+    long long slice;
+};
+
 // The backward's last kernel.  Blocks [0, dq_blocks): dq (bf16, the caller's layout) = dq_acc
-// (fp32 [B][H][Sq][d]), round to nearest even, 8 columns per thread (two 16-byte loads, one
+// (fp32 [B][H][Sq][d]; in the deterministic mode the sum of the row's key-tile slices, added
+// in key-tile order from +0), round to nearest even, 8 columns per thread (16-byte loads, one
 // 16-byte store), grid-stride.  Blocks from dq_blocks on: the split units' dK/dV, one warp per
 // (unit, tensor, key row), D/32 columns per lane.  Launched as a programmatic dependent of the
-// main kernel: it waits for that kernel's memory first.
-template <int D>
+// main kernel: it waits for that kernel's memory first.  kDet: the deterministic mode's
+// instance (ds.nkv slices), kept apart so that the default one stays as lean as before.
+template <int D, bool kDet>
 __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const float* dq_acc, __nv_bfloat16* dq, int H, int Sq,
                                                           long long n8, long long o_sb, long long o_ss,
-                                                          long long o_sh, int dq_blocks, const DkvCombine cb) {
+                                                          long long o_sh, int dq_blocks, const DkvCombine cb,
+                                                          const DqSlices ds) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if ((int)blockIdx.x < dq_blocks) {
         for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
@@ -852,8 +877,44 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const float* dq_acc, _
             const int q = (int)(row % Sq);
             const long long bh = row / Sq;
             const int h = (int)(bh % H), b = (int)(bh / H);
-            const float4* src = reinterpret_cast<const float4*>(dq_acc + row * D + x);
-            const float4 v0 = src[0], v1 = src[1];
+            float4 v0, v1;
+            if constexpr (!kDet) {
+                const float4* src = reinterpret_cast<const float4*>(dq_acc + row * D + x);
+                v0 = src[0];
+                v1 = src[1];
+            } else {
+                // key tiles 0..n-1 hold this row's terms
+                long long last = ds.nkv - 1;
+                if (ds.causal) {
+                    const long long lim = (long long)q + ds.causal_off;
+                    last = lim < 0 ? -1 : (lim / kBN < last ? lim / kBN : last);
+                }
+                v0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                v1 = v0;
+                const float* src = dq_acc + row * D + x;
+                long long j = 0;
+                // four slices' loads in flight, then their adds in order
+                for (; j + 3 <= last; j += 4) {
+                    float4 t[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4* s4 = reinterpret_cast<const float4*>(src + (j + e) * ds.slice);
+                        t[2 * e] = s4[0];
+                        t[2 * e + 1] = s4[1];
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        v0.x += t[2 * e].x; v0.y += t[2 * e].y; v0.z += t[2 * e].z; v0.w += t[2 * e].w;
+                        v1.x += t[2 * e + 1].x; v1.y += t[2 * e + 1].y; v1.z += t[2 * e + 1].z; v1.w += t[2 * e + 1].w;
+                    }
+                }
+                for (; j <= last; ++j) {
+                    const float4* s4 = reinterpret_cast<const float4*>(src + j * ds.slice);
+                    const float4 a = s4[0], c = s4[1];
+                    v0.x += a.x; v0.y += a.y; v0.z += a.z; v0.w += a.w;
+                    v1.x += c.x; v1.y += c.y; v1.z += c.z; v1.w += c.w;
+                }
+            }
             __nv_bfloat16* dst = dq + (long long)b * o_sb + (long long)q * o_ss + (long long)h * o_sh + x;
             *reinterpret_cast<uint4*>(dst) = make_uint4(pack2(v0.x, v0.y), pack2(v0.z, v0.w), pack2(v1.x, v1.y),
                                                         pack2(v1.z, v1.w));
@@ -907,6 +968,17 @@ bool encode_dq(CUtensorMap* m, float* ptr, int64_t BH, int64_t Sq, int64_t d) {
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The deterministic mode's dQ slices [nkv][B*H][Sq][d] fp32 for TMA tile stores: the same
+// 32 x 32 boxes and swizzle, one more coordinate for the key tile.
+bool encode_dq_slices(CUtensorMap* m, float* ptr, int64_t nkv, int64_t BH, int64_t Sq, int64_t d) {
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)Sq, (cuuint64_t)BH, (cuuint64_t)nkv};
+    cuuint64_t strides[3] = {(cuuint64_t)(d * 4), (cuuint64_t)(Sq * d * 4), (cuuint64_t)(BH * Sq * d * 4)};
+    cuuint32_t box[4] = {32, 32, 1, 1}, estr[4] = {1, 1, 1, 1};
+    return g_bwd_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode(CUtensorMap* m, const void* ptr, int64_t B, int64_t H, int64_t S, int64_t d, bool bshd) {
     cuuint64_t dims[4], strides[3];
     cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
@@ -931,6 +1003,7 @@ int check_shape(const attn_bwd_args_t& a) {
     if (a.layout != ATTN_LAYOUT_BSHD && a.layout != ATTN_LAYOUT_BHSD) return ATTN_ERR_INVALID_ARG;
     if ((a.causal != 0 && a.causal != 1) || a.wait_limit_ms < 0) return ATTN_ERR_INVALID_ARG;
     if (a.test_hooks != 0 && a.test_hooks != ATTN_TEST_WITHHOLD_O_READY) return ATTN_ERR_INVALID_ARG;
+    if (a.deterministic != 0 && a.deterministic != 1) return ATTN_ERR_INVALID_ARG;
     if (a.d != 128 && a.d != 64) return ATTN_ERR_UNSUPPORTED;
     const int64_t lim = (int64_t)1 << 30;
     if (a.Sq > lim || a.Skv > lim || a.B * a.H > lim || a.B * a.Hkv * cdiv(a.Skv, kBN) > lim ||
@@ -939,9 +1012,14 @@ int check_shape(const attn_bwd_args_t& a) {
     return ATTN_OK;
 }
 
+// dQ elements held in the workspace: the accumulator, or one slice per key tile
+int64_t dq_elems(const attn_bwd_args_t& a) {
+    return (a.deterministic ? cdiv(a.Skv, kBN) : 1) * a.B * a.H * a.Sq * a.d;
+}
+
 size_t ws_bytes(const attn_bwd_args_t& a) {
     const int64_t rows_pad = a.B * a.H * cdiv(a.Sq, kBM) * kBM;
-    return (size_t)(a.B * a.H * a.Sq * a.d * 4) + (size_t)(2 * rows_pad * 4);
+    return (size_t)dq_elems(a) * 4u + (size_t)(2 * rows_pad * 4);
 }
 
 // Query-range split of the units of the last, partial round (none for causal launches, whose
@@ -1046,9 +1124,13 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
             g_bwd_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
         }
         if (!g_bwd_attr[dev]) {
-            if (cudaFuncSetAttribute(attn_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(attn_bwd_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      smem_alloc<128>()) != cudaSuccess ||
-                cudaFuncSetAttribute(attn_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                cudaFuncSetAttribute(attn_bwd_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     smem_alloc<64>()) != cudaSuccess ||
+                cudaFuncSetAttribute(attn_bwd_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     smem_alloc<128>()) != cudaSuccess ||
+                cudaFuncSetAttribute(attn_bwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      smem_alloc<64>()) != cudaSuccess)
                 return ATTN_ERR_CUDA;
             g_bwd_attr[dev] = true;
@@ -1079,14 +1161,16 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     p.scale = (float)(1.0 / std::sqrt((double)d));
     p.scale_log2 = (float)((1.0 / std::sqrt((double)d)) * 1.4426950408889634);
     float* dq_acc = reinterpret_cast<float*>(workspace);
-    float* lse2 = dq_acc + a.B * a.H * a.Sq * d;
+    float* lse2 = dq_acc + dq_elems(a);
     float* delta = lse2 + a.B * a.H * p.nq_pad_rows;
     p.ws_dkv = delta + a.B * a.H * p.nq_pad_rows;      // split partials (16-byte aligned)
     p.lse2 = lse2;
     p.delta = delta;
     p.dq_acc = dq_acc;
     CUtensorMap dqm, dkm, dvm;
-    if (!encode_dq(&dqm, dq_acc, a.B * a.H, a.Sq, d) || !encode(&dkm, a.dk, a.B, a.Hkv, a.Skv, d, bshd) ||
+    const bool dq_ok = a.deterministic ? encode_dq_slices(&dqm, dq_acc, p.nkv, a.B * a.H, a.Sq, d)
+                                       : encode_dq(&dqm, dq_acc, a.B * a.H, a.Sq, d);
+    if (!dq_ok || !encode(&dkm, a.dk, a.B, a.Hkv, a.Skv, d, bshd) ||
         !encode(&dvm, a.dv, a.B, a.Hkv, a.Skv, d, bshd))
         return ATTN_ERR_CUDA;
     p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
@@ -1102,7 +1186,7 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     p.wait_limit_ns = (unsigned long long)(a.wait_limit_ms > 0 ? a.wait_limit_ms : 2000) * 1000000ull;
     p.test_hooks = a.test_hooks;
 
-    // preprocessing (also zeroes the dQ accumulator) -> main kernel -> dQ rounding, each a
+    // preprocessing (also zeroes the dQ accumulator, if any) -> main kernel -> dQ rounding, each a
     // programmatic dependent of the kernel before it in the stream
     const long long prows = a.B * a.H * (long long)p.nq_pad_rows;
     const long long fill = (long long)sms * 8;             // resident 256-thread blocks
@@ -1119,7 +1203,8 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     pc.attrs = attr;
     pc.numAttrs = 1;
     if (cudaLaunchKernelEx(&pc, prep, reinterpret_cast<const __nv_bfloat16*>(a.o),
-                           reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, lse2, delta, dq_acc, p.H, p.Sq,
+                           reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, lse2, delta,
+                           a.deterministic ? nullptr : dq_acc, p.H, p.Sq,
                            p.nq_pad_rows, prows, q_sb, q_ss, q_sh) != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_CUDA;
@@ -1132,8 +1217,9 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t ce = d == 128 ? cudaLaunchKernelEx(&cfg, attn_bwd_kernel<128>, qm, km, vm, dom, dqm, dkm, dvm, p)
-                              : cudaLaunchKernelEx(&cfg, attn_bwd_kernel<64>, qm, km, vm, dom, dqm, dkm, dvm, p);
+    auto kern = d == 128 ? (a.deterministic ? attn_bwd_kernel<128, true> : attn_bwd_kernel<128, false>)
+                         : (a.deterministic ? attn_bwd_kernel<64, true> : attn_bwd_kernel<64, false>);
+    cudaError_t ce = cudaLaunchKernelEx(&cfg, kern, qm, km, vm, dom, dqm, dkm, dvm, p);
     if (ce != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_CUDA;
@@ -1157,14 +1243,18 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
     cb.kv_sh = p.kv_sh;
     cb.scale = p.scale;
     const long long comb_blocks = sp.T * 2 * kBN / 8;   // one warp per (unit, tensor, key row)
+    DqSlices ds;
+    ds.nkv = a.deterministic ? p.nkv : 0;
+    ds.causal = p.causal;
+    ds.causal_off = p.causal_off;
+    ds.slice = a.B * a.H * a.Sq * d;
     cfg.gridDim = dim3((unsigned)(dq_blocks + comb_blocks));
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     __nv_bfloat16* dqo = reinterpret_cast<__nv_bfloat16*>(a.dq);
-    ce = d == 128 ? cudaLaunchKernelEx(&cfg, attn_bwd_dq_kernel<128>, (const float*)dq_acc, dqo, p.H, p.Sq, n8, q_sb,
-                                       q_ss, q_sh, dq_blocks, cb)
-                  : cudaLaunchKernelEx(&cfg, attn_bwd_dq_kernel<64>, (const float*)dq_acc, dqo, p.H, p.Sq, n8, q_sb,
-                                       q_ss, q_sh, dq_blocks, cb);
+    auto fin = d == 128 ? (a.deterministic ? attn_bwd_dq_kernel<128, true> : attn_bwd_dq_kernel<128, false>)
+                        : (a.deterministic ? attn_bwd_dq_kernel<64, true> : attn_bwd_dq_kernel<64, false>);
+    ce = cudaLaunchKernelEx(&cfg, fin, (const float*)dq_acc, dqo, p.H, p.Sq, n8, q_sb, q_ss, q_sh, dq_blocks, cb, ds);
     if (ce != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_CUDA;

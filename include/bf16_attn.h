@@ -243,9 +243,14 @@ int attn_version(void);
  *   lse          the forward's fp32 [B][H][Sq] natural-log log-sum-exp (attn_fwd_ex's lse)
  *   dq, dk, dv   outputs, bf16, like q, k, v (round to nearest even); must not overlap the
  *                inputs, each other or the workspace.  dk and dv are bitwise reproducible;
- *                the last bits of dq can differ between runs (its fp32 accumulator takes one
- *                addition per key tile, in no fixed order)
+ *                with deterministic = 0 the last bits of dq can differ between runs (its
+ *                fp32 accumulator takes one addition per key tile, in no fixed order)
  *   causal       0 or 1, as in the forward
+ *   deterministic  0 or 1.  1: dq is bitwise reproducible too.  Each key tile's dQ terms go
+ *                to an fp32 slice of their own in the workspace and a final pass adds a row's
+ *                slices in key-tile order, so the workspace holds ceil(Skv/128) dQ-sized fp32
+ *                slices instead of one accumulator, and the call moves that much more memory
+ *   reserved     0
  *   wait_limit_ms  0: 2000 ms; otherwise the bound, in ms, on any single wait in the kernel
  *   test_hooks   0 for normal use; ATTN_TEST_WITHHOLD_O_READY makes the first CTA skip the
  *                signal that its first unit's dK/dV accumulators are complete, so that the
@@ -267,10 +272,11 @@ typedef struct {
     void* dv;
     int64_t B, H, Hkv, Sq, Skv, d;
     int32_t layout, causal, wait_limit_ms, test_hooks;
+    int32_t deterministic, reserved;
 } attn_bwd_args_t;
 
-/* Workspace bytes attn_bwd needs (0 if invalid): the fp32 dQ accumulator and per-row
- * statistics, plus fp32 dK/dV partials when the last, partial round of work units is split by
+/* Workspace bytes attn_bwd needs (0 if invalid): the fp32 dQ accumulator (deterministic: one
+ * fp32 dQ slice per 128-key tile) and per-row statistics, plus fp32 dK/dV partials when the last, partial round of work units is split by
  * query range.  That split depends on the current device's SM count; attn_bwd given a
  * workspace sized without the partials runs unsplit (same results up to rounding). */
 size_t attn_bwd_workspace_size(const attn_bwd_args_t* args);

@@ -195,11 +195,27 @@ def test_test_hooks_and_bwd_wait_limit_are_validated(lib):
         setattr(a, n, (i + 1) * P)
     a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d = 1, 1, 1, 8, 8, 128
     ws = 16 * P
-    for bad in ({"wait_limit_ms": -1}, {"test_hooks": 2}, {"test_hooks": -1}):
-        a.wait_limit_ms, a.test_hooks = 0, 0
+    for bad in ({"wait_limit_ms": -1}, {"test_hooks": 2}, {"test_hooks": -1}, {"deterministic": 2},
+                {"deterministic": -1}):
+        a.wait_limit_ms, a.test_hooks, a.deterministic = 0, 0, 0
         for k_, v_ in bad.items():
             setattr(a, k_, v_)
         assert lib.attn_bwd(ctypes.byref(a), ws, 1 << 20, None) == 1, bad
         assert lib.attn_bwd_workspace_size(ctypes.byref(a)) == 0, bad
-    a.wait_limit_ms, a.test_hooks = 50, 1
+    a.wait_limit_ms, a.test_hooks, a.deterministic = 50, 1, 1
     assert lib.attn_bwd_workspace_size(ctypes.byref(a)) > 0
+
+
+def test_bwd_workspace_size_deterministic(lib):
+    """The deterministic backward holds one fp32 dQ slice per 128-key tile where the default
+    mode holds one accumulator; the per-row statistics are the same.  (No device here, so no
+    tail split and no dK/dV partials.)"""
+    a = attn.BwdArgs()
+    a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d = 2, 4, 2, 300, 700, 128
+    rows_pad = 2 * 4 * 384
+    dq = 2 * 4 * 300 * 128 * 4
+    assert lib.attn_bwd_workspace_size(ctypes.byref(a)) == dq + 2 * rows_pad * 4
+    a.deterministic = 1
+    assert lib.attn_bwd_workspace_size(ctypes.byref(a)) == 6 * dq + 2 * rows_pad * 4
+    a.Skv, a.d = 128, 64
+    assert lib.attn_bwd_workspace_size(ctypes.byref(a)) == dq // 2 + 2 * rows_pad * 4

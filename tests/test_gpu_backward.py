@@ -7,9 +7,11 @@ of dQ, dK or dV passes when |gpu - oracle| <= 2^-7 * A + ulp(oracle), with A the
 sum of term magnitudes (dV: sum_i p |dO|; dQ, dK: c sum p (|dP| + |D|) |k| or |q|, where
 |D| = sum |dO| |O| also covers D formed from the rounded O).  2^-7 is four times bf16's unit
 roundoff: P (or dS) rounding, the rounding of O inside D, and the final bf16 store.  The
-oracle itself is pinned against numerical differentiation of the forward.  dQ is summed with
-reductions in L2 across key tiles in no fixed order, so its last bits may differ between runs; dK and dV are
-accumulated in a fixed order and are bitwise reproducible.
+oracle itself is pinned against numerical differentiation of the forward.  By default dQ is
+summed with reductions in L2 across key tiles in no fixed order, so its last bits may differ
+between runs; in the deterministic mode each key tile's terms are stored to a slice of their
+own and added in key-tile order.  dK and dV are accumulated in a fixed order and are bitwise
+reproducible in both modes.
 """
 import numpy as np
 import pytest
@@ -35,10 +37,11 @@ def _bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def run_bwd(attn, q, k, v, g, layout, causal):
+def run_bwd(attn, q, k, v, g, layout, causal, deterministic=False):
     qd, kd, vd, gd = (t.cuda() for t in (q, k, v, g))
     o, lse = attn.attn_fwd_ex(qd, kd, vd, layout=layout, causal=causal, return_lse=True)
-    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, gd, lse, layout=layout, causal=causal)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, gd, lse, layout=layout, causal=causal,
+                               deterministic=deterministic)
     torch.cuda.synchronize()
     assert attn.device_status()[0] == 0
     st, site = attn.bwd_device_status()
@@ -46,8 +49,8 @@ def run_bwd(attn, q, k, v, g, layout, causal):
     return dq, dk, dv
 
 
-def check_bwd(attn, q, k, v, g, layout, causal=False):
-    dq, dk, dv = run_bwd(attn, q, k, v, g, layout, causal)
+def check_bwd(attn, q, k, v, g, layout, causal=False, deterministic=False):
+    dq, dk, dv = run_bwd(attn, q, k, v, g, layout, causal, deterministic)
     ref = oracle.backward(q, k, v, g, layout, causal=causal, want_a=True)
     worst = {}
     for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
@@ -178,3 +181,28 @@ def test_backward_split_tail_units(attn, shape):
     _, (dq2, dk2, dv2) = check_bwd(attn, q, k, v, g, layout)
     assert torch.equal(dk.view(torch.int16), dk2.view(torch.int16))
     assert torch.equal(dv.view(torch.int16), dv2.view(torch.int16))
+
+
+DET = [  # (B, H, Hkv, Sq, Skv, d, layout, causal)
+    (1, 2, 2, 300, 200, 128, "bshd", False),
+    (2, 4, 2, 257, 640, 128, "bhsd", False),
+    (1, 4, 2, 456, 200, 128, "bshd", True),     # Sq > Skv: rows that see no key
+    (1, 4, 4, 300, 777, 64, "bhsd", True),
+    (1, 5, 5, 1024, 1024, 128, "bshd", False),  # split tail units
+    (1, 3, 3, 1000, 700, 64, "bhsd", False),
+]
+
+
+@pytest.mark.parametrize("case", DET, ids=lambda c: "B%dH%dHkv%dSq%dSkv%dd%d%s" % c[:7] + ("c" if c[7] else ""))
+def test_backward_deterministic_dq(attn, case):
+    # the deterministic mode meets the same criteria, its dQ is bit-for-bit the same on a
+    # second call, and its dK and dV are those of the default mode (the same path)
+    B, H, Hkv, Sq, Skv, d, layout, causal = case
+    q, k, v = make_qkv(B, H, Sq, Skv, d, layout, seed=6300 + Sq + Skv, Hkv=Hkv)
+    g = make_qkv(B, H, Sq, 1, d, layout, seed=6350 + Sq)[0]
+    _, (dq, dk, dv) = check_bwd(attn, q, k, v, g, layout, causal=causal, deterministic=True)
+    dq2, dk2, dv2 = run_bwd(attn, q, k, v, g, layout, causal, deterministic=True)
+    assert torch.equal(dq.view(torch.int16), dq2.view(torch.int16)), "deterministic dQ changed between calls"
+    _, dk0, dv0 = run_bwd(attn, q, k, v, g, layout, causal)
+    assert torch.equal(dk.view(torch.int16), dk0.view(torch.int16))
+    assert torch.equal(dv.view(torch.int16), dv0.view(torch.int16))

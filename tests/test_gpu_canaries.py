@@ -92,8 +92,9 @@ BWD = [  # (B, H, Hkv, Sq, Skv, d, layout, causal)
 ]
 
 
+@pytest.mark.parametrize("det", [False, True], ids=["acc", "det"])
 @pytest.mark.parametrize("case", BWD, ids=lambda c: "B%dH%dHkv%dSq%dSkv%dd%d_%s%s" % (c[:6] + (c[6], "_causal" if c[7] else "")))
-def test_backward_writes_stay_in_bounds(attn, case):
+def test_backward_writes_stay_in_bounds(attn, case, det):
     B, H, Hkv, Sq, Skv, d, layout, causal = case
     q, k, v = (t.cuda() for t in make_qkv(B, H, Sq, Skv, d, layout, seed=7100 + Sq, Hkv=Hkv))
     g = make_qkv(B, H, Sq, 1, d, layout, seed=7200 + Sq)[0].cuda()
@@ -105,11 +106,12 @@ def test_backward_writes_stay_in_bounds(attn, case):
     a = attn.BwdArgs()
     a.B, a.H, a.Hkv, a.Sq, a.Skv, a.d = B, H, Hkv, Sq, Skv, d
     a.layout, a.causal, a.wait_limit_ms, a.test_hooks = attn.LAYOUTS[layout], int(causal), 0, 0
+    a.deterministic = int(det)
     need = int(attn.load().attn_bwd_workspace_size(ctypes.byref(a)))
     assert need > 0
     wbuf, ws = guarded(need, "ws")
     attn.attn_bwd(q, k, v, o, g, lse, layout=layout, causal=causal, dq=outs[0][1], dk=outs[1][1],
-                  dv=outs[2][1], workspace=ws)
+                  dv=outs[2][1], workspace=ws, deterministic=det)
     torch.cuda.synchronize()
     assert attn.bwd_device_status()[0] == 0
     for name, (buf, view) in zip(("dQ", "dK", "dV"), outs):

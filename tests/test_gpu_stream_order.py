@@ -6,8 +6,9 @@ reads or writes global memory.  The attention kernel lets its dependents launch 
 its CTAs start, so the next call's kernels really do run early.  These tests chain calls
 back to back on one stream, each reading what the previous one wrote (as Q, K, V, O, dO or the
 LSE), with no synchronisation in between, and then check every output bit for bit against
-the same call re-run once its inputs have settled.  The forward, and the backward's dK and
-dV, are deterministic, so any read of a stale or half-written input shows up as a mismatch.
+the same call re-run once its inputs have settled.  The forward, the backward's dK and dV, and
+the deterministic backward's dQ are reproducible bit for bit, so any read of a stale or
+half-written input shows up as a mismatch.
 """
 import pytest
 import torch
@@ -80,8 +81,9 @@ def test_forward_writes_do_not_overtake_readers(attn):
     assert torch.equal(bits(buf), bits(want_second))
 
 
+@pytest.mark.parametrize("det", [False, True], ids=["acc", "det"])
 @pytest.mark.parametrize("d", [128, 64])
-def test_backward_between_forward_calls(attn, d):
+def test_backward_between_forward_calls(attn, d, det):
     # forward -> backward (its O, LSE and dO come from the forward calls just before) ->
     # forward on the backward's dK (as Q) and dQ (as V)
     B, H, S, layout = 1, 4, 640, "bshd"
@@ -89,7 +91,7 @@ def test_backward_between_forward_calls(attn, d):
     q2 = make_qkv(B, H, S, S, d, layout, seed=4400 + d)[0].cuda()
     o, lse = attn.attn_fwd_ex(q, k, v, layout=layout, return_lse=True)
     g = attn.attn_fwd(q2, k, v, layout=layout)
-    dq, dk, dv = attn.attn_bwd(q, k, v, o, g, lse, layout=layout)
+    dq, dk, dv = attn.attn_bwd(q, k, v, o, g, lse, layout=layout, deterministic=det)
     o3 = attn.attn_fwd(dk, k, v, layout=layout)
     o4 = attn.attn_fwd(q, k, dq, layout=layout)
     check_status(attn)
@@ -99,9 +101,11 @@ def test_backward_between_forward_calls(attn, d):
     torch.cuda.synchronize()
     assert torch.equal(bits(o), bits(o_ref)) and torch.equal(bits(g), bits(g_ref))
     assert torch.equal(lse.view(torch.int32), lse_ref.view(torch.int32))
-    _, dk_ref, dv_ref = attn.attn_bwd(q, k, v, o, g, lse, layout=layout)
+    dq_ref, dk_ref, dv_ref = attn.attn_bwd(q, k, v, o, g, lse, layout=layout, deterministic=det)
     torch.cuda.synchronize()
     assert torch.equal(bits(dk), bits(dk_ref)) and torch.equal(bits(dv), bits(dv_ref))
+    if det:
+        assert torch.equal(bits(dq), bits(dq_ref)), "deterministic dQ read an unsettled input"
     o3_ref = attn.attn_fwd(dk, k, v, layout=layout)
     o4_ref = attn.attn_fwd(q, k, dq, layout=layout)
     torch.cuda.synchronize()
