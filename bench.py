@@ -31,6 +31,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import itertools
 import json
 import os
 import statistics
@@ -66,8 +67,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", default="fwd", choices=["fwd", "bwd"],
-                    help="bwd: time the attention backward (attn_bwd) instead of the forward")
+    ap.add_argument("--op", default="fwd", choices=["fwd", "bwd", "varlen"],
+                    help="bwd: time the attention backward (attn_bwd) instead of the forward; "
+                         "varlen: the forward on a variable-length causal GQA prefill batch")
     ap.add_argument("--deterministic", action="store_true",
                     help="with --op bwd: the deterministic backward (dQ summed in key-tile order)")
     return ap.parse_args()
@@ -343,6 +345,77 @@ def run_backward(args, w):
     return 0
 
 
+# A variable-length prefill batch: 16 sequences with seeded lengths in [256, 8192], 32 query
+# heads on 8 K/V heads, d = 128, causal, packed along the token axis (attn_fwd_varlen).
+VARLEN_SEQS, VARLEN_H, VARLEN_HKV, VARLEN_D, VARLEN_SEED = 16, 32, 8, 128, 9
+
+
+def varlen_lengths():
+    import numpy as np
+    return np.random.default_rng(VARLEN_SEED).integers(256, 8193, VARLEN_SEQS).tolist()
+
+
+def run_varlen(args):
+    """Time attn_fwd_varlen on resident inputs.  FLOP per call: 4*d per visible (query, key)
+    pair and head, summed over the sequences (the causal mask's hidden half not counted)."""
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    dev = torch.device("cuda", 0)
+    import bf16_attention_forward_gb300 as attn
+    attn.load()
+    steps = args.steps if args.steps is not None else 50
+    warmup = max(3, args.warmup if args.warmup is not None else 10)
+    lens = varlen_lengths()
+    total = sum(lens)
+    q, k, v = (t[0].to(dev) for t in make_qkv(1, VARLEN_H, total, total, VARLEN_D, "bshd", seed=VARLEN_SEED,
+                                               Hkv=VARLEN_HKV))
+    cu = torch.tensor([0] + list(itertools.accumulate(lens)), dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    import ctypes
+    a = attn.VarlenArgs()
+    a.B, a.H, a.Hkv, a.total_q, a.total_k, a.d = len(lens), VARLEN_H, VARLEN_HKV, total, total, VARLEN_D
+    ws = torch.empty(int(attn.load().attn_fwd_varlen_workspace_size(ctypes.byref(a))), dtype=torch.uint8, device=dev)
+
+    def call():
+        attn.attn_fwd_varlen(q, k, v, cu, cu, max_seqlen_q=max(lens), o=o, causal=True, workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0, enabled=not args.no_clocks) as clocks:
+        t0.record()
+        for _ in range(steps):
+            call()
+        t1.record()
+        torch.cuda.synchronize(dev)
+    st, site = attn.device_status()
+    assert st == 0, "device status %d at site %d" % (st, site)
+    ms = t0.elapsed_time(t1) / steps
+    pairs = sum(n * (n + 1) // 2 for n in lens)
+    flop = 4 * VARLEN_H * VARLEN_D * pairs
+    value = flop / (ms * 1e-3) / 1e12
+    peak, _, _, peak_src = measured_peaks()
+    line = {
+        "metric": "attention fwd TFLOPS (4*d per visible pair and head, variable-length batch)",
+        "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": steps, "warmup": warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": "varlen_prefill", "sequences": len(lens), "lengths": lens,
+                   "total_tokens": total, "H": VARLEN_H, "Hkv": VARLEN_HKV, "d": VARLEN_D, "causal": True,
+                   "layout": "packed tokens [T, H, d]", "modes": ["rtne"], "flop_per_call": flop,
+                   "step": "one attn_fwd_varlen call: the offsets/tensor-map preprocessing kernel and "
+                           "the attention kernel",
+                   "l2": "inputs %.0f MB > 126 MB L2" % ((q.numel() + k.numel() + v.numel()) * 2 / 2**20)},
+        "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
+                     "frac": value / peak, "peak_source": peak_src + " burst bf16 (cuBLAS)",
+                     "timed": "whole call"},
+        "clocks": clocks.summary(),
+        "gpu_launches": 2 * steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -351,6 +424,8 @@ def main():
         return run_reference(args, w, rank, world)
     if args.op == "bwd":
         return run_backward(args, w)
+    if args.op == "varlen":
+        return run_varlen(args)
 
     import torch.distributed as dist
     if world > 1:

@@ -21,7 +21,8 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
 EXPORTS = ("attn_fwd", "attn_fwd_ws", "attn_fwd_noalloc", "attn_fwd_ex", "attn_fwd_workspace_size",
            "attn_fwd_workspace_size_opts", "attn_fwd_ex_workspace_size", "attn_plan",
            "attn_plan_ex", "attn_get_device_status", "attn_status_string", "attn_version",
-           "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_get_device_status")
+           "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_get_device_status",
+           "attn_fwd_varlen", "attn_fwd_varlen_workspace_size")
 
 
 class AttnError(RuntimeError):
@@ -51,6 +52,15 @@ class BwdArgs(ctypes.Structure):
                [(n, ctypes.c_int64) for n in ("B", "H", "Hkv", "Sq", "Skv", "d")] + \
                [(n, ctypes.c_int32) for n in ("layout", "causal", "wait_limit_ms", "test_hooks",
                                               "deterministic", "reserved")]
+
+
+class VarlenArgs(ctypes.Structure):
+    """attn_varlen_args_t: the argument set of attn_fwd_varlen."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "o", "lse", "cu_seqlens_q",
+                                               "cu_seqlens_k")] + \
+               [(n, ctypes.c_int64) for n in ("B", "H", "Hkv", "total_q", "total_k",
+                                              "max_seqlen_q", "d")] + \
+               [(n, ctypes.c_int32) for n in ("round_mode", "causal", "reserved", "reserved2")]
 
 
 class Plan(ctypes.Structure):
@@ -106,6 +116,11 @@ def load(path: str | None = None):
         lib.attn_bwd_workspace_size.argtypes = [ctypes.POINTER(BwdArgs)]
         lib.attn_bwd_get_device_status.restype = i32
         lib.attn_bwd_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+        lib.attn_fwd_varlen.restype = i32
+        lib.attn_fwd_varlen.argtypes = [ctypes.POINTER(VarlenArgs), ctypes.POINTER(Options), vp,
+                                        ctypes.c_size_t, vp]
+        lib.attn_fwd_varlen_workspace_size.restype = ctypes.c_size_t
+        lib.attn_fwd_varlen_workspace_size.argtypes = [ctypes.POINTER(VarlenArgs)]
         lib.attn_plan.restype = i32
         lib.attn_plan.argtypes = [i64] * 6 + [ctypes.POINTER(Options), ctypes.POINTER(Plan)]
         lib.attn_get_device_status.restype = i32
@@ -288,6 +303,66 @@ def attn_fwd_ex(q, k, v, o=None, lse=None, layout: str = "bshd", round: str = "r
                          _stream_ptr(stream, q.device))
     if st != 0:
         raise AttnError(st, "attn_fwd_ex")
+    return (o, lse) if (return_lse or lse is not None) else o
+
+
+def _varlen_args(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, round, causal):
+    import torch
+    _check_tensors(q, k, v)
+    if q.dim() != 3 or k.dim() != 3 or tuple(k.shape) != tuple(v.shape) or q.shape[2] != k.shape[2]:
+        raise ValueError("q must be [total_q, H, d] and k, v [total_k, Hkv, d]")
+    H, Hkv, d = q.shape[1], k.shape[1], q.shape[2]
+    for c in (cu_seqlens_q, cu_seqlens_k):
+        if (not isinstance(c, torch.Tensor) or c.dtype != torch.int32 or not c.is_cuda
+                or not c.is_contiguous() or c.dim() != 1):
+            raise ValueError("cu_seqlens_q and cu_seqlens_k must be contiguous CUDA int32 vectors")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold B + 1 >= 2 offsets")
+    a = VarlenArgs()
+    a.q, a.k, a.v, a.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
+    a.lse = None if lse is None else lse.data_ptr()
+    a.cu_seqlens_q, a.cu_seqlens_k = cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr()
+    a.B, a.H, a.Hkv = cu_seqlens_q.numel() - 1, H, Hkv
+    a.total_q, a.total_k, a.max_seqlen_q, a.d = q.shape[0], k.shape[0], int(max_seqlen_q), d
+    a.round_mode, a.causal = MODES[round], int(causal)
+    return a
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int = 0, o=None, lse=None,
+                    round: str = "rtne", causal: bool = False, return_lse: bool = False,
+                    stream=None, workspace=None, max_ctas: int = 0, wait_limit_ms: int = 0,
+                    events=None):
+    """Attention over a variable-length batch packed along the token axis.
+
+    ``q``: [total_q, H, d], ``k``/``v``: [total_k, Hkv, d] (CUDA bf16, contiguous);
+    ``cu_seqlens_q``/``cu_seqlens_k``: CUDA int32 [B + 1] row offsets of each sequence's
+    queries and keys (checked on the device: bad offsets write nothing and are reported by
+    :func:`device_status` as ATTN_ERR_INVALID_ARG).  Every sequence attends only to its own
+    keys, with the causal mask (if asked) aligned at its own last query and key.
+    ``max_seqlen_q``: an upper bound on any sequence's query length, used to size the grid
+    (0: unknown).  ``lse``: optional fp32 [H, total_q].  Returns ``o`` or ``(o, lse)``.
+    """
+    import torch
+    if round not in MODES:
+        raise ValueError("round must be rtne/rtna/rtz")
+    if o is None:
+        o = torch.empty_like(q)
+    _check_out(o, q)
+    if lse is None and return_lse:
+        lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous()
+                            or lse.numel() != q.shape[0] * q.shape[1]):
+        raise ValueError("lse must be a contiguous CUDA fp32 tensor of H*total_q elements")
+    a = _varlen_args(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, round, causal)
+    opts = _opts(0, max_ctas, wait_limit_ms, events)
+    lib = load()
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = lib.attn_fwd_varlen(ctypes.byref(a), ctypes.byref(opts) if opts else None, ws_ptr,
+                             ws_bytes, _stream_ptr(stream, q.device))
+    if st != 0:
+        raise AttnError(st, "attn_fwd_varlen")
     return (o, lse) if (return_lse or lse is not None) else o
 
 

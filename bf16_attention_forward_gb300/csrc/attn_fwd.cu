@@ -106,9 +106,10 @@ struct Geo {
 // wait sites reported through the status word
 enum : uint32_t {
     kSiteQEmpty = 1, kSiteRingEmpty, kSiteQFull, kSiteRingFull, kSitePFull, kSiteSFull,
-    kSiteOFull, kSiteDrain, kSiteTeardown, kSitePVDone, kSiteOEmpty, kSiteStats
+    kSiteOFull, kSiteDrain, kSiteTeardown, kSitePVDone, kSiteOEmpty, kSiteStats, kSiteSeqlens
 };
 static_assert(kSiteOFull == ATTN_SITE_O_READY, "the O-ready wait site is part of the ABI");
+static_assert(kSiteSeqlens == ATTN_SITE_SEQLENS, "the sequence-length check site is part of the ABI");
 
 __device__ uint32_t g_status[2];   // [0] status code, [1] wait site
 
@@ -131,10 +132,20 @@ struct FwdParams {
     float* lse;            // optional [B][H][Sq] natural-log log-sum-exp, or null
     unsigned long long wait_limit_ns;
     int test_hooks;        // ATTN_TEST_WITHHOLD_O_READY: CTA 0 skips its first unit's O-ready signal
+    // variable-length batches (the kVarlen instance only): B sequences packed along the token
+    // axis; per sequence b a tensor map each for Q, K, V and O (vl_maps[4 b + 0..3]) that
+    // covers only its rows, and vl_items[b] = items of sequences before b (vl_items[B]: all)
+    const CUtensorMap* vl_maps;
+    const int* vl_items;
+    const int* cu_q;       // [B + 1] query row offsets
+    const int* cu_k;       // [B + 1] key row offsets
+    long long total_q;     // LSE row stride ([H][total_q])
 };
 
 struct Item {
     int b, h, hk, qb, kv_begin, kv_end, split_slot;   // hk: the K/V head query head h reads
+    int sq, skv, causal_off;   // the sequence's lengths (variable-length batches only)
+    long long q0;              // its first query row in the packed tensors
 };
 
 // The item a CTA runs in its r-th round: round-robin, and for causal launches in alternating
@@ -148,10 +159,46 @@ __device__ __forceinline__ int round_item(int r) {
     return r * (int)gridDim.x + c;
 }
 
+// Work item k of a variable-length batch: sequence b holds items vl_items[b] .. vl_items[b+1]-1,
+// H * ceil(Sq_b / 256) of them (none when it has no queries or no keys), query blocks fastest
+// so that consecutive items share K/V; causal ones run each head's blocks last to first
+// (heaviest first).  Lengths and offsets come from the sequence; nothing is split.
+template <bool kCausal>
+__device__ __forceinline__ Item decode_varlen_item(const FwdParams& p, int k) {
+    Item it;
+    int lo = 0, hi = p.B - 1;             // the last b with vl_items[b] <= k
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.vl_items + mid) <= k) lo = mid;
+        else hi = mid - 1;
+    }
+    it.b = lo;
+    const int r = k - __ldg(p.vl_items + lo);
+    const int q0 = __ldg(p.cu_q + lo), k0 = __ldg(p.cu_k + lo);
+    it.sq = __ldg(p.cu_q + lo + 1) - q0;
+    it.skv = __ldg(p.cu_k + lo + 1) - k0;
+    it.q0 = q0;
+    it.causal_off = it.skv - it.sq;
+    const int nqb = (it.sq + kUnitRows - 1) / kUnitRows;
+    it.h = r / nqb;
+    it.qb = kCausal ? nqb - 1 - r % nqb : r % nqb;
+    it.kv_begin = 0;
+    it.kv_end = (it.skv + kBN - 1) / kBN;
+    it.split_slot = -1;
+    if constexpr (kCausal) {
+        const int last = it.qb * kUnitRows + kUnitRows - 1 + it.causal_off;   // last visible key
+        const int need = last < 0 ? 1 : last / kBN + 1;
+        it.kv_end = need < it.kv_end ? need : it.kv_end;
+    }
+    it.hk = p.group == 1 ? it.h : it.h / p.group;
+    return it;
+}
+
 // Work item k of the static schedule.  kCausal is a template parameter so that the
 // unmasked kernel carries none of the causal code.
-template <bool kCausal>
+template <bool kCausal, bool kVarlen = false>
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int k) {
+    if constexpr (kVarlen) return decode_varlen_item<kCausal>(p, k);
     Item it;
     int unit;
     if (k < p.n_full) {
@@ -283,7 +330,9 @@ __device__ __forceinline__ float weight_exponent(float s, float c, float m) {
     return fmaf(x, 0x1p-126f, ptx::fmax_nan(x, kMinExponent));
 }
 
-template <int D, bool kCausal>
+// kVarlen: a variable-length batch (per-sequence tensor maps from p.vl_maps, items from
+// p.vl_items, both written by attn_varlen_prep_kernel); a separate instance.
+template <int D, bool kCausal, bool kVarlen = false>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -331,6 +380,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // the split-combine kernel may be scheduled as CTAs retire; it waits for this grid's memory
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // a variable-length batch's item count comes from its preprocessing kernel
+    const int n_items = kVarlen ? __ldg(p.vl_items + p.B) : p.n_items;
 
     if (warp >= 8) {
         ptx::reg_dealloc<kRegsOther>();
@@ -341,19 +392,34 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             uint32_t pos = 0;             // ring position (monotonic)
             int u = 0;
             bool ok = true;
-            for (int r = 0, k = round_item<kCausal>(0); k < p.n_items && ok; k = round_item<kCausal>(++r), ++u) {
-                const Item it = decode_item<kCausal>(p, k);
+            for (int r = 0, k = round_item<kCausal>(0); k < n_items && ok; k = round_item<kCausal>(++r), ++u) {
+                const Item it = decode_item<kCausal, kVarlen>(p, k);
                 if (u > 0 && !(ok = wait_bar(bar(G::kBarQEmpty), (u - 1) & 1, kSiteQEmpty, abort_flag, lim)))
                     break;
+                // tensor maps and batch coordinate: a variable-length batch's sequence has maps of
+                // its own (token-major like BSHD, one "batch"), acquired before first use
+                const void* qmp = &qmap;
+                const void* kmp = &kmap;
+                const void* vmp = &vmap;
+                int bc = it.b;
+                if constexpr (kVarlen) {
+                    qmp = p.vl_maps + 4 * it.b;
+                    kmp = p.vl_maps + 4 * it.b + 1;
+                    vmp = p.vl_maps + 4 * it.b + 2;
+                    ptx::tensormap_acquire(qmp);
+                    ptx::tensormap_acquire(kmp);
+                    ptx::tensormap_acquire(vmp);
+                    bc = 0;
+                }
                 ptx::mbar_arrive_expect_tx(bar(G::kBarQFull), kQTiles * G::kTileBytes);
                 for (int t = 0; t < kQTiles; ++t) {
                     const int row = it.qb * kUnitRows + t * kBM;
                     for (int c = 0; c < G::kChunks; ++c) {
                         const uint32_t dst = sbase + G::kSmemQ + t * G::kTileBytes + c * kChunkBytes;
-                        if (p.bshd)
-                            ptx::tma_load_4d(dst, &qmap, bar(G::kBarQFull), c * 64, it.h, row, it.b, pol_q);
+                        if (kVarlen || p.bshd)
+                            ptx::tma_load_4d(dst, qmp, bar(G::kBarQFull), c * 64, it.h, row, bc, pol_q);
                         else
-                            ptx::tma_load_4d(dst, &qmap, bar(G::kBarQFull), c * 64, row, it.h, it.b, pol_q);
+                            ptx::tma_load_4d(dst, qmp, bar(G::kBarQFull), c * 64, row, it.h, bc, pol_q);
                     }
                 }
                 for (int j = it.kv_begin; j < it.kv_end && ok; ++j) {
@@ -363,13 +429,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                         if (!(ok = wait_bar(bar(G::kBarEmpty + slot), ph ^ 1u, kSiteRingEmpty, abort_flag, lim)))
                             break;
                         ptx::mbar_arrive_expect_tx(bar(G::kBarFull + slot), G::kTileBytes);
-                        const void* map = kv ? (const void*)&vmap : (const void*)&kmap;
+                        const void* map = kv ? vmp : kmp;
                         for (int c = 0; c < G::kChunks; ++c) {
                             const uint32_t dst = sbase + G::kSmemRing + slot * G::kTileBytes + c * kChunkBytes;
-                            if (p.bshd)
-                                ptx::tma_load_4d(dst, map, bar(G::kBarFull + slot), c * 64, it.hk, j * kBN, it.b, pol_kv);
+                            if (kVarlen || p.bshd)
+                                ptx::tma_load_4d(dst, map, bar(G::kBarFull + slot), c * 64, it.hk, j * kBN, bc, pol_kv);
                             else
-                                ptx::tma_load_4d(dst, map, bar(G::kBarFull + slot), c * 64, j * kBN, it.hk, it.b, pol_kv);
+                                ptx::tma_load_4d(dst, map, bar(G::kBarFull + slot), c * 64, j * kBN, it.hk, bc, pol_kv);
                         }
                     }
                 }
@@ -426,8 +492,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             uint32_t pcount = 0;   // P_t phases consumed (same count for both tiles)
             int u = 0;
             bool ok = true;
-            for (int r = 0, k = round_item<kCausal>(0); k < p.n_items && ok; k = round_item<kCausal>(++r), ++u) {
-                const Item it = decode_item<kCausal>(p, k);
+            for (int r = 0, k = round_item<kCausal>(0); k < n_items && ok; k = round_item<kCausal>(++r), ++u) {
+                const Item it = decode_item<kCausal, kVarlen>(p, k);
                 const int nk = it.kv_end - it.kv_begin;
                 if (!(ok = wait_bar(bar(G::kBarQFull), u & 1, kSiteQFull, abort_flag, lim))) break;
                 uint32_t kslot = pos % G::kStages;
@@ -497,8 +563,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         uint32_t scount = 0;
         int u = 0;
         bool ok = true;
-        for (int r = 0, k = round_item<kCausal>(0); k < p.n_items && ok; k = round_item<kCausal>(++r), ++u) {
-            const Item it = decode_item<kCausal>(p, k);
+        for (int r = 0, k = round_item<kCausal>(0); k < n_items && ok; k = round_item<kCausal>(++r), ++u) {
+            const Item it = decode_item<kCausal, kVarlen>(p, k);
             float m_ref = -INFINITY;      // running max of raw logits at the last rescale
             float l = 0.0f;               // running sum of weights relative to m_ref
             for (int j = it.kv_begin; j < it.kv_end; ++j) {
@@ -511,12 +577,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 // keys of this tile past `limit` are absent: beyond Skv, or (causal) past this
                 // row's diagonal; they get -inf logits and so weight 0
                 int limit = kBN - 1;
+                const int skv = kVarlen ? it.skv : p.Skv;
                 if constexpr (kCausal) {
-                    limit = p.Skv - j * kBN - 1;
-                    const int diag = it.qb * kUnitRows + t * kBM + row + p.causal_off - j * kBN;
+                    limit = skv - j * kBN - 1;
+                    const int diag = it.qb * kUnitRows + t * kBM + row + (kVarlen ? it.causal_off : p.causal_off) - j * kBN;
                     limit = diag < limit ? diag : limit;
                 } else {
-                    const int valid = p.Skv - j * kBN;   // the same for every row of the tile
+                    const int valid = skv - j * kBN;   // the same for every row of the tile
                     limit = valid < kBN ? valid - 1 : kBN - 1;
                 }
                 float mx, mn;
@@ -650,7 +717,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             ptx::tc_fence_after();
             const int qrow = it.qb * kUnitRows + t * kBM + row;
-            const bool valid_row = qrow < p.Sq;
+            const bool valid_row = qrow < (kVarlen ? it.sq : p.Sq);
             // the whole O_t row in registers with one TMEM wait
             uint32_t o[D];
             if constexpr (D == 128) ptx::tmem_ld128(tO, o);
@@ -658,8 +725,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             if (it.split_slot < 0) {
                 const float inv = 1.0f / l;
                 // natural-log log-sum-exp of the scaled logits: (m_ref*c + log2 l) * ln 2
-                if (p.lse && valid_row)
-                    p.lse[((long long)it.b * p.H + it.h) * p.Sq + qrow] = (m_ref * c + log2f(l)) * kLn2;
+                if (p.lse && valid_row) {
+                    const long long li = kVarlen ? (long long)it.h * p.total_q + it.q0 + qrow
+                                                 : ((long long)it.b * p.H + it.h) * p.Sq + qrow;
+                    p.lse[li] = (m_ref * c + log2f(l)) * kLn2;
+                }
                 const uint32_t region = sbase + G::kSmemStage + (uint32_t)(warp * kStageBytes);
                 const int r0 = it.qb * kUnitRows + t * kBM + quarter * kStageRowsPerWarp;
 #pragma unroll
@@ -679,8 +749,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        if (p.bshd) ptx::tma_store_4d(&omap, region, hc * 64, it.h, r0, it.b);
-                        else ptx::tma_store_4d(&omap, region, hc * 64, r0, it.h, it.b);
+                        if constexpr (kVarlen) {
+                            const CUtensorMap* om = p.vl_maps + 4 * it.b + 3;
+                            if (hc == 0) ptx::tensormap_acquire(om);
+                            ptx::tma_store_4d(om, region, hc * 64, it.h, r0, 0);
+                        } else if (p.bshd) {
+                            ptx::tma_store_4d(&omap, region, hc * 64, it.h, r0, it.b);
+                        } else {
+                            ptx::tma_store_4d(&omap, region, hc * 64, r0, it.h, it.b);
+                        }
                         ptx::bulk_commit();
                     }
                 }
@@ -1348,6 +1425,143 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p
         *reinterpret_cast<uint32_t*>(orow + lane * 2) = bits[0] | (bits[1] << 16);
 }
 
+// ------------------------------------------------------------------------------ varlen prep
+// Preprocessing of a variable-length batch, one CTA, before the attention kernel (which is
+// its programmatic dependent and waits for its memory):
+//   * checks the offsets: cu_q and cu_k start at >= 0, never decrease, and end within the
+//     packed tensors; otherwise it records ATTN_ERR_INVALID_ARG at the sequence-length site and
+//     schedules no work, so no load or store is issued from a bad offset;
+//   * items[b] = items of the sequences before b, items[B] = all of them, with H * ceil(Sq_b /
+//     256) items for a sequence that has both queries and keys;
+//   * per such sequence, tensor maps for its Q, K, V and O rows: copies of the whole-tensor
+//     maps with the base moved to the sequence's first row and the row count set to its
+//     length, so loads past its end read zeros and stores past its end are dropped, as at the
+//     end of a dense tensor (tensormap.replace, then a release fence for the tensor-map
+//     proxy; the attention kernel acquires each map before its first use);
+//   * a sequence with queries but no keys: every query sees no key, so its O rows are NaN
+//     (stored 0x7FC0) and its LSE rows -inf, written here.
+struct VarlenPrep {
+    const int* cu_q;
+    const int* cu_k;
+    int B, H;
+    long long total_q, total_k;
+    long long q_row_bytes, kv_row_bytes;   // bytes per token row: H*d*2, Hkv*d*2
+    const char* q;
+    const char* k;
+    const char* v;
+    char* o;
+    float* lse;                            // optional [H][total_q]
+    CUtensorMap* maps;                     // [B][4]: Q, K, V, O
+    int* items;                            // [B + 1]
+};
+
+__device__ __forceinline__ void copy_map(CUtensorMap* dst, const CUtensorMap* src) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(CUtensorMap) / 16); ++i) d4[i] = s4[i];
+}
+
+// the map at dst (a copy of a whole-tensor map) restricted to `rows` token rows from `base`
+__device__ __forceinline__ void narrow_map(CUtensorMap* dst, const void* base, int rows) {
+    asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst),
+                 "l"(reinterpret_cast<uint64_t>(base))
+                 : "memory");
+    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 2, %1;" ::"l"(dst), "r"(rows) : "memory");
+}
+
+__global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_constant__ CUtensorMap qmap,
+                                                                const __grid_constant__ CUtensorMap kmap,
+                                                                const __grid_constant__ CUtensorMap vmap,
+                                                                const __grid_constant__ CUtensorMap omap,
+                                                                const VarlenPrep a) {
+    __shared__ int bad;
+    __shared__ int warp_sums[32];
+    __shared__ int carry;
+    // the previous kernel in the stream may have written the offsets or still read this
+    // workspace; the attention kernel may launch now and waits for this one's memory
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (tid == 0) {
+        bad = (a.cu_q[0] < 0 || a.cu_k[0] < 0 || a.cu_q[a.B] > a.total_q || a.cu_k[a.B] > a.total_k) ? 1 : 0;
+        carry = 0;
+    }
+    __syncthreads();
+    for (int b = tid; b < a.B; b += blockDim.x)
+        if (a.cu_q[b + 1] < a.cu_q[b] || a.cu_k[b + 1] < a.cu_k[b]) bad = 1;
+    __syncthreads();
+    if (bad) {
+        if (tid == 0) {
+            if (atomicCAS(&g_status[0], 0u, (uint32_t)ATTN_ERR_INVALID_ARG) == 0u) atomicExch(&g_status[1], kSiteSeqlens);
+        }
+        for (int b = tid; b <= a.B; b += blockDim.x) a.items[b] = 0;
+        return;
+    }
+    // exclusive prefix of the per-sequence item counts, 1024 sequences per pass
+    for (int base = 0; base < a.B; base += blockDim.x) {
+        const int b = base + tid;
+        int n = 0, sq = 0, skv = 0;
+        if (b < a.B) {
+            sq = a.cu_q[b + 1] - a.cu_q[b];
+            skv = a.cu_k[b + 1] - a.cu_k[b];
+            n = (sq > 0 && skv > 0) ? a.H * ((sq + kUnitRows - 1) / kUnitRows) : 0;
+        }
+        int incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) warp_sums[wid] = incl;
+        __syncthreads();
+        if (wid == 0) {
+            int w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, w, off);
+                if (lane >= off) w += y;
+            }
+            warp_sums[lane] = w;   // inclusive over warps
+        }
+        __syncthreads();
+        const int before = carry + (wid > 0 ? warp_sums[wid - 1] : 0) + incl - n;
+        // queries with no keys: the warp writes each such sequence's NaN rows and -inf LSE
+        unsigned nan_seqs = __ballot_sync(0xFFFFFFFFu, b < a.B && sq > 0 && skv == 0);
+        while (nan_seqs) {
+            const int src = __ffs(nan_seqs) - 1;
+            nan_seqs &= nan_seqs - 1;
+            const long long q0 = a.cu_q[base + (wid << 5) + src];
+            const long long rows = __shfl_sync(0xFFFFFFFFu, sq, src);
+            const uint4 nan8 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
+            uint4* dst = reinterpret_cast<uint4*>(a.o + q0 * a.q_row_bytes);
+            for (long long e = lane; e < rows * a.q_row_bytes / 16; e += 32) dst[e] = nan8;
+            if (a.lse)
+                for (long long e = lane; e < rows * a.H; e += 32) a.lse[(e / rows) * a.total_q + q0 + e % rows] = -INFINITY;
+        }
+        if (b < a.B) {
+            a.items[b] = before;
+            if (n > 0) {
+                CUtensorMap* m = a.maps + 4 * (long long)b;
+                const long long q0 = a.cu_q[b], k0 = a.cu_k[b];
+                copy_map(m + 0, &qmap);
+                copy_map(m + 1, &kmap);
+                copy_map(m + 2, &vmap);
+                copy_map(m + 3, &omap);
+                narrow_map(m + 0, a.q + q0 * a.q_row_bytes, sq);
+                narrow_map(m + 1, a.k + k0 * a.kv_row_bytes, skv);
+                narrow_map(m + 2, a.v + k0 * a.kv_row_bytes, skv);
+                narrow_map(m + 3, a.o + q0 * a.q_row_bytes, sq);
+            }
+        }
+        __syncthreads();
+        if (tid == blockDim.x - 1) carry = before + n;
+        __syncthreads();
+    }
+    if (tid == 0) a.items[a.B] = carry;
+    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------ host side
 struct DeviceInfo {
     bool init = false;
@@ -1469,6 +1683,14 @@ int device_info(DeviceInfo** out) {
             cudaFuncSetAttribute(attn_fwd_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s64) !=
                 cudaSuccess ||
             cudaFuncSetAttribute(attn_fwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s64) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(attn_fwd_kernel<128, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 s128) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_fwd_kernel<128, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 s128) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_fwd_kernel<64, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s64) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(attn_fwd_kernel<64, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s64) !=
                 cudaSuccess)
             return ATTN_ERR_CUDA;
         const int t128 = sq::Geo<128>::kSmemAlloc, t64 = sq::Geo<64>::kSmemAlloc;
@@ -1718,6 +1940,156 @@ int run(const attn_args_t& a, const attn_options_t* opts, void* workspace, size_
     return launch(a, pl, opts, ws, stream);
 }
 
+// ---------------------------------------------------------------- variable-length batches
+int validate_varlen_shape(const attn_varlen_args_t& a, const attn_options_t* opts) {
+    if (a.B < 1 || a.H < 1 || a.Hkv < 1 || a.total_q < 0 || a.total_k < 0 || a.max_seqlen_q < 0 || a.d < 1)
+        return ATTN_ERR_INVALID_ARG;
+    if (a.H % a.Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (a.round_mode < ATTN_ROUND_RTNE || a.round_mode > ATTN_ROUND_RTZ) return ATTN_ERR_INVALID_ARG;
+    if ((a.causal != 0 && a.causal != 1) || a.reserved != 0 || a.reserved2 != 0) return ATTN_ERR_INVALID_ARG;
+    if (a.d != 128 && a.d != 64) return ATTN_ERR_UNSUPPORTED;
+    if (opts && opts->force_splits > 1) return ATTN_ERR_UNSUPPORTED;
+    if (opts && opts->test_hooks != 0) return ATTN_ERR_INVALID_ARG;
+    // offsets are int32; token rows, item indices and TMA coordinates stay below 2^30
+    const int64_t lim = (int64_t)1 << 30;
+    if (a.total_q > lim || a.total_k > lim || a.B > lim || a.H > lim) return ATTN_ERR_UNSUPPORTED;
+    if (a.H * (a.total_q / kUnitRows + a.B) > lim) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+// workspace: per-sequence tensor maps (128-byte aligned inside it) and the item offsets
+size_t varlen_ws_bytes(const attn_varlen_args_t& a) {
+    return 128 + (size_t)a.B * 4 * sizeof(CUtensorMap) + (size_t)((a.B + 1 + 3) / 4) * 16;
+}
+
+int run_varlen(const attn_varlen_args_t& a, const attn_options_t* opts, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream) {
+    int st = validate_varlen_shape(a, opts);
+    if (st != ATTN_OK) return st;
+    if (!a.q || !a.k || !a.v || !a.o || !a.cu_seqlens_q || !a.cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+    if (((uintptr_t)a.q | (uintptr_t)a.k | (uintptr_t)a.v | (uintptr_t)a.o) & 15u) return ATTN_ERR_MISALIGNED;
+    if (((uintptr_t)a.lse | (uintptr_t)a.cu_seqlens_q | (uintptr_t)a.cu_seqlens_k) & 3u) return ATTN_ERR_MISALIGNED;
+    const uintptr_t qbytes = (uintptr_t)(a.total_q * a.H * a.d * 2), kvbytes = (uintptr_t)(a.total_k * a.Hkv * a.d * 2);
+    auto overlap = [](uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; };
+    const uintptr_t ob = (uintptr_t)a.o, oe = ob + qbytes, qb = (uintptr_t)a.q, qe = qb + qbytes;
+    const uintptr_t kb = (uintptr_t)a.k, ke = kb + kvbytes, vb = (uintptr_t)a.v, ve = vb + kvbytes;
+    if (overlap(ob, oe, qb, qe) || overlap(ob, oe, kb, ke) || overlap(ob, oe, vb, ve)) return ATTN_ERR_ALIAS;
+    if (a.lse) {
+        const uintptr_t lb = (uintptr_t)a.lse, le = lb + (uintptr_t)(a.H * a.total_q * 4);
+        if (overlap(lb, le, ob, oe) || overlap(lb, le, qb, qe) || overlap(lb, le, kb, ke) || overlap(lb, le, vb, ve))
+            return ATTN_ERR_ALIAS;
+    }
+    DeviceInfo* di = nullptr;
+    if ((st = device_info(&di)) != ATTN_OK) return st;
+    const size_t need = varlen_ws_bytes(a);
+    void* ws = nullptr;
+    if (workspace) {
+        if (workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+        if ((uintptr_t)workspace & 15u) return ATTN_ERR_MISALIGNED;
+        ws = workspace;
+    } else if ((st = library_workspace(di, need, &ws)) != ATTN_OK) {
+        return st;
+    }
+    const uintptr_t wsb = (uintptr_t)ws;
+    if (overlap(wsb, wsb + need, ob, oe) || (a.lse && overlap(wsb, wsb + need, (uintptr_t)a.lse,
+                                                              (uintptr_t)a.lse + (uintptr_t)(a.H * a.total_q * 4))))
+        return ATTN_ERR_ALIAS;
+    const int64_t d = a.d;
+    // whole-tensor maps (token-major, one batch), which the preprocessing kernel narrows to
+    // each sequence; a tensor with no rows gets a one-row map that no item ever uses
+    const int64_t tq = a.total_q > 0 ? a.total_q : 1, tk = a.total_k > 0 ? a.total_k : 1;
+    CUtensorMap qm, km, vm, om;
+    if (!encode_map(&qm, a.q, 1, a.H, tq, d, true) || !encode_map(&km, a.k, 1, a.Hkv, tk, d, true) ||
+        !encode_map(&vm, a.v, 1, a.Hkv, tk, d, true) || !encode_map(&om, a.o, 1, a.H, tq, d, true, kStageRowsPerWarp))
+        return ATTN_ERR_CUDA;
+    CUtensorMap* maps = reinterpret_cast<CUtensorMap*>((wsb + 127u) & ~(uintptr_t)127u);
+    int* items = reinterpret_cast<int*>(maps + 4 * a.B);
+    VarlenPrep vp;
+    memset(&vp, 0, sizeof vp);
+    vp.cu_q = a.cu_seqlens_q;
+    vp.cu_k = a.cu_seqlens_k;
+    vp.B = (int)a.B;
+    vp.H = (int)a.H;
+    vp.total_q = a.total_q;
+    vp.total_k = a.total_k;
+    vp.q_row_bytes = a.H * d * 2;
+    vp.kv_row_bytes = a.Hkv * d * 2;
+    vp.q = reinterpret_cast<const char*>(a.q);
+    vp.k = reinterpret_cast<const char*>(a.k);
+    vp.v = reinterpret_cast<const char*>(a.v);
+    vp.o = reinterpret_cast<char*>(a.o);
+    vp.lse = a.lse;
+    vp.maps = maps;
+    vp.items = items;
+
+    FwdParams p;
+    memset(&p, 0, sizeof p);
+    p.B = (int)a.B;
+    p.H = (int)a.H;
+    p.group = (int)(a.H / a.Hkv);
+    p.causal = a.causal;
+    p.nsplit = 1;
+    p.bshd = 1;
+    p.round_mode = a.round_mode;
+    p.scale_log2 = (float)((1.0 / std::sqrt((double)d)) * 1.4426950408889634);
+    p.tau = 8.0f;
+    p.o = reinterpret_cast<__nv_bfloat16*>(a.o);
+    p.lse = a.lse;
+    const uint32_t ms = (opts && opts->wait_limit_ms) ? opts->wait_limit_ms : 2000u;
+    p.wait_limit_ns = (unsigned long long)ms * 1000000ull;
+    p.vl_maps = maps;
+    p.vl_items = items;
+    p.cu_q = a.cu_seqlens_q;
+    p.cu_k = a.cu_seqlens_k;
+    p.total_q = a.total_q;
+
+    int64_t G = di->sms;
+    if (opts && opts->max_ctas > 0 && opts->max_ctas < G) G = opts->max_ctas;
+    if (a.max_seqlen_q > 0) {
+        const int64_t cap = a.B * a.H * cdiv(a.max_seqlen_q, kUnitRows);
+        if (cap < G) G = cap;
+    }
+    if (G < 1) G = 1;
+
+    // preprocessing -> attention kernel, each a programmatic dependent of the kernel before it
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t lc;
+    memset(&lc, 0, sizeof lc);
+    lc.gridDim = dim3(1);
+    lc.blockDim = dim3(1024);
+    lc.stream = stream;
+    lc.attrs = pdl;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, attn_varlen_prep_kernel, qm, km, vm, om, vp) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    const attn_event_t* ev = opts ? opts->events : nullptr;
+    if (ev && ev[0] && cudaEventRecord((cudaEvent_t)ev[0], stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    lc.gridDim = dim3((unsigned)G);
+    lc.blockDim = dim3(kThreads);
+    cudaError_t le;
+    if (d == 128) {
+        lc.dynamicSmemBytes = Geo<128>::kSmemAlloc;
+        le = a.causal ? cudaLaunchKernelEx(&lc, attn_fwd_kernel<128, true, true>, qm, km, vm, om, p)
+                      : cudaLaunchKernelEx(&lc, attn_fwd_kernel<128, false, true>, qm, km, vm, om, p);
+    } else {
+        lc.dynamicSmemBytes = Geo<64>::kSmemAlloc;
+        le = a.causal ? cudaLaunchKernelEx(&lc, attn_fwd_kernel<64, true, true>, qm, km, vm, om, p)
+                      : cudaLaunchKernelEx(&lc, attn_fwd_kernel<64, false, true>, qm, km, vm, om, p);
+    }
+    if (le != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    for (int i = 1; i < 3; ++i)
+        if (ev && ev[i] && cudaEventRecord((cudaEvent_t)ev[i], stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
 size_t workspace_for(const attn_args_t& a, const attn_options_t* opts) {
     if (validate_shape(a, opts) != ATTN_OK) return 0;
     DeviceInfo* di = nullptr;
@@ -1757,6 +2129,17 @@ size_t attn_fwd_workspace_size_opts(int64_t B, int64_t H, int64_t Sq, int64_t Sk
 
 size_t attn_fwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t d) {
     return attn_fwd_workspace_size_opts(B, H, Sq, Skv, d, nullptr);
+}
+
+size_t attn_fwd_varlen_workspace_size(const attn_varlen_args_t* args) {
+    if (!args || validate_varlen_shape(*args, nullptr) != ATTN_OK) return 0;
+    return varlen_ws_bytes(*args);
+}
+
+int attn_fwd_varlen(const attn_varlen_args_t* args, const attn_options_t* opts, void* workspace,
+                    size_t workspace_bytes, attn_stream_t stream) {
+    if (!args) return ATTN_ERR_INVALID_ARG;
+    return run_varlen(*args, opts, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 int attn_fwd_ex(const attn_args_t* args, const attn_options_t* opts, void* workspace, size_t workspace_bytes,
@@ -1813,6 +2196,6 @@ const char* attn_status_string(int status) {
     }
 }
 
-int attn_version(void) { return 100; }
+int attn_version(void) { return 200; }
 
 }  // extern "C"

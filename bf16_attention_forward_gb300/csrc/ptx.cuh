@@ -89,6 +89,12 @@ __device__ __forceinline__ void tma_store_4d(const void* tmap, uint32_t src, int
         : "memory");
 }
 
+// Makes a tensor map in global memory, written by an earlier kernel (generic stores and
+// tensormap.replace, then a release fence), safe for this thread's TMA instructions to use.
+__device__ __forceinline__ void tensormap_acquire(const void* tmap) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(tmap) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

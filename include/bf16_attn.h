@@ -94,6 +94,8 @@ typedef struct {
 #define ATTN_TEST_WITHHOLD_O_READY 1
 #define ATTN_SITE_O_READY 7
 #define ATTN_BWD_SITE_DKV_READY 9
+/* Site reported with ATTN_ERR_INVALID_ARG when attn_fwd_varlen's offsets are inconsistent. */
+#define ATTN_SITE_SEQLENS 13
 
 /* The work split chosen for a shape (host only, launches nothing). */
 typedef struct {
@@ -219,9 +221,51 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, int64
                      attn_stream_t stream);
 
 /*
+ * Variable-length batches -- the third feature the MoonMath article's limitations paragraph
+ * lists as missing from its kernel.  B sequences of different lengths are packed along one
+ * token axis (token-major, like BSHD without the batch axis); sequence b owns query rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1
+ * and attends only to its own keys: row i of sequence b is attention over that sequence's
+ * keys, exactly as attn_fwd_ex on the sequence alone.
+ *   q             bf16 [total_q][H][d];  k, v  bf16 [total_k][Hkv][d];  o  bf16 like q
+ *   lse           optional fp32 [H][total_q] (row (h, i) at h*total_q + i), as in attn_fwd_ex
+ *   cu_seqlens_q, cu_seqlens_k   device int32 [B + 1]: start >= 0, never decrease, end <=
+ *                 total_q (total_k).  Checked on the device: a violation writes no output and
+ *                 reports ATTN_ERR_INVALID_ARG at site ATTN_SITE_SEQLENS through
+ *                 attn_get_device_status().  A sequence may be empty; one with queries but no
+ *                 keys gets NaN outputs and -inf LSE (no key is visible).  Query rows outside
+ *                 every sequence are not written.
+ *   B             sequences (>= 1);  H, Hkv, d  as in attn_fwd_ex;  total_q, total_k >= 0
+ *   max_seqlen_q  an upper bound on any sequence's query length, used only to size the grid
+ *                 (0: unknown, one CTA per SM)
+ *   causal        per sequence, aligned at its last query and key (attn_fwd_ex's rule)
+ *   reserved      must be 0
+ * Keys are never split (opts->force_splits must be 0 or 1).  workspace: caller device memory
+ * of at least attn_fwd_varlen_workspace_size() bytes (per-sequence tensor maps and work-item
+ * offsets), 16-byte aligned; or NULL to use the library-owned workspace as attn_fwd_ex does.
+ * Two kernels run on `stream`: a one-CTA preprocessing kernel, then the attention kernel.
+ */
+typedef struct {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;
+    const int32_t* cu_seqlens_q;
+    const int32_t* cu_seqlens_k;
+    int64_t B, H, Hkv, total_q, total_k, max_seqlen_q, d;
+    int32_t round_mode, causal, reserved, reserved2;
+} attn_varlen_args_t;
+
+size_t attn_fwd_varlen_workspace_size(const attn_varlen_args_t* args);
+int attn_fwd_varlen(const attn_varlen_args_t* args, const attn_options_t* opts, void* workspace,
+                    size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * attn_get_device_status -- synchronizes `stream`, then reads and clears the current
- * device's status word.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT, or ATTN_ERR_CUDA.  If
- * site != NULL it receives the id of the wait that expired (0 if none).
+ * device's status word.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT (a bounded wait expired),
+ * ATTN_ERR_INVALID_ARG (attn_fwd_varlen's offsets), or ATTN_ERR_CUDA.  If site != NULL it
+ * receives the id of the wait or check that failed (0 if none).
  */
 int attn_get_device_status(attn_stream_t stream, int32_t* site);
 

@@ -171,6 +171,62 @@ def attention(q, k, v, layout: str = "bshd", mode: str = "rtne", rows=None,
     return out
 
 
+def attention_varlen(q, k, v, cu_q, cu_k, mode: str = "rtne", causal: bool = False,
+                     want_a: bool = False, want_lse: bool = False, lib=None) -> dict:
+    """Oracle attention over a variable-length batch packed along the token axis.
+
+    The page "MoonMath AI open-sources a HIP attention kernel for AMD MI300X that beats AITER"
+    lists variable-length batching among its kernel's limitations; the plain reading of the
+    feature is that each sequence is an attention problem of its own.  So sequence b (query
+    rows cu_q[b] .. cu_q[b+1]-1, key rows cu_k[b] .. cu_k[b+1]-1 of q [Tq, H, d] and
+    k, v [Tk, Hkv, d]) is passed alone to :func:`attention` as a one-batch BSHD problem, and
+    its rows are put back in place.  A sequence with queries but no keys has no visible key
+    for any query: 0/0, so NaN outputs (0x7FC0) and LSE -inf, as for a causal row that sees
+    no key.
+
+    Returns ``o_bits`` [Tq, H, d] (uint16), ``covered`` [Tq] (rows that belong to a
+    sequence; the others are left 0), and optionally ``a`` [Tq, H, d] and ``lse`` [H, Tq]
+    (natural log).
+    """
+    qb, kb, vb = _as_bits(q), _as_bits(k), _as_bits(v)
+    Tq, H, d = qb.shape
+    cu_q = [int(x) for x in np.asarray(cu_q).reshape(-1)]
+    cu_k = [int(x) for x in np.asarray(cu_k).reshape(-1)]
+    if len(cu_q) != len(cu_k) or len(cu_q) < 2:
+        raise ValueError("cu_q and cu_k must both hold B + 1 >= 2 offsets")
+    o_bits = np.zeros((Tq, H, d), dtype=np.uint16)
+    covered = np.zeros((Tq,), dtype=bool)
+    a = np.zeros((Tq, H, d), dtype=np.float64) if want_a else None
+    lse = np.zeros((H, Tq), dtype=np.float64) if want_lse else None
+    for b in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        if not (0 <= q0 <= q1 <= Tq and 0 <= k0 <= k1 <= kb.shape[0]):
+            raise ValueError("sequence %d: offsets out of order or out of range" % b)
+        if q1 == q0:
+            continue
+        covered[q0:q1] = True
+        if k1 == k0:
+            o_bits[q0:q1] = 0x7FC0
+            if a is not None:
+                a[q0:q1] = np.nan
+            if lse is not None:
+                lse[:, q0:q1] = -np.inf
+            continue
+        r = attention(qb[None, q0:q1], kb[None, k0:k1], vb[None, k0:k1], "bshd", mode,
+                      want_a=want_a, want_lse=want_lse, lib=lib, causal=causal)
+        o_bits[q0:q1] = r["o_bits"][0].transpose(1, 0, 2)
+        if a is not None:
+            a[q0:q1] = r["a"][0].transpose(1, 0, 2)
+        if lse is not None:
+            lse[:, q0:q1] = r["lse"][0]
+    out = {"o_bits": o_bits, "covered": covered}
+    if a is not None:
+        out["a"] = a
+    if lse is not None:
+        out["lse"] = lse
+    return out
+
+
 def round_bf16(x, mode: str = "rtne", lib=None) -> np.ndarray:
     """Round float64 values to bf16 bit patterns with the oracle's rounding rule."""
     lib = lib or load()

@@ -219,3 +219,49 @@ def test_bwd_workspace_size_deterministic(lib):
     assert lib.attn_bwd_workspace_size(ctypes.byref(a)) == 6 * dq + 2 * rows_pad * 4
     a.Skv, a.d = 128, 64
     assert lib.attn_bwd_workspace_size(ctypes.byref(a)) == dq // 2 + 2 * rows_pad * 4
+
+
+def varlen_args(**kw):
+    a = attn.VarlenArgs()
+    a.q, a.k, a.v, a.o = P, 2 * P, 3 * P, 4 * P
+    a.cu_seqlens_q, a.cu_seqlens_k = 5 * P, 6 * P
+    a.B, a.H, a.Hkv, a.total_q, a.total_k, a.max_seqlen_q, a.d = 2, 2, 1, 16, 16, 0, 128
+    for k_, v_ in kw.items():
+        setattr(a, k_, v_)
+    return a
+
+
+def test_varlen_argument_errors(lib):
+    """attn_fwd_varlen checks its arguments before any device call: bad sizes or enums are
+    ATTN_ERR_INVALID_ARG, d not 64/128, a key split or int32 overflow ATTN_ERR_UNSUPPORTED,
+    unaligned pointers ATTN_ERR_MISALIGNED and an output overlapping an input ATTN_ERR_ALIAS;
+    valid arguments get as far as the device query (no GPU here: ATTN_ERR_NO_DEVICE)."""
+    def run(opts=None, **kw):
+        return lib.attn_fwd_varlen(ctypes.byref(varlen_args(**kw)), ctypes.byref(opts) if opts else None,
+                                   None, 0, None)
+    assert lib.attn_fwd_varlen(None, None, None, 0, None) == 1
+    assert run() == 5
+    assert run(B=3, total_q=0, total_k=0, max_seqlen_q=7, d=64) == 5
+    for bad in ({"B": 0}, {"Hkv": 3}, {"total_q": -1}, {"total_k": -1}, {"max_seqlen_q": -1},
+                {"round_mode": 3}, {"causal": 2}, {"reserved": 1}, {"reserved2": 1},
+                {"cu_seqlens_q": 0}, {"cu_seqlens_k": 0}, {"q": 0}, {"o": 0}):
+        assert run(**bad) == 1, bad
+    assert run(d=96) == 2
+    assert run(total_q=(1 << 30) + 1) == 2
+    assert run(opts=attn.Options(2, 0, 0, 0)) == 2
+    assert run(opts=attn.Options(1, 0, 0, 0)) == 5
+    assert run(opts=attn.Options(0, 0, 0, 1)) == 1
+    assert run(q=P + 8) == 3
+    assert run(cu_seqlens_k=6 * P + 2) == 3
+    assert run(lse=7 * P + 2) == 3
+    assert run(o=P) == 4
+    assert run(lse=4 * P + 64) == 4
+
+
+def test_varlen_workspace_size(lib):
+    """Per-sequence tensor maps (4 x 128 bytes) and B + 1 item offsets, plus alignment room."""
+    for B in (1, 2, 7, 1000):
+        a = varlen_args(B=B)
+        assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(a)) == 128 + B * 512 + -(-(B + 1) // 4) * 16
+    assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(varlen_args(B=0))) == 0
+    assert lib.attn_fwd_varlen_workspace_size(None) == 0

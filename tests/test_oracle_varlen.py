@@ -1,0 +1,115 @@
+"""Pins for the oracle's variable-length batches (``oracle.attention_varlen``).
+
+The page "MoonMath AI open-sources a HIP attention kernel for AMD MI300X that beats AITER"
+lists variable-length batching among its kernel's limitations.  The reading taken: each
+sequence of the packed batch is an attention problem of its own.  These checks pin the
+oracle's composition to things other than itself:
+  * a batch of equal-length sequences equals the dense batched oracle on the same data
+    reshaped to [B, S, H, d] (the C oracle's own batch indexing, not the slicing);
+  * sequences do not see each other: rewriting every other sequence's rows (with values
+    including +-inf and NaN) leaves a sequence's outputs bit for bit unchanged, and
+    reordering the sequences reorders the outputs;
+  * a lone sequence equals the dense oracle, and the edge rules hold: empty sequences cover
+    no rows, a sequence with no keys gets NaN (0x7FC0) outputs and LSE -inf, rows outside
+    every sequence stay uncovered.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import make_qkv
+
+
+def _packed(Tq, Tk, H, Hkv, d, seed, sigma=1.0):
+    q, k, v = make_qkv(1, H, Tq, Tk, d, "bshd", seed=seed, sigma=sigma, Hkv=Hkv)
+    return q[0], k[0], v[0]
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("mode", ["rtne", "rtz"])
+def test_equal_lengths_match_the_dense_batch(mode, causal):
+    B, Sq, Skv, H, Hkv, d = 3, 37, 53, 4, 2, 64
+    q, k, v = _packed(B * Sq, B * Skv, H, Hkv, d, seed=11)
+    cu_q = np.arange(B + 1) * Sq
+    cu_k = np.arange(B + 1) * Skv
+    r = oracle.attention_varlen(q, k, v, cu_q, cu_k, mode, causal=causal, want_a=True, want_lse=True)
+    dense = oracle.attention(q.reshape(B, Sq, H, d), k.reshape(B, Skv, Hkv, d), v.reshape(B, Skv, Hkv, d),
+                             "bshd", mode, want_a=True, want_lse=True, causal=causal)
+    # dense is (B, H, Sq, d); the packed rows are token-major
+    assert np.array_equal(r["o_bits"], dense["o_bits"].transpose(0, 2, 1, 3).reshape(B * Sq, H, d))
+    assert np.array_equal(r["a"], dense["a"].transpose(0, 2, 1, 3).reshape(B * Sq, H, d))
+    assert np.array_equal(r["lse"], dense["lse"].transpose(1, 0, 2).reshape(H, B * Sq))
+    assert r["covered"].all()
+
+
+def test_sequences_do_not_see_each_other():
+    H, Hkv, d = 2, 1, 128
+    lq, lk = [130, 1, 57], [70, 300, 5]
+    cu_q, cu_k = np.cumsum([0] + lq), np.cumsum([0] + lk)
+    q, k, v = _packed(sum(lq), sum(lk), H, Hkv, d, seed=12)
+    base = oracle.attention_varlen(q, k, v, cu_q, cu_k, "rtna", want_lse=True)
+    g = torch.Generator().manual_seed(3)
+    for b in range(3):
+        q2, k2, v2 = q.clone(), k.clone(), v.clone()
+        for o in range(3):
+            if o == b:
+                continue
+            for t, cu in ((q2, cu_q), (k2, cu_k), (v2, cu_k)):
+                rows = slice(cu[o], cu[o + 1])
+                x = torch.randn(t[rows].shape, generator=g) * 50
+                x.view(-1)[::7] = float("inf")
+                x.view(-1)[3::11] = float("nan")
+                t[rows] = x.to(torch.bfloat16)
+        r = oracle.attention_varlen(q2, k2, v2, cu_q, cu_k, "rtna", want_lse=True)
+        rows = slice(cu_q[b], cu_q[b + 1])
+        assert np.array_equal(r["o_bits"][rows], base["o_bits"][rows]), b
+        assert np.array_equal(r["lse"][:, rows], base["lse"][:, rows]), b
+
+
+def test_reordering_sequences_reorders_outputs():
+    H, d = 2, 64
+    lq, lk = [40, 9, 23], [17, 64, 3]
+    q, k, v = _packed(sum(lq), sum(lk), H, H, d, seed=13)
+    cu_q, cu_k = np.cumsum([0] + lq), np.cumsum([0] + lk)
+    base = oracle.attention_varlen(q, k, v, cu_q, cu_k, causal=True)
+    perm = [2, 0, 1]
+
+    def gather(t, cu):
+        return torch.cat([t[cu[b]:cu[b + 1]] for b in perm])
+
+    cu_q2 = np.cumsum([0] + [lq[b] for b in perm])
+    cu_k2 = np.cumsum([0] + [lk[b] for b in perm])
+    r = oracle.attention_varlen(gather(q, cu_q), gather(k, cu_k), gather(v, cu_k), cu_q2, cu_k2, causal=True)
+    want = np.concatenate([base["o_bits"][cu_q[b]:cu_q[b + 1]] for b in perm])
+    assert np.array_equal(r["o_bits"], want)
+
+
+def test_single_sequence_and_edge_rules():
+    H, Hkv, d = 4, 2, 128
+    q, k, v = _packed(20, 12, H, Hkv, d, seed=14)
+    # one sequence over rows 2..16 and keys 1..10; rows 0, 1 and 17.. belong to none
+    r = oracle.attention_varlen(q, k, v, [2, 17], [1, 11], want_lse=True)
+    dense = oracle.attention(q[None, 2:17], k[None, 1:11], v[None, 1:11], "bshd", want_lse=True)
+    assert np.array_equal(r["o_bits"][2:17], dense["o_bits"][0].transpose(1, 0, 2))
+    assert np.array_equal(r["lse"][:, 2:17], dense["lse"][0])
+    assert r["covered"].tolist() == [False] * 2 + [True] * 15 + [False] * 3
+    assert not r["o_bits"][:2].any() and not r["o_bits"][17:].any()
+    # an empty sequence, a sequence with queries but no keys, then a normal one
+    r = oracle.attention_varlen(q, k, v, [0, 0, 5, 20], [0, 4, 4, 12], want_lse=True)
+    assert (r["o_bits"][0:5] == 0x7FC0).all()
+    assert np.isneginf(r["lse"][:, 0:5]).all()
+    dense = oracle.attention(q[None, 5:20], k[None, 4:12], v[None, 4:12], "bshd", want_lse=True)
+    assert np.array_equal(r["o_bits"][5:20], dense["o_bits"][0].transpose(1, 0, 2))
+    assert r["covered"].all()
+
+
+def test_rejects_bad_offsets():
+    q, k, v = _packed(8, 8, 1, 1, 64, seed=15)
+    for cu_q, cu_k in (([0, 5, 3], [0, 4, 8]), ([0, 9], [0, 8]), ([0, 8], [-1, 8])):
+        with pytest.raises(ValueError):
+            oracle.attention_varlen(q, k, v, cu_q, cu_k)
