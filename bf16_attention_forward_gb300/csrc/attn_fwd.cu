@@ -134,9 +134,11 @@ struct FwdParams {
     int test_hooks;        // ATTN_TEST_WITHHOLD_O_READY: CTA 0 skips its first unit's O-ready signal
     // variable-length batches (the kVarlen instance only): B sequences packed along the token
     // axis; per sequence b a tensor map each for Q, K, V and O (vl_maps[4 b + 0..3]) that
-    // covers only its rows, and vl_items[b] = items of sequences before b (vl_items[B]: all)
+    // covers only its rows; the (sequence, query block) pairs to run, heaviest first
+    // (vl_blocks), each standing for H items (one per query head), and the item count
     const CUtensorMap* vl_maps;
-    const int* vl_items;
+    const int2* vl_blocks;
+    const int* vl_n_items;
     const int* cu_q;       // [B + 1] query row offsets
     const int* cu_k;       // [B + 1] key row offsets
     long long total_q;     // LSE row stride ([H][total_q])
@@ -145,43 +147,36 @@ struct FwdParams {
 struct Item {
     int b, h, hk, qb, kv_begin, kv_end, split_slot;   // hk: the K/V head query head h reads
     int sq, skv, causal_off;   // the sequence's lengths (variable-length batches only)
-    long long q0;              // its first query row in the packed tensors
+    int q0;                    // its first query row in the packed tensors (< 2^30)
 };
 
-// The item a CTA runs in its r-th round: round-robin, and for causal launches in alternating
-// direction (CTA c takes position c of even rounds and G - 1 - c of odd ones).  Causal items
-// run heaviest first and shrink from round to round, so plain round-robin gives the low CTAs
-// the heavier item of every round (a trace on the causal prefill had the first CTA done 13 %
-// before the last); alternating cancels that.  Within a CTA, items still increase with r.
-template <bool kCausal>
+// The item a CTA runs in its r-th round: round-robin, and for causal launches and
+// variable-length batches in alternating direction (CTA c takes position c of even rounds and
+// G - 1 - c of odd ones).  Their items run heaviest first and shrink from round to round, so
+// plain round-robin gives the low CTAs the heavier item of every round (a trace on the causal
+// prefill had the first CTA done 13 % before the last); alternating cancels that.  Within a
+// CTA, items still increase with r.
+template <bool kAlternate>
 __device__ __forceinline__ int round_item(int r) {
-    const int c = (kCausal && (r & 1)) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    const int c = (kAlternate && (r & 1)) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
     return r * (int)gridDim.x + c;
 }
 
-// Work item k of a variable-length batch: sequence b holds items vl_items[b] .. vl_items[b+1]-1,
-// H * ceil(Sq_b / 256) of them (none when it has no queries or no keys), query blocks fastest
-// so that consecutive items share K/V; causal ones run each head's blocks last to first
-// (heaviest first).  Lengths and offsets come from the sequence; nothing is split.
+// Work item k of a variable-length batch: query head k % H of the (sequence, 256-row query
+// block) pair vl_blocks[k / H], which the preprocessing kernel ordered by the key tiles they
+// run, most first.  Lengths and offsets come from the sequence; nothing is split.
 template <bool kCausal>
 __device__ __forceinline__ Item decode_varlen_item(const FwdParams& p, int k) {
     Item it;
-    int lo = 0, hi = p.B - 1;             // the last b with vl_items[b] <= k
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(p.vl_items + mid) <= k) lo = mid;
-        else hi = mid - 1;
-    }
-    it.b = lo;
-    const int r = k - __ldg(p.vl_items + lo);
-    const int q0 = __ldg(p.cu_q + lo), k0 = __ldg(p.cu_k + lo);
-    it.sq = __ldg(p.cu_q + lo + 1) - q0;
-    it.skv = __ldg(p.cu_k + lo + 1) - k0;
+    const int2 e = __ldg(p.vl_blocks + k / p.H);
+    it.b = e.x;
+    it.qb = e.y;
+    it.h = k % p.H;
+    const int q0 = __ldg(p.cu_q + it.b), k0 = __ldg(p.cu_k + it.b);
+    it.sq = __ldg(p.cu_q + it.b + 1) - q0;
+    it.skv = __ldg(p.cu_k + it.b + 1) - k0;
     it.q0 = q0;
     it.causal_off = it.skv - it.sq;
-    const int nqb = (it.sq + kUnitRows - 1) / kUnitRows;
-    it.h = r / nqb;
-    it.qb = kCausal ? nqb - 1 - r % nqb : r % nqb;
     it.kv_begin = 0;
     it.kv_end = (it.skv + kBN - 1) / kBN;
     it.split_slot = -1;
@@ -381,7 +376,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     // the split-combine kernel may be scheduled as CTAs retire; it waits for this grid's memory
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // a variable-length batch's item count comes from its preprocessing kernel
-    const int n_items = kVarlen ? __ldg(p.vl_items + p.B) : p.n_items;
+    const int n_items = kVarlen ? __ldg(p.vl_n_items) : p.n_items;
 
     if (warp >= 8) {
         ptx::reg_dealloc<kRegsOther>();
@@ -392,7 +387,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             uint32_t pos = 0;             // ring position (monotonic)
             int u = 0;
             bool ok = true;
-            for (int r = 0, k = round_item<kCausal>(0); k < n_items && ok; k = round_item<kCausal>(++r), ++u) {
+            for (int r = 0, k = round_item<kCausal || kVarlen>(0); k < n_items && ok; k = round_item<kCausal || kVarlen>(++r), ++u) {
                 const Item it = decode_item<kCausal, kVarlen>(p, k);
                 if (u > 0 && !(ok = wait_bar(bar(G::kBarQEmpty), (u - 1) & 1, kSiteQEmpty, abort_flag, lim)))
                     break;
@@ -492,7 +487,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             uint32_t pcount = 0;   // P_t phases consumed (same count for both tiles)
             int u = 0;
             bool ok = true;
-            for (int r = 0, k = round_item<kCausal>(0); k < n_items && ok; k = round_item<kCausal>(++r), ++u) {
+            for (int r = 0, k = round_item<kCausal || kVarlen>(0); k < n_items && ok; k = round_item<kCausal || kVarlen>(++r), ++u) {
                 const Item it = decode_item<kCausal, kVarlen>(p, k);
                 const int nk = it.kv_end - it.kv_begin;
                 if (!(ok = wait_bar(bar(G::kBarQFull), u & 1, kSiteQFull, abort_flag, lim))) break;
@@ -563,7 +558,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         uint32_t scount = 0;
         int u = 0;
         bool ok = true;
-        for (int r = 0, k = round_item<kCausal>(0); k < n_items && ok; k = round_item<kCausal>(++r), ++u) {
+        for (int r = 0, k = round_item<kCausal || kVarlen>(0); k < n_items && ok; k = round_item<kCausal || kVarlen>(++r), ++u) {
             const Item it = decode_item<kCausal, kVarlen>(p, k);
             float m_ref = -INFINITY;      // running max of raw logits at the last rescale
             float l = 0.0f;               // running sum of weights relative to m_ref
@@ -1431,19 +1426,23 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p
 //   * checks the offsets: cu_q and cu_k start at >= 0, never decrease, and end within the
 //     packed tensors; otherwise it records ATTN_ERR_INVALID_ARG at the sequence-length site and
 //     schedules no work, so no load or store is issued from a bad offset;
-//   * items[b] = items of the sequences before b, items[B] = all of them, with H * ceil(Sq_b /
-//     256) items for a sequence that has both queries and keys;
-//   * per such sequence, tensor maps for its Q, K, V and O rows: copies of the whole-tensor
-//     maps with the base moved to the sequence's first row and the row count set to its
-//     length, so loads past its end read zeros and stores past its end are dropped, as at the
-//     end of a dense tensor (tensormap.replace, then a release fence for the tensor-map
-//     proxy; the attention kernel acquires each map before its first use);
+//   * per sequence with both queries and keys, tensor maps for its Q, K, V and O rows: copies
+//     of the whole-tensor maps with the base moved to the sequence's first row and the row
+//     count set to its length, so loads past its end read zeros and stores past its end are
+//     dropped, as at the end of a dense tensor (tensormap.replace, then a release fence for
+//     the tensor-map proxy; the attention kernel acquires each map before its first use);
+//   * the work list: every (sequence, 256-row query block) pair, ordered by the key tiles it
+//     runs, most first (a counting sort on that count, capped at kCostBuckets - 1; pairs of
+//     equal count in any order, which moves work between CTAs but changes no result), and
+//     the item count, H per pair;
 //   * a sequence with queries but no keys: every query sees no key, so its O rows are NaN
 //     (stored 0x7FC0) and its LSE rows -inf, written here.
+constexpr int kCostBuckets = 4096;
+
 struct VarlenPrep {
     const int* cu_q;
     const int* cu_k;
-    int B, H;
+    int B, H, causal;
     long long total_q, total_k;
     long long q_row_bytes, kv_row_bytes;   // bytes per token row: H*d*2, Hkv*d*2
     const char* q;
@@ -1452,7 +1451,8 @@ struct VarlenPrep {
     char* o;
     float* lse;                            // optional [H][total_q]
     CUtensorMap* maps;                     // [B][4]: Q, K, V, O
-    int* items;                            // [B + 1]
+    int2* blocks;                          // (sequence, query block) pairs, heaviest first
+    int* n_items;
 };
 
 __device__ __forceinline__ void copy_map(CUtensorMap* dst, const CUtensorMap* src) {
@@ -1470,62 +1470,67 @@ __device__ __forceinline__ void narrow_map(CUtensorMap* dst, const void* base, i
     asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 2, %1;" ::"l"(dst), "r"(rows) : "memory");
 }
 
+// key tiles the attention kernel runs for query block qb of a sequence (its bucket)
+__device__ __forceinline__ int block_cost(int qb, int sq, int skv, int causal) {
+    int tiles = (skv + kBN - 1) / kBN;
+    if (causal) {
+        const int last = qb * kUnitRows + kUnitRows - 1 + skv - sq;   // last visible key
+        const int need = last < 0 ? 1 : last / kBN + 1;
+        tiles = need < tiles ? need : tiles;
+    }
+    return tiles < kCostBuckets - 1 ? tiles : kCostBuckets - 1;
+}
+
 __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_constant__ CUtensorMap qmap,
                                                                 const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 const __grid_constant__ CUtensorMap omap,
                                                                 const VarlenPrep a) {
     __shared__ int bad;
+    __shared__ int bucket[kCostBuckets];   // counts, then (descending) start positions
     __shared__ int warp_sums[32];
-    __shared__ int carry;
     // the previous kernel in the stream may have written the offsets or still read this
     // workspace; the attention kernel may launch now and waits for this one's memory
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    if (tid == 0) {
+    const int nthreads = blockDim.x;
+    if (tid == 0)
         bad = (a.cu_q[0] < 0 || a.cu_k[0] < 0 || a.cu_q[a.B] > a.total_q || a.cu_k[a.B] > a.total_k) ? 1 : 0;
-        carry = 0;
-    }
+    for (int i = tid; i < kCostBuckets; i += nthreads) bucket[i] = 0;
     __syncthreads();
-    for (int b = tid; b < a.B; b += blockDim.x)
+    for (int b = tid; b < a.B; b += nthreads)
         if (a.cu_q[b + 1] < a.cu_q[b] || a.cu_k[b + 1] < a.cu_k[b]) bad = 1;
     __syncthreads();
     if (bad) {
         if (tid == 0) {
+            *a.n_items = 0;
             if (atomicCAS(&g_status[0], 0u, (uint32_t)ATTN_ERR_INVALID_ARG) == 0u) atomicExch(&g_status[1], kSiteSeqlens);
         }
-        for (int b = tid; b <= a.B; b += blockDim.x) a.items[b] = 0;
         return;
     }
-    // exclusive prefix of the per-sequence item counts, 1024 sequences per pass
-    for (int base = 0; base < a.B; base += blockDim.x) {
+    // per sequence: maps, NaN rows, and the cost histogram of its query blocks
+    for (int base = 0; base < a.B; base += nthreads) {
         const int b = base + tid;
-        int n = 0, sq = 0, skv = 0;
+        int sq = 0, skv = 0;
         if (b < a.B) {
             sq = a.cu_q[b + 1] - a.cu_q[b];
             skv = a.cu_k[b + 1] - a.cu_k[b];
-            n = (sq > 0 && skv > 0) ? a.H * ((sq + kUnitRows - 1) / kUnitRows) : 0;
-        }
-        int incl = n;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-            if (lane >= off) incl += y;
-        }
-        if (lane == 31) warp_sums[wid] = incl;
-        __syncthreads();
-        if (wid == 0) {
-            int w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int y = __shfl_up_sync(0xFFFFFFFFu, w, off);
-                if (lane >= off) w += y;
+            if (sq > 0 && skv > 0) {
+                CUtensorMap* m = a.maps + 4 * (long long)b;
+                const long long q0 = a.cu_q[b], k0 = a.cu_k[b];
+                copy_map(m + 0, &qmap);
+                copy_map(m + 1, &kmap);
+                copy_map(m + 2, &vmap);
+                copy_map(m + 3, &omap);
+                narrow_map(m + 0, a.q + q0 * a.q_row_bytes, sq);
+                narrow_map(m + 1, a.k + k0 * a.kv_row_bytes, skv);
+                narrow_map(m + 2, a.v + k0 * a.kv_row_bytes, skv);
+                narrow_map(m + 3, a.o + q0 * a.q_row_bytes, sq);
+                const int nqb = (sq + kUnitRows - 1) / kUnitRows;
+                for (int qb = 0; qb < nqb; ++qb) atomicAdd(&bucket[block_cost(qb, sq, skv, a.causal)], 1);
             }
-            warp_sums[lane] = w;   // inclusive over warps
         }
-        __syncthreads();
-        const int before = carry + (wid > 0 ? warp_sums[wid - 1] : 0) + incl - n;
         // queries with no keys: the warp writes each such sequence's NaN rows and -inf LSE
         unsigned nan_seqs = __ballot_sync(0xFFFFFFFFu, b < a.B && sq > 0 && skv == 0);
         while (nan_seqs) {
@@ -1539,26 +1544,53 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
             if (a.lse)
                 for (long long e = lane; e < rows * a.H; e += 32) a.lse[(e / rows) * a.total_q + q0 + e % rows] = -INFINITY;
         }
-        if (b < a.B) {
-            a.items[b] = before;
-            if (n > 0) {
-                CUtensorMap* m = a.maps + 4 * (long long)b;
-                const long long q0 = a.cu_q[b], k0 = a.cu_k[b];
-                copy_map(m + 0, &qmap);
-                copy_map(m + 1, &kmap);
-                copy_map(m + 2, &vmap);
-                copy_map(m + 3, &omap);
-                narrow_map(m + 0, a.q + q0 * a.q_row_bytes, sq);
-                narrow_map(m + 1, a.k + k0 * a.kv_row_bytes, skv);
-                narrow_map(m + 2, a.v + k0 * a.kv_row_bytes, skv);
-                narrow_map(m + 3, a.o + q0 * a.q_row_bytes, sq);
-            }
-        }
-        __syncthreads();
-        if (tid == blockDim.x - 1) carry = before + n;
-        __syncthreads();
     }
-    if (tid == 0) a.items[a.B] = carry;
+    __syncthreads();
+    // start of each bucket in descending order: thread t owns buckets kCostBuckets - 4t - 1
+    // down to kCostBuckets - 4t - 4; an exclusive scan of the threads' sums over t
+    constexpr int kPer = kCostBuckets / 1024;
+    int local = 0;
+    if (tid < 1024)
+        for (int i = 0; i < kPer; ++i) local += bucket[kCostBuckets - 1 - kPer * tid - i];
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int w = lane < (nthreads >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, w, off);
+            if (lane >= off) w += y;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    int start = (wid > 0 ? warp_sums[wid - 1] : 0) + incl - local;
+    if (tid == nthreads - 1) *a.n_items = (start + local) * a.H;
+    __syncthreads();
+    if (tid < 1024)
+        for (int i = 0; i < kPer; ++i) {
+            const int key = kCostBuckets - 1 - kPer * tid - i;
+            const int c = bucket[key];
+            bucket[key] = start;
+            start += c;
+        }
+    __syncthreads();
+    // scatter every pair to its bucket's next position
+    for (int b = tid; b < a.B; b += nthreads) {
+        const int sq = a.cu_q[b + 1] - a.cu_q[b], skv = a.cu_k[b + 1] - a.cu_k[b];
+        if (sq <= 0 || skv <= 0) continue;
+        const int nqb = (sq + kUnitRows - 1) / kUnitRows;
+        for (int qb = 0; qb < nqb; ++qb) {
+            const int pos = atomicAdd(&bucket[block_cost(qb, sq, skv, a.causal)], 1);
+            a.blocks[pos] = make_int2(b, qb);
+        }
+    }
     asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
 }
 
@@ -1957,9 +1989,12 @@ int validate_varlen_shape(const attn_varlen_args_t& a, const attn_options_t* opt
     return ATTN_OK;
 }
 
-// workspace: per-sequence tensor maps (128-byte aligned inside it) and the item offsets
+// (sequence, query block) pairs a batch can hold: sum_b ceil(Sq_b / 256) <= total_q / 256 + B
+int64_t varlen_max_blocks(const attn_varlen_args_t& a) { return a.total_q / kUnitRows + a.B; }
+
+// workspace: per-sequence tensor maps (128-byte aligned inside it), the item count, the pairs
 size_t varlen_ws_bytes(const attn_varlen_args_t& a) {
-    return 128 + (size_t)a.B * 4 * sizeof(CUtensorMap) + (size_t)((a.B + 1 + 3) / 4) * 16;
+    return 128 + (size_t)a.B * 4 * sizeof(CUtensorMap) + 16 + (size_t)varlen_max_blocks(a) * sizeof(int2);
 }
 
 int run_varlen(const attn_varlen_args_t& a, const attn_options_t* opts, void* workspace, size_t workspace_bytes,
@@ -2003,13 +2038,15 @@ int run_varlen(const attn_varlen_args_t& a, const attn_options_t* opts, void* wo
         !encode_map(&vm, a.v, 1, a.Hkv, tk, d, true) || !encode_map(&om, a.o, 1, a.H, tq, d, true, kStageRowsPerWarp))
         return ATTN_ERR_CUDA;
     CUtensorMap* maps = reinterpret_cast<CUtensorMap*>((wsb + 127u) & ~(uintptr_t)127u);
-    int* items = reinterpret_cast<int*>(maps + 4 * a.B);
+    int* n_items = reinterpret_cast<int*>(maps + 4 * a.B);
+    int2* blocks = reinterpret_cast<int2*>(reinterpret_cast<char*>(n_items) + 16);
     VarlenPrep vp;
     memset(&vp, 0, sizeof vp);
     vp.cu_q = a.cu_seqlens_q;
     vp.cu_k = a.cu_seqlens_k;
     vp.B = (int)a.B;
     vp.H = (int)a.H;
+    vp.causal = a.causal;
     vp.total_q = a.total_q;
     vp.total_k = a.total_k;
     vp.q_row_bytes = a.H * d * 2;
@@ -2020,7 +2057,8 @@ int run_varlen(const attn_varlen_args_t& a, const attn_options_t* opts, void* wo
     vp.o = reinterpret_cast<char*>(a.o);
     vp.lse = a.lse;
     vp.maps = maps;
-    vp.items = items;
+    vp.blocks = blocks;
+    vp.n_items = n_items;
 
     FwdParams p;
     memset(&p, 0, sizeof p);
@@ -2038,7 +2076,8 @@ int run_varlen(const attn_varlen_args_t& a, const attn_options_t* opts, void* wo
     const uint32_t ms = (opts && opts->wait_limit_ms) ? opts->wait_limit_ms : 2000u;
     p.wait_limit_ns = (unsigned long long)ms * 1000000ull;
     p.vl_maps = maps;
-    p.vl_items = items;
+    p.vl_blocks = blocks;
+    p.vl_n_items = n_items;
     p.cu_q = a.cu_seqlens_q;
     p.cu_k = a.cu_seqlens_k;
     p.total_q = a.total_q;

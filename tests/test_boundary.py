@@ -259,9 +259,12 @@ def test_varlen_argument_errors(lib):
 
 
 def test_varlen_workspace_size(lib):
-    """Per-sequence tensor maps (4 x 128 bytes) and B + 1 item offsets, plus alignment room."""
-    for B in (1, 2, 7, 1000):
-        a = varlen_args(B=B)
-        assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(a)) == 128 + B * 512 + -(-(B + 1) // 4) * 16
+    """Per-sequence tensor maps (4 x 128 bytes), the item count (16 bytes) and room for every
+    (sequence, 256-row query block) pair (8 bytes each, at most total_q / 256 + B of them),
+    plus alignment room."""
+    for B, total_q in ((1, 16), (2, 16), (7, 5000), (1000, 1 << 20)):
+        a = varlen_args(B=B, total_q=total_q)
+        want = 128 + B * 512 + 16 + (total_q // 256 + B) * 8
+        assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(a)) == want, B
     assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(varlen_args(B=0))) == 0
     assert lib.attn_fwd_varlen_workspace_size(None) == 0
