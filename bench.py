@@ -67,9 +67,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", default="fwd", choices=["fwd", "bwd", "varlen"],
+    ap.add_argument("--op", default="fwd", choices=["fwd", "bwd", "varlen", "paged"],
                     help="bwd: time the attention backward (attn_bwd) instead of the forward; "
-                         "varlen: the forward on a variable-length causal GQA prefill batch")
+                         "varlen: the forward on a variable-length causal GQA prefill batch; "
+                         "paged: a chunked prefill over a paged K/V cache")
     ap.add_argument("--deterministic", action="store_true",
                     help="with --op bwd: the deterministic backward (dQ summed in key-tile order)")
     return ap.parse_args()
@@ -416,6 +417,92 @@ def run_varlen(args):
     return 0
 
 
+# Chunked prefill over a paged K/V cache: 16 sequences whose caches hold seeded lengths in
+# [2048, 16384] tokens (256-slot pages in a shuffled order), each with its last 512 tokens as
+# the new query chunk (causal, aligned at the end), 32 query heads on 8 K/V heads, d = 128.
+PAGED_SEQS, PAGED_CHUNK, PAGED_PAGE, PAGED_SEED = 16, 512, 256, 10
+
+
+def run_paged(args):
+    """Time attn_fwd_paged on resident inputs.  FLOP per call: 4*d per visible (query, key)
+    pair and head."""
+    import numpy as np
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    dev = torch.device("cuda", 0)
+    import bf16_attention_forward_gb300 as attn
+    attn.load()
+    steps = args.steps if args.steps is not None else 50
+    warmup = max(3, args.warmup if args.warmup is not None else 10)
+    rng = np.random.default_rng(PAGED_SEED)
+    lens_k = rng.integers(2048, 16385, PAGED_SEQS).tolist()
+    need = [-(-n // PAGED_PAGE) for n in lens_k]
+    n_pages = sum(need)
+    H, Hkv, d = VARLEN_H, VARLEN_HKV, VARLEN_D
+    g = torch.Generator(device="cpu").manual_seed(PAGED_SEED)
+    kc = torch.randn((n_pages, PAGED_PAGE, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
+    vc = torch.randn((n_pages, PAGED_PAGE, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
+    order = rng.permutation(n_pages)
+    table = np.zeros((PAGED_SEQS, max(need)), dtype=np.int32)
+    nxt = 0
+    for b, n in enumerate(need):
+        table[b, :n] = order[nxt:nxt + n]
+        nxt += n
+    total_q = PAGED_SEQS * PAGED_CHUNK
+    q = torch.randn((total_q, H, d), generator=g).to(torch.bfloat16).to(dev)
+    o = torch.empty_like(q)
+    cu_q = torch.arange(0, total_q + 1, PAGED_CHUNK, dtype=torch.int32, device=dev)
+    seqlens = torch.tensor(lens_k, dtype=torch.int32, device=dev)
+    bt = torch.as_tensor(table).to(dev)
+    import ctypes
+    a = attn.PagedArgs()
+    a.B, a.H, a.Hkv, a.total_q, a.num_pages, a.page_size, a.max_pages, a.d = \
+        PAGED_SEQS, H, Hkv, total_q, n_pages, PAGED_PAGE, table.shape[1], d
+    ws = torch.empty(int(attn.load().attn_fwd_paged_workspace_size(ctypes.byref(a))), dtype=torch.uint8, device=dev)
+
+    def call():
+        attn.attn_fwd_paged(q, kc, vc, cu_q, seqlens, bt, max_seqlen_q=PAGED_CHUNK, o=o, causal=True, workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0, enabled=not args.no_clocks) as clocks:
+        t0.record()
+        for _ in range(steps):
+            call()
+        t1.record()
+        torch.cuda.synchronize(dev)
+    st, site = attn.device_status()
+    assert st == 0, "device status %d at site %d" % (st, site)
+    ms = t0.elapsed_time(t1) / steps
+    # query i of a chunk sits at position Sk - C + i and sees Sk - C + i + 1 keys
+    pairs = sum(PAGED_CHUNK * n - PAGED_CHUNK * (PAGED_CHUNK - 1) // 2 for n in lens_k)
+    flop = 4 * H * d * pairs
+    value = flop / (ms * 1e-3) / 1e12
+    peak, _, hbm, peak_src = measured_peaks()
+    kv_bytes = 2 * sum(lens_k) * Hkv * d * 2
+    line = {
+        "metric": "attention fwd TFLOPS (4*d per visible pair and head, paged K/V chunked prefill)",
+        "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": steps, "warmup": warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": "paged_chunked_prefill", "sequences": PAGED_SEQS, "cache_lengths": lens_k,
+                   "chunk": PAGED_CHUNK, "page_size": PAGED_PAGE, "pages": n_pages, "H": H, "Hkv": Hkv,
+                   "d": d, "causal": True, "modes": ["rtne"], "flop_per_call": flop,
+                   "kv_bytes_read": kv_bytes,
+                   "step": "one attn_fwd_paged call: the offsets/table/tensor-map preprocessing kernel "
+                           "and the attention kernel",
+                   "l2": "K/V cache %.0f MB > 126 MB L2" % (2 * kc.numel() * 2 / 2**20)},
+        "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
+                     "frac": value / peak, "peak_source": peak_src + " burst bf16 (cuBLAS)",
+                     "timed": "whole call", "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm},
+        "clocks": clocks.summary(),
+        "gpu_launches": 2 * steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -426,6 +513,8 @@ def main():
         return run_backward(args, w)
     if args.op == "varlen":
         return run_varlen(args)
+    if args.op == "paged":
+        return run_paged(args)
 
     import torch.distributed as dist
     if world > 1:

@@ -22,7 +22,8 @@ EXPORTS = ("attn_fwd", "attn_fwd_ws", "attn_fwd_noalloc", "attn_fwd_ex", "attn_f
            "attn_fwd_workspace_size_opts", "attn_fwd_ex_workspace_size", "attn_plan",
            "attn_plan_ex", "attn_get_device_status", "attn_status_string", "attn_version",
            "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_get_device_status",
-           "attn_fwd_varlen", "attn_fwd_varlen_workspace_size")
+           "attn_fwd_varlen", "attn_fwd_varlen_workspace_size", "attn_fwd_paged",
+           "attn_fwd_paged_workspace_size")
 
 
 class AttnError(RuntimeError):
@@ -60,6 +61,15 @@ class VarlenArgs(ctypes.Structure):
                                                "cu_seqlens_k")] + \
                [(n, ctypes.c_int64) for n in ("B", "H", "Hkv", "total_q", "total_k",
                                               "max_seqlen_q", "d")] + \
+               [(n, ctypes.c_int32) for n in ("round_mode", "causal", "reserved", "reserved2")]
+
+
+class PagedArgs(ctypes.Structure):
+    """attn_paged_args_t: the argument set of attn_fwd_paged."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k_cache", "v_cache", "o", "lse", "cu_seqlens_q",
+                                               "seqlens_k", "block_table")] + \
+               [(n, ctypes.c_int64) for n in ("B", "H", "Hkv", "total_q", "num_pages", "page_size",
+                                              "max_pages", "max_seqlen_q", "d")] + \
                [(n, ctypes.c_int32) for n in ("round_mode", "causal", "reserved", "reserved2")]
 
 
@@ -121,6 +131,11 @@ def load(path: str | None = None):
                                         ctypes.c_size_t, vp]
         lib.attn_fwd_varlen_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_varlen_workspace_size.argtypes = [ctypes.POINTER(VarlenArgs)]
+        lib.attn_fwd_paged.restype = i32
+        lib.attn_fwd_paged.argtypes = [ctypes.POINTER(PagedArgs), ctypes.POINTER(Options), vp,
+                                       ctypes.c_size_t, vp]
+        lib.attn_fwd_paged_workspace_size.restype = ctypes.c_size_t
+        lib.attn_fwd_paged_workspace_size.argtypes = [ctypes.POINTER(PagedArgs)]
         lib.attn_plan.restype = i32
         lib.attn_plan.argtypes = [i64] * 6 + [ctypes.POINTER(Options), ctypes.POINTER(Plan)]
         lib.attn_get_device_status.restype = i32
@@ -363,6 +378,70 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int = 0, 
                              ws_bytes, _stream_ptr(stream, q.device))
     if st != 0:
         raise AttnError(st, "attn_fwd_varlen")
+    return (o, lse) if (return_lse or lse is not None) else o
+
+
+def _int32_cuda(t, name, dim):
+    import torch
+    if (not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or not t.is_cuda
+            or not t.is_contiguous() or t.dim() != dim):
+        raise ValueError("%s must be a contiguous CUDA int32 tensor of %d dimension(s)" % (name, dim))
+
+
+def attn_fwd_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table, max_seqlen_q: int = 0,
+                   o=None, lse=None, round: str = "rtne", causal: bool = False,
+                   return_lse: bool = False, stream=None, workspace=None, max_ctas: int = 0,
+                   wait_limit_ms: int = 0, events=None):
+    """Attention of packed queries over a paged K/V cache.
+
+    ``q``: [total_q, H, d]; ``k_cache``/``v_cache``: [num_pages, page_size, Hkv, d] (CUDA bf16,
+    contiguous; page_size a multiple of 128); ``cu_seqlens_q``: CUDA int32 [B + 1];
+    ``seqlens_k``: CUDA int32 [B] keys per sequence; ``block_table``: CUDA int32
+    [B, max_pages], the physical page of each sequence's page (entries past its last used
+    page are not read).  Key j of sequence b is slot j % page_size of page
+    block_table[b, j // page_size].  Causal: aligned at each sequence's last query and key.
+    Bad offsets, lengths or page indices write nothing and are reported by
+    :func:`device_status`.  Returns ``o`` or ``(o, lse)`` (lse: fp32 [H, total_q]).
+    """
+    import torch
+    if round not in MODES:
+        raise ValueError("round must be rtne/rtna/rtz")
+    _check_tensors(q, k_cache, v_cache)
+    if (q.dim() != 3 or k_cache.dim() != 4 or tuple(k_cache.shape) != tuple(v_cache.shape)
+            or q.shape[2] != k_cache.shape[3]):
+        raise ValueError("q must be [total_q, H, d] and k_cache, v_cache [num_pages, page_size, Hkv, d]")
+    _int32_cuda(cu_seqlens_q, "cu_seqlens_q", 1)
+    _int32_cuda(seqlens_k, "seqlens_k", 1)
+    _int32_cuda(block_table, "block_table", 2)
+    B = cu_seqlens_q.numel() - 1
+    if B < 1 or seqlens_k.numel() != B or block_table.shape[0] != B:
+        raise ValueError("cu_seqlens_q needs B + 1 offsets, seqlens_k B lengths, block_table B rows")
+    if o is None:
+        o = torch.empty_like(q)
+    _check_out(o, q)
+    if lse is None and return_lse:
+        lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous()
+                            or lse.numel() != q.shape[0] * q.shape[1]):
+        raise ValueError("lse must be a contiguous CUDA fp32 tensor of H*total_q elements")
+    a = PagedArgs()
+    a.q, a.k_cache, a.v_cache, a.o = q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o.data_ptr()
+    a.lse = None if lse is None else lse.data_ptr()
+    a.cu_seqlens_q, a.seqlens_k, a.block_table = (cu_seqlens_q.data_ptr(), seqlens_k.data_ptr(),
+                                                  block_table.data_ptr())
+    a.B, a.H, a.Hkv, a.total_q = B, q.shape[1], k_cache.shape[2], q.shape[0]
+    a.num_pages, a.page_size, a.max_pages = k_cache.shape[0], k_cache.shape[1], block_table.shape[1]
+    a.max_seqlen_q, a.d = int(max_seqlen_q), q.shape[2]
+    a.round_mode, a.causal = MODES[round], int(causal)
+    opts = _opts(0, max_ctas, wait_limit_ms, events)
+    lib = load()
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = lib.attn_fwd_paged(ctypes.byref(a), ctypes.byref(opts) if opts else None, ws_ptr,
+                            ws_bytes, _stream_ptr(stream, q.device))
+    if st != 0:
+        raise AttnError(st, "attn_fwd_paged")
     return (o, lse) if (return_lse or lse is not None) else o
 
 

@@ -140,8 +140,16 @@ struct FwdParams {
     const int2* vl_blocks;
     const int* vl_n_items;
     const int* cu_q;       // [B + 1] query row offsets
-    const int* cu_k;       // [B + 1] key row offsets
+    const int* cu_k;       // [B + 1] key row offsets (unpaged)
     long long total_q;     // LSE row stride ([H][total_q])
+    // paged K/V (a variable-length batch whose keys sit in cache pages): key j of sequence b
+    // is slot j % page_size of page block_table[b * max_pages + j / page_size]; full pages
+    // load through the whole-cache maps (kmap, vmap), the last page through the sequence's
+    // own maps (vl_maps[4 b + 1, 2], narrowed to its used slots)
+    int paged;
+    const int* seqlens_k;  // [B]
+    const int* block_table;
+    int page_size, max_pages;
 };
 
 struct Item {
@@ -172,9 +180,9 @@ __device__ __forceinline__ Item decode_varlen_item(const FwdParams& p, int k) {
     it.b = e.x;
     it.qb = e.y;
     it.h = k % p.H;
-    const int q0 = __ldg(p.cu_q + it.b), k0 = __ldg(p.cu_k + it.b);
+    const int q0 = __ldg(p.cu_q + it.b);
     it.sq = __ldg(p.cu_q + it.b + 1) - q0;
-    it.skv = __ldg(p.cu_k + it.b + 1) - k0;
+    it.skv = p.paged ? __ldg(p.seqlens_k + it.b) : __ldg(p.cu_k + it.b + 1) - __ldg(p.cu_k + it.b);
     it.q0 = q0;
     it.causal_off = it.skv - it.sq;
     it.kv_begin = 0;
@@ -425,12 +433,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                             break;
                         ptx::mbar_arrive_expect_tx(bar(G::kBarFull + slot), G::kTileBytes);
                         const void* map = kv ? vmp : kmp;
+                        int krow = j * kBN;
+                        if constexpr (kVarlen) {
+                            if (p.paged) {
+                                // the tile lies in one page: the last one through the sequence's
+                                // narrowed map, the others through the whole-cache map
+                                const int pg = krow / p.page_size, slot0 = krow - pg * p.page_size;
+                                if (pg == (it.skv - 1) / p.page_size) {
+                                    krow = slot0;
+                                } else {
+                                    map = kv ? (const void*)&vmap : (const void*)&kmap;
+                                    krow = __ldg(p.block_table + (long long)it.b * p.max_pages + pg) * p.page_size + slot0;
+                                }
+                            }
+                        }
                         for (int c = 0; c < G::kChunks; ++c) {
                             const uint32_t dst = sbase + G::kSmemRing + slot * G::kTileBytes + c * kChunkBytes;
                             if (kVarlen || p.bshd)
-                                ptx::tma_load_4d(dst, map, bar(G::kBarFull + slot), c * 64, it.hk, j * kBN, bc, pol_kv);
+                                ptx::tma_load_4d(dst, map, bar(G::kBarFull + slot), c * 64, it.hk, krow, bc, pol_kv);
                             else
-                                ptx::tma_load_4d(dst, map, bar(G::kBarFull + slot), c * 64, j * kBN, it.hk, bc, pol_kv);
+                                ptx::tma_load_4d(dst, map, bar(G::kBarFull + slot), c * 64, krow, it.hk, bc, pol_kv);
                         }
                     }
                 }
@@ -1441,7 +1463,10 @@ constexpr int kCostBuckets = 4096;
 
 struct VarlenPrep {
     const int* cu_q;
-    const int* cu_k;
+    const int* cu_k;                       // unpaged: key offsets
+    const int* seqlens_k;                  // paged: keys per sequence
+    const int* block_table;                // paged: [B][max_pages]
+    int paged, page_size, max_pages, num_pages;
     int B, H, causal;
     long long total_q, total_k;
     long long q_row_bytes, kv_row_bytes;   // bytes per token row: H*d*2, Hkv*d*2
@@ -1481,6 +1506,11 @@ __device__ __forceinline__ int block_cost(int qb, int sq, int skv, int causal) {
     return tiles < kCostBuckets - 1 ? tiles : kCostBuckets - 1;
 }
 
+// keys of sequence b (its own rows, or the used slots of its pages)
+__device__ __forceinline__ int seq_keys(const VarlenPrep& a, int b) {
+    return a.paged ? a.seqlens_k[b] : a.cu_k[b + 1] - a.cu_k[b];
+}
+
 __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_constant__ CUtensorMap qmap,
                                                                 const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
@@ -1496,11 +1526,27 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int nthreads = blockDim.x;
     if (tid == 0)
-        bad = (a.cu_q[0] < 0 || a.cu_k[0] < 0 || a.cu_q[a.B] > a.total_q || a.cu_k[a.B] > a.total_k) ? 1 : 0;
+        bad = (a.cu_q[0] < 0 || a.cu_q[a.B] > a.total_q ||
+               (!a.paged && (a.cu_k[0] < 0 || a.cu_k[a.B] > a.total_k))) ? 1 : 0;
     for (int i = tid; i < kCostBuckets; i += nthreads) bucket[i] = 0;
     __syncthreads();
-    for (int b = tid; b < a.B; b += nthreads)
-        if (a.cu_q[b + 1] < a.cu_q[b] || a.cu_k[b + 1] < a.cu_k[b]) bad = 1;
+    for (int b = tid; b < a.B; b += nthreads) {
+        if (a.cu_q[b + 1] < a.cu_q[b]) bad = 1;
+        if (!a.paged) {
+            if (a.cu_k[b + 1] < a.cu_k[b]) bad = 1;
+        } else {
+            const int skv = a.seqlens_k[b];
+            if (skv < 0 || skv > a.max_pages * a.page_size) {
+                bad = 1;
+            } else {
+                const int npg = (skv + a.page_size - 1) / a.page_size;
+                for (int pg = 0; pg < npg; ++pg) {
+                    const int phys = a.block_table[(long long)b * a.max_pages + pg];
+                    if (phys < 0 || phys >= a.num_pages) bad = 1;
+                }
+            }
+        }
+    }
     __syncthreads();
     if (bad) {
         if (tid == 0) {
@@ -1515,17 +1561,27 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
         int sq = 0, skv = 0;
         if (b < a.B) {
             sq = a.cu_q[b + 1] - a.cu_q[b];
-            skv = a.cu_k[b + 1] - a.cu_k[b];
+            skv = seq_keys(a, b);
             if (sq > 0 && skv > 0) {
                 CUtensorMap* m = a.maps + 4 * (long long)b;
-                const long long q0 = a.cu_q[b], k0 = a.cu_k[b];
+                const long long q0 = a.cu_q[b];
+                // K/V rows: the sequence's own, or (paged) the used slots of its last page
+                long long k0 = 0;
+                int krows = skv;
+                if (a.paged) {
+                    const int last = (skv - 1) / a.page_size;
+                    k0 = (long long)a.block_table[(long long)b * a.max_pages + last] * a.page_size;
+                    krows = skv - last * a.page_size;
+                } else {
+                    k0 = a.cu_k[b];
+                }
                 copy_map(m + 0, &qmap);
                 copy_map(m + 1, &kmap);
                 copy_map(m + 2, &vmap);
                 copy_map(m + 3, &omap);
                 narrow_map(m + 0, a.q + q0 * a.q_row_bytes, sq);
-                narrow_map(m + 1, a.k + k0 * a.kv_row_bytes, skv);
-                narrow_map(m + 2, a.v + k0 * a.kv_row_bytes, skv);
+                narrow_map(m + 1, a.k + k0 * a.kv_row_bytes, krows);
+                narrow_map(m + 2, a.v + k0 * a.kv_row_bytes, krows);
                 narrow_map(m + 3, a.o + q0 * a.q_row_bytes, sq);
                 const int nqb = (sq + kUnitRows - 1) / kUnitRows;
                 for (int qb = 0; qb < nqb; ++qb) atomicAdd(&bucket[block_cost(qb, sq, skv, a.causal)], 1);
@@ -1583,7 +1639,7 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
     __syncthreads();
     // scatter every pair to its bucket's next position
     for (int b = tid; b < a.B; b += nthreads) {
-        const int sq = a.cu_q[b + 1] - a.cu_q[b], skv = a.cu_k[b + 1] - a.cu_k[b];
+        const int sq = a.cu_q[b + 1] - a.cu_q[b], skv = seq_keys(a, b);
         if (sq <= 0 || skv <= 0) continue;
         const int nqb = (sq + kUnitRows - 1) / kUnitRows;
         for (int qb = 0; qb < nqb; ++qb) {
@@ -1973,38 +2029,87 @@ int run(const attn_args_t& a, const attn_options_t* opts, void* workspace, size_
 }
 
 // ---------------------------------------------------------------- variable-length batches
-int validate_varlen_shape(const attn_varlen_args_t& a, const attn_options_t* opts) {
-    if (a.B < 1 || a.H < 1 || a.Hkv < 1 || a.total_q < 0 || a.total_k < 0 || a.max_seqlen_q < 0 || a.d < 1)
+// The arguments of attn_fwd_varlen and attn_fwd_paged in one form.  kv_rows: token rows of
+// the K/V tensors (total_k, or num_pages * page_size for a paged cache).
+struct SeqBatch {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    const int32_t* seqlens_k;
+    const int32_t* block_table;
+    int64_t B, H, Hkv, total_q, kv_rows, max_seqlen_q, d;
+    int64_t paged, page_size, max_pages, num_pages;
+    int32_t round_mode, causal, reserved, reserved2;
+};
+
+SeqBatch from_varlen(const attn_varlen_args_t& a) {
+    SeqBatch c;
+    memset(&c, 0, sizeof c);
+    c.q = a.q; c.k = a.k; c.v = a.v; c.o = a.o; c.lse = a.lse;
+    c.cu_q = a.cu_seqlens_q; c.cu_k = a.cu_seqlens_k;
+    c.B = a.B; c.H = a.H; c.Hkv = a.Hkv; c.total_q = a.total_q; c.kv_rows = a.total_k;
+    c.max_seqlen_q = a.max_seqlen_q; c.d = a.d;
+    c.round_mode = a.round_mode; c.causal = a.causal; c.reserved = a.reserved; c.reserved2 = a.reserved2;
+    return c;
+}
+
+SeqBatch from_paged(const attn_paged_args_t& a) {
+    SeqBatch c;
+    memset(&c, 0, sizeof c);
+    c.q = a.q; c.k = a.k_cache; c.v = a.v_cache; c.o = a.o; c.lse = a.lse;
+    c.cu_q = a.cu_seqlens_q; c.seqlens_k = a.seqlens_k; c.block_table = a.block_table;
+    c.B = a.B; c.H = a.H; c.Hkv = a.Hkv; c.total_q = a.total_q;
+    c.kv_rows = a.num_pages * a.page_size;
+    c.max_seqlen_q = a.max_seqlen_q; c.d = a.d;
+    c.paged = 1; c.page_size = a.page_size; c.max_pages = a.max_pages; c.num_pages = a.num_pages;
+    c.round_mode = a.round_mode; c.causal = a.causal; c.reserved = a.reserved; c.reserved2 = a.reserved2;
+    return c;
+}
+
+int validate_seq_shape(const SeqBatch& a, const attn_options_t* opts) {
+    if (a.B < 1 || a.H < 1 || a.Hkv < 1 || a.total_q < 0 || a.kv_rows < 0 || a.max_seqlen_q < 0 || a.d < 1)
         return ATTN_ERR_INVALID_ARG;
     if (a.H % a.Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (a.round_mode < ATTN_ROUND_RTNE || a.round_mode > ATTN_ROUND_RTZ) return ATTN_ERR_INVALID_ARG;
     if ((a.causal != 0 && a.causal != 1) || a.reserved != 0 || a.reserved2 != 0) return ATTN_ERR_INVALID_ARG;
+    if (a.paged && (a.num_pages < 1 || a.max_pages < 1 || a.page_size < kBN || a.page_size % kBN != 0))
+        return ATTN_ERR_INVALID_ARG;
     if (a.d != 128 && a.d != 64) return ATTN_ERR_UNSUPPORTED;
     if (opts && opts->force_splits > 1) return ATTN_ERR_UNSUPPORTED;
     if (opts && opts->test_hooks != 0) return ATTN_ERR_INVALID_ARG;
     // offsets are int32; token rows, item indices and TMA coordinates stay below 2^30
     const int64_t lim = (int64_t)1 << 30;
-    if (a.total_q > lim || a.total_k > lim || a.B > lim || a.H > lim) return ATTN_ERR_UNSUPPORTED;
+    if (a.total_q > lim || a.kv_rows > lim || a.B > lim || a.H > lim) return ATTN_ERR_UNSUPPORTED;
+    if (a.paged && (a.num_pages > lim || a.page_size > lim || a.max_pages > lim ||
+                    a.max_pages * a.page_size > lim || a.B * a.max_pages > lim))
+        return ATTN_ERR_UNSUPPORTED;
     if (a.H * (a.total_q / kUnitRows + a.B) > lim) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
 
 // (sequence, query block) pairs a batch can hold: sum_b ceil(Sq_b / 256) <= total_q / 256 + B
-int64_t varlen_max_blocks(const attn_varlen_args_t& a) { return a.total_q / kUnitRows + a.B; }
+int64_t seq_max_blocks(const SeqBatch& a) { return a.total_q / kUnitRows + a.B; }
 
 // workspace: per-sequence tensor maps (128-byte aligned inside it), the item count, the pairs
-size_t varlen_ws_bytes(const attn_varlen_args_t& a) {
-    return 128 + (size_t)a.B * 4 * sizeof(CUtensorMap) + 16 + (size_t)varlen_max_blocks(a) * sizeof(int2);
+size_t seq_ws_bytes(const SeqBatch& a) {
+    return 128 + (size_t)a.B * 4 * sizeof(CUtensorMap) + 16 + (size_t)seq_max_blocks(a) * sizeof(int2);
 }
 
-int run_varlen(const attn_varlen_args_t& a, const attn_options_t* opts, void* workspace, size_t workspace_bytes,
-               cudaStream_t stream) {
-    int st = validate_varlen_shape(a, opts);
+int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream) {
+    int st = validate_seq_shape(a, opts);
     if (st != ATTN_OK) return st;
-    if (!a.q || !a.k || !a.v || !a.o || !a.cu_seqlens_q || !a.cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+    if (!a.q || !a.k || !a.v || !a.o || !a.cu_q) return ATTN_ERR_INVALID_ARG;
+    if (a.paged ? (!a.seqlens_k || !a.block_table) : !a.cu_k) return ATTN_ERR_INVALID_ARG;
     if (((uintptr_t)a.q | (uintptr_t)a.k | (uintptr_t)a.v | (uintptr_t)a.o) & 15u) return ATTN_ERR_MISALIGNED;
-    if (((uintptr_t)a.lse | (uintptr_t)a.cu_seqlens_q | (uintptr_t)a.cu_seqlens_k) & 3u) return ATTN_ERR_MISALIGNED;
-    const uintptr_t qbytes = (uintptr_t)(a.total_q * a.H * a.d * 2), kvbytes = (uintptr_t)(a.total_k * a.Hkv * a.d * 2);
+    if (((uintptr_t)a.lse | (uintptr_t)a.cu_q | (uintptr_t)a.cu_k | (uintptr_t)a.seqlens_k |
+         (uintptr_t)a.block_table) & 3u)
+        return ATTN_ERR_MISALIGNED;
+    const uintptr_t qbytes = (uintptr_t)(a.total_q * a.H * a.d * 2), kvbytes = (uintptr_t)(a.kv_rows * a.Hkv * a.d * 2);
     auto overlap = [](uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; };
     const uintptr_t ob = (uintptr_t)a.o, oe = ob + qbytes, qb = (uintptr_t)a.q, qe = qb + qbytes;
     const uintptr_t kb = (uintptr_t)a.k, ke = kb + kvbytes, vb = (uintptr_t)a.v, ve = vb + kvbytes;
@@ -2016,7 +2121,7 @@ int run_varlen(const attn_varlen_args_t& a, const attn_options_t* opts, void* wo
     }
     DeviceInfo* di = nullptr;
     if ((st = device_info(&di)) != ATTN_OK) return st;
-    const size_t need = varlen_ws_bytes(a);
+    const size_t need = seq_ws_bytes(a);
     void* ws = nullptr;
     if (workspace) {
         if (workspace_bytes < need) return ATTN_ERR_WORKSPACE;
@@ -2031,8 +2136,9 @@ int run_varlen(const attn_varlen_args_t& a, const attn_options_t* opts, void* wo
         return ATTN_ERR_ALIAS;
     const int64_t d = a.d;
     // whole-tensor maps (token-major, one batch), which the preprocessing kernel narrows to
-    // each sequence; a tensor with no rows gets a one-row map that no item ever uses
-    const int64_t tq = a.total_q > 0 ? a.total_q : 1, tk = a.total_k > 0 ? a.total_k : 1;
+    // each sequence (a paged cache's maps also serve its full pages as they are); a tensor
+    // with no rows gets a one-row map that no item ever uses
+    const int64_t tq = a.total_q > 0 ? a.total_q : 1, tk = a.kv_rows > 0 ? a.kv_rows : 1;
     CUtensorMap qm, km, vm, om;
     if (!encode_map(&qm, a.q, 1, a.H, tq, d, true) || !encode_map(&km, a.k, 1, a.Hkv, tk, d, true) ||
         !encode_map(&vm, a.v, 1, a.Hkv, tk, d, true) || !encode_map(&om, a.o, 1, a.H, tq, d, true, kStageRowsPerWarp))
@@ -2042,13 +2148,19 @@ int run_varlen(const attn_varlen_args_t& a, const attn_options_t* opts, void* wo
     int2* blocks = reinterpret_cast<int2*>(reinterpret_cast<char*>(n_items) + 16);
     VarlenPrep vp;
     memset(&vp, 0, sizeof vp);
-    vp.cu_q = a.cu_seqlens_q;
-    vp.cu_k = a.cu_seqlens_k;
+    vp.cu_q = a.cu_q;
+    vp.cu_k = a.cu_k;
+    vp.seqlens_k = a.seqlens_k;
+    vp.block_table = a.block_table;
+    vp.paged = (int)a.paged;
+    vp.page_size = (int)a.page_size;
+    vp.max_pages = (int)a.max_pages;
+    vp.num_pages = (int)a.num_pages;
     vp.B = (int)a.B;
     vp.H = (int)a.H;
     vp.causal = a.causal;
     vp.total_q = a.total_q;
-    vp.total_k = a.total_k;
+    vp.total_k = a.kv_rows;
     vp.q_row_bytes = a.H * d * 2;
     vp.kv_row_bytes = a.Hkv * d * 2;
     vp.q = reinterpret_cast<const char*>(a.q);
@@ -2078,9 +2190,14 @@ int run_varlen(const attn_varlen_args_t& a, const attn_options_t* opts, void* wo
     p.vl_maps = maps;
     p.vl_blocks = blocks;
     p.vl_n_items = n_items;
-    p.cu_q = a.cu_seqlens_q;
-    p.cu_k = a.cu_seqlens_k;
+    p.cu_q = a.cu_q;
+    p.cu_k = a.cu_k;
     p.total_q = a.total_q;
+    p.paged = (int)a.paged;
+    p.seqlens_k = a.seqlens_k;
+    p.block_table = a.block_table;
+    p.page_size = (int)a.page_size;
+    p.max_pages = (int)a.max_pages;
 
     int64_t G = di->sms;
     if (opts && opts->max_ctas > 0 && opts->max_ctas < G) G = opts->max_ctas;
@@ -2171,14 +2288,27 @@ size_t attn_fwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Skv, in
 }
 
 size_t attn_fwd_varlen_workspace_size(const attn_varlen_args_t* args) {
-    if (!args || validate_varlen_shape(*args, nullptr) != ATTN_OK) return 0;
-    return varlen_ws_bytes(*args);
+    if (!args) return 0;
+    const SeqBatch c = from_varlen(*args);
+    return validate_seq_shape(c, nullptr) == ATTN_OK ? seq_ws_bytes(c) : 0;
 }
 
 int attn_fwd_varlen(const attn_varlen_args_t* args, const attn_options_t* opts, void* workspace,
                     size_t workspace_bytes, attn_stream_t stream) {
     if (!args) return ATTN_ERR_INVALID_ARG;
-    return run_varlen(*args, opts, workspace, workspace_bytes, (cudaStream_t)stream);
+    return run_seq_batch(from_varlen(*args), opts, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+size_t attn_fwd_paged_workspace_size(const attn_paged_args_t* args) {
+    if (!args) return 0;
+    const SeqBatch c = from_paged(*args);
+    return validate_seq_shape(c, nullptr) == ATTN_OK ? seq_ws_bytes(c) : 0;
+}
+
+int attn_fwd_paged(const attn_paged_args_t* args, const attn_options_t* opts, void* workspace,
+                   size_t workspace_bytes, attn_stream_t stream) {
+    if (!args) return ATTN_ERR_INVALID_ARG;
+    return run_seq_batch(from_paged(*args), opts, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 int attn_fwd_ex(const attn_args_t* args, const attn_options_t* opts, void* workspace, size_t workspace_bytes,

@@ -94,7 +94,8 @@ typedef struct {
 #define ATTN_TEST_WITHHOLD_O_READY 1
 #define ATTN_SITE_O_READY 7
 #define ATTN_BWD_SITE_DKV_READY 9
-/* Site reported with ATTN_ERR_INVALID_ARG when attn_fwd_varlen's offsets are inconsistent. */
+/* Site reported with ATTN_ERR_INVALID_ARG when attn_fwd_varlen's offsets, or attn_fwd_paged's
+ * offsets, lengths or page indices, are inconsistent. */
 #define ATTN_SITE_SEQLENS 13
 
 /* The work split chosen for a shape (host only, launches nothing). */
@@ -260,6 +261,44 @@ typedef struct {
 size_t attn_fwd_varlen_workspace_size(const attn_varlen_args_t* args);
 int attn_fwd_varlen(const attn_varlen_args_t* args, const attn_options_t* opts, void* workspace,
                     size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * Paged K/V -- "AMD zverejnilo postup pre custom diffusion attention kernel vo FlyDSL na ROCm",
+ * section "Co AMD konkretne popisuje": attention kernels need flexible KV-cache layouts, a
+ * paged cache among them.  Queries are packed as in attn_fwd_varlen; the keys and values of
+ * sequence b are the first seqlens_k[b] token slots of its pages: key j sits in slot
+ * j % page_size of physical page block_table[b * max_pages + j / page_size].  Row i of
+ * sequence b is attention over those keys, exactly as attn_fwd_varlen on the gathered keys
+ * (causal: aligned at the sequence's last query and key, so a chunk of new queries sees the
+ * whole cache before it).
+ *   q, o, lse     as in attn_fwd_varlen (packed [total_q][H][d]; lse [H][total_q])
+ *   k_cache, v_cache  bf16 [num_pages][page_size][Hkv][d]
+ *   cu_seqlens_q  device int32 [B + 1], as in attn_fwd_varlen
+ *   seqlens_k     device int32 [B]: keys per sequence, 0 .. max_pages * page_size
+ *   block_table   device int32 [B][max_pages]; entries past a sequence's last used page are
+ *                 not read.  Pages may be shared between sequences.
+ *   page_size     a multiple of 128 (a key tile never straddles pages)
+ * Checked on the device: bad query offsets, lengths or page indices (outside 0 ..
+ * num_pages - 1) write no output and report ATTN_ERR_INVALID_ARG at ATTN_SITE_SEQLENS.  Slots
+ * of a sequence's last page past its length are never read as keys (they read as zeros), so
+ * stale values there cannot reach the output.  Workspace as attn_fwd_varlen.
+ */
+typedef struct {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    void* o;
+    float* lse;
+    const int32_t* cu_seqlens_q;
+    const int32_t* seqlens_k;
+    const int32_t* block_table;
+    int64_t B, H, Hkv, total_q, num_pages, page_size, max_pages, max_seqlen_q, d;
+    int32_t round_mode, causal, reserved, reserved2;
+} attn_paged_args_t;
+
+size_t attn_fwd_paged_workspace_size(const attn_paged_args_t* args);
+int attn_fwd_paged(const attn_paged_args_t* args, const attn_options_t* opts, void* workspace,
+                   size_t workspace_bytes, attn_stream_t stream);
 
 /*
  * attn_get_device_status -- synchronizes `stream`, then reads and clears the current

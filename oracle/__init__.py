@@ -227,6 +227,42 @@ def attention_varlen(q, k, v, cu_q, cu_k, mode: str = "rtne", causal: bool = Fal
     return out
 
 
+def gather_pages(k_cache, v_cache, seqlens_k, block_table):
+    """The keys and values of a paged cache, gathered in order: sequence b's key j is slot
+    j % page_size of page block_table[b][j // page_size] of the [num_pages, page_size, Hkv,
+    d] caches.  Returns (k, v) packed [sum(seqlens_k), Hkv, d] and the key offsets cu_k."""
+    kb, vb = _as_bits(k_cache), _as_bits(v_cache)
+    P = kb.shape[1]
+    table = np.asarray(block_table)
+    ks, vs, cu_k = [], [], [0]
+    for b, n in enumerate(int(x) for x in np.asarray(seqlens_k).reshape(-1)):
+        for j in range(n):
+            page = int(table[b][j // P])
+            if not 0 <= page < kb.shape[0]:
+                raise ValueError("sequence %d: page index %d out of range" % (b, page))
+            ks.append(kb[page, j % P])
+            vs.append(vb[page, j % P])
+        cu_k.append(cu_k[-1] + n)
+    shape = (0,) + kb.shape[2:]
+    k = np.stack(ks) if ks else np.zeros(shape, dtype=np.uint16)
+    v = np.stack(vs) if vs else np.zeros(shape, dtype=np.uint16)
+    return k, v, np.asarray(cu_k)
+
+
+def attention_paged(q, k_cache, v_cache, cu_q, seqlens_k, block_table, mode: str = "rtne",
+                    causal: bool = False, want_a: bool = False, want_lse: bool = False, lib=None) -> dict:
+    """Oracle attention of packed queries over a paged K/V cache.
+
+    "AMD zverejnilo postup pre custom diffusion attention kernel vo FlyDSL na ROCm" (section
+    on what AMD describes) names a paged KV cache among the layouts an attention kernel has to
+    take.  The plain reading: the cache only says where each key and value lives, so the
+    result is :func:`attention_varlen` over the keys gathered in order (:func:`gather_pages`).
+    """
+    k, v, cu_k = gather_pages(k_cache, v_cache, seqlens_k, block_table)
+    return attention_varlen(q, k, v, cu_q, cu_k, mode, causal=causal, want_a=want_a,
+                            want_lse=want_lse, lib=lib)
+
+
 def round_bf16(x, mode: str = "rtne", lib=None) -> np.ndarray:
     """Round float64 values to bf16 bit patterns with the oracle's rounding rule."""
     lib = lib or load()

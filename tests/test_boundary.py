@@ -268,3 +268,42 @@ def test_varlen_workspace_size(lib):
         assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(a)) == want, B
     assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(varlen_args(B=0))) == 0
     assert lib.attn_fwd_varlen_workspace_size(None) == 0
+
+
+PG = 1 << 24   # fake pointers for the paged calls, far enough apart for their cache sizes
+
+
+def paged_args(**kw):
+    a = attn.PagedArgs()
+    a.q, a.k_cache, a.v_cache, a.o = PG, 2 * PG, 3 * PG, 4 * PG
+    a.cu_seqlens_q, a.seqlens_k, a.block_table = 5 * PG, 6 * PG, 7 * PG
+    a.B, a.H, a.Hkv, a.total_q, a.num_pages, a.page_size, a.max_pages, a.max_seqlen_q, a.d = \
+        2, 2, 1, 16, 4, 128, 2, 0, 128
+    for k_, v_ in kw.items():
+        setattr(a, k_, v_)
+    return a
+
+
+def test_paged_argument_errors(lib):
+    """attn_fwd_paged checks its arguments before any device call, as attn_fwd_varlen does,
+    plus the cache geometry: at least one page, a page size that is a positive multiple of 128,
+    at least one page per sequence in the table, and int32-safe sizes."""
+    def run(**kw):
+        return lib.attn_fwd_paged(ctypes.byref(paged_args(**kw)), None, None, 0, None)
+    assert lib.attn_fwd_paged(None, None, None, 0, None) == 1
+    assert run() == 5
+    assert run(page_size=256, d=64, causal=1) == 5
+    for bad in ({"num_pages": 0}, {"page_size": 0}, {"page_size": 64}, {"page_size": 200}, {"max_pages": 0},
+                {"seqlens_k": 0}, {"block_table": 0}, {"cu_seqlens_q": 0}, {"k_cache": 0}, {"B": 0},
+                {"Hkv": 3}, {"reserved": 1}):
+        assert run(**bad) == 1, bad
+    assert run(max_pages=(1 << 23) + 1) == 2
+    assert run(num_pages=(1 << 23) + 1) == 2
+    assert run(block_table=7 * PG + 2) == 3
+    assert run(o=2 * PG + 4096) == 4     # o overlaps the K cache
+
+
+def test_paged_workspace_size(lib):
+    a = paged_args(B=3, total_q=1000)
+    assert lib.attn_fwd_paged_workspace_size(ctypes.byref(a)) == 128 + 3 * 512 + 16 + (1000 // 256 + 3) * 8
+    assert lib.attn_fwd_paged_workspace_size(ctypes.byref(paged_args(page_size=100))) == 0

@@ -113,3 +113,82 @@ def test_rejects_bad_offsets():
     for cu_q, cu_k in (([0, 5, 3], [0, 4, 8]), ([0, 9], [0, 8]), ([0, 8], [-1, 8])):
         with pytest.raises(ValueError):
             oracle.attention_varlen(q, k, v, cu_q, cu_k)
+
+
+# --------------------------------------------------------------------------- paged K/V
+# oracle.attention_paged gathers each sequence's keys from the cache pages and runs the
+# varlen oracle; pinned by: pages laid out in order equal the contiguous keys, a permutation
+# of the physical pages (with the table following it) changes nothing, values outside the
+# used slots cannot matter, and shared pages behave as copies.
+
+def _paged_from_contiguous(k, v, lens, P, perm=None, fill=None):
+    """Cache pages holding each sequence's keys in order (sequence after sequence, each
+    starting a new page), physical pages renumbered by `perm`; unused slots set to `fill`."""
+    Hkv, d = k.shape[1], k.shape[2]
+    pages, table, row = [], [], 0
+    maxp = max(1, max(-(-n // P) for n in lens))
+    for n in lens:
+        ids = []
+        for p0 in range(0, n, P):
+            page = torch.zeros((P, Hkv, d), dtype=torch.bfloat16)
+            if fill is not None:
+                page.view(torch.int16).fill_(fill)
+            m = min(P, n - p0)
+            page[:m] = k[row + p0: row + p0 + m]
+            vpage = page.clone()
+            vpage[:m] = v[row + p0: row + p0 + m]
+            ids.append(len(pages))
+            pages.append((page, vpage))
+        row += n
+        table.append(ids + [0] * (maxp - len(ids)))
+    order = list(range(len(pages))) if perm is None else perm
+    inv = {old: new for new, old in enumerate(order)}
+    kc = torch.stack([pages[o][0] for o in order])
+    vc = torch.stack([pages[o][1] for o in order])
+    table = [[inv[i] if j < -(-lens[b] // P) else 0 for j, i in enumerate(t)] for b, t in enumerate(table)]
+    return kc, vc, np.asarray(table, dtype=np.int32)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_paged_in_order_equals_contiguous(causal):
+    H, Hkv, d, P = 2, 1, 64, 128
+    lq, lk = [40, 7, 130], [300, 128, 129]
+    q, k, v = _packed(sum(lq), sum(lk), H, Hkv, d, seed=21)
+    kc, vc, table = _paged_from_contiguous(k, v, lk, P)
+    cu_q, cu_k = np.cumsum([0] + lq), np.cumsum([0] + lk)
+    r = oracle.attention_paged(q, kc, vc, cu_q, lk, table, causal=causal, want_lse=True)
+    want = oracle.attention_varlen(q, k, v, cu_q, cu_k, causal=causal, want_lse=True)
+    assert np.array_equal(r["o_bits"], want["o_bits"]) and np.array_equal(r["lse"], want["lse"])
+
+
+def test_paged_page_permutation_and_stale_slots_change_nothing():
+    H, d, P = 2, 128, 256
+    lq, lk = [100, 33], [600, 257]
+    q, k, v = _packed(sum(lq), sum(lk), H, H, d, seed=22)
+    cu_q = np.cumsum([0] + lq)
+    kc, vc, table = _paged_from_contiguous(k, v, lk, P)
+    base = oracle.attention_paged(q, kc, vc, cu_q, lk, table)
+    n = kc.shape[0]
+    perm = list(np.random.default_rng(5).permutation(n))
+    kc2, vc2, table2 = _paged_from_contiguous(k, v, lk, P, perm=perm, fill=0x7F80)   # +inf past the keys
+    assert not np.array_equal(table, table2)
+    r = oracle.attention_paged(q, kc2, vc2, cu_q, lk, table2)
+    assert np.array_equal(r["o_bits"], base["o_bits"])
+
+
+def test_paged_shared_pages_act_as_copies():
+    H, d, P = 1, 64, 128
+    q, k, v = _packed(20, 256, H, H, d, seed=23)
+    kc, vc, table = _paged_from_contiguous(k, v, [256], P)
+    # two sequences reading the same two pages, the second one only its first 130 keys
+    tbl = np.asarray([[0, 1], [0, 1]], dtype=np.int32)
+    r = oracle.attention_paged(q, kc, vc, [0, 12, 20], [256, 130], tbl)
+    want = oracle.attention_varlen(q, torch.cat([k, k[:130]]), torch.cat([v, v[:130]]), [0, 12, 20], [0, 256, 386])
+    assert np.array_equal(r["o_bits"], want["o_bits"])
+
+
+def test_paged_rejects_pages_out_of_range():
+    q, k, v = _packed(8, 128, 1, 1, 64, seed=24)
+    kc, vc, table = _paged_from_contiguous(k, v, [128], 128)
+    with pytest.raises(ValueError):
+        oracle.attention_paged(q, kc, vc, [0, 8], [128], np.asarray([[1]], dtype=np.int32))
