@@ -225,3 +225,76 @@ def test_rounding_modes_bit_exact_on_exact_means(attn, Skv):
     outs = [run(attn, q, k, v, "bhsd", m).view(torch.int16) for m in MODES]
     if Skv == 2:
         assert not torch.equal(outs[0], outs[1]) and not torch.equal(outs[0], outs[2])
+
+
+def _mode_consistent(z, e, a):
+    """RTZ, RTNE and RTNA bf16 patterns (uint16 arrays) that one fp32 value per element can give:
+    every NaN stored as 0x7FC0 in all three; otherwise one sign, RTNE and RTNA each the RTZ
+    magnitude or the next one up, and RTNE != RTNA only on a tie, where RTNE keeps the even
+    RTZ pattern and RTNA takes the next one.  Returns the number of elements that break it."""
+    z, e, a = (x.astype(np.int32) for x in (z, e, a))
+    nan = lambda x: ((x & 0x7F80) == 0x7F80) & ((x & 0x7F) != 0)
+    any_nan = nan(z) | nan(e) | nan(a)
+    bad = any_nan & ~((z == 0x7FC0) & (e == 0x7FC0) & (a == 0x7FC0))
+    f = ~any_nan
+    zs, es, as_ = z & 0x8000, e & 0x8000, a & 0x8000
+    zm, em, am = z & 0x7FFF, e & 0x7FFF, a & 0x7FFF
+    ok = (zs == es) & (zs == as_) & (em >= zm) & (em <= zm + 1) & (am >= zm) & (am <= zm + 1)
+    ok &= (e == a) | ((em == zm) & (am == zm + 1) & ((zm & 1) == 0))
+    bad |= f & ~ok
+    return int(bad.sum())
+
+
+@pytest.mark.parametrize("case", ["plain", "split", "short", "causal_gqa", "d64", "nonfinite"])
+def test_rounding_modes_share_one_fp32_value(attn, case):
+    # the three modes round the same fp32 result: the path's arithmetic does not depend on the
+    # mode, only the final conversion does (checked element by element on every output)
+    kw = {}
+    if case == "plain":
+        q, k, v = make_qkv(2, 4, 700, 900, 128, "bshd", seed=90, sigma=2.0)
+    elif case == "split":
+        q, k, v = make_qkv(1, 3, 300, 2000, 128, "bshd", seed=91)
+        kw = {"force_splits": 3}
+    elif case == "short":
+        q, k, v = make_qkv(2, 4, 100, 1500, 128, "bshd", seed=92)
+    elif case == "causal_gqa":
+        q, k, v = make_qkv(1, 8, 600, 700, 128, "bshd", seed=93, Hkv=2)
+        kw = {"causal": True}
+    elif case == "d64":
+        q, k, v = make_qkv(2, 2, 513, 385, 64, "bshd", seed=94)
+    else:
+        q, k, v = make_qkv(1, 2, 300, 4096, 128, "bshd", seed=95, sigma=4.0, nonfinite_frac=1e-3)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    outs = [attn.attn_fwd_ex(qd, kd, vd, layout="bshd", round=m, **kw) for m in ("rtz", "rtne", "rtna")]
+    torch.cuda.synchronize()
+    assert attn.device_status()[0] == 0
+    z, e, a = (o.cpu().view(torch.int16).numpy().view(np.uint16) for o in outs)
+    assert _mode_consistent(z, e, a) == 0
+    # the modes do differ (RTZ from RTNE on about half the elements), so the check bites
+    if case != "nonfinite":
+        assert (z != e).mean() > 0.2
+
+
+def test_mode_consistency_check_catches_mismatches():
+    # the checker itself, on hand-made patterns
+    z = np.array([0x3F80, 0x3F80, 0x3F81, 0x7F7F, 0xBF80, 0x7FC0], dtype=np.uint16)
+    e = np.array([0x3F80, 0x3F81, 0x3F82, 0x7F80, 0xBF81, 0x7FC0], dtype=np.uint16)
+    a = np.array([0x3F81, 0x3F81, 0x3F82, 0x7F80, 0xBF81, 0x7FC0], dtype=np.uint16)
+    assert _mode_consistent(z, e, a) == 0
+    assert _mode_consistent(z, e + np.uint16(1), a) > 0          # RTNE two codes above RTZ
+    assert _mode_consistent(z[:1], np.array([0x3F81], np.uint16), np.array([0x3F80], np.uint16)) == 1
+    assert _mode_consistent(np.array([0x3F81], np.uint16), np.array([0x3F81], np.uint16),
+                            np.array([0x3F82], np.uint16)) == 1   # a "tie" on an odd RTZ pattern
+    assert _mode_consistent(np.array([0x7FC1], np.uint16), np.array([0x7FC0], np.uint16),
+                            np.array([0x7FC0], np.uint16)) == 1   # a NaN not in canonical form
+
+
+def test_permuting_keys_with_values_matches_the_oracle(attn):
+    # K/V rows permuted together: the same attention up to the order of the sums; the GPU
+    # result must meet the criteria against the oracle of the original order
+    q, k, v = make_qkv(1, 2, 400, 700, 128, "bshd", seed=96)
+    perm = torch.as_tensor(np.random.default_rng(7).permutation(700))
+    o = run(attn, q, k[:, perm], v[:, perm], "bshd", "rtne")
+    ref = oracle.attention(q, k, v, "bshd", "rtne", want_a=True)
+    res = parity.compare(parity.gpu_rows_bits(o, "bshd"), ref["o_bits"], ref["a"])
+    assert res["ok"], res
