@@ -2,7 +2,9 @@
  * bf16_attn.h -- C ABI of the GB300 (sm_103a) bf16 attention forward library.
  *
  * Operation.  O = softmax(Q K^T / sqrt(d)) V, non-causal, head dimension d = 128 (64 is
- * accepted too), bf16 in and out, fp32 accumulation.  Source: "MoonMath AI open-sources a HIP attention kernel for
+ * accepted too), bf16 in and out, fp32 accumulation.  Extensions below: the causal mask,
+ * grouped K/V heads and the row log-sum-exp (attn_fwd_ex), variable-length batches
+ * (attn_fwd_varlen), a paged K/V cache (attn_fwd_paged) and the backward (attn_bwd).  Source: "MoonMath AI open-sources a HIP attention kernel for
  * AMD MI300X that beats AITER" (news.chathome.org), opening section: attention is the fused
  * softmax(QK^T/sqrt(d))V; the kernel takes BSHD or BHSD tensors without transposes, head
  * dimension fixed at 128, any query and key length including cross-attention; its
@@ -31,7 +33,10 @@
  * writes global memory, so calls are ordered exactly as plain stream launches.  attn_fwd() keeps
  * one lazily grown workspace per device (guarded by a mutex): it may call cudaMalloc the
  * first time a shape needs the split path, so call it once before any CUDA-graph capture,
- * or use attn_fwd_ws() with caller memory.
+ * or use attn_fwd_ws() with caller memory.  attn_fwd_ex, attn_fwd_varlen and attn_fwd_paged
+ * use the same library-owned workspace when given none (the last two always need one); calls
+ * that share it and may run at the same time on the GPU (unordered streams) must be
+ * serialized by the caller, or given workspaces of their own.
  *
  * Errors.  Argument problems are reported synchronously before anything is launched.  A
  * launch failure returns ATTN_ERR_CUDA.  Every wait inside the kernels is bounded: if one

@@ -111,3 +111,34 @@ def test_backward_between_forward_calls(attn, d, det):
     torch.cuda.synchronize()
     assert torch.equal(bits(o3), bits(o3_ref)), "forward read dK before the backward finished"
     assert torch.equal(bits(o4), bits(o4_ref)), "forward read dQ before the backward finished"
+
+
+def test_varlen_calls_chained_on_one_workspace(attn):
+    # back-to-back variable-length calls with different offsets on one workspace: each call's
+    # preprocessing rewrites the tensor maps and the work list that the previous call's
+    # attention kernel reads (it waits for that kernel first), and each call reads the
+    # previous call's output as its Q
+    import ctypes
+    import numpy as np
+    H, d, T = 4, 128, 1300
+    mixes = [[300, 129, 700], [1, 1000, 64, 200], [512, 512], [77, 900, 3, 5, 250, 1]]
+    q, k, v = (t[0].contiguous().cuda() for t in make_qkv(1, H, T, T, d, "bshd", seed=4500))
+    a = attn.VarlenArgs()
+    a.B, a.H, a.Hkv, a.total_q, a.total_k, a.d = max(len(m) for m in mixes), H, H, T, T, d
+    ws = torch.empty(int(attn.load().attn_fwd_varlen_workspace_size(ctypes.byref(a))), dtype=torch.uint8,
+                     device="cuda")
+    cus = [torch.as_tensor(np.cumsum([0] + m).astype(np.int32)).cuda() for m in mixes]
+    outs, ins = [], []
+    x = q
+    for i, cu in enumerate(cus):
+        o = torch.zeros_like(q)
+        attn.attn_fwd_varlen(x, k, v, cu, cu, o=o, causal=bool(i & 1), workspace=ws)
+        outs.append(o)
+        ins.append(x)
+        x = o
+    check_status(attn)
+    for i, cu in enumerate(cus):
+        o = torch.zeros_like(q)
+        attn.attn_fwd_varlen(ins[i], k, v, cu, cu, o=o, causal=bool(i & 1))
+        torch.cuda.synchronize()
+        assert torch.equal(bits(o), bits(outs[i])), "call %d read a stale map, list or input" % i
