@@ -23,7 +23,7 @@ EXPORTS = ("attn_fwd", "attn_fwd_ws", "attn_fwd_noalloc", "attn_fwd_ex", "attn_f
            "attn_plan_ex", "attn_get_device_status", "attn_status_string", "attn_version",
            "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_get_device_status",
            "attn_fwd_varlen", "attn_fwd_varlen_workspace_size", "attn_fwd_paged",
-           "attn_fwd_paged_workspace_size")
+           "attn_fwd_paged_workspace_size", "attn_bwd_varlen", "attn_bwd_varlen_workspace_size")
 
 
 class AttnError(RuntimeError):
@@ -71,6 +71,14 @@ class PagedArgs(ctypes.Structure):
                [(n, ctypes.c_int64) for n in ("B", "H", "Hkv", "total_q", "num_pages", "page_size",
                                               "max_pages", "max_seqlen_q", "d")] + \
                [(n, ctypes.c_int32) for n in ("round_mode", "causal", "reserved", "reserved2")]
+
+
+class BwdVarlenArgs(ctypes.Structure):
+    """attn_bwd_varlen_args_t: the argument set of attn_bwd_varlen."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv",
+                                               "cu_seqlens_q", "cu_seqlens_k")] + \
+               [(n, ctypes.c_int64) for n in ("B", "H", "Hkv", "total_q", "total_k", "d")] + \
+               [(n, ctypes.c_int32) for n in ("causal", "wait_limit_ms", "reserved", "reserved2")]
 
 
 class Plan(ctypes.Structure):
@@ -136,6 +144,10 @@ def load(path: str | None = None):
                                        ctypes.c_size_t, vp]
         lib.attn_fwd_paged_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_paged_workspace_size.argtypes = [ctypes.POINTER(PagedArgs)]
+        lib.attn_bwd_varlen.restype = i32
+        lib.attn_bwd_varlen.argtypes = [ctypes.POINTER(BwdVarlenArgs), vp, ctypes.c_size_t, vp]
+        lib.attn_bwd_varlen_workspace_size.restype = ctypes.c_size_t
+        lib.attn_bwd_varlen_workspace_size.argtypes = [ctypes.POINTER(BwdVarlenArgs)]
         lib.attn_plan.restype = i32
         lib.attn_plan.argtypes = [i64] * 6 + [ctypes.POINTER(Options), ctypes.POINTER(Plan)]
         lib.attn_get_device_status.restype = i32
@@ -506,6 +518,49 @@ def attn_bwd(q, k, v, o, dout, lse, layout: str = "bshd", causal: bool = False, 
     st = lib.attn_bwd(ctypes.byref(a), workspace.data_ptr(), nbytes, _stream_ptr(stream, q.device))
     if st != 0:
         raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_varlen(q, k, v, o, dout, lse, cu_seqlens_q, cu_seqlens_k, causal: bool = False, dq=None,
+                    dk=None, dv=None, workspace=None, stream=None, wait_limit_ms: int = 0):
+    """Gradients (dq, dk, dv) of :func:`attn_fwd_varlen`: q, o, dout [total_q, H, d]; k, v
+    [total_k, Hkv, d]; lse fp32 [H, total_q] (attn_fwd_varlen's); cu_seqlens_q/k CUDA int32
+    [B + 1].  Bad offsets write nothing and are reported by :func:`bwd_device_status`."""
+    import torch
+    _check_tensors(q, k, v)
+    _check_tensors(o, dout, dout)
+    if q.dim() != 3 or k.dim() != 3 or tuple(k.shape) != tuple(v.shape) or q.shape[2] != k.shape[2]:
+        raise ValueError("q must be [total_q, H, d] and k, v [total_k, Hkv, d]")
+    for t in (o, dout):
+        if tuple(t.shape) != tuple(q.shape):
+            raise ValueError("o and dout must be shaped like q")
+    if (lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous()
+            or lse.numel() != q.shape[0] * q.shape[1]):
+        raise ValueError("lse must be a contiguous CUDA fp32 tensor of H*total_q elements")
+    _int32_cuda(cu_seqlens_q, "cu_seqlens_q", 1)
+    _int32_cuda(cu_seqlens_k, "cu_seqlens_k", 1)
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold B + 1 >= 2 offsets")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for g, ref in ((dq, q), (dk, k), (dv, v)):
+        _check_out(g, ref)
+    a = BwdVarlenArgs()
+    a.q, a.k, a.v, a.o, a.dout = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr()
+    a.lse, a.dq, a.dk, a.dv = lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    a.cu_seqlens_q, a.cu_seqlens_k = cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr()
+    a.B, a.H, a.Hkv = cu_seqlens_q.numel() - 1, q.shape[1], k.shape[1]
+    a.total_q, a.total_k, a.d = q.shape[0], k.shape[0], q.shape[2]
+    a.causal, a.wait_limit_ms = int(causal), int(wait_limit_ms)
+    lib = load()
+    need = int(lib.attn_bwd_varlen_workspace_size(ctypes.byref(a)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib.attn_bwd_varlen(ctypes.byref(a), workspace.data_ptr(), nbytes, _stream_ptr(stream, q.device))
+    if st != 0:
+        raise AttnError(st, "attn_bwd_varlen")
     return dq, dk, dv
 
 

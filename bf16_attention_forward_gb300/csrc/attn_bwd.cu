@@ -109,9 +109,10 @@ static_assert(smem_alloc<128>() <= 232448, "shared memory over the 227 KB limit"
 enum : uint32_t {
     kSiteKV = 1, kSiteKVEmpty, kSiteQFull, kSiteQEmpty, kSiteSFull, kSitePFull, kSiteDQFull,
     kSiteDQEmpty, kSiteDKVFull, kSiteDKVEmpty, kSiteStats, kSiteDPFull, kSiteRead, kSiteOutStaged,
-    kSiteOutFree
+    kSiteOutFree, kSiteSeqlens
 };
 static_assert(kSiteDKVFull == ATTN_BWD_SITE_DKV_READY, "the dK/dV-ready wait site is part of the ABI");
+static_assert(kSiteSeqlens == ATTN_BWD_SITE_SEQLENS, "the sequence-length check site is part of the ABI");
 
 __device__ uint32_t g_bwd_status[2];   // [0] status code, [1] wait site
 
@@ -135,6 +136,17 @@ struct BwdParams {
     long long kv_sb, kv_ss, kv_sh;   // element strides of dK/dV for b, s, h
     unsigned long long wait_limit_ns;
     int test_hooks;              // ATTN_TEST_WITHHOLD_O_READY: CTA 0 skips its first unit's dK/dV-ready signal
+    // variable-length batches (the kVarlen instance): per sequence b the tensor maps
+    // vl_maps[7 b + 0..6] = Q, dO, K, V, dK, dV (bf16, the sequence's rows) and the dQ
+    // accumulator (fp32 [H][total_q][d], the sequence's rows); the work units (b, K/V head, key
+    // tile), heaviest first, and their count; the sequences' padded statistics row offsets
+    const CUtensorMap* vl_maps;
+    const int4* vl_units;
+    const int* vl_n_units;
+    const int* vl_pad;           // [B + 1], multiples of 128; statistics rows h * stat_stride + ...
+    const int* cu_q;
+    const int* cu_k;
+    long long stat_stride;
 };
 
 struct Unit {
@@ -143,6 +155,8 @@ struct Unit {
     int nsteps;              // query tiles x query heads of the group
     int st0, st1;            // the steps this work item runs, [st0, st1): all of them unless split
     int slot;                // split item: the row of its dV/dK partials in the workspace; else -1
+    int sq, coff, pad;       // variable-length batches: the sequence's query count, causal
+                             // offset (Skv - Sq) and first padded statistics row
 };
 
 __device__ __forceinline__ Unit decode_unit(const BwdParams& p, int k) {
@@ -171,7 +185,11 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams& p, int k) {
 // round, a pair whose lengths add up to about the same total.  A round still covers
 // consecutive (b, K/V head) groups, so the Q and dO those units read stay shared in L2.
 // Pairs are used (p.paired) for causal launches with at least two units per CTA.
+template <bool kVarlen = false>
 __device__ __forceinline__ int sched_pos(const BwdParams& p, int n) {
+    // a variable-length batch's units come heaviest first: rounds alternate direction
+    if constexpr (kVarlen)
+        return n * (int)gridDim.x + ((n & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x);
     if (!p.paired) return n * (int)gridDim.x + (int)blockIdx.x;
     return (n >> 1) * 2 * (int)gridDim.x + 2 * (int)blockIdx.x + (n & 1);
 }
@@ -185,7 +203,32 @@ __device__ __forceinline__ int unit_at(const BwdParams& p, int pos) {
 // Work item at schedule position pos.  Items below n_full are whole units (the paired causal
 // schedule maps positions to units first); the rest split the last, partial round's units into
 // nsplit ranges of query steps each, whose dK/dV partials a final kernel adds in part order.
+__device__ __forceinline__ Unit decode_varlen_unit(const BwdParams& p, int pos) {
+    Unit u;
+    const int4 e = __ldg(p.vl_units + pos);
+    u.b = e.x;
+    u.kvh = e.y;
+    u.jt = e.z;
+    const int q0 = __ldg(p.cu_q + u.b);
+    u.sq = __ldg(p.cu_q + u.b + 1) - q0;
+    u.coff = (__ldg(p.cu_k + u.b + 1) - __ldg(p.cu_k + u.b)) - u.sq;
+    u.pad = __ldg(p.vl_pad + u.b);
+    u.it_lo = 0;
+    if (p.causal) {
+        const int first_q = u.jt * kBN - u.coff;
+        u.it_lo = first_q <= 0 ? 0 : first_q / kBM;
+    }
+    const int nq = (u.sq + kBM - 1) / kBM;
+    u.nsteps = (u.it_lo < nq ? nq - u.it_lo : 0) * p.group;
+    u.st0 = 0;
+    u.st1 = u.nsteps;
+    u.slot = -1;
+    return u;
+}
+
+template <bool kVarlen = false>
 __device__ __forceinline__ Unit decode_item(const BwdParams& p, int pos) {
+    if constexpr (kVarlen) return decode_varlen_unit(p, pos);
     Unit u;
     if (pos < p.n_full) {
         u = decode_unit(p, unit_at(p, pos));
@@ -256,9 +299,10 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
 }
 
 
-// kDet: the deterministic mode (dQ terms stored to per-key-tile slices, not added); a separate
-// instance, so the default one carries none of it.
-template <int D, bool kDet>
+// kDet: the deterministic mode (dQ terms stored to per-key-tile slices, not added); kVarlen: a
+// variable-length batch (units, tensor maps and statistics offsets from its planning kernel).
+// Separate instances, so the default one carries none of either.
+template <int D, bool kDet, bool kVarlen = false>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap domap,
@@ -314,6 +358,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     const unsigned long long lim = p.wait_limit_ns;
     // the dQ rounding kernel may be scheduled as CTAs retire; it waits for this grid's memory
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // a variable-length batch's units and maps come from the kernels before this one: every
+    // thread waits for their memory first
+    if constexpr (kVarlen) asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int n_items = kVarlen ? __ldg(p.vl_n_units) : p.n_items;
     // TMEM: S^T then P^T | dP^T then dS^T, later dQ_i | dV | dK.  dQ_i goes where dP^T was, so
     // the next step's S^T GEMM does not wait for dQ_i to be read out.
     const uint32_t tS = tmem, tDP = tmem + 128u, tDV = tmem + 256u, tDK = tmem + 256u + (uint32_t)D, tDQ = tDP;
@@ -344,7 +392,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             ptx::tmem_ld32(tDP + lane_off + 32u * c, dp);
             const int q0 = it * kBM + 32 * c;
             // every column of this chunk visible to this key: no per-element test
-            const bool all_vis = q0 + 31 < p.Sq && (!p.causal || kj <= q0 + p.causal_off);
+            const int sq = kVarlen ? un.sq : p.Sq, coff = kVarlen ? un.coff : p.causal_off;
+            const bool all_vis = q0 + 31 < sq && (!p.causal || kj <= q0 + coff);
             const float2 c2 = make_float2(cl, cl);
             if (all_vis) {
                 // the packed arithmetic below without the mask
@@ -372,8 +421,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             }
             // pair (this key, query q0 + col) is visible iff lo <= col < hi: hi from Sq, lo from
             // the causal diagonal (key kj <= q + causal_off)
-            const int hi = p.Sq - q0;
-            const long long lo64 = p.causal ? (long long)kj - p.causal_off - q0 : 0ll;
+            const int hi = sq - q0;
+            const long long lo64 = p.causal ? (long long)kj - coff - q0 : 0ll;
             const int lo = lo64 < -1 ? -1 : (lo64 > 33 ? 33 : (int)lo64);
 #pragma unroll
             for (int g4 = 0; g4 < 8; ++g4) {
@@ -446,6 +495,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         // (key tile, query row) is written by one step only, and the final kernel adds the
         // slices in key-tile order.
         int hist_it[kStages] = {0, 0}, hist_bh[kStages] = {0, 0}, hist_jt[kStages] = {0, 0};
+        int hist_b[kStages] = {0, 0};      // (variable-length batches) the sequence, for its dQ map
         // the preprocessing kernel's D, LSE and zeroed accumulator are waited for once, before
         // the first statistics load (every reduction comes after it), and in any case before
         // exit, so this grid's completion implies that kernel's
@@ -466,6 +516,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     const uint32_t src = stage + (uint32_t)((w * (kHC / 32) + cc) * 4096);
                     const int x = kHC * (w >> 2) + 32 * cc, y = hist_it[tg] * kBM + 32 * (w & 3);
                     if constexpr (kDet) ptx::tma_store_4d(&dqmap, src, x, y, hist_bh[tg], hist_jt[tg]);
+                    else if constexpr (kVarlen) tma_reduce_add_3d(p.vl_maps + 7 * hist_b[tg] + 6, src, x, y, hist_bh[tg]);
                     else tma_reduce_add_3d(&dqmap, src, x, y, hist_bh[tg]);
                 }
             ptx::bulk_commit();
@@ -488,7 +539,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             const uint32_t qd = sbase + G::kSmemStage0 + sg * G::kStageBytes;
             for (int c = 0; c < G::kChunks; ++c) {
                 const uint32_t dq = qd + c * kChunkBytes, dd = qd + G::kTileBytes + c * kChunkBytes;
-                if (p.bshd) {
+                if constexpr (kVarlen) {
+                    // the sequence's own maps, token-major, batch coordinate 0
+                    ptx::tma_load_4d(dq, p.vl_maps + 7 * un.b + 0, bar(kBarQFull + sg), c * 64, h, it * kBM, 0, pol_q);
+                    ptx::tma_load_4d(dd, p.vl_maps + 7 * un.b + 1, bar(kBarQFull + sg), c * 64, h, it * kBM, 0, pol_q);
+                } else if (p.bshd) {
                     ptx::tma_load_4d(dq, &qmap, bar(kBarQFull + sg), c * 64, h, it * kBM, un.b, pol_q);
                     ptx::tma_load_4d(dd, &domap, bar(kBarQFull + sg), c * 64, h, it * kBM, un.b, pol_q);
                 } else {
@@ -497,8 +552,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 }
             }
             hist_it[sg] = it;
-            hist_bh[sg] = un.b * p.H + h;
+            hist_bh[sg] = kVarlen ? h : un.b * p.H + h;
             hist_jt[sg] = un.jt;
+            hist_b[sg] = un.b;
             ++q_issued;
             return true;
         };
@@ -507,8 +563,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             c1 = p.bshd ? un.kvh : un.jt * kBN;
             c2 = p.bshd ? un.jt * kBN : un.kvh;
         };
-        for (int n = 0, k = sched_pos(p, 0); k < p.n_items && ok; k = sched_pos(p, ++n), ++u) {
-            const Unit un = decode_item(p, k);
+        for (int n = 0, k = sched_pos<kVarlen>(p, 0); k < n_items && ok; k = sched_pos<kVarlen>(p, ++n), ++u) {
+            const Unit un = decode_item<kVarlen>(p, k);
+            if constexpr (kVarlen) {
+                // the sequence's maps (written by the planning kernel) before their first use;
+                // a sequence without queries has no Q, dO or dQ maps and its units no steps
+                const CUtensorMap* m = p.vl_maps + 7 * un.b;
+                ptx::tensormap_acquire(m + 2);
+                ptx::tensormap_acquire(m + 3);
+                if (un.st1 > un.st0) {
+                    ptx::tensormap_acquire(m + 0);
+                    ptx::tensormap_acquire(m + 1);
+                    ptx::tensormap_acquire(m + 6);
+                }
+            }
             // the unit's first Q/dO goes in before the wait for the previous unit's K/V to be
             // released, so that it does not wait behind that unit's last GEMMs
             if (un.st1 > un.st0 && !(ok = load_q(un, un.st0, s))) break;
@@ -516,10 +584,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             ptx::mbar_arrive_expect_tx(bar(kBarKV), 2 * G::kTileBytes);
             for (int c = 0; c < G::kChunks; ++c) {
                 const uint32_t dk = sbase + G::kSmemK + c * kChunkBytes, dv = sbase + G::kSmemV + c * kChunkBytes;
-                int c1, c2;
-                kv_coords(un, c1, c2);
-                ptx::tma_load_4d(dk, &kmap, bar(kBarKV), c * 64, c1, c2, un.b, pol_kv);
-                ptx::tma_load_4d(dv, &vmap, bar(kBarKV), c * 64, c1, c2, un.b, pol_kv);
+                if constexpr (kVarlen) {
+                    ptx::tma_load_4d(dk, p.vl_maps + 7 * un.b + 2, bar(kBarKV), c * 64, un.kvh, un.jt * kBN, 0, pol_kv);
+                    ptx::tma_load_4d(dv, p.vl_maps + 7 * un.b + 3, bar(kBarKV), c * 64, un.kvh, un.jt * kBN, 0, pol_kv);
+                } else {
+                    int c1, c2;
+                    kv_coords(un, c1, c2);
+                    ptx::tma_load_4d(dk, &kmap, bar(kBarKV), c * 64, c1, c2, un.b, pol_kv);
+                    ptx::tma_load_4d(dv, &vmap, bar(kBarKV), c * 64, c1, c2, un.b, pol_kv);
+                }
             }
             for (int st = un.st0; st < un.st1 && ok; ++st, ++s) {
                 const int h = un.kvh * p.group + st % p.group;
@@ -529,7 +602,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 if (s > 0 && !(ok = bwd_wait(bar(kBarPFull), (s - 1) & 1u, kSitePFull, abort_flag, lim))) break;
                 dep_wait();
                 ptx::mbar_arrive_expect_tx(bar(kBarStats), 2 * kBM * 4);
-                const long long srow = ((long long)un.b * p.H + h) * p.nq_pad_rows + (long long)it * kBM;
+                const long long srow = kVarlen ? (long long)h * p.stat_stride + un.pad + (long long)it * kBM
+                                               : ((long long)un.b * p.H + h) * p.nq_pad_rows + (long long)it * kBM;
                 ptx::bulk_load_1d(sbase + G::kSmemStats, p.lse2 + srow, kBM * 4, bar(kBarStats));
                 ptx::bulk_load_1d(sbase + G::kSmemStats + kBM * 4, p.delta + srow, kBM * 4, bar(kBarStats));
             }
@@ -592,8 +666,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         };
         uint32_t s = 0, u = 0;
         bool ok = true;
-        for (int n = 0, k = sched_pos(p, 0); k < p.n_items && ok; k = sched_pos(p, ++n), ++u) {
-            const Unit un = decode_item(p, k);
+        for (int n = 0, k = sched_pos<kVarlen>(p, 0); k < n_items && ok; k = sched_pos<kVarlen>(p, ++n), ++u) {
+            const Unit un = decode_item<kVarlen>(p, k);
             if (!(ok = bwd_wait(bar(kBarKV), u & 1u, kSiteKV, abort_flag, lim))) break;
             for (int st = un.st0; st < un.st1 && ok; ++st, ++s) {
                 const uint32_t sg = s % kStages;
@@ -649,8 +723,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         static_assert(8 * (kHC / 32) * 4096 == G::kStageBytes, "the dQ boxes fill one Q/dO stage");
         uint32_t s = 0, u = 0;
         bool ok = true;
-        for (int n = 0, k = sched_pos(p, 0); k < p.n_items && ok; k = sched_pos(p, ++n), ++u) {
-            const Unit un = decode_item(p, k);
+        for (int n = 0, k = sched_pos<kVarlen>(p, 0); k < n_items && ok; k = sched_pos<kVarlen>(p, ++n), ++u) {
+            const Unit un = decode_item<kVarlen>(p, k);
             for (int st = un.st0; st < un.st1 && ok; ++st, ++s) {
                 if (!(ok = pds_step(un, un.it_lo + st / p.group, s, half))) break;
                 ok = bwd_wait(bar(kBarDQFull), s & 1u, kSiteDQFull, abort_flag, lim);
@@ -755,10 +829,16 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                         ok = bwd_wait(bar(kBarOutStaged + half), rnd & 1u, kSiteOutStaged, abort_flag, lim);
                         if (ok) {
                             if (!split) {
-                                const int y1 = p.bshd ? un.kvh : un.jt * kBN;
-                                const int y2 = p.bshd ? un.jt * kBN : un.kvh;
-                                ptx::tma_store_4d(half ? (const void*)&dkmap : (const void*)&dvmap, box, cc * 64, y1,
-                                                  y2, un.b);
+                                if constexpr (kVarlen) {
+                                    const CUtensorMap* om = p.vl_maps + 7 * un.b + (half ? 4 : 5);
+                                    if (cc == 0) ptx::tensormap_acquire(om);
+                                    ptx::tma_store_4d(om, box, cc * 64, un.kvh, un.jt * kBN, 0);
+                                } else {
+                                    const int y1 = p.bshd ? un.kvh : un.jt * kBN;
+                                    const int y2 = p.bshd ? un.jt * kBN : un.kvh;
+                                    ptx::tma_store_4d(half ? (const void*)&dkmap : (const void*)&dvmap, box, cc * 64,
+                                                      y1, y2, un.b);
+                                }
                                 ptx::bulk_commit();
                                 ptx::bulk_wait_read0();
                             }
@@ -950,6 +1030,296 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const float* dq_acc, _
         *reinterpret_cast<uint32_t*>(out) = pack2(acc[0] * sc, acc[1] * sc);
 }
 
+// ------------------------------------------------------------------------------ varlen
+// Planning kernel of a variable-length backward, one CTA, first of the four kernels:
+//   * checks the offsets (cu_q, cu_k start at >= 0, never decrease, end within the packed
+//     tensors); otherwise it records ATTN_ERR_INVALID_ARG at the sequence-length site and
+//     schedules no unit, and the later kernels write nothing;
+//   * pad[b]: the first padded statistics row of sequence b (its rows rounded up to 128);
+//   * per sequence, tensor maps narrowed to its rows (tensormap.replace on copies of the
+//     whole-tensor maps, then a release fence for the tensor-map proxy): K, V, dK, dV when it
+//     has keys, Q, dO and the dQ accumulator when it also has queries.  Loads past its end read
+//     zeros and stores and reductions past its end are dropped, as at a dense tensor's end;
+//   * the units (sequence, K/V head, key tile) ordered by their query steps, most first (a
+//     counting sort capped at kCostBuckets - 1; equal counts in any order, which moves work
+//     between CTAs but changes no result).
+constexpr int kCostBuckets = 4096;
+
+struct BwdVarlenPlan {
+    const int* cu_q;
+    const int* cu_k;
+    int B, H, Hkv, group, causal;
+    long long total_q, total_k;
+    long long q_row_bytes, kv_row_bytes, acc_row_bytes;   // bytes per token row (acc: per head)
+    const char* q;
+    const char* dout;
+    const char* k;
+    const char* v;
+    char* dk;
+    char* dv;
+    char* dq_acc;
+    CUtensorMap* maps;           // [B][7]: Q, dO, K, V, dK, dV, dQ accumulator
+    int4* units;
+    int* n_units;
+    int* pad;                    // [B + 1]
+};
+
+__device__ __forceinline__ void bwd_copy_map(CUtensorMap* dst, const CUtensorMap* src) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(CUtensorMap) / 16); ++i) d4[i] = s4[i];
+}
+
+// the map at dst (a copy of a whole-tensor map) moved to `base`, with `rows` rows on axis `ord`
+__device__ __forceinline__ void bwd_narrow_map(CUtensorMap* dst, const void* base, int ord, int rows) {
+    asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst),
+                 "l"(reinterpret_cast<uint64_t>(base))
+                 : "memory");
+    if (ord == 1)
+        asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(dst), "r"(rows) : "memory");
+    else
+        asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 2, %1;" ::"l"(dst), "r"(rows) : "memory");
+}
+
+// query steps of unit (key tile jt) of a sequence with sq queries and skv keys, per K/V head
+__device__ __forceinline__ int unit_steps(int jt, int sq, int skv, int causal, int group) {
+    int it_lo = 0;
+    if (causal) {
+        const int first_q = jt * kBN - (skv - sq);
+        it_lo = first_q <= 0 ? 0 : first_q / kBM;
+    }
+    const int nq = (sq + kBM - 1) / kBM;
+    return (it_lo < nq ? nq - it_lo : 0) * group;
+}
+
+__global__ void __launch_bounds__(1024) attn_bwd_varlen_plan_kernel(
+    const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap domap,
+    const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+    const __grid_constant__ CUtensorMap dkmap, const __grid_constant__ CUtensorMap dvmap,
+    const __grid_constant__ CUtensorMap accmap, const BwdVarlenPlan a) {
+    __shared__ int bad;
+    __shared__ int bucket[kCostBuckets];
+    __shared__ int warp_sums[32];
+    __shared__ int carry;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int nthreads = blockDim.x;
+    if (tid == 0) {
+        bad = (a.cu_q[0] < 0 || a.cu_k[0] < 0 || a.cu_q[a.B] > a.total_q || a.cu_k[a.B] > a.total_k) ? 1 : 0;
+        carry = 0;
+    }
+    for (int i = tid; i < kCostBuckets; i += nthreads) bucket[i] = 0;
+    __syncthreads();
+    for (int b = tid; b < a.B; b += nthreads)
+        if (a.cu_q[b + 1] < a.cu_q[b] || a.cu_k[b + 1] < a.cu_k[b]) bad = 1;
+    __syncthreads();
+    if (bad) {
+        // -1 units: the attention kernel runs nothing and the last kernel writes nothing
+        if (tid == 0) {
+            *a.n_units = -1;
+            if (atomicCAS(&g_bwd_status[0], 0u, (uint32_t)ATTN_ERR_INVALID_ARG) == 0u)
+                atomicExch(&g_bwd_status[1], kSiteSeqlens);
+        }
+        for (int b = tid; b <= a.B; b += nthreads) a.pad[b] = 0;
+        return;
+    }
+    for (int base = 0; base < a.B; base += nthreads) {
+        const int b = base + tid;
+        int sq = 0, skv = 0, rows = 0;
+        if (b < a.B) {
+            sq = a.cu_q[b + 1] - a.cu_q[b];
+            skv = a.cu_k[b + 1] - a.cu_k[b];
+            rows = (sq + kBM - 1) / kBM * kBM;
+        }
+        // exclusive prefix of the padded statistics rows
+        int incl = rows;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) warp_sums[wid] = incl;
+        __syncthreads();
+        if (wid == 0) {
+            int w = lane < (nthreads >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, w, off);
+                if (lane >= off) w += y;
+            }
+            warp_sums[lane] = w;
+        }
+        __syncthreads();
+        const int before = carry + (wid > 0 ? warp_sums[wid - 1] : 0) + incl - rows;
+        if (b < a.B) {
+            a.pad[b] = before;
+            CUtensorMap* m = a.maps + 7 * (long long)b;
+            const long long q0 = a.cu_q[b], k0 = a.cu_k[b];
+            if (skv > 0) {
+                bwd_copy_map(m + 2, &kmap);
+                bwd_copy_map(m + 3, &vmap);
+                bwd_copy_map(m + 4, &dkmap);
+                bwd_copy_map(m + 5, &dvmap);
+                bwd_narrow_map(m + 2, a.k + k0 * a.kv_row_bytes, 2, skv);
+                bwd_narrow_map(m + 3, a.v + k0 * a.kv_row_bytes, 2, skv);
+                bwd_narrow_map(m + 4, a.dk + k0 * a.kv_row_bytes, 2, skv);
+                bwd_narrow_map(m + 5, a.dv + k0 * a.kv_row_bytes, 2, skv);
+                if (sq > 0) {
+                    bwd_copy_map(m + 0, &qmap);
+                    bwd_copy_map(m + 1, &domap);
+                    bwd_copy_map(m + 6, &accmap);
+                    bwd_narrow_map(m + 0, a.q + q0 * a.q_row_bytes, 2, sq);
+                    bwd_narrow_map(m + 1, a.dout + q0 * a.q_row_bytes, 2, sq);
+                    bwd_narrow_map(m + 6, a.dq_acc + q0 * a.acc_row_bytes, 1, sq);
+                }
+                const int nkv = (skv + kBN - 1) / kBN;
+                for (int jt = 0; jt < nkv; ++jt) {
+                    const int c = unit_steps(jt, sq, skv, a.causal, a.group);
+                    atomicAdd(&bucket[c < kCostBuckets - 1 ? c : kCostBuckets - 1], a.Hkv);
+                }
+            }
+        }
+        __syncthreads();
+        if (tid == nthreads - 1) carry = before + rows;
+        __syncthreads();
+    }
+    if (tid == 0) a.pad[a.B] = carry;
+    // start of each bucket, most steps first: thread t owns buckets kCostBuckets - 4t - 1 down
+    // to kCostBuckets - 4t - 4; an exclusive scan of the threads' sums over t
+    constexpr int kPer = kCostBuckets / 1024;
+    int local = 0;
+    for (int i = 0; i < kPer; ++i) local += bucket[kCostBuckets - 1 - kPer * tid - i];
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    __syncthreads();
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int w = lane < (nthreads >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, w, off);
+            if (lane >= off) w += y;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    int start = (wid > 0 ? warp_sums[wid - 1] : 0) + incl - local;
+    if (tid == nthreads - 1) *a.n_units = start + local;
+    __syncthreads();
+    for (int i = 0; i < kPer; ++i) {
+        const int key = kCostBuckets - 1 - kPer * tid - i;
+        const int c = bucket[key];
+        bucket[key] = start;
+        start += c;
+    }
+    __syncthreads();
+    for (int b = tid; b < a.B; b += nthreads) {
+        const int sq = a.cu_q[b + 1] - a.cu_q[b], skv = a.cu_k[b + 1] - a.cu_k[b];
+        const int nkv = (skv + kBN - 1) / kBN;
+        for (int jt = 0; jt < nkv; ++jt) {
+            const int c = unit_steps(jt, sq, skv, a.causal, a.group);
+            const int pos = atomicAdd(&bucket[c < kCostBuckets - 1 ? c : kCostBuckets - 1], a.Hkv);
+            for (int h = 0; h < a.Hkv; ++h) a.units[pos + h] = make_int4(b, h, jt, 0);
+        }
+    }
+    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+
+// Statistics of a variable-length backward, second kernel: per head h and padded row, D = dO . O
+// in fp32 and the base-2 LSE at h * stat_stride + pad[b] + i for query i of sequence b (0 in
+// the padding rows, as in the dense preprocessing), and zeros into the sequence rows of the
+// fp32 dQ accumulator [H][total_q][d].  D / 8 lanes per row, grid-stride; rows past pad[B]
+// are not read by anyone.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_varlen_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout,
+                                                                   const float* lse, float* lse2, float* delta,
+                                                                   float* dq_acc, const int* cu_q, const int* pad,
+                                                                   int B, int H, long long total_q,
+                                                                   long long stat_stride) {
+    constexpr int kL = D / 8;
+    constexpr int kRows = 256 / kL;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int sub = threadIdx.x / kL, c = (threadIdx.x % kL) * 8;
+    const long long used = pad[B];
+    const long long rows = (long long)H * stat_stride;
+    for (long long r = (long long)blockIdx.x * kRows + sub; r < rows; r += (long long)gridDim.x * kRows) {
+        const int h = (int)(r / stat_stride);
+        const long long pr = r % stat_stride;
+        if (pr >= used) continue;             // whole warps: stat_stride and used are multiples of 128
+        int lo = 0, hi = B - 1;               // the last b with pad[b] <= pr
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (pad[mid] <= pr) lo = mid;
+            else hi = mid - 1;
+        }
+        const long long i = pr - pad[lo];
+        const long long q0 = cu_q[lo], sq = cu_q[lo + 1] - q0;
+        float acc = 0.0f;
+        if (i < sq) {
+            const long long off = ((q0 + i) * H + h) * D + c;
+            const uint4 ov = *reinterpret_cast<const uint4*>(o + off);
+            const uint4 gv = *reinterpret_cast<const uint4*>(dout + off);
+            const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+                const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+                acc = fmaf(of.x, gf.x, acc);
+                acc = fmaf(of.y, gf.y, acc);
+            }
+            float4* z = reinterpret_cast<float4*>(dq_acc + ((long long)h * total_q + q0 + i) * D + c);
+            z[0] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            z[1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int sft = kL / 2; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, sft);
+        if (c == 0) {
+            delta[r] = acc;
+            lse2[r] = i < sq ? lse[(long long)h * total_q + q0 + i] * 1.4426950408889634f : 0.0f;
+        }
+    }
+}
+
+// Last kernel of a variable-length backward: dq (bf16, packed [total_q][H][d]) = the fp32
+// accumulator [H][total_q][d], round to nearest even, for the query rows of a sequence with
+// keys (rows of key-less sequences get zeros, rows outside every sequence are not written).
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_varlen_dq_kernel(const float* dq_acc, __nv_bfloat16* dq,
+                                                                 const int* cu_q, const int* cu_k, int B, int H,
+                                                                 long long total_q, const int* n_units) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (*n_units < 0) return;                        // offsets rejected: nothing is written
+    const long long n8 = total_q * H * (D / 8);
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
+        const long long tr = i / (D / 8);             // token row * H + head
+        const int x = (int)(i % (D / 8)) * 8;
+        const long long r = tr / H;
+        const int h = (int)(tr % H);
+        int lo = 0, hi = B - 1;                       // the last b with cu_q[b] <= r
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cu_q[mid] <= r) lo = mid;
+            else hi = mid - 1;
+        }
+        if (r < cu_q[lo] || r >= cu_q[lo + 1]) continue;
+        uint4 out = make_uint4(0u, 0u, 0u, 0u);
+        if (cu_k[lo + 1] > cu_k[lo]) {
+            const float4* src = reinterpret_cast<const float4*>(dq_acc + ((long long)h * total_q + r) * D + x);
+            const float4 v0 = src[0], v1 = src[1];
+            out = make_uint4(pack2(v0.x, v0.y), pack2(v0.z, v0.w), pack2(v1.x, v1.y), pack2(v1.z, v1.w));
+        }
+        *reinterpret_cast<uint4*>(dq + tr * D + x) = out;
+    }
+}
+
 // ------------------------------------------------------------------------------ host side
 std::mutex g_bwd_mutex;
 PFN_cuTensorMapEncodeTiled_v12000 g_bwd_encode = nullptr;
@@ -1066,9 +1436,241 @@ int64_t current_sms() {
     return sms;
 }
 
+// The tensor-map encoder and, once per device, the kernels' shared-memory limits.
+int bwd_setup(int dev) {
+    std::lock_guard<std::mutex> g(g_bwd_mutex);
+    if (!g_bwd_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) !=
+                cudaSuccess ||
+            qr != cudaDriverEntryPointSuccess || !fn)
+            return ATTN_ERR_CUDA;
+        g_bwd_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
+    if (!g_bwd_attr[dev]) {
+        const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+        if (cudaFuncSetAttribute(attn_bwd_kernel<128, false>, attr, smem_alloc<128>()) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_bwd_kernel<64, false>, attr, smem_alloc<64>()) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_bwd_kernel<128, true>, attr, smem_alloc<128>()) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_bwd_kernel<64, true>, attr, smem_alloc<64>()) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_bwd_kernel<128, false, true>, attr, smem_alloc<128>()) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_bwd_kernel<64, false, true>, attr, smem_alloc<64>()) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        g_bwd_attr[dev] = true;
+    }
+    return ATTN_OK;
+}
+
+int check_varlen(const attn_bwd_varlen_args_t& a) {
+    if (a.B < 1 || a.H < 1 || a.Hkv < 1 || a.total_q < 0 || a.total_k < 0 || a.d < 1) return ATTN_ERR_INVALID_ARG;
+    if (a.H % a.Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if ((a.causal != 0 && a.causal != 1) || a.wait_limit_ms < 0 || a.reserved != 0 || a.reserved2 != 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (a.d != 128 && a.d != 64) return ATTN_ERR_UNSUPPORTED;
+    const int64_t lim = (int64_t)1 << 30;
+    if (a.total_q > lim || a.total_k > lim || a.B > lim || a.H > lim || a.total_q + 127 * a.B > lim ||
+        a.Hkv * (a.total_k / kBN + a.B) > lim)
+        return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+// padded statistics rows per head: each sequence's queries rounded up to 128
+int64_t varlen_stat_stride(const attn_bwd_varlen_args_t& a) { return cdiv(a.total_q + 127 * a.B, kBM) * kBM; }
+
+// workspace: dQ accumulator | base-2 LSE | D | tensor maps (128-byte aligned) | item count and
+// padded offsets | units
+struct VarlenWs {
+    size_t acc, stats, maps, misc, units, total;
+};
+VarlenWs varlen_ws(const attn_bwd_varlen_args_t& a) {
+    VarlenWs w;
+    w.acc = 0;
+    w.stats = w.acc + (size_t)(a.H * a.total_q * a.d * 4);
+    w.maps = (w.stats + (size_t)(2 * a.H * varlen_stat_stride(a) * 4) + 127) / 128 * 128;
+    w.misc = w.maps + (size_t)(7 * a.B) * sizeof(CUtensorMap);
+    w.units = w.misc + (size_t)((a.B + 2 + 3) / 4 * 16);
+    w.total = w.units + (size_t)(a.Hkv * (a.total_k / kBN + a.B)) * 16;
+    return w;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t attn_bwd_varlen_workspace_size(const attn_bwd_varlen_args_t* args) {
+    if (!args || check_varlen(*args) != ATTN_OK) return 0;
+    return varlen_ws(*args).total;
+}
+
+int attn_bwd_varlen(const attn_bwd_varlen_args_t* args, void* workspace, size_t workspace_bytes,
+                    attn_stream_t stream_) {
+    if (!args) return ATTN_ERR_INVALID_ARG;
+    const attn_bwd_varlen_args_t& a = *args;
+    if (!a.q || !a.k || !a.v || !a.o || !a.dout || !a.lse || !a.dq || !a.dk || !a.dv || !a.cu_seqlens_q ||
+        !a.cu_seqlens_k)
+        return ATTN_ERR_INVALID_ARG;
+    int st = check_varlen(a);
+    if (st != ATTN_OK) return st;
+    const uintptr_t al = (uintptr_t)a.q | (uintptr_t)a.k | (uintptr_t)a.v | (uintptr_t)a.o | (uintptr_t)a.dout |
+                         (uintptr_t)a.dq | (uintptr_t)a.dk | (uintptr_t)a.dv | (uintptr_t)workspace;
+    if ((al & 15u) || (((uintptr_t)a.lse | (uintptr_t)a.cu_seqlens_q | (uintptr_t)a.cu_seqlens_k) & 3u))
+        return ATTN_ERR_MISALIGNED;
+    const VarlenWs w = varlen_ws(a);
+    if (!workspace || workspace_bytes < w.total) return ATTN_ERR_WORKSPACE;
+    const int64_t d = a.d;
+    const uintptr_t qb = (uintptr_t)(a.total_q * a.H * d * 2), kb = (uintptr_t)(a.total_k * a.Hkv * d * 2);
+    const uintptr_t outs[3][2] = {{(uintptr_t)a.dq, qb}, {(uintptr_t)a.dk, kb}, {(uintptr_t)a.dv, kb}};
+    const uintptr_t ins[6][2] = {{(uintptr_t)a.q, qb}, {(uintptr_t)a.k, kb}, {(uintptr_t)a.v, kb},
+                                 {(uintptr_t)a.o, qb}, {(uintptr_t)a.dout, qb}, {(uintptr_t)workspace, w.total}};
+    for (int i = 0; i < 3; ++i) {
+        if (outs[i][1] == 0) continue;
+        for (int j = 0; j < 6; ++j)
+            if (outs[i][0] < ins[j][0] + ins[j][1] && ins[j][0] < outs[i][0] + outs[i][1]) return ATTN_ERR_ALIAS;
+        for (int j = 0; j < i; ++j)
+            if (outs[i][0] < outs[j][0] + outs[j][1] && outs[j][0] < outs[i][0] + outs[i][1]) return ATTN_ERR_ALIAS;
+    }
+    cudaStream_t stream = (cudaStream_t)stream_;
+    int dev = 0, sms = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_NO_DEVICE;
+    }
+    if (major != 10 || minor != 3) return ATTN_ERR_NO_DEVICE;
+    if ((st = bwd_setup(dev)) != ATTN_OK) return st;
+    char* ws = reinterpret_cast<char*>(workspace);
+    float* dq_acc = reinterpret_cast<float*>(ws + w.acc);
+    const int64_t SP = varlen_stat_stride(a);
+    float* lse2 = reinterpret_cast<float*>(ws + w.stats);
+    float* delta = lse2 + a.H * SP;
+    CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(ws + w.maps);
+    int* n_units = reinterpret_cast<int*>(ws + w.misc);
+    int* pad = n_units + 1;
+    int4* units = reinterpret_cast<int4*>(ws + w.units);
+    // whole-tensor maps, token-major with one batch; the planning kernel narrows copies of them
+    // to each sequence (a tensor without rows gets a one-row map that nothing uses)
+    const int64_t tq = a.total_q > 0 ? a.total_q : 1, tk = a.total_k > 0 ? a.total_k : 1;
+    CUtensorMap qm, dom, km, vm, dkm, dvm, accm;
+    if (!encode(&qm, a.q, 1, a.H, tq, d, true) || !encode(&dom, a.dout, 1, a.H, tq, d, true) ||
+        !encode(&km, a.k, 1, a.Hkv, tk, d, true) || !encode(&vm, a.v, 1, a.Hkv, tk, d, true) ||
+        !encode(&dkm, a.dk, 1, a.Hkv, tk, d, true) || !encode(&dvm, a.dv, 1, a.Hkv, tk, d, true) ||
+        !encode_dq(&accm, dq_acc, a.H, tq, d))
+        return ATTN_ERR_CUDA;
+    BwdVarlenPlan pl;
+    memset(&pl, 0, sizeof pl);
+    pl.cu_q = a.cu_seqlens_q;
+    pl.cu_k = a.cu_seqlens_k;
+    pl.B = (int)a.B;
+    pl.H = (int)a.H;
+    pl.Hkv = (int)a.Hkv;
+    pl.group = (int)(a.H / a.Hkv);
+    pl.causal = a.causal;
+    pl.total_q = a.total_q;
+    pl.total_k = a.total_k;
+    pl.q_row_bytes = a.H * d * 2;
+    pl.kv_row_bytes = a.Hkv * d * 2;
+    pl.acc_row_bytes = d * 4;
+    pl.q = reinterpret_cast<const char*>(a.q);
+    pl.dout = reinterpret_cast<const char*>(a.dout);
+    pl.k = reinterpret_cast<const char*>(a.k);
+    pl.v = reinterpret_cast<const char*>(a.v);
+    pl.dk = reinterpret_cast<char*>(a.dk);
+    pl.dv = reinterpret_cast<char*>(a.dv);
+    pl.dq_acc = reinterpret_cast<char*>(dq_acc);
+    pl.maps = maps;
+    pl.units = units;
+    pl.n_units = n_units;
+    pl.pad = pad;
+
+    BwdParams p;
+    memset(&p, 0, sizeof p);
+    p.B = (int)a.B;
+    p.H = (int)a.H;
+    p.Hkv = (int)a.Hkv;
+    p.group = (int)(a.H / a.Hkv);
+    p.nsplit = 1;
+    p.causal = a.causal;
+    p.bshd = 1;
+    p.scale = (float)(1.0 / std::sqrt((double)d));
+    p.scale_log2 = (float)((1.0 / std::sqrt((double)d)) * 1.4426950408889634);
+    p.lse2 = lse2;
+    p.delta = delta;
+    p.dq_acc = dq_acc;
+    p.wait_limit_ns = (unsigned long long)(a.wait_limit_ms > 0 ? a.wait_limit_ms : 2000) * 1000000ull;
+    p.vl_maps = maps;
+    p.vl_units = units;
+    p.vl_n_units = n_units;
+    p.vl_pad = pad;
+    p.cu_q = a.cu_seqlens_q;
+    p.cu_k = a.cu_seqlens_k;
+    p.stat_stride = SP;
+
+    // planning -> statistics (and dQ zeroing) -> main kernel -> dQ rounding, each a
+    // programmatic dependent of the kernel before it in the stream
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t c;
+    memset(&c, 0, sizeof c);
+    c.gridDim = dim3(1);
+    c.blockDim = dim3(1024);
+    c.stream = stream;
+    c.attrs = attr;
+    c.numAttrs = 1;
+    if (cudaLaunchKernelEx(&c, attn_bwd_varlen_plan_kernel, qm, dom, km, vm, dkm, dvm, accm, pl) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    const long long fill = (long long)sms * 8;
+    const long long prows = a.H * SP;
+    const long long prep_blocks = cdiv(prows, 256 / (d / 8));
+    c.gridDim = dim3((unsigned)(prep_blocks < fill ? (prep_blocks > 0 ? prep_blocks : 1) : fill));
+    c.blockDim = dim3(256);
+    cudaError_t ce = d == 128
+        ? cudaLaunchKernelEx(&c, attn_bwd_varlen_prep_kernel<128>, reinterpret_cast<const __nv_bfloat16*>(a.o),
+                             reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, lse2, delta, dq_acc,
+                             (const int*)a.cu_seqlens_q, (const int*)pad, (int)a.B, (int)a.H, (long long)a.total_q,
+                             (long long)SP)
+        : cudaLaunchKernelEx(&c, attn_bwd_varlen_prep_kernel<64>, reinterpret_cast<const __nv_bfloat16*>(a.o),
+                             reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, lse2, delta, dq_acc,
+                             (const int*)a.cu_seqlens_q, (const int*)pad, (int)a.B, (int)a.H, (long long)a.total_q,
+                             (long long)SP);
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    c.gridDim = dim3((unsigned)sms);
+    c.blockDim = dim3(kThreads);
+    c.dynamicSmemBytes = d == 128 ? smem_alloc<128>() : smem_alloc<64>();
+    ce = cudaLaunchKernelEx(&c, d == 128 ? attn_bwd_kernel<128, false, true> : attn_bwd_kernel<64, false, true>, qm, km,
+                            vm, dom, accm, dkm, dvm, p);
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    const long long n8 = a.total_q * a.H * (d / 8);
+    const long long blocks = cdiv(n8, 256);
+    c.gridDim = dim3((unsigned)(blocks < fill ? (blocks > 0 ? blocks : 1) : fill));
+    c.blockDim = dim3(256);
+    c.dynamicSmemBytes = 0;
+    ce = d == 128 ? cudaLaunchKernelEx(&c, attn_bwd_varlen_dq_kernel<128>, (const float*)dq_acc,
+                                       reinterpret_cast<__nv_bfloat16*>(a.dq), (const int*)a.cu_seqlens_q,
+                                       (const int*)a.cu_seqlens_k, (int)a.B, (int)a.H, (long long)a.total_q,
+                                       (const int*)n_units)
+                  : cudaLaunchKernelEx(&c, attn_bwd_varlen_dq_kernel<64>, (const float*)dq_acc,
+                                       reinterpret_cast<__nv_bfloat16*>(a.dq), (const int*)a.cu_seqlens_q,
+                                       (const int*)a.cu_seqlens_k, (int)a.B, (int)a.H, (long long)a.total_q,
+                                       (const int*)n_units);
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
 
 size_t attn_bwd_workspace_size(const attn_bwd_args_t* args) {
     if (!args || check_shape(*args) != ATTN_OK) return 0;
@@ -1112,30 +1714,7 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
         return ATTN_ERR_NO_DEVICE;
     }
     if (major != 10 || minor != 3) return ATTN_ERR_NO_DEVICE;
-    {
-        std::lock_guard<std::mutex> g(g_bwd_mutex);
-        if (!g_bwd_encode) {
-            void* fn = nullptr;
-            cudaDriverEntryPointQueryResult qr;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) !=
-                    cudaSuccess ||
-                qr != cudaDriverEntryPointSuccess || !fn)
-                return ATTN_ERR_CUDA;
-            g_bwd_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
-        }
-        if (!g_bwd_attr[dev]) {
-            if (cudaFuncSetAttribute(attn_bwd_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     smem_alloc<128>()) != cudaSuccess ||
-                cudaFuncSetAttribute(attn_bwd_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     smem_alloc<64>()) != cudaSuccess ||
-                cudaFuncSetAttribute(attn_bwd_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     smem_alloc<128>()) != cudaSuccess ||
-                cudaFuncSetAttribute(attn_bwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     smem_alloc<64>()) != cudaSuccess)
-                return ATTN_ERR_CUDA;
-            g_bwd_attr[dev] = true;
-        }
-    }
+    if ((st = bwd_setup(dev)) != ATTN_OK) return st;
     const bool bshd = a.layout == ATTN_LAYOUT_BSHD;
     CUtensorMap qm, km, vm, dom;
     const int64_t d = a.d;

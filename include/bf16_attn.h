@@ -381,6 +381,44 @@ int attn_bwd(const attn_bwd_args_t* args, void* workspace, size_t workspace_byte
 /* Synchronize `stream`, then read and clear the backward kernel's device status word. */
 int attn_bwd_get_device_status(attn_stream_t stream, int32_t* site);
 
+/*
+ * Variable-length backward: the gradients of attn_fwd_varlen (sequences packed along the token
+ * axis, each attending to its own keys, causal per sequence, grouped heads).
+ *   q, o, dout, dq   bf16 [total_q][H][d];  k, v, dk, dv  bf16 [total_k][Hkv][d]
+ *   lse              fp32 [H][total_q], attn_fwd_varlen's
+ *   cu_seqlens_q, cu_seqlens_k   device int32 [B + 1], as in attn_fwd_varlen.  Checked on the
+ *                    device: a violation writes no gradient and reports ATTN_ERR_INVALID_ARG
+ *                    at site ATTN_BWD_SITE_SEQLENS through attn_bwd_get_device_status().
+ *   causal, wait_limit_ms  as in attn_bwd;  reserved, reserved2  0
+ * Rows outside every sequence are not written.  Queries of a sequence without keys get zero
+ * dq, keys of a sequence without queries zero dk and dv.  dk, dv are bitwise reproducible; dq's
+ * last bits may vary between runs (fp32 reductions in no fixed order).  Four kernels run on
+ * `stream`: a one-CTA planning kernel (offsets, per-sequence tensor maps, the work units),
+ * the row statistics with the dq accumulator's zeroing, the tcgen05 backward kernel, and the
+ * dq rounding.  workspace: caller device memory of attn_bwd_varlen_workspace_size() bytes,
+ * 16-byte aligned.
+ */
+#define ATTN_BWD_SITE_SEQLENS 16
+typedef struct {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* o;
+    const void* dout;
+    const float* lse;
+    void* dq;
+    void* dk;
+    void* dv;
+    const int32_t* cu_seqlens_q;
+    const int32_t* cu_seqlens_k;
+    int64_t B, H, Hkv, total_q, total_k, d;
+    int32_t causal, wait_limit_ms, reserved, reserved2;
+} attn_bwd_varlen_args_t;
+
+size_t attn_bwd_varlen_workspace_size(const attn_bwd_varlen_args_t* args);
+int attn_bwd_varlen(const attn_bwd_varlen_args_t* args, void* workspace, size_t workspace_bytes,
+                    attn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -227,6 +227,44 @@ def attention_varlen(q, k, v, cu_q, cu_k, mode: str = "rtne", causal: bool = Fal
     return out
 
 
+def backward_varlen(q, k, v, dout, cu_q, cu_k, causal: bool = False, want_a: bool = False,
+                    lib=None) -> dict:
+    """fp64 gradients of the variable-length attention (:func:`attention_varlen`): each
+    sequence's gradients are :func:`backward` of that sequence alone, put back in place.  A
+    sequence without keys has no term in any gradient (dq 0); keys of a sequence without
+    queries get dk = dv = 0.  Returns ``dq``, ``dk``, ``dv`` (float64, packed like the inputs),
+    their RTNE ``*_bits``, ``covered_q``/``covered_k`` (rows that belong to a sequence) and,
+    with ``want_a``, the error scales ``*_a``."""
+    qb, kb, vb, gb = _as_bits(q), _as_bits(k), _as_bits(v), _as_bits(dout)
+    cu_q = [int(x) for x in np.asarray(cu_q).reshape(-1)]
+    cu_k = [int(x) for x in np.asarray(cu_k).reshape(-1)]
+    if len(cu_q) != len(cu_k) or len(cu_q) < 2:
+        raise ValueError("cu_q and cu_k must both hold B + 1 >= 2 offsets")
+    out = {n: np.zeros(t.shape, dtype=np.float64) for n, t in (("dq", qb), ("dk", kb), ("dv", kb))}
+    if want_a:
+        out.update({n + "_a": np.zeros_like(out[n]) for n in ("dq", "dk", "dv")})
+    cov_q = np.zeros((qb.shape[0],), dtype=bool)
+    cov_k = np.zeros((kb.shape[0],), dtype=bool)
+    for b in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        if not (0 <= q0 <= q1 <= qb.shape[0] and 0 <= k0 <= k1 <= kb.shape[0]):
+            raise ValueError("sequence %d: offsets out of order or out of range" % b)
+        cov_q[q0:q1] = True
+        cov_k[k0:k1] = True
+        if q1 == q0 or k1 == k0:
+            continue
+        r = backward(qb[None, q0:q1], kb[None, k0:k1], vb[None, k0:k1], gb[None, q0:q1], "bshd",
+                     causal=causal, want_a=want_a, lib=lib)
+        for n, (a0, a1) in (("dq", (q0, q1)), ("dk", (k0, k1)), ("dv", (k0, k1))):
+            out[n][a0:a1] = r[n][0]
+            if want_a:
+                out[n + "_a"][a0:a1] = r[n + "_a"][0]
+    for n in ("dq", "dk", "dv"):
+        out[n + "_bits"] = round_bf16(out[n], "rtne", lib=lib)
+    out["covered_q"], out["covered_k"] = cov_q, cov_k
+    return out
+
+
 def gather_pages(k_cache, v_cache, seqlens_k, block_table):
     """The keys and values of a paged cache, gathered in order: sequence b's key j is slot
     j % page_size of page block_table[b][j // page_size] of the [num_pages, page_size, Hkv,

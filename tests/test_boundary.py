@@ -307,3 +307,42 @@ def test_paged_workspace_size(lib):
     a = paged_args(B=3, total_q=1000)
     assert lib.attn_fwd_paged_workspace_size(ctypes.byref(a)) == 128 + 3 * 512 + 16 + (1000 // 256 + 3) * 8
     assert lib.attn_fwd_paged_workspace_size(ctypes.byref(paged_args(page_size=100))) == 0
+
+
+def bwd_varlen_args(**kw):
+    a = attn.BwdVarlenArgs()
+    for i, n in enumerate(("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv", "cu_seqlens_q", "cu_seqlens_k")):
+        setattr(a, n, (i + 1) * PG)
+    a.B, a.H, a.Hkv, a.total_q, a.total_k, a.d = 3, 4, 2, 1000, 900, 128
+    for k_, v_ in kw.items():
+        setattr(a, k_, v_)
+    return a
+
+
+def test_bwd_varlen_argument_errors_and_workspace(lib):
+    """attn_bwd_varlen checks its arguments before any device call; its workspace holds the
+    fp32 dQ accumulator [H][total_q][d], the padded row statistics (two fp32 per head and
+    padded row, rows rounded up per sequence: total_q + 127 B, to a multiple of 128), seven
+    tensor maps per sequence (128-byte aligned), the unit count and padded offsets, and one
+    16-byte unit per (K/V head, key tile) it can hold."""
+    ws = 20 * PG
+    def run(**kw):
+        return lib.attn_bwd_varlen(ctypes.byref(bwd_varlen_args(**kw)), ws, 1 << 30, None)
+    assert lib.attn_bwd_varlen(None, ws, 1 << 30, None) == 1
+    assert run() == 5
+    for bad in ({"B": 0}, {"Hkv": 3}, {"total_q": -1}, {"total_k": -1}, {"causal": 2}, {"wait_limit_ms": -1},
+                {"reserved": 1}, {"reserved2": 1}, {"q": 0}, {"lse": 0}, {"cu_seqlens_k": 0}, {"dk": 0}):
+        assert run(**bad) == 1, bad
+    assert run(d=96) == 2
+    assert run(total_q=(1 << 30) + 1) == 2
+    assert run(q=PG + 8) == 3
+    assert run(cu_seqlens_q=10 * PG + 2) == 3
+    assert run(dq=PG + 4096) == 4
+    assert lib.attn_bwd_varlen(ctypes.byref(bwd_varlen_args()), ws, 16, None) == 6
+    a = bwd_varlen_args()
+    sp = -(-(1000 + 127 * 3) // 128) * 128
+    maps = -(-(4 * 1000 * 128 * 4 + 2 * 4 * sp * 4) // 128) * 128
+    misc = maps + 7 * 3 * 128
+    units = misc + -(-(3 + 2) // 4) * 16
+    assert lib.attn_bwd_varlen_workspace_size(ctypes.byref(a)) == units + 2 * (900 // 128 + 3) * 16
+    assert lib.attn_bwd_varlen_workspace_size(ctypes.byref(bwd_varlen_args(d=32))) == 0

@@ -192,3 +192,38 @@ def test_paged_rejects_pages_out_of_range():
     kc, vc, table = _paged_from_contiguous(k, v, [128], 128)
     with pytest.raises(ValueError):
         oracle.attention_paged(q, kc, vc, [0, 8], [128], np.asarray([[1]], dtype=np.int32))
+
+
+# --------------------------------------------------------------------------- varlen backward
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_equal_lengths_match_the_dense_batch(causal):
+    # the same batch through the dense backward oracle (its own batch indexing)
+    B, Sq, Skv, H, Hkv, d = 2, 21, 34, 4, 2, 64
+    q, k, v = _packed(B * Sq, B * Skv, H, Hkv, d, seed=31)
+    g = _packed(B * Sq, 1, H, H, d, seed=32)[0]
+    r = oracle.backward_varlen(q, k, v, g, np.arange(B + 1) * Sq, np.arange(B + 1) * Skv, causal=causal,
+                               want_a=True)
+    dense = oracle.backward(q.reshape(B, Sq, H, d), k.reshape(B, Skv, Hkv, d), v.reshape(B, Skv, Hkv, d),
+                            g.reshape(B, Sq, H, d), "bshd", causal=causal, want_a=True)
+    for n, rows in (("dq", B * Sq), ("dk", B * Skv), ("dv", B * Skv)):
+        assert np.array_equal(r[n], dense[n].reshape(rows, -1, d)), n
+        assert np.array_equal(r[n + "_a"], dense[n + "_a"].reshape(rows, -1, d)), n
+
+
+def test_backward_sequences_do_not_see_each_other_and_edge_rules():
+    H, d = 2, 64
+    lq, lk = [30, 0, 17, 9], [25, 12, 0, 40]     # sequence 1 has no queries, sequence 2 no keys
+    cu_q, cu_k = np.cumsum([0] + lq), np.cumsum([0] + lk)
+    q, k, v = _packed(sum(lq) + 3, sum(lk) + 2, H, H, d, seed=33)   # trailing rows belong to none
+    g = _packed(sum(lq) + 3, 1, H, H, d, seed=34)[0]
+    base = oracle.backward_varlen(q, k, v, g, cu_q, cu_k)
+    assert not base["dk"][cu_k[1]:cu_k[2]].any() and not base["dv"][cu_k[1]:cu_k[2]].any()
+    assert not base["dq"][cu_q[2]:cu_q[3]].any()
+    assert not base["covered_q"][-3:].any() and not base["covered_k"][-2:].any()
+    # rewriting sequence 3's rows leaves sequence 0 alone
+    q2, k2, v2, g2 = q.clone(), k.clone(), v.clone(), g.clone()
+    for t, cu in ((q2, cu_q), (k2, cu_k), (v2, cu_k), (g2, cu_q)):
+        t[cu[3]:cu[4]] = (torch.randn(t[cu[3]:cu[4]].shape) * 30).to(torch.bfloat16)
+    r = oracle.backward_varlen(q2, k2, v2, g2, cu_q, cu_k)
+    for n, cu in (("dq", cu_q), ("dk", cu_k), ("dv", cu_k)):
+        assert np.array_equal(r[n][cu[0]:cu[1]], base[n][cu[0]:cu[1]]), n
