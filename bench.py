@@ -67,9 +67,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", default="fwd", choices=["fwd", "bwd", "varlen", "paged"],
+    ap.add_argument("--op", default="fwd", choices=["fwd", "bwd", "varlen", "varlen_bwd", "paged"],
                     help="bwd: time the attention backward (attn_bwd) instead of the forward; "
                          "varlen: the forward on a variable-length causal GQA prefill batch; "
+                         "varlen_bwd: the backward on that batch; "
                          "paged: a chunked prefill over a paged K/V cache")
     ap.add_argument("--deterministic", action="store_true",
                     help="with --op bwd: the deterministic backward (dQ summed in key-tile order)")
@@ -356,9 +357,11 @@ def varlen_lengths():
     return np.random.default_rng(VARLEN_SEED).integers(256, 8193, VARLEN_SEQS).tolist()
 
 
-def run_varlen(args):
-    """Time attn_fwd_varlen on resident inputs.  FLOP per call: 4*d per visible (query, key)
-    pair and head, summed over the sequences (the causal mask's hidden half not counted)."""
+def run_varlen(args, backward=False):
+    """Time attn_fwd_varlen (or, with ``backward``, attn_bwd_varlen on the forward's output
+    and LSE) on resident inputs.  FLOP per call: 4*d (backward: 10*d, five products) per
+    visible (query, key) pair and head, summed over the sequences (the causal mask's hidden
+    half not counted)."""
     assert torch.cuda.is_available(), "bench.py needs a CUDA device"
     dev = torch.device("cuda", 0)
     import bf16_attention_forward_gb300 as attn
@@ -379,6 +382,18 @@ def run_varlen(args):
     def call():
         attn.attn_fwd_varlen(q, k, v, cu, cu, max_seqlen_q=max(lens), o=o, causal=True, workspace=ws)
 
+    if backward:
+        o, lse = attn.attn_fwd_varlen(q, k, v, cu, cu, causal=True, return_lse=True)
+        g = make_qkv(1, VARLEN_H, total, 1, VARLEN_D, "bshd", seed=VARLEN_SEED + 77)[0][0].to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        b = attn.BwdVarlenArgs()
+        b.B, b.H, b.Hkv, b.total_q, b.total_k, b.d = len(lens), VARLEN_H, VARLEN_HKV, total, total, VARLEN_D
+        bws = torch.empty(int(attn.load().attn_bwd_varlen_workspace_size(ctypes.byref(b))), dtype=torch.uint8,
+                          device=dev)
+
+        def call():
+            attn.attn_bwd_varlen(q, k, v, o, g, lse, cu, cu, causal=True, dq=dq, dk=dk, dv=dv, workspace=bws)
+
     for _ in range(warmup):
         call()
     torch.cuda.synchronize(dev)
@@ -391,27 +406,33 @@ def run_varlen(args):
         torch.cuda.synchronize(dev)
     st, site = attn.device_status()
     assert st == 0, "device status %d at site %d" % (st, site)
+    if backward:
+        st, site = attn.bwd_device_status()
+        assert st == 0, "backward device status %d at site %d" % (st, site)
     ms = t0.elapsed_time(t1) / steps
     pairs = sum(n * (n + 1) // 2 for n in lens)
-    flop = 4 * VARLEN_H * VARLEN_D * pairs
+    flop = (10 if backward else 4) * VARLEN_H * VARLEN_D * pairs
     value = flop / (ms * 1e-3) / 1e12
     peak, _, _, peak_src = measured_peaks()
     line = {
-        "metric": "attention fwd TFLOPS (4*d per visible pair and head, variable-length batch)",
+        "metric": ("attention bwd TFLOPS (10*d per visible pair and head, variable-length batch)" if backward else
+                   "attention fwd TFLOPS (4*d per visible pair and head, variable-length batch)"),
         "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": steps, "warmup": warmup,
         "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16)",
-        "config": {"workload": "varlen_prefill", "sequences": len(lens), "lengths": lens,
+        "config": {"workload": "varlen_prefill" + ("_bwd" if backward else ""), "sequences": len(lens), "lengths": lens,
                    "total_tokens": total, "H": VARLEN_H, "Hkv": VARLEN_HKV, "d": VARLEN_D, "causal": True,
                    "layout": "packed tokens [T, H, d]", "modes": ["rtne"], "flop_per_call": flop,
-                   "step": "one attn_fwd_varlen call: the offsets/tensor-map preprocessing kernel and "
-                           "the attention kernel",
+                   "step": ("one attn_bwd_varlen call: planning (offsets, tensor maps, units), row "
+                            "statistics with the dQ zeroing, the tcgen05 backward kernel, the dQ rounding")
+                           if backward else ("one attn_fwd_varlen call: the offsets/tensor-map preprocessing "
+                                             "kernel and the attention kernel"),
                    "l2": "inputs %.0f MB > 126 MB L2" % ((q.numel() + k.numel() + v.numel()) * 2 / 2**20)},
         "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
                      "frac": value / peak, "peak_source": peak_src + " burst bf16 (cuBLAS)",
                      "timed": "whole call"},
         "clocks": clocks.summary(),
-        "gpu_launches": 2 * steps,
+        "gpu_launches": (4 if backward else 2) * steps,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -511,8 +532,8 @@ def main():
         return run_reference(args, w, rank, world)
     if args.op == "bwd":
         return run_backward(args, w)
-    if args.op == "varlen":
-        return run_varlen(args)
+    if args.op in ("varlen", "varlen_bwd"):
+        return run_varlen(args, backward=args.op == "varlen_bwd")
     if args.op == "paged":
         return run_paged(args)
 
