@@ -32,6 +32,10 @@
 //   * a last kernel rounds the dQ accumulator to bf16 (round to nearest even), or first adds
 //     each row's key-tile slices in key-tile order (deterministic mode), and adds the split
 //     units' dK/dV partials in part order.
+// Variable-length batches (attn_bwd_varlen, the backward of attn_fwd_varlen) add a one-CTA
+// planning kernel in front (per-sequence tensor maps narrowed with tensormap.replace, padded
+// statistics offsets, the units heaviest first) and run varlen instances of the other three
+// ("varlen" below).
 // Each kernel is a programmatic dependent of the one before it in the stream.
 // Roles: warp 8 TMA producer, warp 9 (one thread) MMA issuer; warpgroups 0 and 1 recompute P
 // and form dS for query columns 0..63 and 64..127 of each step, then each drains half of dQ's

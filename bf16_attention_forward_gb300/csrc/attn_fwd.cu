@@ -35,7 +35,12 @@
 //   * the kernels are templates on the head dimension and on the causal mask.  The causal
 //     mask and grouped K/V heads are the features the [MoonMath] limitations paragraph lists
 //     as missing; d = 64 is the second tile configuration of "HipKittens: Fast and Furious
-//     AMD Kernels (MLSys 2026)", "Experiments and results".
+//     AMD Kernels (MLSys 2026)", "Experiments and results";
+//   * variable-length batches (the third missing feature of that paragraph) and a paged K/V
+//     cache ("AMD zverejnilo postup pre custom diffusion attention kernel vo FlyDSL na ROCm",
+//     the section on what AMD describes) run on a third template flag of the main kernel,
+//     after a one-CTA kernel that narrows tensor maps to each sequence with tensormap.replace
+//     and lays out the work list ("variable-length batches" below).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -333,8 +338,9 @@ __device__ __forceinline__ float weight_exponent(float s, float c, float m) {
     return fmaf(x, 0x1p-126f, ptx::fmax_nan(x, kMinExponent));
 }
 
-// kVarlen: a variable-length batch (per-sequence tensor maps from p.vl_maps, items from
-// p.vl_items, both written by attn_varlen_prep_kernel); a separate instance.
+// kVarlen: a variable-length batch or a paged K/V cache (per-sequence tensor maps from
+// p.vl_maps, the work list from p.vl_blocks, both written by attn_varlen_prep_kernel); a
+// separate instance.
 template <int D, bool kCausal, bool kVarlen = false>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -1442,7 +1448,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p
         *reinterpret_cast<uint32_t*>(orow + lane * 2) = bits[0] | (bits[1] << 16);
 }
 
-// ------------------------------------------------------------------------------ varlen prep
+// ------------------------------------------------------------------------------ variable-length batches
 // Preprocessing of a variable-length batch, one CTA, before the attention kernel (which is
 // its programmatic dependent and waits for its memory):
 //   * checks the offsets: cu_q and cu_k start at >= 0, never decrease, and end within the
