@@ -6,7 +6,11 @@ K/V heads (grouped or not), query and key lengths around and away from the 128-r
 three rounding modes, the causal mask, forced key splits and the logit scale.  Every output
 element (and the LSE) must meet the same criteria as everywhere else: within 2 bf16 ULP of
 the oracle or its forward-error bound, non-finite values bitwise equal.  The backward draws
-smaller shapes and checks dQ, dK and dV element by element.
+smaller shapes and checks dQ, dK and dV element by element.  Variable-length batches draw
+sequence lengths from 0, 1, 2 and the tile edges up to 700 (empty and key-less sequences
+included); each goes through attn_fwd_varlen against the oracle, through attn_fwd_paged with
+its keys in shuffled cache pages (bit for bit the varlen result), and through the varlen
+backward.
 """
 import random
 
@@ -80,3 +84,56 @@ def test_backward_random_shape(attn, case):
                        Hkv=c["Hkv"])
     g = make_qkv(c["B"], c["H"], c["Sq"], 1, c["d"], c["layout"], seed=c["seed"] + 1)[0]
     check_bwd(attn, q, k, v, g, c["layout"], causal=c["causal"])
+
+
+LEN = (0, 1, 2, 63, 127, 128, 129, 255, 256, 257, 300, 511, 700)
+
+
+def _varlen_cases(n=12, seed=20261205):
+    rng = random.Random(seed)
+    out = []
+    for i in range(n):
+        Hkv = rng.choice((1, 2))
+        B = rng.choice((1, 2, 3, 5))
+        causal = rng.random() < 0.5
+        lq = [rng.choice(LEN) for _ in range(B)]
+        lk = lq if causal and rng.random() < 0.5 else [rng.choice(LEN) for _ in range(B)]
+        out.append(dict(lq=lq, lk=lk, H=Hkv * rng.choice((1, 2, 4)), Hkv=Hkv, d=rng.choice((128, 64)),
+                        mode=rng.choice(("rtne", "rtna", "rtz")), causal=causal, P=rng.choice((128, 256)),
+                        seed=7000 + i))
+    return out
+
+
+def _vid(c):
+    return "B%dH%dKV%dd%d%s" % (len(c["lq"]), c["H"], c["Hkv"], c["d"], "c" if c["causal"] else "")
+
+
+@pytest.mark.parametrize("case", _varlen_cases(), ids=_vid)
+def test_varlen_paged_random(attn, case):
+    # the same random batch through attn_fwd_varlen (against the oracle) and through
+    # attn_fwd_paged with its keys in shuffled cache pages (bit for bit the varlen result)
+    from tests.test_gpu_paged import build_cache, run_paged
+    from tests.test_gpu_varlen import check_varlen, offsets, packed
+    c = case
+    if sum(c["lq"]) == 0:
+        c["lq"][0] = 1
+    q, k, v = packed(sum(c["lq"]), max(sum(c["lk"]), 1), c["H"], c["Hkv"], c["d"], seed=c["seed"])
+    cu_q, cu_k = offsets(c["lq"]), offsets(c["lk"])
+    o, lse = check_varlen(attn, q, k, v, cu_q, cu_k, c["mode"], c["causal"])
+    kc, vc, table = build_cache(k, v, c["lk"], c["P"], seed=c["seed"])
+    op, lp = run_paged(attn, q, kc, vc, cu_q, c["lk"], table, c["mode"], c["causal"])
+    assert attn.device_status()[0] == 0
+    assert torch.equal(op.view(torch.int16), o.view(torch.int16))
+    assert torch.equal(lp.view(torch.int32), lse.view(torch.int32))
+
+
+@pytest.mark.parametrize("case", _varlen_cases(n=6, seed=20261206), ids=_vid)
+def test_varlen_backward_random(attn, case):
+    from tests.test_gpu_backward_varlen import check
+    from tests.test_gpu_varlen import offsets, packed
+    c = case
+    if sum(c["lq"]) == 0:
+        c["lq"][0] = 1
+    q, k, v = packed(sum(c["lq"]), max(sum(c["lk"]), 1), c["H"], c["Hkv"], c["d"], seed=c["seed"])
+    g = packed(sum(c["lq"]), 1, c["H"], c["H"], c["d"], seed=c["seed"] + 1)[0]
+    check(attn, q, k, v, g, offsets(c["lq"]), offsets(c["lk"]), c["causal"])
