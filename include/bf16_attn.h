@@ -64,7 +64,9 @@ typedef enum { ATTN_ROUND_RTNE = 0, ATTN_ROUND_RTNA = 1, ATTN_ROUND_RTZ = 2 } at
 
 typedef enum {
     ATTN_OK = 0,
-    ATTN_ERR_INVALID_ARG = 1,    /* null pointer, a size < 1, a bad enum value            */
+    ATTN_ERR_INVALID_ARG = 1,    /* null pointer, a size < 1, a bad enum value; also read
+                                    back from the device for bad variable-length offsets,
+                                    lengths or page indices                               */
     ATTN_ERR_UNSUPPORTED = 2,    /* d not 64 or 128, or a size beyond the kernels' int32 indexing */
     ATTN_ERR_MISALIGNED = 3,     /* a tensor or workspace base not 16-byte aligned         */
     ATTN_ERR_ALIAS = 4,          /* o overlaps q, k or v                                   */
