@@ -67,11 +67,14 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", default="fwd", choices=["fwd", "bwd", "varlen", "varlen_bwd", "paged"],
+    ap.add_argument("--op", default="fwd", choices=["fwd", "bwd", "varlen", "varlen_bwd", "paged", "paged_decode"],
                     help="bwd: time the attention backward (attn_bwd) instead of the forward; "
                          "varlen: the forward on a variable-length causal GQA prefill batch; "
                          "varlen_bwd: the backward on that batch; "
-                         "paged: a chunked prefill over a paged K/V cache")
+                         "paged: a chunked prefill over a paged K/V cache; "
+                         "paged_decode: one query per sequence over a paged cache, heads packed")
+    ap.add_argument("--no-pack", action="store_true",
+                    help="with --op paged_decode: one query head per tile (no head packing)")
     ap.add_argument("--deterministic", action="store_true",
                     help="with --op bwd: the deterministic backward (dQ summed in key-tile order)")
     return ap.parse_args()
@@ -442,11 +445,15 @@ def run_varlen(args, backward=False):
 # [2048, 16384] tokens (256-slot pages in a shuffled order), each with its last 512 tokens as
 # the new query chunk (causal, aligned at the end), 32 query heads on 8 K/V heads, d = 128.
 PAGED_SEQS, PAGED_CHUNK, PAGED_PAGE, PAGED_SEED = 16, 512, 256, 10
+# Decoding over a paged cache: 64 sequences with seeded cache lengths in [4096, 16384], one new
+# query each (the last cache slot), query heads packed per K/V head unless --no-pack.
+DECODE_SEQS, DECODE_SEED = 64, 11
 
 
-def run_paged(args):
+def run_paged(args, decode=False):
     """Time attn_fwd_paged on resident inputs.  FLOP per call: 4*d per visible (query, key)
-    pair and head."""
+    pair and head.  Decoding is memory-bound: its line also reports the K/V bytes per second
+    against the HBM peak."""
     import numpy as np
     assert torch.cuda.is_available(), "bench.py needs a CUDA device"
     dev = torch.device("cuda", 0)
@@ -454,8 +461,10 @@ def run_paged(args):
     attn.load()
     steps = args.steps if args.steps is not None else 50
     warmup = max(3, args.warmup if args.warmup is not None else 10)
-    rng = np.random.default_rng(PAGED_SEED)
-    lens_k = rng.integers(2048, 16385, PAGED_SEQS).tolist()
+    seqs, chunk = (DECODE_SEQS, 1) if decode else (PAGED_SEQS, PAGED_CHUNK)
+    pack = decode and not args.no_pack
+    rng = np.random.default_rng(DECODE_SEED if decode else PAGED_SEED)
+    lens_k = rng.integers(4096 if decode else 2048, 16385, seqs).tolist()
     need = [-(-n // PAGED_PAGE) for n in lens_k]
     n_pages = sum(need)
     H, Hkv, d = VARLEN_H, VARLEN_HKV, VARLEN_D
@@ -463,25 +472,27 @@ def run_paged(args):
     kc = torch.randn((n_pages, PAGED_PAGE, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
     vc = torch.randn((n_pages, PAGED_PAGE, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
     order = rng.permutation(n_pages)
-    table = np.zeros((PAGED_SEQS, max(need)), dtype=np.int32)
+    table = np.zeros((seqs, max(need)), dtype=np.int32)
     nxt = 0
     for b, n in enumerate(need):
         table[b, :n] = order[nxt:nxt + n]
         nxt += n
-    total_q = PAGED_SEQS * PAGED_CHUNK
+    total_q = seqs * chunk
     q = torch.randn((total_q, H, d), generator=g).to(torch.bfloat16).to(dev)
     o = torch.empty_like(q)
-    cu_q = torch.arange(0, total_q + 1, PAGED_CHUNK, dtype=torch.int32, device=dev)
+    cu_q = torch.arange(0, total_q + 1, chunk, dtype=torch.int32, device=dev)
     seqlens = torch.tensor(lens_k, dtype=torch.int32, device=dev)
     bt = torch.as_tensor(table).to(dev)
     import ctypes
     a = attn.PagedArgs()
     a.B, a.H, a.Hkv, a.total_q, a.num_pages, a.page_size, a.max_pages, a.d = \
-        PAGED_SEQS, H, Hkv, total_q, n_pages, PAGED_PAGE, table.shape[1], d
+        seqs, H, Hkv, total_q, n_pages, PAGED_PAGE, table.shape[1], d
+    a.pack_heads = int(pack)
     ws = torch.empty(int(attn.load().attn_fwd_paged_workspace_size(ctypes.byref(a))), dtype=torch.uint8, device=dev)
 
     def call():
-        attn.attn_fwd_paged(q, kc, vc, cu_q, seqlens, bt, max_seqlen_q=PAGED_CHUNK, o=o, causal=True, workspace=ws)
+        attn.attn_fwd_paged(q, kc, vc, cu_q, seqlens, bt, max_seqlen_q=chunk, o=o, causal=True, workspace=ws,
+                            pack_heads=pack)
 
     for _ in range(warmup):
         call()
@@ -497,26 +508,31 @@ def run_paged(args):
     assert st == 0, "device status %d at site %d" % (st, site)
     ms = t0.elapsed_time(t1) / steps
     # query i of a chunk sits at position Sk - C + i and sees Sk - C + i + 1 keys
-    pairs = sum(PAGED_CHUNK * n - PAGED_CHUNK * (PAGED_CHUNK - 1) // 2 for n in lens_k)
+    pairs = sum(chunk * n - chunk * (chunk - 1) // 2 for n in lens_k)
     flop = 4 * H * d * pairs
     value = flop / (ms * 1e-3) / 1e12
     peak, _, hbm, peak_src = measured_peaks()
     kv_bytes = 2 * sum(lens_k) * Hkv * d * 2
     line = {
-        "metric": "attention fwd TFLOPS (4*d per visible pair and head, paged K/V chunked prefill)",
-        "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": steps, "warmup": warmup,
+        "metric": ("attention fwd K/V GB/s (paged K/V decoding: each cache's keys and values read once)" if decode
+                   else "attention fwd TFLOPS (4*d per visible pair and head, paged K/V chunked prefill)"),
+        "value": kv_bytes / (ms * 1e-3) / 1e9 if decode else value, "unit": "GB/s" if decode else "TFLOPS",
+        "n_gpus": 1, "steps": steps, "warmup": warmup,
         "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16)",
-        "config": {"workload": "paged_chunked_prefill", "sequences": PAGED_SEQS, "cache_lengths": lens_k,
-                   "chunk": PAGED_CHUNK, "page_size": PAGED_PAGE, "pages": n_pages, "H": H, "Hkv": Hkv,
-                   "d": d, "causal": True, "modes": ["rtne"], "flop_per_call": flop,
-                   "kv_bytes_read": kv_bytes,
+        "config": {"workload": "paged_decode" if decode else "paged_chunked_prefill", "sequences": seqs,
+                   "cache_lengths": lens_k, "chunk": chunk, "page_size": PAGED_PAGE, "pages": n_pages, "H": H,
+                   "Hkv": Hkv, "d": d, "causal": True, "pack_heads": pack, "modes": ["rtne"], "flop_per_call": flop,
+                   "tflops": value, "kv_bytes_read": kv_bytes,
                    "step": "one attn_fwd_paged call: the offsets/table/tensor-map preprocessing kernel "
                            "and the attention kernel",
                    "l2": "K/V cache %.0f MB > 126 MB L2" % (2 * kc.numel() * 2 / 2**20)},
-        "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
-                     "frac": value / peak, "peak_source": peak_src + " burst bf16 (cuBLAS)",
-                     "timed": "whole call", "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm},
+        "roofline": ({"bound": "hbm", "achieved": kv_bytes / (ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                      "frac": kv_bytes / (ms * 1e-3) / 1e9 / hbm, "peak_source": peak_src + " HBM copy",
+                      "timed": "whole call"} if decode else
+                     {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
+                      "frac": value / peak, "peak_source": peak_src + " burst bf16 (cuBLAS)",
+                      "timed": "whole call", "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm}),
         "clocks": clocks.summary(),
         "gpu_launches": 2 * steps,
     }
@@ -536,6 +552,8 @@ def main():
         return run_varlen(args, backward=args.op == "varlen_bwd")
     if args.op == "paged":
         return run_paged(args)
+    if args.op == "paged_decode":
+        return run_paged(args, decode=True)
 
     import torch.distributed as dist
     if world > 1:

@@ -155,6 +155,10 @@ struct FwdParams {
     const int* seqlens_k;  // [B]
     const int* block_table;
     int page_size, max_pages;
+    // head packing (variable-length batches): the 2^pack_shift query heads that share a K/V
+    // head are the rows of one tile, row r = token (r >> pack_shift), head h + (r & mask), so a
+    // 256-row block holds 256 >> pack_shift tokens; 0: one head per tile
+    int pack_shift;
 };
 
 struct Item {
@@ -181,10 +185,11 @@ __device__ __forceinline__ int round_item(int r) {
 template <bool kCausal>
 __device__ __forceinline__ Item decode_varlen_item(const FwdParams& p, int k) {
     Item it;
-    const int2 e = __ldg(p.vl_blocks + k / p.H);
+    const int per_block = p.H >> p.pack_shift;        // items per (sequence, query block)
+    const int2 e = __ldg(p.vl_blocks + k / per_block);
     it.b = e.x;
     it.qb = e.y;
-    it.h = k % p.H;
+    it.h = (k % per_block) << p.pack_shift;          // the first of the tile's heads
     const int q0 = __ldg(p.cu_q + it.b);
     it.sq = __ldg(p.cu_q + it.b + 1) - q0;
     it.skv = p.paged ? __ldg(p.seqlens_k + it.b) : __ldg(p.cu_k + it.b + 1) - __ldg(p.cu_k + it.b);
@@ -194,7 +199,7 @@ __device__ __forceinline__ Item decode_varlen_item(const FwdParams& p, int k) {
     it.kv_end = (it.skv + kBN - 1) / kBN;
     it.split_slot = -1;
     if constexpr (kCausal) {
-        const int last = it.qb * kUnitRows + kUnitRows - 1 + it.causal_off;   // last visible key
+        const int last = ((it.qb + 1) * kUnitRows >> p.pack_shift) - 1 + it.causal_off;   // last visible key
         const int need = last < 0 ? 1 : last / kBN + 1;
         it.kv_end = need < it.kv_end ? need : it.kv_end;
     }
@@ -422,7 +427,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 }
                 ptx::mbar_arrive_expect_tx(bar(G::kBarQFull), kQTiles * G::kTileBytes);
                 for (int t = 0; t < kQTiles; ++t) {
-                    const int row = it.qb * kUnitRows + t * kBM;
+                    // first token of the tile (with head packing, 128 >> pack_shift tokens
+                    // of 2^pack_shift heads each: the Q map's box is (64, 2^shift, 128 >> shift))
+                    const int row = kVarlen ? (it.qb * kUnitRows + t * kBM) >> p.pack_shift : it.qb * kUnitRows + t * kBM;
                     for (int c = 0; c < G::kChunks; ++c) {
                         const uint32_t dst = sbase + G::kSmemQ + t * G::kTileBytes + c * kChunkBytes;
                         if (kVarlen || p.bshd)
@@ -603,7 +610,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 const int skv = kVarlen ? it.skv : p.Skv;
                 if constexpr (kCausal) {
                     limit = skv - j * kBN - 1;
-                    const int diag = it.qb * kUnitRows + t * kBM + row + (kVarlen ? it.causal_off : p.causal_off) - j * kBN;
+                    const int qpos = kVarlen ? (it.qb * kUnitRows + t * kBM + row) >> p.pack_shift
+                                             : it.qb * kUnitRows + t * kBM + row;   // the row's query
+                    const int diag = qpos + (kVarlen ? it.causal_off : p.causal_off) - j * kBN;
                     limit = diag < limit ? diag : limit;
                 } else {
                     const int valid = skv - j * kBN;   // the same for every row of the tile
@@ -739,7 +748,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             ok = wait_bar(bar(G::kBarOFull + t), u & 1, kSiteOFull, abort_flag, lim);
             if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             ptx::tc_fence_after();
-            const int qrow = it.qb * kUnitRows + t * kBM + row;
+            const int qrow = kVarlen ? (it.qb * kUnitRows + t * kBM + row) >> p.pack_shift
+                                     : it.qb * kUnitRows + t * kBM + row;
             const bool valid_row = qrow < (kVarlen ? it.sq : p.Sq);
             // the whole O_t row in registers with one TMEM wait
             uint32_t o[D];
@@ -749,12 +759,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 const float inv = 1.0f / l;
                 // natural-log log-sum-exp of the scaled logits: (m_ref*c + log2 l) * ln 2
                 if (p.lse && valid_row) {
-                    const long long li = kVarlen ? (long long)it.h * p.total_q + it.q0 + qrow
+                    const int hrow = kVarlen ? it.h + (row & ((1 << p.pack_shift) - 1)) : it.h;
+                    const long long li = kVarlen ? (long long)hrow * p.total_q + it.q0 + qrow
                                                  : ((long long)it.b * p.H + it.h) * p.Sq + qrow;
                     p.lse[li] = (m_ref * c + log2f(l)) * kLn2;
                 }
                 const uint32_t region = sbase + G::kSmemStage + (uint32_t)(warp * kStageBytes);
-                const int r0 = it.qb * kUnitRows + t * kBM + quarter * kStageRowsPerWarp;
+                // the warp's first token (with head packing its 32 rows are 32 >> pack_shift
+                // tokens of 2^pack_shift heads: the O map's box is (64, 2^shift, 32 >> shift))
+                const int r0 = kVarlen ? (it.qb * kUnitRows + t * kBM + quarter * kStageRowsPerWarp) >> p.pack_shift
+                                       : it.qb * kUnitRows + t * kBM + quarter * kStageRowsPerWarp;
 #pragma unroll
                 for (int hc = 0; hc < D / 64; ++hc) {
                     uint32_t w[32];
@@ -1473,6 +1487,7 @@ struct VarlenPrep {
     const int* seqlens_k;                  // paged: keys per sequence
     const int* block_table;                // paged: [B][max_pages]
     int paged, page_size, max_pages, num_pages;
+    int pack_shift;                        // head packing: 2^shift heads per tile row group
     int B, H, causal;
     long long total_q, total_k;
     long long q_row_bytes, kv_row_bytes;   // bytes per token row: H*d*2, Hkv*d*2
@@ -1501,11 +1516,12 @@ __device__ __forceinline__ void narrow_map(CUtensorMap* dst, const void* base, i
     asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 2, %1;" ::"l"(dst), "r"(rows) : "memory");
 }
 
-// key tiles the attention kernel runs for query block qb of a sequence (its bucket)
-__device__ __forceinline__ int block_cost(int qb, int sq, int skv, int causal) {
+// key tiles the attention kernel runs for query block qb of a sequence (its bucket); a block
+// holds 256 >> shift tokens (shift: the head packing's)
+__device__ __forceinline__ int block_cost(int qb, int sq, int skv, int causal, int shift) {
     int tiles = (skv + kBN - 1) / kBN;
     if (causal) {
-        const int last = qb * kUnitRows + kUnitRows - 1 + skv - sq;   // last visible key
+        const int last = ((qb + 1) * kUnitRows >> shift) - 1 + skv - sq;   // last visible key
         const int need = last < 0 ? 1 : last / kBN + 1;
         tiles = need < tiles ? need : tiles;
     }
@@ -1589,8 +1605,10 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
                 narrow_map(m + 1, a.k + k0 * a.kv_row_bytes, krows);
                 narrow_map(m + 2, a.v + k0 * a.kv_row_bytes, krows);
                 narrow_map(m + 3, a.o + q0 * a.q_row_bytes, sq);
-                const int nqb = (sq + kUnitRows - 1) / kUnitRows;
-                for (int qb = 0; qb < nqb; ++qb) atomicAdd(&bucket[block_cost(qb, sq, skv, a.causal)], 1);
+                const int tb = kUnitRows >> a.pack_shift;        // tokens per block
+                const int nqb = (sq + tb - 1) / tb;
+                for (int qb = 0; qb < nqb; ++qb)
+                    atomicAdd(&bucket[block_cost(qb, sq, skv, a.causal, a.pack_shift)], 1);
             }
         }
         // queries with no keys: the warp writes each such sequence's NaN rows and -inf LSE
@@ -1633,7 +1651,7 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
     }
     __syncthreads();
     int start = (wid > 0 ? warp_sums[wid - 1] : 0) + incl - local;
-    if (tid == nthreads - 1) *a.n_items = (start + local) * a.H;
+    if (tid == nthreads - 1) *a.n_items = (start + local) * (a.H >> a.pack_shift);
     __syncthreads();
     if (tid < 1024)
         for (int i = 0; i < kPer; ++i) {
@@ -1647,9 +1665,10 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
     for (int b = tid; b < a.B; b += nthreads) {
         const int sq = a.cu_q[b + 1] - a.cu_q[b], skv = seq_keys(a, b);
         if (sq <= 0 || skv <= 0) continue;
-        const int nqb = (sq + kUnitRows - 1) / kUnitRows;
+        const int tb = kUnitRows >> a.pack_shift;
+        const int nqb = (sq + tb - 1) / tb;
         for (int qb = 0; qb < nqb; ++qb) {
-            const int pos = atomicAdd(&bucket[block_cost(qb, sq, skv, a.causal)], 1);
+            const int pos = atomicAdd(&bucket[block_cost(qb, sq, skv, a.causal, a.pack_shift)], 1);
             a.blocks[pos] = make_int2(b, qb);
         }
     }
@@ -1815,14 +1834,14 @@ int device_info(DeviceInfo** out) {
 // Tensor map over one bf16 tensor, dims ordered innermost-first so strides increase:
 // BSHD -> (d, H, S, B), BHSD -> (d, S, H, B); box = 64 d x 128 rows, 128-byte swizzle.
 bool encode_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t H, int64_t S, int64_t d, bool bshd,
-                uint32_t rows = kBM) {
+                uint32_t rows = kBM, uint32_t heads = 1) {
     cuuint64_t dims[4], strides[3];
     cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
     dims[0] = (cuuint64_t)d;
     if (bshd) {
         dims[1] = H; dims[2] = S; dims[3] = B;
         strides[0] = d * 2; strides[1] = H * d * 2; strides[2] = S * H * d * 2;
-        box[0] = 64; box[1] = 1; box[2] = rows; box[3] = 1;
+        box[0] = 64; box[1] = heads; box[2] = rows; box[3] = 1;
     } else {
         dims[1] = S; dims[2] = H; dims[3] = B;
         strides[0] = d * 2; strides[1] = S * d * 2; strides[2] = H * S * d * 2;
@@ -2049,8 +2068,16 @@ struct SeqBatch {
     const int32_t* block_table;
     int64_t B, H, Hkv, total_q, kv_rows, max_seqlen_q, d;
     int64_t paged, page_size, max_pages, num_pages;
-    int32_t round_mode, causal, reserved, reserved2;
+    int32_t round_mode, causal, pack_heads, reserved;
 };
+
+// log2 of the heads packed into one tile's rows (0: no packing)
+int pack_shift(const SeqBatch& a) {
+    int sh = 0;
+    if (a.pack_heads)
+        while ((int64_t(1) << sh) < a.H / a.Hkv) ++sh;
+    return sh;
+}
 
 SeqBatch from_varlen(const attn_varlen_args_t& a) {
     SeqBatch c;
@@ -2059,7 +2086,7 @@ SeqBatch from_varlen(const attn_varlen_args_t& a) {
     c.cu_q = a.cu_seqlens_q; c.cu_k = a.cu_seqlens_k;
     c.B = a.B; c.H = a.H; c.Hkv = a.Hkv; c.total_q = a.total_q; c.kv_rows = a.total_k;
     c.max_seqlen_q = a.max_seqlen_q; c.d = a.d;
-    c.round_mode = a.round_mode; c.causal = a.causal; c.reserved = a.reserved; c.reserved2 = a.reserved2;
+    c.round_mode = a.round_mode; c.causal = a.causal; c.pack_heads = a.pack_heads; c.reserved = a.reserved;
     return c;
 }
 
@@ -2072,7 +2099,7 @@ SeqBatch from_paged(const attn_paged_args_t& a) {
     c.kv_rows = a.num_pages * a.page_size;
     c.max_seqlen_q = a.max_seqlen_q; c.d = a.d;
     c.paged = 1; c.page_size = a.page_size; c.max_pages = a.max_pages; c.num_pages = a.num_pages;
-    c.round_mode = a.round_mode; c.causal = a.causal; c.reserved = a.reserved; c.reserved2 = a.reserved2;
+    c.round_mode = a.round_mode; c.causal = a.causal; c.pack_heads = a.pack_heads; c.reserved = a.reserved;
     return c;
 }
 
@@ -2081,7 +2108,14 @@ int validate_seq_shape(const SeqBatch& a, const attn_options_t* opts) {
         return ATTN_ERR_INVALID_ARG;
     if (a.H % a.Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (a.round_mode < ATTN_ROUND_RTNE || a.round_mode > ATTN_ROUND_RTZ) return ATTN_ERR_INVALID_ARG;
-    if ((a.causal != 0 && a.causal != 1) || a.reserved != 0 || a.reserved2 != 0) return ATTN_ERR_INVALID_ARG;
+    if ((a.causal != 0 && a.causal != 1) || (a.pack_heads != 0 && a.pack_heads != 1) || a.reserved != 0)
+        return ATTN_ERR_INVALID_ARG;
+    // packed heads: a power of two of at most 32 per K/V head, so that a warp's 32 rows hold
+    // whole tokens
+    if (a.pack_heads) {
+        const int64_t g = a.H / a.Hkv;
+        if (g > 32 || (g & (g - 1)) != 0) return ATTN_ERR_UNSUPPORTED;
+    }
     if (a.paged && (a.num_pages < 1 || a.max_pages < 1 || a.page_size < kBN || a.page_size % kBN != 0))
         return ATTN_ERR_INVALID_ARG;
     if (a.d != 128 && a.d != 64) return ATTN_ERR_UNSUPPORTED;
@@ -2097,8 +2131,9 @@ int validate_seq_shape(const SeqBatch& a, const attn_options_t* opts) {
     return ATTN_OK;
 }
 
-// (sequence, query block) pairs a batch can hold: sum_b ceil(Sq_b / 256) <= total_q / 256 + B
-int64_t seq_max_blocks(const SeqBatch& a) { return a.total_q / kUnitRows + a.B; }
+// (sequence, query block) pairs a batch can hold: a block has 256 >> shift tokens, so
+// sum_b ceil(Sq_b / tokens) <= total_q / tokens + B
+int64_t seq_max_blocks(const SeqBatch& a) { return a.total_q / (kUnitRows >> pack_shift(a)) + a.B; }
 
 // workspace: per-sequence tensor maps (128-byte aligned inside it), the item count, the pairs
 size_t seq_ws_bytes(const SeqBatch& a) {
@@ -2145,9 +2180,13 @@ int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace
     // each sequence (a paged cache's maps also serve its full pages as they are); a tensor
     // with no rows gets a one-row map that no item ever uses
     const int64_t tq = a.total_q > 0 ? a.total_q : 1, tk = a.kv_rows > 0 ? a.kv_rows : 1;
+    // with head packing a Q box is 2^shift heads x (128 >> shift) tokens and an O box 2^shift
+    // heads x (32 >> shift) tokens: the same 128 and 32 rows, ordered token-major
+    const int sh = pack_shift(a);
     CUtensorMap qm, km, vm, om;
-    if (!encode_map(&qm, a.q, 1, a.H, tq, d, true) || !encode_map(&km, a.k, 1, a.Hkv, tk, d, true) ||
-        !encode_map(&vm, a.v, 1, a.Hkv, tk, d, true) || !encode_map(&om, a.o, 1, a.H, tq, d, true, kStageRowsPerWarp))
+    if (!encode_map(&qm, a.q, 1, a.H, tq, d, true, (uint32_t)(kBM >> sh), 1u << sh) ||
+        !encode_map(&km, a.k, 1, a.Hkv, tk, d, true) || !encode_map(&vm, a.v, 1, a.Hkv, tk, d, true) ||
+        !encode_map(&om, a.o, 1, a.H, tq, d, true, (uint32_t)(kStageRowsPerWarp >> sh), 1u << sh))
         return ATTN_ERR_CUDA;
     CUtensorMap* maps = reinterpret_cast<CUtensorMap*>((wsb + 127u) & ~(uintptr_t)127u);
     int* n_items = reinterpret_cast<int*>(maps + 4 * a.B);
@@ -2162,6 +2201,7 @@ int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace
     vp.page_size = (int)a.page_size;
     vp.max_pages = (int)a.max_pages;
     vp.num_pages = (int)a.num_pages;
+    vp.pack_shift = sh;
     vp.B = (int)a.B;
     vp.H = (int)a.H;
     vp.causal = a.causal;
@@ -2204,11 +2244,12 @@ int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace
     p.block_table = a.block_table;
     p.page_size = (int)a.page_size;
     p.max_pages = (int)a.max_pages;
+    p.pack_shift = sh;
 
     int64_t G = di->sms;
     if (opts && opts->max_ctas > 0 && opts->max_ctas < G) G = opts->max_ctas;
     if (a.max_seqlen_q > 0) {
-        const int64_t cap = a.B * a.H * cdiv(a.max_seqlen_q, kUnitRows);
+        const int64_t cap = a.B * (a.H >> sh) * cdiv(a.max_seqlen_q, kUnitRows >> sh);
         if (cap < G) G = cap;
     }
     if (G < 1) G = 1;

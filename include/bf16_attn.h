@@ -247,6 +247,12 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, int64
  *   max_seqlen_q  an upper bound on any sequence's query length, used only to size the grid
  *                 (0: unknown, one CTA per SM)
  *   causal        per sequence, aligned at its last query and key (attn_fwd_ex's rule)
+ *   pack_heads    0 or 1.  1: the H / Hkv query heads that read one K/V head (a power of two,
+ *                 at most 32; otherwise ATTN_ERR_UNSUPPORTED) share the rows of one 128-row
+ *                 tile, 128 / (H / Hkv) tokens of each, so short query chunks (decoding, a
+ *                 few speculative tokens) fill the tiles and each K/V tile is read once for
+ *                 the group.  Every row is computed exactly as without packing: the results
+ *                 are bit for bit the same.  Pays off when sequences have few queries.
  *   reserved      must be 0
  * Keys are never split (opts->force_splits must be 0 or 1).  workspace: caller device memory
  * of at least attn_fwd_varlen_workspace_size() bytes (per-sequence tensor maps and work-item
@@ -262,7 +268,7 @@ typedef struct {
     const int32_t* cu_seqlens_q;
     const int32_t* cu_seqlens_k;
     int64_t B, H, Hkv, total_q, total_k, max_seqlen_q, d;
-    int32_t round_mode, causal, reserved, reserved2;
+    int32_t round_mode, causal, pack_heads, reserved;
 } attn_varlen_args_t;
 
 size_t attn_fwd_varlen_workspace_size(const attn_varlen_args_t* args);
@@ -285,6 +291,7 @@ int attn_fwd_varlen(const attn_varlen_args_t* args, const attn_options_t* opts, 
  *   block_table   device int32 [B][max_pages]; entries past a sequence's last used page are
  *                 not read.  Pages may be shared between sequences.
  *   page_size     a multiple of 128 (a key tile never straddles pages)
+ *   pack_heads    as in attn_fwd_varlen (the natural setting for decoding over a paged cache)
  * Checked on the device: bad query offsets, lengths or page indices (outside 0 ..
  * num_pages - 1) write no output and report ATTN_ERR_INVALID_ARG at ATTN_SITE_SEQLENS.  Slots
  * of a sequence's last page past its length are never read as keys (they read as zeros), so
@@ -300,7 +307,7 @@ typedef struct {
     const int32_t* seqlens_k;
     const int32_t* block_table;
     int64_t B, H, Hkv, total_q, num_pages, page_size, max_pages, max_seqlen_q, d;
-    int32_t round_mode, causal, reserved, reserved2;
+    int32_t round_mode, causal, pack_heads, reserved;
 } attn_paged_args_t;
 
 size_t attn_fwd_paged_workspace_size(const attn_paged_args_t* args);

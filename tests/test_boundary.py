@@ -243,11 +243,16 @@ def test_varlen_argument_errors(lib):
     assert run() == 5
     assert run(B=3, total_q=0, total_k=0, max_seqlen_q=7, d=64) == 5
     for bad in ({"B": 0}, {"Hkv": 3}, {"total_q": -1}, {"total_k": -1}, {"max_seqlen_q": -1},
-                {"round_mode": 3}, {"causal": 2}, {"reserved": 1}, {"reserved2": 1},
+                {"round_mode": 3}, {"causal": 2}, {"reserved": 1}, {"pack_heads": 2},
                 {"cu_seqlens_q": 0}, {"cu_seqlens_k": 0}, {"q": 0}, {"o": 0}):
         assert run(**bad) == 1, bad
     assert run(d=96) == 2
     assert run(total_q=(1 << 30) + 1) == 2
+    # packed heads: H / Hkv a power of two of at most 32
+    assert run(pack_heads=1) == 5
+    assert run(pack_heads=1, H=32, Hkv=1) == 5
+    assert run(pack_heads=1, H=6, Hkv=2) == 2
+    assert run(pack_heads=1, H=64, Hkv=1) == 2
     assert run(opts=attn.Options(2, 0, 0, 0)) == 2
     assert run(opts=attn.Options(1, 0, 0, 0)) == 5
     assert run(opts=attn.Options(0, 0, 0, 1)) == 1
@@ -268,6 +273,9 @@ def test_varlen_workspace_size(lib):
         assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(a)) == want, B
     assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(varlen_args(B=0))) == 0
     assert lib.attn_fwd_varlen_workspace_size(None) == 0
+    # with packed heads (here 2 per K/V head) a block holds 128 tokens: room for more pairs
+    a = varlen_args(B=7, total_q=5000, pack_heads=1)
+    assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(a)) == 128 + 7 * 512 + 16 + (5000 // 128 + 7) * 8
 
 
 PG = 1 << 24   # fake pointers for the paged calls, far enough apart for their cache sizes

@@ -188,3 +188,21 @@ def test_paged_bad_tables_are_reported_and_write_nothing(attn, bad):
     assert (o.view(torch.int16) == BF16_SENTINEL).all() and (lse.view(torch.int32) == F32_SENTINEL).all()
     o, _ = run_paged(attn, q, kc, vc, offsets(lq), lk, build_cache(k, v, lk, P, seed=6, spare=0)[2])
     status_ok(attn)
+
+
+def test_paged_decode_with_packed_heads(attn):
+    # one query per sequence over long paged caches, query heads packed per K/V head: the
+    # same bits as without packing, and the oracle's criteria
+    lq, lk, P, H, Hkv, d = [1] * 6, [3000, 1, 257, 1024, 700, 129], 256, 16, 4, 128
+    q, k, v = packed(sum(lq), sum(lk), H, Hkv, d, seed=9950)
+    kc, vc, table = build_cache(k, v, lk, P, seed=9951)
+    cu_q = offsets(lq)
+    o0, l0 = run_paged(attn, q, kc, vc, cu_q, lk, table, "rtne", True)
+    o1, l1 = run_paged(attn, q, kc, vc, cu_q, lk, table, "rtne", True, pack_heads=True, max_seqlen_q=1)
+    status_ok(attn)
+    assert torch.equal(o1.view(torch.int16), o0.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l0.view(torch.int32))
+    ref = oracle.attention_paged(q, kc, vc, cu_q, lk, table, "rtne", causal=True, want_a=True)
+    ob = o1.cpu().view(torch.int16).numpy().view(np.uint16)
+    res = parity.compare(ob.reshape(-1, d), ref["o_bits"].reshape(-1, d), ref["a"].reshape(-1, d))
+    assert res["ok"], res

@@ -222,3 +222,48 @@ def test_varlen_bad_offsets_are_reported_and_write_nothing(attn, bad):
     assert (o.view(torch.int16) == BF16_SENTINEL).all() and (lse.view(torch.int32) == F32_SENTINEL).all()
     # the device stays usable and the status word was cleared by reading it
     check_varlen(attn, q, k, v, cu, cu)
+
+
+PACK = [  # (lens_q, lens_k, H, Hkv, d, causal): decoding-sized and prefill-sized chunks
+    ([1, 1, 1, 1, 1], [700, 129, 1, 300, 2000], 8, 2, 128, True),
+    ([1, 4, 16, 3], [5000, 64, 300, 128], 32, 8, 128, True),
+    ([7, 1, 33], [900, 1000, 33], 16, 2, 64, False),
+    ([300, 129, 700, 0], [300, 700, 700, 5], 8, 1, 128, True),
+    ([257, 64], [513, 64], 4, 4, 128, False),       # one head per K/V head: packing is a no-op
+    ([2, 130], [4000, 600], 64, 2, 64, True),       # 32 heads per K/V head
+]
+
+
+@pytest.mark.parametrize("case", PACK, ids=lambda c: "n%d_H%dKV%d_d%d%s" % (len(c[0]), c[2], c[3], c[4],
+                                                                             "_causal" if c[5] else ""))
+def test_packed_heads_are_bitwise_the_unpacked_result(attn, case):
+    # packing the query heads of a K/V head into one tile changes which rows share a tile,
+    # not any row's arithmetic: outputs and LSE must be the same bits, and meet the oracle
+    lq, lk, H, Hkv, d, causal = case
+    q, k, v = packed(sum(lq), sum(lk), H, Hkv, d, seed=8800 + H + d)
+    cu_q, cu_k = offsets(lq), offsets(lk)
+    o0, l0 = run_varlen(attn, q, k, v, cu_q, cu_k, "rtne", causal)
+    o1, l1 = run_varlen(attn, q, k, v, cu_q, cu_k, "rtne", causal, pack_heads=True, max_seqlen_q=max(lq))
+    status_ok(attn)
+    assert torch.equal(o1.view(torch.int16), o0.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l0.view(torch.int32))
+    check_varlen(attn, q, k, v, cu_q, cu_k, "rtne", causal, pack_heads=True)
+
+
+def test_packed_heads_writes_stay_in_bounds(attn):
+    lq, lk, H, Hkv, d = [1, 3, 77, 130], [200, 5, 129, 400], 8, 2, 128
+    q, k, v = packed(sum(lq), sum(lk), H, Hkv, d, seed=8900)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    obuf, o = guarded(q.numel(), "bf16")
+    lbuf, lse = guarded(H * q.shape[0], "f32")
+    a = attn.VarlenArgs()
+    a.B, a.H, a.Hkv, a.total_q, a.total_k, a.d, a.pack_heads = len(lq), H, Hkv, q.shape[0], k.shape[0], d, 1
+    wbytes = int(attn.load().attn_fwd_varlen_workspace_size(ctypes.byref(a)))
+    wbuf, ws = guarded(wbytes, "ws")
+    cq, ck = (torch.as_tensor(offsets(x)).cuda() for x in (lq, lk))
+    attn.attn_fwd_varlen(qd, kd, vd, cq, ck, o=o.view(q.shape), lse=lse.view(H, -1), workspace=ws, causal=True,
+                         pack_heads=True)
+    torch.cuda.synchronize()
+    status_ok(attn)
+    assert guards_intact(obuf, "bf16") and guards_intact(lbuf, "f32") and guards_intact(wbuf, "ws")
+    assert not (o.view(torch.int16) == 0x7BAD).any() and not (lse.view(torch.int32) == 0x7F7BAD01).any()
