@@ -75,6 +75,8 @@ def parse():
                          "paged_decode: one query per sequence over a paged cache, heads packed")
     ap.add_argument("--no-pack", action="store_true",
                     help="with --op paged_decode: one query head per tile (no head packing)")
+    ap.add_argument("--pack", action="store_true",
+                    help="with --op varlen or paged: pack the query heads of each K/V head into one tile")
     ap.add_argument("--deterministic", action="store_true",
                     help="with --op bwd: the deterministic backward (dQ summed in key-tile order)")
     return ap.parse_args()
@@ -382,8 +384,12 @@ def run_varlen(args, backward=False):
     a.B, a.H, a.Hkv, a.total_q, a.total_k, a.d = len(lens), VARLEN_H, VARLEN_HKV, total, total, VARLEN_D
     ws = torch.empty(int(attn.load().attn_fwd_varlen_workspace_size(ctypes.byref(a))), dtype=torch.uint8, device=dev)
 
+    a.pack_heads = int(args.pack and not backward)
+    ws = torch.empty(int(attn.load().attn_fwd_varlen_workspace_size(ctypes.byref(a))), dtype=torch.uint8, device=dev)
+
     def call():
-        attn.attn_fwd_varlen(q, k, v, cu, cu, max_seqlen_q=max(lens), o=o, causal=True, workspace=ws)
+        attn.attn_fwd_varlen(q, k, v, cu, cu, max_seqlen_q=max(lens), o=o, causal=True, workspace=ws,
+                             pack_heads=args.pack)
 
     if backward:
         o, lse = attn.attn_fwd_varlen(q, k, v, cu, cu, causal=True, return_lse=True)
@@ -424,6 +430,7 @@ def run_varlen(args, backward=False):
         "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16)",
         "config": {"workload": "varlen_prefill" + ("_bwd" if backward else ""), "sequences": len(lens), "lengths": lens,
+                   "pack_heads": bool(args.pack and not backward),
                    "total_tokens": total, "H": VARLEN_H, "Hkv": VARLEN_HKV, "d": VARLEN_D, "causal": True,
                    "layout": "packed tokens [T, H, d]", "modes": ["rtne"], "flop_per_call": flop,
                    "step": ("one attn_bwd_varlen call: planning (offsets, tensor maps, units), row "
@@ -462,7 +469,7 @@ def run_paged(args, decode=False):
     steps = args.steps if args.steps is not None else 50
     warmup = max(3, args.warmup if args.warmup is not None else 10)
     seqs, chunk = (DECODE_SEQS, 1) if decode else (PAGED_SEQS, PAGED_CHUNK)
-    pack = decode and not args.no_pack
+    pack = (decode and not args.no_pack) or (not decode and args.pack)
     rng = np.random.default_rng(DECODE_SEED if decode else PAGED_SEED)
     lens_k = rng.integers(4096 if decode else 2048, 16385, seqs).tolist()
     need = [-(-n // PAGED_PAGE) for n in lens_k]
