@@ -252,7 +252,8 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, int64
  *                 tile, 128 / (H / Hkv) tokens of each, so short query chunks (decoding, a
  *                 few speculative tokens) fill the tiles and each K/V tile is read once for
  *                 the group.  Every row is computed exactly as without packing: the results
- *                 are bit for bit the same.  Pays off when sequences have few queries.
+ *                 are bit for bit the same.  Pays off when sequences have few queries
+ *                 (for decoding a dense batch, pass cu_seqlens = 0, Sq, 2 Sq, ... here).
  *   reserved      must be 0
  * Keys are never split (opts->force_splits must be 0 or 1).  workspace: caller device memory
  * of at least attn_fwd_varlen_workspace_size() bytes (per-sequence tensor maps and work-item
