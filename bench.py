@@ -77,6 +77,11 @@ def parse():
                     help="with --op paged_decode: one query head per tile (no head packing)")
     ap.add_argument("--pack", action="store_true",
                     help="with --op varlen or paged: pack the query heads of each K/V head into one tile")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="with --op varlen, paged or paged_decode: max_splits (>= 2: split the keys of "
+                         "query blocks into up to that many parts when the items number fewer than the CTAs)")
+    ap.add_argument("--decode-seqs", type=int, default=None,
+                    help="with --op paged_decode: the number of sequences (default %d)" % 64)
     ap.add_argument("--deterministic", action="store_true",
                     help="with --op bwd: the deterministic backward (dQ summed in key-tile order)")
     return ap.parse_args()
@@ -385,11 +390,12 @@ def run_varlen(args, backward=False):
     ws = torch.empty(int(attn.load().attn_fwd_varlen_workspace_size(ctypes.byref(a))), dtype=torch.uint8, device=dev)
 
     a.pack_heads = int(args.pack and not backward)
+    a.max_splits = 0 if backward else args.splits
     ws = torch.empty(int(attn.load().attn_fwd_varlen_workspace_size(ctypes.byref(a))), dtype=torch.uint8, device=dev)
 
     def call():
         attn.attn_fwd_varlen(q, k, v, cu, cu, max_seqlen_q=max(lens), o=o, causal=True, workspace=ws,
-                             pack_heads=args.pack)
+                             pack_heads=args.pack, max_splits=args.splits)
 
     if backward:
         o, lse = attn.attn_fwd_varlen(q, k, v, cu, cu, causal=True, return_lse=True)
@@ -431,6 +437,7 @@ def run_varlen(args, backward=False):
         "data": "synthetic (seeded N(0,1) bf16)",
         "config": {"workload": "varlen_prefill" + ("_bwd" if backward else ""), "sequences": len(lens), "lengths": lens,
                    "pack_heads": bool(args.pack and not backward),
+                   "max_splits": 0 if backward else args.splits,
                    "total_tokens": total, "H": VARLEN_H, "Hkv": VARLEN_HKV, "d": VARLEN_D, "causal": True,
                    "layout": "packed tokens [T, H, d]", "modes": ["rtne"], "flop_per_call": flop,
                    "step": ("one attn_bwd_varlen call: planning (offsets, tensor maps, units), row "
@@ -442,7 +449,7 @@ def run_varlen(args, backward=False):
                      "frac": value / peak, "peak_source": peak_src + " burst bf16 (cuBLAS)",
                      "timed": "whole call"},
         "clocks": clocks.summary(),
-        "gpu_launches": (4 if backward else 2) * steps,
+        "gpu_launches": (4 if backward else (3 if args.splits > 1 else 2)) * steps,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -468,7 +475,7 @@ def run_paged(args, decode=False):
     attn.load()
     steps = args.steps if args.steps is not None else 50
     warmup = max(3, args.warmup if args.warmup is not None else 10)
-    seqs, chunk = (DECODE_SEQS, 1) if decode else (PAGED_SEQS, PAGED_CHUNK)
+    seqs, chunk = (args.decode_seqs or DECODE_SEQS, 1) if decode else (PAGED_SEQS, PAGED_CHUNK)
     pack = (decode and not args.no_pack) or (not decode and args.pack)
     rng = np.random.default_rng(DECODE_SEED if decode else PAGED_SEED)
     lens_k = rng.integers(4096 if decode else 2048, 16385, seqs).tolist()
@@ -495,11 +502,12 @@ def run_paged(args, decode=False):
     a.B, a.H, a.Hkv, a.total_q, a.num_pages, a.page_size, a.max_pages, a.d = \
         seqs, H, Hkv, total_q, n_pages, PAGED_PAGE, table.shape[1], d
     a.pack_heads = int(pack)
+    a.max_splits = args.splits
     ws = torch.empty(int(attn.load().attn_fwd_paged_workspace_size(ctypes.byref(a))), dtype=torch.uint8, device=dev)
 
     def call():
         attn.attn_fwd_paged(q, kc, vc, cu_q, seqlens, bt, max_seqlen_q=chunk, o=o, causal=True, workspace=ws,
-                            pack_heads=pack)
+                            pack_heads=pack, max_splits=args.splits)
 
     for _ in range(warmup):
         call()
@@ -529,10 +537,11 @@ def run_paged(args, decode=False):
         "data": "synthetic (seeded N(0,1) bf16)",
         "config": {"workload": "paged_decode" if decode else "paged_chunked_prefill", "sequences": seqs,
                    "cache_lengths": lens_k, "chunk": chunk, "page_size": PAGED_PAGE, "pages": n_pages, "H": H,
-                   "Hkv": Hkv, "d": d, "causal": True, "pack_heads": pack, "modes": ["rtne"], "flop_per_call": flop,
+                   "Hkv": Hkv, "d": d, "causal": True, "pack_heads": pack, "max_splits": args.splits,
+                   "modes": ["rtne"], "flop_per_call": flop,
                    "tflops": value, "kv_bytes_read": kv_bytes,
                    "step": "one attn_fwd_paged call: the offsets/table/tensor-map preprocessing kernel "
-                           "and the attention kernel",
+                           "and the attention kernel" + (" (and the merge of key parts)" if args.splits > 1 else ""),
                    "l2": "K/V cache %.0f MB > 126 MB L2" % (2 * kc.numel() * 2 / 2**20)},
         "roofline": ({"bound": "hbm", "achieved": kv_bytes / (ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
                       "frac": kv_bytes / (ms * 1e-3) / 1e9 / hbm, "peak_source": peak_src + " HBM copy",
@@ -541,7 +550,7 @@ def run_paged(args, decode=False):
                       "frac": value / peak, "peak_source": peak_src + " burst bf16 (cuBLAS)",
                       "timed": "whole call", "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm}),
         "clocks": clocks.summary(),
-        "gpu_launches": 2 * steps,
+        "gpu_launches": (3 if args.splits > 1 else 2) * steps,
     }
     print(json.dumps(line), flush=True)
     return 0

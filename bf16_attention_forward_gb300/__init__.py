@@ -61,7 +61,7 @@ class VarlenArgs(ctypes.Structure):
                                                "cu_seqlens_k")] + \
                [(n, ctypes.c_int64) for n in ("B", "H", "Hkv", "total_q", "total_k",
                                               "max_seqlen_q", "d")] + \
-               [(n, ctypes.c_int32) for n in ("round_mode", "causal", "pack_heads", "reserved")]
+               [(n, ctypes.c_int32) for n in ("round_mode", "causal", "pack_heads", "max_splits")]
 
 
 class PagedArgs(ctypes.Structure):
@@ -70,7 +70,7 @@ class PagedArgs(ctypes.Structure):
                                                "seqlens_k", "block_table")] + \
                [(n, ctypes.c_int64) for n in ("B", "H", "Hkv", "total_q", "num_pages", "page_size",
                                               "max_pages", "max_seqlen_q", "d")] + \
-               [(n, ctypes.c_int32) for n in ("round_mode", "causal", "pack_heads", "reserved")]
+               [(n, ctypes.c_int32) for n in ("round_mode", "causal", "pack_heads", "max_splits")]
 
 
 class BwdVarlenArgs(ctypes.Structure):
@@ -333,7 +333,8 @@ def attn_fwd_ex(q, k, v, o=None, lse=None, layout: str = "bshd", round: str = "r
     return (o, lse) if (return_lse or lse is not None) else o
 
 
-def _varlen_args(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, round, causal, pack_heads=False):
+def _varlen_args(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, round, causal, pack_heads=False,
+                 max_splits=0):
     import torch
     _check_tensors(q, k, v)
     if q.dim() != 3 or k.dim() != 3 or tuple(k.shape) != tuple(v.shape) or q.shape[2] != k.shape[2]:
@@ -352,13 +353,14 @@ def _varlen_args(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, roun
     a.B, a.H, a.Hkv = cu_seqlens_q.numel() - 1, H, Hkv
     a.total_q, a.total_k, a.max_seqlen_q, a.d = q.shape[0], k.shape[0], int(max_seqlen_q), d
     a.round_mode, a.causal, a.pack_heads = MODES[round], int(causal), int(bool(pack_heads))
+    a.max_splits = int(max_splits)
     return a
 
 
 def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int = 0, o=None, lse=None,
                     round: str = "rtne", causal: bool = False, return_lse: bool = False,
                     stream=None, workspace=None, max_ctas: int = 0, wait_limit_ms: int = 0,
-                    events=None, pack_heads: bool = False):
+                    events=None, pack_heads: bool = False, max_splits: int = 0):
     """Attention over a variable-length batch packed along the token axis.
 
     ``q``: [total_q, H, d], ``k``/``v``: [total_k, Hkv, d] (CUDA bf16, contiguous);
@@ -369,7 +371,10 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int = 0, 
     ``max_seqlen_q``: an upper bound on any sequence's query length, used to size the grid
     (0: unknown).  ``lse``: optional fp32 [H, total_q].  ``pack_heads``: the query heads of
     each K/V head share one tile's rows (H / Hkv a power of two up to 32): same results, faster
-    for short query chunks.  Returns ``o`` or ``(o, lse)``.
+    for short query chunks.  ``max_splits`` >= 2: when the items number fewer than the CTAs
+    (a few long sequences, decoding), split each query block's keys into up to that many parts
+    and merge them (deterministic; differs from the unsplit result by rounding).  Returns ``o``
+    or ``(o, lse)``.
     """
     import torch
     if round not in MODES:
@@ -382,7 +387,8 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int = 0, 
     if lse is not None and (lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous()
                             or lse.numel() != q.shape[0] * q.shape[1]):
         raise ValueError("lse must be a contiguous CUDA fp32 tensor of H*total_q elements")
-    a = _varlen_args(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, round, causal, pack_heads)
+    a = _varlen_args(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, round, causal, pack_heads,
+                     max_splits)
     opts = _opts(0, max_ctas, wait_limit_ms, events)
     lib = load()
     ws_ptr, ws_bytes = None, 0
@@ -405,9 +411,9 @@ def _int32_cuda(t, name, dim):
 def attn_fwd_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table, max_seqlen_q: int = 0,
                    o=None, lse=None, round: str = "rtne", causal: bool = False,
                    return_lse: bool = False, stream=None, workspace=None, max_ctas: int = 0,
-                   wait_limit_ms: int = 0, events=None, pack_heads: bool = False):
-    """Attention of packed queries over a paged K/V cache (``pack_heads`` as in
-    :func:`attn_fwd_varlen`).
+                   wait_limit_ms: int = 0, events=None, pack_heads: bool = False, max_splits: int = 0):
+    """Attention of packed queries over a paged K/V cache (``pack_heads`` and ``max_splits``
+    as in :func:`attn_fwd_varlen`).
 
     ``q``: [total_q, H, d]; ``k_cache``/``v_cache``: [num_pages, page_size, Hkv, d] (CUDA bf16,
     contiguous; page_size a multiple of 128); ``cu_seqlens_q``: CUDA int32 [B + 1];
@@ -448,6 +454,7 @@ def attn_fwd_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table, ma
     a.num_pages, a.page_size, a.max_pages = k_cache.shape[0], k_cache.shape[1], block_table.shape[1]
     a.max_seqlen_q, a.d = int(max_seqlen_q), q.shape[2]
     a.round_mode, a.causal, a.pack_heads = MODES[round], int(causal), int(bool(pack_heads))
+    a.max_splits = int(max_splits)
     opts = _opts(0, max_ctas, wait_limit_ms, events)
     lib = load()
     ws_ptr, ws_bytes = None, 0

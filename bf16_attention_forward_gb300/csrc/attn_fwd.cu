@@ -139,10 +139,11 @@ struct FwdParams {
     int test_hooks;        // ATTN_TEST_WITHHOLD_O_READY: CTA 0 skips its first unit's O-ready signal
     // variable-length batches (the kVarlen instance only): B sequences packed along the token
     // axis; per sequence b a tensor map each for Q, K, V and O (vl_maps[4 b + 0..3]) that
-    // covers only its rows; the (sequence, query block) pairs to run, heaviest first
-    // (vl_blocks), each standing for H items (one per query head), and the item count
+    // covers only its rows; the work list, heaviest first (vl_blocks: sequence, query block,
+    // key part, parts), each entry standing for H >> pack_shift items (one per query head or
+    // packed head group), and the item count
     const CUtensorMap* vl_maps;
-    const int2* vl_blocks;
+    const int4* vl_blocks;
     const int* vl_n_items;
     const int* cu_q;       // [B + 1] query row offsets
     const int* cu_k;       // [B + 1] key row offsets (unpaged)
@@ -179,14 +180,16 @@ __device__ __forceinline__ int round_item(int r) {
     return r * (int)gridDim.x + c;
 }
 
-// Work item k of a variable-length batch: query head k % H of the (sequence, 256-row query
-// block) pair vl_blocks[k / H], which the preprocessing kernel ordered by the key tiles they
-// run, most first.  Lengths and offsets come from the sequence; nothing is split.
+// Work item k of a variable-length batch: query head (or packed head group) k % per_block of
+// the entry vl_blocks[k / per_block], which the preprocessing kernel ordered by the key tiles
+// they run, most first.  Lengths and offsets come from the sequence.  An entry (b, qb, part,
+// parts) with parts > 1 runs the part-th of `parts` near-equal contiguous ranges of the block's
+// key tiles into split slot k, and the variable-length combine kernel merges the parts.
 template <bool kCausal>
 __device__ __forceinline__ Item decode_varlen_item(const FwdParams& p, int k) {
     Item it;
-    const int per_block = p.H >> p.pack_shift;        // items per (sequence, query block)
-    const int2 e = __ldg(p.vl_blocks + k / per_block);
+    const int per_block = p.H >> p.pack_shift;        // items per entry
+    const int4 e = __ldg(p.vl_blocks + k / per_block);
     it.b = e.x;
     it.qb = e.y;
     it.h = (k % per_block) << p.pack_shift;          // the first of the tile's heads
@@ -195,13 +198,21 @@ __device__ __forceinline__ Item decode_varlen_item(const FwdParams& p, int k) {
     it.skv = p.paged ? __ldg(p.seqlens_k + it.b) : __ldg(p.cu_k + it.b + 1) - __ldg(p.cu_k + it.b);
     it.q0 = q0;
     it.causal_off = it.skv - it.sq;
-    it.kv_begin = 0;
-    it.kv_end = (it.skv + kBN - 1) / kBN;
-    it.split_slot = -1;
+    int tiles = (it.skv + kBN - 1) / kBN;
     if constexpr (kCausal) {
         const int last = ((it.qb + 1) * kUnitRows >> p.pack_shift) - 1 + it.causal_off;   // last visible key
         const int need = last < 0 ? 1 : last / kBN + 1;
-        it.kv_end = need < it.kv_end ? need : it.kv_end;
+        tiles = need < tiles ? need : tiles;
+    }
+    if (e.w > 1) {
+        const int base = tiles / e.w, rem = tiles % e.w;
+        it.kv_begin = e.z * base + (e.z < rem ? e.z : rem);
+        it.kv_end = it.kv_begin + base + (e.z < rem ? 1 : 0);
+        it.split_slot = k;
+    } else {
+        it.kv_begin = 0;
+        it.kv_end = tiles;
+        it.split_slot = -1;
     }
     it.hk = p.group == 1 ? it.h : it.h / p.group;
     return it;
@@ -1476,10 +1487,18 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p
 //   * the work list: every (sequence, 256-row query block) pair, ordered by the key tiles it
 //     runs, most first (a counting sort on that count, capped at kCostBuckets - 1; pairs of
 //     equal count in any order, which moves work between CTAs but changes no result), and
-//     the item count, H per pair;
+//     the item count, H >> pack_shift per entry;
+//   * key splits (max_splits >= 2), when the pairs' items number fewer than the attention
+//     kernel's CTAs: with P pairs and Gp = CTAs / (items per pair) entry places, a pair of
+//     cost c becomes n(c) = min(max_splits, Gp, ceil(c / M)) consecutive entries (b, qb,
+//     part, n) for the smallest M (tiles in the longest part) with sum n(c) <= Gp.  Every item then
+//     has a CTA of its own and a split slot below the CTA count, and the longest part is as
+//     short as one wave allows.  n depends only on c (and the launch), so the result is a
+//     function of the inputs and the CTA count;
 //   * a sequence with queries but no keys: every query sees no key, so its O rows are NaN
 //     (stored 0x7FC0) and its LSE rows -inf, written here.
 constexpr int kCostBuckets = 4096;
+constexpr int kMaxDistinct = 1024;        // key splits: distinct pair costs considered
 
 struct VarlenPrep {
     const int* cu_q;
@@ -1488,6 +1507,8 @@ struct VarlenPrep {
     const int* block_table;                // paged: [B][max_pages]
     int paged, page_size, max_pages, num_pages;
     int pack_shift;                        // head packing: 2^shift heads per tile row group
+    int max_splits;                        // key parts per pair at most (< 2: no splits)
+    int grid;                              // the attention kernel's CTAs
     int B, H, causal;
     long long total_q, total_k;
     long long q_row_bytes, kv_row_bytes;   // bytes per token row: H*d*2, Hkv*d*2
@@ -1497,7 +1518,7 @@ struct VarlenPrep {
     char* o;
     float* lse;                            // optional [H][total_q]
     CUtensorMap* maps;                     // [B][4]: Q, K, V, O
-    int2* blocks;                          // (sequence, query block) pairs, heaviest first
+    int4* blocks;                          // (sequence, query block, part, parts), heaviest first
     int* n_items;
 };
 
@@ -1528,6 +1549,13 @@ __device__ __forceinline__ int block_cost(int qb, int sq, int skv, int causal, i
     return tiles < kCostBuckets - 1 ? tiles : kCostBuckets - 1;
 }
 
+// key parts of a pair of cost c with at most M tiles a part (c >= 1, so every part has a tile:
+// ceil(c / M) <= c)
+__device__ __forceinline__ int split_parts(int c, int M, int max_splits) {
+    const int n = (c + M - 1) / M;
+    return n < max_splits ? n : max_splits;
+}
+
 // keys of sequence b (its own rows, or the used slots of its pages)
 __device__ __forceinline__ int seq_keys(const VarlenPrep& a, int b) {
     return a.paged ? a.seqlens_k[b] : a.cu_k[b + 1] - a.cu_k[b];
@@ -1541,6 +1569,9 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
     __shared__ int bad;
     __shared__ int bucket[kCostBuckets];   // counts, then (descending) start positions
     __shared__ int warp_sums[32];
+    __shared__ int2 dist[kMaxDistinct];    // key splits: (cost, pairs) of each cost present
+    __shared__ int n_dist, n_pairs, max_cost, feasible[32];
+    __shared__ int part_tiles, part_cap;   // M of the key split (0: none), parts at most
     // the previous kernel in the stream may have written the offsets or still read this
     // workspace; the attention kernel may launch now and waits for this one's memory
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1626,6 +1657,74 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
         }
     }
     __syncthreads();
+    // key splits: the costs present, then the smallest feasible M (tiles per part), found by
+    // narrowing [1, max cost] with 32 candidates a round, one per warp; each bucket's count
+    // then becomes its entries
+    if (a.max_splits > 1) {
+        if (tid == 0) {
+            n_dist = 0;
+            n_pairs = 0;
+            max_cost = 0;
+        }
+        __syncthreads();
+        for (int i = tid; i < kCostBuckets; i += nthreads) {
+            const int n = bucket[i];
+            if (n > 0) {
+                const int pos = atomicAdd(&n_dist, 1);
+                if (pos < kMaxDistinct) dist[pos] = make_int2(i, n);
+                atomicAdd(&n_pairs, n);
+                atomicMax(&max_cost, i);
+            }
+        }
+        __syncthreads();
+        const int per_block = a.H >> a.pack_shift;
+        const int gp = a.grid / per_block;
+        const int ms = a.max_splits < gp ? a.max_splits : gp;
+        int M = 0;
+        if (n_pairs > 0 && gp > n_pairs && n_dist <= kMaxDistinct) {
+            // entries for M tiles per part, against the gp places (M = max cost always fits)
+            auto fits = [&](int m) {
+                int e = 0;
+                for (int i = lane; i < n_dist; i += 32) {
+                    const int n = (dist[i].x + m - 1) / m;
+                    e += dist[i].y * (n < ms ? n : ms);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(0xFFFFFFFFu, e, off);
+                return e <= gp;
+            };
+            int lo = 1, hi = max_cost;      // the answer lies in [lo, hi]; hi fits
+            while (true) {
+                const int step = (hi - lo + 32) / 32;
+                const int m = min(hi, lo - 1 + (wid + 1) * step);
+                if (wid < (nthreads >> 5)) {
+                    const bool f = fits(m);
+                    if (lane == 0) feasible[wid] = f ? 1 : 0;
+                }
+                __syncthreads();
+                int w = 31;
+                for (int i = 0; i < 32; ++i)
+                    if (feasible[i]) { w = i; break; }
+                const int nhi = min(hi, lo - 1 + (w + 1) * step);
+                const int nlo = w == 0 ? lo : lo + w * step;
+                __syncthreads();
+                lo = nlo;
+                hi = nhi;
+                if (step == 1) break;
+            }
+            M = hi;
+        }
+        if (tid == 0) {
+            part_tiles = M;
+            part_cap = ms;
+        }
+        __syncthreads();
+        if (M > 0)
+            for (int i = tid; i < kCostBuckets; i += nthreads) bucket[i] *= split_parts(i, M, ms);
+        __syncthreads();
+    } else if (tid == 0) {
+        part_tiles = 0;
+    }
     // start of each bucket in descending order: thread t owns buckets kCostBuckets - 4t - 1
     // down to kCostBuckets - 4t - 4; an exclusive scan of the threads' sums over t
     constexpr int kPer = kCostBuckets / 1024;
@@ -1668,11 +1767,95 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
         const int tb = kUnitRows >> a.pack_shift;
         const int nqb = (sq + tb - 1) / tb;
         for (int qb = 0; qb < nqb; ++qb) {
-            const int pos = atomicAdd(&bucket[block_cost(qb, sq, skv, a.causal, a.pack_shift)], 1);
-            a.blocks[pos] = make_int2(b, qb);
+            const int cost = block_cost(qb, sq, skv, a.causal, a.pack_shift);
+            const int n = part_tiles > 0 ? split_parts(cost, part_tiles, part_cap) : 1;
+            const int pos = atomicAdd(&bucket[cost], n);
+            for (int i = 0; i < n; ++i) a.blocks[pos + i] = make_int4(b, qb, i, n);
         }
     }
     asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+
+// Merge of a variable-length batch's key parts, a programmatic dependent of the attention
+// kernel.  Block (k, y) takes tile rows 32 y .. 32 y + 31 of item k when k's entry is the first
+// part of a split pair (every other block returns at once); warp w merges rows 32 y + 4 w ..
+// + 3, lane l holding columns kC l .. kC l + kC - 1.  The parts' slots are k + i * per_block
+// (i = 0 .. n - 1: the pair's entries are consecutive).  Weights follow the dense combine:
+// 2^(LSE_i - max), clamped at >= 2^-125 for a finite LSE_i, 0 for -inf; a NaN LSE or an
+// all -inf row gives a NaN row (0x7FC0).  Parts are summed in order, so the result is
+// deterministic.  Tile row r is token (256 qb + r) >> shift of the sequence, head
+// h + (r & (2^shift - 1)).  [MoonMath] "Data placement and the 16x16x16 choice" (key splits of
+// the tail), applied to the variable-length work list.
+struct VarlenCombine {
+    const int4* blocks;
+    const int* n_items;
+    const int* cu_q;
+    const float* ws_o;                     // [slot][256][D]
+    const float* ws_lse;                   // [slot][256], log2 units
+    __nv_bfloat16* o;                      // [total_q][H][D]
+    float* lse;                            // optional [H][total_q], natural log
+    long long total_q;
+    int H, pack_shift, round_mode;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) attn_varlen_combine_kernel(const VarlenCombine p) {
+    constexpr int kC = D / 32;             // columns per lane: 4 or 2
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int k = blockIdx.x;
+    if (k >= __ldg(p.n_items)) return;
+    const int per_block = p.H >> p.pack_shift;
+    const int4 e = __ldg(p.blocks + k / per_block);
+    if (e.w < 2 || e.z != 0) return;
+    const int q0 = __ldg(p.cu_q + e.x);
+    const int sq = __ldg(p.cu_q + e.x + 1) - q0;
+    const int h0 = (k % per_block) << p.pack_shift;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = 0; i < 4; ++i) {
+        const int r = blockIdx.y * 32 + warp * 4 + i;
+        const int tok = (e.y * kUnitRows + r) >> p.pack_shift;
+        if (tok >= sq) break;              // tokens do not decrease with r
+        const int h = h0 + (r & ((1 << p.pack_shift) - 1));
+        float mx = -INFINITY;
+        bool any_nan = false;
+        for (int s = 0; s < e.w; ++s) {
+            const float l = p.ws_lse[(long long)(k + s * per_block) * kUnitRows + r];
+            any_nan |= (l != l);
+            mx = fmaxf(mx, l);
+        }
+        float acc[kC];
+#pragma unroll
+        for (int c = 0; c < kC; ++c) acc[c] = 0.f;
+        float wsum = 0.f;
+        for (int s = 0; s < e.w; ++s) {
+            const long long sr = (long long)(k + s * per_block) * kUnitRows + r;
+            const float l = p.ws_lse[sr];
+            const float wt = (l == -INFINITY) ? 0.0f : ptx::ex2_approx(fmaxf(l - mx, -125.0f));
+            float v[kC];
+            if constexpr (kC == 4) {
+                const float4 x = *reinterpret_cast<const float4*>(p.ws_o + sr * D + lane * 4);
+                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+            } else {
+                const float2 x = *reinterpret_cast<const float2*>(p.ws_o + sr * D + lane * 2);
+                v[0] = x.x; v[1] = x.y;
+            }
+            wsum += wt;
+#pragma unroll
+            for (int c = 0; c < kC; ++c) acc[c] += wt * v[c];
+        }
+        const bool nan_row = any_nan || mx == -INFINITY;
+        const float inv = 1.0f / wsum;
+        if (p.lse && lane == 0)
+            p.lse[(long long)h * p.total_q + q0 + tok] = any_nan ? NAN : (mx + log2f(wsum)) * kLn2;
+        uint32_t bits[kC];
+#pragma unroll
+        for (int c = 0; c < kC; ++c) bits[c] = nan_row ? 0x7FC0u : round_bf16_bits(acc[c] * inv, p.round_mode);
+        __nv_bfloat16* orow = p.o + ((long long)(q0 + tok) * p.H + h) * D;
+        if constexpr (kC == 4)
+            *reinterpret_cast<uint2*>(orow + lane * 4) = make_uint2(bits[0] | (bits[1] << 16), bits[2] | (bits[3] << 16));
+        else
+            *reinterpret_cast<uint32_t*>(orow + lane * 2) = bits[0] | (bits[1] << 16);
+    }
 }
 
 // ------------------------------------------------------------------------------ host side
@@ -2068,7 +2251,7 @@ struct SeqBatch {
     const int32_t* block_table;
     int64_t B, H, Hkv, total_q, kv_rows, max_seqlen_q, d;
     int64_t paged, page_size, max_pages, num_pages;
-    int32_t round_mode, causal, pack_heads, reserved;
+    int32_t round_mode, causal, pack_heads, max_splits;
 };
 
 // log2 of the heads packed into one tile's rows (0: no packing)
@@ -2086,7 +2269,7 @@ SeqBatch from_varlen(const attn_varlen_args_t& a) {
     c.cu_q = a.cu_seqlens_q; c.cu_k = a.cu_seqlens_k;
     c.B = a.B; c.H = a.H; c.Hkv = a.Hkv; c.total_q = a.total_q; c.kv_rows = a.total_k;
     c.max_seqlen_q = a.max_seqlen_q; c.d = a.d;
-    c.round_mode = a.round_mode; c.causal = a.causal; c.pack_heads = a.pack_heads; c.reserved = a.reserved;
+    c.round_mode = a.round_mode; c.causal = a.causal; c.pack_heads = a.pack_heads; c.max_splits = a.max_splits;
     return c;
 }
 
@@ -2099,7 +2282,7 @@ SeqBatch from_paged(const attn_paged_args_t& a) {
     c.kv_rows = a.num_pages * a.page_size;
     c.max_seqlen_q = a.max_seqlen_q; c.d = a.d;
     c.paged = 1; c.page_size = a.page_size; c.max_pages = a.max_pages; c.num_pages = a.num_pages;
-    c.round_mode = a.round_mode; c.causal = a.causal; c.pack_heads = a.pack_heads; c.reserved = a.reserved;
+    c.round_mode = a.round_mode; c.causal = a.causal; c.pack_heads = a.pack_heads; c.max_splits = a.max_splits;
     return c;
 }
 
@@ -2108,7 +2291,7 @@ int validate_seq_shape(const SeqBatch& a, const attn_options_t* opts) {
         return ATTN_ERR_INVALID_ARG;
     if (a.H % a.Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (a.round_mode < ATTN_ROUND_RTNE || a.round_mode > ATTN_ROUND_RTZ) return ATTN_ERR_INVALID_ARG;
-    if ((a.causal != 0 && a.causal != 1) || (a.pack_heads != 0 && a.pack_heads != 1) || a.reserved != 0)
+    if ((a.causal != 0 && a.causal != 1) || (a.pack_heads != 0 && a.pack_heads != 1) || a.max_splits < 0)
         return ATTN_ERR_INVALID_ARG;
     // packed heads: a power of two of at most 32 per K/V head, so that a warp's 32 rows hold
     // whole tokens
@@ -2131,13 +2314,38 @@ int validate_seq_shape(const SeqBatch& a, const attn_options_t* opts) {
     return ATTN_OK;
 }
 
-// (sequence, query block) pairs a batch can hold: a block has 256 >> shift tokens, so
-// sum_b ceil(Sq_b / tokens) <= total_q / tokens + B
-int64_t seq_max_blocks(const SeqBatch& a) { return a.total_q / (kUnitRows >> pack_shift(a)) + a.B; }
+// work-list entries a batch can need: a block has 256 >> shift tokens, so there are at most
+// sum_b ceil(Sq_b / tokens) <= total_q / tokens + B pairs, and with key splits at most one
+// entry per CTA (sms: the device's SMs, which bound the CTA count)
+int64_t seq_max_blocks(const SeqBatch& a, int64_t sms) {
+    const int64_t pairs = a.total_q / (kUnitRows >> pack_shift(a)) + a.B;
+    return a.max_splits > 1 && sms > pairs ? sms : pairs;
+}
 
-// workspace: per-sequence tensor maps (128-byte aligned inside it), the item count, the pairs
-size_t seq_ws_bytes(const SeqBatch& a) {
-    return 128 + (size_t)a.B * 4 * sizeof(CUtensorMap) + 16 + (size_t)seq_max_blocks(a) * sizeof(int2);
+bool seq_split(const SeqBatch& a) { return a.max_splits > 1; }
+
+// workspace: per-sequence tensor maps (128-byte aligned inside it), the item count, the work
+// list, and with key splits (256-byte aligned) the parts' fp32 rows and LSEs, one slot per CTA
+size_t seq_list_bytes(const SeqBatch& a, int64_t sms) {
+    return 128 + (size_t)a.B * 4 * sizeof(CUtensorMap) + 16 + (size_t)seq_max_blocks(a, sms) * sizeof(int4);
+}
+size_t seq_ws_bytes(const SeqBatch& a, int64_t sms) {
+    size_t n = seq_list_bytes(a, sms);
+    if (seq_split(a)) n = ((n + 255) & ~(size_t)255) + (size_t)sms * kUnitRows * (size_t)(a.d + 1) * 4;
+    return n;
+}
+
+// the SM count the workspace of a batch is sized for (0 if a split batch finds no device)
+int64_t seq_sms(const SeqBatch& a) {
+    if (!seq_split(a)) return 0;
+    DeviceInfo* di = nullptr;
+    return device_info(&di) == ATTN_OK ? di->sms : 0;
+}
+size_t seq_ws_query(const SeqBatch& a) {
+    if (validate_seq_shape(a, nullptr) != ATTN_OK) return 0;
+    const int64_t sms = seq_sms(a);
+    if (seq_split(a) && sms < 1) return 0;
+    return seq_ws_bytes(a, sms);
 }
 
 int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace, size_t workspace_bytes,
@@ -2162,7 +2370,9 @@ int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace
     }
     DeviceInfo* di = nullptr;
     if ((st = device_info(&di)) != ATTN_OK) return st;
-    const size_t need = seq_ws_bytes(a);
+    const bool split = seq_split(a);
+    const int64_t sms = split ? di->sms : 0;
+    const size_t need = seq_ws_bytes(a, sms);
     void* ws = nullptr;
     if (workspace) {
         if (workspace_bytes < need) return ATTN_ERR_WORKSPACE;
@@ -2190,7 +2400,13 @@ int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace
         return ATTN_ERR_CUDA;
     CUtensorMap* maps = reinterpret_cast<CUtensorMap*>((wsb + 127u) & ~(uintptr_t)127u);
     int* n_items = reinterpret_cast<int*>(maps + 4 * a.B);
-    int2* blocks = reinterpret_cast<int2*>(reinterpret_cast<char*>(n_items) + 16);
+    int4* blocks = reinterpret_cast<int4*>(reinterpret_cast<char*>(n_items) + 16);
+    float* ws_o = nullptr;
+    float* ws_lse = nullptr;
+    if (split) {
+        ws_o = reinterpret_cast<float*>((wsb + seq_list_bytes(a, sms) + 255u) & ~(uintptr_t)255u);
+        ws_lse = ws_o + (size_t)sms * kUnitRows * d;
+    }
     VarlenPrep vp;
     memset(&vp, 0, sizeof vp);
     vp.cu_q = a.cu_q;
@@ -2202,6 +2418,7 @@ int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace
     vp.max_pages = (int)a.max_pages;
     vp.num_pages = (int)a.num_pages;
     vp.pack_shift = sh;
+    vp.max_splits = a.max_splits;
     vp.B = (int)a.B;
     vp.H = (int)a.H;
     vp.causal = a.causal;
@@ -2245,14 +2462,20 @@ int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace
     p.page_size = (int)a.page_size;
     p.max_pages = (int)a.max_pages;
     p.pack_shift = sh;
+    p.ws_o = ws_o;
+    p.ws_lse = ws_lse;
 
+    // CTAs: one per SM, at most max_ctas, and no more than the items can use (max_seqlen_q
+    // bounds the pairs; key splits multiply them by up to max_splits)
     int64_t G = di->sms;
     if (opts && opts->max_ctas > 0 && opts->max_ctas < G) G = opts->max_ctas;
     if (a.max_seqlen_q > 0) {
-        const int64_t cap = a.B * (a.H >> sh) * cdiv(a.max_seqlen_q, kUnitRows >> sh);
+        int64_t cap = a.B * (a.H >> sh) * cdiv(a.max_seqlen_q, kUnitRows >> sh);
+        if (split) cap = cap > G ? G : cap * a.max_splits;
         if (cap < G) G = cap;
     }
     if (G < 1) G = 1;
+    vp.grid = (int)G;
 
     // preprocessing -> attention kernel, each a programmatic dependent of the kernel before it
     cudaLaunchAttribute pdl[1];
@@ -2288,8 +2511,32 @@ int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace
         return ATTN_ERR_CUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    for (int i = 1; i < 3; ++i)
-        if (ev && ev[i] && cudaEventRecord((cudaEvent_t)ev[i], stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (ev && ev[1] && cudaEventRecord((cudaEvent_t)ev[1], stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (split) {
+        // merge of the key parts (every block whose item is not a first part returns at once)
+        VarlenCombine vc;
+        vc.blocks = blocks;
+        vc.n_items = n_items;
+        vc.cu_q = a.cu_q;
+        vc.ws_o = ws_o;
+        vc.ws_lse = ws_lse;
+        vc.o = reinterpret_cast<__nv_bfloat16*>(a.o);
+        vc.lse = a.lse;
+        vc.total_q = a.total_q;
+        vc.H = (int)a.H;
+        vc.pack_shift = sh;
+        vc.round_mode = a.round_mode;
+        lc.gridDim = dim3((unsigned)G, kUnitRows / 32);
+        lc.blockDim = dim3(256);
+        lc.dynamicSmemBytes = 0;
+        le = d == 128 ? cudaLaunchKernelEx(&lc, attn_varlen_combine_kernel<128>, vc)
+                      : cudaLaunchKernelEx(&lc, attn_varlen_combine_kernel<64>, vc);
+        if (le != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+    }
+    if (ev && ev[2] && cudaEventRecord((cudaEvent_t)ev[2], stream) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
 
@@ -2337,7 +2584,7 @@ size_t attn_fwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Skv, in
 size_t attn_fwd_varlen_workspace_size(const attn_varlen_args_t* args) {
     if (!args) return 0;
     const SeqBatch c = from_varlen(*args);
-    return validate_seq_shape(c, nullptr) == ATTN_OK ? seq_ws_bytes(c) : 0;
+    return seq_ws_query(c);
 }
 
 int attn_fwd_varlen(const attn_varlen_args_t* args, const attn_options_t* opts, void* workspace,
@@ -2349,7 +2596,7 @@ int attn_fwd_varlen(const attn_varlen_args_t* args, const attn_options_t* opts, 
 size_t attn_fwd_paged_workspace_size(const attn_paged_args_t* args) {
     if (!args) return 0;
     const SeqBatch c = from_paged(*args);
-    return validate_seq_shape(c, nullptr) == ATTN_OK ? seq_ws_bytes(c) : 0;
+    return seq_ws_query(c);
 }
 
 int attn_fwd_paged(const attn_paged_args_t* args, const attn_options_t* opts, void* workspace,
@@ -2412,6 +2659,6 @@ const char* attn_status_string(int status) {
     }
 }
 
-int attn_version(void) { return 200; }
+int attn_version(void) { return 300; }
 
 }  // extern "C"

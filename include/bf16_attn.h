@@ -254,11 +254,23 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, int64
  *                 the group.  Every row is computed exactly as without packing: the results
  *                 are bit for bit the same.  Pays off when sequences have few queries
  *                 (for decoding a dense batch, pass cu_seqlens = 0, Sq, 2 Sq, ... here).
- *   reserved      must be 0
- * Keys are never split (opts->force_splits must be 0 or 1).  workspace: caller device memory
- * of at least attn_fwd_varlen_workspace_size() bytes (per-sequence tensor maps and work-item
- * offsets), 16-byte aligned; or NULL to use the library-owned workspace as attn_fwd_ex does.
- * Two kernels run on `stream`: a one-CTA preprocessing kernel, then the attention kernel.
+ *   max_splits    >= 0.  0 or 1: a query block's keys are never split.  n >= 2: when the
+ *                 batch's (sequence, query block, head) items number fewer than the CTAs (a
+ *                 few long sequences, decoding), the preprocessing kernel splits each block's
+ *                 key tiles into up to n contiguous parts, more for costlier blocks: the
+ *                 shortest longest part for which every part still has a CTA of its own (the
+ *                 MoonMath article's key split of the tail, on the variable-length work list);
+ *                 a third kernel merges the parts.  The choice depends on the lengths and the CTA count
+ *                 only, so results are deterministic for a given device and max_ctas; they
+ *                 differ from the unsplit ones by rounding (same criteria against the exact
+ *                 result).  Batches with at least as many items as CTAs run unsplit.
+ * opts->force_splits must be 0 or 1.  workspace: caller device memory of at least
+ * attn_fwd_varlen_workspace_size() bytes (per-sequence tensor maps and the work list; with
+ * max_splits >= 2 also one fp32 partial tile per SM of the current device), 16-byte aligned;
+ * or NULL to use the library-owned workspace as attn_fwd_ex does.  The size query returns 0
+ * for invalid arguments, and for max_splits >= 2 when no CUDA device is usable.  Kernels on
+ * `stream`: a one-CTA preprocessing kernel, the attention kernel, and with max_splits >= 2
+ * the merge of the parts.
  */
 typedef struct {
     const void* q;
@@ -269,7 +281,7 @@ typedef struct {
     const int32_t* cu_seqlens_q;
     const int32_t* cu_seqlens_k;
     int64_t B, H, Hkv, total_q, total_k, max_seqlen_q, d;
-    int32_t round_mode, causal, pack_heads, reserved;
+    int32_t round_mode, causal, pack_heads, max_splits;
 } attn_varlen_args_t;
 
 size_t attn_fwd_varlen_workspace_size(const attn_varlen_args_t* args);
@@ -293,6 +305,7 @@ int attn_fwd_varlen(const attn_varlen_args_t* args, const attn_options_t* opts, 
  *                 not read.  Pages may be shared between sequences.
  *   page_size     a multiple of 128 (a key tile never straddles pages)
  *   pack_heads    as in attn_fwd_varlen (the natural setting for decoding over a paged cache)
+ *   max_splits    as in attn_fwd_varlen (decoding a few long sequences)
  * Checked on the device: bad query offsets, lengths or page indices (outside 0 ..
  * num_pages - 1) write no output and report ATTN_ERR_INVALID_ARG at ATTN_SITE_SEQLENS.  Slots
  * of a sequence's last page past its length are never read as keys (they read as zeros), so
@@ -308,7 +321,7 @@ typedef struct {
     const int32_t* seqlens_k;
     const int32_t* block_table;
     int64_t B, H, Hkv, total_q, num_pages, page_size, max_pages, max_seqlen_q, d;
-    int32_t round_mode, causal, pack_heads, reserved;
+    int32_t round_mode, causal, pack_heads, max_splits;
 } attn_paged_args_t;
 
 size_t attn_fwd_paged_workspace_size(const attn_paged_args_t* args);

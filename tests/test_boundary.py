@@ -243,7 +243,7 @@ def test_varlen_argument_errors(lib):
     assert run() == 5
     assert run(B=3, total_q=0, total_k=0, max_seqlen_q=7, d=64) == 5
     for bad in ({"B": 0}, {"Hkv": 3}, {"total_q": -1}, {"total_k": -1}, {"max_seqlen_q": -1},
-                {"round_mode": 3}, {"causal": 2}, {"reserved": 1}, {"pack_heads": 2},
+                {"round_mode": 3}, {"causal": 2}, {"max_splits": -1}, {"pack_heads": 2},
                 {"cu_seqlens_q": 0}, {"cu_seqlens_k": 0}, {"q": 0}, {"o": 0}):
         assert run(**bad) == 1, bad
     assert run(d=96) == 2
@@ -253,6 +253,9 @@ def test_varlen_argument_errors(lib):
     assert run(pack_heads=1, H=32, Hkv=1) == 5
     assert run(pack_heads=1, H=6, Hkv=2) == 2
     assert run(pack_heads=1, H=64, Hkv=1) == 2
+    # key splits: any count >= 0 (0 and 1: none)
+    for n in (0, 1, 2, 64, 1 << 20):
+        assert run(max_splits=n) == 5, n
     assert run(opts=attn.Options(2, 0, 0, 0)) == 2
     assert run(opts=attn.Options(1, 0, 0, 0)) == 5
     assert run(opts=attn.Options(0, 0, 0, 1)) == 1
@@ -265,17 +268,28 @@ def test_varlen_argument_errors(lib):
 
 def test_varlen_workspace_size(lib):
     """Per-sequence tensor maps (4 x 128 bytes), the item count (16 bytes) and room for every
-    (sequence, 256-row query block) pair (8 bytes each, at most total_q / 256 + B of them),
-    plus alignment room."""
+    (sequence, 256-row query block) pair (16 bytes each, at most total_q / 256 + B of them),
+    plus alignment room.  With key splits the size depends on the device's SM count: with no
+    device it is 0."""
     for B, total_q in ((1, 16), (2, 16), (7, 5000), (1000, 1 << 20)):
         a = varlen_args(B=B, total_q=total_q)
-        want = 128 + B * 512 + 16 + (total_q // 256 + B) * 8
+        want = 128 + B * 512 + 16 + (total_q // 256 + B) * 16
         assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(a)) == want, B
     assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(varlen_args(B=0))) == 0
     assert lib.attn_fwd_varlen_workspace_size(None) == 0
     # with packed heads (here 2 per K/V head) a block holds 128 tokens: room for more pairs
     a = varlen_args(B=7, total_q=5000, pack_heads=1)
-    assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(a)) == 128 + 7 * 512 + 16 + (5000 // 128 + 7) * 8
+    assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(a)) == 128 + 7 * 512 + 16 + (5000 // 128 + 7) * 16
+    a = varlen_args(B=7, total_q=5000, max_splits=1)
+    assert lib.attn_fwd_varlen_workspace_size(ctypes.byref(a)) == 128 + 7 * 512 + 16 + (5000 // 256 + 7) * 16
+    a = varlen_args(B=7, total_q=5000, max_splits=2)
+    got = lib.attn_fwd_varlen_workspace_size(ctypes.byref(a))
+    if torch.cuda.is_available():
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        base = 128 + 7 * 512 + 16 + max(5000 // 256 + 7, sms) * 16
+        assert got == -(-base // 256) * 256 + sms * 256 * 129 * 4
+    else:
+        assert got == 0
 
 
 PG = 1 << 24   # fake pointers for the paged calls, far enough apart for their cache sizes
@@ -303,7 +317,7 @@ def test_paged_argument_errors(lib):
     assert run(page_size=256, d=64, causal=1) == 5
     for bad in ({"num_pages": 0}, {"page_size": 0}, {"page_size": 64}, {"page_size": 200}, {"max_pages": 0},
                 {"seqlens_k": 0}, {"block_table": 0}, {"cu_seqlens_q": 0}, {"k_cache": 0}, {"B": 0},
-                {"Hkv": 3}, {"reserved": 1}):
+                {"Hkv": 3}, {"max_splits": -1}):
         assert run(**bad) == 1, bad
     assert run(max_pages=(1 << 23) + 1) == 2
     assert run(num_pages=(1 << 23) + 1) == 2
@@ -313,7 +327,7 @@ def test_paged_argument_errors(lib):
 
 def test_paged_workspace_size(lib):
     a = paged_args(B=3, total_q=1000)
-    assert lib.attn_fwd_paged_workspace_size(ctypes.byref(a)) == 128 + 3 * 512 + 16 + (1000 // 256 + 3) * 8
+    assert lib.attn_fwd_paged_workspace_size(ctypes.byref(a)) == 128 + 3 * 512 + 16 + (1000 // 256 + 3) * 16
     assert lib.attn_fwd_paged_workspace_size(ctypes.byref(paged_args(page_size=100))) == 0
 
 
