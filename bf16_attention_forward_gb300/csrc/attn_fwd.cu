@@ -608,11 +608,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             const Item it = decode_item<kCausal, kVarlen>(p, k);
             float m_ref = -INFINITY;      // running max of raw logits at the last rescale
             float l = 0.0f;               // running sum of weights relative to m_ref
+            // A warp whose 32 rows all lie past the queries (the tail of a block; all but the
+            // first few rows of a decoding step) keeps every wait and arrival but skips its
+            // softmax and epilogue work: a row's S, P and O are its own TMEM lane, and these
+            // rows are never stored.  The softmax warps sharing its scheduler run faster.
+            const int first_row = kVarlen ? (it.qb * kUnitRows + t * kBM + quarter * 32) >> p.pack_shift
+                                          : it.qb * kUnitRows + t * kBM + quarter * 32;
+            const bool live = first_row < (kVarlen ? it.sq : p.Sq);
             for (int j = it.kv_begin; j < it.kv_end; ++j) {
                 ok = wait_bar(bar(G::kBarSFull + t), scount & 1u, kSiteSFull, abort_flag, lim);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 ++scount;
                 ptx::tc_fence_after();
+                if (!live) {
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(bar(G::kBarPFull + t));
+                    continue;
+                }
                 uint32_t s[128];
                 ptx::tmem_ld128(tS, s);
                 // keys of this tile past `limit` are absent: beyond Skv, or (causal) past this
@@ -759,6 +771,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             ok = wait_bar(bar(G::kBarOFull + t), u & 1, kSiteOFull, abort_flag, lim);
             if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             ptx::tc_fence_after();
+            if (!live) continue;
             const int qrow = kVarlen ? (it.qb * kUnitRows + t * kBM + row) >> p.pack_shift
                                      : it.qb * kUnitRows + t * kBM + row;
             const bool valid_row = qrow < (kVarlen ? it.sq : p.Sq);
