@@ -611,160 +611,167 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             // A warp whose 32 rows all lie past the queries (the tail of a block; all but the
             // first few rows of a decoding step) keeps every wait and arrival but skips its
             // softmax and epilogue work: a row's S, P and O are its own TMEM lane, and these
-            // rows are never stored.  The softmax warps sharing its scheduler run faster.
+            // rows are never stored.  The softmax warps sharing its scheduler run faster.  A
+            // loop of its own, so that the live loop below compiles as it would alone.
             const int first_row = kVarlen ? (it.qb * kUnitRows + t * kBM + quarter * 32) >> p.pack_shift
                                           : it.qb * kUnitRows + t * kBM + quarter * 32;
             const bool live = first_row < (kVarlen ? it.sq : p.Sq);
-            for (int j = it.kv_begin; j < it.kv_end; ++j) {
-                ok = wait_bar(bar(G::kBarSFull + t), scount & 1u, kSiteSFull, abort_flag, lim);
-                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-                ++scount;
-                ptx::tc_fence_after();
-                if (!live) {
+            if (!live) {
+                for (int j = it.kv_begin; j < it.kv_end; ++j) {
+                    ok = wait_bar(bar(G::kBarSFull + t), scount & 1u, kSiteSFull, abort_flag, lim);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                    ++scount;
+                    ptx::tc_fence_after();
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(bar(G::kBarPFull + t));
-                    continue;
                 }
-                uint32_t s[128];
-                ptx::tmem_ld128(tS, s);
-                // keys of this tile past `limit` are absent: beyond Skv, or (causal) past this
-                // row's diagonal; they get -inf logits and so weight 0
-                int limit = kBN - 1;
-                const int skv = kVarlen ? it.skv : p.Skv;
-                if constexpr (kCausal) {
-                    limit = skv - j * kBN - 1;
-                    const int qpos = kVarlen ? (it.qb * kUnitRows + t * kBM + row) >> p.pack_shift
-                                             : it.qb * kUnitRows + t * kBM + row;   // the row's query
-                    const int diag = qpos + (kVarlen ? it.causal_off : p.causal_off) - j * kBN;
-                    limit = diag < limit ? diag : limit;
-                } else {
-                    const int valid = skv - j * kBN;   // the same for every row of the tile
-                    limit = valid < kBN ? valid - 1 : kBN - 1;
-                }
-                float mx, mn;
-                const bool any_masked = __any_sync(0xFFFFFFFFu, limit < kBN - 1);
-                if (D == 64 && any_masked) {
-                    // at d = 64 (MMA-issue-bound) the split form below measured 4 % slower:
-                    // mask first, then the fused max/min
-#pragma unroll
-                    for (int e = 0; e < 128; ++e)
-                        if (e > limit) s[e] = __float_as_uint(-INFINITY);
-                }
-                if (D == 128 && any_masked) {
-                    // the row min (which only decides whether the exponent clamp below can be
-                    // skipped) over the raw logits, before the mask: a masked key's weight is
-                    // exactly 0 from its -inf and needs no clamp, and counting masked keys' raw
-                    // logits (zero past Skv, where K is zero-filled) only makes the test stricter
-                    float mna[4], mxa[4];
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) mna[q4] = __uint_as_float(s[q4]);
-#pragma unroll
-                    for (int e = 4; e < 124; e += 8) {
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4)
-                            mna[q4] = ptx::fmin3(mna[q4], __uint_as_float(s[e + q4]), __uint_as_float(s[e + 4 + q4]));
-                    }
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) mna[q4] = fminf(mna[q4], __uint_as_float(s[124 + q4]));
-                    mn = ptx::fmin3(mna[0], mna[1], fminf(mna[2], mna[3]));
-#pragma unroll
-                    for (int e = 0; e < 128; ++e)
-                        if (e > limit) s[e] = __float_as_uint(-INFINITY);
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) mxa[q4] = __uint_as_float(s[q4]);
-#pragma unroll
-                    for (int e = 4; e < 124; e += 8) {
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4)
-                            mxa[q4] = ptx::fmax3(mxa[q4], __uint_as_float(s[e + q4]), __uint_as_float(s[e + 4 + q4]));
-                    }
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) mxa[q4] = fmaxf(mxa[q4], __uint_as_float(s[124 + q4]));
-                    mx = ptx::fmax3(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3]));
-                } else {
-                    // row max and min: 3-input trees over 4 independent chains each
-                    float mxa[4], mna[4];
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) mxa[q4] = mna[q4] = __uint_as_float(s[q4]);
-#pragma unroll
-                    for (int e = 4; e < 124; e += 8) {
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const float a = __uint_as_float(s[e + q4]), b = __uint_as_float(s[e + 4 + q4]);
-                            mxa[q4] = ptx::fmax3(mxa[q4], a, b);
-                            mna[q4] = ptx::fmin3(mna[q4], a, b);
-                        }
-                    }
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        mxa[q4] = fmaxf(mxa[q4], __uint_as_float(s[124 + q4]));
-                        mna[q4] = fminf(mna[q4], __uint_as_float(s[124 + q4]));
-                    }
-                    mx = ptx::fmax3(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3]));
-                    mn = ptx::fmin3(mna[0], mna[1], fminf(mna[2], mna[3]));
-                }
-                const float m_new = fmaxf(m_ref, mx);
-                bool rescale_o = false;
-                float alpha = 1.0f;
-                if (m_new > m_ref && (m_new - m_ref) * c > p.tau) {
-                    if (m_ref == -INFINITY) {
-                        alpha = 0.0f;      // nothing accumulated yet but 0*v terms
+            } else {
+                for (int j = it.kv_begin; j < it.kv_end; ++j) {
+                    ok = wait_bar(bar(G::kBarSFull + t), scount & 1u, kSiteSFull, abort_flag, lim);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                    ++scount;
+                    ptx::tc_fence_after();
+                    uint32_t s[128];
+                    ptx::tmem_ld128(tS, s);
+                    // keys of this tile past `limit` are absent: beyond Skv, or (causal) past this
+                    // row's diagonal; they get -inf logits and so weight 0
+                    int limit = kBN - 1;
+                    const int skv = kVarlen ? it.skv : p.Skv;
+                    if constexpr (kCausal) {
+                        limit = skv - j * kBN - 1;
+                        const int qpos = kVarlen ? (it.qb * kUnitRows + t * kBM + row) >> p.pack_shift
+                                                 : it.qb * kUnitRows + t * kBM + row;   // the row's query
+                        const int diag = qpos + (kVarlen ? it.causal_off : p.causal_off) - j * kBN;
+                        limit = diag < limit ? diag : limit;
                     } else {
-                        alpha = ptx::ex2_approx(fmaxf((m_ref - m_new) * c, -125.0f));
-                        rescale_o = j > it.kv_begin;
+                        const int valid = skv - j * kBN;   // the same for every row of the tile
+                        limit = valid < kBN ? valid - 1 : kBN - 1;
                     }
-                    l *= alpha;
-                    m_ref = m_new;
-                }
-                const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
-                // Every exponent of this row is >= -124 and no logit is -inf: the clamp that
-                // keeps underflowing finite weights positive cannot fire, so skip it.
-                const bool plain = mn > -INFINITY && (mn - m_use) * c >= kMinExponent;
-                const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
-                float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                  make_float2(0.f, 0.f)};
-                uint32_t pk[64];
-                if (__all_sync(0xFFFFFFFFu, plain)) {
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) {
-                        const float2 x = __fmul2_rn(
-                            __fadd2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), nm2), c2);
-                        const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
-                        lsum[e & 3] = __fadd2_rn(lsum[e & 3], pp);
-                        pk[e] = ptx::pack_bf16x2(pp.x, pp.y);
+                    float mx, mn;
+                    const bool any_masked = __any_sync(0xFFFFFFFFu, limit < kBN - 1);
+                    if (D == 64 && any_masked) {
+                        // at d = 64 (MMA-issue-bound) the split form below measured 4 % slower:
+                        // mask first, then the fused max/min
+    #pragma unroll
+                        for (int e = 0; e < 128; ++e)
+                            if (e > limit) s[e] = __float_as_uint(-INFINITY);
                     }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) {
-                        const float p0 = ptx::ex2_approx(weight_exponent(__uint_as_float(s[2 * e]), c, m_use));
-                        const float p1 = ptx::ex2_approx(weight_exponent(__uint_as_float(s[2 * e + 1]), c, m_use));
-                        lsum[e & 3] = __fadd2_rn(lsum[e & 3], make_float2(p0, p1));
-                        pk[e] = ptx::pack_bf16x2(p0, p1);
-                    }
-                }
-                ptx::tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-                ptx::tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-                const float2 ls = __fadd2_rn(__fadd2_rn(lsum[0], lsum[1]), __fadd2_rn(lsum[2], lsum[3]));
-                l += ls.x + ls.y;
-                if (__any_sync(0xFFFFFFFFu, rescale_o)) {
-                    const float a = rescale_o ? alpha : 1.0f;
-                    const float2 a2 = make_float2(a, a);
-#pragma unroll 1
-                    for (int ch = 0; ch < D / 32; ++ch) {
-                        uint32_t o[32];
-                        ptx::tmem_ld32(tO + ch * 32, o);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), a2);
-                            o[2 * e] = __float_as_uint(v.x);
-                            o[2 * e + 1] = __float_as_uint(v.y);
+                    if (D == 128 && any_masked) {
+                        // the row min (which only decides whether the exponent clamp below can be
+                        // skipped) over the raw logits, before the mask: a masked key's weight is
+                        // exactly 0 from its -inf and needs no clamp, and counting masked keys' raw
+                        // logits (zero past Skv, where K is zero-filled) only makes the test stricter
+                        float mna[4], mxa[4];
+    #pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) mna[q4] = __uint_as_float(s[q4]);
+    #pragma unroll
+                        for (int e = 4; e < 124; e += 8) {
+    #pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                mna[q4] = ptx::fmin3(mna[q4], __uint_as_float(s[e + q4]), __uint_as_float(s[e + 4 + q4]));
                         }
-                        ptx::tmem_st32(tO + ch * 32, o);
+    #pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) mna[q4] = fminf(mna[q4], __uint_as_float(s[124 + q4]));
+                        mn = ptx::fmin3(mna[0], mna[1], fminf(mna[2], mna[3]));
+    #pragma unroll
+                        for (int e = 0; e < 128; ++e)
+                            if (e > limit) s[e] = __float_as_uint(-INFINITY);
+    #pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) mxa[q4] = __uint_as_float(s[q4]);
+    #pragma unroll
+                        for (int e = 4; e < 124; e += 8) {
+    #pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                mxa[q4] = ptx::fmax3(mxa[q4], __uint_as_float(s[e + q4]), __uint_as_float(s[e + 4 + q4]));
+                        }
+    #pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) mxa[q4] = fmaxf(mxa[q4], __uint_as_float(s[124 + q4]));
+                        mx = ptx::fmax3(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3]));
+                    } else {
+                        // row max and min: 3-input trees over 4 independent chains each
+                        float mxa[4], mna[4];
+    #pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) mxa[q4] = mna[q4] = __uint_as_float(s[q4]);
+    #pragma unroll
+                        for (int e = 4; e < 124; e += 8) {
+    #pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const float a = __uint_as_float(s[e + q4]), b = __uint_as_float(s[e + 4 + q4]);
+                                mxa[q4] = ptx::fmax3(mxa[q4], a, b);
+                                mna[q4] = ptx::fmin3(mna[q4], a, b);
+                            }
+                        }
+    #pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            mxa[q4] = fmaxf(mxa[q4], __uint_as_float(s[124 + q4]));
+                            mna[q4] = fminf(mna[q4], __uint_as_float(s[124 + q4]));
+                        }
+                        mx = ptx::fmax3(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3]));
+                        mn = ptx::fmin3(mna[0], mna[1], fminf(mna[2], mna[3]));
                     }
+                    const float m_new = fmaxf(m_ref, mx);
+                    bool rescale_o = false;
+                    float alpha = 1.0f;
+                    if (m_new > m_ref && (m_new - m_ref) * c > p.tau) {
+                        if (m_ref == -INFINITY) {
+                            alpha = 0.0f;      // nothing accumulated yet but 0*v terms
+                        } else {
+                            alpha = ptx::ex2_approx(fmaxf((m_ref - m_new) * c, -125.0f));
+                            rescale_o = j > it.kv_begin;
+                        }
+                        l *= alpha;
+                        m_ref = m_new;
+                    }
+                    const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+                    // Every exponent of this row is >= -124 and no logit is -inf: the clamp that
+                    // keeps underflowing finite weights positive cannot fire, so skip it.
+                    const bool plain = mn > -INFINITY && (mn - m_use) * c >= kMinExponent;
+                    const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
+                    float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                      make_float2(0.f, 0.f)};
+                    uint32_t pk[64];
+                    if (__all_sync(0xFFFFFFFFu, plain)) {
+    #pragma unroll
+                        for (int e = 0; e < 64; ++e) {
+                            const float2 x = __fmul2_rn(
+                                __fadd2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), nm2), c2);
+                            const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+                            lsum[e & 3] = __fadd2_rn(lsum[e & 3], pp);
+                            pk[e] = ptx::pack_bf16x2(pp.x, pp.y);
+                        }
+                    } else {
+    #pragma unroll
+                        for (int e = 0; e < 64; ++e) {
+                            const float p0 = ptx::ex2_approx(weight_exponent(__uint_as_float(s[2 * e]), c, m_use));
+                            const float p1 = ptx::ex2_approx(weight_exponent(__uint_as_float(s[2 * e + 1]), c, m_use));
+                            lsum[e & 3] = __fadd2_rn(lsum[e & 3], make_float2(p0, p1));
+                            pk[e] = ptx::pack_bf16x2(p0, p1);
+                        }
+                    }
+                    ptx::tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+                    ptx::tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+                    const float2 ls = __fadd2_rn(__fadd2_rn(lsum[0], lsum[1]), __fadd2_rn(lsum[2], lsum[3]));
+                    l += ls.x + ls.y;
+                    if (__any_sync(0xFFFFFFFFu, rescale_o)) {
+                        const float a = rescale_o ? alpha : 1.0f;
+                        const float2 a2 = make_float2(a, a);
+    #pragma unroll 1
+                        for (int ch = 0; ch < D / 32; ++ch) {
+                            uint32_t o[32];
+                            ptx::tmem_ld32(tO + ch * 32, o);
+    #pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), a2);
+                                o[2 * e] = __float_as_uint(v.x);
+                                o[2 * e + 1] = __float_as_uint(v.y);
+                            }
+                            ptx::tmem_st32(tO + ch * 32, o);
+                        }
+                    }
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(bar(G::kBarPFull + t));
                 }
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(bar(G::kBarPFull + t));
             }
             if (!ok) break;
             // epilogue: O / l, rounding, store
