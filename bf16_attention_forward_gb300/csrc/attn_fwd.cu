@@ -1609,14 +1609,18 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
             if (a.cu_k[b + 1] < a.cu_k[b]) bad = 1;
         } else {
             const int skv = a.seqlens_k[b];
-            if (skv < 0 || skv > a.max_pages * a.page_size) {
-                bad = 1;
-            } else {
-                const int npg = (skv + a.page_size - 1) / a.page_size;
-                for (int pg = 0; pg < npg; ++pg) {
-                    const int phys = a.block_table[(long long)b * a.max_pages + pg];
-                    if (phys < 0 || phys >= a.num_pages) bad = 1;
-                }
+            if (skv < 0 || skv > a.max_pages * a.page_size) bad = 1;
+        }
+    }
+    // the used page indices of each sequence: a warp per sequence, its lanes across the pages
+    if (a.paged) {
+        for (int b = wid; b < a.B; b += (nthreads >> 5)) {
+            const int skv = a.seqlens_k[b];
+            if (skv < 0 || skv > a.max_pages * a.page_size) continue;   // reported above
+            const int npg = (skv + a.page_size - 1) / a.page_size;
+            for (int pg = lane; pg < npg; pg += 32) {
+                const int phys = a.block_table[(long long)b * a.max_pages + pg];
+                if (phys < 0 || phys >= a.num_pages) bad = 1;
             }
         }
     }
@@ -1798,14 +1802,16 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
 
 // Merge of a variable-length batch's key parts, a programmatic dependent of the attention
 // kernel.  Block (k, y) takes tile rows 32 y .. 32 y + 31 of item k when k's entry is the first
-// part of a split pair (every other block returns at once); warp w merges rows 32 y + 4 w ..
-// + 3, lane l holding columns kC l .. kC l + kC - 1.  The parts' slots are k + i * per_block
-// (i = 0 .. n - 1: the pair's entries are consecutive).  Weights follow the dense combine:
-// 2^(LSE_i - max), clamped at >= 2^-125 for a finite LSE_i, 0 for -inf; a NaN LSE or an
-// all -inf row gives a NaN row (0x7FC0).  Parts are summed in order, so the result is
-// deterministic.  Tile row r is token (256 qb + r) >> shift of the sequence, head
-// h + (r & (2^shift - 1)).  [MoonMath] "Data placement and the 16x16x16 choice" (key splits of
-// the tail), applied to the variable-length work list.
+// part of a split pair (every other block returns at once); warp w merges rows 32 y + w + 8 i
+// (i = 0 .. 3, so that the few rows of a decoding step fall to different warps), lane l holding
+// columns kC l .. kC l + kC - 1.  The parts' slots are k + s * per_block (s = 0 .. n - 1: the
+// pair's entries are consecutive).  A row's part LSEs are read across the lanes at once, and
+// its parts' partial rows four at a time.  Weights follow the dense combine: 2^(LSE_s - max),
+// clamped at >= 2^-125 for a finite LSE_s, 0 for -inf; a NaN LSE or an all -inf row gives a
+// NaN row (0x7FC0).  Parts are summed in order, so the result is deterministic.  Tile row r is
+// token (256 qb + r) >> shift of the sequence, head h + (r & (2^shift - 1)).  [MoonMath] "Data
+// placement and the 16x16x16 choice" (key splits of the tail), applied to the variable-length
+// work list.
 struct VarlenCombine {
     const int4* blocks;
     const int* n_items;
@@ -1821,47 +1827,72 @@ struct VarlenCombine {
 template <int D>
 __global__ void __launch_bounds__(256) attn_varlen_combine_kernel(const VarlenCombine p) {
     constexpr int kC = D / 32;             // columns per lane: 4 or 2
+    constexpr int kLoads = 4;              // parts' rows in flight
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int k = blockIdx.x;
     if (k >= __ldg(p.n_items)) return;
     const int per_block = p.H >> p.pack_shift;
     const int4 e = __ldg(p.blocks + k / per_block);
     if (e.w < 2 || e.z != 0) return;
+    const int n = e.w;
     const int q0 = __ldg(p.cu_q + e.x);
     const int sq = __ldg(p.cu_q + e.x + 1) - q0;
     const int h0 = (k % per_block) << p.pack_shift;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long pstride = (long long)per_block * kUnitRows;   // rows from one part to the next
     for (int i = 0; i < 4; ++i) {
-        const int r = blockIdx.y * 32 + warp * 4 + i;
+        const int r = blockIdx.y * 32 + warp + 8 * i;
         const int tok = (e.y * kUnitRows + r) >> p.pack_shift;
         if (tok >= sq) break;              // tokens do not decrease with r
         const int h = h0 + (r & ((1 << p.pack_shift) - 1));
+        const long long row0 = (long long)k * kUnitRows + r;      // part 0's row
         float mx = -INFINITY;
         bool any_nan = false;
-        for (int s = 0; s < e.w; ++s) {
-            const float l = p.ws_lse[(long long)(k + s * per_block) * kUnitRows + r];
+        for (int s = lane; s < n; s += 32) {
+            const float l = p.ws_lse[row0 + s * pstride];
             any_nan |= (l != l);
             mx = fmaxf(mx, l);
         }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+        any_nan = __any_sync(0xFFFFFFFFu, any_nan);
         float acc[kC];
 #pragma unroll
         for (int c = 0; c < kC; ++c) acc[c] = 0.f;
         float wsum = 0.f;
-        for (int s = 0; s < e.w; ++s) {
-            const long long sr = (long long)(k + s * per_block) * kUnitRows + r;
-            const float l = p.ws_lse[sr];
-            const float wt = (l == -INFINITY) ? 0.0f : ptx::ex2_approx(fmaxf(l - mx, -125.0f));
-            float v[kC];
-            if constexpr (kC == 4) {
-                const float4 x = *reinterpret_cast<const float4*>(p.ws_o + sr * D + lane * 4);
-                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-            } else {
-                const float2 x = *reinterpret_cast<const float2*>(p.ws_o + sr * D + lane * 2);
-                v[0] = x.x; v[1] = x.y;
+        for (int s0 = 0; s0 < n; s0 += 32) {
+            // lane j holds the weight of part s0 + j
+            float wt = 0.f;
+            if (s0 + lane < n) {
+                const float l = p.ws_lse[row0 + (s0 + lane) * pstride];
+                wt = (l == -INFINITY) ? 0.0f : ptx::ex2_approx(fmaxf(l - mx, -125.0f));
             }
-            wsum += wt;
+            const int m = n - s0 < 32 ? n - s0 : 32;
+            for (int j0 = 0; j0 < m; j0 += kLoads) {
+                float v[kLoads][kC];
 #pragma unroll
-            for (int c = 0; c < kC; ++c) acc[c] += wt * v[c];
+                for (int j = 0; j < kLoads; ++j) {
+                    if (j0 + j < m) {
+                        const float* src = p.ws_o + (row0 + (s0 + j0 + j) * pstride) * D + lane * kC;
+                        if constexpr (kC == 4) {
+                            const float4 x = *reinterpret_cast<const float4*>(src);
+                            v[j][0] = x.x; v[j][1] = x.y; v[j][2] = x.z; v[j][3] = x.w;
+                        } else {
+                            const float2 x = *reinterpret_cast<const float2*>(src);
+                            v[j][0] = x.x; v[j][1] = x.y;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kLoads; ++j) {
+                    if (j0 + j < m) {
+                        const float w = __shfl_sync(0xFFFFFFFFu, wt, j0 + j);
+                        wsum += w;
+#pragma unroll
+                        for (int c = 0; c < kC; ++c) acc[c] += w * v[j][c];
+                    }
+                }
+            }
         }
         const bool nan_row = any_nan || mx == -INFINITY;
         const float inv = 1.0f / wsum;
@@ -2546,7 +2577,7 @@ int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace
         vc.H = (int)a.H;
         vc.pack_shift = sh;
         vc.round_mode = a.round_mode;
-        lc.gridDim = dim3((unsigned)G, kUnitRows / 32);
+        lc.gridDim = dim3((unsigned)G, kUnitRows / 32);   // 32 tile rows a block, 4 a warp
         lc.blockDim = dim3(256);
         lc.dynamicSmemBytes = 0;
         le = d == 128 ? cudaLaunchKernelEx(&lc, attn_varlen_combine_kernel<128>, vc)
