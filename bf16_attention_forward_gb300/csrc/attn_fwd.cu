@@ -1508,17 +1508,21 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p
 //     runs, most first (a counting sort on that count, capped at kCostBuckets - 1; pairs of
 //     equal count in any order, which moves work between CTAs but changes no result), and
 //     the item count, H >> pack_shift per entry;
-//   * key splits (max_splits >= 2), when the pairs' items number fewer than the attention
-//     kernel's CTAs: with P pairs and Gp = CTAs / (items per pair) entry places, a pair of
-//     cost c becomes n(c) = min(max_splits, Gp, ceil(c / M)) consecutive entries (b, qb,
-//     part, n) for the smallest M (tiles in the longest part) with sum n(c) <= Gp.  Every item then
-//     has a CTA of its own and a split slot below the CTA count, and the longest part is as
-//     short as one wave allows.  n depends only on c (and the launch), so the result is a
-//     function of the inputs and the CTA count;
+//   * key splits (max_splits >= 2), when the pairs' items number fewer than twice the
+//     attention kernel's CTAs: with P pairs and Gp = CTAs / (items per pair) entry places, a
+//     pair of cost c becomes n(c) = min(max_splits, Gp, ceil(c / M)) consecutive entries (b,
+//     qb, part, n).  M is one of: the largest cost (no split); the smallest M with sum n(c) <=
+//     Gp (one wave: every item a CTA of its own); the smallest with sum n(c) <= 2 Gp (two
+//     waves, whose alternating order pairs a CTA's heavy first item with a light second one),
+//     whichever gives the busiest CTA the least modelled work (key tiles plus a fixed cost per
+//     item), the first of equals.  Split slots stay below twice the CTA count.  n depends only
+//     on c (and the launch), so the result is a function of the inputs and the CTA count;
 //   * a sequence with queries but no keys: every query sees no key, so its O rows are NaN
 //     (stored 0x7FC0) and its LSE rows -inf, written here.
 constexpr int kCostBuckets = 4096;
 constexpr int kMaxDistinct = 1024;        // key splits: distinct pair costs considered
+constexpr int kMaxSplitGrid = 1024;       // key splits: attention CTAs considered
+constexpr int kItemOverheadTiles = 2;     // key splits: modelled fixed cost of an item, in key tiles
 
 struct VarlenPrep {
     const int* cu_q;
@@ -1590,7 +1594,8 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
     __shared__ int bucket[kCostBuckets];   // counts, then (descending) start positions
     __shared__ int warp_sums[32];
     __shared__ int2 dist[kMaxDistinct];    // key splits: (cost, pairs) of each cost present
-    __shared__ int n_dist, n_pairs, max_cost, feasible[32];
+    __shared__ int n_dist, n_pairs, max_cost, feasible[32], red_max[32];
+    __shared__ int cta_load[kMaxSplitGrid];   // key splits: modelled busy time of each CTA
     __shared__ int part_tiles, part_cap;   // M of the key split (0: none), parts at most
     // the previous kernel in the stream may have written the offsets or still read this
     // workspace; the attention kernel may launch now and waits for this one's memory
@@ -1681,9 +1686,10 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
         }
     }
     __syncthreads();
-    // key splits: the costs present, then the smallest feasible M (tiles per part), found by
-    // narrowing [1, max cost] with 32 candidates a round, one per warp; each bucket's count
-    // then becomes its entries
+    // key splits: the costs present; for one wave and for two, the smallest M (tiles per part)
+    // whose entries fit, found by narrowing [1, max cost] with 32 candidates a round, one per
+    // warp; then the candidate (no split, one wave, two waves) whose busiest CTA has the least
+    // modelled work.  Each bucket's count then becomes its entries.
     if (a.max_splits > 1) {
         if (tid == 0) {
             n_dist = 0;
@@ -1705,38 +1711,82 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
         const int gp = a.grid / per_block;
         const int ms = a.max_splits < gp ? a.max_splits : gp;
         int M = 0;
-        if (n_pairs > 0 && gp > n_pairs && n_dist <= kMaxDistinct) {
-            // entries for M tiles per part, against the gp places (M = max cost always fits)
-            auto fits = [&](int m) {
+        if (n_pairs > 0 && 2 * gp > n_pairs && n_dist <= kMaxDistinct && a.grid <= kMaxSplitGrid) {
+            // entries for M tiles per part against `places` (M = max cost always fits one wave
+            // or two, as P < places then)
+            auto fits = [&](int m, int places) {
                 int e = 0;
-                for (int i = lane; i < n_dist; i += 32) {
-                    const int n = (dist[i].x + m - 1) / m;
-                    e += dist[i].y * (n < ms ? n : ms);
-                }
+                for (int i = lane; i < n_dist; i += 32) e += dist[i].y * split_parts(dist[i].x, m, ms);
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(0xFFFFFFFFu, e, off);
-                return e <= gp;
+                return e <= places;
             };
-            int lo = 1, hi = max_cost;      // the answer lies in [lo, hi]; hi fits
-            while (true) {
-                const int step = (hi - lo + 32) / 32;
-                const int m = min(hi, lo - 1 + (wid + 1) * step);
-                if (wid < (nthreads >> 5)) {
-                    const bool f = fits(m);
+            auto smallest_fit = [&](int places) {
+                int lo = 1, hi = max_cost;      // the answer lies in [lo, hi]; hi fits
+                while (true) {
+                    const int step = (hi - lo + 32) / 32;
+                    const int m = min(hi, lo - 1 + (wid + 1) * step);
+                    const bool f = fits(m, places);
                     if (lane == 0) feasible[wid] = f ? 1 : 0;
+                    __syncthreads();
+                    int w = 31;
+                    for (int i = 0; i < 32; ++i)
+                        if (feasible[i]) { w = i; break; }
+                    const int nhi = min(hi, lo - 1 + (w + 1) * step);
+                    const int nlo = w == 0 ? lo : lo + w * step;
+                    __syncthreads();
+                    lo = nlo;
+                    hi = nhi;
+                    if (step == 1) break;
+                }
+                return hi;
+            };
+            // the busiest CTA's work under M: entries heaviest first (a pair's parts in a row,
+            // near-equal), item k = entry * per_block + head group, run by the CTA that
+            // round_item gives it; an item costs its key tiles plus kItemOverheadTiles
+            auto busiest = [&](int m) {
+                for (int i = tid; i < a.grid; i += nthreads) cta_load[i] = 0;
+                __syncthreads();
+                for (int i = wid; i < n_dist; i += (nthreads >> 5)) {
+                    const int c = dist[i].x, n = split_parts(c, m, ms);
+                    int before = 0;             // entries of the costlier pairs
+                    for (int j = lane; j < n_dist; j += 32)
+                        if (dist[j].x > c) before += dist[j].y * split_parts(dist[j].x, m, ms);
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) before += __shfl_xor_sync(0xFFFFFFFFu, before, off);
+                    const int base = c / n, rem = c % n;
+                    const int n_it = dist[i].y * n * per_block;
+                    for (int q = lane; q < n_it; q += 32) {
+                        const int e = q / per_block;
+                        const int k = (before + e) * per_block + q % per_block;
+                        const int r = k / a.grid, col = k - r * a.grid;
+                        atomicAdd(&cta_load[(r & 1) ? a.grid - 1 - col : col],
+                                  base + (e % n < rem ? 1 : 0) + kItemOverheadTiles);
+                    }
                 }
                 __syncthreads();
-                int w = 31;
-                for (int i = 0; i < 32; ++i)
-                    if (feasible[i]) { w = i; break; }
-                const int nhi = min(hi, lo - 1 + (w + 1) * step);
-                const int nlo = w == 0 ? lo : lo + w * step;
+                int mx = 0;
+                for (int i = tid; i < a.grid; i += nthreads) mx = max(mx, cta_load[i]);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+                if (lane == 0) red_max[wid] = mx;
                 __syncthreads();
-                lo = nlo;
-                hi = nhi;
-                if (step == 1) break;
+                for (int i = 0; i < (nthreads >> 5); ++i) mx = max(mx, red_max[i]);
+                __syncthreads();
+                return mx;
+            };
+            M = max_cost;                       // no split
+            int best = busiest(M);
+            if (gp > n_pairs) {
+                const int m1 = smallest_fit(gp);
+                const int t1 = busiest(m1);
+                if (t1 < best) {
+                    M = m1;
+                    best = t1;
+                }
             }
-            M = hi;
+            const int m2 = smallest_fit(2 * gp);
+            if (busiest(m2) < best) M = m2;
         }
         if (tid == 0) {
             part_tiles = M;
@@ -2366,23 +2416,23 @@ int validate_seq_shape(const SeqBatch& a, const attn_options_t* opts) {
 }
 
 // work-list entries a batch can need: a block has 256 >> shift tokens, so there are at most
-// sum_b ceil(Sq_b / tokens) <= total_q / tokens + B pairs, and with key splits at most one
-// entry per CTA (sms: the device's SMs, which bound the CTA count)
+// sum_b ceil(Sq_b / tokens) <= total_q / tokens + B pairs, and with key splits at most two
+// items per CTA (sms: the device's SMs, which bound the CTA count)
 int64_t seq_max_blocks(const SeqBatch& a, int64_t sms) {
     const int64_t pairs = a.total_q / (kUnitRows >> pack_shift(a)) + a.B;
-    return a.max_splits > 1 && sms > pairs ? sms : pairs;
+    return a.max_splits > 1 && 2 * sms > pairs ? 2 * sms : pairs;
 }
 
 bool seq_split(const SeqBatch& a) { return a.max_splits > 1; }
 
 // workspace: per-sequence tensor maps (128-byte aligned inside it), the item count, the work
-// list, and with key splits (256-byte aligned) the parts' fp32 rows and LSEs, one slot per CTA
+// list, and with key splits (256-byte aligned) the parts' fp32 rows and LSEs, two slots per CTA
 size_t seq_list_bytes(const SeqBatch& a, int64_t sms) {
     return 128 + (size_t)a.B * 4 * sizeof(CUtensorMap) + 16 + (size_t)seq_max_blocks(a, sms) * sizeof(int4);
 }
 size_t seq_ws_bytes(const SeqBatch& a, int64_t sms) {
     size_t n = seq_list_bytes(a, sms);
-    if (seq_split(a)) n = ((n + 255) & ~(size_t)255) + (size_t)sms * kUnitRows * (size_t)(a.d + 1) * 4;
+    if (seq_split(a)) n = ((n + 255) & ~(size_t)255) + (size_t)2 * sms * kUnitRows * (size_t)(a.d + 1) * 4;
     return n;
 }
 
@@ -2456,7 +2506,7 @@ int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace
     float* ws_lse = nullptr;
     if (split) {
         ws_o = reinterpret_cast<float*>((wsb + seq_list_bytes(a, sms) + 255u) & ~(uintptr_t)255u);
-        ws_lse = ws_o + (size_t)sms * kUnitRows * d;
+        ws_lse = ws_o + (size_t)2 * sms * kUnitRows * d;
     }
     VarlenPrep vp;
     memset(&vp, 0, sizeof vp);
@@ -2577,7 +2627,7 @@ int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace
         vc.H = (int)a.H;
         vc.pack_shift = sh;
         vc.round_mode = a.round_mode;
-        lc.gridDim = dim3((unsigned)G, kUnitRows / 32);   // 32 tile rows a block, 4 a warp
+        lc.gridDim = dim3((unsigned)(2 * G), kUnitRows / 32);   // items < 2 G; 32 tile rows a block, 4 a warp
         lc.blockDim = dim3(256);
         lc.dynamicSmemBytes = 0;
         le = d == 128 ? cudaLaunchKernelEx(&lc, attn_varlen_combine_kernel<128>, vc)

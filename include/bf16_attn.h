@@ -255,10 +255,11 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, int64
  *                 are bit for bit the same.  Pays off when sequences have few queries
  *                 (for decoding a dense batch, pass cu_seqlens = 0, Sq, 2 Sq, ... here).
  *   max_splits    >= 0.  0 or 1: a query block's keys are never split.  n >= 2: when the
- *                 batch's (sequence, query block, head) items number fewer than the CTAs (a
- *                 few long sequences, decoding), the preprocessing kernel splits each block's
- *                 key tiles into up to n contiguous parts, more for costlier blocks: the
- *                 shortest longest part for which every part still has a CTA of its own (the
+ *                 batch's (sequence, query block, head) items number fewer than twice the
+ *                 CTAs (a few long sequences, decoding), the preprocessing kernel may split
+ *                 each block's key tiles into up to n contiguous parts, more for costlier
+ *                 blocks, so that the CTAs finish together: in one wave (every part a CTA of
+ *                 its own) or two, or not at all, whichever a model of the work favours (the
  *                 MoonMath article's key split of the tail, on the variable-length work list);
  *                 a third kernel merges the parts.  The choice depends on the lengths and the CTA count
  *                 only, so results are deterministic for a given device and max_ctas; they
@@ -266,7 +267,7 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, int64
  *                 result).  Batches with at least as many items as CTAs run unsplit.
  * opts->force_splits must be 0 or 1.  workspace: caller device memory of at least
  * attn_fwd_varlen_workspace_size() bytes (per-sequence tensor maps and the work list; with
- * max_splits >= 2 also one fp32 partial tile per SM of the current device), 16-byte aligned;
+ * max_splits >= 2 also two fp32 partial tiles per SM of the current device), 16-byte aligned;
  * or NULL to use the library-owned workspace as attn_fwd_ex does.  The size query returns 0
  * for invalid arguments, and for max_splits >= 2 when no CUDA device is usable.  Kernels on
  * `stream`: a one-CTA preprocessing kernel, the attention kernel, and with max_splits >= 2

@@ -60,11 +60,32 @@ def grid_for(lq, H, Hkv, pack, max_splits, max_ctas=0, max_seqlen_q=0):
     return max(G, 1)
 
 
+ITEM_OVERHEAD_TILES = 2
+
+
+def busiest(costs, M, cap, per, grid):
+    """The busiest CTA's modelled work: pairs heaviest first, each as min(cap, ceil(c / M))
+    near-equal parts in a row, per items an entry, item k on the CTA the alternating
+    round-robin gives it, an item costing its tiles plus ITEM_OVERHEAD_TILES."""
+    load = [0] * grid
+    k = 0
+    for c in sorted(costs, reverse=True):
+        n = min(cap, cdiv(c, M))
+        for i in range(n):
+            t = c // n + (1 if i < c % n else 0)
+            for _ in range(per):
+                r, col = divmod(k, grid)
+                load[grid - 1 - col if r & 1 else col] += t + ITEM_OVERHEAD_TILES
+                k += 1
+    return max(load)
+
+
 def expected_schedule(lq, lk, H, Hkv, causal, pack, grid, max_splits):
-    """Entries (b, qb, part, parts) and costs by the stated rule: with P pairs and Gp = grid //
-    (H >> shift) entry places (max_splits >= 2 and Gp > P), a pair of cost c gets n(c) =
-    min(max_splits, Gp, ceil(c / M)) parts for the smallest M with sum n(c) <= Gp (searched
-    here by brute force)."""
+    """Entries (b, qb, part, parts) and costs by the stated rule.  With P pairs and Gp = grid //
+    (H >> shift) entry places (max_splits >= 2, 2 Gp > P), a pair of cost c gets n(c) =
+    min(max_splits, Gp, ceil(c / M)) parts, M the best of: the largest cost (no split), the
+    smallest M with sum n(c) <= Gp (if Gp > P), the smallest with sum n(c) <= 2 Gp; best = the
+    least busiest-CTA work, the first of equals (searches by brute force here)."""
     sh = pack_shift(H, Hkv, pack)
     tb = 256 >> sh
     pairs = []
@@ -80,10 +101,22 @@ def expected_schedule(lq, lk, H, Hkv, causal, pack, grid, max_splits):
     per = H >> sh
     P, gp = len(pairs), grid // per
     cap = min(max_splits, gp)
+    costs = [p[2] for p in pairs]
     M = 0
-    if max_splits > 1 and P > 0 and gp > P:
-        M = next(m for m in range(1, max(p[2] for p in pairs) + 1)
-                 if sum(min(cap, cdiv(c, m)) for *_, c in pairs) <= gp)
+    if max_splits > 1 and P > 0 and 2 * gp > P and grid <= 1024:
+        def smallest(places):
+            return next(m for m in range(1, max(costs) + 1)
+                        if sum(min(cap, cdiv(c, m)) for c in costs) <= places)
+        M = max(costs)
+        best = busiest(costs, M, cap, per, grid)
+        if gp > P:
+            m1 = smallest(gp)
+            t1 = busiest(costs, m1, cap, per, grid)
+            if t1 < best:
+                M, best = m1, t1
+        m2 = smallest(2 * gp)
+        if busiest(costs, m2, cap, per, grid) < best:
+            M = m2
     entries, cost = [], {}
     for b, qb, c in pairs:
         n = min(cap, cdiv(c, M)) if M else 1
@@ -115,7 +148,7 @@ def check_schedule(ws, lq, lk, H, Hkv, causal, pack, grid, max_splits):
         if part > 0:
             assert got[i - 1] == (b, qb, part - 1, n)
     if any(n > 1 for *_, n in entries):
-        assert n_items <= grid, "a split item without a CTA of its own"
+        assert n_items <= 2 * grid, "more split items than slots"
     return entries
 
 
@@ -152,6 +185,8 @@ CASES = [  # (lens_q, lens_k, H, Hkv, d, mode, causal, pack, max_splits, max_cta
     ([300, 40], [200, 1000], 2, 2, 128, "rtz", True, False, 16, 0, 0),                  # rows with no visible key
     ([129, 1], [900, 4000], 4, 1, 128, "rtne", False, False, 3, 20, 0),                 # few CTAs: uneven parts
     ([3, 2], [700, 260], 8, 1, 64, "rtz", True, True, 8, 0, 0),                         # speculative tokens, packed
+    ([1] * 12, [2870, 2837, 6945, 5115, 7500, 2250, 4000, 6000, 4500, 8000, 3500, 5500],
+     32, 8, 128, "rtne", True, True, 16, 0, 1),                                         # 12 caches: two waves
 ]
 
 
