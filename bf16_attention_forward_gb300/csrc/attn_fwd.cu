@@ -1508,19 +1508,20 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p
 //     runs, most first (a counting sort on that count, capped at kCostBuckets - 1; pairs of
 //     equal count in any order, which moves work between CTAs but changes no result), and
 //     the item count, H >> pack_shift per entry;
-//   * key splits (max_splits >= 2), when the pairs' items number fewer than twice the
-//     attention kernel's CTAs: with P pairs and Gp = CTAs / (items per pair) entry places, a
+//   * key splits (max_splits >= 2), when the pairs' items number fewer than the attention
+//     kernel's CTAs: with P pairs and Gp = CTAs / (items per pair) entry places (P < Gp), a
 //     pair of cost c becomes n(c) = min(max_splits, Gp, ceil(c / M)) consecutive entries (b,
-//     qb, part, n).  M is one of: the largest cost (no split); the smallest M with sum n(c) <=
-//     Gp (one wave: every item a CTA of its own); the smallest with sum n(c) <= 2 Gp (two
-//     waves, whose alternating order pairs a CTA's heavy first item with a light second one),
-//     whichever gives the busiest CTA the least modelled work (key tiles plus a fixed cost per
-//     item), the first of equals.  Split slots stay below twice the CTA count.  n depends only
-//     on c (and the launch), so the result is a function of the inputs and the CTA count;
+//     qb, part, n).  M is the smallest with sum n(c) <= Gp (one wave: every item a CTA of its
+//     own), or, when the pairs' items fill at least half of the CTAs, the smallest with
+//     sum n(c) <= 2 Gp (two waves, whose alternating order pairs a CTA's heavy first item
+//     with a light second one) if that gives the busiest CTA less modelled work (key tiles
+//     plus a fixed cost per item).  Split slots stay below twice the CTA count.  n depends
+//     only on c (and the launch), so the result is a function of the inputs and the CTA
+//     count;
 //   * a sequence with queries but no keys: every query sees no key, so its O rows are NaN
 //     (stored 0x7FC0) and its LSE rows -inf, written here.
 constexpr int kCostBuckets = 4096;
-constexpr int kMaxDistinct = 1024;        // key splits: distinct pair costs considered
+constexpr int kMaxDistinct = 512;         // key splits: distinct pair costs considered
 constexpr int kMaxSplitGrid = 1024;       // key splits: attention CTAs considered
 constexpr int kItemOverheadTiles = 2;     // key splits: modelled fixed cost of an item, in key tiles
 
@@ -1543,7 +1544,7 @@ struct VarlenPrep {
     float* lse;                            // optional [H][total_q]
     CUtensorMap* maps;                     // [B][4]: Q, K, V, O
     int4* blocks;                          // (sequence, query block, part, parts), heaviest first
-    int* n_items;
+    int* n_items;                          // [0] items; [1] items with key splits, else 0
 };
 
 __device__ __forceinline__ void copy_map(CUtensorMap* dst, const CUtensorMap* src) {
@@ -1594,8 +1595,9 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
     __shared__ int bucket[kCostBuckets];   // counts, then (descending) start positions
     __shared__ int warp_sums[32];
     __shared__ int2 dist[kMaxDistinct];    // key splits: (cost, pairs) of each cost present
-    __shared__ int n_dist, n_pairs, max_cost, feasible[32], red_max[32];
-    __shared__ int cta_load[kMaxSplitGrid];   // key splits: modelled busy time of each CTA
+    __shared__ int2 sdist[kMaxDistinct];   // key splits: the same, heaviest first
+    __shared__ int spre[2][kMaxDistinct];  // key splits: entries before each cost, per candidate
+    __shared__ int n_dist, n_pairs, max_cost, cand[2], cand_load[2];
     __shared__ int part_tiles, part_cap;   // M of the key split (0: none), parts at most
     // the previous kernel in the stream may have written the offsets or still read this
     // workspace; the attention kernel may launch now and waits for this one's memory
@@ -1632,7 +1634,8 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
     __syncthreads();
     if (bad) {
         if (tid == 0) {
-            *a.n_items = 0;
+            a.n_items[0] = 0;
+            a.n_items[1] = 0;
             if (atomicCAS(&g_status[0], 0u, (uint32_t)ATTN_ERR_INVALID_ARG) == 0u) atomicExch(&g_status[1], kSiteSeqlens);
         }
         return;
@@ -1686,10 +1689,17 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
         }
     }
     __syncthreads();
-    // key splits: the costs present; for one wave and for two, the smallest M (tiles per part)
-    // whose entries fit, found by narrowing [1, max cost] with 32 candidates a round, one per
-    // warp; then the candidate (no split, one wave, two waves) whose busiest CTA has the least
-    // modelled work.  Each bucket's count then becomes its entries.
+    // key splits, when the pairs' items number fewer than the CTAs (P < Gp).  Warp 0: the
+    // smallest M (tiles per part) whose entries fit one wave, Gp places, by bisection with the
+    // lanes summing over the costs present; every item then has a CTA of its own, and this
+    // never loses to no split (its longest part is at most the largest cost).  When the items
+    // fill at least half of the CTAs, warp 1 also finds the smallest M fitting two waves,
+    // 2 Gp places, and warps 0 and 1 model the busiest CTA's work under each: with the costs
+    // heaviest first (a rank sort; each cost is a bucket of its own), item k belongs to entry
+    // k / per_block, which a search of the prefix of entries places in its cost and part; CTA c
+    // runs items c and 2G - 1 - c (round_item's alternation); an item costs its key tiles plus
+    // kItemOverheadTiles.  Two waves are taken only when that is less.  Each bucket's count
+    // then becomes its entries.
     if (a.max_splits > 1) {
         if (tid == 0) {
             n_dist = 0;
@@ -1710,89 +1720,82 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
         const int per_block = a.H >> a.pack_shift;
         const int gp = a.grid / per_block;
         const int ms = a.max_splits < gp ? a.max_splits : gp;
+        const int nd = n_dist, np = n_pairs, cmax = max_cost;
         int M = 0;
-        if (n_pairs > 0 && 2 * gp > n_pairs && n_dist <= kMaxDistinct && a.grid <= kMaxSplitGrid) {
-            // entries for M tiles per part against `places` (M = max cost always fits one wave
-            // or two, as P < places then)
-            auto fits = [&](int m, int places) {
-                int e = 0;
-                for (int i = lane; i < n_dist; i += 32) e += dist[i].y * split_parts(dist[i].x, m, ms);
+        if (np > 0 && gp > np && nd <= kMaxDistinct && a.grid <= kMaxSplitGrid) {
+            const bool two = 2 * np * per_block >= a.grid;
+            if (wid < (two ? 2 : 1)) {
+                const int places = (wid + 1) * gp;
+                int lo = 1, hi = cmax;         // cmax fits: every pair one entry, np < places
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    int e = 0;
+                    for (int i = lane; i < nd; i += 32) e += dist[i].y * split_parts(dist[i].x, mid, ms);
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(0xFFFFFFFFu, e, off);
-                return e <= places;
-            };
-            auto smallest_fit = [&](int places) {
-                int lo = 1, hi = max_cost;      // the answer lies in [lo, hi]; hi fits
-                while (true) {
-                    const int step = (hi - lo + 32) / 32;
-                    const int m = min(hi, lo - 1 + (wid + 1) * step);
-                    const bool f = fits(m, places);
-                    if (lane == 0) feasible[wid] = f ? 1 : 0;
-                    __syncthreads();
-                    int w = 31;
-                    for (int i = 0; i < 32; ++i)
-                        if (feasible[i]) { w = i; break; }
-                    const int nhi = min(hi, lo - 1 + (w + 1) * step);
-                    const int nlo = w == 0 ? lo : lo + w * step;
-                    __syncthreads();
-                    lo = nlo;
-                    hi = nhi;
-                    if (step == 1) break;
+                    for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(0xFFFFFFFFu, e, off);
+                    if (e <= places) hi = mid;
+                    else lo = mid + 1;
                 }
-                return hi;
-            };
-            // the busiest CTA's work under M: entries heaviest first (a pair's parts in a row,
-            // near-equal), item k = entry * per_block + head group, run by the CTA that
-            // round_item gives it; an item costs its key tiles plus kItemOverheadTiles
-            auto busiest = [&](int m) {
-                for (int i = tid; i < a.grid; i += nthreads) cta_load[i] = 0;
-                __syncthreads();
-                for (int i = wid; i < n_dist; i += (nthreads >> 5)) {
-                    const int c = dist[i].x, n = split_parts(c, m, ms);
-                    int before = 0;             // entries of the costlier pairs
-                    for (int j = lane; j < n_dist; j += 32)
-                        if (dist[j].x > c) before += dist[j].y * split_parts(dist[j].x, m, ms);
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) before += __shfl_xor_sync(0xFFFFFFFFu, before, off);
-                    const int base = c / n, rem = c % n;
-                    const int n_it = dist[i].y * n * per_block;
-                    for (int q = lane; q < n_it; q += 32) {
-                        const int e = q / per_block;
-                        const int k = (before + e) * per_block + q % per_block;
-                        const int r = k / a.grid, col = k - r * a.grid;
-                        atomicAdd(&cta_load[(r & 1) ? a.grid - 1 - col : col],
-                                  base + (e % n < rem ? 1 : 0) + kItemOverheadTiles);
-                    }
-                }
-                __syncthreads();
-                int mx = 0;
-                for (int i = tid; i < a.grid; i += nthreads) mx = max(mx, cta_load[i]);
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-                if (lane == 0) red_max[wid] = mx;
-                __syncthreads();
-                for (int i = 0; i < (nthreads >> 5); ++i) mx = max(mx, red_max[i]);
-                __syncthreads();
-                return mx;
-            };
-            M = max_cost;                       // no split
-            int best = busiest(M);
-            if (gp > n_pairs) {
-                const int m1 = smallest_fit(gp);
-                const int t1 = busiest(m1);
-                if (t1 < best) {
-                    M = m1;
-                    best = t1;
-                }
+                if (lane == 0) cand[wid] = lo;
             }
-            const int m2 = smallest_fit(2 * gp);
-            if (busiest(m2) < best) M = m2;
+            if (two)
+                for (int i = tid; i < nd; i += nthreads) {
+                    const int c = dist[i].x;
+                    int rank = 0;
+                    for (int j = 0; j < nd; ++j) rank += dist[j].x > c ? 1 : 0;
+                    sdist[rank] = dist[i];
+                }
+            __syncthreads();
+            if (two) {
+                if (wid < 2) {
+                    const int m = cand[wid];
+                    int* pre = spre[wid];
+                    int carry = 0;
+                    for (int i0 = 0; i0 < nd; i0 += 32) {
+                        const int i = i0 + lane;
+                        const int ent = i < nd ? sdist[i].y * split_parts(sdist[i].x, m, ms) : 0;
+                        int incl = ent;
+#pragma unroll
+                        for (int off = 1; off < 32; off <<= 1) {
+                            const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+                            if (lane >= off) incl += y;
+                        }
+                        if (i < nd) pre[i] = carry + incl - ent;
+                        carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+                    }
+                    __syncwarp();
+                    const int n_it = carry * per_block;   // items: at most 2 G
+                    int worst = 0;
+                    for (int c = lane; c < a.grid; c += 32) {
+                        int load = 0;
+                        for (int t = 0; t < 2; ++t) {
+                            const int k = t == 0 ? c : 2 * a.grid - 1 - c;
+                            if (k >= n_it) continue;
+                            const int e = k / per_block;
+                            int lo = 0, hi = nd - 1;  // the last cost whose entries start at or before e
+                            while (lo < hi) {
+                                const int mid = (lo + hi + 1) >> 1;
+                                if (pre[mid] <= e) lo = mid;
+                                else hi = mid - 1;
+                            }
+                            const int cst = sdist[lo].x, n = split_parts(cst, m, ms);
+                            const int part = (e - pre[lo]) % n;
+                            load += cst / n + (part < cst % n ? 1 : 0) + kItemOverheadTiles;
+                        }
+                        worst = max(worst, load);
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) worst = max(worst, __shfl_xor_sync(0xFFFFFFFFu, worst, off));
+                    if (lane == 0) cand_load[wid] = worst;
+                }
+                __syncthreads();
+            }
+            M = (two && cand_load[1] < cand_load[0]) ? cand[1] : cand[0];
         }
         if (tid == 0) {
             part_tiles = M;
             part_cap = ms;
         }
-        __syncthreads();
         if (M > 0)
             for (int i = tid; i < kCostBuckets; i += nthreads) bucket[i] *= split_parts(i, M, ms);
         __syncthreads();
@@ -1824,7 +1827,10 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
     }
     __syncthreads();
     int start = (wid > 0 ? warp_sums[wid - 1] : 0) + incl - local;
-    if (tid == nthreads - 1) *a.n_items = (start + local) * (a.H >> a.pack_shift);
+    if (tid == nthreads - 1) {
+        a.n_items[0] = (start + local) * (a.H >> a.pack_shift);
+        a.n_items[1] = part_tiles > 0 ? a.n_items[0] : 0;   // items the merge kernel visits
+    }
     __syncthreads();
     if (tid < 1024)
         for (int i = 0; i < kPer; ++i) {
@@ -1851,9 +1857,10 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
 }
 
 // Merge of a variable-length batch's key parts, a programmatic dependent of the attention
-// kernel.  Block (k, y) takes tile rows 32 y .. 32 y + 31 of item k when k's entry is the first
-// part of a split pair (every other block returns at once); warp w merges rows 32 y + w + 8 i
-// (i = 0 .. 3, so that the few rows of a decoding step fall to different warps), lane l holding
+// kernel.  Block (x, y) takes tile rows 32 y .. 32 y + 31 of items k = x, x + G, ... (G blocks
+// along x) whose entry is the first part of a split pair (others are skipped); warp w merges
+// rows 32 y + w + 8 i (i = 0 .. 3, so that the few rows of a decoding step fall to different
+// warps), lane l holding
 // columns kC l .. kC l + kC - 1.  The parts' slots are k + s * per_block (s = 0 .. n - 1: the
 // pair's entries are consecutive).  A row's part LSEs are read across the lanes at once, and
 // its parts' partial rows four at a time.  Weights follow the dense combine: 2^(LSE_s - max),
@@ -1864,7 +1871,7 @@ __global__ void __launch_bounds__(1024) attn_varlen_prep_kernel(const __grid_con
 // work list.
 struct VarlenCombine {
     const int4* blocks;
-    const int* n_items;
+    const int* n_items;                    // [1]: items when keys were split, else 0
     const int* cu_q;
     const float* ws_o;                     // [slot][256][D]
     const float* ws_lse;                   // [slot][256], log2 units
@@ -1879,83 +1886,84 @@ __global__ void __launch_bounds__(256) attn_varlen_combine_kernel(const VarlenCo
     constexpr int kC = D / 32;             // columns per lane: 4 or 2
     constexpr int kLoads = 4;              // parts' rows in flight
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int k = blockIdx.x;
-    if (k >= __ldg(p.n_items)) return;
+    const int n_items = __ldg(p.n_items + 1);
     const int per_block = p.H >> p.pack_shift;
-    const int4 e = __ldg(p.blocks + k / per_block);
-    if (e.w < 2 || e.z != 0) return;
-    const int n = e.w;
-    const int q0 = __ldg(p.cu_q + e.x);
-    const int sq = __ldg(p.cu_q + e.x + 1) - q0;
-    const int h0 = (k % per_block) << p.pack_shift;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long pstride = (long long)per_block * kUnitRows;   // rows from one part to the next
-    for (int i = 0; i < 4; ++i) {
-        const int r = blockIdx.y * 32 + warp + 8 * i;
-        const int tok = (e.y * kUnitRows + r) >> p.pack_shift;
-        if (tok >= sq) break;              // tokens do not decrease with r
-        const int h = h0 + (r & ((1 << p.pack_shift) - 1));
-        const long long row0 = (long long)k * kUnitRows + r;      // part 0's row
-        float mx = -INFINITY;
-        bool any_nan = false;
-        for (int s = lane; s < n; s += 32) {
-            const float l = p.ws_lse[row0 + s * pstride];
-            any_nan |= (l != l);
-            mx = fmaxf(mx, l);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-        any_nan = __any_sync(0xFFFFFFFFu, any_nan);
-        float acc[kC];
-#pragma unroll
-        for (int c = 0; c < kC; ++c) acc[c] = 0.f;
-        float wsum = 0.f;
-        for (int s0 = 0; s0 < n; s0 += 32) {
-            // lane j holds the weight of part s0 + j
-            float wt = 0.f;
-            if (s0 + lane < n) {
-                const float l = p.ws_lse[row0 + (s0 + lane) * pstride];
-                wt = (l == -INFINITY) ? 0.0f : ptx::ex2_approx(fmaxf(l - mx, -125.0f));
+    for (int k = blockIdx.x; k < n_items; k += gridDim.x) {
+        const int4 e = __ldg(p.blocks + k / per_block);
+        if (e.w < 2 || e.z != 0) continue;
+        const int n = e.w;
+        const int q0 = __ldg(p.cu_q + e.x);
+        const int sq = __ldg(p.cu_q + e.x + 1) - q0;
+        const int h0 = (k % per_block) << p.pack_shift;
+        for (int i = 0; i < 4; ++i) {
+            const int r = blockIdx.y * 32 + warp + 8 * i;
+            const int tok = (e.y * kUnitRows + r) >> p.pack_shift;
+            if (tok >= sq) break;              // tokens do not decrease with r
+            const int h = h0 + (r & ((1 << p.pack_shift) - 1));
+            const long long row0 = (long long)k * kUnitRows + r;      // part 0's row
+            float mx = -INFINITY;
+            bool any_nan = false;
+            for (int s = lane; s < n; s += 32) {
+                const float l = p.ws_lse[row0 + s * pstride];
+                any_nan |= (l != l);
+                mx = fmaxf(mx, l);
             }
-            const int m = n - s0 < 32 ? n - s0 : 32;
-            for (int j0 = 0; j0 < m; j0 += kLoads) {
-                float v[kLoads][kC];
-#pragma unroll
-                for (int j = 0; j < kLoads; ++j) {
-                    if (j0 + j < m) {
-                        const float* src = p.ws_o + (row0 + (s0 + j0 + j) * pstride) * D + lane * kC;
-                        if constexpr (kC == 4) {
-                            const float4 x = *reinterpret_cast<const float4*>(src);
-                            v[j][0] = x.x; v[j][1] = x.y; v[j][2] = x.z; v[j][3] = x.w;
-                        } else {
-                            const float2 x = *reinterpret_cast<const float2*>(src);
-                            v[j][0] = x.x; v[j][1] = x.y;
+    #pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+            any_nan = __any_sync(0xFFFFFFFFu, any_nan);
+            float acc[kC];
+    #pragma unroll
+            for (int c = 0; c < kC; ++c) acc[c] = 0.f;
+            float wsum = 0.f;
+            for (int s0 = 0; s0 < n; s0 += 32) {
+                // lane j holds the weight of part s0 + j
+                float wt = 0.f;
+                if (s0 + lane < n) {
+                    const float l = p.ws_lse[row0 + (s0 + lane) * pstride];
+                    wt = (l == -INFINITY) ? 0.0f : ptx::ex2_approx(fmaxf(l - mx, -125.0f));
+                }
+                const int m = n - s0 < 32 ? n - s0 : 32;
+                for (int j0 = 0; j0 < m; j0 += kLoads) {
+                    float v[kLoads][kC];
+    #pragma unroll
+                    for (int j = 0; j < kLoads; ++j) {
+                        if (j0 + j < m) {
+                            const float* src = p.ws_o + (row0 + (s0 + j0 + j) * pstride) * D + lane * kC;
+                            if constexpr (kC == 4) {
+                                const float4 x = *reinterpret_cast<const float4*>(src);
+                                v[j][0] = x.x; v[j][1] = x.y; v[j][2] = x.z; v[j][3] = x.w;
+                            } else {
+                                const float2 x = *reinterpret_cast<const float2*>(src);
+                                v[j][0] = x.x; v[j][1] = x.y;
+                            }
+                        }
+                    }
+    #pragma unroll
+                    for (int j = 0; j < kLoads; ++j) {
+                        if (j0 + j < m) {
+                            const float w = __shfl_sync(0xFFFFFFFFu, wt, j0 + j);
+                            wsum += w;
+    #pragma unroll
+                            for (int c = 0; c < kC; ++c) acc[c] += w * v[j][c];
                         }
                     }
                 }
-#pragma unroll
-                for (int j = 0; j < kLoads; ++j) {
-                    if (j0 + j < m) {
-                        const float w = __shfl_sync(0xFFFFFFFFu, wt, j0 + j);
-                        wsum += w;
-#pragma unroll
-                        for (int c = 0; c < kC; ++c) acc[c] += w * v[j][c];
-                    }
-                }
             }
+            const bool nan_row = any_nan || mx == -INFINITY;
+            const float inv = 1.0f / wsum;
+            if (p.lse && lane == 0)
+                p.lse[(long long)h * p.total_q + q0 + tok] = any_nan ? NAN : (mx + log2f(wsum)) * kLn2;
+            uint32_t bits[kC];
+    #pragma unroll
+            for (int c = 0; c < kC; ++c) bits[c] = nan_row ? 0x7FC0u : round_bf16_bits(acc[c] * inv, p.round_mode);
+            __nv_bfloat16* orow = p.o + ((long long)(q0 + tok) * p.H + h) * D;
+            if constexpr (kC == 4)
+                *reinterpret_cast<uint2*>(orow + lane * 4) = make_uint2(bits[0] | (bits[1] << 16), bits[2] | (bits[3] << 16));
+            else
+                *reinterpret_cast<uint32_t*>(orow + lane * 2) = bits[0] | (bits[1] << 16);
         }
-        const bool nan_row = any_nan || mx == -INFINITY;
-        const float inv = 1.0f / wsum;
-        if (p.lse && lane == 0)
-            p.lse[(long long)h * p.total_q + q0 + tok] = any_nan ? NAN : (mx + log2f(wsum)) * kLn2;
-        uint32_t bits[kC];
-#pragma unroll
-        for (int c = 0; c < kC; ++c) bits[c] = nan_row ? 0x7FC0u : round_bf16_bits(acc[c] * inv, p.round_mode);
-        __nv_bfloat16* orow = p.o + ((long long)(q0 + tok) * p.H + h) * D;
-        if constexpr (kC == 4)
-            *reinterpret_cast<uint2*>(orow + lane * 4) = make_uint2(bits[0] | (bits[1] << 16), bits[2] | (bits[3] << 16));
-        else
-            *reinterpret_cast<uint32_t*>(orow + lane * 2) = bits[0] | (bits[1] << 16);
     }
 }
 
@@ -2627,7 +2635,7 @@ int run_seq_batch(const SeqBatch& a, const attn_options_t* opts, void* workspace
         vc.H = (int)a.H;
         vc.pack_shift = sh;
         vc.round_mode = a.round_mode;
-        lc.gridDim = dim3((unsigned)(2 * G), kUnitRows / 32);   // items < 2 G; 32 tile rows a block, 4 a warp
+        lc.gridDim = dim3((unsigned)G, kUnitRows / 32);   // items < 2 G, two a block; 32 tile rows a block, 4 a warp
         lc.blockDim = dim3(256);
         lc.dynamicSmemBytes = 0;
         le = d == 128 ? cudaLaunchKernelEx(&lc, attn_varlen_combine_kernel<128>, vc)

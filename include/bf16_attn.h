@@ -255,13 +255,13 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, int64
  *                 are bit for bit the same.  Pays off when sequences have few queries
  *                 (for decoding a dense batch, pass cu_seqlens = 0, Sq, 2 Sq, ... here).
  *   max_splits    >= 0.  0 or 1: a query block's keys are never split.  n >= 2: when the
- *                 batch's (sequence, query block, head) items number fewer than twice the
- *                 CTAs (a few long sequences, decoding), the preprocessing kernel may split
- *                 each block's key tiles into up to n contiguous parts, more for costlier
- *                 blocks, so that the CTAs finish together: in one wave (every part a CTA of
- *                 its own) or two, or not at all, whichever a model of the work favours (the
- *                 MoonMath article's key split of the tail, on the variable-length work list);
- *                 a third kernel merges the parts.  The choice depends on the lengths and the CTA count
+ *                 batch's (sequence, query block, head) items number fewer than the CTAs (a
+ *                 few long sequences, decoding), the preprocessing kernel splits each block's
+ *                 key tiles into up to n contiguous parts, more for costlier blocks, so that
+ *                 the CTAs finish together: in one wave (every part a CTA of its own) or, when
+ *                 the items already fill half the CTAs and a model of the work favours it, in
+ *                 two (the MoonMath article's key split of the tail, on the variable-length
+ *                 work list); a third kernel merges the parts.  The choice depends on the lengths and the CTA count
  *                 only, so results are deterministic for a given device and max_ctas; they
  *                 differ from the unsplit ones by rounding (same criteria against the exact
  *                 result).  Batches with at least as many items as CTAs run unsplit.

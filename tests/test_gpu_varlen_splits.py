@@ -82,10 +82,10 @@ def busiest(costs, M, cap, per, grid):
 
 def expected_schedule(lq, lk, H, Hkv, causal, pack, grid, max_splits):
     """Entries (b, qb, part, parts) and costs by the stated rule.  With P pairs and Gp = grid //
-    (H >> shift) entry places (max_splits >= 2, 2 Gp > P), a pair of cost c gets n(c) =
-    min(max_splits, Gp, ceil(c / M)) parts, M the best of: the largest cost (no split), the
-    smallest M with sum n(c) <= Gp (if Gp > P), the smallest with sum n(c) <= 2 Gp; best = the
-    least busiest-CTA work, the first of equals (searches by brute force here)."""
+    (H >> shift) entry places (max_splits >= 2, Gp > P), a pair of cost c gets n(c) =
+    min(max_splits, Gp, ceil(c / M)) parts, M the smallest with sum n(c) <= Gp; or, when
+    2 P (H >> shift) >= grid, the smallest with sum n(c) <= 2 Gp if its busiest CTA has less
+    work (searches by brute force here)."""
     sh = pack_shift(H, Hkv, pack)
     tb = 256 >> sh
     pairs = []
@@ -103,20 +103,15 @@ def expected_schedule(lq, lk, H, Hkv, causal, pack, grid, max_splits):
     cap = min(max_splits, gp)
     costs = [p[2] for p in pairs]
     M = 0
-    if max_splits > 1 and P > 0 and 2 * gp > P and grid <= 1024:
+    if max_splits > 1 and P > 0 and gp > P and grid <= 1024:
         def smallest(places):
             return next(m for m in range(1, max(costs) + 1)
                         if sum(min(cap, cdiv(c, m)) for c in costs) <= places)
-        M = max(costs)
-        best = busiest(costs, M, cap, per, grid)
-        if gp > P:
-            m1 = smallest(gp)
-            t1 = busiest(costs, m1, cap, per, grid)
-            if t1 < best:
-                M, best = m1, t1
-        m2 = smallest(2 * gp)
-        if busiest(costs, m2, cap, per, grid) < best:
-            M = m2
+        M = smallest(gp)
+        if 2 * P * per >= grid:
+            m2 = smallest(2 * gp)
+            if busiest(costs, m2, cap, per, grid) < busiest(costs, M, cap, per, grid):
+                M = m2
     entries, cost = [], {}
     for b, qb, c in pairs:
         n = min(cap, cdiv(c, M)) if M else 1
