@@ -545,7 +545,9 @@ def run_paged(args, decode=False):
                    "l2": "K/V cache %.0f MB > 126 MB L2" % (2 * kc.numel() * 2 / 2**20)},
         "roofline": ({"bound": "hbm", "achieved": kv_bytes / (ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
                       "frac": kv_bytes / (ms * 1e-3) / 1e9 / hbm, "peak_source": peak_src + " HBM copy",
-                      "timed": "whole call"} if decode else
+                      "timed": "whole call",
+                      "traffic": (recorded_traffic("paged_decode")
+                                  if seqs == DECODE_SEQS and pack and args.splits < 2 else None)} if decode else
                      {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
                       "frac": value / peak, "peak_source": peak_src + " burst bf16 (cuBLAS)",
                       "timed": "whole call", "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm}),
