@@ -299,10 +299,15 @@ def test_planted_missing_statistics_release_is_caught():
 class MainModel(Model):
     """attn_fwd_kernel's protocol: one CTA, units of two query tiles, a K,V,K,V ring of
     `stages` slots with full/empty barriers, one MMA thread issuing S_t(j+1) right after
-    PV_t(j) (in order), and two softmax warpgroups that each run their tile's epilogue."""
+    PV_t(j) (in order), and two softmax warpgroups that each run their tile's epilogue.
+    Units in `dead1` have no query in their second tile (a decoding step's rows all sit in
+    the first): that tile's softmax warps keep every wait and arrival but read no S, store
+    no P and read no O; the GEMMs still run on whatever the tile holds ("X": released by the
+    softmax without a P).  `dead_arrives=False` plants the mistake of skipping the arrival."""
 
-    def __init__(self, units, rng, stages=4, wait_empty=True):
+    def __init__(self, units, rng, stages=4, wait_empty=True, dead1=frozenset(), dead_arrives=True):
         self.units, self.rng, self.S, self.wait_empty = units, rng, stages, wait_empty
+        self.dead1, self.dead_arrives = dead1, dead_arrives
         self.b = {}
         for i in range(stages):
             self.b[("Full", i)] = Barrier("Full[%d]" % i, 1)
@@ -388,14 +393,15 @@ class MainModel(Model):
         def run():
             self.check(self.q == u, "S GEMM read another unit's Q")
             self.check(self.ring[kslot] == kpos, "S GEMM read the wrong K")
-            self.check(self.s_buf[t] in (None, ("P", g - 1)), "S overwrote P before its PV")
+            self.check(self.s_buf[t] in (None, ("P", g - 1), ("X", g - 1)), "S overwrote P before its PV")
             self.s_buf[t] = ("S", g)
             self.b[("SFull", t)].arrive()
         return run
 
     def _pv(self, t, u, g, jj, vslot, vpos):
         def run():
-            self.check(self.s_buf[t] == ("P", g), "PV read the wrong P")
+            released = "X" if (t == 1 and u in self.dead1) else "P"
+            self.check(self.s_buf[t] == (released, g), "PV read the wrong P")
             self.check(self.ring[vslot] == vpos, "PV read the wrong V")
             if jj == 0:
                 self.check(self.o[t] is None, "PV overwrote O before the epilogue read it")
@@ -407,20 +413,24 @@ class MainModel(Model):
     def softmax(self, t):
         g = 0
         for u, nk in enumerate(self.units):
+            dead = t == 1 and u in self.dead1
             for jj in range(nk):
                 yield from self.wait(("SFull", t), g)
-                self.check(self.s_buf[t] == ("S", g), "softmax read the wrong S")
-                if jj > 0 and self.rng.random() < 0.2:
-                    # lazy rescale reads O_t: S_t(g) completing implies PV_t(g-1) did (in order)
-                    self.check(self.o[t] == (u, jj), "rescale met O mid-update")
+                if not dead:
+                    self.check(self.s_buf[t] == ("S", g), "softmax read the wrong S")
+                    if jj > 0 and self.rng.random() < 0.2:
+                        # lazy rescale reads O_t: S_t(g) completing implies PV_t(g-1) did (in order)
+                        self.check(self.o[t] == (u, jj), "rescale met O mid-update")
                 yield ("step",)
-                self.s_buf[t] = ("P", g)
-                self.b[("PFull", t)].arrive()
+                self.s_buf[t] = ("X", g) if dead else ("P", g)
+                if not dead or self.dead_arrives:
+                    self.b[("PFull", t)].arrive()
                 g += 1
             yield from self.wait(("OFull", t), u)
-            self.check(self.o[t] == (u, nk), "epilogue read an unfinished O")
+            if not dead:
+                self.check(self.o[t] == (u, nk), "epilogue read an unfinished O")
             yield ("step",)
-            self.o[t] = None                   # read out; the next unit's first PV may write
+            self.o[t] = None                   # read out (or, dead, passed over); the next unit's first PV may write
 
     def run(self, max_events=200000):
         roles = {"producer": self.producer(), "mma": self.mma(), "sm0": self.softmax(0),
@@ -435,6 +445,21 @@ class MainModel(Model):
 def test_main_kernel_protocol(units, stages):
     for seed in range(100):
         MainModel(units, random.Random(seed * 104729 + stages), stages).run()
+
+
+@pytest.mark.parametrize("units", UNIT_PATTERNS, ids=lambda u: "-".join(map(str, u)))
+def test_main_kernel_protocol_with_dead_second_tiles(units):
+    # decoding blocks: some units' second query tile holds no query
+    for seed in range(60):
+        rng = random.Random(seed * 7919 + len(units))
+        dead1 = frozenset(u for u in range(len(units)) if rng.random() < 0.5)
+        MainModel(units, rng, 4, dead1=dead1).run()
+
+
+def test_main_kernel_dead_tile_without_arrival_is_caught():
+    # dead softmax warps that skip the P-ready arrival leave the MMA thread waiting
+    with pytest.raises(Deadlock):
+        MainModel([3, 2], random.Random(1), 4, dead1=frozenset({0}), dead_arrives=False).run()
 
 
 def test_main_kernel_planted_missing_release_is_caught():
