@@ -82,6 +82,10 @@ def parse():
                          "query blocks into up to that many parts when the items number fewer than the CTAs)")
     ap.add_argument("--decode-seqs", type=int, default=None,
                     help="with --op paged_decode: the number of sequences (default %d)" % 64)
+    ap.add_argument("--paged-seqs", type=int, default=None,
+                    help="with --op paged: the number of sequences (default %d)" % 16)
+    ap.add_argument("--chunk", type=int, default=None,
+                    help="with --op paged: the query chunk per sequence (default %d)" % 512)
     ap.add_argument("--deterministic", action="store_true",
                     help="with --op bwd: the deterministic backward (dQ summed in key-tile order)")
     return ap.parse_args()
@@ -475,7 +479,8 @@ def run_paged(args, decode=False):
     attn.load()
     steps = args.steps if args.steps is not None else 50
     warmup = max(3, args.warmup if args.warmup is not None else 10)
-    seqs, chunk = (args.decode_seqs or DECODE_SEQS, 1) if decode else (PAGED_SEQS, PAGED_CHUNK)
+    seqs, chunk = ((args.decode_seqs or DECODE_SEQS, 1) if decode
+                   else (args.paged_seqs or PAGED_SEQS, args.chunk or PAGED_CHUNK))
     pack = (decode and not args.no_pack) or (not decode and args.pack)
     rng = np.random.default_rng(DECODE_SEED if decode else PAGED_SEED)
     lens_k = rng.integers(4096 if decode else 2048, 16385, seqs).tolist()
