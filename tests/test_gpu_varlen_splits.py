@@ -313,3 +313,27 @@ def test_varlen_key_split_schedule_random(attn):
         st, site = attn.device_status()
         assert st == 0, (trial, st, site)
         check_schedule(ws, lq, lk, H, Hkv, causal, pack, grid_for(lq, H, Hkv, pack, ms, max_ctas, msq), ms)
+
+
+def test_varlen_key_splits_nonfinite_values(attn):
+    # +inf in one key of one cache (a +inf or -inf logit, by the sign of the query's element)
+    # and NaN in one value of another, both inside a part of a split: the merge must give the
+    # oracle's NaN rows and NaN or finite LSE, bit for bit where non-finite
+    lq, lk, H, Hkv, d = [1, 1, 1, 1], [3000, 2000, 5000, 900], 8, 2, 128
+    q, k, v = packed(sum(lq), sum(lk), H, Hkv, d, seed=10500)
+    cu_q, cu_k = offsets(lq), offsets(lk)
+    k.view(torch.int16)[cu_k[1] + 700, 0, 5] = 0x7F80        # +inf
+    v.view(torch.int16)[cu_k[2] + 4000, 1, 17] = 0x7FC1      # NaN
+    ws = torch.empty(varlen_ws_bytes(attn, lq, lk, H, Hkv, d, True, 8, q.shape[0]), dtype=torch.uint8, device="cuda")
+    o, lse = run(attn, q, k, v, cu_q, cu_k, ws, "rtne", True, pack_heads=True, max_splits=8, max_seqlen_q=1)
+    entries = check_schedule(ws, lq, lk, H, Hkv, True, True, grid_for(lq, H, Hkv, True, 8, 0, 1), 8)
+    assert any(n > 1 for *_, n in entries)
+    ref = oracle.attention_varlen(q, k, v, cu_q, cu_k, "rtne", causal=True, want_a=True, want_lse=True)
+    ob = o.cpu().view(torch.int16).numpy().view(np.uint16)
+    res = parity.compare(ob.reshape(-1, d), ref["o_bits"].reshape(-1, d), ref["a"].reshape(-1, d))
+    assert res["ok"], res
+    assert res["n_nonfinite"] > 0, "the planted values reach no row"
+    # the LSE's error scale from finite keys (the planted +inf would make it inf or NaN)
+    k_fin = k.clone()
+    k_fin.view(torch.int16)[cu_k[1] + 700, 0, 5] = 0
+    check_lse(lse.cpu().numpy().reshape(-1), ref["lse"].reshape(-1), lse_scale(q, k_fin, cu_q, cu_k).reshape(-1))
